@@ -1,0 +1,334 @@
+"""fp64 CPU oracle of the NOSA decode step.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module. The library never calls it
+and shares no code, header, table or helper with it: it is the plain, slow
+definition the CUDA path is checked against.
+
+Source: "Technical Summary: NOSA: Native and Offloadable Sparse Attention"
+(gist.science/paper/2510.13602), section Methodology, part 1 "Algorithm: NOSA"
+(dual selection, locality guarantee, block-wise two-stage pooling, ED-DMA) and
+part 2 "System: NOSI" (block-sized KV units, set-difference, UVA transfer).
+The page states the method in prose only; where it is silent this file takes
+the plainest reading and says so at the spot (readings R1..R20):
+
+* R1  The block-level max pools sub-block *scores*: each sub-block's mean key is
+      dotted with the query, then the block score is the max over its sub-blocks.
+* R2  Selection is per KV head; the group of G query heads that share it is
+      represented by the mean query q_bar (equal to averaging the heads' scores
+      before the max).
+* R3  Scores are scaled by 1/sqrt(d) like attention logits (order-neutral).
+* R4  The eviction score of a block is pooled the same way as keys: mean of the
+      per-token eviction logits inside each sub-block, max over sub-blocks.
+* R5  Eviction eligibility is kept only by blocks in Gamma_e(t); a block that
+      Gamma_e did not pick (even one Gamma_q picked) is never eligible again.
+* R6  Gamma_q may pick any candidate outside Gamma_e, evicted or not.
+* R7  The block holding the newest token is always attended and never a
+      candidate; it becomes a candidate (and eligible) when the next token opens
+      a new block.
+* R9  ED-DMA: the pre-exp eviction logit is added to the scaled q.k logit before
+      the softmax (natural-log domain); selection uses the pre-exp block score.
+* R10 Ties: the lower block index wins.
+* R11 After the prompt every candidate block is eligible and no block is
+      resident; no eviction happens during the prompt.
+* R12 With too few candidates, take all of them; Gamma_q fills the budget to k.
+* R13 Loads are ordered by block index, free slots by slot index, paired by rank.
+      A load of the block that was the tail one step earlier is sourced from the
+      old tail buffer (TAIL), every other load from the host store (HOST).
+* R14 Decisions that turn floating point into indices (the top-k cuts) are taken
+      in fp32, the kernels' precision: the fp64 score is rounded to fp32 first.
+
+Every other quantity is fp64.
+"""
+from __future__ import annotations
+
+import math
+import numpy as np
+
+HOST = 0
+TAIL = 1
+
+__all__ = [
+    "HOST", "TAIL", "pool_block", "group_query", "block_scores", "decision_values",
+    "top_m", "dual_select", "set_difference", "attend", "encode_payload",
+    "payload_bytes", "UnitOracle",
+]
+
+
+# ----------------------------------------------------------------------------
+# Methodology §1, Block-Wise Implementation: two-stage pooling.
+# ----------------------------------------------------------------------------
+def pool_block(k_blk: np.ndarray, e_blk: np.ndarray, sub_block: int):
+    """First pooling stage of one complete block.
+
+    k_blk [B][d] and e_blk [B] are fp64. Returns the sub-block mean keys
+    K_bar [B/S][d], the sub-block mean eviction logits e_bar [B/S] and the block's
+    eviction score se = max over sub-blocks of e_bar (R4).
+    """
+    B, d = k_blk.shape
+    P = B // sub_block
+    k_sub = k_blk.reshape(P, sub_block, d)
+    e_sub = e_blk.reshape(P, sub_block)
+    k_bar = k_sub.sum(axis=1) / sub_block
+    e_bar = e_sub.sum(axis=1) / sub_block
+    return k_bar, e_bar, float(e_bar.max())
+
+
+def group_query(q_group: np.ndarray) -> np.ndarray:
+    """R2: the mean of the G query heads that share one KV head, [G][d] -> [d]."""
+    return q_group.sum(axis=0) / q_group.shape[0]
+
+
+def block_scores(q_bar: np.ndarray, k_bar: np.ndarray) -> np.ndarray:
+    """Second pooling stage and query-aware score (R1, R3).
+
+    k_bar [N][P][d]: sq(i) = max_s (q_bar . K_bar[i, s]) / sqrt(d).
+    """
+    d = k_bar.shape[-1]
+    if k_bar.shape[0] == 0:
+        return np.zeros(0)
+    return (k_bar @ q_bar).max(axis=1) / math.sqrt(d)
+
+
+# ----------------------------------------------------------------------------
+# Methodology §1, Dual-Selection Mechanism.
+# ----------------------------------------------------------------------------
+def decision_values(scores: np.ndarray) -> np.ndarray:
+    """R14: the fp32 value a top-k cut compares (-0 is the same key as +0)."""
+    return np.asarray(scores, dtype=np.float64).astype(np.float32) + np.float32(0.0)
+
+
+def top_m(scores: np.ndarray, cand: np.ndarray, m: int) -> np.ndarray:
+    """The m best candidates by score (descending), lower index first on ties (R10).
+
+    ``scores`` is indexed by block; ``cand`` lists candidate block indices.
+    Returns the chosen block indices in ascending order.
+    """
+    cand = np.asarray(cand, dtype=np.int64)
+    m = max(0, min(int(m), len(cand)))
+    if m == len(cand):
+        return np.sort(cand)
+    s = decision_values(np.asarray(scores)[cand]).astype(np.float64)
+    order = np.lexsort((cand, -s))
+    return np.sort(cand[order[:m]])
+
+
+def dual_select(sq: np.ndarray, se: np.ndarray, elig: np.ndarray, n_cand: int,
+                k: int, k_e: int):
+    """Gamma = Gamma_e U Gamma_q over the n_cand candidate blocks.
+
+    Gamma_e: top-k_e of the eviction scores se among eligible blocks (query-agnostic,
+    strict eviction). Gamma_q: top-(k - |Gamma_e|) of the query-aware scores sq among
+    the other candidates (R6, R12). The new eligibility is membership of Gamma_e (R5).
+    """
+    cands = np.arange(n_cand, dtype=np.int64)
+    eligible = cands[np.asarray(elig[:n_cand], dtype=bool)]
+    g_e = top_m(se, eligible, min(k_e, len(eligible)))
+    rest = np.setdiff1d(cands, g_e, assume_unique=True)
+    g_q = top_m(sq, rest, min(k - len(g_e), len(rest)))
+    new_elig = np.zeros(n_cand, dtype=bool)
+    new_elig[g_e] = True
+    return g_e, g_q, new_elig
+
+
+# ----------------------------------------------------------------------------
+# Methodology §2, Optimized Memory Layout: set-difference for block swapping.
+# ----------------------------------------------------------------------------
+def set_difference(gamma, slot2blk: np.ndarray, just_completed: int):
+    """Loads, free slots and the new slot table for the selected set ``gamma`` (R13).
+
+    slot2blk[s] is the block held by slot s (-1: empty). Returns
+    (loads [(blk, slot, src)], free_slots, new_slot2blk).
+    """
+    gamma = set(int(b) for b in gamma)
+    resident = set(int(b) for b in slot2blk if b >= 0)
+    load_blocks = sorted(gamma - resident)
+    free = [s for s in range(len(slot2blk))
+            if slot2blk[s] < 0 or int(slot2blk[s]) not in gamma]
+    assert len(free) >= len(load_blocks)
+    new = np.array(slot2blk, dtype=np.int64).copy()
+    loads = []
+    for blk, slot in zip(load_blocks, free):
+        loads.append((blk, slot, TAIL if blk == just_completed else HOST))
+        new[slot] = blk
+    for slot in free[len(load_blocks):]:
+        new[slot] = -1
+    return loads, free, new
+
+
+# ----------------------------------------------------------------------------
+# Methodology §1, ED-DMA: attention with the eviction logit added before the exp.
+# ----------------------------------------------------------------------------
+def attend(q_group: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray, e_tok: np.ndarray):
+    """Softmax attention of G query rows over n tokens with an additive eviction logit.
+
+    l_j = q . k_j / sqrt(d) + e_j (R9); out = sum_j softmax(l)_j v_j; lse = log sum_j exp(l_j).
+    """
+    d = q_group.shape[1]
+    logits = q_group @ k_tok.T / math.sqrt(d) + e_tok[None, :]
+    m = logits.max(axis=1, keepdims=True)
+    w = np.exp(logits - m)
+    l = w.sum(axis=1)
+    out = (w @ v_tok) / l[:, None]
+    lse = m[:, 0] + np.log(l)
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# The block payload bytes (the library's documented block unit layout).
+# ----------------------------------------------------------------------------
+def payload_bytes(block: int, head_dim: int, dtype: str) -> int:
+    elt = 4 if dtype == "f32" else 2
+    raw = 2 * block * head_dim * elt + 4 * block
+    return (raw + 255) // 256 * 256
+
+
+def encode_payload(k_raw: np.ndarray, v_raw: np.ndarray, e: np.ndarray, dtype: str) -> np.ndarray:
+    """Bytes of one block unit: K in 16-byte chunk-major order, V token-major, e fp32, zero pad.
+
+    K: element (t, dim) sits at byte ((dim // c) * B + t) * 16 + (dim % c) * elt with
+    c = 16 // elt; V: element (t, dim) at B*d*elt + (t*d + dim) * elt; e[t] at
+    2*B*d*elt + 4*t.
+    """
+    B, d = k_raw.shape
+    elt = 4 if dtype == "f32" else 2
+    c = 16 // elt
+    kc = np.ascontiguousarray(k_raw.reshape(B, d // c, c).transpose(1, 0, 2))
+    out = np.zeros(payload_bytes(B, d, dtype), dtype=np.uint8)
+    kb = kc.view(np.uint8).reshape(-1)
+    vb = np.ascontiguousarray(v_raw).view(np.uint8).reshape(-1)
+    eb = np.ascontiguousarray(e, dtype=np.float32).view(np.uint8).reshape(-1)
+    out[:kb.size] = kb
+    out[kb.size:kb.size + vb.size] = vb
+    out[kb.size + vb.size:kb.size + vb.size + eb.size] = eb
+    return out
+
+
+# ----------------------------------------------------------------------------
+# One (request, KV head) unit over time.
+# ----------------------------------------------------------------------------
+def _to_f64(raw: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        return np.asarray(raw, dtype=np.float32).astype(np.float64)
+    return (np.asarray(raw, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+        np.float32).astype(np.float64)
+
+
+class UnitOracle:
+    """State of one unit: every token, pooled candidates, eligibility and the slot table.
+
+    Tokens are kept in their stored form (fp32 or bf16 bit patterns) and widened
+    to fp64 where used.
+    """
+
+    def __init__(self, head_dim: int, dtype: str, k: int, k_e: int, capacity: int,
+                 block: int = 64, sub_block: int = 16):
+        if block % sub_block or k_e > k:
+            raise ValueError("bad configuration")
+        self.d, self.dtype, self.k, self.k_e = head_dim, dtype, k, k_e
+        self.B, self.S = block, sub_block
+        self.P = block // sub_block
+        self.cap = capacity
+        raw_t = np.float32 if dtype == "f32" else np.uint16
+        self.k_raw = np.zeros((capacity, head_dim), raw_t)
+        self.v_raw = np.zeros((capacity, head_dim), raw_t)
+        self.e = np.zeros(capacity, np.float32)
+        nblk = (capacity + block - 1) // block
+        self.k_bar = np.zeros((nblk, self.P, head_dim))
+        self.e_bar = np.zeros((nblk, self.P))
+        self.se = np.zeros(nblk)
+        self.elig = np.zeros(nblk, dtype=bool)
+        self.slot2blk = -np.ones(k, dtype=np.int64)
+        self.L = 0
+        self.steps = 0
+        self.just_completed = -1
+        self.n_cand_prev = 0
+
+    # -- R7: appending a token; a block becomes a candidate when the next opens --
+    @property
+    def n_cand(self) -> int:
+        return (self.L - 1) // self.B if self.L > 0 else 0
+
+    def _push(self, k_raw, v_raw, e) -> int:
+        if self.L >= self.cap:
+            raise ValueError("context capacity exceeded")
+        t = self.L
+        self.k_raw[t], self.v_raw[t], self.e[t] = k_raw, v_raw, e
+        self.L += 1
+        opened = -1
+        if t % self.B == 0 and t > 0:
+            blk = t // self.B - 1
+            lo, hi = blk * self.B, (blk + 1) * self.B
+            kb, eb, sb = pool_block(_to_f64(self.k_raw[lo:hi], self.dtype),
+                                    self.e[lo:hi].astype(np.float64), self.S)
+            self.k_bar[blk], self.e_bar[blk], self.se[blk] = kb, eb, sb
+            self.elig[blk] = True
+            opened = blk
+        return opened
+
+    def append(self, k_raw: np.ndarray, v_raw: np.ndarray, e: np.ndarray) -> None:
+        """Prompt append of n tokens: no selection, no eviction (R11)."""
+        for i in range(len(e)):
+            self._push(k_raw[i], v_raw[i], e[i])
+        self.just_completed = -1
+
+    def tokens_f64(self, lo: int, hi: int):
+        return (_to_f64(self.k_raw[lo:hi], self.dtype), _to_f64(self.v_raw[lo:hi], self.dtype),
+                self.e[lo:hi].astype(np.float64))
+
+    # -- one decode step, in phases so a harness can compare each one --
+    def begin_step(self, k_raw, v_raw, e) -> None:
+        """Append the step's token; remember the block that just became a candidate."""
+        self.just_completed = self._push(k_raw, v_raw, e)
+
+    def scores(self, q_group_raw: np.ndarray):
+        """Query-aware and eviction scores of the current candidates, fp64."""
+        q = _to_f64(q_group_raw, self.dtype)
+        n = self.n_cand
+        sq = block_scores(group_query(q), self.k_bar[:n])
+        return sq, self.se[:n].copy()
+
+    def select(self, sq: np.ndarray, se: np.ndarray):
+        return dual_select(sq, se, self.elig, self.n_cand, self.k, self.k_e)
+
+    def commit(self, g_e: np.ndarray, g_q: np.ndarray) -> dict:
+        """Apply a selection: eligibility update (R5), set-difference (R13), locality."""
+        n = self.n_cand
+        new_elig = np.zeros(n, dtype=bool)
+        new_elig[np.asarray(g_e, dtype=np.int64)] = True
+        self.elig[:n] = new_elig
+        gamma = sorted(set(int(x) for x in g_e) | set(int(x) for x in g_q))
+        resident_prev = set(int(b) for b in self.slot2blk if b >= 0)
+        if self.just_completed >= 0:
+            resident_prev.add(self.just_completed)
+        loads, free, new = set_difference(gamma, self.slot2blk, self.just_completed)
+        self.slot2blk = new
+        self.steps += 1
+        hits = len(set(gamma) & resident_prev)
+        return {"loads": loads, "free": free, "gamma": gamma, "hits": hits,
+                "n_host": sum(1 for l in loads if l[2] == HOST),
+                "gamma_locality": hits / self.k}
+
+    def attention(self, q_group_raw: np.ndarray):
+        """Attention over the resident selected blocks plus the tail tokens (R7, R9)."""
+        q = _to_f64(q_group_raw, self.dtype)
+        parts = [np.arange(b * self.B, (b + 1) * self.B) for b in sorted(self.slot2blk) if b >= 0]
+        parts.append(np.arange(self.n_cand * self.B, self.L))
+        idx = np.concatenate(parts)
+        k, v, e = (_to_f64(self.k_raw[idx], self.dtype), _to_f64(self.v_raw[idx], self.dtype),
+                   self.e[idx].astype(np.float64))
+        return attend(q, k, v, e)
+
+    def decode_step(self, q_group_raw, k_raw, v_raw, e) -> dict:
+        """A whole step with the oracle's own selection."""
+        self.begin_step(k_raw, v_raw, e)
+        sq, se = self.scores(q_group_raw)
+        g_e, g_q, _ = self.select(sq, se)
+        info = self.commit(g_e, g_q)
+        out, lse = self.attention(q_group_raw)
+        info.update({"g_e": g_e, "g_q": g_q, "sq": sq, "se": se, "out": out, "lse": lse})
+        return info
+
+    def block_payload(self, blk: int) -> np.ndarray:
+        lo, hi = blk * self.B, (blk + 1) * self.B
+        return encode_payload(self.k_raw[lo:hi], self.v_raw[lo:hi], self.e[lo:hi], self.dtype)

@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for the NOSA decode path.
+
+This module is data plumbing shared by the fp64 oracle (tests) and the GPU side
+(tests, bench). It holds none of the method's arithmetic: it only defines how the
+keys, values, eviction logits and queries of the five workloads are drawn.
+
+Definition (the CUDA generator in ``synth/gen.cu`` implements the same one and is
+checked against this file bit for bit):
+
+* ``splitmix64`` is the published 64-bit finaliser of Steele, Lea and Flood
+  (golden-gamma increment, then two xor-shift-multiply rounds).
+* A draw is addressed by a counter with fields
+  ``stream:3 | a:10 | h:7 | t:26 | i:18`` (high to low bits); ``a`` is the request,
+  ``h`` the head, ``t`` the token (or block, or decode step) and ``i = 4*dim + j``.
+  The word for ``j`` is ``splitmix64(counter ^ splitmix64(seed))``.
+* A standard-normal stand-in is the centred Irwin-Hall sum of twelve 16-bit
+  uniforms (the four 16-bit lanes of the words ``j = 0, 1, 2``):
+  ``(sum - 393210) / 65536``. Mean 0, variance 1 - 2**-32, support (-6, 6).
+  Every value is a multiple of 2**-16 below 2**3, so it is exact in fp32 and
+  fp64 on any machine; no transcendental function is involved.
+* Keys: ``k = c[b, h, block(t)] + 0.5 * n[b, h, t]``, one centre ``c`` per
+  (request, KV head, 64-token block) and i.i.d. noise ``n``; exact in fp32.
+* Values ``v ~ N(0, 1)``; eviction logits ``e ~ N(0, 1)`` (fp32, fixed at write).
+* Queries: AR(1) per (request, query head, dim), ``q_0 = eps_0``,
+  ``q_s = rho * q_{s-1} + eps_s`` in fp64 (a product, then a sum: no fused
+  multiply-add), stored as fp64 -> fp32 (RNE) -> dtype.
+* bf16 storage rounds fp32 to nearest even.
+
+The GPU kernels never see this module's code; they get the arrays it (or its
+CUDA twin) writes.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+import numpy as np
+
+__all__ = [
+    "Workload", "WORKLOADS", "splitmix64", "normals", "keys", "values", "evict",
+    "queries", "to_storage", "storage_to_f64", "bf16_bits_to_f64",
+    "STREAM_CENTER", "STREAM_KNOISE", "STREAM_VALUE", "STREAM_EVICT", "STREAM_QINNOV",
+]
+
+_M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_C1 = np.uint64(0xBF58476D1CE4E5B9)
+_C2 = np.uint64(0x94D049BB133111EB)
+
+STREAM_CENTER = 0
+STREAM_KNOISE = 1
+STREAM_VALUE = 2
+STREAM_EVICT = 3
+STREAM_QINNOV = 4
+
+IH_MEAN = 393210          # 12 * 65535 / 2
+IH_SCALE = 1.0 / 65536.0  # exact power of two
+
+
+@dataclass(frozen=True)
+class Workload:
+    """Shape of one synthetic decode workload (one layer)."""
+    name: str
+    batch: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    dtype: str            # "f32" or "bf16"
+    prompt: int           # tokens appended before the first decode step
+    steps: int            # decode steps, one token appended per step
+    k: int
+    k_e: int
+    rho: float = 0.95
+    block: int = 64
+    sub_block: int = 16
+    seed: int = 0
+
+    @property
+    def group(self) -> int:
+        return self.n_q_heads // self.n_kv_heads
+
+    @property
+    def units(self) -> int:
+        return self.batch * self.n_kv_heads
+
+    @property
+    def max_context(self) -> int:
+        return self.prompt + self.steps
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads: one tiny fp32 case and four bf16 cases shaped like the
+# 1B / 3B / 8B models of the NOSA paper's decode experiments.
+WORKLOADS = {
+    "tiny-f32": Workload("tiny-f32", 1, 4, 1, 64, "f32", 2048, 32, 8, 6),
+    "1b-bf16": Workload("1b-bf16", 8, 16, 8, 64, "bf16", 16384, 128, 64, 48),
+    "3b-bf16": Workload("3b-bf16", 16, 24, 8, 128, "bf16", 32768, 256, 64, 48),
+    "8b-longgen-bf16": Workload("8b-longgen-bf16", 16, 32, 8, 128, "bf16", 8192, 16384,
+                                128, 96, rho=0.9),
+    "8b-offload-bf16": Workload("8b-offload-bf16", 32, 32, 8, 128, "bf16", 65536, 64, 64, 48),
+}
+
+
+def splitmix64(x):
+    """splitmix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    x = np.asarray(x, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = x + _GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _C1
+        z = (z ^ (z >> np.uint64(27))) * _C2
+    return z ^ (z >> np.uint64(31))
+
+
+def _counter(stream, a, h, t, i):
+    u = np.uint64
+    a = np.asarray(a, dtype=np.uint64)
+    h = np.asarray(h, dtype=np.uint64)
+    t = np.asarray(t, dtype=np.uint64)
+    i = np.asarray(i, dtype=np.uint64)
+    return ((u(stream) << u(61)) | (a << u(51)) | (h << u(44)) | (t << u(18)) | i)
+
+
+def normals(seed: int, stream: int, a, h, t, dim) -> np.ndarray:
+    """Exact Irwin-Hall(12) normal stand-ins, broadcast over a, h, t, dim (fp64)."""
+    smix = splitmix64(np.uint64(seed))
+    dim4 = np.asarray(dim, dtype=np.uint64) * np.uint64(4)
+    acc = None
+    for j in range(3):
+        w = splitmix64(_counter(stream, a, h, t, dim4 + np.uint64(j)) ^ smix)
+        s = ((w & np.uint64(0xFFFF)) + ((w >> np.uint64(16)) & np.uint64(0xFFFF))
+             + ((w >> np.uint64(32)) & np.uint64(0xFFFF)) + (w >> np.uint64(48)))
+        acc = s if acc is None else acc + s
+    return (acc.astype(np.int64) - IH_MEAN).astype(np.float64) * IH_SCALE
+
+
+def _f32_to_bf16_bits(x32: np.ndarray) -> np.ndarray:
+    b = x32.astype(np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    return ((b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def to_storage(x64: np.ndarray, dtype: str) -> np.ndarray:
+    """fp64 -> fp32 (RNE) -> storage dtype; bf16 is returned as uint16 bit patterns."""
+    x32 = np.asarray(x64, dtype=np.float64).astype(np.float32)
+    if dtype == "f32":
+        return x32
+    if dtype == "bf16":
+        return _f32_to_bf16_bits(x32)
+    raise ValueError(dtype)
+
+
+def storage_to_f64(s: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        return np.asarray(s, dtype=np.float32).astype(np.float64)
+    return bf16_bits_to_f64(np.asarray(s, dtype=np.uint16))
+
+
+def keys(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
+    """Stored keys of tokens [t0, t0+n) of (request b, KV head h): [n][d] storage dtype."""
+    t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
+    dim = np.arange(w.head_dim, dtype=np.int64)[None, :]
+    c = normals(w.seed, STREAM_CENTER, b, h, t // w.block, dim)
+    noise = normals(w.seed, STREAM_KNOISE, b, h, t, dim)
+    return to_storage(c + 0.5 * noise, w.dtype)
+
+
+def values(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
+    t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
+    dim = np.arange(w.head_dim, dtype=np.int64)[None, :]
+    return to_storage(normals(w.seed, STREAM_VALUE, b, h, t, dim), w.dtype)
+
+
+def evict(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
+    """Per-token eviction logits of (b, KV head h): [n] fp32."""
+    t = np.arange(t0, t0 + n, dtype=np.int64)
+    return normals(w.seed, STREAM_EVICT, b, h, t, 0).astype(np.float32)
+
+
+def queries(w: Workload, b: int, heads, steps: int) -> np.ndarray:
+    """AR(1) queries of request b for the given query heads: [steps][len(heads)][d] storage."""
+    heads = np.asarray(list(heads), dtype=np.int64)
+    dim = np.arange(w.head_dim, dtype=np.int64)[None, :]
+    out = np.empty((steps, len(heads), w.head_dim),
+                   dtype=np.float32 if w.dtype == "f32" else np.uint16)
+    q = None
+    for s in range(steps):
+        eps = normals(w.seed, STREAM_QINNOV, b, heads[:, None], s, dim)
+        if q is None:
+            q = eps
+        else:
+            q = np.float64(w.rho) * q
+            q = q + eps
+        out[s] = to_storage(q, w.dtype)
+    return out
