@@ -1,0 +1,243 @@
+/*
+ * nosa.h -- C ABI of the NOSA decode-step hot path on one GB300 (sm_103a).
+ *
+ * NOSA ("Native and Offloadable Sparse Attention", technical summary at
+ * gist.science/paper/2510.13602) keeps the KV cache of long contexts in host
+ * memory in block-sized units and, at every decode step, attends only to k
+ * selected blocks per (request, KV head) that are cached on the GPU:
+ *
+ *   1. two-stage pooled block scoring (Methodology §1, "Block-Wise
+ *      Implementation": mean pooling inside 16-token sub-blocks, max pooling
+ *      over the sub-blocks of a 64-token block);
+ *   2. dual selection Gamma = Gamma_e U Gamma_q (Methodology §1, "Dual-Selection
+ *      Mechanism"): a query-agnostic top-k_e over eviction scores under the
+ *      strict rule that a block left out of Gamma_e is never eligible again,
+ *      plus a query-aware top-(k - |Gamma_e|) over q . pooled-key scores;
+ *   3. the set-difference of Gamma against the GPU-resident block slots
+ *      (Methodology §2, "Optimized Memory Layout");
+ *   4. a UVA gather of the missing blocks from pinned host memory into the
+ *      freed slots (Methodology §2, "High-Bandwidth Communication");
+ *   5. block-sparse flash-decoding attention over the selected blocks and the
+ *      newest (tail) block, with each token's eviction logit added to its
+ *      scaled q.k logit before the softmax (Methodology §1, "ED-DMA").
+ *
+ * A "unit" is one (request b, KV head h); units are independent. Query head g
+ * of a request belongs to KV head g / G with G = n_q_heads / n_kv_heads.
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device (or managed) addresses and stay valid
+ *     until the stream has reached the call. q, k, v, out and block units must
+ *     be 16-byte aligned; e, lse and index tables 4-byte aligned
+ *     (NOSA_ERR_INVALID_ARG otherwise).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls marked "async" only enqueue work on it.
+ *   - Every call returns a nosa_status; nosa_last_error(h) gives a message.
+ *     After a CUDA error the handle enters NOSA_ERR_STATE and refuses further
+ *     steps (destroy it).
+ *   - A handle is not thread-safe; use one host thread per handle.
+ */
+#ifndef NOSA_H
+#define NOSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NOSA_OK = 0,
+  NOSA_ERR_INVALID_ARG = 1, /* bad configuration, pointer, size or alignment     */
+  NOSA_ERR_OOM = 2,         /* device allocation failed                          */
+  NOSA_ERR_HOST_OOM = 3,    /* pinned host allocation failed                     */
+  NOSA_ERR_CAPACITY = 4,    /* the context would exceed max_context              */
+  NOSA_ERR_CUDA = 5,        /* a CUDA call or kernel failed                      */
+  NOSA_ERR_STATE = 6,       /* handle unusable after an earlier CUDA error       */
+  NOSA_ERR_UNSUPPORTED = 7  /* shape outside the compiled kernel variants        */
+} nosa_status;
+
+typedef enum { NOSA_F32 = 0, NOSA_BF16 = 1 } nosa_dtype;
+
+/* Flags of nosa_config.flags. */
+#define NOSA_FLAG_TIMING 1u /* record CUDA events around each phase (stats.t_us) */
+
+/*
+ * Configuration, fixed at nosa_create.
+ *   batch, n_q_heads, n_kv_heads : requests and heads; n_q_heads % n_kv_heads == 0,
+ *                                  G = n_q_heads / n_kv_heads in {1,2,3,4,6,8}.
+ *   head_dim                     : d, 64 or 128.
+ *   dtype                        : nosa_dtype of q, k, v and out.
+ *   block, sub_block             : B and S tokens; B = 64, S = 16 (P = 4 sub-blocks).
+ *   k, k_e                       : selected blocks per unit and the query-agnostic
+ *                                  share; 0 <= k_e <= k, 1 <= k <= 256.
+ *   max_context                  : capacity in tokens per request (sizes the host store);
+ *                                  ceil(max_context / B) <= 32768,
+ *                                  batch * n_kv_heads <= 65535.
+ *   device                       : CUDA device ordinal.
+ *   flags                        : NOSA_FLAG_* bits.
+ */
+typedef struct {
+  int32_t batch, n_q_heads, n_kv_heads, head_dim;
+  int32_t dtype;
+  int32_t block, sub_block, k, k_e;
+  int32_t max_context;
+  int32_t device;
+  uint32_t flags;
+} nosa_config;
+
+/*
+ * Block unit ("minimal block-sized unit", Methodology §2). One unit holds the
+ * B tokens of one (request, KV head, block) and is the byte image copied
+ * between the host store, the tail buffers and the slot pool:
+ *   K : bytes [0, B*d*elt)        16-byte chunk-major: element (t, dim) at
+ *                                 ((dim / c) * B + t) * 16 + (dim % c) * elt, c = 16 / elt
+ *   V : bytes [B*d*elt, 2*B*d*elt) token-major: element (t, dim) at + (t*d + dim) * elt
+ *   e : fp32 eviction logits, e[t] at 2*B*d*elt + 4*t
+ *   zero padding to a multiple of 256 bytes.
+ * elt = 4 (NOSA_F32) or 2 (NOSA_BF16). Returns the unit size in bytes
+ * (33024 for B=64, d=128 bf16 or d=64 fp32; 16640 for d=64 bf16), 0 if invalid.
+ */
+size_t nosa_payload_bytes(const nosa_config* cfg);
+
+/*
+ * Checks a configuration without touching any GPU. Writes a reason into msg
+ * (if non-NULL, NUL-terminated, at most msg_len bytes) when it is rejected.
+ */
+nosa_status nosa_config_validate(const nosa_config* cfg, char* msg, size_t msg_len);
+
+typedef struct nosa_handle nosa_handle;
+
+/*
+ * Creates a handle: allocates, on cfg->device, the slot pool [U][k] units, the
+ * double-buffered tail [U][2] units, pooled keys [U][maxBlk][P][d] fp32,
+ * eviction scores, eligibility bitmasks, slot tables and scratch; and the host
+ * store [U][maxBlk] units in pinned, mapped host memory (U = batch *
+ * n_kv_heads, maxBlk = ceil(max_context / B)). The handle owns all of it.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, HOST_OOM, CUDA. *out is NULL on error.
+ */
+nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out);
+
+/*
+ * Appends n_tokens tokens to every request (the prompt, or more context).
+ * Async. k, v : device [batch][n_tokens][n_kv_heads][d] of cfg dtype;
+ * e : device fp32 [batch][n_tokens][n_kv_heads]. Blocks that become candidates
+ * (every block but the newest) are pooled, marked eligible and written to the
+ * host store; no selection or eviction happens here (the cold start: the next
+ * decode step loads min(k, N) blocks). CAPACITY if the context would exceed
+ * max_context (nothing is enqueued). n_tokens = 0 is a no-op.
+ */
+nosa_status nosa_append_kv(nosa_handle* h, int32_t n_tokens, const void* k, const void* v,
+                           const float* e, void* stream);
+
+/*
+ * One decode step for every request. Async.
+ *   q     : device [batch][n_q_heads][d] cfg dtype (the step's queries)
+ *   k_new : device [batch][n_kv_heads][d] cfg dtype (the step's new key)
+ *   v_new : device [batch][n_kv_heads][d] cfg dtype
+ *   e_new : device fp32 [batch][n_kv_heads] (the new token's eviction logit)
+ *   out   : device [batch][n_q_heads][d] cfg dtype (written)
+ *   lse   : device fp32 [batch][n_q_heads] natural-log sum-exp of the logits, or NULL
+ * Order: append the token (incremental pooling: a completed 16-token sub-block
+ * is averaged, the block's eviction score is the max of its sub-block means;
+ * the block before a newly opened one becomes a candidate, eligible, and is
+ * written back to the host store) -> score -> dual select -> set-difference ->
+ * gather -> split-K attention -> combine. The context must be >= 1 token
+ * before the call (STATE otherwise). CAPACITY when the context is full.
+ */
+nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
+                             const float* e_new, void* out, float* lse, void* stream);
+
+/* Counters, host-readable. gamma_* covers steps after the first decode step
+ * with at least k candidates; gamma(t) = |Gamma(t) ∩ R(t-1)| / k where R(t-1)
+ * is the resident blocks plus the block that was the tail at t-1. */
+typedef struct {
+  int64_t steps;                 /* decode steps run                               */
+  int64_t context;               /* tokens per request after the last call         */
+  int64_t host_loads;            /* blocks gathered from the host store            */
+  int64_t tail_loads;            /* blocks copied from the old tail buffer         */
+  int64_t host_bytes;            /* bytes gathered from the host store             */
+  int64_t cold_host_loads;       /* host loads of the first decode step            */
+  int32_t max_host_loads_unit;   /* max host loads of one unit in one step (warm)  */
+  int32_t min_hits;              /* min |Gamma ∩ R(t-1)| over units and warm steps */
+  int64_t sum_hits;              /* sum of |Gamma ∩ R(t-1)| over the same          */
+  int64_t hit_samples;           /* number of (unit, step) samples in sum_hits     */
+  double gamma_min, gamma_mean;  /* min_hits / k and sum_hits / (k * hit_samples)  */
+  int64_t near_ties;             /* top-k cuts whose k-th and (k+1)-th fp32 scores
+                                    differ by < 1e-5 * max |score|                  */
+  int32_t device_error;          /* nonzero: a bounded wait in a kernel gave up     */
+  int32_t pad_;
+  /* Accumulated device time (microseconds) of each phase when NOSA_FLAG_TIMING:
+   * [0] append+pool, [1] score, [2] select, [3] set-difference, [4] gather,
+   * [5] attention, [6] combine, [7] whole step.  t_count = steps timed. */
+  double t_us[8];
+  int64_t t_count;
+} nosa_stats_t;
+
+/* Synchronises the handle's last stream and fills *out. */
+nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out);
+
+/* Clears the counters and timers of nosa_stats (not the state). */
+nosa_status nosa_stats_reset(nosa_handle* h);
+
+/*
+ * Debug read-back (synchronous, for tests). Copies `bytes` bytes starting at
+ * byte `offset` of the chosen array into host memory `dst`. INVALID_ARG if the
+ * range is outside the array. Arrays (U units, W = ceil(maxBlk / 32)):
+ *   NOSA_DBG_SEL      int32 [U][k]   Gamma_e ascending then Gamma_q ascending, -1 pad
+ *   NOSA_DBG_NSEL     int32 [U][2]   |Gamma_e|, |Gamma_q|
+ *   NOSA_DBG_ELIG     uint32 [U][W]  eligibility bitmask (bit i%32 of word i/32)
+ *   NOSA_DBG_SLOTS    int32 [U][k]   block held by each slot, -1 empty
+ *   NOSA_DBG_LOADS    int32 [U][k][3] load list (block, slot, src: 0 host, 1 tail)
+ *   NOSA_DBG_NLOAD    int32 [U]      loads of the last step
+ *   NOSA_DBG_POOLED   fp32 [U][maxBlk][P][d] sub-block mean keys
+ *   NOSA_DBG_SE       fp32 [U][maxBlk] block eviction scores (max of sub-block means)
+ *   NOSA_DBG_SQ       fp32 [U][maxBlk] query-aware block scores of the last step
+ *   NOSA_DBG_SLOTPOOL bytes [U][k][payload]  slot pool
+ *   NOSA_DBG_HOST     bytes [U][maxBlk][payload] host store
+ *   NOSA_DBG_TAIL     bytes [U][2][payload] tail buffers (block b uses buffer b % 2)
+ */
+enum {
+  NOSA_DBG_SEL = 0, NOSA_DBG_NSEL, NOSA_DBG_ELIG, NOSA_DBG_SLOTS, NOSA_DBG_LOADS,
+  NOSA_DBG_NLOAD, NOSA_DBG_POOLED, NOSA_DBG_SE, NOSA_DBG_SQ, NOSA_DBG_SLOTPOOL,
+  NOSA_DBG_HOST, NOSA_DBG_TAIL, NOSA_DBG_COUNT_
+};
+nosa_status nosa_debug_read(nosa_handle* h, int32_t what, size_t offset, void* dst, size_t bytes);
+
+/* Size in bytes of a debug array (0 for an unknown id). */
+size_t nosa_debug_size(const nosa_handle* h, int32_t what);
+
+/* Releases everything the handle owns (synchronises its device first). NULL is a no-op. */
+void nosa_destroy(nosa_handle* h);
+
+/* Last error message of the handle ("" if none); valid until the next call on h.
+ * With h == NULL: the last error of nosa_create on this thread. */
+const char* nosa_last_error(const nosa_handle* h);
+
+/*
+ * Block-sparse decode attention (step 5 alone) over caller-owned block units,
+ * the same split-K kernel nosa_decode_step runs. Async.
+ *   units      : device array of n_units block units (layout above)
+ *   n_units    : number of units in `units`
+ *   block_tab  : device int32 [U][n_blocks] unit index of each attended block,
+ *                -1 = skip; an index outside [0, n_units) is skipped and flagged
+ *                in the workspace's error word (see below)
+ *   tail       : device units [U] (the partial newest block of each unit) or NULL
+ *   tail_len   : tokens valid in each tail unit (0..B; ignored if tail is NULL)
+ *   q, out, lse: as in nosa_decode_step (lse may be NULL)
+ *   workspace  : device scratch of nosa_attention_workspace_bytes(...) bytes,
+ *                16-byte aligned; holds the split-K partials. Its last 16 bytes
+ *                start with an int32 error word (0 = ok, 2 = bad block index,
+ *                1 = a bounded wait gave up), cleared by each call.
+ * U = batch * n_kv_heads from cfg; only the shape fields of cfg are used.
+ */
+size_t nosa_attention_workspace_bytes(const nosa_config* cfg, int32_t n_blocks);
+nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int64_t n_units,
+                                  const int32_t* block_tab, int32_t n_blocks, const void* tail,
+                                  int32_t tail_len, const void* q, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NOSA_H */

@@ -1,0 +1,125 @@
+// CUDA twin of synth/__init__.py: writes the same seeded synthetic inputs on the
+// device, bit for bit (integer hashing, exact fp64 arithmetic, then the same
+// RNE roundings). Shared by the tests and the bench; holds none of the method's
+// arithmetic.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace {
+
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+
+// Irwin-Hall(12) normal stand-in addressed by (stream, a, h, t, dim); exact.
+__device__ __forceinline__ double ih_normal(uint64_t smix, uint64_t stream, uint64_t a, uint64_t h,
+                                            uint64_t t, uint64_t dim) {
+  const uint64_t base = (stream << 61) | (a << 51) | (h << 44) | (t << 18) | (dim * 4);
+  long long s = 0;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const uint64_t w = splitmix64((base + (uint64_t)j) ^ smix);
+    s += (long long)((w & 0xFFFF) + ((w >> 16) & 0xFFFF) + ((w >> 32) & 0xFFFF) + (w >> 48));
+  }
+  return (double)(s - 393210) * (1.0 / 65536.0);
+}
+
+template <typename T> __device__ __forceinline__ T store_as(double x);
+template <> __device__ __forceinline__ float store_as<float>(double x) { return __double2float_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 store_as<__nv_bfloat16>(double x) {
+  return __float2bfloat16_rn(__double2float_rn(x));
+}
+
+// k, v: [batch][n][Hkv][d]; e: [batch][n][Hkv] for tokens t0 .. t0+n-1
+// (token-major [n][batch][Hkv][d] and [n][batch][Hkv] when step_major).
+template <typename T>
+__global__ void kv_kernel(T* k, T* v, float* e, int batch, int hkv, int d, long long t0, int n,
+                          int block, uint64_t smix, int step_major) {
+  const long long total = (long long)batch * n * hkv * d;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int dim = (int)(i % d);
+    long long r = i / d;
+    const int h = (int)(r % hkv);
+    r /= hkv;
+    long long t;
+    int b;
+    if (step_major) {
+      b = (int)(r % batch);
+      t = t0 + r / batch;
+    } else {
+      t = t0 + r % n;
+      b = (int)(r / n);
+    }
+    const double c = ih_normal(smix, 0, b, h, t / block, dim);
+    const double nz = ih_normal(smix, 1, b, h, t, dim);
+    k[i] = store_as<T>(c + 0.5 * nz);
+    if (v) v[i] = store_as<T>(ih_normal(smix, 2, b, h, t, dim));
+    if (e && dim == 0) e[i / d] = (float)ih_normal(smix, 3, b, h, t, 0);
+  }
+}
+
+// q: [steps][batch][hq][d], AR(1) over steps, fp64 state (no fused multiply-add).
+template <typename T>
+__global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, uint64_t smix) {
+  const int total = batch * hq * d;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int dim = i % d, g = (i / d) % hq, b = i / (d * hq);
+  double x = 0.0;
+  for (int s = 0; s < steps; ++s) {
+    const double eps = ih_normal(smix, 4, b, g, s, dim);
+    x = (s == 0) ? eps : __dadd_rn(__dmul_rn(rho, x), eps);
+    q[(long long)s * total + i] = store_as<T>(x);
+  }
+}
+
+uint64_t seed_mix(uint64_t seed) {
+  uint64_t x = seed + 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+// dtype 0 = fp32, 1 = bf16. Returns a cudaError_t.
+int synth_kv(void* k, void* v, float* e, int batch, int hkv, int d, long long t0, int n,
+             int block, unsigned long long seed, int dtype, int step_major, void* stream) {
+  const uint64_t smix = seed_mix(seed);
+  const long long total = (long long)batch * n * hkv * d;
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int grid = (int)(want < 65536 ? want : 65536);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (total == 0) return 0;
+  if (dtype == 0)
+    kv_kernel<float><<<grid, threads, 0, s>>>((float*)k, (float*)v, e, batch, hkv, d, t0, n,
+                                               block, smix, step_major);
+  else
+    kv_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>((__nv_bfloat16*)k, (__nv_bfloat16*)v, e,
+                                                       batch, hkv, d, t0, n, block, smix, step_major);
+  return (int)cudaGetLastError();
+}
+
+int synth_queries(void* q, int batch, int hq, int d, int steps, double rho,
+                  unsigned long long seed, int dtype, void* stream) {
+  const uint64_t smix = seed_mix(seed);
+  const int total = batch * hq * d;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (total == 0 || steps == 0) return 0;
+  if (dtype == 0)
+    q_kernel<float><<<(total + 127) / 128, 128, 0, s>>>((float*)q, batch, hq, d, steps, rho, smix);
+  else
+    q_kernel<__nv_bfloat16><<<(total + 127) / 128, 128, 0, s>>>((__nv_bfloat16*)q, batch, hq, d,
+                                                                 steps, rho, smix);
+  return (int)cudaGetLastError();
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+"""CPU checks of the boundary: the library loads, exports every symbol the
+header declares, agrees with the header's struct layout, and validates
+configurations on the host (no GPU needed)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+import trainable_sparse_attention_decode_gb300 as nosa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nosa.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nosa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert len(names) >= 13
+    lib = C.CDLL(nosa.lib_path)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_struct_layout_matches_header(tmp_path):
+    prog = tmp_path / "layout.c"
+    prog.write_text(r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "nosa.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(nosa_config), sizeof(nosa_stats_t),
+         offsetof(nosa_stats_t, gamma_min), offsetof(nosa_stats_t, near_ties),
+         offsetof(nosa_stats_t, t_us), offsetof(nosa_stats_t, t_count),
+         offsetof(nosa_config, flags));
+  return 0;
+}
+''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(prog), "-o",
+                    str(exe)], check=True)
+    vals = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True,
+                                        check=True).stdout.split()))
+    S = nosa.NosaStats
+    assert vals == [C.sizeof(nosa.NosaConfig), C.sizeof(S), S.gamma_min.offset,
+                    S.near_ties.offset, S.t_us.offset, S.t_count.offset,
+                    nosa.NosaConfig.flags.offset]
+
+
+def _cfg(**kw):
+    base = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, dtype="bf16", k=8, k_e=6,
+                max_context=4096)
+    base.update(kw)
+    return nosa.nosa_config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"dtype": "f32", "head_dim": 64}, 0),
+    ({"k_e": 9}, 1),
+    ({"k": 0, "k_e": 0}, 1),
+    ({"n_q_heads": 7}, 1),
+    ({"n_q_heads": 10}, 7),          # G = 5 is not compiled
+    ({"head_dim": 96}, 7),
+    ({"block": 32}, 7),
+    ({"block": 64, "sub_block": 24}, 1),
+    ({"max_context": 0}, 1),
+    ({"max_context": 64 * 32768 + 1}, 7),
+    ({"k": 257, "k_e": 0}, 7),
+    ({"flags": 2}, 1),
+])
+def test_config_validation(kw, status):
+    st, msg = nosa.nosa_config_validate(_cfg(**kw))
+    assert st == status, msg
+    assert (st == 0) == (msg == "")
+
+
+def test_payload_bytes():
+    assert nosa.nosa_payload_bytes(_cfg()) == 33024
+    assert nosa.nosa_payload_bytes(_cfg(dtype="f32", head_dim=64)) == 33024
+    assert nosa.nosa_payload_bytes(_cfg(head_dim=64)) == 16640
+    assert nosa.nosa_payload_bytes(_cfg(dtype="f32", head_dim=128)) == 65792
+    assert nosa.nosa_payload_bytes(_cfg(k_e=99)) == 0
+
+
+def test_create_without_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(nosa.NosaError) as ei:
+        nosa.nosa_create(_cfg())
+    assert ei.value.status == 5 and nosa.nosa_last_error() != ""
+
+
+def test_workspace_query_rejects_bad_config():
+    assert nosa.nosa_attention_workspace_bytes(_cfg(k_e=99), 8) == 0

@@ -1,0 +1,124 @@
+"""Parity of the CUDA decode path with the fp64 oracle, through the C ABI.
+
+Every step: selections (lock-step near-tie rule), load lists, slot tables and
+gathered bytes exact; attention within 1e-5 absolute (fp32) or 1e-2 x row RMS
+(bf16). The five workloads run at their full shapes; the large ones are checked
+on sampled units (units are independent, so a sampled unit is checked exactly).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import synth.gpu
+import trainable_sparse_attention_decode_gb300 as nosa
+from nosa_harness import GpuRun
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, units=None, steps=None, check_every=1, attn_every=1, pieces=None, check_bytes=True):
+    steps = w.steps if steps is None else steps
+    run = GpuRun(w, units=units, prompt_pieces=pieces, check_bytes=check_bytes,
+                 oracle_attention_every=attn_every)
+    q = synth.gpu.queries(w, steps)
+    worst, worst_lse = 0.0, 0.0
+    try:
+        for s in range(steps):
+            _, _, res = run.step(q[s], check=(s % check_every == 0))
+            if res:
+                worst = max(worst, res["worst_attn"])
+                worst_lse = max(worst_lse, res["worst_lse"])
+        st = run.stats()
+    finally:
+        run.close()
+    assert st["device_error"] == 0
+    assert worst <= 1.0, f"attention error / tolerance = {worst}"
+    assert worst_lse <= (1e-5 if w.dtype == "f32" else 1e-4) * 10
+    return st, run
+
+
+def test_tiny_f32_full():
+    st, run = _run(synth.WORKLOADS["tiny-f32"])
+    assert st["steps"] == 32 and st["cold_host_loads"] in (7, 8)
+
+
+def test_1b_bf16_sampled_units():
+    w = synth.WORKLOADS["1b-bf16"]
+    st, _ = _run(w, units=[0, 9, 37, 63])
+    k, ke = w.k, w.k_e
+    assert st["gamma_min"] >= ke / k - 1e-12          # locality bound on every unit
+    assert st["max_host_loads_unit"] <= k - ke
+
+
+def test_3b_bf16_sampled_units():
+    w = synth.WORKLOADS["3b-bf16"]
+    st, _ = _run(w, units=[5, 127], steps=96)
+    assert st["gamma_min"] >= w.k_e / w.k - 1e-12
+
+
+def test_8b_offload_sampled_units():
+    w = synth.WORKLOADS["8b-offload-bf16"]
+    st, _ = _run(w, units=[0, 255], steps=24, pieces=[4096] * 16, check_bytes=True)
+    assert st["gamma_min"] >= w.k_e / w.k - 1e-12
+
+
+@pytest.mark.parametrize("case", [
+    dict(prompt=37, steps=70, k=4, k_e=2),            # starts with no candidate block
+    dict(prompt=64 * 3, steps=70, k=8, k_e=3),        # fewer candidates than k for a while
+    dict(prompt=64 * 10 + 5, steps=80, k=4, k_e=0),   # no query-agnostic part
+    dict(prompt=64 * 10 + 63, steps=80, k=4, k_e=4),  # no query-aware part
+])
+def test_edge_cases_f32(case):
+    w = synth.WORKLOADS["tiny-f32"].with_(**case)
+    _run(w)
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(8, 8, 128, "bf16"), (12, 2, 64, "bf16"),
+                                           (16, 2, 128, "f32"), (12, 4, 64, "f32"),
+                                           (48, 8, 64, "bf16")])
+def test_group_and_dtype_variants(hq, hkv, d, dtype):
+    w = synth.Workload("var", 2, hq, hkv, d, dtype, 64 * 40 + 17, 40, 16, 10)
+    _run(w)
+
+
+def test_prompt_in_ragged_pieces():
+    w = synth.WORKLOADS["tiny-f32"].with_(prompt=64 * 20 + 9, steps=20)
+    _run(w, pieces=[1, 63, 64, 100, 28, 64 * 10, 64 * 5 + 9, 64])
+
+
+def test_capacity_and_state_errors():
+    w = synth.WORKLOADS["tiny-f32"].with_(prompt=128, steps=1)
+    cfg = nosa.nosa_config(1, 4, 1, 64, "f32", 4, 2, 129)
+    h = nosa.nosa_create(cfg)
+    try:
+        q = torch.zeros((1, 4, 64), device="cuda")
+        kv = torch.zeros((1, 1, 64), device="cuda")
+        e = torch.zeros((1, 1), device="cuda")
+        out = torch.empty_like(q)
+        with pytest.raises(nosa.NosaError) as ei:
+            nosa.nosa_decode_step(h, q, kv, kv, e, out)
+        assert ei.value.status == 6
+        k, v, ee = synth.gpu.kv(w, 0, 128)
+        nosa.nosa_append_kv(h, k, v, ee)
+        nosa.nosa_decode_step(h, q, kv, kv, e, out)
+        with pytest.raises(nosa.NosaError) as ei:
+            nosa.nosa_decode_step(h, q, kv, kv, e, out)
+        assert ei.value.status == 4
+        with pytest.raises(nosa.NosaError) as ei:
+            nosa.nosa_append_kv(h, k[:, :1], v[:, :1], ee[:, :1])
+        assert ei.value.status == 4
+        torch.cuda.synchronize()
+        assert nosa.nosa_stats(h)["device_error"] == 0
+    finally:
+        nosa.nosa_destroy(h)
+
+
+@pytest.mark.slow
+def test_8b_longgen_sampled_units_long_horizon():
+    # 16384 decode steps: selection, loads and slots checked every step on two
+    # units, attention every 16th step.
+    w = synth.WORKLOADS["8b-longgen-bf16"]
+    st, run = _run(w, units=[3, 100], attn_every=16, check_bytes=False)
+    assert st["gamma_min"] >= w.k_e / w.k - 1e-12
+    assert st["max_host_loads_unit"] <= w.k - w.k_e

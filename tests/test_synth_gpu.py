@@ -1,0 +1,37 @@
+"""The CUDA twin of the input generator writes exactly what the numpy generator defines."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import synth.gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "1b-bf16", "8b-offload-bf16"])
+def test_kv_matches_numpy(name):
+    w = synth.WORKLOADS[name]
+    t0, n = 2000, 150
+    k, v, e = synth.gpu.kv(w, t0, n)
+    ks, vs, es = synth.gpu.kv(w, t0, n, step_major=True)
+    for b, h in [(0, 0), (w.batch - 1, w.n_kv_heads - 1), (w.batch // 2, 0)]:
+        assert np.array_equal(_np(k[b, :, h]), synth.keys(w, b, h, t0, n))
+        assert np.array_equal(_np(v[b, :, h]), synth.values(w, b, h, t0, n))
+        assert np.array_equal(_np(e[b, :, h]), synth.evict(w, b, h, t0, n))
+        assert np.array_equal(_np(ks[:, b, h]), synth.keys(w, b, h, t0, n))
+        assert np.array_equal(_np(es[:, b, h]), synth.evict(w, b, h, t0, n))
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "8b-longgen-bf16"])
+def test_queries_match_numpy(name):
+    w = synth.WORKLOADS[name]
+    q = synth.gpu.queries(w, 300)
+    for b, heads in [(0, [0, 1]), (w.batch - 1, [w.n_q_heads - 1])]:
+        assert np.array_equal(_np(q[:, b, heads]), synth.queries(w, b, heads, 300))

@@ -1,0 +1,248 @@
+"""Python binding of libnosa (the NOSA decode-step hot path on one GB300).
+
+Thin ctypes marshalling over the C ABI declared in ``include/nosa.h``: every
+function here has the C function's name, checks tensor shapes, dtypes, devices
+and alignment, passes raw pointers and the current CUDA stream, and raises
+``NosaError`` on a non-OK status. All arithmetic runs in the CUDA kernels of
+``_lib/libnosa.so``; there is no CPU path. If the library has not been built the
+import fails loudly (build it with ``__graft_entry__.build()`` or
+``python -m trainable_sparse_attention_decode_gb300._build``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+__all__ = [
+    "NosaError", "NosaConfig", "NosaStats", "lib", "lib_path",
+    "NOSA_F32", "NOSA_BF16", "NOSA_FLAG_TIMING", "DBG",
+    "nosa_config", "nosa_config_validate", "nosa_payload_bytes", "nosa_create",
+    "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset",
+    "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
+    "nosa_attention_workspace_bytes", "nosa_sparse_attention",
+]
+
+NOSA_F32, NOSA_BF16 = 0, 1
+NOSA_FLAG_TIMING = 1
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "OOM", 3: "HOST_OOM", 4: "CAPACITY", 5: "CUDA",
+          6: "STATE", 7: "UNSUPPORTED"}
+DBG = {name: i for i, name in enumerate(
+    ["SEL", "NSEL", "ELIG", "SLOTS", "LOADS", "NLOAD", "POOLED", "SE", "SQ", "SLOTPOOL",
+     "HOST", "TAIL"])}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "_lib", "libnosa.so")
+
+
+class NosaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class NosaConfig(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("n_q_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("dtype", C.c_int32), ("block", C.c_int32),
+                ("sub_block", C.c_int32), ("k", C.c_int32), ("k_e", C.c_int32),
+                ("max_context", C.c_int32), ("device", C.c_int32), ("flags", C.c_uint32)]
+
+
+class NosaStats(C.Structure):
+    _fields_ = [("steps", C.c_int64), ("context", C.c_int64), ("host_loads", C.c_int64),
+                ("tail_loads", C.c_int64), ("host_bytes", C.c_int64),
+                ("cold_host_loads", C.c_int64), ("max_host_loads_unit", C.c_int32),
+                ("min_hits", C.c_int32), ("sum_hits", C.c_int64), ("hit_samples", C.c_int64),
+                ("gamma_min", C.c_double), ("gamma_mean", C.c_double),
+                ("near_ties", C.c_int64), ("device_error", C.c_int32), ("pad_", C.c_int32),
+                ("t_us", C.c_double * 8), ("t_count", C.c_int64)]
+
+
+def _load():
+    if not os.path.exists(lib_path):
+        raise ImportError(f"{lib_path} is missing: the CUDA library has not been built "
+                          "(run __graft_entry__.build())")
+    L = C.CDLL(lib_path)
+    P, I32, SZ, VP = C.POINTER, C.c_int32, C.c_size_t, C.c_void_p
+    sigs = {
+        "nosa_payload_bytes": (SZ, [P(NosaConfig)]),
+        "nosa_config_validate": (C.c_int, [P(NosaConfig), C.c_char_p, SZ]),
+        "nosa_create": (C.c_int, [P(NosaConfig), P(VP)]),
+        "nosa_append_kv": (C.c_int, [VP, I32, VP, VP, VP, VP]),
+        "nosa_decode_step": (C.c_int, [VP, VP, VP, VP, VP, VP, VP, VP]),
+        "nosa_stats": (C.c_int, [VP, P(NosaStats)]),
+        "nosa_stats_reset": (C.c_int, [VP]),
+        "nosa_debug_read": (C.c_int, [VP, I32, SZ, VP, SZ]),
+        "nosa_debug_size": (SZ, [VP, I32]),
+        "nosa_destroy": (None, [VP]),
+        "nosa_last_error": (C.c_char_p, [VP]),
+        "nosa_attention_workspace_bytes": (SZ, [P(NosaConfig), I32]),
+        "nosa_sparse_attention": (C.c_int, [P(NosaConfig), VP, C.c_int64, VP, I32, VP, I32, VP,
+                                            VP, VP, VP, SZ, VP]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_of(cfg: NosaConfig):
+    torch = _torch()
+    return torch.float32 if cfg.dtype == NOSA_F32 else torch.bfloat16
+
+
+def _ptr(t, shape=None, dtype=None, what="tensor", align=16, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{what} is required")
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    p = t.data_ptr()
+    if p % align:
+        raise ValueError(f"{what} must be {align}-byte aligned")
+    return p
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, handle=None):
+    if status != 0:
+        raise NosaError(status, nosa_last_error(handle))
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one wrapper per entry point
+# ---------------------------------------------------------------------------
+def nosa_config(batch, n_q_heads, n_kv_heads, head_dim, dtype, k, k_e, max_context,
+                block=64, sub_block=16, device=0, flags=0) -> NosaConfig:
+    if isinstance(dtype, str):
+        dtype = NOSA_F32 if dtype == "f32" else NOSA_BF16
+    return NosaConfig(batch, n_q_heads, n_kv_heads, head_dim, dtype, block, sub_block, k, k_e,
+                      max_context, device, flags)
+
+
+def nosa_config_validate(cfg: NosaConfig):
+    buf = C.create_string_buffer(256)
+    st = lib.nosa_config_validate(C.byref(cfg), buf, 256)
+    return st, buf.value.decode()
+
+
+def nosa_payload_bytes(cfg: NosaConfig) -> int:
+    return int(lib.nosa_payload_bytes(C.byref(cfg)))
+
+
+def nosa_last_error(handle=None) -> str:
+    r = lib.nosa_last_error(handle)
+    return r.decode() if r else ""
+
+
+def nosa_create(cfg: NosaConfig):
+    h = C.c_void_p()
+    _check(lib.nosa_create(C.byref(cfg), C.byref(h)))
+    h.cfg = cfg
+    return h
+
+
+def nosa_append_kv(h, k, v, e, stream=None):
+    cfg = h.cfg
+    dt = _dtype_of(cfg)
+    torch = _torch()
+    n = k.shape[1] if not isinstance(k, int) else None
+    if n is None:
+        raise ValueError("pass tensors to nosa_append_kv")
+    shp = (cfg.batch, n, cfg.n_kv_heads, cfg.head_dim)
+    _check(lib.nosa_append_kv(h, n, _ptr(k, shp, dt, "k"), _ptr(v, shp, dt, "v"),
+                              _ptr(e, shp[:3], torch.float32, "e", 4), _stream(stream)), h)
+
+
+def nosa_decode_step(h, q, k_new, v_new, e_new, out, lse=None, stream=None):
+    cfg = h.cfg
+    dt = _dtype_of(cfg)
+    torch = _torch()
+    qs = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    ks = (cfg.batch, cfg.n_kv_heads, cfg.head_dim)
+    _check(lib.nosa_decode_step(
+        h, _ptr(q, qs, dt, "q"), _ptr(k_new, ks, dt, "k_new"), _ptr(v_new, ks, dt, "v_new"),
+        _ptr(e_new, ks[:2], torch.float32, "e_new", 4), _ptr(out, qs, dt, "out"),
+        _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True), _stream(stream)), h)
+
+
+def nosa_stats(h) -> dict:
+    s = NosaStats()
+    _check(lib.nosa_stats(h, C.byref(s)), h)
+    d = {f: getattr(s, f) for f, _ in NosaStats._fields_ if f not in ("t_us", "pad_")}
+    d["t_us"] = list(s.t_us)
+    return d
+
+
+def nosa_stats_reset(h):
+    _check(lib.nosa_stats_reset(h), h)
+
+
+def nosa_debug_size(h, what) -> int:
+    return int(lib.nosa_debug_size(h, DBG[what] if isinstance(what, str) else what))
+
+
+def nosa_debug_read(h, what, offset=0, nbytes=None) -> np.ndarray:
+    """Synchronous read-back of a debug array (or a byte range of it) as uint8."""
+    w = DBG[what] if isinstance(what, str) else what
+    if nbytes is None:
+        nbytes = nosa_debug_size(h, w) - offset
+    out = np.empty(nbytes, dtype=np.uint8)
+    _check(lib.nosa_debug_read(h, w, offset, out.ctypes.data, nbytes), h)
+    return out
+
+
+def nosa_destroy(h):
+    if h is not None and h.value:
+        lib.nosa_destroy(h)
+        h.value = None
+
+
+def nosa_attention_workspace_bytes(cfg: NosaConfig, n_blocks: int) -> int:
+    return int(lib.nosa_attention_workspace_bytes(C.byref(cfg), n_blocks))
+
+
+def nosa_sparse_attention(cfg: NosaConfig, units, block_tab, tail, tail_len, q, out, lse,
+                          workspace, stream=None):
+    torch = _torch()
+    dt = _dtype_of(cfg)
+    U = cfg.batch * cfg.n_kv_heads
+    n_blocks = block_tab.shape[1]
+    qs = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    _check(lib.nosa_sparse_attention(
+        C.byref(cfg), _ptr(units, None, torch.uint8, "units"),
+        units.numel() // nosa_payload_bytes(cfg),
+        _ptr(block_tab, (U, n_blocks), torch.int32, "block_tab", 4), n_blocks,
+        _ptr(tail, None, torch.uint8, "tail", allow_none=True), int(tail_len),
+        _ptr(q, qs, dt, "q"), _ptr(out, qs, dt, "out"),
+        _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True),
+        _ptr(workspace, None, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))

@@ -1,0 +1,474 @@
+// Block-sparse flash-decoding attention with the exp-delayed eviction logit.
+//
+// NOSA technical summary, Methodology §1 "ED-DMA (Exp-Delayed DMA)": selection
+// works on pre-exp eviction scores and the exponential is applied in the
+// attention stage. For a query head g of unit (b, h) and every attended token j
+// (the tokens of the unit's selected blocks and of its tail block):
+//     l_j = q_g . k_j / sqrt(d) + e_j,   out_g = sum_j softmax(l)_j v_j,
+//     lse_g = log sum_j exp(l_j).
+// The kernel works in the log2 domain (q is pre-scaled by log2(e)/sqrt(d) and
+// e_j by log2(e)), an identity.
+//
+// Split-K: grid = (splits, units). A CTA (4 warps) walks its share of the unit's
+// block list; one thread streams whole block units (K | V | e, 16.6 or 33 KB)
+// into a ring of shared-memory stages with bulk asynchronous copies completing
+// on mbarriers (no tensor map: the units are contiguous). Each warp owns 16 of
+// the 64 tokens of every block and keeps its own running max / sum / accumulator;
+// the 4 warps merge at the end and the CTA writes one partial per query head.
+// A combine kernel merges the splits.
+//
+// Token work inside a warp:
+//   logits : lane (t = lane % 16, half = lane / 16) dots token t with one half of
+//            the head dimension (K is 16-byte-chunk-major in the unit, so the 16
+//            lanes of a half read 16 consecutive chunks: no bank conflicts), the
+//            halves are added with one shuffle;
+//   p . V  : lane (chunk c = lane % NCH, token group) accumulates one 16-byte
+//            chunk of the head dimension over its tokens (V is token-major).
+// Every spin on an mbarrier gives up after ~2 s, sets an error word and drains
+// the copies already issued before the CTA exits.
+#pragma once
+
+#include "nosa_internal.cuh"
+
+namespace nosa {
+
+struct AttnKParams {
+  const uint8_t* units;
+  long long n_units;
+  const int32_t* block_tab;
+  int n_blocks;
+  const uint8_t* tail;
+  long long tail_stride;
+  int tail_len;
+  const void* q;
+  float* part_acc;
+  float* part_ml;
+  int nsplit, bps, stages;
+  long long payload;
+  int Hq, Hkv;
+  float qscale;  // log2(e) / sqrt(d)
+  int* err;
+};
+
+template <typename T> struct Unpack16;
+template <> struct Unpack16<__nv_bfloat16> {
+  static __device__ __forceinline__ void run(const uint4 r, float* f) {
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
+    f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z);
+    f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+  }
+};
+template <> struct Unpack16<float> {
+  static __device__ __forceinline__ void run(const uint4 r, float* f) {
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+  }
+};
+
+template <typename T, int D, int G>
+struct AttnGeom {
+  static constexpr int B = 64;
+  static constexpr int ELT = (int)sizeof(T);
+  static constexpr int CE = 16 / ELT;     // elements per 16-byte chunk
+  static constexpr int NCH = D / CE;      // chunks per token row
+  static constexpr int NCH2 = NCH / 2;    // chunks per half row (logit lanes)
+  static constexpr int TG = 32 / NCH;     // token groups of the p.V lanes
+  static constexpr int TPL = 16 / TG;     // tokens per p.V lane per block
+  static constexpr int GP = (G + 3) / 4 * 4;
+  static constexpr int QH = D / 2 + 4;    // padded floats per half query row
+  static_assert(NCH >= 2 && NCH <= 32, "token row must be 32..512 bytes");
+  static size_t smem_bytes(int stages, long long payload, int bps) {
+    size_t off = (size_t)stages * payload;
+    off += (size_t)G * 2 * QH * 4 + (size_t)4 * 16 * GP * 4 + (size_t)(bps + 1) * 4;
+    off = (off + 7) & ~(size_t)7;
+    off += (size_t)2 * stages * 8;
+    return off;
+  }
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
+  using Gm = AttnGeom<T, D, G>;
+  constexpr int B = Gm::B, ELT = Gm::ELT, CE = Gm::CE, NCH = Gm::NCH, NCH2 = Gm::NCH2;
+  constexpr int TG = Gm::TG, TPL = Gm::TPL, GP = Gm::GP, QH = Gm::QH;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const long long payload = p.payload;
+  uint8_t* stage_buf = smem;
+  float* q_s = reinterpret_cast<float*>(smem + (size_t)p.stages * payload);
+  float* p_s = q_s + G * 2 * QH;
+  int* list = reinterpret_cast<int*>(p_s + 4 * 16 * GP);
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(list + p.bps + 1) + 7) & ~uintptr_t(7));
+  uint64_t* empty = full + p.stages;
+  __shared__ int s_nl;
+  __shared__ volatile int s_bad;
+
+  const int u = blockIdx.y, sp = blockIdx.x;
+  const int b = u / p.Hkv, h = u % p.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Virtual item list: the n_blocks table entries, then the tail (if any),
+  // spread evenly over the splits.
+  const int nv = p.n_blocks + (p.tail != nullptr ? 1 : 0);
+  const int v0 = (int)((long long)sp * nv / p.nsplit);
+  const int v1 = (int)((long long)(sp + 1) * nv / p.nsplit);
+  const int j0 = v0, j1 = min(v1, p.n_blocks);
+  const bool has_tail = (p.tail != nullptr) && (v1 > p.n_blocks);
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    fence_mbar_init();
+    s_bad = 0;
+  }
+  if (warp == 0) {  // compact the valid blocks of this split, in order
+    int cnt = 0;
+    for (int base = j0; base < j1; base += 32) {
+      const int j = base + lane;
+      int idx = (j < j1) ? p.block_tab[(long long)u * p.n_blocks + j] : -1;
+      if (idx >= 0 && (long long)idx >= p.n_units) {  // bad index: skip it, flag it
+        atomicExch(p.err, kDevErrBadIndex);
+        idx = -1;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, idx >= 0);
+      if (idx >= 0) list[cnt + __popc(m & ((1u << lane) - 1u))] = idx;
+      cnt += __popc(m);
+    }
+    if (lane == 0) {
+      if (has_tail) list[cnt] = -2;
+      s_nl = cnt + (has_tail ? 1 : 0);
+    }
+  }
+  {
+    const T* qg = reinterpret_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)h * G) * D;
+    for (int i = tid; i < G * D; i += 128) {
+      const int g = i / D, dim = i % D;
+      q_s[g * 2 * QH + (dim / (D / 2)) * QH + (dim % (D / 2))] = to_f32(qg[i]) * p.qscale;
+    }
+  }
+  __syncthreads();
+  const int nl = s_nl;
+
+  int issued = 0;  // meaningful in thread 0 only
+  if (tid == 0) {
+    const int pre = min(p.stages, nl);
+    for (int s = 0; s < pre; ++s) {
+      const int idx = list[s];
+      const uint8_t* src = idx >= 0 ? p.units + (long long)idx * payload
+                                    : p.tail + (long long)u * p.tail_stride;
+      mbar_arrive_expect_tx(&full[s], (uint32_t)payload);
+      bulk_g2s(stage_buf + (size_t)s * payload, src, (uint32_t)payload, &full[s]);
+    }
+    issued = pre;
+  }
+
+  float m_run[G], l_run[G];
+  float2 acc[G][CE / 2];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = -1e30f;
+    l_run[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < CE / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
+  }
+  const int t = lane & 15, hh = lane >> 4;
+  const int tok = warp * 16 + t;
+  const int c = lane % NCH, tg = lane / NCH;
+
+  for (int it = 0; it < nl; ++it) {
+    if (__any_sync(0xffffffffu, s_bad != 0)) break;
+    const int si = it % p.stages;
+    const uint32_t par = (uint32_t)((it / p.stages) & 1);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[si], par));
+    if (!ok) {
+      if (lane == 0) {
+        s_bad = 1;
+        atomicExch(p.err, kDevErrWaitTimeout);
+      }
+      break;
+    }
+    const uint8_t* buf = stage_buf + (size_t)si * payload;
+    const bool valid = (list[it] >= 0) || (tok < p.tail_len);
+
+    // ---- logits of this warp's 16 tokens ----
+    float2 d2[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) d2[g] = make_float2(0.f, 0.f);
+    const uint4* kp = reinterpret_cast<const uint4*>(buf) + (hh * NCH2) * B + tok;
+#pragma unroll
+    for (int cc = 0; cc < NCH2; ++cc) {
+      float kf[CE];
+      Unpack16<T>::run(kp[cc * B], kf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float4* qp = reinterpret_cast<const float4*>(q_s + g * 2 * QH + hh * QH + cc * CE);
+#pragma unroll
+        for (int e4 = 0; e4 < CE / 4; ++e4) {
+          const float4 qv = qp[e4];
+          d2[g] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kf[4 * e4], kf[4 * e4 + 1]), d2[g]);
+          d2[g] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kf[4 * e4 + 2], kf[4 * e4 + 3]), d2[g]);
+        }
+      }
+    }
+    const float ev = reinterpret_cast<const float*>(buf + 2 * B * D * ELT)[tok] * kLog2e;
+    float pg[G], alpha[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float dot = d2[g].x + d2[g].y;
+      dot += __shfl_xor_sync(0xffffffffu, dot, 16);
+      const float lg = valid ? dot + ev : -INFINITY;
+      float mx = lg;
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      const float mn = fmaxf(m_run[g], mx);
+      alpha[g] = exp2f(m_run[g] - mn);
+      pg[g] = exp2f(lg - mn);
+      l_run[g] = l_run[g] * alpha[g] + pg[g];
+      m_run[g] = mn;
+    }
+    if (hh == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) p_s[tok * GP + g] = pg[g];
+    }
+    __syncwarp();
+
+    // ---- acc = acc * alpha + sum_t p_t v_t ----
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float2 a2 = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+      for (int e = 0; e < CE / 2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
+    }
+    const uint8_t* vbase = buf + (size_t)B * D * ELT;
+#pragma unroll
+    for (int i = 0; i < TPL; ++i) {
+      const int tk = warp * 16 + tg + i * TG;
+      float vf[CE];
+      Unpack16<T>::run(*reinterpret_cast<const uint4*>(vbase + ((size_t)tk * D + c * CE) * ELT), vf);
+      float pv[GP];
+#pragma unroll
+      for (int g4 = 0; g4 < GP / 4; ++g4) {
+        const float4 x = *reinterpret_cast<const float4*>(p_s + tk * GP + 4 * g4);
+        pv[4 * g4] = x.x;
+        pv[4 * g4 + 1] = x.y;
+        pv[4 * g4 + 2] = x.z;
+        pv[4 * g4 + 3] = x.w;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float2 p2 = make_float2(pv[g], pv[g]);
+#pragma unroll
+        for (int e = 0; e < CE / 2; ++e)
+          acc[g][e] = __ffma2_rn(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[g][e]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[si]);
+
+    // ---- refill this stage with the block `stages` items ahead ----
+    if (tid == 0 && issued < nl && s_bad == 0) {
+      if (!mbar_wait_bounded(&empty[si], par)) {
+        s_bad = 1;
+        atomicExch(p.err, kDevErrWaitTimeout);
+      } else {
+        const int idx = list[issued];
+        const uint8_t* src = idx >= 0 ? p.units + (long long)idx * payload
+                                      : p.tail + (long long)u * p.tail_stride;
+        mbar_arrive_expect_tx(&full[si], (uint32_t)payload);
+        bulk_g2s(stage_buf + (size_t)si * payload, src, (uint32_t)payload, &full[si]);
+        ++issued;
+      }
+    }
+  }
+
+  // Warp totals: each token's p sits in both halves of the warp; sum one half.
+  float lw[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float x = l_run[g];
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    lw[g] = x;
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < CE / 2; ++e)
+#pragma unroll
+      for (int o = NCH; o < 32; o <<= 1) {
+        acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
+        acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
+      }
+
+  __syncthreads();
+  if (s_bad != 0 && tid == 0) {
+    // Drain: wait (bounded) for the last copy issued into each stage.
+    for (int s = 0; s < p.stages; ++s) {
+      int last = -1;
+      for (int li = s; li < issued; li += p.stages) last = li;
+      if (last >= 0) mbar_wait_bounded(&full[s], (uint32_t)((last / p.stages) & 1));
+    }
+  }
+  __syncthreads();
+
+  float* red_acc = reinterpret_cast<float*>(stage_buf);  // [4][G][D]
+  float* red_m = red_acc + 4 * G * D;                    // [4][G]
+  float* red_l = red_m + 4 * G;                          // [4][G]
+  if (tg == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < CE / 2; ++e) {
+        red_acc[(warp * G + g) * D + c * CE + 2 * e] = acc[g][e].x;
+        red_acc[(warp * G + g) * D + c * CE + 2 * e + 1] = acc[g][e].y;
+      }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      red_m[warp * G + g] = m_run[g];
+      red_l[warp * G + g] = lw[g];
+    }
+  }
+  __syncthreads();
+  const long long pbase = ((long long)u * p.nsplit + sp) * G;
+  for (int i = tid; i < G * D; i += 128) {
+    const int g = i / D, dim = i % D;
+    float M = red_m[g];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) M = fmaxf(M, red_m[w * G + g]);
+    float A = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float sc = exp2f(red_m[w * G + g] - M);
+      A += red_acc[(w * G + g) * D + dim] * sc;
+      L += red_l[w * G + g] * sc;
+    }
+    p.part_acc[(pbase + g) * D + dim] = A;
+    if (dim == 0) {
+      p.part_ml[(pbase + g) * 2] = M;
+      p.part_ml[(pbase + g) * 2 + 1] = L;
+    }
+  }
+}
+
+// Merges the split partials of each unit. grid = U, block = 128.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ part_acc,
+                                                           const float* __restrict__ part_ml,
+                                                           int nsplit, int Hq, int Hkv, T* out,
+                                                           float* lse) {
+  const int u = blockIdx.x, b = u / Hkv, h = u % Hkv;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int g = i / D, dim = i % D;
+    const float* ml = part_ml + ((long long)u * nsplit * G + g) * 2;
+    const float* ac = part_acc + ((long long)u * nsplit * G + g) * D + dim;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, ml[(long long)sp * G * 2]);
+    float A = 0.f, L = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float sc = exp2f(ml[(long long)sp * G * 2] - M);
+      A += ac[(long long)sp * G * D] * sc;
+      L += ml[(long long)sp * G * 2 + 1] * sc;
+    }
+    const long long row = (long long)b * Hq + (long long)h * G + g;
+    out[row * D + dim] = from_f32<T>(L > 0.f ? A / L : 0.f);
+    if (dim == 0 && lse != nullptr) lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, int bps,
+                                cudaStream_t stream) {
+  AttnKParams p;
+  p.units = a.units;
+  p.n_units = a.n_units;
+  p.block_tab = a.block_tab;
+  p.n_blocks = a.n_blocks;
+  p.tail = a.tail;
+  p.tail_stride = a.tail_stride;
+  p.tail_len = a.tail_len;
+  p.q = a.q;
+  p.part_acc = a.part_acc;
+  p.part_ml = a.part_ml;
+  p.nsplit = a.nsplit;
+  p.bps = bps;
+  p.stages = stages;
+  p.payload = s.payload;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.qscale = (float)(1.4426950408889634 / sqrt((double)D));
+  p.err = a.err;
+  const size_t smem = AttnGeom<T, D, G>::smem_bytes(stages, s.payload, bps);
+  cudaError_t err = cudaFuncSetAttribute(attn_split_kernel<T, D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid(a.nsplit, s.U);
+  attn_split_kernel<T, D, G><<<grid, 128, smem, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (a.mid != nullptr) cudaEventRecord(a.mid, stream);
+  attn_combine_kernel<T, D, G><<<s.U, 128, 0, stream>>>(a.part_acc, a.part_ml, a.nsplit, s.Hq,
+                                                        s.Hkv, reinterpret_cast<T*>(a.out), a.lse);
+  return cudaGetLastError();
+}
+
+// CTAs per SM of one variant at the given pipeline depth (0 if it cannot run).
+template <typename T, int D, int G>
+int attn_occupancy_variant(const Shape& s, int stages, int bps) {
+  const size_t smem = AttnGeom<T, D, G>::smem_bytes(stages, s.payload, bps);
+  if (cudaFuncSetAttribute(attn_split_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<T, D, G>, 128, smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <typename T, int D>
+int attn_occupancy_dispatch_g(const Shape& s, int stages, int bps) {
+  switch (s.G) {
+    case 1: return attn_occupancy_variant<T, D, 1>(s, stages, bps);
+    case 2: return attn_occupancy_variant<T, D, 2>(s, stages, bps);
+    case 3: return attn_occupancy_variant<T, D, 3>(s, stages, bps);
+    case 4: return attn_occupancy_variant<T, D, 4>(s, stages, bps);
+    case 6: return attn_occupancy_variant<T, D, 6>(s, stages, bps);
+    case 8: return attn_occupancy_variant<T, D, 8>(s, stages, bps);
+    default: return 0;
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_attn_dispatch_g(const Shape& s, const AttnArgs& a, int stages, int bps,
+                                   cudaStream_t stream) {
+  switch (s.G) {
+    case 1: return launch_attn_variant<T, D, 1>(s, a, stages, bps, stream);
+    case 2: return launch_attn_variant<T, D, 2>(s, a, stages, bps, stream);
+    case 3: return launch_attn_variant<T, D, 3>(s, a, stages, bps, stream);
+    case 4: return launch_attn_variant<T, D, 4>(s, a, stages, bps, stream);
+    case 6: return launch_attn_variant<T, D, 6>(s, a, stages, bps, stream);
+    case 8: return launch_attn_variant<T, D, 8>(s, a, stages, bps, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_attention_f32(const Shape& s, const AttnArgs& a, int stages, int bps,
+                                 cudaStream_t stream);
+int attention_occupancy_f32(const Shape& s, int stages, int bps);
+int attention_occupancy_bf16(const Shape& s, int stages, int bps);
+cudaError_t launch_attention_bf16(const Shape& s, const AttnArgs& a, int stages, int bps,
+                                  cudaStream_t stream);
+
+}  // namespace nosa

@@ -1,0 +1,636 @@
+// C ABI of the NOSA decode-step hot path: handle lifecycle, argument checks and
+// the per-step launch sequence. The kernels live in k_*.cu; this file owns the
+// device memory (slot pool, tail buffers, pooled metadata, bitmasks, scratch)
+// and the pinned, mapped host store of block units.
+#include "nosa.h"
+#include "nosa_internal.cuh"
+#include "k_attn.cuh"
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace nosa;
+
+namespace {
+
+constexpr int kMaxSplits = 64;
+constexpr int kRing = 64;     // timing event sets in flight
+constexpr int kNumEv = 8;
+
+thread_local std::string g_thread_err;
+
+struct DeviceGuard {
+  int prev = -1;
+  int want;
+  explicit DeviceGuard(int dev) : want(dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0 && prev != want) cudaSetDevice(prev);
+  }
+};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Host-only validation. Returns NOSA_OK, NOSA_ERR_INVALID_ARG or NOSA_ERR_UNSUPPORTED.
+nosa_status validate(const nosa_config* c, std::string& why) {
+  if (!c) { why = "config is NULL"; return NOSA_ERR_INVALID_ARG; }
+  if (c->batch < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1) {
+    why = "batch and head counts must be >= 1"; return NOSA_ERR_INVALID_ARG;
+  }
+  if (c->n_q_heads % c->n_kv_heads != 0) {
+    why = "n_q_heads must be a multiple of n_kv_heads"; return NOSA_ERR_INVALID_ARG;
+  }
+  if (c->dtype != NOSA_F32 && c->dtype != NOSA_BF16) { why = "unknown dtype"; return NOSA_ERR_INVALID_ARG; }
+  if (c->block < 1 || c->sub_block < 1 || c->block % c->sub_block != 0) {
+    why = "block must be a positive multiple of sub_block"; return NOSA_ERR_INVALID_ARG;
+  }
+  if (c->k < 1 || c->k_e < 0 || c->k_e > c->k) { why = "need 0 <= k_e <= k and k >= 1"; return NOSA_ERR_INVALID_ARG; }
+  if (c->max_context < 1) { why = "max_context must be >= 1"; return NOSA_ERR_INVALID_ARG; }
+  if (c->device < 0) { why = "device must be >= 0"; return NOSA_ERR_INVALID_ARG; }
+  if (c->flags & ~NOSA_FLAG_TIMING) { why = "unknown flag bits"; return NOSA_ERR_INVALID_ARG; }
+  if (c->head_dim < 1) { why = "head_dim must be >= 1"; return NOSA_ERR_INVALID_ARG; }
+  if (c->block != 64 || c->sub_block != 16) {
+    why = "compiled for block = 64, sub_block = 16"; return NOSA_ERR_UNSUPPORTED;
+  }
+  if (c->head_dim != 64 && c->head_dim != 128) { why = "head_dim must be 64 or 128"; return NOSA_ERR_UNSUPPORTED; }
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (!(G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8)) {
+    why = "n_q_heads / n_kv_heads must be 1, 2, 3, 4, 6 or 8"; return NOSA_ERR_UNSUPPORTED;
+  }
+  if (c->k > kMaxK) { why = "k must be <= 256"; return NOSA_ERR_UNSUPPORTED; }
+  const long long maxblk = (c->max_context + (long long)c->block - 1) / c->block;
+  if (maxblk > 32768) { why = "max_context must be <= 32768 blocks"; return NOSA_ERR_UNSUPPORTED; }
+  if ((long long)c->batch * c->n_kv_heads > 65535) {
+    why = "batch * n_kv_heads must be <= 65535"; return NOSA_ERR_UNSUPPORTED;
+  }
+  return NOSA_OK;
+}
+
+long long payload_of(int block, int d, int dtype) {
+  const int elt = dtype == NOSA_F32 ? 4 : 2;
+  const long long raw = 2LL * block * d * elt + 4LL * block;
+  return (raw + 255) / 256 * 256;
+}
+
+Shape shape_of(const nosa_config& c) {
+  Shape s;
+  s.batch = c.batch;
+  s.Hq = c.n_q_heads;
+  s.Hkv = c.n_kv_heads;
+  s.U = c.batch * c.n_kv_heads;
+  s.G = c.n_q_heads / c.n_kv_heads;
+  s.d = c.head_dim;
+  s.B = c.block;
+  s.S = c.sub_block;
+  s.P = c.block / c.sub_block;
+  s.k = c.k;
+  s.ke = c.k_e;
+  s.maxBlk = (c.max_context + c.block - 1) / c.block;
+  s.W = (s.maxBlk + 31) / 32;
+  s.dtype = c.dtype;
+  s.elt = c.dtype == NOSA_F32 ? 4 : 2;
+  s.kbytes = c.block * c.head_dim * s.elt;
+  s.payload = payload_of(c.block, c.head_dim, c.dtype);
+  return s;
+}
+
+int attn_stages(long long payload) { return payload > 20000 ? 3 : 4; }
+
+int sm_count_current() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Attention helpers shared by nosa_decode_step and nosa_sparse_attention.
+// ---------------------------------------------------------------------------
+namespace nosa {
+
+bool attention_supported(int dtype, int d, int G) {
+  return (dtype == 0 || dtype == 1) && (d == 64 || d == 128) &&
+         (G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8);
+}
+
+size_t attention_workspace_bytes(const Shape& s, int nsplit) {
+  size_t acc = (size_t)s.U * nsplit * s.G * s.d * 4;
+  size_t ml = (size_t)s.U * nsplit * s.G * 2 * 4;
+  return ((acc + 15) & ~(size_t)15) + ((ml + 15) & ~(size_t)15) + 16;
+}
+
+// Splits per unit: the smallest count whose CTA total fills the GPU's resident
+// CTA slots in whole waves within 2% of the best, with >= 2 blocks per split.
+int attention_pick_nsplit(const Shape& s, int n_blocks, int /*has_tail*/) {
+  const int nv = n_blocks + 1;
+  const int stages = attn_stages(s.payload);
+  const int bps_est = std::min(nv, 64);
+  int occ = s.dtype == 0 ? attention_occupancy_f32(s, stages, bps_est)
+                         : attention_occupancy_bf16(s, stages, bps_est);
+  if (occ < 1) occ = 1;
+  const double slots = (double)sm_count_current() * occ;
+  int best = 1;
+  double best_eff = 0.0;
+  const int max_ns = std::max(1, std::min(kMaxSplits, nv / 2));
+  for (int ns = 1; ns <= max_ns; ++ns) {
+    const double w = (double)s.U * ns / slots;
+    const double eff = w / std::ceil(w);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t stream) {
+  const int stages = attn_stages(s.payload);
+  const int nv = a.n_blocks + (a.tail ? 1 : 0);
+  const int bps = std::max(1, (nv + a.nsplit - 1) / a.nsplit);
+  return s.dtype == 0 ? launch_attention_f32(s, a, stages, bps, stream)
+                      : launch_attention_bf16(s, a, stages, bps, stream);
+}
+
+}  // namespace nosa
+
+// ---------------------------------------------------------------------------
+// The handle
+// ---------------------------------------------------------------------------
+struct nosa_handle {
+  nosa_config cfg;
+  Shape s;
+  State st;
+  std::vector<void*> dev_allocs;
+  uint8_t* host_store = nullptr;
+  size_t host_bytes = 0;
+  long long L = 0;
+  long long steps = 0;
+  int nsplit = 1;
+  int gather_grid = 1;
+  bool broken = false;
+  std::string err;
+  cudaStream_t last_stream = nullptr;
+  bool timing = false;
+  cudaEvent_t ev[kRing][kNumEv];
+  bool pending[kRing];
+  int ring_pos = 0;
+  double t_us[8];
+  long long t_count = 0;
+
+  nosa_status fail(nosa_status code, const std::string& msg) {
+    err = msg;
+    if (code == NOSA_ERR_CUDA) broken = true;
+    return code;
+  }
+  nosa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(NOSA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  }
+};
+
+namespace {
+
+template <typename T>
+cudaError_t dev_alloc(nosa_handle* h, T** p, size_t bytes) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, std::max<size_t>(bytes, 16));
+  if (e != cudaSuccess) return e;
+  h->dev_allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return cudaSuccess;
+}
+
+void free_all(nosa_handle* h) {
+  for (void* p : h->dev_allocs) cudaFree(p);
+  h->dev_allocs.clear();
+  if (h->host_store) cudaFreeHost(h->host_store);
+  h->host_store = nullptr;
+  if (h->timing) {
+    for (int r = 0; r < kRing; ++r)
+      for (int i = 0; i < kNumEv; ++i) cudaEventDestroy(h->ev[r][i]);
+    h->timing = false;
+  }
+}
+
+void harvest(nosa_handle* h, int r) {
+  if (!h->pending[r]) return;
+  if (cudaEventSynchronize(h->ev[r][kNumEv - 1]) != cudaSuccess) return;
+  float ms;
+  for (int i = 0; i < kNumEv - 1; ++i)
+    if (cudaEventElapsedTime(&ms, h->ev[r][i], h->ev[r][i + 1]) == cudaSuccess)
+      h->t_us[i] += ms * 1000.0;
+  if (cudaEventElapsedTime(&ms, h->ev[r][0], h->ev[r][kNumEv - 1]) == cudaSuccess)
+    h->t_us[7] += ms * 1000.0;
+  h->t_count += 1;
+  h->pending[r] = false;
+}
+
+DevStats fresh_stats() {
+  DevStats d;
+  std::memset(&d, 0, sizeof(d));
+  d.min_hits = INT_MAX;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nosa_payload_bytes(const nosa_config* cfg) {
+  std::string why;
+  if (validate(cfg, why) != NOSA_OK) return 0;
+  return (size_t)payload_of(cfg->block, cfg->head_dim, cfg->dtype);
+}
+
+nosa_status nosa_config_validate(const nosa_config* cfg, char* msg, size_t msg_len) {
+  std::string why;
+  nosa_status st = validate(cfg, why);
+  if (msg && msg_len > 0) {
+    std::snprintf(msg, msg_len, "%s", why.c_str());
+  }
+  return st;
+}
+
+const char* nosa_last_error(const nosa_handle* h) {
+  return h ? h->err.c_str() : g_thread_err.c_str();
+}
+
+nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
+  if (!out) { g_thread_err = "out is NULL"; return NOSA_ERR_INVALID_ARG; }
+  *out = nullptr;
+  std::string why;
+  nosa_status vs = validate(cfg, why);
+  if (vs != NOSA_OK) { g_thread_err = why; return vs; }
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device >= ndev) {
+    g_thread_err = "no such CUDA device";
+    cudaGetLastError();
+    return NOSA_ERR_CUDA;
+  }
+  DeviceGuard guard(cfg->device);
+  nosa_handle* h = new nosa_handle();
+  h->cfg = *cfg;
+  h->s = shape_of(*cfg);
+  std::memset(&h->st, 0, sizeof(h->st));
+  std::memset(h->pending, 0, sizeof(h->pending));
+  std::memset(h->t_us, 0, sizeof(h->t_us));
+  const Shape& s = h->s;
+  State& st = h->st;
+  const size_t U = s.U, k = s.k, mb = s.maxBlk, W = s.W;
+  h->nsplit = attention_pick_nsplit(s, s.k, 1);
+  cudaError_t e = cudaSuccess;
+  auto A = [&](auto** p, size_t bytes) {
+    if (e == cudaSuccess) e = dev_alloc(h, p, bytes);
+  };
+  A(&st.slots, U * k * s.payload);
+  A(&st.tail, U * 2 * s.payload);
+  A(&st.pk, U * mb * s.P * s.d * 4);
+  A(&st.sube, U * mb * s.P * 4);
+  A(&st.se, U * mb * 4);
+  A(&st.sq, U * mb * 4);
+  A(&st.elig, U * W * 4);
+  A(&st.selmask, U * W * 4);
+  A(&st.resmask, U * W * 4);
+  A(&st.sel, U * k * 4);
+  A(&st.nsel, U * 2 * 4);
+  A(&st.slot2blk, U * k * 4);
+  A(&st.loads, U * k * 3 * 4);
+  A(&st.nload, U * 4);
+  A(&st.work, U * k * 4);
+  A(&st.work_count, 16);
+  A(&st.block_tab, U * k * 4);
+  A(&st.part_acc, U * kMaxSplits * s.G * s.d * 4);
+  A(&st.part_ml, U * kMaxSplits * s.G * 2 * 4);
+  A(&st.stats, sizeof(DevStats));
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("device allocation failed: ") + cudaGetErrorString(e);
+    cudaGetLastError();
+    free_all(h);
+    delete h;
+    return NOSA_ERR_OOM;
+  }
+  // Zeroed state: empty slots (-1), nothing eligible or resident.
+  if (e == cudaSuccess) e = cudaMemset(st.slots, 0, U * k * s.payload);
+  if (e == cudaSuccess) e = cudaMemset(st.tail, 0, U * 2 * s.payload);
+  if (e == cudaSuccess) e = cudaMemset(st.pk, 0, U * mb * s.P * s.d * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.sube, 0, U * mb * s.P * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.se, 0, U * mb * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.sq, 0, U * mb * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.elig, 0, U * W * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.selmask, 0, U * W * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.resmask, 0, U * W * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.sel, 0xFF, U * k * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.nsel, 0, U * 2 * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.slot2blk, 0xFF, U * k * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.loads, 0, U * k * 3 * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.nload, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.work_count, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(st.block_tab, 0xFF, U * k * 4);
+  DevStats ds = fresh_stats();
+  if (e == cudaSuccess) e = cudaMemcpy(st.stats, &ds, sizeof(ds), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("device initialisation failed: ") + cudaGetErrorString(e);
+    free_all(h);
+    delete h;
+    return NOSA_ERR_CUDA;
+  }
+  h->host_bytes = U * mb * (size_t)s.payload;
+  void* hp = nullptr;
+  e = cudaHostAlloc(&hp, h->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("pinned host allocation failed: ") + cudaGetErrorString(e);
+    cudaGetLastError();
+    free_all(h);
+    delete h;
+    return NOSA_ERR_HOST_OOM;
+  }
+  h->host_store = static_cast<uint8_t*>(hp);
+  void* dp = nullptr;
+  e = cudaHostGetDevicePointer(&dp, hp, 0);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("no device view of the host store: ") + cudaGetErrorString(e);
+    free_all(h);
+    delete h;
+    return NOSA_ERR_CUDA;
+  }
+  st.host = static_cast<uint8_t*>(dp);
+  h->gather_grid = sm_count_current() * 8;
+  if (cfg->flags & NOSA_FLAG_TIMING) {
+    for (int r = 0; r < kRing; ++r)
+      for (int i = 0; i < kNumEv; ++i) cudaEventCreate(&h->ev[r][i]);
+    h->timing = true;
+  }
+  *out = h;
+  return NOSA_OK;
+}
+
+nosa_status nosa_append_kv(nosa_handle* h, int32_t n_tokens, const void* k, const void* v,
+                           const float* e, void* stream) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  if (h->broken) return h->fail(NOSA_ERR_STATE, "handle unusable after an earlier CUDA error");
+  if (n_tokens < 0) return h->fail(NOSA_ERR_INVALID_ARG, "n_tokens < 0");
+  if (n_tokens == 0) return NOSA_OK;
+  if (!k || !v || !e) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(e, 4))
+    return h->fail(NOSA_ERR_INVALID_ARG, "k, v need 16-byte and e 4-byte alignment");
+  if (h->L + n_tokens > h->cfg.max_context)
+    return h->fail(NOSA_ERR_CAPACITY, "context would exceed max_context");
+  DeviceGuard guard(h->cfg.device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaSuccess;
+  const int L = (int)h->L;
+  if (L > 0 && L % h->s.B == 0) err = launch_promote_tail(h->s, h->st, L / h->s.B - 1, s);
+  if (err == cudaSuccess) err = launch_append_bulk(h->s, h->st, k, v, e, L, n_tokens, s);
+  if (err != cudaSuccess) return h->cuda_fail(err, "append launch");
+  h->L += n_tokens;
+  h->last_stream = s;
+  return NOSA_OK;
+}
+
+nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
+                             const float* e_new, void* out, float* lse, void* stream) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  if (h->broken) return h->fail(NOSA_ERR_STATE, "handle unusable after an earlier CUDA error");
+  if (h->L < 1) return h->fail(NOSA_ERR_STATE, "decode step before any context was appended");
+  if (h->L + 1 > h->cfg.max_context) return h->fail(NOSA_ERR_CAPACITY, "context is full");
+  if (!q || !k_new || !v_new || !e_new || !out) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
+      !aligned(e_new, 4) || (lse && !aligned(lse, 4)))
+    return h->fail(NOSA_ERR_INVALID_ARG, "q, k_new, v_new, out need 16-byte alignment");
+  DeviceGuard guard(h->cfg.device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Shape& sh = h->s;
+  State& st = h->st;
+  cudaEvent_t* ev = nullptr;
+  if (h->timing) {
+    const int r = h->ring_pos;
+    harvest(h, r);
+    ev = h->ev[r];
+    h->pending[r] = true;
+    h->ring_pos = (r + 1) % kRing;
+    cudaEventRecord(ev[0], s);
+  }
+  const int L_old = (int)h->L;
+  const int N = L_old / sh.B;                       // candidates after the append
+  const int T = L_old + 1 - N * sh.B;               // tokens in the tail block
+  const int jc = (L_old % sh.B == 0) ? N - 1 : -1;  // block that just became a candidate
+  cudaError_t err = launch_append_step(sh, st, k_new, v_new, e_new, L_old, s);
+  if (ev) cudaEventRecord(ev[1], s);
+  if (err == cudaSuccess) err = launch_score(sh, st, q, N, s);
+  if (ev) cudaEventRecord(ev[2], s);
+  if (err == cudaSuccess) err = launch_select(sh, st, N, s);
+  if (ev) cudaEventRecord(ev[3], s);
+  if (err == cudaSuccess) err = launch_setdiff(sh, st, N, jc, h->steps == 0 ? 1 : 0, s);
+  if (ev) cudaEventRecord(ev[4], s);
+  if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, s);
+  if (ev) cudaEventRecord(ev[5], s);
+  if (err == cudaSuccess) {
+    AttnArgs a;
+    a.units = st.slots;
+    a.n_units = (long long)sh.U * sh.k;
+    a.block_tab = st.block_tab;
+    a.n_blocks = sh.k;
+    a.tail = st.tail + (long long)(N & 1) * sh.payload;
+    a.tail_stride = 2 * sh.payload;
+    a.tail_len = T;
+    a.q = q;
+    a.out = out;
+    a.lse = lse;
+    a.part_acc = st.part_acc;
+    a.part_ml = st.part_ml;
+    a.nsplit = h->nsplit;
+    a.err = &st.stats->error;
+    a.mid = ev ? ev[6] : nullptr;
+    err = launch_attention(sh, a, s);
+  }
+  if (ev) cudaEventRecord(ev[7], s);
+  if (err != cudaSuccess) return h->cuda_fail(err, "decode step launch");
+  h->L += 1;
+  h->steps += 1;
+  h->last_stream = s;
+  return NOSA_OK;
+}
+
+nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out) {
+  if (!h || !out) return NOSA_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
+  if (h->timing)
+    for (int r = 0; r < kRing; ++r) harvest(h, r);
+  DevStats ds;
+  e = cudaMemcpy(&ds, h->st.stats, sizeof(ds), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return h->cuda_fail(e, "stats read");
+  std::memset(out, 0, sizeof(*out));
+  out->steps = h->steps;
+  out->context = h->L;
+  out->host_loads = (int64_t)ds.host_loads;
+  out->tail_loads = (int64_t)ds.tail_loads;
+  out->host_bytes = (int64_t)ds.host_loads * h->s.payload;
+  out->cold_host_loads = (int64_t)ds.cold_host_loads;
+  out->max_host_loads_unit = ds.max_host_loads_unit;
+  out->min_hits = ds.hit_samples ? ds.min_hits : 0;
+  out->sum_hits = (int64_t)ds.sum_hits;
+  out->hit_samples = (int64_t)ds.hit_samples;
+  out->gamma_min = ds.hit_samples ? (double)ds.min_hits / h->s.k : 0.0;
+  out->gamma_mean = ds.hit_samples ? (double)ds.sum_hits / ((double)h->s.k * ds.hit_samples) : 0.0;
+  out->near_ties = (int64_t)ds.near_ties;
+  out->device_error = ds.error;
+  for (int i = 0; i < 8; ++i) out->t_us[i] = h->t_us[i];
+  out->t_count = h->t_count;
+  return NOSA_OK;
+}
+
+nosa_status nosa_stats_reset(nosa_handle* h) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
+  if (h->timing)
+    for (int r = 0; r < kRing; ++r) harvest(h, r);
+  DevStats old;
+  e = cudaMemcpy(&old, h->st.stats, sizeof(old), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return h->cuda_fail(e, "stats read");
+  DevStats ds = fresh_stats();
+  ds.error = old.error;  // a device error is not a counter
+  e = cudaMemcpy(h->st.stats, &ds, sizeof(ds), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return h->cuda_fail(e, "stats reset");
+  std::memset(h->t_us, 0, sizeof(h->t_us));
+  h->t_count = 0;
+  return NOSA_OK;
+}
+
+size_t nosa_debug_size(const nosa_handle* h, int32_t what) {
+  if (!h) return 0;
+  const Shape& s = h->s;
+  const size_t U = s.U, k = s.k, mb = s.maxBlk, W = s.W;
+  switch (what) {
+    case NOSA_DBG_SEL: return U * k * 4;
+    case NOSA_DBG_NSEL: return U * 2 * 4;
+    case NOSA_DBG_ELIG: return U * W * 4;
+    case NOSA_DBG_SLOTS: return U * k * 4;
+    case NOSA_DBG_LOADS: return U * k * 3 * 4;
+    case NOSA_DBG_NLOAD: return U * 4;
+    case NOSA_DBG_POOLED: return U * mb * s.P * s.d * 4;
+    case NOSA_DBG_SE: return U * mb * 4;
+    case NOSA_DBG_SQ: return U * mb * 4;
+    case NOSA_DBG_SLOTPOOL: return U * k * (size_t)s.payload;
+    case NOSA_DBG_HOST: return h->host_bytes;
+    case NOSA_DBG_TAIL: return U * 2 * (size_t)s.payload;
+    default: return 0;
+  }
+}
+
+nosa_status nosa_debug_read(nosa_handle* h, int32_t what, size_t offset, void* dst, size_t bytes) {
+  if (!h || !dst) return NOSA_ERR_INVALID_ARG;
+  const size_t size = nosa_debug_size(h, what);
+  if (size == 0) return h->fail(NOSA_ERR_INVALID_ARG, "unknown debug array");
+  if (offset > size || bytes > size - offset) return h->fail(NOSA_ERR_INVALID_ARG, "range outside the array");
+  DeviceGuard guard(h->cfg.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
+  const State& st = h->st;
+  const void* base = nullptr;
+  switch (what) {
+    case NOSA_DBG_SEL: base = st.sel; break;
+    case NOSA_DBG_NSEL: base = st.nsel; break;
+    case NOSA_DBG_ELIG: base = st.elig; break;
+    case NOSA_DBG_SLOTS: base = st.slot2blk; break;
+    case NOSA_DBG_LOADS: base = st.loads; break;
+    case NOSA_DBG_NLOAD: base = st.nload; break;
+    case NOSA_DBG_POOLED: base = st.pk; break;
+    case NOSA_DBG_SE: base = st.se; break;
+    case NOSA_DBG_SQ: base = st.sq; break;
+    case NOSA_DBG_SLOTPOOL: base = st.slots; break;
+    case NOSA_DBG_TAIL: base = st.tail; break;
+    case NOSA_DBG_HOST:
+      std::memcpy(dst, h->host_store + offset, bytes);
+      return NOSA_OK;
+  }
+  e = cudaMemcpy(dst, static_cast<const uint8_t*>(base) + offset, bytes, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return h->cuda_fail(e, "debug read");
+  return NOSA_OK;
+}
+
+void nosa_destroy(nosa_handle* h) {
+  if (!h) return;
+  {
+    DeviceGuard guard(h->cfg.device);
+    cudaDeviceSynchronize();
+    free_all(h);
+  }
+  delete h;
+}
+
+size_t nosa_attention_workspace_bytes(const nosa_config* cfg, int32_t n_blocks) {
+  std::string why;
+  if (validate(cfg, why) != NOSA_OK || n_blocks < 0) return 0;
+  DeviceGuard guard(cfg->device);
+  const Shape s = shape_of(*cfg);
+  return attention_workspace_bytes(s, attention_pick_nsplit(s, n_blocks, 1));
+}
+
+nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int64_t n_units,
+                                  const int32_t* block_tab, int32_t n_blocks, const void* tail,
+                                  int32_t tail_len, const void* q, void* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  std::string why;
+  nosa_status vs = validate(cfg, why);
+  if (vs != NOSA_OK) { g_thread_err = why; return vs; }
+  if (n_blocks < 0 || n_units < 0 || (n_blocks > 0 && (!units || !block_tab)) || !q || !out ||
+      !workspace) {
+    g_thread_err = "NULL or negative argument"; return NOSA_ERR_INVALID_ARG;
+  }
+  if (tail && (tail_len < 0 || tail_len > cfg->block)) {
+    g_thread_err = "tail_len must be in [0, block]"; return NOSA_ERR_INVALID_ARG;
+  }
+  if (!aligned(units, 16) || !aligned(tail, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16) || !aligned(block_tab, 4) || (lse && !aligned(lse, 4))) {
+    g_thread_err = "misaligned pointer"; return NOSA_ERR_INVALID_ARG;
+  }
+  DeviceGuard guard(cfg->device);
+  const Shape s = shape_of(*cfg);
+  const int nsplit = attention_pick_nsplit(s, n_blocks, 1);
+  const size_t need = attention_workspace_bytes(s, nsplit);
+  if (workspace_bytes < need) {
+    g_thread_err = "workspace too small (see nosa_attention_workspace_bytes)";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t acc_bytes = ((size_t)s.U * nsplit * s.G * s.d * 4 + 15) & ~(size_t)15;
+  const size_t ml_bytes = ((size_t)s.U * nsplit * s.G * 2 * 4 + 15) & ~(size_t)15;
+  AttnArgs a;
+  a.units = static_cast<const uint8_t*>(units);
+  a.n_units = units ? n_units : 0;
+  a.block_tab = block_tab;
+  a.n_blocks = n_blocks;
+  a.tail = static_cast<const uint8_t*>(tail);
+  a.tail_stride = s.payload;
+  a.tail_len = tail_len;
+  a.q = q;
+  a.out = out;
+  a.lse = lse;
+  a.part_acc = reinterpret_cast<float*>(ws);
+  a.part_ml = reinterpret_cast<float*>(ws + acc_bytes);
+  a.nsplit = nsplit;
+  a.err = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes);
+  a.mid = nullptr;
+  cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_attention(s, a, st);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("attention launch: ") + cudaGetErrorString(e);
+    return NOSA_ERR_CUDA;
+  }
+  return NOSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// Internal declarations shared by the NOSA kernels and the C ABI.
+//
+// Device state of one handle (U units = batch * n_kv_heads, maxBlk blocks of
+// capacity per unit, W = ceil(maxBlk / 32) bitmask words per unit). Every array
+// is unit-major so that one CTA (or one warp) per unit touches a contiguous
+// range.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace nosa {
+
+constexpr int kMaxK = 256;         // selected blocks per unit
+constexpr int kMaxBlocks = 65535;  // capacity in blocks per unit
+
+// Shape of a handle (all host-derived, passed by value to kernels).
+struct Shape {
+  int U, batch, Hq, Hkv, G, d, B, S, P, k, ke, maxBlk, W;
+  int dtype;  // 0 fp32, 1 bf16
+  int elt;    // bytes per element of q, k, v, out
+  int kbytes; // B * d * elt  (K part of a block unit, = V part)
+  long long payload;  // bytes per block unit
+};
+
+// Device-side error codes (written to DevStats::error by a kernel that gives up).
+enum : int { kDevErrNone = 0, kDevErrWaitTimeout = 1, kDevErrBadIndex = 2 };
+
+// Device-side counters (updated with atomics by the set-difference and select kernels).
+struct DevStats {
+  unsigned long long host_loads, tail_loads, cold_host_loads, sum_hits, hit_samples, near_ties;
+  int max_host_loads_unit;
+  int min_hits;
+  int error;
+  int pad_;
+};
+
+struct State {
+  uint8_t* slots;      // [U][k] block units (device)
+  uint8_t* tail;       // [U][2] block units (device); block b lives in buffer b % 2
+  uint8_t* host;       // [U][maxBlk] block units (pinned, mapped host memory; device view)
+  float* pk;           // [U][maxBlk][P][d] sub-block mean keys
+  float* sube;         // [U][maxBlk][P]    sub-block mean eviction logits
+  float* se;           // [U][maxBlk]       block eviction score (max of sube)
+  float* sq;           // [U][maxBlk]       query-aware block score of the current step
+  uint32_t* elig;      // [U][W]            eviction eligibility bitmask
+  uint32_t* selmask;   // [U][W]            Gamma of the current step
+  uint32_t* resmask;   // [U][W]            blocks held by slots
+  int32_t* sel;        // [U][k]            Gamma_e ascending, then Gamma_q ascending, -1 pad
+  int32_t* nsel;       // [U][2]
+  int32_t* slot2blk;   // [U][k]
+  int32_t* loads;      // [U][k][3]         (block, slot, src)
+  int32_t* nload;      // [U]
+  int32_t* work;       // [U*k]             gather work list (entry = u*k + j)
+  int32_t* work_count; // [1]
+  int32_t* block_tab;  // [U][k]            slot pool index of each valid slot, -1 empty
+  float* part_acc;     // split-K partial accumulators
+  float* part_ml;      // split-K partial (max, sum)
+  DevStats* stats;
+};
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (each returns the launch error, if any).
+// ---------------------------------------------------------------------------
+cudaError_t launch_append_step(const Shape& s, const State& st, const void* k_new,
+                               const void* v_new, const float* e_new, int L_old,
+                               cudaStream_t stream);
+cudaError_t launch_promote_tail(const Shape& s, const State& st, int blk, cudaStream_t stream);
+cudaError_t launch_append_bulk(const Shape& s, const State& st, const void* k, const void* v,
+                               const float* e, int L_old, int n, cudaStream_t stream);
+cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand,
+                         cudaStream_t stream);
+cudaError_t launch_select(const Shape& s, const State& st, int n_cand, cudaStream_t stream);
+cudaError_t launch_setdiff(const Shape& s, const State& st, int n_cand, int just_completed,
+                           int cold, cudaStream_t stream);
+cudaError_t launch_gather(const Shape& s, const State& st, int grid, cudaStream_t stream);
+
+// Split-K attention over block units. block_tab [U][n_blocks] holds unit indices
+// into `units` (-1 skip). The tail unit of unit u is at tail + u * tail_stride.
+struct AttnArgs {
+  const uint8_t* units;
+  long long n_units;        // valid unit indices are [0, n_units)
+  const int32_t* block_tab;
+  int n_blocks;
+  const uint8_t* tail;      // may be null
+  long long tail_stride;    // bytes
+  int tail_len;
+  const void* q;
+  void* out;
+  float* lse;
+  float* part_acc;          // [U][nsplit][G][d]
+  float* part_ml;           // [U][nsplit][G][2]
+  int nsplit;
+  int* err;                 // device error word
+  cudaEvent_t mid;          // recorded between the split and combine kernels (may be null)
+};
+size_t attention_workspace_bytes(const Shape& s, int nsplit);
+int attention_pick_nsplit(const Shape& s, int n_blocks, int has_tail);
+cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t stream);
+bool attention_supported(int dtype, int d, int G);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Byte offsets inside a block unit (layout documented in include/nosa.h).
+__device__ __forceinline__ long long k_off(int t, int dim, int B, int elt) {
+  const int c = 16 / elt;
+  return ((long long)(dim / c) * B + t) * 16 + (long long)(dim % c) * elt;
+}
+__device__ __forceinline__ long long v_off(int t, int dim, int B, int d, int elt) {
+  return (long long)B * d * elt + ((long long)t * d + dim) * elt;
+}
+__device__ __forceinline__ long long e_off(int t, int B, int d, int elt) {
+  return 2LL * B * d * elt + 4LL * t;
+}
+
+// Monotone map of fp32 scores to uint32 (larger float -> larger key); -0 == +0.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier and bulk-copy primitives (inline PTX, sm_90+ forms) ----------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete; gives up after
+// `limit_ns` nanoseconds and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+// One bulk (non-tensor) global -> shared copy completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace nosa
