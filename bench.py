@@ -1,0 +1,482 @@
+"""Decode-step benchmark of the NOSA hot path on GB300.
+
+One step = one nosa_decode_step over every request of the workload (append +
+pooling, block scoring, dual selection, set-difference, UVA gather, split-K
+attention, combine). Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl nosa|reference]
+
+Under torchrun every rank runs its own copy of the workload on its own GPU
+(weak scaling: units are independent, no collective on the data path); the
+value is all ranks' tokens over the max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the only reference this method has)
+on a bounded sample of units per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s per layer step; attn HBM GB/s & recall H2D GB/s vs peak"
+DEFAULT_WORKLOAD = "8b-offload-bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host logic; tested with gloo on CPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(seconds: float, tokens: int, world: int):
+    """(max seconds over ranks, total tokens over ranks). Plain values at world 1."""
+    if world == 1:
+        return seconds, tokens
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.lines, self.proc, self.windows = [], None, []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            inside = any(a - 0.06 <= ts <= b + 0.06 for a, b in self.windows)
+            rows.append((inside, parts))
+        use = [p for ins, p in rows if ins] or [p for _, p in rows]
+        if not use:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in use if num(p[2]) is not None]
+        mx = [num(p[3]) for p in use if num(p[3]) is not None]
+        reasons = sorted({name for p in use for name, v in zip(self.REASONS, p[6:10])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": sum(1 for i, _ in rows if i)}
+
+
+def gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip() != ""]
+    if ids and all(v.strip().isdigit() for v in ids):
+        return int(ids[min(local_rank, len(ids) - 1)])
+    return local_rank
+
+
+# ---------------------------------------------------------------------------
+# roofline bookkeeping
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_bytes_per_launch(w, n_cand, tail_len):
+    """Algorithmic bytes of one attention launch: every attended token's K, V and e,
+    plus the queries and the outputs."""
+    elt = 4 if w.dtype == "f32" else 2
+    per_tok = 2 * w.head_dim * elt + 4
+    toks = min(w.k, n_cand) * w.block + tail_len
+    return w.units * (toks * per_tok + 2 * w.group * w.head_dim * elt)
+
+
+def score_bytes_per_launch(w, n_cand):
+    """Algorithmic bytes of one scoring launch: all pooled keys (fp32), the scores
+    written, and the queries."""
+    elt = 4 if w.dtype == "f32" else 2
+    return w.units * (n_cand * 4 * w.head_dim * 4 + n_cand * 4 + w.group * w.head_dim * elt)
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+ATTN_SOURCES = ["trainable_sparse_attention_decode_gb300/csrc/k_attn.cuh",
+                "trainable_sparse_attention_decode_gb300/csrc/k_attn_bf16.cu"]
+
+
+def ncu_traffic(workload_name):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary,
+    or None when the summary is missing or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", f"attn_split_kernel_{workload_name}.md")
+    if not os.path.exists(p):
+        return None
+    src_hash = kernel_source_hash(ATTN_SOURCES)
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_hash") != src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def h2d_peak_gbs(torch, nbytes=1 << 30, reps=5):
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = float("inf")
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b) / 1e3)
+    del src, dst
+    return nbytes / best / 1e9
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import synth
+    import synth.gpu
+    import trainable_sparse_attention_decode_gb300 as nosa
+
+    torch.cuda.set_device(local_rank)
+    w0 = synth.WORKLOADS[args.workload]
+    W, K = args.warmup, args.steps
+    KE = args.e2e_steps
+    total_steps = W + K + KE
+    w = w0.with_(steps=total_steps)
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                           w.max_context, device=local_rank, flags=nosa.NOSA_FLAG_TIMING)
+    h = nosa.nosa_create(cfg)
+    # prompt, appended in chunks generated on the device
+    chunk = 4096
+    t = 0
+    while t < w.prompt:
+        n = min(chunk, w.prompt - t)
+        k, v, e = synth.gpu.kv(w, t, n)
+        nosa.nosa_append_kv(h, k, v, e)
+        t += n
+        del k, v, e
+    torch.cuda.synchronize()
+    # per-step inputs staged in HBM before the timed region
+    q_all = synth.gpu.queries(w, total_steps)
+    k_all, v_all, e_all = synth.gpu.kv(w, w.prompt, total_steps, step_major=True)
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
+    lse = torch.empty((w.batch, w.n_q_heads), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    peak_h2d = h2d_peak_gbs(torch) if rank == 0 else None
+
+    for s in range(W):
+        nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
+    torch.cuda.synchronize()
+    nosa.nosa_stats_reset(h)
+
+    sampler = ClockSampler(gpu_index(local_rank)) if rank == 0 else None
+    time.sleep(0.15 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0t = time.time()
+    ev0.record(stream)
+    for s in range(W, W + K):
+        nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    w1t = time.time()
+    barrier(world)
+    if sampler:
+        sampler.mark(w0t, w1t)
+    secs = ev0.elapsed_time(ev1) / 1e3
+    st = nosa.nosa_stats(h)
+    context_after = st["context"]
+
+    # end to end: pinned host inputs -> device, step, result -> pinned host
+    qh = q_all[W + K:].cpu().pin_memory()
+    kh, vh, eh = (x[W + K:].cpu().pin_memory() for x in (k_all, v_all, e_all))
+    qd, kd, vd, ed = (torch.empty_like(x[0], device="cuda") for x in (qh, kh, vh, eh))
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0t = time.time()
+    e0.record(stream)
+    for s in range(KE):
+        qd.copy_(qh[s], non_blocking=True)
+        kd.copy_(kh[s], non_blocking=True)
+        vd.copy_(vh[s], non_blocking=True)
+        ed.copy_(eh[s], non_blocking=True)
+        nosa.nosa_decode_step(h, qd, kd, vd, ed, out, None, stream)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    x1t = time.time()
+    if sampler:
+        sampler.mark(x0t, x1t)
+    e2e_secs = e0.elapsed_time(e1) / 1e3
+    bi = sum(x[0].numel() * x.element_size() for x in (qh, kh, vh, eh))
+    bo = out_h.numel() * out_h.element_size()
+    clocks = sampler.stop() if sampler else None
+    nosa.nosa_destroy(h)
+
+    max_secs, tokens = aggregate(secs, w.batch * K, world)
+    e2e_max, e2e_tokens = aggregate(e2e_secs, w.batch * KE, world)
+    if rank != 0:
+        return None
+
+    n_cand = (w.prompt + W + K // 2) // w.block       # mid-region candidate count
+    tail_mid = (w.prompt + W + K // 2) % w.block + 1
+    tu = st["t_us"]
+    nt = max(st["t_count"], 1)
+    phase_us = {name: tu[i] / nt for i, name in enumerate(
+        ["append_pool", "score", "select", "setdiff", "gather", "attention", "combine", "step"])}
+    attn_bytes = attn_bytes_per_launch(w, n_cand, tail_mid)
+    score_bytes = score_bytes_per_launch(w, n_cand)
+    peak, peak_kind = measured_peaks()
+    attn_gbs = attn_bytes / (phase_us["attention"] * 1e-6) / 1e9
+    score_gbs = score_bytes / (phase_us["score"] * 1e-6) / 1e9
+    host_bytes_step = st["host_bytes"] / max(st["steps"] - W, 1) if st["steps"] > W else 0.0
+    recall_gbs = (host_bytes_step / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
+    dominant = "attention" if phase_us["attention"] >= phase_us["score"] else "score"
+    dom_bytes, dom_us = ((attn_bytes, phase_us["attention"]) if dominant == "attention"
+                         else (score_bytes, phase_us["score"]))
+    traffic = ncu_traffic(w0.name) if dominant == "attention" else None
+    value = tokens / max_secs
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(max_secs / K * 1e3, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded counter-based generator; shapes of the workload)",
+        "config": {"workload": w0.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k, "k_e": w.k_e,
+                   "context_start": w.prompt, "context_end": context_after,
+                   "l2": "inputs larger than L2 (slot pool %.0f MiB, pooled keys %.0f MiB > %d MiB)"
+                         % (w.units * w.k * 33024 / 2 ** 20,
+                            w.units * n_cand * 4 * w.head_dim * 4 / 2 ** 20, L2_BYTES >> 20),
+                   "parallelism": f"replicas x{world} (independent requests per GPU)"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(dom_bytes / (dom_us * 1e-6) / 1e9, 1),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(dom_bytes / (dom_us * 1e-6) / 1e9 / peak, 4),
+                     "traffic": traffic, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": dom_bytes},
+        "attn_hbm_gbs": round(attn_gbs, 1),
+        "attn_frac_of_peak": round(attn_gbs / peak, 4),
+        "score_hbm_gbs": round(score_gbs, 1),
+        "recall_h2d_gbs": round(recall_gbs, 2),
+        "h2d_peak_gbs": round(peak_h2d, 2) if peak_h2d else None,
+        "recall_frac_of_h2d_peak": round(recall_gbs / peak_h2d, 4) if peak_h2d else None,
+        "host_bytes_per_step": round(host_bytes_step),
+        "phase_us": {k_: round(v_, 3) for k_, v_ in phase_us.items()},
+        "gamma_mean": round(st["gamma_mean"], 4), "gamma_min": st["gamma_min"],
+        "near_ties": st["near_ties"],
+        "e2e": {"value": round(e2e_tokens / e2e_max, 3), "unit": "tokens/s",
+                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": KE},
+        "gpu_launches": 7 * K,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_step_rate(workload: str, units, steps: int, warm: int = 1):
+    """Seconds per (unit, decode step) of the fp64 oracle, steady state."""
+    import synth
+    from oracle import nosa_oracle as O
+    w = synth.WORKLOADS[workload]
+    w = w.with_(steps=max(w.steps, warm + steps))
+    per = []
+    for u in units:
+        b, h = divmod(u, w.n_kv_heads)
+        uo = O.UnitOracle(w.head_dim, w.dtype, w.k, w.k_e, w.max_context, w.block, w.sub_block)
+        uo.append(synth.keys(w, b, h, 0, w.prompt), synth.values(w, b, h, 0, w.prompt),
+                  synth.evict(w, b, h, 0, w.prompt))
+        G = w.group
+        q = synth.queries(w, b, range(h * G, (h + 1) * G), warm + steps)
+        toks = [(synth.keys(w, b, h, w.prompt + s, 1)[0], synth.values(w, b, h, w.prompt + s, 1)[0],
+                 synth.evict(w, b, h, w.prompt + s, 1)[0]) for s in range(warm + steps)]
+        for s in range(warm):
+            uo.decode_step(q[s], *toks[s])
+        t0 = time.perf_counter()
+        for s in range(warm, warm + steps):
+            uo.decode_step(q[s], *toks[s])
+        per.append((time.perf_counter() - t0) / steps)
+    return statistics.mean(per)
+
+
+def cpu_baseline(workload: str, units=(0, 1), steps=6):
+    """Runs the oracle in a single-threaded child process (BLAS pinned to one thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", workload,
+           ",".join(map(str, units)), str(steps)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1200)
+    if r.returncode != 0:
+        return None
+    sec = float(r.stdout.strip().splitlines()[-1])
+    import synth
+    w = synth.WORKLOADS[workload]
+    return {"value": round(w.batch / (sec * w.units), 4), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{len(units)} of {w.units} units x {steps} decode steps (after 1 warm step), "
+                      f"scaled to the full batch; fp64 numpy, one thread"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    units = [0] if args.steps > 4 else [0, 1]
+    steps_per = max(1, min(args.steps, 40))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", args.workload,
+           ",".join(map(str, units)), str(steps_per)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=3000)
+    if r.returncode != 0:
+        return {"impl": "reference", "unavailable": "oracle worker failed: " + r.stderr[-200:]}
+    sec = float(r.stdout.strip().splitlines()[-1])
+    value = w.batch / (sec * w.units)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * w.units * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "context_start": w.prompt},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"{len(units)} unit(s) x {steps_per} steps per timed pass, "
+                                       "scaled to the full batch"},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-worker":
+        wl, units, steps = sys.argv[2], [int(x) for x in sys.argv[3].split(",")], int(sys.argv[4])
+        print(oracle_step_rate(wl, units, steps))
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="nosa", choices=["nosa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -44,13 +44,29 @@ def near_tie_equivalent(scores, cand, oracle_set, gpu_set, rel=TIE_REL):
     return all(nxt - tol <= s[i] <= kth + tol for i in (o ^ g)), True
 
 
+def bf16_half_ulp(x):
+    """Half a bf16 ulp at |x|: the largest error of storing x in bf16 (8-bit significand)."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(ax)) - 8)
+
+
 def attn_close(out, ref, dtype):
-    """Per-row check; returns the worst ratio of error to tolerance (<= 1 passes)."""
+    """Per-row check; returns the worst ratio of error to tolerance (<= 1 passes).
+
+    fp32: max |o - o*| <= 1e-5. bf16: the 1e-2 x RMS(o*) bound is read as a
+    relative RMS error, RMS(o - o*) <= 1e-2 RMS(o*), and elementwise
+    |o - o*| <= 1e-2 RMS(o*) + half a bf16 ulp of o* (the rounding of the stored
+    bf16 output alone exceeds 1e-2 RMS for elements above ~2.5 RMS).
+    """
     worst = 0.0
     for g in range(ref.shape[0]):
-        err = float(np.max(np.abs(out[g] - ref[g])))
-        tol = 1e-5 if dtype == "f32" else 1e-2 * float(np.sqrt(np.mean(ref[g] ** 2)))
-        worst = max(worst, err / tol)
+        diff = np.abs(out[g] - ref[g])
+        if dtype == "f32":
+            worst = max(worst, float(np.max(diff)) / 1e-5)
+            continue
+        rms = float(np.sqrt(np.mean(ref[g] ** 2)))
+        worst = max(worst, float(np.sqrt(np.mean(diff ** 2))) / (1e-2 * rms),
+                    float(np.max(diff / (1e-2 * rms + bf16_half_ulp(ref[g])))))
     return worst
 
 
