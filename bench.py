@@ -220,6 +220,10 @@ def run_gpu(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     w0 = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w0 = w0.with_(name=f"{w0.name}-b{args.batch}", batch=args.batch)
+    if args.prompt:
+        w0 = w0.with_(name=f"{w0.name}-p{args.prompt}", prompt=args.prompt)
     W, K = args.warmup, args.steps
     KE = args.e2e_steps
     total_steps = W + K + KE
@@ -257,10 +261,12 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0t = time.time()
+    torch.cuda.nvtx.range_push("timed")
     ev0.record(stream)
     for s in range(W, W + K):
         nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
     ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     w1t = time.time()
     barrier(world)
@@ -450,6 +456,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="nosa", choices=["nosa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
+    ap.add_argument("--prompt", type=int, default=0, help="override the workload's prompt")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
