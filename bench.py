@@ -313,17 +313,26 @@ def run_gpu(args, rank, world, local_rank):
     tail_mid = (w.prompt + W + K // 2) % w.block + 1
     tu = st["t_us"]
     nt = max(st["t_count"], 1)
+    # phases of nosa_stats: append+pool, score, select+set-difference, attention
+    # over the slots kept from the previous step (runs while the gather runs on a
+    # side stream), gather, attention over the filled slots (waits for the gather)
     phase_us = {name: tu[i] / nt for i, name in enumerate(
-        ["append_pool", "score", "select", "setdiff", "gather", "attention", "combine", "step"])}
+        ["append_pool", "score", "select_setdiff", "attention_kept", "gather",
+         "attention_loaded", "unused", "step"])}
+    phase_us.pop("unused")
+    loads_per_unit = (st["host_loads"] + st["tail_loads"]) / max(K * w.units, 1)
+    elt = 4 if w.dtype == "f32" else 2
+    per_block = w.block * (2 * w.head_dim * elt + 4)
     attn_bytes = attn_bytes_per_launch(w, n_cand, tail_mid)
+    attn_kept_bytes = attn_bytes - w.units * loads_per_unit * per_block
     score_bytes = score_bytes_per_launch(w, n_cand)
     peak, peak_kind = measured_peaks()
-    attn_gbs = attn_bytes / (phase_us["attention"] * 1e-6) / 1e9
+    attn_gbs = attn_kept_bytes / (phase_us["attention_kept"] * 1e-6) / 1e9
     score_gbs = score_bytes / (phase_us["score"] * 1e-6) / 1e9
     host_bytes_step = st["host_bytes"] / max(st["steps"] - W, 1) if st["steps"] > W else 0.0
     recall_gbs = (host_bytes_step / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
-    dominant = "attention" if phase_us["attention"] >= phase_us["score"] else "score"
-    dom_bytes, dom_us = ((attn_bytes, phase_us["attention"]) if dominant == "attention"
+    dominant = "attention" if phase_us["attention_kept"] >= phase_us["score"] else "score"
+    dom_bytes, dom_us = ((attn_kept_bytes, phase_us["attention_kept"]) if dominant == "attention"
                          else (score_bytes, phase_us["score"]))
     traffic = ncu_traffic(w0.name) if dominant == "attention" else None
     value = tokens / max_secs
@@ -364,7 +373,8 @@ def run_gpu(args, rank, world, local_rank):
         "near_ties": st["near_ties"],
         "e2e": {"value": round(e2e_tokens / e2e_max, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": KE},
-        "gpu_launches": 7 * K,
+        "gpu_launches": 6 * K,
+        "loads_per_unit_step": round(loads_per_unit, 3),
         "clocks": clocks,
     }
     return line

@@ -168,8 +168,11 @@ typedef struct {
   int32_t device_error;          /* nonzero: a bounded wait in a kernel gave up     */
   int32_t pad_;
   /* Accumulated device time (microseconds) of each phase when NOSA_FLAG_TIMING:
-   * [0] append+pool, [1] score, [2] select, [3] set-difference, [4] gather,
-   * [5] attention, [6] combine, [7] whole step.  t_count = steps timed. */
+   * [0] append+pool, [1] score, [2] select + set-difference, [3] attention over
+   * the slots kept from the previous step (runs while the gather runs), [4]
+   * gather (on the handle's side stream), [5] attention over the slots the
+   * gather filled, including the wait for the gather, and the merge of all
+   * partials, [6] unused (0), [7] whole step.  t_count = steps timed. */
   double t_us[8];
   int64_t t_count;
 } nosa_stats_t;

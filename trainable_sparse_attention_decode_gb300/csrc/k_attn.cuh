@@ -15,7 +15,10 @@
 // on mbarriers (no tensor map: the units are contiguous). Each warp owns 16 of
 // the 64 tokens of every block and keeps its own running max / sum / accumulator;
 // the 4 warps merge at the end and the CTA writes one partial per query head.
-// A combine kernel merges the splits.
+// Several launches may contribute partials to the same units (the decode step
+// runs one over the slots it already held while the gather fills the others,
+// then one over the freshly filled slots); the CTA that publishes a unit's last
+// partial merges them all into the output (a fence-and-count pattern, no spin).
 //
 // Token work inside a warp:
 //   logits : lane (t = lane % 16, half = lane / 16) dots token t with one half of
@@ -44,6 +47,10 @@ struct AttnKParams {
   float* part_acc;
   float* part_ml;
   int nsplit, bps, stages;
+  int split_base, nsplit_total;
+  int* counters;
+  void* out;
+  float* lse;
   long long payload;
   int Hq, Hkv;
   float qscale;  // log2(e) / sqrt(d)
@@ -341,7 +348,8 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
     }
   }
   __syncthreads();
-  const long long pbase = ((long long)u * p.nsplit + sp) * G;
+  const int nst = p.nsplit_total;
+  const long long pbase = ((long long)u * nst + p.split_base + sp) * G;
   for (int i = tid; i < G * D; i += 128) {
     const int g = i / D, dim = i % D;
     float M = red_m[g];
@@ -360,31 +368,52 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
       p.part_ml[(pbase + g) * 2 + 1] = L;
     }
   }
-}
 
-// Merges the split partials of each unit. grid = U, block = 128.
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ part_acc,
-                                                           const float* __restrict__ part_ml,
-                                                           int nsplit, int Hq, int Hkv, T* out,
-                                                           float* lse) {
-  const int u = blockIdx.x, b = u / Hkv, h = u % Hkv;
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int g = i / D, dim = i % D;
-    const float* ml = part_ml + ((long long)u * nsplit * G + g) * 2;
-    const float* ac = part_acc + ((long long)u * nsplit * G + g) * D + dim;
+  // The CTA that writes the unit's last partial merges all of them (no waiting:
+  // every other CTA has already published its partial before counting itself).
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) s_last = (atomicAdd(&p.counters[u], 1) == nst - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // All (max, sum) pairs of the unit are contiguous: stage them, turn them into
+  // per-partial weights exp2(m_j - M) / L, then sum the accumulators with
+  // independent (unrolled) loads.
+  const long long ubase = (long long)u * nst * G;
+  float* ml_s = reinterpret_cast<float*>(stage_buf);   // [nst][G][2]
+  float* w_s = ml_s + 2 * nst * G;                     // [nst][G]
+  __shared__ float s_M[8], s_L[8];
+  for (int i = tid; i < 2 * nst * G; i += 128) ml_s[i] = __ldcg(p.part_ml + ubase * 2 + i);
+  __syncthreads();
+  if (tid < G) {
     float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, ml[(long long)sp * G * 2]);
-    float A = 0.f, L = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float sc = exp2f(ml[(long long)sp * G * 2] - M);
-      A += ac[(long long)sp * G * D] * sc;
-      L += ml[(long long)sp * G * 2 + 1] * sc;
+    for (int j = 0; j < nst; ++j) M = fmaxf(M, ml_s[(j * G + tid) * 2]);
+    float L = 0.f;
+    for (int j = 0; j < nst; ++j) {
+      const float sc = exp2f(ml_s[(j * G + tid) * 2] - M);
+      w_s[j * G + tid] = sc;
+      L += ml_s[(j * G + tid) * 2 + 1] * sc;
     }
-    const long long row = (long long)b * Hq + (long long)h * G + g;
-    out[row * D + dim] = from_f32<T>(L > 0.f ? A / L : 0.f);
-    if (dim == 0 && lse != nullptr) lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    s_M[tid] = M;
+    s_L[tid] = L;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int j = 0; j < nst; ++j) w_s[j * G + tid] *= inv;
   }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += 128) {
+    const int g = i / D, dim = i % D;
+    const float* ac = p.part_acc + (ubase + g) * D + dim;
+    float A = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < nst; ++j) A += __ldcg(ac + (long long)j * G * D) * w_s[j * G + g];
+    const long long row = (long long)b * p.Hq + (long long)h * G + g;
+    reinterpret_cast<T*>(p.out)[row * D + dim] = from_f32<T>(A);
+    if (dim == 0 && p.lse != nullptr)
+      p.lse[row] = s_L[g] > 0.f ? (s_M[g] + log2f(s_L[g])) * kLn2 : -INFINITY;
+  }
+  if (tid == 0) p.counters[u] = 0;
 }
 
 template <typename T, int D, int G>
@@ -402,6 +431,11 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
   p.nsplit = a.nsplit;
+  p.split_base = a.split_base;
+  p.nsplit_total = a.nsplit_total;
+  p.counters = a.counters;
+  p.out = a.out;
+  p.lse = a.lse;
   p.bps = bps;
   p.stages = stages;
   p.payload = s.payload;
@@ -415,11 +449,6 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   if (err != cudaSuccess) return err;
   dim3 grid(a.nsplit, s.U);
   attn_split_kernel<T, D, G><<<grid, 128, smem, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  if (a.mid != nullptr) cudaEventRecord(a.mid, stream);
-  attn_combine_kernel<T, D, G><<<s.U, 128, 0, stream>>>(a.part_acc, a.part_ml, a.nsplit, s.Hq,
-                                                        s.Hkv, reinterpret_cast<T*>(a.out), a.lse);
   return cudaGetLastError();
 }
 

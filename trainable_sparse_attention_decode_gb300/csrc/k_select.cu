@@ -24,8 +24,6 @@ namespace {
 
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kDiffThreads = 128;
-constexpr int kDiffWarps = kDiffThreads / 32;
 
 // Exclusive prefix (in thread order) of one int per thread; *total gets the sum.
 template <int NWARPS>
@@ -179,9 +177,16 @@ __device__ void near_tie_stat(const uint32_t* key, const uint8_t* flag, uint8_t 
   __syncthreads();
 }
 
+template <int NT>
+__device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
+                              int cold);
+
 // grid = U, block = 256. Dynamic shared memory: key [maxBlk] u32 + flag [maxBlk] u8.
-// flag bits: 1 = eligible, 2 = in Gamma_e, 4 = in Gamma_q.
-__global__ void __launch_bounds__(kSelThreads) select_kernel(Shape s, State st, int n) {
+// flag bits: 1 = eligible, 2 = in Gamma_e, 4 = in Gamma_q. The set-difference
+// against the unit's slots runs in the same CTA once Gamma is known.
+__global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, State st, int n,
+                                                                     int just_completed,
+                                                                     int cold) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ SelShared sh;
   uint32_t* key = reinterpret_cast<uint32_t*>(dyn);
@@ -237,16 +242,24 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Shape s, State st, 
     st.nsel[2 * u] = need_e;
     st.nsel[2 * u + 1] = need_q;
   }
+  __syncthreads();  // selmask and nsel of this unit are visible to the whole CTA
+  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold);
 }
 
-// grid = U, block = 128.
-__global__ void __launch_bounds__(kDiffThreads) setdiff_kernel(Shape s, State st, int n,
-                                                               int just_completed, int cold) {
+// Set-difference of the unit's Gamma (selmask) against its slots. Writes the
+// load list (ascending block, paired by rank with the ascending free slots), the
+// new slot table and residency mask, the two attention block tables (slots kept
+// from the previous step; slots filled by this step's loads) and the gather
+// work list entries.
+template <int NT>
+__device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
+                              int cold) {
+  constexpr int kDiffThreads = NT;
+  constexpr int kDiffWarps = NT / 32;
   __shared__ int load_blk[kMaxK];
   __shared__ int free_list[kMaxK];
   __shared__ int warp_tot[kDiffWarps];
   __shared__ int s_base, s_tail_loaded;
-  const int u = blockIdx.x;
   const uint32_t* selm = st.selmask + (long long)u * s.W;
   uint32_t* resm = st.resmask + (long long)u * s.W;
   int32_t* s2b = st.slot2blk + (long long)u * s.k;
@@ -300,8 +313,20 @@ __global__ void __launch_bounds__(kDiffThreads) setdiff_kernel(Shape s, State st
     s_base = atomicAdd(st.work_count, nload);
   }
   __syncthreads();
-  for (int sl = threadIdx.x; sl < s.k; sl += kDiffThreads)
-    st.block_tab[(long long)u * s.k + sl] = (s2b[sl] >= 0) ? u * s.k + sl : -1;
+  // Attention tables: slots kept from the previous step (usable while the gather
+  // runs) and slots that this step's loads fill.
+  int32_t* tres = st.block_tab + (long long)u * s.k;
+  int32_t* tnew = st.tab_new + (long long)u * s.k;
+  for (int sl = threadIdx.x; sl < s.k; sl += kDiffThreads) tres[sl] = (s2b[sl] >= 0) ? u * s.k + sl : -1;
+  __syncthreads();
+  for (int j = threadIdx.x; j < s.k; j += kDiffThreads) {
+    if (j < nload) {
+      tres[free_list[j]] = -1;
+      tnew[j] = u * s.k + free_list[j];
+    } else {
+      tnew[j] = -1;
+    }
+  }
   for (int j = threadIdx.x; j < nload; j += kDiffThreads) st.work[s_base + j] = u * s.k + j;
 
   if (threadIdx.x == 0) {
@@ -325,18 +350,13 @@ __global__ void __launch_bounds__(kDiffThreads) setdiff_kernel(Shape s, State st
 
 }  // namespace
 
-cudaError_t launch_select(const Shape& s, const State& st, int n_cand, cudaStream_t stream) {
+cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
+                                  int just_completed, int cold, cudaStream_t stream) {
   const size_t smem = (size_t)s.maxBlk * 5;
-  cudaError_t err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+  cudaError_t err = cudaFuncSetAttribute(select_setdiff_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  select_kernel<<<s.U, kSelThreads, smem, stream>>>(s, st, n_cand);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_setdiff(const Shape& s, const State& st, int n_cand, int just_completed,
-                           int cold, cudaStream_t stream) {
-  setdiff_kernel<<<s.U, kDiffThreads, 0, stream>>>(s, st, n_cand, just_completed, cold);
+  select_setdiff_kernel<<<s.U, kSelThreads, smem, stream>>>(s, st, n_cand, just_completed, cold);
   return cudaGetLastError();
 }
 

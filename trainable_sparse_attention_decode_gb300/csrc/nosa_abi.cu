@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -122,10 +123,13 @@ bool attention_supported(int dtype, int d, int G) {
          (G == 1 || G == 2 || G == 3 || G == 4 || G == 6 || G == 8);
 }
 
+// Standalone-attention workspace: partial accumulators, partial (max, sum),
+// per-unit split counters, then a 16-byte tail whose first int is the error word.
 size_t attention_workspace_bytes(const Shape& s, int nsplit) {
   size_t acc = (size_t)s.U * nsplit * s.G * s.d * 4;
   size_t ml = (size_t)s.U * nsplit * s.G * 2 * 4;
-  return ((acc + 15) & ~(size_t)15) + ((ml + 15) & ~(size_t)15) + 16;
+  size_t cnt = (size_t)s.U * 4;
+  return ((acc + 15) & ~(size_t)15) + ((ml + 15) & ~(size_t)15) + ((cnt + 15) & ~(size_t)15) + 16;
 }
 
 // Splits per unit: the smallest count whose CTA total fills the GPU's resident
@@ -174,11 +178,13 @@ struct nosa_handle {
   size_t host_bytes = 0;
   long long L = 0;
   long long steps = 0;
-  int nsplit = 1;
+  int nsplit = 1;       // attention splits over the slots kept from the previous step
   int gather_grid = 1;
   bool broken = false;
   std::string err;
   cudaStream_t last_stream = nullptr;
+  cudaStream_t side = nullptr;  // high-priority stream of the gather
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   bool timing = false;
   cudaEvent_t ev[kRing][kNumEv];
   bool pending[kRing];
@@ -218,17 +224,27 @@ void free_all(nosa_handle* h) {
       for (int i = 0; i < kNumEv; ++i) cudaEventDestroy(h->ev[r][i]);
     h->timing = false;
   }
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
+  h->ev_fork = h->ev_join = nullptr;
+  h->side = nullptr;
 }
 
+// Events of one step: e0 start, e1 after append, e2 after score, e3 after
+// select + set-difference (main stream); e4, e5 around the gather (side
+// stream); e6 after attention over kept slots, e7 after attention over loaded
+// slots and the merge (main stream).
 void harvest(nosa_handle* h, int r) {
   if (!h->pending[r]) return;
-  if (cudaEventSynchronize(h->ev[r][kNumEv - 1]) != cudaSuccess) return;
-  float ms;
-  for (int i = 0; i < kNumEv - 1; ++i)
-    if (cudaEventElapsedTime(&ms, h->ev[r][i], h->ev[r][i + 1]) == cudaSuccess)
-      h->t_us[i] += ms * 1000.0;
-  if (cudaEventElapsedTime(&ms, h->ev[r][0], h->ev[r][kNumEv - 1]) == cudaSuccess)
-    h->t_us[7] += ms * 1000.0;
+  cudaEvent_t* e = h->ev[r];
+  if (cudaEventSynchronize(e[7]) != cudaSuccess) return;
+  const int pairs[7][3] = {{0, 0, 1}, {1, 1, 2}, {2, 2, 3}, {3, 3, 6}, {4, 4, 5}, {5, 6, 7},
+                           {7, 0, 7}};
+  for (const auto& pr : pairs) {
+    float ms;
+    if (cudaEventElapsedTime(&ms, e[pr[1]], e[pr[2]]) == cudaSuccess) h->t_us[pr[0]] += ms * 1000.0;
+  }
   h->t_count += 1;
   h->pending[r] = false;
 }
@@ -307,8 +323,10 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.work, U * k * 4);
   A(&st.work_count, 16);
   A(&st.block_tab, U * k * 4);
-  A(&st.part_acc, U * kMaxSplits * s.G * s.d * 4);
-  A(&st.part_ml, U * kMaxSplits * s.G * 2 * 4);
+  A(&st.tab_new, U * k * 4);
+  A(&st.att_cnt, U * 4);
+  A(&st.part_acc, U * 2 * kMaxSplits * s.G * s.d * 4);
+  A(&st.part_ml, U * 2 * kMaxSplits * s.G * 2 * 4);
   A(&st.stats, sizeof(DevStats));
   if (e != cudaSuccess) {
     g_thread_err = std::string("device allocation failed: ") + cudaGetErrorString(e);
@@ -334,6 +352,8 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(st.nload, 0, U * 4);
   if (e == cudaSuccess) e = cudaMemset(st.work_count, 0, 16);
   if (e == cudaSuccess) e = cudaMemset(st.block_tab, 0xFF, U * k * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.tab_new, 0xFF, U * k * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.att_cnt, 0, U * 4);
   DevStats ds = fresh_stats();
   if (e == cudaSuccess) e = cudaMemcpy(st.stats, &ds, sizeof(ds), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
@@ -362,7 +382,25 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     return NOSA_ERR_CUDA;
   }
   st.host = static_cast<uint8_t*>(dp);
-  h->gather_grid = sm_count_current() * 8;
+  // The gather shares the GPU with attention over the kept slots: one CTA per
+  // SM keeps enough host reads in flight for the link without taking the SMs'
+  // thread slots (NOSA_GATHER_CTAS overrides the grid, for tuning).
+  h->gather_grid = sm_count_current();
+  if (const char* g = std::getenv("NOSA_GATHER_CTAS")) {
+    const int v = std::atoi(g);
+    if (v > 0) h->gather_grid = v;
+  }
+  int prio_lo = 0, prio_hi = 0;
+  cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
+  e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_hi);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("stream/event creation failed: ") + cudaGetErrorString(e);
+    free_all(h);
+    delete h;
+    return NOSA_ERR_CUDA;
+  }
   if (cfg->flags & NOSA_FLAG_TIMING) {
     for (int r = 0; r < kRing; ++r)
       for (int i = 0; i < kNumEv; ++i) cudaEventCreate(&h->ev[r][i]);
@@ -426,29 +464,48 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
   if (ev) cudaEventRecord(ev[1], s);
   if (err == cudaSuccess) err = launch_score(sh, st, q, N, s);
   if (ev) cudaEventRecord(ev[2], s);
-  if (err == cudaSuccess) err = launch_select(sh, st, N, s);
+  const bool cold = (h->steps == 0);
+  if (err == cudaSuccess) err = launch_select_setdiff(sh, st, N, jc, cold ? 1 : 0, s);
   if (ev) cudaEventRecord(ev[3], s);
-  if (err == cudaSuccess) err = launch_setdiff(sh, st, N, jc, h->steps == 0 ? 1 : 0, s);
-  if (ev) cudaEventRecord(ev[4], s);
-  if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, s);
-  if (ev) cudaEventRecord(ev[5], s);
+  // Fork: the gather fills this step's free slots on the side stream while the
+  // main stream attends over the slots kept from the previous step (and the
+  // tail); then the main stream joins and attends over the filled slots.
+  if (err == cudaSuccess) err = cudaEventRecord(h->ev_fork, s);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+  if (ev) cudaEventRecord(ev[4], h->side);
+  if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->side);
+  if (ev) cudaEventRecord(ev[5], h->side);
+  if (err == cudaSuccess) err = cudaEventRecord(h->ev_join, h->side);
+  const int ns_kept = h->nsplit;
+  const int ns_new = cold ? h->nsplit : 1;
+  AttnArgs a;
+  a.units = st.slots;
+  a.n_units = (long long)sh.U * sh.k;
+  a.n_blocks = sh.k;
+  a.tail_stride = 2 * sh.payload;
+  a.tail_len = T;
+  a.q = q;
+  a.out = out;
+  a.lse = lse;
+  a.part_acc = st.part_acc;
+  a.part_ml = st.part_ml;
+  a.nsplit_total = ns_kept + ns_new;
+  a.counters = st.att_cnt;
+  a.err = &st.stats->error;
   if (err == cudaSuccess) {
-    AttnArgs a;
-    a.units = st.slots;
-    a.n_units = (long long)sh.U * sh.k;
     a.block_tab = st.block_tab;
-    a.n_blocks = sh.k;
     a.tail = st.tail + (long long)(N & 1) * sh.payload;
-    a.tail_stride = 2 * sh.payload;
-    a.tail_len = T;
-    a.q = q;
-    a.out = out;
-    a.lse = lse;
-    a.part_acc = st.part_acc;
-    a.part_ml = st.part_ml;
-    a.nsplit = h->nsplit;
-    a.err = &st.stats->error;
-    a.mid = ev ? ev[6] : nullptr;
+    a.nsplit = ns_kept;
+    a.split_base = 0;
+    err = launch_attention(sh, a, s);
+  }
+  if (ev) cudaEventRecord(ev[6], s);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(s, h->ev_join, 0);
+  if (err == cudaSuccess) {
+    a.block_tab = st.tab_new;
+    a.tail = nullptr;
+    a.nsplit = ns_new;
+    a.split_base = ns_kept;
     err = launch_attention(sh, a, s);
   }
   if (ev) cudaEventRecord(ev[7], s);
@@ -619,12 +676,16 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
   a.q = q;
   a.out = out;
   a.lse = lse;
+  const size_t cnt_bytes = ((size_t)s.U * 4 + 15) & ~(size_t)15;
   a.part_acc = reinterpret_cast<float*>(ws);
   a.part_ml = reinterpret_cast<float*>(ws + acc_bytes);
   a.nsplit = nsplit;
-  a.err = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes);
-  a.mid = nullptr;
-  cudaError_t e = cudaMemsetAsync(a.err, 0, sizeof(int), st);
+  a.split_base = 0;
+  a.nsplit_total = nsplit;
+  a.counters = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes);
+  a.err = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes + cnt_bytes);
+  // counters and error word start at zero (one memset over both)
+  cudaError_t e = cudaMemsetAsync(a.counters, 0, cnt_bytes + sizeof(int), st);
   if (e == cudaSuccess) e = launch_attention(s, a, st);
   if (e != cudaSuccess) {
     g_thread_err = std::string("attention launch: ") + cudaGetErrorString(e);

@@ -55,7 +55,9 @@ struct State {
   int32_t* nload;      // [U]
   int32_t* work;       // [U*k]             gather work list (entry = u*k + j)
   int32_t* work_count; // [1]
-  int32_t* block_tab;  // [U][k]            slot pool index of each valid slot, -1 empty
+  int32_t* block_tab;  // [U][k]            slots kept from the previous step (slot pool index), -1 none
+  int32_t* tab_new;    // [U][k]            slots filled by this step's loads, -1 none
+  int32_t* att_cnt;    // [U]               split CTAs finished (the last one merges; self-resetting)
   float* part_acc;     // split-K partial accumulators
   float* part_ml;      // split-K partial (max, sum)
   DevStats* stats;
@@ -72,13 +74,15 @@ cudaError_t launch_append_bulk(const Shape& s, const State& st, const void* k, c
                                const float* e, int L_old, int n, cudaStream_t stream);
 cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand,
                          cudaStream_t stream);
-cudaError_t launch_select(const Shape& s, const State& st, int n_cand, cudaStream_t stream);
-cudaError_t launch_setdiff(const Shape& s, const State& st, int n_cand, int just_completed,
-                           int cold, cudaStream_t stream);
+cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
+                                  int just_completed, int cold, cudaStream_t stream);
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, cudaStream_t stream);
 
 // Split-K attention over block units. block_tab [U][n_blocks] holds unit indices
 // into `units` (-1 skip). The tail unit of unit u is at tail + u * tail_stride.
+// One launch writes partials [split_base, split_base + nsplit) of each unit; the
+// CTA that finishes last among all nsplit_total partials of a unit (counted in
+// counters[u], which it resets to 0) merges them into out / lse.
 struct AttnArgs {
   const uint8_t* units;
   long long n_units;        // valid unit indices are [0, n_units)
@@ -93,8 +97,10 @@ struct AttnArgs {
   float* part_acc;          // [U][nsplit][G][d]
   float* part_ml;           // [U][nsplit][G][2]
   int nsplit;
+  int split_base;
+  int nsplit_total;
+  int* counters;            // [U]
   int* err;                 // device error word
-  cudaEvent_t mid;          // recorded between the split and combine kernels (may be null)
 };
 size_t attention_workspace_bytes(const Shape& s, int nsplit);
 int attention_pick_nsplit(const Shape& s, int n_blocks, int has_tail);
