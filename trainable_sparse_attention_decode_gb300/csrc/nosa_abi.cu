@@ -179,6 +179,7 @@ struct nosa_handle {
   long long L = 0;
   long long steps = 0;
   int nsplit = 1;       // attention splits over the slots kept from the previous step
+  int nsplit_new = 1;   // attention splits over the slots the gather filled (warm steps)
   int gather_grid = 1;
   bool broken = false;
   std::string err;
@@ -390,6 +391,10 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     const int v = std::atoi(g);
     if (v > 0) h->gather_grid = v;
   }
+  if (const char* g = std::getenv("NOSA_LOADED_SPLITS")) {
+    const int v = std::atoi(g);
+    if (v > 0 && v <= kMaxSplits) h->nsplit_new = v;
+  }
   int prio_lo = 0, prio_hi = 0;
   cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
   e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_hi);
@@ -477,7 +482,7 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
   if (ev) cudaEventRecord(ev[5], h->side);
   if (err == cudaSuccess) err = cudaEventRecord(h->ev_join, h->side);
   const int ns_kept = h->nsplit;
-  const int ns_new = cold ? h->nsplit : 1;
+  const int ns_new = cold ? h->nsplit : h->nsplit_new;
   AttnArgs a;
   a.units = st.slots;
   a.n_units = (long long)sh.U * sh.k;
