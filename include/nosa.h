@@ -240,6 +240,31 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
                                   int32_t tail_len, const void* q, void* out, float* lse,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * nosa_sparse_attention without a caller workspace and without allocating.
+ * (The NOSA pages have no counterpart of this call: it serves callers.)
+ *
+ * For callers that cannot allocate device memory: a serving engine or
+ * framework that reserves all device memory up front in its own pool (an
+ * allocation from inside this library could fail although the pool has free
+ * memory, and would escape the pool's accounting), or a latency-critical loop
+ * that must avoid cudaMalloc / cudaFree because they can synchronise the device.
+ * Arguments are those of nosa_sparse_attention minus the workspace; the caller
+ * still passes the inputs and outputs. The split-K scratch lives in one static
+ * 16 MiB array in the library's device memory, held by every GPU that loads the
+ * library until the process exits; nothing is allocated. The first call on a
+ * device (with cfg->device made current for the lookup) finds that array's
+ * device address; make it before any stream capture. All calls share the array
+ * and it keeps the last call's contents (each call clears its counters and
+ * error word); calls that overlap on the GPU race. Shapes whose scratch
+ * (nosa_attention_workspace_bytes) exceeds 16 MiB are rejected with
+ * NOSA_ERR_CAPACITY and a message in nosa_last_error(NULL). Async.
+ */
+nosa_status nosa_sparse_attention_noalloc(const nosa_config* cfg, const void* units,
+                                          int64_t n_units, const int32_t* block_tab,
+                                          int32_t n_blocks, const void* tail, int32_t tail_len,
+                                          const void* q, void* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ __all__ = [
     "nosa_config", "nosa_config_validate", "nosa_payload_bytes", "nosa_create",
     "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset",
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
-    "nosa_attention_workspace_bytes", "nosa_sparse_attention",
+    "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -80,6 +80,8 @@ def _load():
         "nosa_attention_workspace_bytes": (SZ, [P(NosaConfig), I32]),
         "nosa_sparse_attention": (C.c_int, [P(NosaConfig), VP, C.c_int64, VP, I32, VP, I32, VP,
                                             VP, VP, VP, SZ, VP]),
+        "nosa_sparse_attention_noalloc": (C.c_int, [P(NosaConfig), VP, C.c_int64, VP, I32, VP,
+                                                    I32, VP, VP, VP, VP]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -246,3 +248,22 @@ def nosa_sparse_attention(cfg: NosaConfig, units, block_tab, tail, tail_len, q, 
         _ptr(q, qs, dt, "q"), _ptr(out, qs, dt, "out"),
         _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True),
         _ptr(workspace, None, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def nosa_sparse_attention_noalloc(cfg: NosaConfig, units, block_tab, tail, tail_len, q, out,
+                                  lse, stream=None):
+    """nosa_sparse_attention with the library's static device scratch instead of a
+    caller workspace: nothing is allocated, for callers that cannot allocate device
+    memory (see include/nosa.h). Calls that overlap on the GPU share that scratch."""
+    torch = _torch()
+    dt = _dtype_of(cfg)
+    U = cfg.batch * cfg.n_kv_heads
+    n_blocks = block_tab.shape[1]
+    qs = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    _check(lib.nosa_sparse_attention_noalloc(
+        C.byref(cfg), _ptr(units, None, torch.uint8, "units"),
+        units.numel() // nosa_payload_bytes(cfg),
+        _ptr(block_tab, (U, n_blocks), torch.int32, "block_tab", 4), n_blocks,
+        _ptr(tail, None, torch.uint8, "tail", allow_none=True), int(tail_len),
+        _ptr(q, qs, dt, "q"), _ptr(out, qs, dt, "out"),
+        _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True), _stream(stream)))

@@ -156,6 +156,9 @@ int attention_pick_nsplit(const Shape& s, int n_blocks, int /*has_tail*/) {
   return best;
 }
 
+// Message returned by nosa_last_error(NULL) on this thread.
+void set_thread_error(const std::string& msg) { g_thread_err = msg; }
+
 cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t stream) {
   const int stages = attn_stages(s.payload);
   const int nv = a.n_blocks + (a.tail ? 1 : 0);
