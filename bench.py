@@ -234,18 +234,17 @@ def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20):
     ws = torch.empty(nosa.nosa_attention_workspace_bytes(cfg, nb), dtype=torch.uint8, device="cuda")
     for _ in range(3):
         nosa.nosa_sparse_attention(cfg, body, tab, tail, tail_len, q, out, lse, ws)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    total = 0.0
+    # The units (hundreds of MB) exceed L2, so back-to-back launches read HBM; queueing
+    # them hides the host's per-call work.
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
     for _ in range(reps):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
         nosa.nosa_sparse_attention(cfg, body, tab, tail, tail_len, q, out, lse, ws)
-        b.record()
-        b.synchronize()
-        total += a.elapsed_time(b) / 1e3
-    del units, flush
-    return total / reps, attn_bytes_per_launch(w, n_cand, tail_len)
+    b.record()
+    b.synchronize()
+    del units
+    return a.elapsed_time(b) / 1e3 / reps, attn_bytes_per_launch(w, n_cand, tail_len)
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -299,8 +298,10 @@ def run_gpu(args, rank, world, local_rank):
     w0t = time.time()
     torch.cuda.nvtx.range_push("timed")
     ev0.record(stream)
+    h0 = time.perf_counter()
     for s in range(W, W + K):
         nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
+    host_enqueue_us = (time.perf_counter() - h0) / K * 1e6
     ev1.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
@@ -356,10 +357,13 @@ def run_gpu(args, rank, world, local_rank):
     # phases of nosa_stats: append+pool, score, select+set-difference, attention
     # over the slots kept from the previous step (runs while the gather runs on a
     # side stream), gather, attention over the filled slots (waits for the gather)
+    # phases of nosa_stats (the step is pipelined over unit chunks, so they overlap;
+    # each spans its first start to its last end)
     phase_us = {name: tu[i] / nt for i, name in enumerate(
-        ["append_pool", "score", "select_setdiff", "attention_kept", "gather",
-         "attention_loaded", "unused", "step"])}
-    phase_us.pop("unused")
+        ["append_pool", "score_select", "unused2", "attention_kept", "gather",
+         "after_kept", "unused6", "step"])}
+    phase_us.pop("unused2")
+    phase_us.pop("unused6")
     loads_per_unit = (st["host_loads"] + st["tail_loads"]) / max(K * w.units, 1)
     elt = 4 if w.dtype == "f32" else 2
     per_block = w.block * (2 * w.head_dim * elt + 4)
@@ -368,7 +372,7 @@ def run_gpu(args, rank, world, local_rank):
     score_bytes = score_bytes_per_launch(w, n_cand)
     peak, peak_kind = measured_peaks()
     attn_gbs = attn_kept_bytes / (phase_us["attention_kept"] * 1e-6) / 1e9
-    score_gbs = score_bytes / (phase_us["score"] * 1e-6) / 1e9
+    score_gbs = score_bytes / (phase_us["score_select"] * 1e-6) / 1e9  # incl. selection
     host_bytes_step = st["host_bytes"] / max(st["steps"] - W, 1) if st["steps"] > W else 0.0
     recall_gbs = (host_bytes_step / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
     # Roofline kernel: the split-K attention, timed alone on the step's shape (in the
@@ -415,8 +419,9 @@ def run_gpu(args, rank, world, local_rank):
         "near_ties": st["near_ties"],
         "e2e": {"value": round(e2e_tokens / e2e_max, 3), "unit": "tokens/s",
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": KE},
-        "gpu_launches": 6 * K,
+        "gpu_launches": st["launches"],
         "loads_per_unit_step": round(loads_per_unit, 3),
+        "host_enqueue_us_per_step": round(host_enqueue_us, 2),
         "clocks": clocks,
     }
     return line

@@ -167,14 +167,17 @@ typedef struct {
                                     differ by < 1e-5 * max |score|                  */
   int32_t device_error;          /* nonzero: a bounded wait in a kernel gave up     */
   int32_t pad_;
-  /* Accumulated device time (microseconds) of each phase when NOSA_FLAG_TIMING:
-   * [0] append+pool, [1] score, [2] select + set-difference, [3] attention over
-   * the slots kept from the previous step (runs while the gather runs), [4]
-   * gather (on the handle's side stream), [5] attention over the slots the
-   * gather filled, including the wait for the gather, and the merge of all
-   * partials, [6] unused (0), [7] whole step.  t_count = steps timed. */
+  /* Accumulated device time (microseconds) of each phase when NOSA_FLAG_TIMING.
+   * The step is pipelined over chunks of units on internal streams, so the
+   * phases overlap; each entry spans a phase's first start to its last end:
+   * [0] append+pool, [1] scoring + selection + set-difference of all chunks,
+   * [2] unused (0), [3] attention over the slots kept from the previous step,
+   * [4] gather, [5] from the end of [3] to the end of the step (attention over
+   * the filled slots, the merge), [6] unused (0), [7] whole step.
+   * t_count = steps timed. */
   double t_us[8];
   int64_t t_count;
+  int64_t launches;              /* kernels launched by decode steps (host count)    */
 } nosa_stats_t;
 
 /* Synchronises the handle's last stream and fills *out. */

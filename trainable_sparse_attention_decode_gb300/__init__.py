@@ -56,7 +56,7 @@ class NosaStats(C.Structure):
                 ("min_hits", C.c_int32), ("sum_hits", C.c_int64), ("hit_samples", C.c_int64),
                 ("gamma_min", C.c_double), ("gamma_mean", C.c_double),
                 ("near_ties", C.c_int64), ("device_error", C.c_int32), ("pad_", C.c_int32),
-                ("t_us", C.c_double * 8), ("t_count", C.c_int64)]
+                ("t_us", C.c_double * 8), ("t_count", C.c_int64), ("launches", C.c_int64)]
 
 
 def _load():

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st,
   const int t = L_old;
   const int blk = t / s.B, pos = t % s.B;
   uint8_t* cur = st.tail + ((long long)u * 2 + (blk & 1)) * s.payload;
-  if (u == 0 && threadIdx.x == 0) *st.work_count = 0;
+  if (u == 0 && threadIdx.x < kMaxChunks) st.work_count[threadIdx.x] = 0;
 
   // The block before a newly opened one becomes a candidate.
   if (pos == 0 && blk > 0) {

@@ -48,6 +48,7 @@ struct AttnKParams {
   float* part_ml;
   int nsplit, bps, stages;
   int split_base, nsplit_total;
+  int unit_base;
   int* counters;
   void* out;
   float* lse;
@@ -73,21 +74,25 @@ template <> struct Unpack16<float> {
   }
 };
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, int W>
 struct AttnGeom {
   static constexpr int B = 64;
+  static constexpr int NT = 32 * W;       // threads per CTA
+  static constexpr int TPW = B / W;       // tokens of each block per warp
+  static constexpr int PARTS = 32 / TPW;  // head-dim parts of the logit lanes
   static constexpr int ELT = (int)sizeof(T);
   static constexpr int CE = 16 / ELT;     // elements per 16-byte chunk
   static constexpr int NCH = D / CE;      // chunks per token row
-  static constexpr int NCH2 = NCH / 2;    // chunks per half row (logit lanes)
+  static constexpr int NCHP = NCH / PARTS;  // chunks per part (logit lanes)
   static constexpr int TG = 32 / NCH;     // token groups of the p.V lanes
-  static constexpr int TPL = 16 / TG;     // tokens per p.V lane per block
+  static constexpr int TPL = TPW / TG;    // tokens per p.V lane per block
   static constexpr int GP = (G + 3) / 4 * 4;
-  static constexpr int QH = D / 2 + 4;    // padded floats per half query row
+  static constexpr int QP = D / PARTS + 4;  // padded floats per query part row
   static_assert(NCH >= 2 && NCH <= 32, "token row must be 32..512 bytes");
+  static_assert(NCHP >= 1 && TPL >= 1, "warp split does not fit the row");
   static size_t smem_bytes(int stages, long long payload, int bps) {
     size_t off = (size_t)stages * payload;
-    off += (size_t)G * 2 * QH * 4 + (size_t)4 * 16 * GP * 4 + (size_t)(bps + 1) * 4;
+    off += (size_t)G * PARTS * QP * 4 + (size_t)B * GP * 4 + (size_t)(bps + 1) * 4;
     off = (off + 7) & ~(size_t)7;
     off += (size_t)2 * stages * 8;
     return off;
@@ -97,25 +102,26 @@ struct AttnGeom {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
-  using Gm = AttnGeom<T, D, G>;
-  constexpr int B = Gm::B, ELT = Gm::ELT, CE = Gm::CE, NCH = Gm::NCH, NCH2 = Gm::NCH2;
-  constexpr int TG = Gm::TG, TPL = Gm::TPL, GP = Gm::GP, QH = Gm::QH;
+template <typename T, int D, int G, int W>
+__global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
+  using Gm = AttnGeom<T, D, G, W>;
+  constexpr int B = Gm::B, ELT = Gm::ELT, CE = Gm::CE, NCH = Gm::NCH, NCHP = Gm::NCHP;
+  constexpr int TG = Gm::TG, TPL = Gm::TPL, GP = Gm::GP, QP = Gm::QP;
+  constexpr int NT = Gm::NT, TPW = Gm::TPW, PARTS = Gm::PARTS;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const long long payload = p.payload;
   uint8_t* stage_buf = smem;
   float* q_s = reinterpret_cast<float*>(smem + (size_t)p.stages * payload);
-  float* p_s = q_s + G * 2 * QH;
-  int* list = reinterpret_cast<int*>(p_s + 4 * 16 * GP);
+  float* p_s = q_s + G * PARTS * QP;
+  int* list = reinterpret_cast<int*>(p_s + B * GP);
   uint64_t* full =
       reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(list + p.bps + 1) + 7) & ~uintptr_t(7));
   uint64_t* empty = full + p.stages;
   __shared__ int s_nl;
   __shared__ volatile int s_bad;
 
-  const int u = blockIdx.y, sp = blockIdx.x;
+  const int u = p.unit_base + blockIdx.y, sp = blockIdx.x;
   const int b = u / p.Hkv, h = u % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Virtual item list: the n_blocks table entries, then the tail (if any),
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
+      mbar_init(&empty[s], W);
     }
     fence_mbar_init();
     s_bad = 0;
@@ -154,9 +160,9 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
   }
   {
     const T* qg = reinterpret_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)h * G) * D;
-    for (int i = tid; i < G * D; i += 128) {
+    for (int i = tid; i < G * D; i += NT) {
       const int g = i / D, dim = i % D;
-      q_s[g * 2 * QH + (dim / (D / 2)) * QH + (dim % (D / 2))] = to_f32(qg[i]) * p.qscale;
+      q_s[(g * PARTS + dim / (D / PARTS)) * QP + (dim % (D / PARTS))] = to_f32(qg[i]) * p.qscale;
     }
   }
   __syncthreads();
@@ -184,8 +190,8 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
 #pragma unroll
     for (int e = 0; e < CE / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
   }
-  const int t = lane & 15, hh = lane >> 4;
-  const int tok = warp * 16 + t;
+  const int t = lane % TPW, hh = lane / TPW;  // logit lane: token, head-dim part
+  const int tok = warp * TPW + t;
   const int c = lane % NCH, tg = lane / NCH;
 
   for (int it = 0; it < nl; ++it) {
@@ -203,18 +209,18 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
     const uint8_t* buf = stage_buf + (size_t)si * payload;
     const bool valid = (list[it] >= 0) || (tok < p.tail_len);
 
-    // ---- logits of this warp's 16 tokens ----
+    // ---- logits of this warp's TPW tokens ----
     float2 d2[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) d2[g] = make_float2(0.f, 0.f);
-    const uint4* kp = reinterpret_cast<const uint4*>(buf) + (hh * NCH2) * B + tok;
+    const uint4* kp = reinterpret_cast<const uint4*>(buf) + (hh * NCHP) * B + tok;
 #pragma unroll
-    for (int cc = 0; cc < NCH2; ++cc) {
+    for (int cc = 0; cc < NCHP; ++cc) {
       float kf[CE];
       Unpack16<T>::run(kp[cc * B], kf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float4* qp = reinterpret_cast<const float4*>(q_s + g * 2 * QH + hh * QH + cc * CE);
+        const float4* qp = reinterpret_cast<const float4*>(q_s + (g * PARTS + hh) * QP + cc * CE);
 #pragma unroll
         for (int e4 = 0; e4 < CE / 4; ++e4) {
           const float4 qv = qp[e4];
@@ -228,13 +234,12 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float dot = d2[g].x + d2[g].y;
-      dot += __shfl_xor_sync(0xffffffffu, dot, 16);
+#pragma unroll
+      for (int o = TPW; o < 32; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
       const float lg = valid ? dot + ev : -INFINITY;
       float mx = lg;
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+#pragma unroll
+      for (int o = 1; o < TPW; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float mn = fmaxf(m_run[g], mx);
       alpha[g] = exp2f(m_run[g] - mn);
       pg[g] = exp2f(lg - mn);
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
     const uint8_t* vbase = buf + (size_t)B * D * ELT;
 #pragma unroll
     for (int i = 0; i < TPL; ++i) {
-      const int tk = warp * 16 + tg + i * TG;
+      const int tk = warp * TPW + tg + i * TG;
       float vf[CE];
       Unpack16<T>::run(*reinterpret_cast<const uint4*>(vbase + ((size_t)tk * D + c * CE) * ELT), vf);
       float pv[GP];
@@ -296,15 +301,14 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
     }
   }
 
-  // Warp totals: each token's p sits in both halves of the warp; sum one half.
+  // Warp totals: each token's p sits in every head-dim part of the warp; sum
+  // over the tokens of one part.
   float lw[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float x = l_run[g];
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
+#pragma unroll
+    for (int o = 1; o < TPW; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     lw[g] = x;
   }
 #pragma unroll
@@ -328,9 +332,9 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
   }
   __syncthreads();
 
-  float* red_acc = reinterpret_cast<float*>(stage_buf);  // [4][G][D]
-  float* red_m = red_acc + 4 * G * D;                    // [4][G]
-  float* red_l = red_m + 4 * G;                          // [4][G]
+  float* red_acc = reinterpret_cast<float*>(stage_buf);  // [W][G][D]
+  float* red_m = red_acc + W * G * D;                    // [W][G]
+  float* red_l = red_m + W * G;                          // [W][G]
   if (tg == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -350,14 +354,14 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
   __syncthreads();
   const int nst = p.nsplit_total;
   const long long pbase = ((long long)u * nst + p.split_base + sp) * G;
-  for (int i = tid; i < G * D; i += 128) {
+  for (int i = tid; i < G * D; i += NT) {
     const int g = i / D, dim = i % D;
     float M = red_m[g];
 #pragma unroll
-    for (int w = 1; w < 4; ++w) M = fmaxf(M, red_m[w * G + g]);
+    for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w * G + g]);
     float A = 0.f, L = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < W; ++w) {
       const float sc = exp2f(red_m[w * G + g] - M);
       A += red_acc[(w * G + g) * D + dim] * sc;
       L += red_l[w * G + g] * sc;
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
   float* ml_s = reinterpret_cast<float*>(stage_buf);   // [nst][G][2]
   float* w_s = ml_s + 2 * nst * G;                     // [nst][G]
   __shared__ float s_M[8], s_L[8];
-  for (int i = tid; i < 2 * nst * G; i += 128) ml_s[i] = __ldcg(p.part_ml + ubase * 2 + i);
+  for (int i = tid; i < 2 * nst * G; i += NT) ml_s[i] = __ldcg(p.part_ml + ubase * 2 + i);
   __syncthreads();
   if (tid < G) {
     float M = -INFINITY;
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
     for (int j = 0; j < nst; ++j) w_s[j * G + tid] *= inv;
   }
   __syncthreads();
-  for (int i = tid; i < G * D; i += 128) {
+  for (int i = tid; i < G * D; i += NT) {
     const int g = i / D, dim = i % D;
     const float* ac = p.part_acc + (ubase + g) * D + dim;
     float A = 0.f;
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(AttnKParams p) {
   if (tid == 0) p.counters[u] = 0;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, int W>
 cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, int bps,
                                 cudaStream_t stream) {
   AttnKParams p;
@@ -433,6 +437,7 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.nsplit = a.nsplit;
   p.split_base = a.split_base;
   p.nsplit_total = a.nsplit_total;
+  p.unit_base = a.unit_base;
   p.counters = a.counters;
   p.out = a.out;
   p.lse = a.lse;
@@ -443,61 +448,74 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.Hkv = s.Hkv;
   p.qscale = (float)(1.4426950408889634 / sqrt((double)D));
   p.err = a.err;
-  const size_t smem = AttnGeom<T, D, G>::smem_bytes(stages, s.payload, bps);
-  cudaError_t err = cudaFuncSetAttribute(attn_split_kernel<T, D, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps);
+  static std::atomic<int> lim[64];
+  cudaError_t err = raise_smem_limit((const void*)attn_split_kernel<T, D, G, W>, smem, lim);
   if (err != cudaSuccess) return err;
-  dim3 grid(a.nsplit, s.U);
-  attn_split_kernel<T, D, G><<<grid, 128, smem, stream>>>(p);
+  dim3 grid(a.nsplit, a.unit_count);
+  attn_split_kernel<T, D, G, W><<<grid, 32 * W, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 // CTAs per SM of one variant at the given pipeline depth (0 if it cannot run).
-template <typename T, int D, int G>
+template <typename T, int D, int G, int W>
 int attn_occupancy_variant(const Shape& s, int stages, int bps) {
-  const size_t smem = AttnGeom<T, D, G>::smem_bytes(stages, s.payload, bps);
-  if (cudaFuncSetAttribute(attn_split_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const size_t smem = AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps);
+  static std::atomic<int> lim[64];
+  if (raise_smem_limit((const void*)attn_split_kernel<T, D, G, W>, smem, lim) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<T, D, G>, 128, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_split_kernel<T, D, G, W>, 32 * W, smem) !=
       cudaSuccess)
     return 0;
   return n;
 }
 
-template <typename T, int D>
+template <typename T, int D, int W>
 int attn_occupancy_dispatch_g(const Shape& s, int stages, int bps) {
   switch (s.G) {
-    case 1: return attn_occupancy_variant<T, D, 1>(s, stages, bps);
-    case 2: return attn_occupancy_variant<T, D, 2>(s, stages, bps);
-    case 3: return attn_occupancy_variant<T, D, 3>(s, stages, bps);
-    case 4: return attn_occupancy_variant<T, D, 4>(s, stages, bps);
-    case 6: return attn_occupancy_variant<T, D, 6>(s, stages, bps);
-    case 8: return attn_occupancy_variant<T, D, 8>(s, stages, bps);
+    case 1: return attn_occupancy_variant<T, D, 1, W>(s, stages, bps);
+    case 2: return attn_occupancy_variant<T, D, 2, W>(s, stages, bps);
+    case 3: return attn_occupancy_variant<T, D, 3, W>(s, stages, bps);
+    case 4: return attn_occupancy_variant<T, D, 4, W>(s, stages, bps);
+    case 6: return attn_occupancy_variant<T, D, 6, W>(s, stages, bps);
+    case 8: return attn_occupancy_variant<T, D, 8, W>(s, stages, bps);
     default: return 0;
   }
 }
 
 template <typename T, int D>
+int attn_occupancy_dispatch_w(const Shape& s, int stages, int bps, int warps) {
+  return warps == 8 ? attn_occupancy_dispatch_g<T, D, 8>(s, stages, bps)
+                    : attn_occupancy_dispatch_g<T, D, 4>(s, stages, bps);
+}
+
+template <typename T, int D, int W>
 cudaError_t launch_attn_dispatch_g(const Shape& s, const AttnArgs& a, int stages, int bps,
                                    cudaStream_t stream) {
   switch (s.G) {
-    case 1: return launch_attn_variant<T, D, 1>(s, a, stages, bps, stream);
-    case 2: return launch_attn_variant<T, D, 2>(s, a, stages, bps, stream);
-    case 3: return launch_attn_variant<T, D, 3>(s, a, stages, bps, stream);
-    case 4: return launch_attn_variant<T, D, 4>(s, a, stages, bps, stream);
-    case 6: return launch_attn_variant<T, D, 6>(s, a, stages, bps, stream);
-    case 8: return launch_attn_variant<T, D, 8>(s, a, stages, bps, stream);
+    case 1: return launch_attn_variant<T, D, 1, W>(s, a, stages, bps, stream);
+    case 2: return launch_attn_variant<T, D, 2, W>(s, a, stages, bps, stream);
+    case 3: return launch_attn_variant<T, D, 3, W>(s, a, stages, bps, stream);
+    case 4: return launch_attn_variant<T, D, 4, W>(s, a, stages, bps, stream);
+    case 6: return launch_attn_variant<T, D, 6, W>(s, a, stages, bps, stream);
+    case 8: return launch_attn_variant<T, D, 8, W>(s, a, stages, bps, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
+template <typename T, int D>
+cudaError_t launch_attn_dispatch_w(const Shape& s, const AttnArgs& a, int stages, int bps,
+                                   int warps, cudaStream_t stream) {
+  return warps == 8 ? launch_attn_dispatch_g<T, D, 8>(s, a, stages, bps, stream)
+                    : launch_attn_dispatch_g<T, D, 4>(s, a, stages, bps, stream);
+}
+
 cudaError_t launch_attention_f32(const Shape& s, const AttnArgs& a, int stages, int bps,
-                                 cudaStream_t stream);
-int attention_occupancy_f32(const Shape& s, int stages, int bps);
-int attention_occupancy_bf16(const Shape& s, int stages, int bps);
+                                 int warps, cudaStream_t stream);
 cudaError_t launch_attention_bf16(const Shape& s, const AttnArgs& a, int stages, int bps,
-                                  cudaStream_t stream);
+                                  int warps, cudaStream_t stream);
+int attention_occupancy_f32(const Shape& s, int stages, int bps, int warps);
+int attention_occupancy_bf16(const Shape& s, int stages, int bps, int warps);
 
 }  // namespace nosa

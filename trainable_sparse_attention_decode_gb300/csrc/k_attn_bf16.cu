@@ -3,14 +3,14 @@
 
 namespace nosa {
 cudaError_t launch_attention_bf16(const Shape& s, const AttnArgs& a, int stages, int bps,
-                                  cudaStream_t stream) {
-  if (s.d == 64) return launch_attn_dispatch_g<__nv_bfloat16, 64>(s, a, stages, bps, stream);
-  if (s.d == 128) return launch_attn_dispatch_g<__nv_bfloat16, 128>(s, a, stages, bps, stream);
+                                  int warps, cudaStream_t stream) {
+  if (s.d == 64) return launch_attn_dispatch_w<__nv_bfloat16, 64>(s, a, stages, bps, warps, stream);
+  if (s.d == 128) return launch_attn_dispatch_w<__nv_bfloat16, 128>(s, a, stages, bps, warps, stream);
   return cudaErrorInvalidValue;
 }
-int attention_occupancy_bf16(const Shape& s, int stages, int bps) {
-  if (s.d == 64) return attn_occupancy_dispatch_g<__nv_bfloat16, 64>(s, stages, bps);
-  if (s.d == 128) return attn_occupancy_dispatch_g<__nv_bfloat16, 128>(s, stages, bps);
+int attention_occupancy_bf16(const Shape& s, int stages, int bps, int warps) {
+  if (s.d == 64) return attn_occupancy_dispatch_w<__nv_bfloat16, 64>(s, stages, bps, warps);
+  if (s.d == 128) return attn_occupancy_dispatch_w<__nv_bfloat16, 128>(s, stages, bps, warps);
   return 0;
 }
 }  // namespace nosa

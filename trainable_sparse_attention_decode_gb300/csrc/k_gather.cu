@@ -16,11 +16,13 @@ namespace {
 constexpr int kGatherThreads = 256;
 constexpr int kGatherVPT = 9;  // 16-byte vectors per thread per pass
 
-__global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State st) {
-  const int n = *st.work_count;
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State st, int ubase,
+                                                                int chunk) {
+  const int n = st.work_count[chunk];
+  const int32_t* work = st.work + (long long)ubase * s.k;  // this chunk's list
   const int vpp = (int)(s.payload / 16);
   for (int w = blockIdx.x; w < n; w += gridDim.x) {
-    const int entry = st.work[w];
+    const int entry = work[w];
     const int u = entry / s.k;
     const int blk = st.loads[3 * entry], slot = st.loads[3 * entry + 1];
     const int src = st.loads[3 * entry + 2];
@@ -46,8 +48,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State s
 
 }  // namespace
 
-cudaError_t launch_gather(const Shape& s, const State& st, int grid, cudaStream_t stream) {
-  gather_kernel<<<grid, kGatherThreads, 0, stream>>>(s, st);
+cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
+                          cudaStream_t stream) {
+  gather_kernel<<<grid, kGatherThreads, 0, stream>>>(s, st, ubase, chunk);
   return cudaGetLastError();
 }
 

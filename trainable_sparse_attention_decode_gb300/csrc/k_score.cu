@@ -22,10 +22,10 @@ constexpr int kScoreBPC = kScoreWarps * kScoreBPW;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* __restrict__ q,
-                                                    int n_cand, float inv_sqrt_d) {
+                                                    int n_cand, float inv_sqrt_d, int ubase) {
   constexpr int M = D / 32;  // float4 per lane per pooled row
   __shared__ __align__(16) float qbar[D];
-  const int u = blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
+  const int u = ubase + blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
   const T* qg = q + ((long long)b * s.Hq + (long long)h * s.G) * D;
   const float inv_g = 1.0f / (float)s.G;
   for (int dim = threadIdx.x; dim < D; dim += blockDim.x) {
@@ -74,19 +74,19 @@ __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* 
 
 }  // namespace
 
-cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand,
-                         cudaStream_t stream) {
-  if (n_cand <= 0) return cudaSuccess;
-  dim3 grid((n_cand + kScoreBPC - 1) / kScoreBPC, s.U);
+cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
+                         int ucount, cudaStream_t stream) {
+  if (n_cand <= 0 || ucount <= 0) return cudaSuccess;
+  dim3 grid((n_cand + kScoreBPC - 1) / kScoreBPC, ucount);
   const float isd = (float)(1.0 / sqrt((double)s.d));
   if (s.dtype == 0) {
-    if (s.d == 64) score_kernel<float, 64><<<grid, 256, 0, stream>>>(s, st, (const float*)q, n_cand, isd);
-    else score_kernel<float, 128><<<grid, 256, 0, stream>>>(s, st, (const float*)q, n_cand, isd);
+    if (s.d == 64) score_kernel<float, 64><<<grid, 256, 0, stream>>>(s, st, (const float*)q, n_cand, isd, ubase);
+    else score_kernel<float, 128><<<grid, 256, 0, stream>>>(s, st, (const float*)q, n_cand, isd, ubase);
   } else {
     if (s.d == 64)
-      score_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(s, st, (const __nv_bfloat16*)q, n_cand, isd);
+      score_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(s, st, (const __nv_bfloat16*)q, n_cand, isd, ubase);
     else
-      score_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(s, st, (const __nv_bfloat16*)q, n_cand, isd);
+      score_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(s, st, (const __nv_bfloat16*)q, n_cand, isd, ubase);
   }
   return cudaGetLastError();
 }

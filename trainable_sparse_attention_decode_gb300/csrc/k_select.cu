@@ -179,19 +179,20 @@ __device__ void near_tie_stat(const uint32_t* key, const uint8_t* flag, uint8_t 
 
 template <int NT>
 __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
-                              int cold);
+                              int cold, int ubase, int chunk);
 
 // grid = U, block = 256. Dynamic shared memory: key [maxBlk] u32 + flag [maxBlk] u8.
 // flag bits: 1 = eligible, 2 = in Gamma_e, 4 = in Gamma_q. The set-difference
 // against the unit's slots runs in the same CTA once Gamma is known.
 __global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, State st, int n,
                                                                      int just_completed,
-                                                                     int cold) {
+                                                                     int cold, int ubase,
+                                                                     int chunk) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ SelShared sh;
   uint32_t* key = reinterpret_cast<uint32_t*>(dyn);
   uint8_t* flag = dyn + (size_t)s.maxBlk * 4;
-  const int u = blockIdx.x;
+  const int u = ubase + blockIdx.x;
   const float* se = st.se + (long long)u * s.maxBlk;
   const float* sq = st.sq + (long long)u * s.maxBlk;
   uint32_t* elig = st.elig + (long long)u * s.W;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, St
     st.nsel[2 * u + 1] = need_q;
   }
   __syncthreads();  // selmask and nsel of this unit are visible to the whole CTA
-  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold);
+  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, ubase, chunk);
 }
 
 // Set-difference of the unit's Gamma (selmask) against its slots. Writes the
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, St
 // work list entries.
 template <int NT>
 __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
-                              int cold) {
+                              int cold, int ubase, int chunk) {
   constexpr int kDiffThreads = NT;
   constexpr int kDiffWarps = NT / 32;
   __shared__ int load_blk[kMaxK];
@@ -310,7 +311,7 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
   for (int w = threadIdx.x; w < s.W; w += kDiffThreads) resm[w] = (w < nw) ? selm[w] : 0u;
   if (threadIdx.x == 0) {
     st.nload[u] = nload;
-    s_base = atomicAdd(st.work_count, nload);
+    s_base = atomicAdd(&st.work_count[chunk], nload);
   }
   __syncthreads();
   // Attention tables: slots kept from the previous step (usable while the gather
@@ -327,7 +328,8 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
       tnew[j] = -1;
     }
   }
-  for (int j = threadIdx.x; j < nload; j += kDiffThreads) st.work[s_base + j] = u * s.k + j;
+  int32_t* work = st.work + (long long)ubase * s.k;  // this chunk's list
+  for (int j = threadIdx.x; j < nload; j += kDiffThreads) work[s_base + j] = u * s.k + j;
 
   if (threadIdx.x == 0) {
     const int n_tail = s_tail_loaded;
@@ -351,12 +353,14 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
 }  // namespace
 
 cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
-                                  int just_completed, int cold, cudaStream_t stream) {
+                                  int just_completed, int cold, int ubase, int ucount, int chunk,
+                                  cudaStream_t stream) {
   const size_t smem = (size_t)s.maxBlk * 5;
-  cudaError_t err = cudaFuncSetAttribute(select_setdiff_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<int> lim[64];
+  cudaError_t err = raise_smem_limit((const void*)select_setdiff_kernel, smem, lim);
   if (err != cudaSuccess) return err;
-  select_setdiff_kernel<<<s.U, kSelThreads, smem, stream>>>(s, st, n_cand, just_completed, cold);
+  select_setdiff_kernel<<<ucount, kSelThreads, smem, stream>>>(s, st, n_cand, just_completed,
+                                                                cold, ubase, chunk);
   return cudaGetLastError();
 }
 

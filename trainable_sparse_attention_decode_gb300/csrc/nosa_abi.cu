@@ -7,7 +7,10 @@
 #include "k_attn.cuh"
 
 #include <algorithm>
+#include <array>
 #include <climits>
+#include <map>
+#include <mutex>
 #include <cstdlib>
 #include <cmath>
 #include <cstdio>
@@ -104,6 +107,15 @@ Shape shape_of(const nosa_config& c) {
 
 int attn_stages(long long payload) { return payload > 20000 ? 3 : 4; }
 
+// Warps per attention CTA (4 or 8; NOSA_ATTN_WARPS overrides, read once).
+int attn_warps() {
+  static const int w = [] {
+    const char* g = std::getenv("NOSA_ATTN_WARPS");
+    return (g && std::atoi(g) == 8) ? 8 : 4;
+  }();
+  return w;
+}
+
 int sm_count_current() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -134,12 +146,33 @@ size_t attention_workspace_bytes(const Shape& s, int nsplit) {
 
 // Splits per unit: the smallest count whose CTA total fills the GPU's resident
 // CTA slots in whole waves within 2% of the best, with >= 2 blocks per split.
+int attention_pick_nsplit_uncached(const Shape& s, int n_blocks);
+
+// The pick depends only on the shape and the device; it is cached (the
+// occupancy query behind it costs a driver call).
 int attention_pick_nsplit(const Shape& s, int n_blocks, int /*has_tail*/) {
+  static std::mutex mu;
+  static std::map<std::array<long long, 7>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const std::array<long long, 7> key = {dev, s.dtype, s.d, s.G, s.U, n_blocks, attn_warps()};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const int ns = attention_pick_nsplit_uncached(s, n_blocks);
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = ns;
+  return ns;
+}
+
+int attention_pick_nsplit_uncached(const Shape& s, int n_blocks) {
   const int nv = n_blocks + 1;
   const int stages = attn_stages(s.payload);
   const int bps_est = std::min(nv, 64);
-  int occ = s.dtype == 0 ? attention_occupancy_f32(s, stages, bps_est)
-                         : attention_occupancy_bf16(s, stages, bps_est);
+  int occ = s.dtype == 0 ? attention_occupancy_f32(s, stages, bps_est, attn_warps())
+                         : attention_occupancy_bf16(s, stages, bps_est, attn_warps());
   if (occ < 1) occ = 1;
   const double slots = (double)sm_count_current() * occ;
   int best = 1;
@@ -163,8 +196,8 @@ cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t str
   const int stages = attn_stages(s.payload);
   const int nv = a.n_blocks + (a.tail ? 1 : 0);
   const int bps = std::max(1, (nv + a.nsplit - 1) / a.nsplit);
-  return s.dtype == 0 ? launch_attention_f32(s, a, stages, bps, stream)
-                      : launch_attention_bf16(s, a, stages, bps, stream);
+  return s.dtype == 0 ? launch_attention_f32(s, a, stages, bps, attn_warps(), stream)
+                      : launch_attention_bf16(s, a, stages, bps, attn_warps(), stream);
 }
 
 }  // namespace nosa
@@ -187,14 +220,21 @@ struct nosa_handle {
   bool broken = false;
   std::string err;
   cudaStream_t last_stream = nullptr;
-  cudaStream_t side = nullptr;  // high-priority stream of the gather
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // Internal streams of the pipelined step: selection chain (medium priority),
+  // gather (highest), attention over kept slots (lowest), attention over filled
+  // slots (medium); events order them per unit chunk.
+  cudaStream_t s_sel = nullptr, s_gat = nullptr, s_att = nullptr, s_new = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_att = nullptr, ev_new = nullptr;
+  cudaEvent_t ev_sel[kMaxChunks] = {}, ev_gat[kMaxChunks] = {};
+  int nchunks = 1;
+  int cu_base[kMaxChunks] = {}, cu_count[kMaxChunks] = {}, nsplit_c[kMaxChunks] = {};
   bool timing = false;
   cudaEvent_t ev[kRing][kNumEv];
   bool pending[kRing];
   int ring_pos = 0;
   double t_us[8];
   long long t_count = 0;
+  long long launches = 0;  // kernels launched by decode steps
 
   nosa_status fail(nosa_status code, const std::string& msg) {
     err = msg;
@@ -228,23 +268,26 @@ void free_all(nosa_handle* h) {
       for (int i = 0; i < kNumEv; ++i) cudaEventDestroy(h->ev[r][i]);
     h->timing = false;
   }
-  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-  if (h->ev_join) cudaEventDestroy(h->ev_join);
-  if (h->side) cudaStreamDestroy(h->side);
-  h->ev_fork = h->ev_join = nullptr;
-  h->side = nullptr;
+  for (cudaEvent_t* e : {&h->ev_in, &h->ev_att, &h->ev_new})
+    if (*e) cudaEventDestroy(*e), *e = nullptr;
+  for (int c = 0; c < kMaxChunks; ++c) {
+    if (h->ev_sel[c]) cudaEventDestroy(h->ev_sel[c]), h->ev_sel[c] = nullptr;
+    if (h->ev_gat[c]) cudaEventDestroy(h->ev_gat[c]), h->ev_gat[c] = nullptr;
+  }
+  for (cudaStream_t* t : {&h->s_sel, &h->s_gat, &h->s_att, &h->s_new})
+    if (*t) cudaStreamDestroy(*t), *t = nullptr;
 }
 
-// Events of one step: e0 start, e1 after append, e2 after score, e3 after
-// select + set-difference (main stream); e4, e5 around the gather (side
-// stream); e6 after attention over kept slots, e7 after attention over loaded
-// slots and the merge (main stream).
+// Events of one step: e0 start (caller's stream); e1 after the append and e2
+// after the last chunk's select + set-difference (selection stream); e4 before
+// the first and e5 after the last chunk's gather (gather stream); e3 before the
+// first and e6 after the last attention over kept slots (attention stream); e7
+// after the join (caller's stream).
 void harvest(nosa_handle* h, int r) {
   if (!h->pending[r]) return;
   cudaEvent_t* e = h->ev[r];
   if (cudaEventSynchronize(e[7]) != cudaSuccess) return;
-  const int pairs[7][3] = {{0, 0, 1}, {1, 1, 2}, {2, 2, 3}, {3, 3, 6}, {4, 4, 5}, {5, 6, 7},
-                           {7, 0, 7}};
+  const int pairs[6][3] = {{0, 0, 1}, {1, 1, 2}, {3, 3, 6}, {4, 4, 5}, {5, 6, 7}, {7, 0, 7}};
   for (const auto& pr : pairs) {
     float ms;
     if (cudaEventElapsedTime(&ms, e[pr[1]], e[pr[2]]) == cudaSuccess) h->t_us[pr[0]] += ms * 1000.0;
@@ -325,7 +368,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.loads, U * k * 3 * 4);
   A(&st.nload, U * 4);
   A(&st.work, U * k * 4);
-  A(&st.work_count, 16);
+  A(&st.work_count, kMaxChunks * 4);
   A(&st.block_tab, U * k * 4);
   A(&st.tab_new, U * k * 4);
   A(&st.att_cnt, U * 4);
@@ -354,7 +397,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(st.slot2blk, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.loads, 0, U * k * 3 * 4);
   if (e == cudaSuccess) e = cudaMemset(st.nload, 0, U * 4);
-  if (e == cudaSuccess) e = cudaMemset(st.work_count, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(st.work_count, 0, kMaxChunks * 4);
   if (e == cudaSuccess) e = cudaMemset(st.block_tab, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.tab_new, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.att_cnt, 0, U * 4);
@@ -386,10 +429,10 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     return NOSA_ERR_CUDA;
   }
   st.host = static_cast<uint8_t*>(dp);
-  // The gather shares the GPU with attention over the kept slots: one CTA per
-  // SM keeps enough host reads in flight for the link without taking the SMs'
-  // thread slots (NOSA_GATHER_CTAS overrides the grid, for tuning).
-  h->gather_grid = sm_count_current();
+  // The gather shares the GPU with scoring and attention: 64 CTAs keep enough
+  // host reads in flight for the link without flooding the memory system with
+  // slow requests (NOSA_GATHER_CTAS overrides the grid, for tuning).
+  h->gather_grid = 64;
   if (const char* g = std::getenv("NOSA_GATHER_CTAS")) {
     const int v = std::atoi(g);
     if (v > 0) h->gather_grid = v;
@@ -398,11 +441,34 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     const int v = std::atoi(g);
     if (v > 0 && v <= kMaxSplits) h->nsplit_new = v;
   }
+  // Unit chunks of the pipelined step (NOSA_UNIT_CHUNKS overrides the count).
+  int nchunks = 2;
+  if (const char* g = std::getenv("NOSA_UNIT_CHUNKS")) {
+    const int v = std::atoi(g);
+    if (v > 0) nchunks = v;
+  }
+  nchunks = std::max(1, std::min(std::min(nchunks, kMaxChunks), s.U));
+  h->nchunks = nchunks;
+  for (int c = 0; c < nchunks; ++c) {
+    h->cu_base[c] = (int)((long long)s.U * c / nchunks);
+    h->cu_count[c] = (int)((long long)s.U * (c + 1) / nchunks) - h->cu_base[c];
+    Shape sc = s;
+    sc.U = h->cu_count[c];
+    h->nsplit_c[c] = attention_pick_nsplit(sc, s.k, 1);
+  }
   int prio_lo = 0, prio_hi = 0;
   cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
-  e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, prio_hi);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  const int prio_mid = (prio_lo + prio_hi) / 2;
+  e = cudaStreamCreateWithPriority(&h->s_gat, cudaStreamNonBlocking, prio_hi);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sel, cudaStreamNonBlocking, prio_mid);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_new, cudaStreamNonBlocking, prio_mid);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_att, cudaStreamNonBlocking, prio_lo);
+  for (cudaEvent_t* ep : {&h->ev_in, &h->ev_att, &h->ev_new})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ep, cudaEventDisableTiming);
+  for (int c = 0; c < kMaxChunks && e == cudaSuccess; ++c) {
+    e = cudaEventCreateWithFlags(&h->ev_sel[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_gat[c], cudaEventDisableTiming);
+  }
   if (e != cudaSuccess) {
     g_thread_err = std::string("stream/event creation failed: ") + cudaGetErrorString(e);
     free_all(h);
@@ -468,24 +534,25 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
   const int N = L_old / sh.B;                       // candidates after the append
   const int T = L_old + 1 - N * sh.B;               // tokens in the tail block
   const int jc = (L_old % sh.B == 0) ? N - 1 : -1;  // block that just became a candidate
-  cudaError_t err = launch_append_step(sh, st, k_new, v_new, e_new, L_old, s);
-  if (ev) cudaEventRecord(ev[1], s);
-  if (err == cudaSuccess) err = launch_score(sh, st, q, N, s);
-  if (ev) cudaEventRecord(ev[2], s);
   const bool cold = (h->steps == 0);
-  if (err == cudaSuccess) err = launch_select_setdiff(sh, st, N, jc, cold ? 1 : 0, s);
-  if (ev) cudaEventRecord(ev[3], s);
-  // Fork: the gather fills this step's free slots on the side stream while the
-  // main stream attends over the slots kept from the previous step (and the
-  // tail); then the main stream joins and attends over the filled slots.
-  if (err == cudaSuccess) err = cudaEventRecord(h->ev_fork, s);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
-  if (ev) cudaEventRecord(ev[4], h->side);
-  if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->side);
-  if (ev) cudaEventRecord(ev[5], h->side);
-  if (err == cudaSuccess) err = cudaEventRecord(h->ev_join, h->side);
-  const int ns_kept = h->nsplit;
-  const int ns_new = cold ? h->nsplit : h->nsplit_new;
+  // The units are processed in chunks that form a pipeline over four internal
+  // streams: scoring and selection of chunk c+1 (HBM) run while chunk c's
+  // gather (host link) and its attention over kept slots (HBM) run; attention
+  // over the filled slots of chunk c follows its gather. The caller's stream
+  // forks at the start and joins at the end.
+  h->launches += 1 + h->nchunks * ((N > 0 ? 1 : 0) + 4);  // append; per chunk score, select, gather, 2 x attention
+  cudaError_t err = cudaEventRecord(h->ev_in, s);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sel, h->ev_in, 0);
+  if (err == cudaSuccess) err = launch_append_step(sh, st, k_new, v_new, e_new, L_old, h->s_sel);
+  if (ev) cudaEventRecord(ev[1], h->s_sel);
+  for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
+    err = launch_score(sh, st, q, N, h->cu_base[c], h->cu_count[c], h->s_sel);
+    if (err == cudaSuccess)
+      err = launch_select_setdiff(sh, st, N, jc, cold ? 1 : 0, h->cu_base[c], h->cu_count[c], c,
+                                  h->s_sel);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_sel[c], h->s_sel);
+  }
+  if (ev) cudaEventRecord(ev[2], h->s_sel);
   AttnArgs a;
   a.units = st.slots;
   a.n_units = (long long)sh.U * sh.k;
@@ -497,25 +564,45 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
   a.lse = lse;
   a.part_acc = st.part_acc;
   a.part_ml = st.part_ml;
-  a.nsplit_total = ns_kept + ns_new;
   a.counters = st.att_cnt;
   a.err = &st.stats->error;
-  if (err == cudaSuccess) {
-    a.block_tab = st.block_tab;
-    a.tail = st.tail + (long long)(N & 1) * sh.payload;
-    a.nsplit = ns_kept;
-    a.split_base = 0;
-    err = launch_attention(sh, a, s);
+  for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
+    const int ns_kept = h->nsplit_c[c];
+    const int ns_new = cold ? ns_kept : h->nsplit_new;
+    a.nsplit_total = ns_kept + ns_new;
+    a.unit_base = h->cu_base[c];
+    a.unit_count = h->cu_count[c];
+    // gather of chunk c (host link)
+    err = cudaStreamWaitEvent(h->s_gat, h->ev_sel[c], 0);
+    if (ev && c == 0) cudaEventRecord(ev[4], h->s_gat);
+    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], c, h->s_gat);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], h->s_gat);
+    if (ev && c == h->nchunks - 1) cudaEventRecord(ev[5], h->s_gat);
+    // attention over the slots kept from the previous step, plus the tail
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_att, h->ev_sel[c], 0);
+    if (ev && c == 0) cudaEventRecord(ev[3], h->s_att);
+    if (err == cudaSuccess) {
+      a.block_tab = st.block_tab;
+      a.tail = st.tail + (long long)(N & 1) * sh.payload;
+      a.nsplit = ns_kept;
+      a.split_base = 0;
+      err = launch_attention(sh, a, h->s_att);
+    }
+    // attention over the slots this chunk's gather filled
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_new, h->ev_gat[c], 0);
+    if (err == cudaSuccess) {
+      a.block_tab = st.tab_new;
+      a.tail = nullptr;
+      a.nsplit = ns_new;
+      a.split_base = ns_kept;
+      err = launch_attention(sh, a, h->s_new);
+    }
   }
-  if (ev) cudaEventRecord(ev[6], s);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(s, h->ev_join, 0);
-  if (err == cudaSuccess) {
-    a.block_tab = st.tab_new;
-    a.tail = nullptr;
-    a.nsplit = ns_new;
-    a.split_base = ns_kept;
-    err = launch_attention(sh, a, s);
-  }
+  if (ev) cudaEventRecord(ev[6], h->s_att);
+  if (err == cudaSuccess) err = cudaEventRecord(h->ev_att, h->s_att);
+  if (err == cudaSuccess) err = cudaEventRecord(h->ev_new, h->s_new);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(s, h->ev_att, 0);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(s, h->ev_new, 0);
   if (ev) cudaEventRecord(ev[7], s);
   if (err != cudaSuccess) return h->cuda_fail(err, "decode step launch");
   h->L += 1;
@@ -551,6 +638,7 @@ nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out) {
   out->device_error = ds.error;
   for (int i = 0; i < 8; ++i) out->t_us[i] = h->t_us[i];
   out->t_count = h->t_count;
+  out->launches = h->launches;
   return NOSA_OK;
 }
 
@@ -570,6 +658,7 @@ nosa_status nosa_stats_reset(nosa_handle* h) {
   if (e != cudaSuccess) return h->cuda_fail(e, "stats reset");
   std::memset(h->t_us, 0, sizeof(h->t_us));
   h->t_count = 0;
+  h->launches = 0;
   return NOSA_OK;
 }
 
@@ -690,6 +779,8 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
   a.nsplit = nsplit;
   a.split_base = 0;
   a.nsplit_total = nsplit;
+  a.unit_base = 0;
+  a.unit_count = s.U;
   a.counters = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes);
   a.err = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes + cnt_bytes);
   // counters and error word start at zero (one memset over both)

@@ -11,9 +11,12 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+
 namespace nosa {
 
 constexpr int kMaxK = 256;         // selected blocks per unit
+constexpr int kMaxChunks = 16;     // unit chunks of a pipelined decode step
 constexpr int kMaxBlocks = 65535;  // capacity in blocks per unit
 
 // Shape of a handle (all host-derived, passed by value to kernels).
@@ -54,7 +57,7 @@ struct State {
   int32_t* loads;      // [U][k][3]         (block, slot, src)
   int32_t* nload;      // [U]
   int32_t* work;       // [U*k]             gather work list (entry = u*k + j)
-  int32_t* work_count; // [1]
+  int32_t* work_count; // [kMaxChunks]     entries per chunk (chunk c's list starts at c's first unit * k)
   int32_t* block_tab;  // [U][k]            slots kept from the previous step (slot pool index), -1 none
   int32_t* tab_new;    // [U][k]            slots filled by this step's loads, -1 none
   int32_t* att_cnt;    // [U]               split CTAs finished (the last one merges; self-resetting)
@@ -72,11 +75,14 @@ cudaError_t launch_append_step(const Shape& s, const State& st, const void* k_ne
 cudaError_t launch_promote_tail(const Shape& s, const State& st, int blk, cudaStream_t stream);
 cudaError_t launch_append_bulk(const Shape& s, const State& st, const void* k, const void* v,
                                const float* e, int L_old, int n, cudaStream_t stream);
-cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand,
-                         cudaStream_t stream);
+// The per-unit kernels below handle units [ubase, ubase + ucount) of one chunk.
+cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
+                         int ucount, cudaStream_t stream);
 cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
-                                  int just_completed, int cold, cudaStream_t stream);
-cudaError_t launch_gather(const Shape& s, const State& st, int grid, cudaStream_t stream);
+                                  int just_completed, int cold, int ubase, int ucount, int chunk,
+                                  cudaStream_t stream);
+cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
+                          cudaStream_t stream);
 
 // Split-K attention over block units. block_tab [U][n_blocks] holds unit indices
 // into `units` (-1 skip). The tail unit of unit u is at tail + u * tail_stride.
@@ -99,6 +105,8 @@ struct AttnArgs {
   int nsplit;
   int split_base;
   int nsplit_total;
+  int unit_base;            // this launch covers units [unit_base, unit_base + unit_count)
+  int unit_count;
   int* counters;            // [U]
   int* err;                 // device error word
 };
@@ -106,6 +114,19 @@ size_t attention_workspace_bytes(const Shape& s, int nsplit);
 int attention_pick_nsplit(const Shape& s, int n_blocks, int has_tail);
 cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t stream);
 bool attention_supported(int dtype, int d, int G);
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device, calling the driver only when the limit must grow (the caller
+// passes one cache array of 64 per kernel).
+inline cudaError_t raise_smem_limit(const void* func, size_t bytes, std::atomic<int>* cache) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cache[dev].load(std::memory_order_relaxed) >= (int)bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev < 64) cache[dev].store((int)bytes, std::memory_order_relaxed);
+  return e;
+}
 
 // ---------------------------------------------------------------------------
 // Device helpers
