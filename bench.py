@@ -264,7 +264,8 @@ def run_gpu(args, rank, world, local_rank):
     total_steps = W + K + KE
     w = w0.with_(steps=total_steps)
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
-                           w.max_context, device=local_rank, flags=nosa.NOSA_FLAG_TIMING)
+                           w.max_context, device=local_rank,
+                           flags=0 if args.no_timing else nosa.NOSA_FLAG_TIMING)
     h = nosa.nosa_create(cfg)
     # prompt, appended in chunks generated on the device
     chunk = 4096
@@ -290,6 +291,10 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     nosa.nosa_stats_reset(h)
 
+    # raw pointers for the timed loop (shapes were checked by the warm-up calls)
+    ptrs = [(q_all[s].data_ptr(), k_all[s].data_ptr(), v_all[s].data_ptr(), e_all[s].data_ptr())
+            for s in range(total_steps)]
+    out_p, lse_p, stream_p = out.data_ptr(), lse.data_ptr(), stream.cuda_stream
     sampler = ClockSampler(gpu_index(local_rank)) if rank == 0 else None
     time.sleep(0.15 if sampler else 0)
     barrier(world)
@@ -300,7 +305,8 @@ def run_gpu(args, rank, world, local_rank):
     ev0.record(stream)
     h0 = time.perf_counter()
     for s in range(W, W + K):
-        nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
+        nosa.nosa_decode_step(h, ptrs[s][0], ptrs[s][1], ptrs[s][2], ptrs[s][3], out_p, lse_p,
+                              stream_p)
     host_enqueue_us = (time.perf_counter() - h0) / K * 1e6
     ev1.record(stream)
     torch.cuda.nvtx.range_pop()
@@ -371,8 +377,10 @@ def run_gpu(args, rank, world, local_rank):
     attn_kept_bytes = attn_bytes - w.units * loads_per_unit * per_block
     score_bytes = score_bytes_per_launch(w, n_cand)
     peak, peak_kind = measured_peaks()
-    attn_gbs = attn_kept_bytes / (phase_us["attention_kept"] * 1e-6) / 1e9
-    score_gbs = score_bytes / (phase_us["score_select"] * 1e-6) / 1e9  # incl. selection
+    def rate(nbytes, us):
+        return nbytes / (us * 1e-6) / 1e9 if us > 0 else 0.0
+    attn_gbs = rate(attn_kept_bytes, phase_us["attention_kept"])
+    score_gbs = rate(score_bytes, phase_us["score_select"])  # includes the selection
     host_bytes_step = st["host_bytes"] / max(st["steps"] - W, 1) if st["steps"] > W else 0.0
     recall_gbs = (host_bytes_step / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
     # Roofline kernel: the split-K attention, timed alone on the step's shape (in the
@@ -513,6 +521,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="nosa", choices=["nosa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="time only the split-K attention on the step shape (profiling aid)")
+    ap.add_argument("--no-timing", action="store_true",
+                    help="run without the library's per-phase CUDA events")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--prompt", type=int, default=0, help="override the workload's prompt")
     args = ap.parse_args()
@@ -532,6 +544,25 @@ def main():
         line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+    if args.attention_only:
+        # Profiling aid: only the split-K attention on the workload's step shape,
+        # inside an NVTX range "attention" (for ncu --nvtx-include attention/).
+        import torch
+        import synth
+        import trainable_sparse_attention_decode_gb300 as nosa
+        torch.cuda.set_device(local_rank)
+        w = synth.WORKLOADS[args.workload]
+        if args.batch:
+            w = w.with_(batch=args.batch)
+        n_cand = w.prompt // w.block
+        torch.cuda.nvtx.range_push("attention")
+        secs, nbytes = attention_alone(nosa, torch, w, n_cand, 33, reps=args.steps)
+        torch.cuda.nvtx.range_pop()
+        peak, kind = measured_peaks()
+        print(json.dumps({"attention_alone_us": round(secs * 1e6, 2), "bytes": nbytes,
+                          "gbs": round(nbytes / secs / 1e9, 1),
+                          "frac_of_" + kind + "_peak": round(nbytes / secs / 1e9 / peak, 4)}))
         return
     line = run_gpu(args, rank, world, local_rank)
     if rank == 0:

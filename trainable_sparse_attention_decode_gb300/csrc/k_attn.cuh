@@ -157,6 +157,22 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
       if (has_tail) list[cnt] = -2;
       s_nl = cnt + (has_tail ? 1 : 0);
     }
+    __syncwarp();
+  }
+  // Thread 0 (which initialised the barriers and, with warp 0, built the list)
+  // starts the first copies before the queries are staged, so the pipeline fill
+  // overlaps the query load.
+  int issued = 0;  // meaningful in thread 0 only
+  if (tid == 0) {
+    const int pre = min(p.stages, s_nl);
+    for (int s = 0; s < pre; ++s) {
+      const int idx = list[s];
+      const uint8_t* src = idx >= 0 ? p.units + (long long)idx * payload
+                                    : p.tail + (long long)u * p.tail_stride;
+      mbar_arrive_expect_tx(&full[s], (uint32_t)payload);
+      bulk_g2s(stage_buf + (size_t)s * payload, src, (uint32_t)payload, &full[s]);
+    }
+    issued = pre;
   }
   {
     const T* qg = reinterpret_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)h * G) * D;
@@ -167,19 +183,6 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   }
   __syncthreads();
   const int nl = s_nl;
-
-  int issued = 0;  // meaningful in thread 0 only
-  if (tid == 0) {
-    const int pre = min(p.stages, nl);
-    for (int s = 0; s < pre; ++s) {
-      const int idx = list[s];
-      const uint8_t* src = idx >= 0 ? p.units + (long long)idx * payload
-                                    : p.tail + (long long)u * p.tail_stride;
-      mbar_arrive_expect_tx(&full[s], (uint32_t)payload);
-      bulk_g2s(stage_buf + (size_t)s * payload, src, (uint32_t)payload, &full[s]);
-    }
-    issued = pre;
-  }
 
   float m_run[G], l_run[G];
   float2 acc[G][CE / 2];

@@ -3,44 +3,85 @@
 // NOSA technical summary, Methodology §2 "High-Bandwidth Communication": the
 // host-to-device recall is done by custom kernels that read pinned host memory
 // through unified virtual addressing, instead of many small copy calls. Here
-// every load-list entry (block, slot, src) of every unit is one work item in a
-// flat list built by the set-difference kernel; a grid of CTAs strides over the
-// items, and each CTA copies one block unit at a time with all its threads
-// issuing up to 9 independent 16-byte loads each before storing, so that many
-// host-link transactions are in flight per SM.
+// every load-list entry (block, slot, src) of a chunk of units is one work item
+// in a flat list built by the set-difference; a small grid of CTAs strides over
+// the items, and each CTA copies one block unit at a time, every thread issuing
+// all its loads before storing, so that enough host-link transactions are in
+// flight without flooding the memory system (the gather runs next to HBM-bound
+// kernels, whose traffic queues behind slow host reads).
+//
+// Two load widths: 16-byte vectors (9 per thread per pass), or 32-byte vectors
+// (ld.global.nc.v8.b32 with a 256-byte L2 fetch hint, 5 per thread per pass),
+// which halve the number of host read requests per byte.
 #include "nosa_internal.cuh"
+
+#include <cstdlib>
 
 namespace nosa {
 namespace {
 
 constexpr int kGatherThreads = 256;
-constexpr int kGatherVPT = 9;  // 16-byte vectors per thread per pass
 
+struct alignas(32) V32 {
+  uint32_t r[8];
+};
+
+__device__ __forceinline__ V32 load_host32(const V32* p) {
+  V32 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::256B.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(v.r[0]), "=r"(v.r[1]), "=r"(v.r[2]), "=r"(v.r[3]), "=r"(v.r[4]), "=r"(v.r[5]),
+        "=r"(v.r[6]), "=r"(v.r[7])
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void store32(V32* p, const V32& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.r[0]),
+               "r"(v.r[1]), "r"(v.r[2]), "r"(v.r[3]), "r"(v.r[4]), "r"(v.r[5]), "r"(v.r[6]),
+               "r"(v.r[7])
+               : "memory");
+}
+
+template <typename V> struct Mover;
+template <> struct Mover<int4> {
+  static constexpr int kPer = 9;
+  static __device__ __forceinline__ int4 load(const int4* p) { return __ldcs(p); }
+  static __device__ __forceinline__ void store(int4* p, const int4& v) { *p = v; }
+};
+template <> struct Mover<V32> {
+  static constexpr int kPer = 5;
+  static __device__ __forceinline__ V32 load(const V32* p) { return load_host32(p); }
+  static __device__ __forceinline__ void store(V32* p, const V32& v) { store32(p, v); }
+};
+
+template <typename V>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State st, int ubase,
                                                                 int chunk) {
+  constexpr int kPer = Mover<V>::kPer;
   const int n = st.work_count[chunk];
   const int32_t* work = st.work + (long long)ubase * s.k;  // this chunk's list
-  const int vpp = (int)(s.payload / 16);
+  const int vpp = (int)(s.payload / sizeof(V));            // payload is a multiple of 256 B
   for (int w = blockIdx.x; w < n; w += gridDim.x) {
     const int entry = work[w];
     const int u = entry / s.k;
     const int blk = st.loads[3 * entry], slot = st.loads[3 * entry + 1];
     const int src = st.loads[3 * entry + 2];
-    const int4* sp = reinterpret_cast<const int4*>(
+    const V* sp = reinterpret_cast<const V*>(
         src ? st.tail + ((long long)u * 2 + (blk & 1)) * s.payload
             : st.host + ((long long)u * s.maxBlk + blk) * s.payload);
-    int4* dp = reinterpret_cast<int4*>(st.slots + ((long long)u * s.k + slot) * s.payload);
-    for (int base = 0; base < vpp; base += kGatherThreads * kGatherVPT) {
-      int4 r[kGatherVPT];
+    V* dp = reinterpret_cast<V*>(st.slots + ((long long)u * s.k + slot) * s.payload);
+    for (int base = 0; base < vpp; base += kGatherThreads * kPer) {
+      V r[kPer];
 #pragma unroll
-      for (int i = 0; i < kGatherVPT; ++i) {
+      for (int i = 0; i < kPer; ++i) {
         const int idx = base + i * kGatherThreads + threadIdx.x;
-        if (idx < vpp) r[i] = __ldcs(sp + idx);
+        if (idx < vpp) r[i] = Mover<V>::load(sp + idx);
       }
 #pragma unroll
-      for (int i = 0; i < kGatherVPT; ++i) {
+      for (int i = 0; i < kPer; ++i) {
         const int idx = base + i * kGatherThreads + threadIdx.x;
-        if (idx < vpp) dp[idx] = r[i];
+        if (idx < vpp) Mover<V>::store(dp + idx, r[i]);
       }
     }
   }
@@ -50,7 +91,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State s
 
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
                           cudaStream_t stream) {
-  gather_kernel<<<grid, kGatherThreads, 0, stream>>>(s, st, ubase, chunk);
+  static const bool wide = [] {
+    const char* g = std::getenv("NOSA_GATHER_VEC");
+    return g != nullptr && std::atoi(g) == 32;
+  }();
+  if (wide)
+    gather_kernel<V32><<<grid, kGatherThreads, 0, stream>>>(s, st, ubase, chunk);
+  else
+    gather_kernel<int4><<<grid, kGatherThreads, 0, stream>>>(s, st, ubase, chunk);
   return cudaGetLastError();
 }
 

@@ -215,7 +215,7 @@ struct nosa_handle {
   long long L = 0;
   long long steps = 0;
   int nsplit = 1;       // attention splits over the slots kept from the previous step
-  int nsplit_new = 1;   // attention splits over the slots the gather filled (warm steps)
+  int nsplit_new = 2;   // attention splits over the slots the gather filled (warm steps)
   int gather_grid = 1;
   bool broken = false;
   std::string err;
