@@ -215,10 +215,13 @@ def h2d_peak_gbs(torch, nbytes=1 << 30, reps=5):
 def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20):
     """Times the split-K attention kernel alone on the step's shape: every unit
     attends over min(k, N) full blocks plus a tail of tail_len tokens, all block
-    units fresh in HBM (more than L2, and L2 is flushed before each launch).
+    units fresh in HBM (more than L2).
     Returns (seconds per launch, algorithmic bytes per launch)."""
-    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
-                           w.max_context)
+    # the standalone call uses only the shape fields of the config (k is capped to
+    # the decode step's limit for validation; the block table sets the blocks)
+    kk = min(w.k, 256)
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, kk,
+                           min(w.k_e, kk), w.max_context)
     payload = nosa.nosa_payload_bytes(cfg)
     nb = min(w.k, n_cand)
     U = w.units
@@ -247,6 +250,45 @@ def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20):
     return a.elapsed_time(b) / 1e3 / reps, attn_bytes_per_launch(w, n_cand, tail_len)
 
 
+def run_fullattn(args, rank, world, local_rank):
+    """Comparator: dense decode attention with the whole KV cache resident in HBM
+    (no selection, no recall), on the same split-K kernel: every unit attends
+    over all N complete blocks plus the tail. One step = one attention launch
+    for the batch."""
+    import torch
+    import synth
+    import trainable_sparse_attention_decode_gb300 as nosa
+    torch.cuda.set_device(local_rank)
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(batch=args.batch)
+    n_cand = w.prompt // w.block
+    wf = w.with_(k=n_cand)               # attend to every block
+    W, K = args.warmup, args.steps
+    barrier(world)
+    secs_w, _ = attention_alone(nosa, torch, wf, n_cand, 33, reps=W)
+    barrier(world)
+    secs, nbytes = attention_alone(nosa, torch, wf, n_cand, 33, reps=K)
+    max_secs, tokens = aggregate(secs * K, w.batch * K, world)
+    if rank != 0:
+        return None
+    peak, kind = measured_peaks()
+    gbs = nbytes / secs / 1e9
+    return {"metric": METRIC, "value": round(tokens / max_secs, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(secs * 1e3, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "mode": "fullattn",
+            "config": {"workload": w.name + "-fullattn", "batch": w.batch,
+                       "context": w.prompt, "blocks_per_unit": n_cand,
+                       "kv_bytes_in_hbm": w.units * (n_cand + 1) * 33024,
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (dense)",
+                         "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None, "peak_source": kind,
+                         "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches": K}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import synth
@@ -259,6 +301,9 @@ def run_gpu(args, rank, world, local_rank):
         w0 = w0.with_(name=f"{w0.name}-b{args.batch}", batch=args.batch)
     if args.prompt:
         w0 = w0.with_(name=f"{w0.name}-p{args.prompt}", prompt=args.prompt)
+    if args.mode == "infllmv2":
+        # comparator: no query-agnostic part, every block chosen by the query
+        w0 = w0.with_(name=f"{w0.name}-ke0", k_e=0)
     W, K = args.warmup, args.steps
     KE = args.e2e_steps
     total_steps = W + K + KE
@@ -402,6 +447,7 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded counter-based generator; shapes of the workload)",
+        "mode": args.mode,
         "config": {"workload": w0.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k, "k_e": w.k_e,
                    "context_start": w.prompt, "context_end": context_after,
@@ -521,6 +567,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="nosa", choices=["nosa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="nosa", choices=["nosa", "infllmv2", "fullattn"],
+                    help="nosa (the method); comparators: infllmv2 = k_e 0 (no query-agnostic "
+                         "part), fullattn = dense attention over the whole cache in HBM")
     ap.add_argument("--attention-only", action="store_true",
                     help="time only the split-K attention on the step shape (profiling aid)")
     ap.add_argument("--no-timing", action="store_true",
@@ -563,6 +612,11 @@ def main():
         print(json.dumps({"attention_alone_us": round(secs * 1e6, 2), "bytes": nbytes,
                           "gbs": round(nbytes / secs / 1e9, 1),
                           "frac_of_" + kind + "_peak": round(nbytes / secs / 1e9 / peak, 4)}))
+        return
+    if args.mode == "fullattn":
+        line = run_fullattn(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         return
     line = run_gpu(args, rank, world, local_rank)
     if rank == 0:

@@ -105,7 +105,19 @@ Shape shape_of(const nosa_config& c) {
   return s;
 }
 
-int attn_stages(long long payload) { return payload > 20000 ? 3 : 4; }
+// Pipeline stages of the attention CTA (NOSA_ATTN_STAGES overrides, read once).
+int attn_stages(long long payload) {
+  static const int forced = [] {
+    const char* g = std::getenv("NOSA_ATTN_STAGES");
+    const int v = g ? std::atoi(g) : 0;
+    return (v >= 2 && v <= 6) ? v : 0;
+  }();
+  if (forced) return (int)std::min<long long>(forced, 200000 / payload);
+  // Measured on GB300: three resident CTAs with a 2-stage ring beat two CTAs
+  // with 3 stages (71.9% vs 63.5% of HBM peak at d = 128 bf16), so the ring is
+  // sized to leave room for three CTAs per SM.
+  return (int)std::max<long long>(2, std::min<long long>(4, 70000 / payload));
+}
 
 // Warps per attention CTA (4 or 8; NOSA_ATTN_WARPS overrides, read once).
 int attn_warps() {
