@@ -244,6 +244,18 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Self-test of the kernels' bounded waits (failure detection without a GPU
+ * fault): launches one thread that waits, with the same bounded mbarrier wait
+ * the attention kernel uses, on a barrier nothing ever completes. The wait must
+ * give up after limit_ns (0 < limit_ns <= 10 s) and report it; the context stays
+ * usable. Synchronous. *timed_out = 1 when the wait gave up, *waited_ms = the
+ * time it waited. (No counterpart in the NOSA pages: a robustness check of this
+ * implementation.)
+ */
+nosa_status nosa_selftest_bounded_wait(int32_t device, int64_t limit_ns, int32_t* timed_out,
+                                       int32_t* waited_ms);
+
+/*
  * nosa_sparse_attention without a caller workspace and without allocating.
  * (The NOSA pages have no counterpart of this call: it serves callers.)
  *

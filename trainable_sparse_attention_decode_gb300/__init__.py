@@ -22,6 +22,7 @@ __all__ = [
     "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset",
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
+    "nosa_selftest_bounded_wait",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -82,6 +83,7 @@ def _load():
                                             VP, VP, VP, SZ, VP]),
         "nosa_sparse_attention_noalloc": (C.c_int, [P(NosaConfig), VP, C.c_int64, VP, I32, VP,
                                                     I32, VP, VP, VP, VP]),
+        "nosa_selftest_bounded_wait": (C.c_int, [I32, C.c_int64, P(I32), P(I32)]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -227,6 +229,13 @@ def nosa_destroy(h):
     if h is not None and h.value:
         lib.nosa_destroy(h)
         h.value = None
+
+
+def nosa_selftest_bounded_wait(device=0, limit_ns=200_000_000):
+    """(timed_out, waited_ms) of a bounded device wait that nothing completes."""
+    t, m = C.c_int32(), C.c_int32()
+    _check(lib.nosa_selftest_bounded_wait(device, limit_ns, C.byref(t), C.byref(m)))
+    return bool(t.value), int(m.value)
 
 
 def nosa_attention_workspace_bytes(cfg: NosaConfig, n_blocks: int) -> int:

@@ -103,3 +103,31 @@ cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, 
 }
 
 }  // namespace nosa
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: one thread arms an mbarrier that nothing will
+// ever complete and waits on it with the same bounded wait the attention kernel
+// uses; the wait must give up after limit_ns and report it.
+// ---------------------------------------------------------------------------
+namespace nosa {
+namespace {
+__global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, int* result) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint64_t t0 = global_ns();
+    const bool done = mbar_wait_bounded(&bar, 0, limit_ns);
+    result[0] = done ? kDevErrNone : kDevErrWaitTimeout;
+    result[1] = (int)((global_ns() - t0) / 1000000ull);  // elapsed ms
+    mbar_arrive(&bar);  // complete the phase so the barrier is left quiescent
+  }
+}
+}  // namespace
+
+cudaError_t launch_bounded_wait_probe(unsigned long long limit_ns, int* result,
+                                      cudaStream_t stream) {
+  bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, result);
+  return cudaGetLastError();
+}
+}  // namespace nosa

@@ -806,3 +806,29 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
 }
 
 }  // extern "C"
+
+extern "C" nosa_status nosa_selftest_bounded_wait(int32_t device, int64_t limit_ns,
+                                                  int32_t* timed_out, int32_t* waited_ms) {
+  if (!timed_out || !waited_ms || limit_ns <= 0 || limit_ns > 10000000000LL) {
+    g_thread_err = "bad argument";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  DeviceGuard guard(device);
+  int* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, 2 * sizeof(int));
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("cudaMalloc: ") + cudaGetErrorString(e);
+    return NOSA_ERR_OOM;
+  }
+  int h[2] = {-1, -1};
+  e = launch_bounded_wait_probe((unsigned long long)limit_ns, d, nullptr);
+  if (e == cudaSuccess) e = cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("bounded-wait probe: ") + cudaGetErrorString(e);
+    return NOSA_ERR_CUDA;
+  }
+  *timed_out = (h[0] == kDevErrWaitTimeout) ? 1 : 0;
+  *waited_ms = h[1];
+  return NOSA_OK;
+}

@@ -83,6 +83,9 @@ cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
                                   cudaStream_t stream);
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
                           cudaStream_t stream);
+// result[0] = error code of a bounded wait that nothing completes, result[1] = ms waited.
+cudaError_t launch_bounded_wait_probe(unsigned long long limit_ns, int* result,
+                                      cudaStream_t stream);
 
 // Split-K attention over block units. block_tab [U][n_blocks] holds unit indices
 // into `units` (-1 skip). The tail unit of unit u is at tail + u * tail_stride.
