@@ -49,11 +49,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
   return off + x - v;
 }
 
+constexpr int kSmallCut = 256;  // candidates ranked directly (one per thread)
+
 struct SelShared {
   uint32_t hist[256];
   int warp_tot[kSelWarps];
-  int bcast[2];
+  int bcast[3];
   uint32_t red[3];
+  int list[kSmallCut];              // compacted candidates of a small cut
+  unsigned long long comp[kSmallCut];  // their (key, lower-index-first) composites
 };
 
 // Candidate i takes part in a cut when (flag[i] & tmask) == tval.
@@ -62,7 +66,7 @@ struct SelShared {
 // Requires 1 <= need < number of candidates.
 __device__ void radix_threshold(const uint32_t* key, const uint8_t* flag, uint8_t tmask,
                                 uint8_t tval, int n, int need, SelShared& sh, uint32_t* thr,
-                                int* take_eq) {
+                                int* take_eq, int* count_eq) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t prefix = 0, pmask = 0;
   int remaining = need;
@@ -99,6 +103,7 @@ __device__ void radix_threshold(const uint32_t* key, const uint8_t* flag, uint8_
           if (cum + cnt[j] >= remaining) {
             sh.bcast[0] = 255 - 8 * lane - j;
             sh.bcast[1] = remaining - cum;
+            sh.bcast[2] = cnt[j];
             break;
           }
           cum += cnt[j];
@@ -112,6 +117,7 @@ __device__ void radix_threshold(const uint32_t* key, const uint8_t* flag, uint8_
   }
   *thr = prefix;
   *take_eq = remaining;
+  *count_eq = sh.bcast[2];  // after the last pass: candidates whose key equals thr
 }
 
 // Marks (flag |= setbit) the `need` best candidates of a cut, ties to lower index.
@@ -125,8 +131,14 @@ __device__ void mark_top(const uint32_t* key, uint8_t* flag, uint8_t tmask, uint
     return;
   }
   uint32_t thr;
-  int take_eq;
-  radix_threshold(key, flag, tmask, tval, n, need, sh, &thr, &take_eq);
+  int take_eq, count_eq;
+  radix_threshold(key, flag, tmask, tval, n, need, sh, &thr, &take_eq, &count_eq);
+  if (take_eq == count_eq) {  // no tie at the cut to break: one pass
+    for (int i = threadIdx.x; i < n; i += kSelThreads)
+      if ((flag[i] & tmask) == tval && key[i] >= thr) flag[i] |= setbit;
+    __syncthreads();
+    return;
+  }
   int run = 0;
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + threadIdx.x;
@@ -138,6 +150,59 @@ __device__ void mark_top(const uint32_t* key, uint8_t* flag, uint8_t tmask, uint
     run += tot;
   }
   __syncthreads();
+}
+
+// Gamma_e when few blocks are eligible (the steady state: the previous Gamma_e
+// plus at most one new block): compact the eligible blocks in index order from
+// the bitmask words, give each one thread, and rank it against the others by
+// (key, lower index first); the `need` best are chosen. Also counts a near-tie
+// at the cut. Requires 1 <= need < count <= kSmallCut.
+__device__ void mark_top_small_eligible(const uint32_t* key, uint8_t* flag, const uint32_t* elig,
+                                        int n, int need, int count, SelShared& sh,
+                                        unsigned long long* near_ties) {
+  const int nw = (n + 31) >> 5;
+  int base = 0;
+  for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
+    const int w = w0 + threadIdx.x;
+    uint32_t bits = 0;
+    if (w < nw) {
+      bits = elig[w];
+      if (w == nw - 1 && (n & 31)) bits &= (1u << (n & 31)) - 1u;
+    }
+    int tot;
+    int pos = base + block_excl_scan<kSelWarps>(__popc(bits), sh.warp_tot, &tot);
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      const int i = w * 32 + b;
+      sh.list[pos] = i;
+      sh.comp[pos] = ((unsigned long long)key[i] << 32) | (0xFFFFFFFFu - (uint32_t)i);
+      ++pos;
+      bits &= bits - 1;
+    }
+    base += tot;
+  }
+  if (threadIdx.x == 0) {
+    sh.red[0] = 0xFFFFFFFFu;
+    sh.red[1] = 0u;
+    sh.red[2] = 0u;
+  }
+  __syncthreads();
+  if (threadIdx.x < count) {
+    const unsigned long long mine = sh.comp[threadIdx.x];
+    int rank = 0;
+    for (int j = 0; j < count; ++j) rank += (sh.comp[j] > mine) ? 1 : 0;
+    const int i = sh.list[threadIdx.x];
+    const uint32_t kk = key[i];
+    if (rank < need) flag[i] |= 2;
+    if (rank == need - 1) sh.red[0] = kk;  // weakest chosen
+    if (rank == need) sh.red[1] = kk;      // strongest left out
+    atomicMax(&sh.red[2], __float_as_uint(fabsf(key_to_float(kk))));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float gap = key_to_float(sh.red[0]) - key_to_float(sh.red[1]);
+    if (gap < 1e-5f * __uint_as_float(sh.red[2])) atomicAdd(near_ties, 1ull);
+  }
 }
 
 // Counts a near-tie at a cut: the weakest chosen and the strongest left-out fp32
@@ -207,8 +272,13 @@ __global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, St
   int cnt_e;
   block_excl_scan<kSelWarps>(my_elig, sh.warp_tot, &cnt_e);  // also orders the writes above
   const int need_e = min(s.ke, cnt_e);
-  mark_top(key, flag, 1, 1, 2, n, need_e, cnt_e, sh);
-  if (need_e > 0 && need_e < cnt_e) near_tie_stat(key, flag, 1, 1, 2, n, sh, &st.stats->near_ties);
+  if (need_e > 0 && need_e < cnt_e && cnt_e <= kSmallCut) {
+    mark_top_small_eligible(key, flag, elig, n, need_e, cnt_e, sh, &st.stats->near_ties);
+  } else {
+    mark_top(key, flag, 1, 1, 2, n, need_e, cnt_e, sh);
+    if (need_e > 0 && need_e < cnt_e)
+      near_tie_stat(key, flag, 1, 1, 2, n, sh, &st.stats->near_ties);
+  }
 
   for (int i = threadIdx.x; i < n; i += kSelThreads) key[i] = ordered_key(sq[i]);
   __syncthreads();
@@ -223,9 +293,10 @@ __global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, St
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + threadIdx.x;
     const uint8_t f = (i < n) ? flag[i] : 0;
-    int te, tq;
-    const int xe = block_excl_scan<kSelWarps>((f & 2) ? 1 : 0, sh.warp_tot, &te);
-    const int xq = block_excl_scan<kSelWarps>((f & 4) ? 1 : 0, sh.warp_tot, &tq);
+    int tot;  // Gamma_e count in the low 16 bits, Gamma_q count in the high 16 bits
+    const int x = block_excl_scan<kSelWarps>(((f & 2) ? 1 : 0) | ((f & 4) ? 0x10000 : 0),
+                                             sh.warp_tot, &tot);
+    const int xe = x & 0xFFFF, xq = x >> 16, te = tot & 0xFFFF, tq = tot >> 16;
     if (f & 2) sel[run_e + xe] = i;
     if (f & 4) sel[need_e + run_q + xq] = i;
     run_e += te;
