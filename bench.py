@@ -154,11 +154,11 @@ def attn_bytes_per_launch(w, n_cand, tail_len):
     return w.units * (toks * per_tok + 2 * w.group * w.head_dim * elt)
 
 
-def score_bytes_per_launch(w, n_cand):
-    """Algorithmic bytes of one scoring launch: all pooled keys (fp32), the scores
-    written, and the queries."""
+def score_bytes_per_launch(w, n_cand, pk_elt=4):
+    """Algorithmic bytes of one scoring launch: all pooled keys (fp32, or bf16 in
+    the pooled-bf16 variant), the scores written, and the queries."""
     elt = 4 if w.dtype == "f32" else 2
-    return w.units * (n_cand * 4 * w.head_dim * 4 + n_cand * 4 + w.group * w.head_dim * elt)
+    return w.units * (n_cand * 4 * w.head_dim * pk_elt + n_cand * 4 + w.group * w.head_dim * elt)
 
 
 def kernel_source_hash(files):
@@ -310,7 +310,8 @@ def run_gpu(args, rank, world, local_rank):
     w = w0.with_(steps=total_steps)
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
                            w.max_context, device=local_rank,
-                           flags=0 if args.no_timing else nosa.NOSA_FLAG_TIMING)
+                           flags=(0 if args.no_timing else nosa.NOSA_FLAG_TIMING)
+                           | (nosa.NOSA_FLAG_POOLED_BF16 if args.pooled_bf16 else 0))
     h = nosa.nosa_create(cfg)
     # prompt, appended in chunks generated on the device
     chunk = 4096
@@ -420,7 +421,7 @@ def run_gpu(args, rank, world, local_rank):
     per_block = w.block * (2 * w.head_dim * elt + 4)
     attn_bytes = attn_bytes_per_launch(w, n_cand, tail_mid)
     attn_kept_bytes = attn_bytes - w.units * loads_per_unit * per_block
-    score_bytes = score_bytes_per_launch(w, n_cand)
+    score_bytes = score_bytes_per_launch(w, n_cand, 2 if args.pooled_bf16 else 4)
     peak, peak_kind = measured_peaks()
     def rate(nbytes, us):
         return nbytes / (us * 1e-6) / 1e9 if us > 0 else 0.0
@@ -447,7 +448,7 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded counter-based generator; shapes of the workload)",
-        "mode": args.mode,
+        "mode": args.mode + ("+pooled_bf16" if args.pooled_bf16 else ""),
         "config": {"workload": w0.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k, "k_e": w.k_e,
                    "context_start": w.prompt, "context_end": context_after,
@@ -572,6 +573,8 @@ def main():
                          "part), fullattn = dense attention over the whole cache in HBM")
     ap.add_argument("--attention-only", action="store_true",
                     help="time only the split-K attention on the step shape (profiling aid)")
+    ap.add_argument("--pooled-bf16", action="store_true",
+                    help="variant: pooled keys stored in bf16 (halves the scoring traffic)")
     ap.add_argument("--no-timing", action="store_true",
                     help="run without the library's per-phase CUDA events")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")

@@ -61,6 +61,11 @@ typedef enum { NOSA_F32 = 0, NOSA_BF16 = 1 } nosa_dtype;
 
 /* Flags of nosa_config.flags. */
 #define NOSA_FLAG_TIMING 1u /* record CUDA events around each phase (stats.t_us) */
+/* Store the pooled (sub-block mean) keys in bf16 instead of fp32: each mean is the
+ * fp32 sum of the sub-block's keys in token order times 1/16, rounded to nearest
+ * even in bf16. Halves the scoring traffic (the largest HBM stream of a step at
+ * long context); selections then follow the rounded pooled keys. */
+#define NOSA_FLAG_POOLED_BF16 2u
 
 /*
  * Configuration, fixed at nosa_create.
@@ -196,7 +201,7 @@ nosa_status nosa_stats_reset(nosa_handle* h);
  *   NOSA_DBG_SLOTS    int32 [U][k]   block held by each slot, -1 empty
  *   NOSA_DBG_LOADS    int32 [U][k][3] load list (block, slot, src: 0 host, 1 tail)
  *   NOSA_DBG_NLOAD    int32 [U]      loads of the last step
- *   NOSA_DBG_POOLED   fp32 [U][maxBlk][P][d] sub-block mean keys
+ *   NOSA_DBG_POOLED   fp32 (bf16 with NOSA_FLAG_POOLED_BF16) [U][maxBlk][P][d] sub-block mean keys
  *   NOSA_DBG_SE       fp32 [U][maxBlk] block eviction scores (max of sub-block means)
  *   NOSA_DBG_SQ       fp32 [U][maxBlk] query-aware block scores of the last step
  *   NOSA_DBG_SLOTPOOL bytes [U][k][payload]  slot pool

@@ -51,7 +51,7 @@ TAIL = 1
 __all__ = [
     "HOST", "TAIL", "pool_block", "group_query", "block_scores", "decision_values",
     "top_m", "dual_select", "set_difference", "attend", "encode_payload",
-    "payload_bytes", "UnitOracle",
+    "payload_bytes", "UnitOracle", "pooled_keys_bf16", "round_bf16",
 ]
 
 
@@ -72,6 +72,30 @@ def pool_block(k_blk: np.ndarray, e_blk: np.ndarray, sub_block: int):
     k_bar = k_sub.sum(axis=1) / sub_block
     e_bar = e_sub.sum(axis=1) / sub_block
     return k_bar, e_bar, float(e_bar.max())
+
+
+def round_bf16(x32: np.ndarray) -> np.ndarray:
+    """fp32 values rounded to nearest even in bf16, returned as fp64."""
+    b = np.asarray(x32, dtype=np.float32).view(np.uint32)
+    r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32).astype(np.float64)
+
+
+def pooled_keys_bf16(k_blk: np.ndarray, sub_block: int) -> np.ndarray:
+    """Sub-block mean keys of the bf16 pooled-key variant (R14 with bf16 storage).
+
+    The sum of each sub-block's keys is taken in fp32, in token order, starting
+    from 0; it is multiplied by the fp32 value of 1/S and rounded to nearest even
+    in bf16. k_blk [B][d] holds the stored keys (exact in fp32). Returns [B/S][d] fp64.
+    """
+    B, d = k_blk.shape
+    P = B // sub_block
+    k32 = np.asarray(k_blk, dtype=np.float64).astype(np.float32).reshape(P, sub_block, d)
+    acc = np.zeros((P, d), dtype=np.float32)
+    for j in range(sub_block):
+        acc = np.add(acc, k32[:, j, :], dtype=np.float32)
+    mean = np.multiply(acc, np.float32(1.0 / sub_block), dtype=np.float32)
+    return round_bf16(mean)
 
 
 def group_query(q_group: np.ndarray) -> np.ndarray:
@@ -222,10 +246,11 @@ class UnitOracle:
     """
 
     def __init__(self, head_dim: int, dtype: str, k: int, k_e: int, capacity: int,
-                 block: int = 64, sub_block: int = 16):
+                 block: int = 64, sub_block: int = 16, pooled: str = "f32"):
         if block % sub_block or k_e > k:
             raise ValueError("bad configuration")
         self.d, self.dtype, self.k, self.k_e = head_dim, dtype, k, k_e
+        self.pooled = pooled  # "f32": exact means (R14); "bf16": the bf16 pooled-key variant
         self.B, self.S = block, sub_block
         self.P = block // sub_block
         self.cap = capacity
@@ -259,8 +284,10 @@ class UnitOracle:
         if t % self.B == 0 and t > 0:
             blk = t // self.B - 1
             lo, hi = blk * self.B, (blk + 1) * self.B
-            kb, eb, sb = pool_block(_to_f64(self.k_raw[lo:hi], self.dtype),
-                                    self.e[lo:hi].astype(np.float64), self.S)
+            k_blk = _to_f64(self.k_raw[lo:hi], self.dtype)
+            kb, eb, sb = pool_block(k_blk, self.e[lo:hi].astype(np.float64), self.S)
+            if self.pooled == "bf16":
+                kb = pooled_keys_bf16(k_blk, self.S)
             self.k_bar[blk], self.e_bar[blk], self.se[blk] = kb, eb, sb
             self.elig[blk] = True
             opened = blk

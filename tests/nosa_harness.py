@@ -104,7 +104,8 @@ class GpuRun:
         self.oracles = {}
         for u in self.units:
             b, hh = divmod(u, w.n_kv_heads)
-            uo = O.UnitOracle(w.head_dim, w.dtype, w.k, w.k_e, w.max_context, w.block, w.sub_block)
+            uo = O.UnitOracle(w.head_dim, w.dtype, w.k, w.k_e, w.max_context, w.block, w.sub_block,
+                              pooled="bf16" if flags & nosa.NOSA_FLAG_POOLED_BF16 else "f32")
             uo.append(synth.keys(w, b, hh, 0, w.prompt), synth.values(w, b, hh, 0, w.prompt),
                       synth.evict(w, b, hh, 0, w.prompt))
             self.oracles[u] = uo

@@ -73,7 +73,8 @@ def _cfg(**kw):
     ({"max_context": 0}, 1),
     ({"max_context": 64 * 32768 + 1}, 7),
     ({"k": 257, "k_e": 0}, 7),
-    ({"flags": 2}, 1),
+    ({"flags": 4}, 1),                # unknown flag bit
+    ({"flags": 3}, 0),                # timing + bf16 pooled keys
 ])
 def test_config_validation(kw, status):
     st, msg = nosa.nosa_config_validate(_cfg(**kw))

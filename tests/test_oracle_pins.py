@@ -318,3 +318,29 @@ def test_cold_step_loads_everything_from_host():
     assert len(info["loads"]) == 8
     srcs = {l[0]: l[2] for l in info["loads"]}
     assert all(v == (O.TAIL if b == 11 else O.HOST) for b, v in srcs.items())
+
+
+# --------------------------------------------------------------------------
+# bf16 pooled-key variant: rounding and fp32 token-order summation
+# --------------------------------------------------------------------------
+def test_round_bf16_ties_to_even():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -8 + 2 ** -20, -3.0],
+                 dtype=np.float32)
+    assert list(O.round_bf16(x)) == [1.0, 1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -3.0]
+
+
+def test_pooled_bf16_exact_means_unchanged():
+    c = np.arange(8) * 0.25 - 1.0                      # bf16-exact values
+    kb = O.pooled_keys_bf16(np.tile(c, (64, 1)), 16)
+    assert np.array_equal(kb, np.tile(c, (4, 1)))
+
+
+def test_pooled_bf16_follows_fp32_token_order():
+    # 2**24 + 1 is not an fp32 value: summed in token order the ones vanish, so the
+    # sub-block mean is 0, not the exact 14/16.
+    k = np.zeros((64, 2))
+    k[:16, 0] = [2.0 ** 24] + [1.0] * 14 + [-(2.0 ** 24)]
+    k[:16, 1] = [1.0] * 14 + [2.0 ** 24, -(2.0 ** 24)]  # other order: exact 14/16
+    kb = O.pooled_keys_bf16(k, 16)
+    assert kb[0, 0] == 0.0 and kb[0, 1] == 0.875
+    assert O.pool_block(k, np.zeros(64), 16)[0][0, 0] == 0.875

@@ -17,9 +17,10 @@ from nosa_harness import GpuRun
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, units=None, steps=None, check_every=1, attn_every=1, pieces=None, check_bytes=True):
+def _run(w, units=None, steps=None, check_every=1, attn_every=1, pieces=None, check_bytes=True,
+         flags=0):
     steps = w.steps if steps is None else steps
-    run = GpuRun(w, units=units, prompt_pieces=pieces, check_bytes=check_bytes,
+    run = GpuRun(w, units=units, flags=flags, prompt_pieces=pieces, check_bytes=check_bytes,
                  oracle_attention_every=attn_every)
     q = synth.gpu.queries(w, steps)
     worst, worst_lse = 0.0, 0.0
@@ -80,6 +81,17 @@ def test_edge_cases_f32(case):
 def test_group_and_dtype_variants(hq, hkv, d, dtype):
     w = synth.Workload("var", 2, hq, hkv, d, dtype, 64 * 40 + 17, 40, 16, 10)
     _run(w)
+
+
+@pytest.mark.parametrize("name,units,steps", [("tiny-f32", None, 32), ("1b-bf16", [2, 50], 64),
+                                              ("8b-offload-bf16", [7, 200], 16)])
+def test_pooled_bf16_variant(name, units, steps):
+    # bf16 pooled keys: the oracle models the fp32 token-order sum and bf16 rounding
+    w = synth.WORKLOADS[name]
+    pieces = [4096] * 16 if name == "8b-offload-bf16" else None
+    st, _ = _run(w, units=units, steps=steps, pieces=pieces, flags=nosa.NOSA_FLAG_POOLED_BF16)
+    if w.prompt >= 64 * w.k:
+        assert st["gamma_min"] >= w.k_e / w.k - 1e-12
 
 
 def test_prompt_in_ragged_pieces():

@@ -17,7 +17,7 @@ import numpy as np
 
 __all__ = [
     "NosaError", "NosaConfig", "NosaStats", "lib", "lib_path",
-    "NOSA_F32", "NOSA_BF16", "NOSA_FLAG_TIMING", "DBG",
+    "NOSA_F32", "NOSA_BF16", "NOSA_FLAG_TIMING", "NOSA_FLAG_POOLED_BF16", "DBG",
     "nosa_config", "nosa_config_validate", "nosa_payload_bytes", "nosa_create",
     "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset",
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
@@ -27,6 +27,7 @@ __all__ = [
 
 NOSA_F32, NOSA_BF16 = 0, 1
 NOSA_FLAG_TIMING = 1
+NOSA_FLAG_POOLED_BF16 = 2
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "OOM", 3: "HOST_OOM", 4: "CAPACITY", 5: "CUDA",
           6: "STATE", 7: "UNSUPPORTED"}
 DBG = {name: i for i, name in enumerate(

@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st,
       for (int j = 0; j < s.S - 1; ++j)
         acc += to_f32(*reinterpret_cast<const T*>(cur + k_off(p0 + j, dim, s.B, s.elt)));
       acc += to_f32(k_new[in_row + dim]);
-      st.pk[(((long long)u * s.maxBlk + blk) * s.P + sb) * s.d + dim] = acc * (1.0f / s.S);
+      store_pooled(s, st.pk, (((long long)u * s.maxBlk + blk) * s.P + sb) * s.d + dim,
+                   acc * (1.0f / s.S));
     }
     if (threadIdx.x == 0) {
       float ea = 0.f;
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(256) append_bulk_kernel(Shape s, State st,
       float acc = 0.f;
       for (int j = 0; j < s.S; ++j)
         acc += to_f32(*reinterpret_cast<const T*>(unit_s + k_off(sb * s.S + j, dim, s.B, s.elt)));
-      st.pk[(bi * s.P + sb) * s.d + dim] = acc * (1.0f / s.S);
+      store_pooled(s, st.pk, (bi * s.P + sb) * s.d + dim, acc * (1.0f / s.S));
     }
   }
   if (threadIdx.x == 0) {

@@ -20,10 +20,24 @@ constexpr int kScoreWarps = 8;
 constexpr int kScoreBPW = 4;  // blocks per warp
 constexpr int kScoreBPC = kScoreWarps * kScoreBPW;
 
-template <typename T, int D>
+// Pooled keys are fp32 (PT = float) or bf16 (PT = __nv_bfloat16): each lane
+// loads 16-byte chunks of its row (4 fp32 or 8 bf16 values) and widens them.
+template <typename PT> __device__ __forceinline__ void widen16(const uint4 r, float* f);
+template <> __device__ __forceinline__ void widen16<float>(const uint4 r, float* f) {
+  f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+  f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+}
+template <> __device__ __forceinline__ void widen16<__nv_bfloat16>(const uint4 r, float* f) {
+  f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x); f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+  f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z); f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+}
+
+template <typename T, typename PT, int D>
 __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* __restrict__ q,
                                                     int n_cand, float inv_sqrt_d, int ubase) {
-  constexpr int M = D / 32;  // float4 per lane per pooled row
+  constexpr int EPC = 16 / (int)sizeof(PT);  // pooled values per 16-byte chunk
+  constexpr int M = D / EPC / 8;             // chunks per lane per pooled row
+  static_assert(M >= 1, "row too short for 8 lanes");
   __shared__ __align__(16) float qbar[D];
   const int u = ubase + blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
   const T* qg = q + ((long long)b * s.Hq + (long long)h * s.G) * D;
@@ -37,30 +51,33 @@ __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 3, c = lane & 7;
-  float4 qr[M];
+  float qr[M][EPC];
 #pragma unroll
-  for (int m = 0; m < M; ++m) qr[m] = *reinterpret_cast<const float4*>(&qbar[c * 4 + 32 * m]);
+  for (int m = 0; m < M; ++m)
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) qr[m][e] = qbar[(c + 8 * m) * EPC + e];
 
   const int base = blockIdx.x * kScoreBPC + warp * kScoreBPW;
-  float4 x[kScoreBPW][M];
+  const PT* pk = reinterpret_cast<const PT*>(st.pk);
+  uint4 x[kScoreBPW][M];
 #pragma unroll
   for (int j = 0; j < kScoreBPW; ++j) {
     const int i = base + j;
-    const float4* row = reinterpret_cast<const float4*>(
-        st.pk + (((long long)u * s.maxBlk + (i < n_cand ? i : 0)) * 4 + r) * D);
+    const uint4* row = reinterpret_cast<const uint4*>(
+        pk + (((long long)u * s.maxBlk + (i < n_cand ? i : 0)) * 4 + r) * D);
 #pragma unroll
     for (int m = 0; m < M; ++m)
-      x[j][m] = (i < n_cand) ? __ldg(row + c + 8 * m) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[j][m] = (i < n_cand) ? __ldg(row + c + 8 * m) : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
   for (int j = 0; j < kScoreBPW; ++j) {
     float p = 0.f;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      p = fmaf(x[j][m].x, qr[m].x, p);
-      p = fmaf(x[j][m].y, qr[m].y, p);
-      p = fmaf(x[j][m].z, qr[m].z, p);
-      p = fmaf(x[j][m].w, qr[m].w, p);
+      float f[EPC];
+      widen16<PT>(x[j][m], f);
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) p = fmaf(f[e], qr[m][e], p);
     }
     p += __shfl_xor_sync(0xffffffffu, p, 1);
     p += __shfl_xor_sync(0xffffffffu, p, 2);
@@ -74,21 +91,27 @@ __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* 
 
 }  // namespace
 
+template <typename T, typename PT>
+cudaError_t launch_score_t(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
+                           dim3 grid, float isd, cudaStream_t stream) {
+  if (s.d == 64)
+    score_kernel<T, PT, 64><<<grid, 256, 0, stream>>>(s, st, (const T*)q, n_cand, isd, ubase);
+  else
+    score_kernel<T, PT, 128><<<grid, 256, 0, stream>>>(s, st, (const T*)q, n_cand, isd, ubase);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
                          int ucount, cudaStream_t stream) {
   if (n_cand <= 0 || ucount <= 0) return cudaSuccess;
   dim3 grid((n_cand + kScoreBPC - 1) / kScoreBPC, ucount);
   const float isd = (float)(1.0 / sqrt((double)s.d));
-  if (s.dtype == 0) {
-    if (s.d == 64) score_kernel<float, 64><<<grid, 256, 0, stream>>>(s, st, (const float*)q, n_cand, isd, ubase);
-    else score_kernel<float, 128><<<grid, 256, 0, stream>>>(s, st, (const float*)q, n_cand, isd, ubase);
-  } else {
-    if (s.d == 64)
-      score_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(s, st, (const __nv_bfloat16*)q, n_cand, isd, ubase);
-    else
-      score_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(s, st, (const __nv_bfloat16*)q, n_cand, isd, ubase);
-  }
-  return cudaGetLastError();
+  if (s.dtype == 0)
+    return s.pkb ? launch_score_t<float, __nv_bfloat16>(s, st, q, n_cand, ubase, grid, isd, stream)
+                 : launch_score_t<float, float>(s, st, q, n_cand, ubase, grid, isd, stream);
+  return s.pkb
+             ? launch_score_t<__nv_bfloat16, __nv_bfloat16>(s, st, q, n_cand, ubase, grid, isd, stream)
+             : launch_score_t<__nv_bfloat16, float>(s, st, q, n_cand, ubase, grid, isd, stream);
 }
 
 }  // namespace nosa

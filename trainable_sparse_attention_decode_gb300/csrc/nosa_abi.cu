@@ -58,7 +58,9 @@ nosa_status validate(const nosa_config* c, std::string& why) {
   if (c->k < 1 || c->k_e < 0 || c->k_e > c->k) { why = "need 0 <= k_e <= k and k >= 1"; return NOSA_ERR_INVALID_ARG; }
   if (c->max_context < 1) { why = "max_context must be >= 1"; return NOSA_ERR_INVALID_ARG; }
   if (c->device < 0) { why = "device must be >= 0"; return NOSA_ERR_INVALID_ARG; }
-  if (c->flags & ~NOSA_FLAG_TIMING) { why = "unknown flag bits"; return NOSA_ERR_INVALID_ARG; }
+  if (c->flags & ~(NOSA_FLAG_TIMING | NOSA_FLAG_POOLED_BF16)) {
+    why = "unknown flag bits"; return NOSA_ERR_INVALID_ARG;
+  }
   if (c->head_dim < 1) { why = "head_dim must be >= 1"; return NOSA_ERR_INVALID_ARG; }
   if (c->block != 64 || c->sub_block != 16) {
     why = "compiled for block = 64, sub_block = 16"; return NOSA_ERR_UNSUPPORTED;
@@ -102,6 +104,7 @@ Shape shape_of(const nosa_config& c) {
   s.elt = c.dtype == NOSA_F32 ? 4 : 2;
   s.kbytes = c.block * c.head_dim * s.elt;
   s.payload = payload_of(c.block, c.head_dim, c.dtype);
+  s.pkb = (c.flags & NOSA_FLAG_POOLED_BF16) ? 1 : 0;
   return s;
 }
 
@@ -367,7 +370,8 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   };
   A(&st.slots, U * k * s.payload);
   A(&st.tail, U * 2 * s.payload);
-  A(&st.pk, U * mb * s.P * s.d * 4);
+  const size_t pk_elt = s.pkb ? 2 : 4;
+  A(&st.pk, U * mb * s.P * s.d * pk_elt);
   A(&st.sube, U * mb * s.P * 4);
   A(&st.se, U * mb * 4);
   A(&st.sq, U * mb * 4);
@@ -397,7 +401,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // Zeroed state: empty slots (-1), nothing eligible or resident.
   if (e == cudaSuccess) e = cudaMemset(st.slots, 0, U * k * s.payload);
   if (e == cudaSuccess) e = cudaMemset(st.tail, 0, U * 2 * s.payload);
-  if (e == cudaSuccess) e = cudaMemset(st.pk, 0, U * mb * s.P * s.d * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.pk, 0, U * mb * s.P * s.d * pk_elt);
   if (e == cudaSuccess) e = cudaMemset(st.sube, 0, U * mb * s.P * 4);
   if (e == cudaSuccess) e = cudaMemset(st.se, 0, U * mb * 4);
   if (e == cudaSuccess) e = cudaMemset(st.sq, 0, U * mb * 4);
@@ -685,7 +689,7 @@ size_t nosa_debug_size(const nosa_handle* h, int32_t what) {
     case NOSA_DBG_SLOTS: return U * k * 4;
     case NOSA_DBG_LOADS: return U * k * 3 * 4;
     case NOSA_DBG_NLOAD: return U * 4;
-    case NOSA_DBG_POOLED: return U * mb * s.P * s.d * 4;
+    case NOSA_DBG_POOLED: return U * mb * s.P * s.d * (s.pkb ? 2 : 4);
     case NOSA_DBG_SE: return U * mb * 4;
     case NOSA_DBG_SQ: return U * mb * 4;
     case NOSA_DBG_SLOTPOOL: return U * k * (size_t)s.payload;

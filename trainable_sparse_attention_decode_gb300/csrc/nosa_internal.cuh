@@ -23,6 +23,7 @@ constexpr int kMaxBlocks = 65535;  // capacity in blocks per unit
 struct Shape {
   int U, batch, Hq, Hkv, G, d, B, S, P, k, ke, maxBlk, W;
   int dtype;  // 0 fp32, 1 bf16
+  int pkb;    // pooled keys stored in bf16 (else fp32)
   int elt;    // bytes per element of q, k, v, out
   int kbytes; // B * d * elt  (K part of a block unit, = V part)
   long long payload;  // bytes per block unit
@@ -44,7 +45,7 @@ struct State {
   uint8_t* slots;      // [U][k] block units (device)
   uint8_t* tail;       // [U][2] block units (device); block b lives in buffer b % 2
   uint8_t* host;       // [U][maxBlk] block units (pinned, mapped host memory; device view)
-  float* pk;           // [U][maxBlk][P][d] sub-block mean keys
+  float* pk;           // [U][maxBlk][P][d] sub-block mean keys (fp32, or bf16 when Shape::pkb)
   float* sube;         // [U][maxBlk][P]    sub-block mean eviction logits
   float* se;           // [U][maxBlk]       block eviction score (max of sube)
   float* sq;           // [U][maxBlk]       query-aware block score of the current step
@@ -148,6 +149,14 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
+}
+
+// Stores a sub-block mean key in the handle's pooled-key precision.
+__device__ __forceinline__ void store_pooled(const Shape& s, float* pk, long long idx, float v) {
+  if (s.pkb)
+    reinterpret_cast<__nv_bfloat16*>(pk)[idx] = __float2bfloat16_rn(v);
+  else
+    pk[idx] = v;
 }
 
 // Byte offsets inside a block unit (layout documented in include/nosa.h).
