@@ -306,12 +306,12 @@ def run_gpu(args, rank, world, local_rank):
         w0 = w0.with_(name=f"{w0.name}-ke0", k_e=0)
     W, K = args.warmup, args.steps
     KE = args.e2e_steps
-    total_steps = W + K + KE
+    KT = 0 if args.no_timing else args.phase_steps  # per-phase event timing window
+    total_steps = W + K + KE + KT
     w = w0.with_(steps=total_steps)
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
                            w.max_context, device=local_rank,
-                           flags=(0 if args.no_timing else nosa.NOSA_FLAG_TIMING)
-                           | (nosa.NOSA_FLAG_POOLED_BF16 if args.pooled_bf16 else 0))
+                           flags=(nosa.NOSA_FLAG_POOLED_BF16 if args.pooled_bf16 else 0))
     h = nosa.nosa_create(cfg)
     # prompt, appended in chunks generated on the device
     chunk = 4096
@@ -366,8 +366,8 @@ def run_gpu(args, rank, world, local_rank):
     context_after = st["context"]
 
     # end to end: pinned host inputs -> device, step, result -> pinned host
-    qh = q_all[W + K:].cpu().pin_memory()
-    kh, vh, eh = (x[W + K:].cpu().pin_memory() for x in (k_all, v_all, e_all))
+    qh = q_all[W + K:W + K + KE].cpu().pin_memory()
+    kh, vh, eh = (x[W + K:W + K + KE].cpu().pin_memory() for x in (k_all, v_all, e_all))
     qd, kd, vd, ed = (torch.empty_like(x[0], device="cuda") for x in (qh, kh, vh, eh))
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     barrier(world)
@@ -391,6 +391,18 @@ def run_gpu(args, rank, world, local_rank):
     bi = sum(x[0].numel() * x.element_size() for x in (qh, kh, vh, eh))
     bo = out_h.numel() * out_h.element_size()
     clocks = sampler.stop() if sampler else None
+
+    # Per-phase device times from the library's events, in a window of their own
+    # (the events cost some device time, so the timed loops above run without).
+    st_ph = None
+    if KT > 0:
+        nosa.nosa_set_timing(h, True)
+        torch.cuda.synchronize()
+        nosa.nosa_stats_reset(h)
+        for s in range(W + K + KE, W + K + KE + KT):
+            nosa.nosa_decode_step(h, ptrs[s][0], ptrs[s][1], ptrs[s][2], ptrs[s][3], out_p, lse_p,
+                                  stream_p)
+        st_ph = nosa.nosa_stats(h)
     nosa.nosa_destroy(h)
     del q_all, k_all, v_all, e_all
     n_mid = (w.prompt + W + K // 2) // w.block
@@ -404,8 +416,8 @@ def run_gpu(args, rank, world, local_rank):
 
     n_cand = (w.prompt + W + K // 2) // w.block       # mid-region candidate count
     tail_mid = (w.prompt + W + K // 2) % w.block + 1
-    tu = st["t_us"]
-    nt = max(st["t_count"], 1)
+    tu = st_ph["t_us"] if st_ph else [0.0] * 8
+    nt = max(st_ph["t_count"], 1) if st_ph else 1
     # phases of nosa_stats: append+pool, score, select+set-difference, attention
     # over the slots kept from the previous step (runs while the gather runs on a
     # side stream), gather, attention over the filled slots (waits for the gather)
@@ -427,8 +439,9 @@ def run_gpu(args, rank, world, local_rank):
         return nbytes / (us * 1e-6) / 1e9 if us > 0 else 0.0
     attn_gbs = rate(attn_kept_bytes, phase_us["attention_kept"])
     score_gbs = rate(score_bytes, phase_us["score_select"])  # includes the selection
-    host_bytes_step = st["host_bytes"] / max(st["steps"] - W, 1) if st["steps"] > W else 0.0
-    recall_gbs = (host_bytes_step / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
+    host_bytes_step = st["host_bytes"] / K
+    host_bytes_window = st_ph["host_bytes"] / KT if st_ph else 0.0
+    recall_gbs = (host_bytes_window / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
     # Roofline kernel: the split-K attention, timed alone on the step's shape (in the
     # step it shares the GPU with the gather, which would blur its own bound).
     dominant = "attn_split_kernel (alone, step shape)"
@@ -477,6 +490,8 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": st["launches"],
         "loads_per_unit_step": round(loads_per_unit, 3),
         "host_enqueue_us_per_step": round(host_enqueue_us, 2),
+        "step_graphs": os.environ.get("NOSA_GRAPHS", "1") != "0",
+        "phase_window_steps": KT,
         "clocks": clocks,
     }
     return line
@@ -576,7 +591,9 @@ def main():
     ap.add_argument("--pooled-bf16", action="store_true",
                     help="variant: pooled keys stored in bf16 (halves the scoring traffic)")
     ap.add_argument("--no-timing", action="store_true",
-                    help="run without the library's per-phase CUDA events")
+                    help="skip the per-phase timing window")
+    ap.add_argument("--phase-steps", type=int, default=64,
+                    help="decode steps of the per-phase timing window (after the timed loops)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--prompt", type=int, default=0, help="override the workload's prompt")
     args = ap.parse_args()

@@ -149,6 +149,10 @@ nosa_status nosa_append_kv(nosa_handle* h, int32_t n_tokens, const void* k, cons
  * written back to the host store) -> score -> dual select -> set-difference ->
  * gather -> split-K attention -> combine. The context must be >= 1 token
  * before the call (STATE otherwise). CAPACITY when the context is full.
+ * Every step after the first replays a CUDA graph of the whole step captured
+ * by the handle (rebuilt when the candidate count leaves a 32-block window), so
+ * its host cost is one graph-node update and one graph launch; the environment
+ * variable NOSA_GRAPHS=0 at create time launches every kernel instead.
  */
 nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
                              const float* e_new, void* out, float* lse, void* stream);
@@ -190,6 +194,15 @@ nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out);
 
 /* Clears the counters and timers of nosa_stats (not the state). */
 nosa_status nosa_stats_reset(nosa_handle* h);
+
+/*
+ * Switches the per-phase timing of nosa_stats.t_us on (on != 0) or off for the
+ * decode steps that follow (NOSA_FLAG_TIMING at create time starts with it
+ * on). Timing records eight CUDA events per step, which costs some device
+ * time: leave it off when measuring throughput. The events are created on the
+ * first switch-on. Errors: INVALID_ARG (NULL handle), CUDA.
+ */
+nosa_status nosa_set_timing(nosa_handle* h, int32_t on);
 
 /*
  * Debug read-back (synchronous, for tests). Copies `bytes` bytes starting at

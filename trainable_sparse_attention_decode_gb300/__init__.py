@@ -19,7 +19,7 @@ __all__ = [
     "NosaError", "NosaConfig", "NosaStats", "lib", "lib_path",
     "NOSA_F32", "NOSA_BF16", "NOSA_FLAG_TIMING", "NOSA_FLAG_POOLED_BF16", "DBG",
     "nosa_config", "nosa_config_validate", "nosa_payload_bytes", "nosa_create",
-    "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset",
+    "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset", "nosa_set_timing",
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
     "nosa_selftest_bounded_wait",
@@ -75,6 +75,7 @@ def _load():
         "nosa_decode_step": (C.c_int, [VP, VP, VP, VP, VP, VP, VP, VP]),
         "nosa_stats": (C.c_int, [VP, P(NosaStats)]),
         "nosa_stats_reset": (C.c_int, [VP]),
+        "nosa_set_timing": (C.c_int, [VP, C.c_int32]),
         "nosa_debug_read": (C.c_int, [VP, I32, SZ, VP, SZ]),
         "nosa_debug_size": (SZ, [VP, I32]),
         "nosa_destroy": (None, [VP]),
@@ -210,6 +211,11 @@ def nosa_stats(h) -> dict:
 
 def nosa_stats_reset(h):
     _check(lib.nosa_stats_reset(h), h)
+
+
+def nosa_set_timing(h, on: bool):
+    """Per-phase event timing of the following decode steps on or off."""
+    _check(lib.nosa_set_timing(h, 1 if on else 0), h)
 
 
 def nosa_debug_size(h, what) -> int:

@@ -27,17 +27,29 @@ __device__ __forceinline__ void copy_unit(uint8_t* dst, const uint8_t* src, long
 }
 
 // One decode-step token per unit. grid = U, block = 128 threads (d <= 128).
+// CTA 0 also publishes the step's arguments (StepIO) for the kernels after it.
 template <typename T>
-__global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st,
-                                                          const T* __restrict__ k_new,
-                                                          const T* __restrict__ v_new,
-                                                          const float* __restrict__ e_new,
-                                                          int L_old) {
+__global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st, StepArgs a) {
+  const T* __restrict__ k_new = static_cast<const T*>(a.k_new);
+  const T* __restrict__ v_new = static_cast<const T*>(a.v_new);
+  const float* __restrict__ e_new = a.e_new;
   const int u = blockIdx.x;
-  const int t = L_old;
+  const int t = a.L_old;
   const int blk = t / s.B, pos = t % s.B;
   uint8_t* cur = st.tail + ((long long)u * 2 + (blk & 1)) * s.payload;
   if (u == 0 && threadIdx.x < kMaxChunks) st.work_count[threadIdx.x] = 0;
+  if (u == 0 && threadIdx.x == 0) {
+    StepIO io;
+    io.q = a.q;
+    io.out = a.out;
+    io.lse = a.lse;
+    io.L_old = a.L_old;
+    io.n_cand = blk;  // (L_old + 1 - 1) / B complete blocks precede the tail
+    io.tail_len = pos + 1;
+    io.just_completed = (pos == 0 && blk > 0) ? blk - 1 : -1;
+    io.tail_off = (long long)(blk & 1) * s.payload;
+    *st.io = io;
+  }
 
   // The block before a newly opened one becomes a candidate.
   if (pos == 0 && blk > 0) {
@@ -183,15 +195,12 @@ __global__ void __launch_bounds__(256) append_bulk_kernel(Shape s, State st,
 
 }  // namespace
 
-cudaError_t launch_append_step(const Shape& s, const State& st, const void* k_new,
-                               const void* v_new, const float* e_new, int L_old,
+cudaError_t launch_append_step(const Shape& s, const State& st, const StepArgs& a,
                                cudaStream_t stream) {
   if (s.dtype == 0)
-    append_step_kernel<float><<<s.U, 128, 0, stream>>>(
-        s, st, (const float*)k_new, (const float*)v_new, e_new, L_old);
+    append_step_kernel<float><<<s.U, 128, 0, stream>>>(s, st, a);
   else
-    append_step_kernel<__nv_bfloat16><<<s.U, 128, 0, stream>>>(
-        s, st, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, e_new, L_old);
+    append_step_kernel<__nv_bfloat16><<<s.U, 128, 0, stream>>>(s, st, a);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ struct AttnKParams {
   int Hq, Hkv;
   float qscale;  // log2(e) / sqrt(d)
   int* err;
+  const StepIO* dyn;  // decode step: q, out, lse, tail_len and the tail offset live here
 };
 
 template <typename T> struct Unpack16;
@@ -124,13 +125,25 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   const int u = p.unit_base + blockIdx.y, sp = blockIdx.x;
   const int b = u / p.Hkv, h = u % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const void* q_in = p.q;
+  void* out = p.out;
+  float* lse = p.lse;
+  int tail_len = p.tail_len;
+  const uint8_t* tail = p.tail;
+  if (p.dyn != nullptr) {
+    q_in = p.dyn->q;
+    out = p.dyn->out;
+    lse = p.dyn->lse;
+    tail_len = p.dyn->tail_len;
+    if (tail != nullptr) tail += p.dyn->tail_off;
+  }
   // Virtual item list: the n_blocks table entries, then the tail (if any),
   // spread evenly over the splits.
-  const int nv = p.n_blocks + (p.tail != nullptr ? 1 : 0);
+  const int nv = p.n_blocks + (tail != nullptr ? 1 : 0);
   const int v0 = (int)((long long)sp * nv / p.nsplit);
   const int v1 = (int)((long long)(sp + 1) * nv / p.nsplit);
   const int j0 = v0, j1 = min(v1, p.n_blocks);
-  const bool has_tail = (p.tail != nullptr) && (v1 > p.n_blocks);
+  const bool has_tail = (tail != nullptr) && (v1 > p.n_blocks);
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -168,14 +181,14 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
     for (int s = 0; s < pre; ++s) {
       const int idx = list[s];
       const uint8_t* src = idx >= 0 ? p.units + (long long)idx * payload
-                                    : p.tail + (long long)u * p.tail_stride;
+                                    : tail + (long long)u * p.tail_stride;
       mbar_arrive_expect_tx(&full[s], (uint32_t)payload);
       bulk_g2s(stage_buf + (size_t)s * payload, src, (uint32_t)payload, &full[s]);
     }
     issued = pre;
   }
   {
-    const T* qg = reinterpret_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)h * G) * D;
+    const T* qg = reinterpret_cast<const T*>(q_in) + ((long long)b * p.Hq + (long long)h * G) * D;
     for (int i = tid; i < G * D; i += NT) {
       const int g = i / D, dim = i % D;
       q_s[(g * PARTS + dim / (D / PARTS)) * QP + (dim % (D / PARTS))] = to_f32(qg[i]) * p.qscale;
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
       break;
     }
     const uint8_t* buf = stage_buf + (size_t)si * payload;
-    const bool valid = (list[it] >= 0) || (tok < p.tail_len);
+    const bool valid = (list[it] >= 0) || (tok < tail_len);
 
     // ---- logits of this warp's TPW tokens ----
     float2 d2[G];
@@ -296,7 +309,7 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
       } else {
         const int idx = list[issued];
         const uint8_t* src = idx >= 0 ? p.units + (long long)idx * payload
-                                      : p.tail + (long long)u * p.tail_stride;
+                                      : tail + (long long)u * p.tail_stride;
         mbar_arrive_expect_tx(&full[si], (uint32_t)payload);
         bulk_g2s(stage_buf + (size_t)si * payload, src, (uint32_t)payload, &full[si]);
         ++issued;
@@ -416,9 +429,9 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
 #pragma unroll 8
     for (int j = 0; j < nst; ++j) A += __ldcg(ac + (long long)j * G * D) * w_s[j * G + g];
     const long long row = (long long)b * p.Hq + (long long)h * G + g;
-    reinterpret_cast<T*>(p.out)[row * D + dim] = from_f32<T>(A);
-    if (dim == 0 && p.lse != nullptr)
-      p.lse[row] = s_L[g] > 0.f ? (s_M[g] + log2f(s_L[g])) * kLn2 : -INFINITY;
+    reinterpret_cast<T*>(out)[row * D + dim] = from_f32<T>(A);
+    if (dim == 0 && lse != nullptr)
+      lse[row] = s_L[g] > 0.f ? (s_M[g] + log2f(s_L[g])) * kLn2 : -INFINITY;
   }
   if (tid == 0) p.counters[u] = 0;
 }
@@ -451,6 +464,7 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.Hkv = s.Hkv;
   p.qscale = (float)(1.4426950408889634 / sqrt((double)D));
   p.err = a.err;
+  p.dyn = a.dyn;
   const size_t smem = AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps);
   static std::atomic<int> lim[64];
   cudaError_t err = raise_smem_limit((const void*)attn_split_kernel<T, D, G, W>, smem, lim);

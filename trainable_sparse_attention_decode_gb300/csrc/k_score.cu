@@ -33,12 +33,15 @@ template <> __device__ __forceinline__ void widen16<__nv_bfloat16>(const uint4 r
 }
 
 template <typename T, typename PT, int D>
-__global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* __restrict__ q,
-                                                    int n_cand, float inv_sqrt_d, int ubase) {
+__global__ void __launch_bounds__(256) score_kernel(Shape s, State st, float inv_sqrt_d,
+                                                    int ubase) {
   constexpr int EPC = 16 / (int)sizeof(PT);  // pooled values per 16-byte chunk
   constexpr int M = D / EPC / 8;             // chunks per lane per pooled row
   static_assert(M >= 1, "row too short for 8 lanes");
   __shared__ __align__(16) float qbar[D];
+  const int n_cand = st.io->n_cand;
+  if (blockIdx.x * kScoreBPC >= n_cand) return;  // grid sized for a larger count
+  const T* __restrict__ q = static_cast<const T*>(st.io->q);
   const int u = ubase + blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
   const T* qg = q + ((long long)b * s.Hq + (long long)h * s.G) * D;
   const float inv_g = 1.0f / (float)s.G;
@@ -92,26 +95,25 @@ __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, const T* 
 }  // namespace
 
 template <typename T, typename PT>
-cudaError_t launch_score_t(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
-                           dim3 grid, float isd, cudaStream_t stream) {
+cudaError_t launch_score_t(const Shape& s, const State& st, int ubase, dim3 grid, float isd,
+                           cudaStream_t stream) {
   if (s.d == 64)
-    score_kernel<T, PT, 64><<<grid, 256, 0, stream>>>(s, st, (const T*)q, n_cand, isd, ubase);
+    score_kernel<T, PT, 64><<<grid, 256, 0, stream>>>(s, st, isd, ubase);
   else
-    score_kernel<T, PT, 128><<<grid, 256, 0, stream>>>(s, st, (const T*)q, n_cand, isd, ubase);
+    score_kernel<T, PT, 128><<<grid, 256, 0, stream>>>(s, st, isd, ubase);
   return cudaGetLastError();
 }
 
-cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
-                         int ucount, cudaStream_t stream) {
-  if (n_cand <= 0 || ucount <= 0) return cudaSuccess;
-  dim3 grid((n_cand + kScoreBPC - 1) / kScoreBPC, ucount);
+cudaError_t launch_score(const Shape& s, const State& st, int n_cap, int ubase, int ucount,
+                         cudaStream_t stream) {
+  if (n_cap <= 0 || ucount <= 0) return cudaSuccess;
+  dim3 grid((n_cap + kScoreBPC - 1) / kScoreBPC, ucount);
   const float isd = (float)(1.0 / sqrt((double)s.d));
   if (s.dtype == 0)
-    return s.pkb ? launch_score_t<float, __nv_bfloat16>(s, st, q, n_cand, ubase, grid, isd, stream)
-                 : launch_score_t<float, float>(s, st, q, n_cand, ubase, grid, isd, stream);
-  return s.pkb
-             ? launch_score_t<__nv_bfloat16, __nv_bfloat16>(s, st, q, n_cand, ubase, grid, isd, stream)
-             : launch_score_t<__nv_bfloat16, float>(s, st, q, n_cand, ubase, grid, isd, stream);
+    return s.pkb ? launch_score_t<float, __nv_bfloat16>(s, st, ubase, grid, isd, stream)
+                 : launch_score_t<float, float>(s, st, ubase, grid, isd, stream);
+  return s.pkb ? launch_score_t<__nv_bfloat16, __nv_bfloat16>(s, st, ubase, grid, isd, stream)
+               : launch_score_t<__nv_bfloat16, float>(s, st, ubase, grid, isd, stream);
 }
 
 }  // namespace nosa

@@ -249,11 +249,11 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
 // grid = U, block = 256. Dynamic shared memory: key [maxBlk] u32 + flag [maxBlk] u8.
 // flag bits: 1 = eligible, 2 = in Gamma_e, 4 = in Gamma_q. The set-difference
 // against the unit's slots runs in the same CTA once Gamma is known.
-__global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, State st, int n,
-                                                                     int just_completed,
-                                                                     int cold, int ubase,
-                                                                     int chunk) {
+__global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, State st, int cold,
+                                                                     int ubase, int chunk) {
   extern __shared__ __align__(16) uint8_t dyn[];
+  const int n = st.io->n_cand;
+  const int just_completed = st.io->just_completed;
   __shared__ SelShared sh;
   uint32_t* key = reinterpret_cast<uint32_t*>(dyn);
   uint8_t* flag = dyn + (size_t)s.maxBlk * 4;
@@ -423,15 +423,13 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
 
 }  // namespace
 
-cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
-                                  int just_completed, int cold, int ubase, int ucount, int chunk,
-                                  cudaStream_t stream) {
+cudaError_t launch_select_setdiff(const Shape& s, const State& st, int cold, int ubase,
+                                  int ucount, int chunk, cudaStream_t stream) {
   const size_t smem = (size_t)s.maxBlk * 5;
   static std::atomic<int> lim[64];
   cudaError_t err = raise_smem_limit((const void*)select_setdiff_kernel, smem, lim);
   if (err != cudaSuccess) return err;
-  select_setdiff_kernel<<<ucount, kSelThreads, smem, stream>>>(s, st, n_cand, just_completed,
-                                                                cold, ubase, chunk);
+  select_setdiff_kernel<<<ucount, kSelThreads, smem, stream>>>(s, st, cold, ubase, chunk);
   return cudaGetLastError();
 }
 

@@ -23,8 +23,10 @@ using namespace nosa;
 namespace {
 
 constexpr int kMaxSplits = 64;
-constexpr int kRing = 64;     // timing event sets in flight
+constexpr int kRing = 64;     // timing event sets in flight (eager steps)
 constexpr int kNumEv = 8;
+constexpr int kGraphRing = 16; // step graphs in flight when timing (each owns an event set)
+constexpr int kScoreCap = 32; // a step graph's score grid covers this many more candidates
 
 thread_local std::string g_thread_err;
 
@@ -220,6 +222,21 @@ cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t str
 // ---------------------------------------------------------------------------
 // The handle
 // ---------------------------------------------------------------------------
+// A captured warm decode step. Every per-step value reaches the kernels through
+// the append node's arguments (the append kernel publishes StepIO), so between
+// rebuilds a step costs one node update and one graph launch. The score grids
+// cover candidates [0, n_cap); the graph is rebuilt when the count leaves
+// [n_cap - kScoreCap, n_cap).
+struct StepGraph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t append_node = nullptr;
+  cudaKernelNodeParams append_params{};
+  int n_cap = 0;
+  bool pending = false;        // timing events of the last launch not yet read
+  cudaEvent_t done = nullptr;  // recorded after each launch: a rebuild waits for it
+};
+
 struct nosa_handle {
   nosa_config cfg;
   Shape s;
@@ -238,12 +255,21 @@ struct nosa_handle {
   // Internal streams of the pipelined step: selection chain (medium priority),
   // gather (highest), attention over kept slots (lowest), attention over filled
   // slots (medium); events order them per unit chunk.
-  cudaStream_t s_sel = nullptr, s_gat = nullptr, s_att = nullptr, s_new = nullptr;
+  cudaStream_t s_sco = nullptr, s_sel = nullptr, s_gat = nullptr, s_att = nullptr, s_new = nullptr;
   cudaEvent_t ev_in = nullptr, ev_att = nullptr, ev_new = nullptr;
-  cudaEvent_t ev_sel[kMaxChunks] = {}, ev_gat[kMaxChunks] = {};
+  cudaEvent_t ev_jsco = nullptr, ev_jsel = nullptr, ev_jgat = nullptr;  // joins of a captured step
+  cudaStream_t s_cap = nullptr;                       // origin stream of captures
+  bool use_graphs = true;
+  StepGraph plain;               // step graph without timing events
+  StepGraph graphs[kGraphRing];  // step graphs with timing events (ring)
+  cudaEvent_t gev[kGraphRing][kNumEv];
+  int graph_pos = 0;
+  long long graph_builds = 0;
+  cudaEvent_t ev_sco[kMaxChunks] = {}, ev_sel[kMaxChunks] = {}, ev_gat[kMaxChunks] = {};
   int nchunks = 1;
   int cu_base[kMaxChunks] = {}, cu_count[kMaxChunks] = {}, nsplit_c[kMaxChunks] = {};
-  bool timing = false;
+  bool timing = false;    // timing events recorded for the next steps
+  bool ev_made = false;   // the event sets below exist
   cudaEvent_t ev[kRing][kNumEv];
   bool pending[kRing];
   int ring_pos = 0;
@@ -278,29 +304,44 @@ void free_all(nosa_handle* h) {
   h->dev_allocs.clear();
   if (h->host_store) cudaFreeHost(h->host_store);
   h->host_store = nullptr;
-  if (h->timing) {
+  for (StepGraph* gp : {&h->plain}) {
+    if (gp->exec) cudaGraphExecDestroy(gp->exec);
+    if (gp->graph) cudaGraphDestroy(gp->graph);
+    if (gp->done) cudaEventDestroy(gp->done);
+    *gp = StepGraph();
+  }
+  for (StepGraph& g : h->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+    if (g.done) cudaEventDestroy(g.done);
+    g = StepGraph();
+  }
+  if (h->ev_made) {
     for (int r = 0; r < kRing; ++r)
       for (int i = 0; i < kNumEv; ++i) cudaEventDestroy(h->ev[r][i]);
+    for (int r = 0; r < kGraphRing; ++r)
+      for (int i = 0; i < kNumEv; ++i) cudaEventDestroy(h->gev[r][i]);
+    h->ev_made = false;
     h->timing = false;
   }
-  for (cudaEvent_t* e : {&h->ev_in, &h->ev_att, &h->ev_new})
+  for (cudaEvent_t* e : {&h->ev_in, &h->ev_att, &h->ev_new, &h->ev_jsco, &h->ev_jsel, &h->ev_jgat})
     if (*e) cudaEventDestroy(*e), *e = nullptr;
   for (int c = 0; c < kMaxChunks; ++c) {
+    if (h->ev_sco[c]) cudaEventDestroy(h->ev_sco[c]), h->ev_sco[c] = nullptr;
     if (h->ev_sel[c]) cudaEventDestroy(h->ev_sel[c]), h->ev_sel[c] = nullptr;
     if (h->ev_gat[c]) cudaEventDestroy(h->ev_gat[c]), h->ev_gat[c] = nullptr;
   }
-  for (cudaStream_t* t : {&h->s_sel, &h->s_gat, &h->s_att, &h->s_new})
+  for (cudaStream_t* t : {&h->s_sco, &h->s_sel, &h->s_gat, &h->s_att, &h->s_new, &h->s_cap})
     if (*t) cudaStreamDestroy(*t), *t = nullptr;
 }
 
-// Events of one step: e0 start (caller's stream); e1 after the append and e2
-// after the last chunk's select + set-difference (selection stream); e4 before
+// Events of one step: e0 start (caller's stream); e1 after the append (scoring
+// stream); e2 after the last chunk's select + set-difference (selection stream); e4 before
 // the first and e5 after the last chunk's gather (gather stream); e3 before the
 // first and e6 after the last attention over kept slots (attention stream); e7
 // after the join (caller's stream).
-void harvest(nosa_handle* h, int r) {
-  if (!h->pending[r]) return;
-  cudaEvent_t* e = h->ev[r];
+void harvest_set(nosa_handle* h, cudaEvent_t* e, bool* pending) {
+  if (!*pending) return;
   if (cudaEventSynchronize(e[7]) != cudaSuccess) return;
   const int pairs[6][3] = {{0, 0, 1}, {1, 1, 2}, {3, 3, 6}, {4, 4, 5}, {5, 6, 7}, {7, 0, 7}};
   for (const auto& pr : pairs) {
@@ -308,7 +349,34 @@ void harvest(nosa_handle* h, int r) {
     if (cudaEventElapsedTime(&ms, e[pr[1]], e[pr[2]]) == cudaSuccess) h->t_us[pr[0]] += ms * 1000.0;
   }
   h->t_count += 1;
-  h->pending[r] = false;
+  *pending = false;
+}
+
+void harvest(nosa_handle* h, int r) { harvest_set(h, h->ev[r], &h->pending[r]); }
+
+void harvest_all(nosa_handle* h) {
+  if (!h->ev_made) return;
+  for (int r = 0; r < kRing; ++r) harvest(h, r);
+  for (int r = 0; r < kGraphRing; ++r) harvest_set(h, h->gev[r], &h->graphs[r].pending);
+}
+
+cudaError_t make_timing_events(nosa_handle* h) {
+  if (h->ev_made) return cudaSuccess;
+  std::vector<cudaEvent_t*> slots;
+  for (int r = 0; r < kRing; ++r)
+    for (int i = 0; i < kNumEv; ++i) slots.push_back(&h->ev[r][i]);
+  for (int r = 0; r < kGraphRing; ++r)
+    for (int i = 0; i < kNumEv; ++i) slots.push_back(&h->gev[r][i]);
+  for (size_t j = 0; j < slots.size(); ++j) {
+    const cudaError_t e = cudaEventCreate(slots[j]);
+    if (e != cudaSuccess) {
+      for (size_t m = 0; m < j; ++m) cudaEventDestroy(*slots[m]);
+      return e;
+    }
+  }
+  std::memset(h->pending, 0, sizeof(h->pending));
+  h->ev_made = true;
+  return cudaSuccess;
 }
 
 DevStats fresh_stats() {
@@ -391,6 +459,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.part_acc, U * 2 * kMaxSplits * s.G * s.d * 4);
   A(&st.part_ml, U * 2 * kMaxSplits * s.G * 2 * 4);
   A(&st.stats, sizeof(DevStats));
+  A(&st.io, sizeof(StepIO));
   if (e != cudaSuccess) {
     g_thread_err = std::string("device allocation failed: ") + cudaGetErrorString(e);
     cudaGetLastError();
@@ -465,9 +534,31 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   }
   nchunks = std::max(1, std::min(std::min(nchunks, kMaxChunks), s.U));
   h->nchunks = nchunks;
+  // Chunk c holds a share of the units proportional to growth^c: a small first
+  // chunk starts the gather early, later chunks are scored while it runs
+  // (NOSA_CHUNK_GROWTH overrides the ratio).
+  double growth = 1.0;
+  if (const char* g = std::getenv("NOSA_CHUNK_GROWTH")) {
+    const double v = std::atof(g);
+    if (v >= 0.25 && v <= 16.0) growth = v;
+  }
+  {
+    double total = 0.0, w = 1.0;
+    for (int c = 0; c < nchunks; ++c, w *= growth) total += w;
+    double acc = 0.0;
+    w = 1.0;
+    int prev = 0;
+    for (int c = 0; c < nchunks; ++c, w *= growth) {
+      acc += w;
+      int end = (c == nchunks - 1) ? s.U : (int)std::llround(s.U * acc / total);
+      end = std::max(end, prev + 1);                    // every chunk holds a unit
+      end = std::min(end, s.U - (nchunks - 1 - c));     // and leaves one for each later chunk
+      h->cu_base[c] = prev;
+      h->cu_count[c] = end - prev;
+      prev = end;
+    }
+  }
   for (int c = 0; c < nchunks; ++c) {
-    h->cu_base[c] = (int)((long long)s.U * c / nchunks);
-    h->cu_count[c] = (int)((long long)s.U * (c + 1) / nchunks) - h->cu_base[c];
     Shape sc = s;
     sc.U = h->cu_count[c];
     h->nsplit_c[c] = attention_pick_nsplit(sc, s.k, 1);
@@ -475,14 +566,21 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   int prio_lo = 0, prio_hi = 0;
   cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
   const int prio_mid = (prio_lo + prio_hi) / 2;
+  // Priorities: gather (keeps the host link busy) over selection (short, on the
+  // path to the next gather) over scoring and the filled-slot attention over the
+  // kept-slot attention (the bulk of the HBM work, with the most slack).
+  const int prio_sel = (prio_hi < prio_mid) ? prio_hi + 1 : prio_hi;
   e = cudaStreamCreateWithPriority(&h->s_gat, cudaStreamNonBlocking, prio_hi);
-  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sel, cudaStreamNonBlocking, prio_mid);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sel, cudaStreamNonBlocking, prio_sel);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sco, cudaStreamNonBlocking, prio_mid);
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_new, cudaStreamNonBlocking, prio_mid);
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_att, cudaStreamNonBlocking, prio_lo);
-  for (cudaEvent_t* ep : {&h->ev_in, &h->ev_att, &h->ev_new})
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_cap, cudaStreamNonBlocking);
+  for (cudaEvent_t* ep : {&h->ev_in, &h->ev_att, &h->ev_new, &h->ev_jsco, &h->ev_jsel, &h->ev_jgat})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ep, cudaEventDisableTiming);
   for (int c = 0; c < kMaxChunks && e == cudaSuccess; ++c) {
     e = cudaEventCreateWithFlags(&h->ev_sel[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_sco[c], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_gat[c], cudaEventDisableTiming);
   }
   if (e != cudaSuccess) {
@@ -492,10 +590,18 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     return NOSA_ERR_CUDA;
   }
   if (cfg->flags & NOSA_FLAG_TIMING) {
-    for (int r = 0; r < kRing; ++r)
-      for (int i = 0; i < kNumEv; ++i) cudaEventCreate(&h->ev[r][i]);
+    e = make_timing_events(h);
+    if (e != cudaSuccess) {
+      g_thread_err = std::string("event creation failed: ") + cudaGetErrorString(e);
+      free_all(h);
+      delete h;
+      return NOSA_ERR_CUDA;
+    }
     h->timing = true;
   }
+  // Warm decode steps replay a captured graph (NOSA_GRAPHS=0 launches every
+  // kernel from the host instead).
+  if (const char* g = std::getenv("NOSA_GRAPHS")) h->use_graphs = std::atoi(g) != 0;
   *out = h;
   return NOSA_OK;
 }
@@ -523,61 +629,59 @@ nosa_status nosa_append_kv(nosa_handle* h, int32_t n_tokens, const void* k, cons
   return NOSA_OK;
 }
 
-nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
-                             const float* e_new, void* out, float* lse, void* stream) {
-  if (!h) return NOSA_ERR_INVALID_ARG;
-  if (h->broken) return h->fail(NOSA_ERR_STATE, "handle unusable after an earlier CUDA error");
-  if (h->L < 1) return h->fail(NOSA_ERR_STATE, "decode step before any context was appended");
-  if (h->L + 1 > h->cfg.max_context) return h->fail(NOSA_ERR_CAPACITY, "context is full");
-  if (!q || !k_new || !v_new || !e_new || !out) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
-  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
-      !aligned(e_new, 4) || (lse && !aligned(lse, 4)))
-    return h->fail(NOSA_ERR_INVALID_ARG, "q, k_new, v_new, out need 16-byte alignment");
-  DeviceGuard guard(h->cfg.device);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// Enqueues one decode step on `origin`: the units are processed in chunks that
+// form a pipeline over five internal streams. Scoring of chunk c+1 (HBM) runs
+// while chunk c is selected, gathered (host link) and attended over its kept
+// slots (HBM); attention over the filled slots of chunk c follows its gather. `origin` forks at the start and joins at the end. Under stream
+// capture (`capture`), timing events become graph nodes and the append node is
+// returned in *append_node.
+cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& args, int n_cap,
+                         bool cold, cudaEvent_t* ev, bool capture, cudaGraphNode_t* append_node) {
   const Shape& sh = h->s;
   State& st = h->st;
-  cudaEvent_t* ev = nullptr;
-  if (h->timing) {
-    const int r = h->ring_pos;
-    harvest(h, r);
-    ev = h->ev[r];
-    h->pending[r] = true;
-    h->ring_pos = (r + 1) % kRing;
-    cudaEventRecord(ev[0], s);
+  auto mark = [&](cudaEvent_t e, cudaStream_t t) {
+    if (capture) cudaEventRecordWithFlags(e, t, cudaEventRecordExternal);
+    else cudaEventRecord(e, t);
+  };
+  if (ev) mark(ev[0], origin);
+  cudaError_t err = cudaEventRecord(h->ev_in, origin);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sco, h->ev_in, 0);
+  if (err == cudaSuccess) err = launch_append_step(sh, st, args, h->s_sco);
+  if (err == cudaSuccess && capture && append_node) {
+    cudaStreamCaptureStatus cs;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t nd = 0;
+    err = cudaStreamGetCaptureInfo(h->s_sco, &cs, nullptr, nullptr, &deps, nullptr, &nd);
+    if (err == cudaSuccess && (nd != 1 || cs != cudaStreamCaptureStatusActive))
+      err = cudaErrorStreamCaptureInvalidated;
+    if (err == cudaSuccess) *append_node = deps[0];
   }
-  const int L_old = (int)h->L;
-  const int N = L_old / sh.B;                       // candidates after the append
-  const int T = L_old + 1 - N * sh.B;               // tokens in the tail block
-  const int jc = (L_old % sh.B == 0) ? N - 1 : -1;  // block that just became a candidate
-  const bool cold = (h->steps == 0);
-  // The units are processed in chunks that form a pipeline over four internal
-  // streams: scoring and selection of chunk c+1 (HBM) run while chunk c's
-  // gather (host link) and its attention over kept slots (HBM) run; attention
-  // over the filled slots of chunk c follows its gather. The caller's stream
-  // forks at the start and joins at the end.
-  h->launches += 1 + h->nchunks * ((N > 0 ? 1 : 0) + 4);  // append; per chunk score, select, gather, 2 x attention
-  cudaError_t err = cudaEventRecord(h->ev_in, s);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sel, h->ev_in, 0);
-  if (err == cudaSuccess) err = launch_append_step(sh, st, k_new, v_new, e_new, L_old, h->s_sel);
-  if (ev) cudaEventRecord(ev[1], h->s_sel);
+  if (ev) mark(ev[1], h->s_sco);
+  // Scoring of every chunk back to back on one stream; each chunk's selection
+  // on another, as soon as its scores exist.
   for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
-    err = launch_score(sh, st, q, N, h->cu_base[c], h->cu_count[c], h->s_sel);
+    err = launch_score(sh, st, n_cap, h->cu_base[c], h->cu_count[c], h->s_sco);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_sco[c], h->s_sco);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sel, h->ev_sco[c], 0);
     if (err == cudaSuccess)
-      err = launch_select_setdiff(sh, st, N, jc, cold ? 1 : 0, h->cu_base[c], h->cu_count[c], c,
-                                  h->s_sel);
+      err = launch_select_setdiff(sh, st, cold ? 1 : 0, h->cu_base[c], h->cu_count[c], c, h->s_sel);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_sel[c], h->s_sel);
   }
-  if (ev) cudaEventRecord(ev[2], h->s_sel);
+  if (ev) mark(ev[2], h->s_sel);
   AttnArgs a;
   a.units = st.slots;
   a.n_units = (long long)sh.U * sh.k;
   a.n_blocks = sh.k;
   a.tail_stride = 2 * sh.payload;
-  a.tail_len = T;
-  a.q = q;
-  a.out = out;
-  a.lse = lse;
+  a.tail_len = 0;  // from StepIO
+  a.q = nullptr;
+  a.out = nullptr;
+  a.lse = nullptr;
+  a.dyn = st.io;
   a.part_acc = st.part_acc;
   a.part_ml = st.part_ml;
   a.counters = st.att_cnt;
@@ -590,16 +694,16 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
     a.unit_count = h->cu_count[c];
     // gather of chunk c (host link)
     err = cudaStreamWaitEvent(h->s_gat, h->ev_sel[c], 0);
-    if (ev && c == 0) cudaEventRecord(ev[4], h->s_gat);
+    if (ev && c == 0) mark(ev[4], h->s_gat);
     if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], c, h->s_gat);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], h->s_gat);
-    if (ev && c == h->nchunks - 1) cudaEventRecord(ev[5], h->s_gat);
+    if (ev && c == h->nchunks - 1) mark(ev[5], h->s_gat);
     // attention over the slots kept from the previous step, plus the tail
     if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_att, h->ev_sel[c], 0);
-    if (ev && c == 0) cudaEventRecord(ev[3], h->s_att);
+    if (ev && c == 0) mark(ev[3], h->s_att);
     if (err == cudaSuccess) {
       a.block_tab = st.block_tab;
-      a.tail = st.tail + (long long)(N & 1) * sh.payload;
+      a.tail = st.tail;  // + StepIO::tail_off
       a.nsplit = ns_kept;
       a.split_base = 0;
       err = launch_attention(sh, a, h->s_att);
@@ -614,13 +718,123 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
       err = launch_attention(sh, a, h->s_new);
     }
   }
-  if (ev) cudaEventRecord(ev[6], h->s_att);
+  if (ev) mark(ev[6], h->s_att);
   if (err == cudaSuccess) err = cudaEventRecord(h->ev_att, h->s_att);
   if (err == cudaSuccess) err = cudaEventRecord(h->ev_new, h->s_new);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(s, h->ev_att, 0);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(s, h->ev_new, 0);
-  if (ev) cudaEventRecord(ev[7], s);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_att, 0);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_new, 0);
+  if (capture) {
+    // A capture must join every stream it forked, including their last nodes.
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_jsco, h->s_sco);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jsco, 0);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_jsel, h->s_sel);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_jgat, h->s_gat);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jsel, 0);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jgat, 0);
+  }
+  if (ev) mark(ev[7], origin);
+  return err;
+}
+
+// Captures a warm step into g (replacing what it held) with these arguments.
+cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args, int N,
+                             cudaEvent_t* ev) {
+  if (g.done == nullptr) {
+    const cudaError_t e = cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  } else if (g.exec != nullptr) {
+    const cudaError_t e = cudaEventSynchronize(g.done);  // its last launch has finished
+    if (e != cudaSuccess) return e;
+  }
+  if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (g.graph) cudaGraphDestroy(g.graph);
+  g.exec = nullptr;
+  g.graph = nullptr;
+  const int n_cap = (N / kScoreCap + 1) * kScoreCap;
+  cudaError_t err = cudaStreamBeginCapture(h->s_cap, cudaStreamCaptureModeRelaxed);
+  if (err != cudaSuccess) return err;
+  cudaGraphNode_t node = nullptr;
+  const cudaError_t e_enq = enqueue_step(h, h->s_cap, args, n_cap, false, ev, true, &node);
+  cudaGraph_t graph = nullptr;
+  err = cudaStreamEndCapture(h->s_cap, &graph);
+  if (e_enq != cudaSuccess) err = e_enq;
+  if (err == cudaSuccess)
+    err = cudaGraphInstantiateWithFlags(&g.exec, graph, cudaGraphInstantiateFlagUseNodePriority);
+  if (err == cudaSuccess) err = cudaGraphKernelNodeGetParams(node, &g.append_params);
+  if (err != cudaSuccess) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (graph) cudaGraphDestroy(graph);
+    g.exec = nullptr;
+    return err;
+  }
+  g.graph = graph;
+  g.append_node = node;
+  g.n_cap = n_cap;
+  h->graph_builds += 1;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
+                             const float* e_new, void* out, float* lse, void* stream) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  if (h->broken) return h->fail(NOSA_ERR_STATE, "handle unusable after an earlier CUDA error");
+  if (h->L < 1) return h->fail(NOSA_ERR_STATE, "decode step before any context was appended");
+  if (h->L + 1 > h->cfg.max_context) return h->fail(NOSA_ERR_CAPACITY, "context is full");
+  if (!q || !k_new || !v_new || !e_new || !out) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
+      !aligned(e_new, 4) || (lse && !aligned(lse, 4)))
+    return h->fail(NOSA_ERR_INVALID_ARG, "q, k_new, v_new, out need 16-byte alignment");
+  DeviceGuard guard(h->cfg.device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Shape& sh = h->s;
+  StepArgs args;
+  args.k_new = k_new;
+  args.v_new = v_new;
+  args.e_new = e_new;
+  args.q = q;
+  args.out = out;
+  args.lse = lse;
+  args.L_old = (int)h->L;
+  const int N = args.L_old / sh.B;  // candidates after the append
+  const bool cold = (h->steps == 0);
+  cudaError_t err = cudaSuccess;
+  if (h->use_graphs && !cold && N > 0) {
+    const int r = h->timing ? h->graph_pos : 0;
+    StepGraph& g = h->timing ? h->graphs[r] : h->plain;
+    cudaEvent_t* ev = h->timing ? h->gev[r] : nullptr;
+    if (h->timing) harvest_set(h, ev, &g.pending);
+    if (g.exec == nullptr || N >= g.n_cap || N < g.n_cap - kScoreCap) {
+      err = build_step_graph(h, g, args, N, ev);
+    } else {
+      cudaKernelNodeParams kp = g.append_params;
+      void* kargs[3] = {const_cast<Shape*>(&h->s), &h->st, &args};
+      kp.kernelParams = kargs;
+      kp.extra = nullptr;
+      err = cudaGraphExecKernelNodeSetParams(g.exec, g.append_node, &kp);
+    }
+    if (err == cudaSuccess) err = cudaGraphLaunch(g.exec, s);
+    if (err == cudaSuccess) err = cudaEventRecord(g.done, s);
+    if (err == cudaSuccess && h->timing) {
+      g.pending = true;
+      h->graph_pos = (r + 1) % kGraphRing;
+    }
+  } else {
+    cudaEvent_t* ev = nullptr;
+    if (h->timing) {
+      const int r = h->ring_pos;
+      harvest(h, r);
+      ev = h->ev[r];
+      h->pending[r] = true;
+      h->ring_pos = (r + 1) % kRing;
+    }
+    err = enqueue_step(h, s, args, N, cold, ev, false, nullptr);
+  }
   if (err != cudaSuccess) return h->cuda_fail(err, "decode step launch");
+  h->launches += 1 + h->nchunks * ((N > 0 ? 1 : 0) + 4);  // append; per chunk score, select, gather, 2 x attention
   h->L += 1;
   h->steps += 1;
   h->last_stream = s;
@@ -632,8 +846,7 @@ nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out) {
   DeviceGuard guard(h->cfg.device);
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
-  if (h->timing)
-    for (int r = 0; r < kRing; ++r) harvest(h, r);
+  harvest_all(h);
   DevStats ds;
   e = cudaMemcpy(&ds, h->st.stats, sizeof(ds), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return h->cuda_fail(e, "stats read");
@@ -663,8 +876,7 @@ nosa_status nosa_stats_reset(nosa_handle* h) {
   DeviceGuard guard(h->cfg.device);
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
-  if (h->timing)
-    for (int r = 0; r < kRing; ++r) harvest(h, r);
+  harvest_all(h);
   DevStats old;
   e = cudaMemcpy(&old, h->st.stats, sizeof(old), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return h->cuda_fail(e, "stats read");
@@ -675,6 +887,19 @@ nosa_status nosa_stats_reset(nosa_handle* h) {
   std::memset(h->t_us, 0, sizeof(h->t_us));
   h->t_count = 0;
   h->launches = 0;
+  return NOSA_OK;
+}
+
+nosa_status nosa_set_timing(nosa_handle* h, int32_t on) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  if (!on) {
+    h->timing = false;
+    return NOSA_OK;
+  }
+  DeviceGuard guard(h->cfg.device);
+  const cudaError_t e = make_timing_events(h);
+  if (e != cudaSuccess) return h->cuda_fail(e, "event creation");
+  h->timing = true;
   return NOSA_OK;
 }
 

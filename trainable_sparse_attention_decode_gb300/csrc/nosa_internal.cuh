@@ -41,6 +41,31 @@ struct DevStats {
   int pad_;
 };
 
+// Arguments of one decode step. The append kernel (the step's first kernel)
+// receives them by value and publishes StepIO for every kernel after it, so a
+// captured step graph needs new arguments on its first node only.
+struct StepArgs {
+  const void* k_new;   // [batch][Hkv][d]
+  const void* v_new;   // [batch][Hkv][d]
+  const float* e_new;  // [batch][Hkv]
+  const void* q;       // [batch][Hq][d]
+  void* out;           // [batch][Hq][d]
+  float* lse;          // [batch][Hq] or null
+  int L_old;           // context before this step's token
+};
+
+// Per-step values derived from StepArgs (device-resident, written by the append kernel).
+struct StepIO {
+  const void* q;
+  void* out;
+  float* lse;
+  int L_old;
+  int n_cand;          // candidate blocks after the append: L_old / B
+  int tail_len;        // tokens in the tail block after the append (1..B)
+  int just_completed;  // block that just became a candidate, else -1
+  long long tail_off;  // byte offset of the tail block's buffer: (n_cand % 2) * payload
+};
+
 struct State {
   uint8_t* slots;      // [U][k] block units (device)
   uint8_t* tail;       // [U][2] block units (device); block b lives in buffer b % 2
@@ -65,23 +90,24 @@ struct State {
   float* part_acc;     // split-K partial accumulators
   float* part_ml;      // split-K partial (max, sum)
   DevStats* stats;
+  StepIO* io;          // the current decode step's arguments
 };
 
 // ---------------------------------------------------------------------------
 // Host-side launchers (each returns the launch error, if any).
 // ---------------------------------------------------------------------------
-cudaError_t launch_append_step(const Shape& s, const State& st, const void* k_new,
-                               const void* v_new, const float* e_new, int L_old,
+cudaError_t launch_append_step(const Shape& s, const State& st, const StepArgs& a,
                                cudaStream_t stream);
 cudaError_t launch_promote_tail(const Shape& s, const State& st, int blk, cudaStream_t stream);
 cudaError_t launch_append_bulk(const Shape& s, const State& st, const void* k, const void* v,
                                const float* e, int L_old, int n, cudaStream_t stream);
-// The per-unit kernels below handle units [ubase, ubase + ucount) of one chunk.
-cudaError_t launch_score(const Shape& s, const State& st, const void* q, int n_cand, int ubase,
-                         int ucount, cudaStream_t stream);
-cudaError_t launch_select_setdiff(const Shape& s, const State& st, int n_cand,
-                                  int just_completed, int cold, int ubase, int ucount, int chunk,
-                                  cudaStream_t stream);
+// The per-unit kernels below handle units [ubase, ubase + ucount) of one chunk
+// and read the step's query, candidate count and tail from State::io. The score
+// grid covers n_cap >= n_cand candidates (surplus CTAs return at once).
+cudaError_t launch_score(const Shape& s, const State& st, int n_cap, int ubase, int ucount,
+                         cudaStream_t stream);
+cudaError_t launch_select_setdiff(const Shape& s, const State& st, int cold, int ubase,
+                                  int ucount, int chunk, cudaStream_t stream);
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
                           cudaStream_t stream);
 // result[0] = error code of a bounded wait that nothing completes, result[1] = ms waited.
@@ -113,6 +139,9 @@ struct AttnArgs {
   int unit_count;
   int* counters;            // [U]
   int* err;                 // device error word
+  // Decode step: q, out, lse and tail_len come from *dyn, and the tail pointer
+  // (when not null) is offset by dyn->tail_off. Null for the standalone call.
+  const StepIO* dyn = nullptr;
 };
 size_t attention_workspace_bytes(const Shape& s, int nsplit);
 int attention_pick_nsplit(const Shape& s, int n_blocks, int has_tail);
