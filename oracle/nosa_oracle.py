@@ -37,6 +37,12 @@ the plainest reading and says so at the spot (readings R1..R20):
       old tail buffer (TAIL), every other load from the host store (HOST).
 * R14 Decisions that turn floating point into indices (the top-k cuts) are taken
       in fp32, the kernels' precision: the fp64 score is rounded to fp32 first.
+* R21 Fused front-end: the eviction head is a linear map of the layer's hidden
+      state, one pre-exp logit per KV head; its rows are packed after the query,
+      key and value rows of the layer's projection, W [F][D] with
+      F = (Hq + 2 Hkv) d + Hkv (query heads, key heads, value heads, eviction).
+* R22 The projected q, k, v are stored in the handle's dtype (fp64 -> fp32 ->
+      bf16, nearest even) and e in fp32, like the inputs of the plain step.
 
 Every other quantity is fp64.
 """
@@ -52,6 +58,7 @@ __all__ = [
     "HOST", "TAIL", "pool_block", "group_query", "block_scores", "decision_values",
     "top_m", "dual_select", "set_difference", "attend", "encode_payload",
     "payload_bytes", "UnitOracle", "pooled_keys_bf16", "round_bf16",
+    "frontend_rows", "project", "frontend_storage",
 ]
 
 
@@ -226,6 +233,58 @@ def encode_payload(k_raw: np.ndarray, v_raw: np.ndarray, e: np.ndarray, dtype: s
     out[kb.size:kb.size + vb.size] = vb
     out[kb.size + vb.size:kb.size + vb.size + eb.size] = eb
     return out
+
+
+# ----------------------------------------------------------------------------
+# Methodology §1 Dual-Selection (the eviction head scores tokens independently
+# of the query) and §2 Kernel Fusion (eviction head, QKV split and pooling in
+# one kernel): the front-end that produces a decode step's q, k, v and e from
+# the layer's hidden states (R21, R22). The pooling that follows is the unit
+# state machine below, unchanged.
+# ----------------------------------------------------------------------------
+def frontend_rows(n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+    """Rows F of the packed projection: query, key and value heads, then eviction rows."""
+    return (n_q_heads + 2 * n_kv_heads) * head_dim + n_kv_heads
+
+
+def project(x: np.ndarray, W: np.ndarray, n_q_heads: int, n_kv_heads: int, head_dim: int):
+    """y = W x for every request, split into the step's inputs (R21).
+
+    x [batch][D] and W [F][D] (fp64). Returns q [batch][Hq][d], k and v
+    [batch][Hkv][d], e [batch][Hkv], all fp64 and unrounded: rows [0, Hq d) are
+    query head g = row // d, dim = row % d; the next Hkv d rows are the key heads,
+    the next Hkv d the value heads; the last Hkv rows the eviction logits.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    assert W.shape == (frontend_rows(n_q_heads, n_kv_heads, head_dim), x.shape[1])
+    y = x @ W.T
+    nb, d = x.shape[0], head_dim
+    fq = n_q_heads * d
+    fk = fq + n_kv_heads * d
+    fv = fk + n_kv_heads * d
+    q = y[:, :fq].reshape(nb, n_q_heads, d)
+    k = y[:, fq:fk].reshape(nb, n_kv_heads, d)
+    v = y[:, fk:fv].reshape(nb, n_kv_heads, d)
+    e = y[:, fv:]
+    return q, k, v, e
+
+
+def _bf16_bits(x64: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 (nearest even) -> bf16 (nearest even), as uint16 bit patterns."""
+    b = np.asarray(x64, dtype=np.float64).astype(np.float32).view(np.uint32)
+    r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def frontend_storage(q, k, v, e, dtype: str):
+    """Stored forms of the projected inputs (R22): q, k, v in dtype (bf16 as
+    uint16 bit patterns), e in fp32."""
+    if dtype == "f32":
+        conv = lambda a: np.asarray(a, dtype=np.float64).astype(np.float32)
+    else:
+        conv = _bf16_bits
+    return conv(q), conv(k), conv(v), np.asarray(e, dtype=np.float64).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------

@@ -25,6 +25,13 @@ checked against this file bit for bit):
   ``q_s = rho * q_{s-1} + eps_s`` in fp64 (a product, then a sum: no fused
   multiply-add), stored as fp64 -> fp32 (RNE) -> dtype.
 * bf16 storage rounds fp32 to nearest even.
+* Front-end inputs (hidden states and the packed projection weights): small
+  integers ``(word % 17) - 8`` from word ``j = 0`` of the counter, scaled by
+  ``2**-3`` (hidden states, counter ``(5, b, 0, t, 4*i)``) and ``2**-8`` (weights,
+  counter ``(6, 0, 0, row, 4*col)``). Every product is an integer multiple of
+  ``2**-11`` below ``2**-5`` in magnitude, so every partial sum of a projection
+  with fewer than ``2**18`` terms is exact in fp32, whatever the order of the
+  additions: the projected values are then the same bits on any correct path.
 
 The GPU kernels never see this module's code; they get the arrays it (or its
 CUDA twin) writes.
@@ -38,6 +45,7 @@ __all__ = [
     "Workload", "WORKLOADS", "splitmix64", "normals", "keys", "values", "evict",
     "queries", "to_storage", "storage_to_f64", "bf16_bits_to_f64",
     "STREAM_CENTER", "STREAM_KNOISE", "STREAM_VALUE", "STREAM_EVICT", "STREAM_QINNOV",
+    "STREAM_HIDDEN", "STREAM_WEIGHT", "small_ints", "hidden", "proj_weights", "hidden_width",
 ]
 
 _M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
@@ -50,6 +58,10 @@ STREAM_KNOISE = 1
 STREAM_VALUE = 2
 STREAM_EVICT = 3
 STREAM_QINNOV = 4
+STREAM_HIDDEN = 5
+STREAM_WEIGHT = 6
+HIDDEN_SCALE = 2.0 ** -3
+WEIGHT_SCALE = 2.0 ** -8
 
 IH_MEAN = 393210          # 12 * 65535 / 2
 IH_SCALE = 1.0 / 65536.0  # exact power of two
@@ -196,3 +208,37 @@ def queries(w: Workload, b: int, heads, steps: int) -> np.ndarray:
             q = q + eps
         out[s] = to_storage(q, w.dtype)
     return out
+
+
+def small_ints(seed: int, stream: int, a, h, t, col) -> np.ndarray:
+    """Integers in [-8, 8]: (word % 17) - 8 of word j = 0 of the counter (int64)."""
+    smix = splitmix64(np.uint64(seed))
+    c = _counter(stream, a, h, t, np.asarray(col, dtype=np.uint64) * np.uint64(4))
+    w = splitmix64(c ^ smix)
+    return (w % np.uint64(17)).astype(np.int64) - 8
+
+
+def hidden_width(w: Workload) -> int:
+    """Width D of the hidden states fed to the front-end: n_q_heads * head_dim."""
+    return w.n_q_heads * w.head_dim
+
+
+def hidden(w: Workload, b: int, t0: int, n: int, D: int | None = None) -> np.ndarray:
+    """Hidden states of request b for tokens [t0, t0+n): [n][D] fp64 (exact in bf16)."""
+    D = hidden_width(w) if D is None else D
+    t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
+    col = np.arange(D, dtype=np.int64)[None, :]
+    return small_ints(w.seed, STREAM_HIDDEN, b, 0, t, col).astype(np.float64) * HIDDEN_SCALE
+
+
+def proj_weights(w: Workload, D: int | None = None, rows=None) -> np.ndarray:
+    """Packed front-end weights [F][D] fp64 (exact in bf16), or the given rows of it.
+
+    F = (n_q_heads + 2 n_kv_heads) head_dim + n_kv_heads: query heads, key heads,
+    value heads, then one eviction-head row per KV head.
+    """
+    D = hidden_width(w) if D is None else D
+    F = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim + w.n_kv_heads
+    r = np.arange(F, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    col = np.arange(D, dtype=np.int64)[None, :]
+    return small_ints(w.seed, STREAM_WEIGHT, 0, 0, r[:, None], col).astype(np.float64) * WEIGHT_SCALE

@@ -344,3 +344,64 @@ def test_pooled_bf16_follows_fp32_token_order():
     kb = O.pooled_keys_bf16(k, 16)
     assert kb[0, 0] == 0.0 and kb[0, 1] == 0.875
     assert O.pool_block(k, np.zeros(64), 16)[0][0, 0] == 0.875
+
+
+# --------------------------------------------------------------------------
+# Fused front-end: the packed projection and its split (R21, R22)
+# --------------------------------------------------------------------------
+def test_project_split_layout_one_hot():
+    # W[r] picks hidden element r % D: each output names the row it came from.
+    Hq, Hkv, d, D = 4, 2, 4, 64
+    F = O.frontend_rows(Hq, Hkv, d)
+    assert F == (4 + 4) * 4 + 2
+    W = np.zeros((F, D))
+    W[np.arange(F), np.arange(F) % D] = 1.0
+    x = np.stack([np.arange(D) + 1000.0 * b for b in range(3)])
+    q, k, v, e = O.project(x, W, Hq, Hkv, d)
+    for b in range(3):
+        for g in range(Hq):
+            for dim in range(d):
+                assert q[b, g, dim] == x[b, (g * d + dim) % D]
+        for h in range(Hkv):
+            for dim in range(d):
+                assert k[b, h, dim] == x[b, (Hq * d + h * d + dim) % D]
+                assert v[b, h, dim] == x[b, ((Hq + Hkv) * d + h * d + dim) % D]
+            assert e[b, h] == x[b, ((Hq + 2 * Hkv) * d + h) % D]
+
+
+def test_project_matches_integer_arithmetic():
+    # The generator's hidden states and weights are small integers times powers
+    # of two: the exact result is an integer dot product.
+    w = synth.WORKLOADS["1b-bf16"]
+    D = synth.hidden_width(w)
+    rows = np.arange(0, O.frontend_rows(w.n_q_heads, w.n_kv_heads, w.head_dim), 37)
+    xi = synth.small_ints(w.seed, synth.STREAM_HIDDEN, 3, 0, np.array([[70000]]),
+                          np.arange(D)[None, :])[0]
+    Wi = synth.small_ints(w.seed, synth.STREAM_WEIGHT, 0, 0, rows[:, None], np.arange(D)[None, :])
+    exact = [sum(int(a) * int(c) for a, c in zip(xi, Wi[j])) * 2.0 ** -11 for j in range(len(rows))]
+    x = synth.hidden(w, 3, 70000, 1, D)
+    Wf = np.zeros((O.frontend_rows(w.n_q_heads, w.n_kv_heads, w.head_dim), D))
+    Wf[rows] = synth.proj_weights(w, D, rows)
+    q, k, v, e = O.project(x, Wf, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    y = np.concatenate([q.reshape(-1), k.reshape(-1), v.reshape(-1), e.reshape(-1)])
+    assert list(y[rows]) == exact
+    # Any fp32 summation order gives the same bits (every partial sum is exact).
+    rng = np.random.default_rng(0)
+    prod = (x[0][None, :] * Wf[rows]).astype(np.float32)
+    for _ in range(3):
+        perm = rng.permutation(D)
+        acc = np.zeros(len(rows), dtype=np.float32)
+        for i in perm:
+            acc = np.add(acc, prod[:, i], dtype=np.float32)
+        assert list(acc.astype(np.float64)) == exact
+
+
+def test_frontend_storage_rounds_to_nearest_even():
+    # ties to even; a value above the tie rounds up; and R22's fp32 step first:
+    # 2**-30 does not survive fp64 -> fp32, so that value is a tie in bf16.
+    q = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 1.0 + 2 ** -8 + 2 ** -20,
+                  1.0 + 2 ** -8 + 2 ** -30])
+    qs, ks, vs, es = O.frontend_storage(q, q, q, q, "bf16")
+    vals = (qs.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    assert list(vals) == [1.0, 1.0 + 2 ** -6, -2.5, 1.0 + 2 ** -7, 1.0]
+    assert es.dtype == np.float32 and es[0] == np.float32(1.0 + 2 ** -8)
