@@ -157,6 +157,39 @@ nosa_status nosa_append_kv(nosa_handle* h, int32_t n_tokens, const void* k, cons
 nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
                              const float* e_new, void* out, float* lse, void* stream);
 
+/*
+ * Fused front-end (NOSA technical summary, Methodology §2 "Kernel Fusion": the
+ * eviction head, the QKV split and the pooling in one kernel; §1 "Dual-Selection
+ * Mechanism": the eviction head scores tokens independently of the query).
+ *
+ * Rows of the packed projection for this configuration:
+ * F = (n_q_heads + 2 * n_kv_heads) * head_dim + n_kv_heads (0 if cfg is invalid).
+ */
+size_t nosa_frontend_rows(const nosa_config* cfg);
+
+/*
+ * One decode step whose inputs are projected from the layer's hidden states by
+ * the library: y = W x for every request, split into the query heads (rows
+ * [0, Hq d): head g = row / d), the key heads (next Hkv d rows), the value
+ * heads (next Hkv d rows) and the eviction logits (last Hkv rows, one pre-exp
+ * logit per KV head); q, k, v are rounded to bf16 (nearest even), e stays fp32.
+ * The projection runs on the tensor cores (fp32 accumulation; the order of the
+ * additions is unspecified) in the same kernel as the append and the pooling;
+ * the rest of the step is nosa_decode_step's.
+ *   x      : device bf16 [batch][hidden], row-major (the step's hidden states)
+ *   hidden : width D, a multiple of 64 in [64, 65536]
+ *   w      : device bf16 [F][hidden], row-major (F = nosa_frontend_rows), read only
+ *   q_out  : device bf16 [batch][n_q_heads][head_dim] receiving the step's
+ *            queries, or NULL (then they stay in an internal buffer)
+ *   out, lse, stream: as for nosa_decode_step.
+ * x, w, q_out and out need 16-byte alignment. UNSUPPORTED unless cfg->dtype is
+ * NOSA_BF16 and batch <= 256 (or when the driver offers no tensor-map encoder);
+ * OOM if the front-end's scratch (split partials, about ksplit * batch * F * 4
+ * bytes) cannot be allocated on the first call. Other errors as nosa_decode_step.
+ */
+nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden, const void* w,
+                                    void* q_out, void* out, float* lse, void* stream);
+
 /* Counters, host-readable. gamma_* covers steps after the first decode step
  * with at least k candidates; gamma(t) = |Gamma(t) ∩ R(t-1)| / k where R(t-1)
  * is the resident blocks plus the block that was the tail at t-1. */

@@ -78,6 +78,38 @@ __global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, 
   }
 }
 
+// Integer in [-8, 8] from word j = 0 of the counter (front-end inputs).
+__device__ __forceinline__ int small_int(uint64_t smix, uint64_t stream, uint64_t a, uint64_t h,
+                                         uint64_t t, uint64_t col) {
+  const uint64_t base = (stream << 61) | (a << 51) | (h << 44) | (t << 18) | (col * 4);
+  return (int)(splitmix64(base ^ smix) % 17ull) - 8;
+}
+
+// x: [n][batch][D] bf16 hidden states of tokens t0 .. t0+n-1 (integers x 2^-3).
+__global__ void hidden_kernel(__nv_bfloat16* x, int batch, int D, long long t0, int n,
+                              uint64_t smix) {
+  const long long total = (long long)n * batch * D;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int col = (int)(i % D);
+    const long long r = i / D;
+    const int b = (int)(r % batch);
+    const long long t = t0 + r / batch;
+    x[i] = __float2bfloat16_rn((float)small_int(smix, 5, b, 0, t, col) * 0.125f);
+  }
+}
+
+// W: [F][D] bf16 packed front-end weights (integers x 2^-8).
+__global__ void weight_kernel(__nv_bfloat16* W, int F, int D, uint64_t smix) {
+  const long long total = (long long)F * D;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int col = (int)(i % D);
+    const long long row = i / D;
+    W[i] = __float2bfloat16_rn((float)small_int(smix, 6, 0, 0, row, col) * 0.00390625f);
+  }
+}
+
 uint64_t seed_mix(uint64_t seed) {
   uint64_t x = seed + 0x9E3779B97F4A7C15ull;
   x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
@@ -119,6 +151,25 @@ int synth_queries(void* q, int batch, int hq, int d, int steps, double rho,
   else
     q_kernel<__nv_bfloat16><<<(total + 127) / 128, 128, 0, s>>>((__nv_bfloat16*)q, batch, hq, d,
                                                                  steps, rho, smix);
+  return (int)cudaGetLastError();
+}
+
+int synth_hidden(void* x, int batch, int D, long long t0, int n, unsigned long long seed,
+                 void* stream) {
+  const long long total = (long long)n * batch * D;
+  if (total == 0) return 0;
+  const long long want = (total + 255) / 256;
+  hidden_kernel<<<(int)(want < 65536 ? want : 65536), 256, 0, (cudaStream_t)stream>>>(
+      (__nv_bfloat16*)x, batch, D, t0, n, seed_mix(seed));
+  return (int)cudaGetLastError();
+}
+
+int synth_proj_weights(void* W, int F, int D, unsigned long long seed, void* stream) {
+  const long long total = (long long)F * D;
+  if (total == 0) return 0;
+  const long long want = (total + 255) / 256;
+  weight_kernel<<<(int)(want < 65536 ? want : 65536), 256, 0, (cudaStream_t)stream>>>(
+      (__nv_bfloat16*)W, F, D, seed_mix(seed));
   return (int)cudaGetLastError();
 }
 

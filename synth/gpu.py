@@ -41,6 +41,11 @@ def _get():
         L.synth_kv.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                C.c_longlong, C.c_int, C.c_int, C.c_ulonglong, C.c_int, C.c_int,
                                C.c_void_p]
+        L.synth_hidden.restype = C.c_int
+        L.synth_hidden.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_longlong, C.c_int,
+                                   C.c_ulonglong, C.c_void_p]
+        L.synth_proj_weights.restype = C.c_int
+        L.synth_proj_weights.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_ulonglong, C.c_void_p]
         L.synth_queries.restype = C.c_int
         L.synth_queries.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double,
                                     C.c_ulonglong, C.c_int, C.c_void_p]
@@ -86,3 +91,30 @@ def queries(w: Workload, steps: int, device="cuda"):
     if err:
         raise RuntimeError(f"synth_queries: CUDA error {err}")
     return q
+
+
+def hidden(w: Workload, t0: int, n: int, D: int | None = None, device="cuda"):
+    """Front-end hidden states of tokens t0..t0+n-1: [n][batch][D] bf16 (token-major)."""
+    import torch
+    from . import hidden_width
+    D = hidden_width(w) if D is None else D
+    x = torch.empty((n, w.batch, D), dtype=torch.bfloat16, device=device)
+    err = _get().synth_hidden(x.data_ptr(), w.batch, D, t0, n, w.seed,
+                              torch.cuda.current_stream().cuda_stream)
+    if err:
+        raise RuntimeError(f"synth_hidden: CUDA error {err}")
+    return x
+
+
+def proj_weights(w: Workload, D: int | None = None, device="cuda"):
+    """Packed front-end weights [F][D] bf16 (query, key, value heads, eviction rows)."""
+    import torch
+    from . import hidden_width
+    D = hidden_width(w) if D is None else D
+    F = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim + w.n_kv_heads
+    W = torch.empty((F, D), dtype=torch.bfloat16, device=device)
+    err = _get().synth_proj_weights(W.data_ptr(), F, D, w.seed,
+                                    torch.cuda.current_stream().cuda_stream)
+    if err:
+        raise RuntimeError(f"synth_proj_weights: CUDA error {err}")
+    return W

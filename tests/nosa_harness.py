@@ -156,6 +156,21 @@ class GpuRun:
         self.step_idx += 1
         if not check:
             return out, lse, {}
+        t = w.prompt + s
+
+        def tokens(b, hh):
+            return (synth.keys(w, b, hh, t, 1)[0], synth.values(w, b, hh, t, 1)[0],
+                    synth.evict(w, b, hh, t, 1)[0])
+
+        return out, lse, self.check_units(s, out, lse, tokens, lambda b, hh: self.q_oracle(b, hh, s))
+
+    def check_units(self, s, out, lse, tokens, q_group):
+        """Advances every sampled unit's oracle by one step and compares it with the GPU.
+
+        tokens(b, hh) -> the step's stored (k, v, e) of unit (b, hh);
+        q_group(b, hh) -> the stored queries of its G query heads.
+        """
+        w = self.w
         res = {"worst_attn": 0.0, "worst_lse": 0.0}
         do_attn = (s % self.attn_every == 0)
         out_np, lse_np = (to_f64(out), lse.cpu().numpy().astype(np.float64)) if do_attn else (None, None)
@@ -163,10 +178,8 @@ class GpuRun:
         for u in self.units:
             b, hh = divmod(u, w.n_kv_heads)
             uo = self.oracles[u]
-            t = w.prompt + s
-            uo.begin_step(synth.keys(w, b, hh, t, 1)[0], synth.values(w, b, hh, t, 1)[0],
-                          synth.evict(w, b, hh, t, 1)[0])
-            qg = self.q_oracle(b, hh, s)
+            uo.begin_step(*tokens(b, hh))
+            qg = q_group(b, hh)
             sq64, se64 = uo.scores(qg)
             n = uo.n_cand
             ne, nq = nsel_all[u]
@@ -200,7 +213,7 @@ class GpuRun:
                 rows = slice(hh * self.G, (hh + 1) * self.G)
                 res["worst_attn"] = max(res["worst_attn"], attn_close(out_np[b, rows], o_ref, w.dtype))
                 res["worst_lse"] = max(res["worst_lse"], float(np.max(np.abs(lse_np[b, rows] - lse_ref))))
-        return out, lse, res
+        return res
 
     def q_oracle(self, b, hh, s):
         key = (b, hh)
@@ -216,3 +229,50 @@ class GpuRun:
 
     def close(self):
         nosa.nosa_destroy(self.h)
+
+
+class FrontRun(GpuRun):
+    """GpuRun whose decode steps start from hidden states (the fused front-end).
+
+    The prompt is appended as in GpuRun; every decode step projects the
+    generator's hidden states with the packed weights. The oracle projects the
+    same inputs itself (fp64, then the stored forms) and the GPU's queries are
+    compared bit for bit with it before the unit checks.
+    """
+
+    def __init__(self, w, units=None, D=None, **kw):
+        super().__init__(w, units=units, **kw)
+        self.D = synth.hidden_width(w) if D is None else D
+        self.W_dev = synth.gpu.proj_weights(w, self.D)
+        self.W64 = synth.proj_weights(w, self.D)
+        self.requests = sorted({u // w.n_kv_heads for u in self.units})
+
+    def step_hidden(self, check=True):
+        w, s = self.w, self.step_idx
+        t = w.prompt + s
+        x = synth.gpu.hidden(w, t, 1, self.D)[0]
+        out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.batch, w.n_q_heads), dtype=torch.float32, device="cuda")
+        q_out = torch.empty_like(out)
+        nosa.nosa_decode_step_hidden(self.h, x, self.W_dev, out, lse, q_out=q_out)
+        torch.cuda.synchronize()
+        self.step_idx += 1
+        if not check:
+            return out, lse, {}
+        proj = {}
+        q_gpu = q_out.view(torch.int16).cpu().numpy().view(np.uint16)
+        for b in self.requests:
+            x64 = synth.hidden(w, b, t, 1, self.D)
+            q, k, v, e = O.project(x64, self.W64, w.n_q_heads, w.n_kv_heads, w.head_dim)
+            qs, ks, vs, es = O.frontend_storage(q, k, v, e, "bf16")
+            assert np.array_equal(q_gpu[b], qs[0]), f"step {s}: projected queries of request {b} differ"
+            proj[b] = (qs[0], ks[0], vs[0], es[0])
+
+        def tokens(b, hh):
+            _, ks, vs, es = proj[b]
+            return ks[hh], vs[hh], es[hh]
+
+        def q_group(b, hh):
+            return proj[b][0][hh * self.G:(hh + 1) * self.G]
+
+        return out, lse, self.check_units(s, out, lse, tokens, q_group)

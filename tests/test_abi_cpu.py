@@ -101,3 +101,10 @@ def test_create_without_gpu_fails_cleanly():
 
 def test_workspace_query_rejects_bad_config():
     assert nosa.nosa_attention_workspace_bytes(_cfg(k_e=99), 8) == 0
+
+
+def test_frontend_rows():
+    cfg = nosa.nosa_config(32, 32, 8, 128, "bf16", 64, 48, 70000)
+    assert nosa.nosa_frontend_rows(cfg) == (32 + 16) * 128 + 8
+    bad = nosa.nosa_config(32, 30, 8, 128, "bf16", 64, 48, 70000)
+    assert nosa.nosa_frontend_rows(bad) == 0

@@ -35,3 +35,16 @@ def test_queries_match_numpy(name):
     q = synth.gpu.queries(w, 300)
     for b, heads in [(0, [0, 1]), (w.batch - 1, [w.n_q_heads - 1])]:
         assert np.array_equal(_np(q[:, b, heads]), synth.queries(w, b, heads, 300))
+
+
+@pytest.mark.parametrize("name", ["1b-bf16", "8b-offload-bf16"])
+def test_frontend_inputs_match_numpy(name):
+    w = synth.WORKLOADS[name]
+    D = synth.hidden_width(w)
+    x = synth.gpu.hidden(w, 65530, 3)
+    W = synth.gpu.proj_weights(w)
+    for b in (0, w.batch - 1):
+        ref = synth.to_storage(synth.hidden(w, b, 65530, 3, D), "bf16")
+        assert np.array_equal(_np(x[:, b]), ref)
+    rows = np.array([0, 1, 777, W.shape[0] - 1])
+    assert np.array_equal(_np(W[rows]), synth.to_storage(synth.proj_weights(w, D, rows), "bf16"))

@@ -22,7 +22,7 @@ __all__ = [
     "nosa_append_kv", "nosa_decode_step", "nosa_stats", "nosa_stats_reset", "nosa_set_timing",
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
-    "nosa_selftest_bounded_wait",
+    "nosa_selftest_bounded_wait", "nosa_frontend_rows", "nosa_decode_step_hidden",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -86,6 +86,8 @@ def _load():
         "nosa_sparse_attention_noalloc": (C.c_int, [P(NosaConfig), VP, C.c_int64, VP, I32, VP,
                                                     I32, VP, VP, VP, VP]),
         "nosa_selftest_bounded_wait": (C.c_int, [I32, C.c_int64, P(I32), P(I32)]),
+        "nosa_frontend_rows": (SZ, [P(NosaConfig)]),
+        "nosa_decode_step_hidden": (C.c_int, [VP, VP, I32, VP, VP, VP, VP, VP]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -198,6 +200,28 @@ def nosa_decode_step(h, q, k_new, v_new, e_new, out, lse=None, stream=None):
     _check(lib.nosa_decode_step(
         h, _ptr(q, qs, dt, "q"), _ptr(k_new, ks, dt, "k_new"), _ptr(v_new, ks, dt, "v_new"),
         _ptr(e_new, ks[:2], torch.float32, "e_new", 4), _ptr(out, qs, dt, "out"),
+        _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True), _stream(stream)), h)
+
+
+def nosa_frontend_rows(cfg: NosaConfig) -> int:
+    """Rows of the packed front-end projection: (Hq + 2 Hkv) d + Hkv."""
+    return int(lib.nosa_frontend_rows(C.byref(cfg)))
+
+
+def nosa_decode_step_hidden(h, x, w, out, lse=None, q_out=None, stream=None):
+    """One decode step from hidden states x [batch][D] and packed weights w [F][D] (bf16)."""
+    cfg = h.cfg
+    torch = _torch()
+    if isinstance(x, int) or isinstance(w, int):
+        raise ValueError("pass tensors to nosa_decode_step_hidden")
+    D = x.shape[-1]
+    F = nosa_frontend_rows(cfg)
+    qs = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
+    _check(lib.nosa_decode_step_hidden(
+        h, _ptr(x, (cfg.batch, D), torch.bfloat16, "x"), D,
+        _ptr(w, (F, D), torch.bfloat16, "w"),
+        _ptr(q_out, qs, torch.bfloat16, "q_out", allow_none=True),
+        _ptr(out, qs, torch.bfloat16, "out"),
         _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True), _stream(stream)), h)
 
 

@@ -233,6 +233,7 @@ struct StepGraph {
   cudaGraphNode_t append_node = nullptr;
   cudaKernelNodeParams append_params{};
   int n_cap = 0;
+  bool front = false;          // first node is the fused front-end (else the append)
   bool pending = false;        // timing events of the last launch not yet read
   cudaEvent_t done = nullptr;  // recorded after each launch: a rebuild waits for it
 };
@@ -276,6 +277,11 @@ struct nosa_handle {
   double t_us[8];
   long long t_count = 0;
   long long launches = 0;  // kernels launched by decode steps
+  // Fused front-end buffers (allocated on the first nosa_decode_step_hidden).
+  void* q_buf = nullptr;     // [batch][Hq][d] bf16 step queries
+  float* fe_part = nullptr;  // [ksplit][npad][Fpad] fp32 split partials
+  int* fe_cnt = nullptr;     // [tiles] tile counters
+  int fe_hidden = 0, fe_ksplit = 0;
 
   nosa_status fail(nosa_status code, const std::string& msg) {
     err = msg;
@@ -300,6 +306,11 @@ cudaError_t dev_alloc(nosa_handle* h, T** p, size_t bytes) {
 }
 
 void free_all(nosa_handle* h) {
+  for (void* p : {(void*)h->q_buf, (void*)h->fe_part, (void*)h->fe_cnt})
+    if (p) cudaFree(p);
+  h->q_buf = nullptr;
+  h->fe_part = nullptr;
+  h->fe_cnt = nullptr;
   for (void* p : h->dev_allocs) cudaFree(p);
   h->dev_allocs.clear();
   if (h->host_store) cudaFreeHost(h->host_store);
@@ -639,8 +650,9 @@ namespace {
 // slots (HBM); attention over the filled slots of chunk c follows its gather. `origin` forks at the start and joins at the end. Under stream
 // capture (`capture`), timing events become graph nodes and the append node is
 // returned in *append_node.
-cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& args, int n_cap,
-                         bool cold, cudaEvent_t* ev, bool capture, cudaGraphNode_t* append_node) {
+cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& args,
+                         const FrontArgs* front, int n_cap, bool cold, cudaEvent_t* ev,
+                         bool capture, cudaGraphNode_t* append_node) {
   const Shape& sh = h->s;
   State& st = h->st;
   auto mark = [&](cudaEvent_t e, cudaStream_t t) {
@@ -650,7 +662,8 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
   if (ev) mark(ev[0], origin);
   cudaError_t err = cudaEventRecord(h->ev_in, origin);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sco, h->ev_in, 0);
-  if (err == cudaSuccess) err = launch_append_step(sh, st, args, h->s_sco);
+  if (err == cudaSuccess)
+    err = front ? launch_frontend(sh, st, *front, h->s_sco) : launch_append_step(sh, st, args, h->s_sco);
   if (err == cudaSuccess && capture && append_node) {
     cudaStreamCaptureStatus cs;
     const cudaGraphNode_t* deps = nullptr;
@@ -737,8 +750,8 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
 }
 
 // Captures a warm step into g (replacing what it held) with these arguments.
-cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args, int N,
-                             cudaEvent_t* ev) {
+cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args,
+                             const FrontArgs* front, int N, cudaEvent_t* ev) {
   if (g.done == nullptr) {
     const cudaError_t e = cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming);
     if (e != cudaSuccess) return e;
@@ -754,7 +767,7 @@ cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args,
   cudaError_t err = cudaStreamBeginCapture(h->s_cap, cudaStreamCaptureModeRelaxed);
   if (err != cudaSuccess) return err;
   cudaGraphNode_t node = nullptr;
-  const cudaError_t e_enq = enqueue_step(h, h->s_cap, args, n_cap, false, ev, true, &node);
+  const cudaError_t e_enq = enqueue_step(h, h->s_cap, args, front, n_cap, false, ev, true, &node);
   cudaGraph_t graph = nullptr;
   err = cudaStreamEndCapture(h->s_cap, &graph);
   if (e_enq != cudaSuccess) err = e_enq;
@@ -770,35 +783,16 @@ cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args,
   g.graph = graph;
   g.append_node = node;
   g.n_cap = n_cap;
+  g.front = front != nullptr;
   h->graph_builds += 1;
   return cudaSuccess;
 }
 
-}  // namespace
-
-extern "C" {
-
-nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
-                             const float* e_new, void* out, float* lse, void* stream) {
-  if (!h) return NOSA_ERR_INVALID_ARG;
-  if (h->broken) return h->fail(NOSA_ERR_STATE, "handle unusable after an earlier CUDA error");
-  if (h->L < 1) return h->fail(NOSA_ERR_STATE, "decode step before any context was appended");
-  if (h->L + 1 > h->cfg.max_context) return h->fail(NOSA_ERR_CAPACITY, "context is full");
-  if (!q || !k_new || !v_new || !e_new || !out) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
-  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) ||
-      !aligned(e_new, 4) || (lse && !aligned(lse, 4)))
-    return h->fail(NOSA_ERR_INVALID_ARG, "q, k_new, v_new, out need 16-byte alignment");
-  DeviceGuard guard(h->cfg.device);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Runs one decode step whose first kernel is the append (front == NULL) or the
+// fused front-end; the checks of the public entry points come first.
+nosa_status run_step(nosa_handle* h, const StepArgs& args, const FrontArgs* front,
+                     cudaStream_t s) {
   const Shape& sh = h->s;
-  StepArgs args;
-  args.k_new = k_new;
-  args.v_new = v_new;
-  args.e_new = e_new;
-  args.q = q;
-  args.out = out;
-  args.lse = lse;
-  args.L_old = (int)h->L;
   const int N = args.L_old / sh.B;  // candidates after the append
   const bool cold = (h->steps == 0);
   cudaError_t err = cudaSuccess;
@@ -807,12 +801,21 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
     StepGraph& g = h->timing ? h->graphs[r] : h->plain;
     cudaEvent_t* ev = h->timing ? h->gev[r] : nullptr;
     if (h->timing) harvest_set(h, ev, &g.pending);
-    if (g.exec == nullptr || N >= g.n_cap || N < g.n_cap - kScoreCap) {
-      err = build_step_graph(h, g, args, N, ev);
+    if (g.exec == nullptr || g.front != (front != nullptr) || N >= g.n_cap ||
+        N < g.n_cap - kScoreCap) {
+      err = build_step_graph(h, g, args, front, N, ev);
     } else {
       cudaKernelNodeParams kp = g.append_params;
-      void* kargs[3] = {const_cast<Shape*>(&h->s), &h->st, &args};
-      kp.kernelParams = kargs;
+      StepArgs a = args;
+      FrontArgs fa;
+      void* kargs_append[3] = {const_cast<Shape*>(&h->s), &h->st, &a};
+      void* kargs_front[5] = {&fa.tw, &fa.tx, const_cast<Shape*>(&h->s), &h->st, &fa.p};
+      if (front) {
+        fa = *front;
+        kp.kernelParams = kargs_front;
+      } else {
+        kp.kernelParams = kargs_append;
+      }
       kp.extra = nullptr;
       err = cudaGraphExecKernelNodeSetParams(g.exec, g.append_node, &kp);
     }
@@ -831,14 +834,126 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
       h->pending[r] = true;
       h->ring_pos = (r + 1) % kRing;
     }
-    err = enqueue_step(h, s, args, N, cold, ev, false, nullptr);
+    err = enqueue_step(h, s, args, front, N, cold, ev, false, nullptr);
   }
   if (err != cudaSuccess) return h->cuda_fail(err, "decode step launch");
-  h->launches += 1 + h->nchunks * ((N > 0 ? 1 : 0) + 4);  // append; per chunk score, select, gather, 2 x attention
+  h->launches += 1 + h->nchunks * ((N > 0 ? 1 : 0) + 4);  // first kernel; per chunk score, select, gather, 2 x attention
   h->L += 1;
   h->steps += 1;
   h->last_stream = s;
   return NOSA_OK;
+}
+
+nosa_status step_checks(nosa_handle* h, const void* out, const float* lse) {
+  if (h->broken) return h->fail(NOSA_ERR_STATE, "handle unusable after an earlier CUDA error");
+  if (h->L < 1) return h->fail(NOSA_ERR_STATE, "decode step before any context was appended");
+  if (h->L + 1 > h->cfg.max_context) return h->fail(NOSA_ERR_CAPACITY, "context is full");
+  if (!out) return h->fail(NOSA_ERR_INVALID_ARG, "NULL output");
+  if (!aligned(out, 16) || (lse && !aligned(lse, 4)))
+    return h->fail(NOSA_ERR_INVALID_ARG, "out needs 16-byte and lse 4-byte alignment");
+  return NOSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, const void* v_new,
+                             const float* e_new, void* out, float* lse, void* stream) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  const nosa_status cs = step_checks(h, out, lse);
+  if (cs != NOSA_OK) return cs;
+  if (!q || !k_new || !v_new || !e_new) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(e_new, 4))
+    return h->fail(NOSA_ERR_INVALID_ARG, "q, k_new, v_new need 16-byte alignment");
+  DeviceGuard guard(h->cfg.device);
+  StepArgs args;
+  args.k_new = k_new;
+  args.v_new = v_new;
+  args.e_new = e_new;
+  args.q = q;
+  args.out = out;
+  args.lse = lse;
+  args.L_old = (int)h->L;
+  return run_step(h, args, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t nosa_frontend_rows(const nosa_config* cfg) {
+  std::string why;
+  if (validate(cfg, why) != NOSA_OK) return 0;
+  return (size_t)(cfg->n_q_heads + 2 * cfg->n_kv_heads) * cfg->head_dim + cfg->n_kv_heads;
+}
+
+nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden, const void* w,
+                                    void* q_out, void* out, float* lse, void* stream) {
+  if (!h) return NOSA_ERR_INVALID_ARG;
+  const nosa_status cs = step_checks(h, out, lse);
+  if (cs != NOSA_OK) return cs;
+  const Shape& sh = h->s;
+  if (sh.dtype != NOSA_BF16) return h->fail(NOSA_ERR_UNSUPPORTED, "the fused front-end needs bf16");
+  if (sh.batch > 256) return h->fail(NOSA_ERR_UNSUPPORTED, "the fused front-end needs batch <= 256");
+  if (!x || !w) return h->fail(NOSA_ERR_INVALID_ARG, "NULL input");
+  if (hidden < 64 || hidden > 65536 || hidden % 64 != 0)
+    return h->fail(NOSA_ERR_INVALID_ARG, "hidden must be a multiple of 64 in [64, 65536]");
+  if (!aligned(x, 16) || !aligned(w, 16) || (q_out && !aligned(q_out, 16)))
+    return h->fail(NOSA_ERR_INVALID_ARG, "x, w, q_out need 16-byte alignment");
+  DeviceGuard guard(h->cfg.device);
+  if (!frontend_available())
+    return h->fail(NOSA_ERR_UNSUPPORTED, "the driver offers no tensor-map encoder");
+  const int F = (sh.Hq + 2 * sh.Hkv) * sh.d + sh.Hkv;
+  const int tiles = (F + 127) / 128;
+  const int kblocks = hidden / 64;
+  const int npad = sh.batch <= 16 ? 16 : (sh.batch + 15) / 16 * 16;
+  int ksplit = std::max(1, std::min(std::min(kblocks, 8), sm_count_current() / tiles));
+  if (h->fe_hidden != hidden) {
+    // (Re)size the front-end buffers: partials for this split count.
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
+    for (void** p : {(void**)&h->fe_part, (void**)&h->fe_cnt})
+      if (*p) cudaFree(*p), *p = nullptr;
+    e = cudaMalloc((void**)&h->fe_part, (size_t)ksplit * npad * tiles * 128 * 4);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&h->fe_cnt, (size_t)tiles * 4);
+    if (e == cudaSuccess) e = cudaMemset(h->fe_cnt, 0, (size_t)tiles * 4);
+    if (e == cudaSuccess && !h->q_buf)
+      e = cudaMalloc(&h->q_buf, (size_t)sh.batch * sh.Hq * sh.d * 2);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      h->fe_hidden = 0;
+      return h->fail(NOSA_ERR_OOM, "front-end buffers");
+    }
+    h->fe_hidden = hidden;
+    h->fe_ksplit = ksplit;
+  }
+  ksplit = h->fe_ksplit;
+  FrontArgs fa;
+  std::memset(&fa, 0, sizeof(fa));
+  FrontParams& p = fa.p;
+  p.F = F;
+  p.Fpad = tiles * 128;
+  p.D = hidden;
+  p.kblocks = kblocks;
+  p.ksplit = ksplit;
+  p.tiles = tiles;
+  p.npad = npad;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < npad) p.tmem_cols *= 2;
+  p.batch = sh.batch;
+  p.L_old = (int)h->L;
+  p.q = q_out ? q_out : h->q_buf;
+  p.out = out;
+  p.lse = lse;
+  p.part = h->fe_part;
+  p.counters = h->fe_cnt;
+  p.err = &h->st.stats->error;
+  if (!frontend_encode(fa, x, w, sh.batch, hidden, F))
+    return h->fail(NOSA_ERR_INVALID_ARG, "tensor-map encoding of x or w failed");
+  StepArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.q = p.q;
+  args.out = out;
+  args.lse = lse;
+  args.L_old = p.L_old;
+  return run_step(h, args, &fa, static_cast<cudaStream_t>(stream));
 }
 
 nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out) {

@@ -6,6 +6,7 @@
 // range.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the driver itself is reached through the runtime's entry-point query)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -66,6 +67,37 @@ struct StepIO {
   long long tail_off;  // byte offset of the tail block's buffer: (n_cand % 2) * payload
 };
 
+// Fused front-end (projection of the hidden states + QKV split + append and
+// pooling), launched instead of the append kernel. Grid = (tiles, ksplit).
+struct FrontParams {
+  int F, Fpad;      // packed rows of W ((Hq + 2 Hkv) d + Hkv) and rows padded to the tile
+  int D;            // hidden width (multiple of 64)
+  int kblocks;      // D / 64
+  int ksplit;       // splits of the hidden width (<= kblocks)
+  int tiles;        // Fpad / 128
+  int npad;         // batch padded to a multiple of 16 (the MMA's N)
+  int tmem_cols;    // tensor-memory columns allocated (power of two >= max(32, npad))
+  int batch;
+  int L_old;        // context before this step's token
+  void* q;          // [batch][Hq][d] bf16, written (the step's queries)
+  void* out;        // published in StepIO
+  float* lse;
+  float* part;      // [ksplit][npad][Fpad] fp32 split partials
+  int* counters;    // [tiles], self-resetting
+  int* err;         // device error word
+};
+struct FrontArgs {
+  CUtensorMap tw;   // W [F][D] bf16, box 64 x 128
+  CUtensorMap tx;   // x [batch][D] bf16, box 64 x npad
+  FrontParams p;
+};
+bool frontend_available();
+size_t frontend_smem_bytes(int npad);
+// Encodes fa.tx and fa.tw (fa.p.npad must be set). False if the driver's tensor-map
+// encoder is unavailable or rejects the arguments.
+bool frontend_encode(FrontArgs& fa, const void* x, const void* w, int batch, int D, int F);
+const void* frontend_kernel_ptr();
+
 struct State {
   uint8_t* slots;      // [U][k] block units (device)
   uint8_t* tail;       // [U][2] block units (device); block b lives in buffer b % 2
@@ -99,6 +131,8 @@ struct State {
 cudaError_t launch_append_step(const Shape& s, const State& st, const StepArgs& a,
                                cudaStream_t stream);
 cudaError_t launch_promote_tail(const Shape& s, const State& st, int blk, cudaStream_t stream);
+cudaError_t launch_frontend(const Shape& s, const State& st, const FrontArgs& fa,
+                            cudaStream_t stream);
 cudaError_t launch_append_bulk(const Shape& s, const State& st, const void* k, const void* v,
                                const float* e, int L_old, int n, cudaStream_t stream);
 // The per-unit kernels below handle units [ubase, ubase + ucount) of one chunk
