@@ -161,6 +161,13 @@ def score_bytes_per_launch(w, n_cand, pk_elt=4):
     return w.units * (n_cand * 4 * w.head_dim * pk_elt + n_cand * 4 + w.group * w.head_dim * elt)
 
 
+def frontend_bytes_per_launch(w, D):
+    """Algorithmic bytes of one fused front-end launch: the packed weights and the
+    hidden states read once, every projected value written once (bf16)."""
+    F = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim + w.n_kv_heads
+    return F * D * 2 + w.batch * D * 2 + w.batch * F * 2
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -324,23 +331,48 @@ def run_gpu(args, rank, world, local_rank):
         del k, v, e
     torch.cuda.synchronize()
     # per-step inputs staged in HBM before the timed region
-    q_all = synth.gpu.queries(w, total_steps)
-    k_all, v_all, e_all = synth.gpu.kv(w, w.prompt, total_steps, step_major=True)
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
     lse = torch.empty((w.batch, w.n_q_heads), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     peak_h2d = h2d_peak_gbs(torch) if rank == 0 else None
+    out_p, lse_p, stream_p = out.data_ptr(), lse.data_ptr(), stream.cuda_stream
+    D = synth.hidden_width(w)
+    if args.frontend:
+        # the step starts from hidden states: the fused front-end projects them
+        Wf = nosa.nosa_frontend_pack(cfg, synth.gpu.proj_weights(w, D))  # packed once
+        x_all = synth.gpu.hidden(w, w.prompt, total_steps, D)
+        for s in range(W):
+            nosa.nosa_decode_step_hidden(h, x_all[s], Wf, out, lse, stream=stream)
+        ptrs = [x_all[s].data_ptr() for s in range(total_steps)]
+        w_p = Wf.data_ptr()
+        step_fn = nosa.lib.nosa_decode_step_hidden
 
-    for s in range(W):
-        nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
+        def raw_step(s):
+            r = step_fn(h, ptrs[s], D, w_p, None, out_p, lse_p, stream_p)
+            if r:
+                raise nosa.NosaError(r, nosa.nosa_last_error(h))
+        e2e_hosts = lambda: [x_all[W + K:W + K + KE].cpu().pin_memory()]
+        e2e_step = lambda devs: nosa.nosa_decode_step_hidden(h, devs[0], Wf, out, None, stream=stream)
+    else:
+        q_all = synth.gpu.queries(w, total_steps)
+        k_all, v_all, e_all = synth.gpu.kv(w, w.prompt, total_steps, step_major=True)
+        for s in range(W):
+            nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
+        # raw pointers for the timed loop (shapes were checked by the warm-up calls)
+        ptrs = [(q_all[s].data_ptr(), k_all[s].data_ptr(), v_all[s].data_ptr(), e_all[s].data_ptr())
+                for s in range(total_steps)]
+        step_fn = nosa.lib.nosa_decode_step
+
+        def raw_step(s):
+            p_ = ptrs[s]
+            r = step_fn(h, p_[0], p_[1], p_[2], p_[3], out_p, lse_p, stream_p)
+            if r:
+                raise nosa.NosaError(r, nosa.nosa_last_error(h))
+        e2e_hosts = lambda: [x[W + K:W + K + KE].cpu().pin_memory() for x in (q_all, k_all, v_all, e_all)]
+        e2e_step = lambda devs: nosa.nosa_decode_step(h, *devs, out, None, stream)
     torch.cuda.synchronize()
     nosa.nosa_stats_reset(h)
-
-    # raw pointers for the timed loop (shapes were checked by the warm-up calls)
-    ptrs = [(q_all[s].data_ptr(), k_all[s].data_ptr(), v_all[s].data_ptr(), e_all[s].data_ptr())
-            for s in range(total_steps)]
-    out_p, lse_p, stream_p = out.data_ptr(), lse.data_ptr(), stream.cuda_stream
     sampler = ClockSampler(gpu_index(local_rank)) if rank == 0 else None
     time.sleep(0.15 if sampler else 0)
     barrier(world)
@@ -351,8 +383,7 @@ def run_gpu(args, rank, world, local_rank):
     ev0.record(stream)
     h0 = time.perf_counter()
     for s in range(W, W + K):
-        nosa.nosa_decode_step(h, ptrs[s][0], ptrs[s][1], ptrs[s][2], ptrs[s][3], out_p, lse_p,
-                              stream_p)
+        raw_step(s)
     host_enqueue_us = (time.perf_counter() - h0) / K * 1e6
     ev1.record(stream)
     torch.cuda.nvtx.range_pop()
@@ -366,9 +397,8 @@ def run_gpu(args, rank, world, local_rank):
     context_after = st["context"]
 
     # end to end: pinned host inputs -> device, step, result -> pinned host
-    qh = q_all[W + K:W + K + KE].cpu().pin_memory()
-    kh, vh, eh = (x[W + K:W + K + KE].cpu().pin_memory() for x in (k_all, v_all, e_all))
-    qd, kd, vd, ed = (torch.empty_like(x[0], device="cuda") for x in (qh, kh, vh, eh))
+    hosts = e2e_hosts()
+    devs = [torch.empty_like(x[0], device="cuda") for x in hosts]
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -376,11 +406,9 @@ def run_gpu(args, rank, world, local_rank):
     x0t = time.time()
     e0.record(stream)
     for s in range(KE):
-        qd.copy_(qh[s], non_blocking=True)
-        kd.copy_(kh[s], non_blocking=True)
-        vd.copy_(vh[s], non_blocking=True)
-        ed.copy_(eh[s], non_blocking=True)
-        nosa.nosa_decode_step(h, qd, kd, vd, ed, out, None, stream)
+        for d_, h_ in zip(devs, hosts):
+            d_.copy_(h_[s], non_blocking=True)
+        e2e_step(devs)
         out_h.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -388,7 +416,7 @@ def run_gpu(args, rank, world, local_rank):
     if sampler:
         sampler.mark(x0t, x1t)
     e2e_secs = e0.elapsed_time(e1) / 1e3
-    bi = sum(x[0].numel() * x.element_size() for x in (qh, kh, vh, eh))
+    bi = sum(x[0].numel() * x.element_size() for x in hosts)
     bo = out_h.numel() * out_h.element_size()
     clocks = sampler.stop() if sampler else None
 
@@ -400,11 +428,10 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         nosa.nosa_stats_reset(h)
         for s in range(W + K + KE, W + K + KE + KT):
-            nosa.nosa_decode_step(h, ptrs[s][0], ptrs[s][1], ptrs[s][2], ptrs[s][3], out_p, lse_p,
-                                  stream_p)
+            raw_step(s)
         st_ph = nosa.nosa_stats(h)
     nosa.nosa_destroy(h)
-    del q_all, k_all, v_all, e_all
+    del ptrs
     n_mid = (w.prompt + W + K // 2) // w.block
     alone_secs, alone_bytes = attention_alone(nosa, torch, w, n_mid,
                                               (w.prompt + W + K // 2) % w.block + 1)
@@ -461,7 +488,8 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded counter-based generator; shapes of the workload)",
-        "mode": args.mode + ("+pooled_bf16" if args.pooled_bf16 else ""),
+        "mode": args.mode + ("+pooled_bf16" if args.pooled_bf16 else "")
+                + ("+frontend" if args.frontend else ""),
         "config": {"workload": w0.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k, "k_e": w.k_e,
                    "context_start": w.prompt, "context_end": context_after,
@@ -477,6 +505,15 @@ def run_gpu(args, rank, world, local_rank):
         "attn_hbm_gbs": round(dom_bytes / (dom_us * 1e-6) / 1e9, 1),
         "attn_frac_of_peak": round(dom_bytes / (dom_us * 1e-6) / 1e9 / peak, 4),
         "attn_kept_in_step_gbs": round(attn_gbs, 1),
+        **({"frontend": {"hidden": D, "rows": (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim
+                         + w.n_kv_heads,
+                         "kernel_us": round(phase_us["append_pool"], 3),
+                         "hbm_gbs": round(rate(frontend_bytes_per_launch(w, D),
+                                               phase_us["append_pool"]), 1),
+                         "frac_of_peak": round(rate(frontend_bytes_per_launch(w, D),
+                                                    phase_us["append_pool"]) / peak, 4),
+                         "algorithmic_bytes_per_launch": frontend_bytes_per_launch(w, D)}}
+           if args.frontend else {}),
         "score_hbm_gbs": round(score_gbs, 1),
         "recall_h2d_gbs": round(recall_gbs, 2),
         "h2d_peak_gbs": round(peak_h2d, 2) if peak_h2d else None,
@@ -590,6 +627,9 @@ def main():
                     help="time only the split-K attention on the step shape (profiling aid)")
     ap.add_argument("--pooled-bf16", action="store_true",
                     help="variant: pooled keys stored in bf16 (halves the scoring traffic)")
+    ap.add_argument("--frontend", action="store_true",
+                    help="steps start from hidden states: the fused front-end (projection on the "
+                         "tensor cores + QKV split + append and pooling) runs first")
     ap.add_argument("--no-timing", action="store_true",
                     help="skip the per-phase timing window")
     ap.add_argument("--phase-steps", type=int, default=64,

@@ -168,6 +168,25 @@ nosa_status nosa_decode_step(nosa_handle* h, const void* q, const void* k_new, c
 size_t nosa_frontend_rows(const nosa_config* cfg);
 
 /*
+ * Bytes of the packed form of the front-end weights for this configuration and
+ * hidden width: ceil(F / 128) * (hidden / 64) * 16384 (0 if invalid).
+ */
+size_t nosa_frontend_packed_bytes(const nosa_config* cfg, int32_t hidden);
+
+/*
+ * Packs the front-end weights once (they are static) into the layout the fused
+ * front-end streams: every 128-row x 64-column tile of W becomes one contiguous
+ * 16 KB run, rows stored in the 128-byte-swizzled order the tensor cores read
+ * (row r's 16-byte chunk c at r * 128 + (c XOR (r mod 8)) * 16), the tiles of a
+ * row block consecutive along the hidden width; rows past F are zeros. Async.
+ *   w        : device bf16 [F][hidden], row-major (F = nosa_frontend_rows)
+ *   w_packed : device, nosa_frontend_packed_bytes(cfg, hidden) bytes, written
+ * Both 16-byte aligned. Errors: INVALID_ARG, CUDA.
+ */
+nosa_status nosa_frontend_pack(const nosa_config* cfg, int32_t hidden, const void* w,
+                               void* w_packed, void* stream);
+
+/*
  * One decode step whose inputs are projected from the layer's hidden states by
  * the library: y = W x for every request, split into the query heads (rows
  * [0, Hq d): head g = row / d), the key heads (next Hkv d rows), the value
@@ -178,17 +197,18 @@ size_t nosa_frontend_rows(const nosa_config* cfg);
  * the rest of the step is nosa_decode_step's.
  *   x      : device bf16 [batch][hidden], row-major (the step's hidden states)
  *   hidden : width D, a multiple of 64 in [64, 65536]
- *   w      : device bf16 [F][hidden], row-major (F = nosa_frontend_rows), read only
+ *   w_packed : the weights W [F][hidden] packed by nosa_frontend_pack, read only
  *   q_out  : device bf16 [batch][n_q_heads][head_dim] receiving the step's
  *            queries, or NULL (then they stay in an internal buffer)
  *   out, lse, stream: as for nosa_decode_step.
- * x, w, q_out and out need 16-byte alignment. UNSUPPORTED unless cfg->dtype is
+ * x, w_packed, q_out and out need 16-byte alignment. UNSUPPORTED unless cfg->dtype is
  * NOSA_BF16 and batch <= 256 (or when the driver offers no tensor-map encoder);
  * OOM if the front-end's scratch (split partials, about ksplit * batch * F * 4
  * bytes) cannot be allocated on the first call. Other errors as nosa_decode_step.
  */
-nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden, const void* w,
-                                    void* q_out, void* out, float* lse, void* stream);
+nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden,
+                                    const void* w_packed, void* q_out, void* out, float* lse,
+                                    void* stream);
 
 /* Counters, host-readable. gamma_* covers steps after the first decode step
  * with at least k candidates; gamma(t) = |Gamma(t) ∩ R(t-1)| / k where R(t-1)

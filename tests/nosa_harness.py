@@ -243,7 +243,7 @@ class FrontRun(GpuRun):
     def __init__(self, w, units=None, D=None, **kw):
         super().__init__(w, units=units, **kw)
         self.D = synth.hidden_width(w) if D is None else D
-        self.W_dev = synth.gpu.proj_weights(w, self.D)
+        self.W_dev = nosa.nosa_frontend_pack(self.cfg, synth.gpu.proj_weights(w, self.D))
         self.W64 = synth.proj_weights(w, self.D)
         self.requests = sorted({u // w.n_kv_heads for u in self.units})
 

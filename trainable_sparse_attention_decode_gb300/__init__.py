@@ -23,6 +23,7 @@ __all__ = [
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
     "nosa_selftest_bounded_wait", "nosa_frontend_rows", "nosa_decode_step_hidden",
+    "nosa_frontend_packed_bytes", "nosa_frontend_pack",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -88,6 +89,8 @@ def _load():
         "nosa_selftest_bounded_wait": (C.c_int, [I32, C.c_int64, P(I32), P(I32)]),
         "nosa_frontend_rows": (SZ, [P(NosaConfig)]),
         "nosa_decode_step_hidden": (C.c_int, [VP, VP, I32, VP, VP, VP, VP, VP]),
+        "nosa_frontend_packed_bytes": (SZ, [P(NosaConfig), I32]),
+        "nosa_frontend_pack": (C.c_int, [P(NosaConfig), I32, VP, VP, VP]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -208,18 +211,34 @@ def nosa_frontend_rows(cfg: NosaConfig) -> int:
     return int(lib.nosa_frontend_rows(C.byref(cfg)))
 
 
-def nosa_decode_step_hidden(h, x, w, out, lse=None, q_out=None, stream=None):
-    """One decode step from hidden states x [batch][D] and packed weights w [F][D] (bf16)."""
+def nosa_frontend_packed_bytes(cfg: NosaConfig, hidden: int) -> int:
+    return int(lib.nosa_frontend_packed_bytes(C.byref(cfg), hidden))
+
+
+def nosa_frontend_pack(cfg: NosaConfig, w, stream=None):
+    """Packs the front-end weights w [F][D] bf16 (row-major); returns the packed uint8 tensor."""
+    torch = _torch()
+    F, D = nosa_frontend_rows(cfg), w.shape[-1]
+    packed = torch.empty(nosa_frontend_packed_bytes(cfg, D), dtype=torch.uint8, device=w.device)
+    st = lib.nosa_frontend_pack(C.byref(cfg), D, _ptr(w, (F, D), torch.bfloat16, "w"),
+                                _ptr(packed, None, torch.uint8, "w_packed"), _stream(stream))
+    _check(st)
+    return packed
+
+
+def nosa_decode_step_hidden(h, x, w_packed, out, lse=None, q_out=None, stream=None):
+    """One decode step from hidden states x [batch][D] (bf16) and packed weights."""
     cfg = h.cfg
     torch = _torch()
-    if isinstance(x, int) or isinstance(w, int):
+    if isinstance(x, int) or isinstance(w_packed, int):
         raise ValueError("pass tensors to nosa_decode_step_hidden")
     D = x.shape[-1]
-    F = nosa_frontend_rows(cfg)
+    if w_packed.numel() != nosa_frontend_packed_bytes(cfg, D):
+        raise ValueError("w_packed is not the packed form for this configuration and width")
     qs = (cfg.batch, cfg.n_q_heads, cfg.head_dim)
     _check(lib.nosa_decode_step_hidden(
         h, _ptr(x, (cfg.batch, D), torch.bfloat16, "x"), D,
-        _ptr(w, (F, D), torch.bfloat16, "w"),
+        _ptr(w_packed, None, torch.uint8, "w_packed"),
         _ptr(q_out, qs, torch.bfloat16, "q_out", allow_none=True),
         _ptr(out, qs, torch.bfloat16, "out"),
         _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True), _stream(stream)), h)

@@ -69,27 +69,27 @@ __global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st, Ste
   const float e_tok = e_new[u];
   if (threadIdx.x == 0) *reinterpret_cast<float*>(cur + e_off(pos, s.B, s.d, s.elt)) = e_tok;
 
-  // A completed sub-block: mean key, mean eviction logit, running block max.
-  if (pos % s.S == s.S - 1) {
-    const int sb = pos / s.S;
-    const int p0 = sb * s.S;
-    for (int dim = threadIdx.x; dim < s.d; dim += blockDim.x) {
-      float acc = 0.f;
-      for (int j = 0; j < s.S - 1; ++j)
-        acc += to_f32(*reinterpret_cast<const T*>(cur + k_off(p0 + j, dim, s.B, s.elt)));
-      acc += to_f32(k_new[in_row + dim]);
+  // Running fp32 sums of the open sub-block (0 + k_0 + k_1 + ..., token order);
+  // when the sub-block completes: mean key, mean eviction logit, running block max.
+  const bool first = (pos % s.S) == 0, last = (pos % s.S) == s.S - 1;
+  const int sb = pos / s.S;
+  for (int dim = threadIdx.x; dim < s.d; dim += blockDim.x) {
+    const float r = (first ? 0.f : st.ksum[in_row + dim]) + to_f32(k_new[in_row + dim]);
+    if (last)
       store_pooled(s, st.pk, (((long long)u * s.maxBlk + blk) * s.P + sb) * s.d + dim,
-                   acc * (1.0f / s.S));
-    }
-    if (threadIdx.x == 0) {
-      float ea = 0.f;
-      for (int j = 0; j < s.S - 1; ++j)
-        ea += *reinterpret_cast<const float*>(cur + e_off(p0 + j, s.B, s.d, s.elt));
-      ea += e_tok;
-      const float eb = ea * (1.0f / s.S);
+                   r * (1.0f / s.S));
+    else
+      st.ksum[in_row + dim] = r;
+  }
+  if (threadIdx.x == 0) {
+    const float r = (first ? 0.f : st.esum[u]) + e_tok;
+    if (last) {
+      const float eb = r * (1.0f / s.S);
       const long long bi = (long long)u * s.maxBlk + blk;
       st.sube[bi * s.P + sb] = eb;
       st.se[bi] = (sb == 0) ? eb : fmaxf(st.se[bi], eb);
+    } else {
+      st.esum[u] = r;
     }
   }
 }
@@ -157,6 +157,23 @@ __global__ void __launch_bounds__(256) append_bulk_kernel(Shape s, State st,
       for (int j = 0; j < s.S; ++j)
         acc += to_f32(*reinterpret_cast<const T*>(unit_s + k_off(sb * s.S + j, dim, s.B, s.elt)));
       store_pooled(s, st.pk, (bi * s.P + sb) * s.d + dim, acc * (1.0f / s.S));
+    }
+  }
+  // A call that ends inside a sub-block leaves that sub-block's running sums
+  // (token order, from 0) for the decode steps that complete it.
+  if (blk == last_blk && pos_hi % s.S != 0) {
+    const int o0 = (pos_hi / s.S) * s.S;
+    for (int dim = threadIdx.x; dim < s.d; dim += blockDim.x) {
+      float r = 0.f;
+      for (int j = o0; j < pos_hi; ++j)
+        r += to_f32(*reinterpret_cast<const T*>(unit_s + k_off(j, dim, s.B, s.elt)));
+      st.ksum[(long long)u * s.d + dim] = r;
+    }
+    if (threadIdx.x == 0) {
+      float r = 0.f;
+      for (int j = o0; j < pos_hi; ++j)
+        r += *reinterpret_cast<const float*>(unit_s + e_off(j, s.B, s.d, s.elt));
+      st.esum[u] = r;
     }
   }
   if (threadIdx.x == 0) {

@@ -14,11 +14,16 @@
 // MMA's M side: CTA (tile, split) computes a 128-row x N tile (N = the batch
 // padded to a multiple of 16) over its share of the hidden width with
 // tcgen05.mma (kind::f16: bf16 operands, fp32 accumulator in tensor memory).
-// TMA streams 128 x 64 weight tiles and N x 64 hidden-state tiles into a ring of
-// 128-byte-swizzled shared-memory stages (the K-major layout the MMA reads).
-// With several splits, each CTA stores its fp32 partial tile; the CTA that
-// finishes a tile last sums the partials in split order (deterministic) and runs
-// the epilogue:
+// The weights are packed once (frontend_pack_kernel) so that every 128-row x
+// 64-column tile is one contiguous 16 KB run already in the 128-byte-swizzled
+// K-major order the MMA reads, tiles of a row block consecutive along the hidden
+// width: a CTA streams one contiguous range with bulk copies (full DRAM pages),
+// and TMA brings the matching N x 64 hidden-state tiles (same swizzle) into a
+// ring of shared-memory stages.
+// The splits of a row tile form one thread-block cluster: each CTA leaves its
+// fp32 partial tile in shared memory and, after a cluster barrier, sums a share
+// of the tile's entries over all ranks (rank order, deterministic) through
+// distributed shared memory, then runs the epilogue for that share:
 //   query rows    -> q [batch][Hq][d], bf16 (nearest even);
 //   key rows      -> the unit's tail block (chunk-major K), value rows -> V
 //                    (token-major), both bf16; eviction rows -> e (fp32);
@@ -44,7 +49,7 @@ namespace {
 constexpr int kFrontThreads = 192;
 constexpr int kTileM = 128;                   // rows of W per CTA (MMA M)
 constexpr int kTileK = 64;                    // hidden elements per stage: 128 bytes of bf16
-constexpr int kStages = 4;
+constexpr int kMaxStages = 10;
 constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB weight tile per stage
 
 // Shared-memory matrix descriptor of a K-major operand tile in the canonical
@@ -105,66 +110,147 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Writes row f of the projection for request n (value y, fp32) where it belongs.
-__device__ __forceinline__ void emit(const Shape& s, const State& st, const FrontParams& p, int f,
-                                     int n, float y, int blk, int pos) {
+// Writes rows f0 .. f0 + 7 of the projection for request n (values v8, fp32).
+// 8 rows of one kind never straddle a boundary (the boundaries are multiples of
+// 64), so a query, key or value item is one aligned 16-byte store (8 bf16: one K
+// chunk, or 8 consecutive V or q elements) and its key running sums are two
+// float4. The sums run in token order from 0; the sub-block's last token turns
+// them into means. Eviction rows (one fp32 pre-exp logit per KV head) are
+// written one by one.
+// pre: the item's running sums, loaded earlier (NULL: load them here).
+__device__ __forceinline__ void store_item(const Shape& s, const State& st, const FrontParams& p,
+                                           int n, int f0, const float* v8, const float* pre,
+                                           int blk, int pos) {
   const int Fq = s.Hq * s.d, Fk = Fq + s.Hkv * s.d, Fv = Fk + s.Hkv * s.d;
-  const bool sub_end = (pos % s.S) == s.S - 1;
-  const int p0 = pos - (s.S - 1);  // first token of the completed sub-block
-  if (f < Fq) {
-    reinterpret_cast<__nv_bfloat16*>(p.q)[(long long)n * Fq + f] = __float2bfloat16_rn(y);
-    return;
-  }
-  if (f < Fv) {
-    const bool is_k = f < Fk;
-    const int r = is_k ? f - Fq : f - Fk;
-    const int h = r / s.d, dim = r % s.d;
-    const int u = n * s.Hkv + h;
-    uint8_t* cur = st.tail + ((long long)u * 2 + (blk & 1)) * s.payload;
-    const __nv_bfloat16 yb = __float2bfloat16_rn(y);
-    if (!is_k) {
-      *reinterpret_cast<__nv_bfloat16*>(cur + v_off(pos, dim, s.B, s.d, 2)) = yb;
+  const bool first = (pos % s.S) == 0, last = (pos % s.S) == s.S - 1;
+  const int sb = pos / s.S;
+  const long long tail_sel = (long long)(blk & 1) * s.payload;
+  if (f0 < Fv) {
+    __align__(16) __nv_bfloat16 b8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) b8[e] = __float2bfloat16_rn(v8[e]);
+    const int4 packed = *reinterpret_cast<const int4*>(b8);
+    if (f0 < Fq) {
+      *reinterpret_cast<int4*>(reinterpret_cast<__nv_bfloat16*>(p.q) + (long long)n * Fq + f0) = packed;
       return;
     }
-    *reinterpret_cast<__nv_bfloat16*>(cur + k_off(pos, dim, s.B, 2)) = yb;
-    if (sub_end) {
-      float acc = 0.f;
-      for (int j = 0; j < s.S - 1; ++j)
-        acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(cur + k_off(p0 + j, dim, s.B, 2)));
-      acc += __bfloat162float(yb);
-      const int sb = pos / s.S;
-      store_pooled(s, st.pk, (((long long)u * s.maxBlk + blk) * s.P + sb) * s.d + dim,
-                   acc * (1.0f / s.S));
+    const bool is_k = f0 < Fk;
+    const int r = is_k ? f0 - Fq : f0 - Fk;
+    const int h = r / s.d, dim0 = r % s.d;
+    const int u = n * s.Hkv + h;
+    uint8_t* cur = st.tail + (long long)u * 2 * s.payload + tail_sel;
+    if (!is_k) {
+      *reinterpret_cast<int4*>(cur + v_off(pos, dim0, s.B, s.d, 2)) = packed;
+      return;
+    }
+    *reinterpret_cast<int4*>(cur + k_off(pos, dim0, s.B, 2)) = packed;
+    float4* ks = reinterpret_cast<float4*>(st.ksum + (long long)u * s.d + dim0);
+    float rs[8];
+    if (first) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rs[e] = 0.f;
+    } else if (pre) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rs[e] = pre[e];
+    } else {
+      const float4 a = ks[0], b = ks[1];
+      rs[0] = a.x; rs[1] = a.y; rs[2] = a.z; rs[3] = a.w;
+      rs[4] = b.x; rs[5] = b.y; rs[6] = b.z; rs[7] = b.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rs[e] += __bfloat162float(b8[e]);
+    if (last) {
+      const long long pk0 = (((long long)u * s.maxBlk + blk) * s.P + sb) * s.d + dim0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) store_pooled(s, st.pk, pk0 + e, rs[e] * (1.0f / s.S));
+    } else {
+      ks[0] = make_float4(rs[0], rs[1], rs[2], rs[3]);
+      ks[1] = make_float4(rs[4], rs[5], rs[6], rs[7]);
     }
     return;
   }
-  const int h = f - Fv;  // eviction row of KV head h
-  const int u = n * s.Hkv + h;
-  uint8_t* cur = st.tail + ((long long)u * 2 + (blk & 1)) * s.payload;
-  *reinterpret_cast<float*>(cur + e_off(pos, s.B, s.d, 2)) = y;
-  if (sub_end) {
-    float ea = 0.f;
-    for (int j = 0; j < s.S - 1; ++j)
-      ea += *reinterpret_cast<const float*>(cur + e_off(p0 + j, s.B, s.d, 2));
-    ea += y;
-    const float eb = ea * (1.0f / s.S);
-    const int sb = pos / s.S;
-    const long long bi = (long long)u * s.maxBlk + blk;
-    st.sube[bi * s.P + sb] = eb;
-    st.se[bi] = (sb == 0) ? eb : fmaxf(st.se[bi], eb);
+  const int ne = min(8, p.F - f0);
+  float run[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)  // every load before the first store
+    run[e] = (e < ne && !first) ? (pre ? pre[e] : st.esum[n * s.Hkv + (f0 + e - Fv)]) : 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (e >= ne) break;
+    const int u = n * s.Hkv + (f0 + e - Fv);
+    uint8_t* cur = st.tail + (long long)u * 2 * s.payload + tail_sel;
+    *reinterpret_cast<float*>(cur + e_off(pos, s.B, s.d, 2)) = v8[e];
+    const float rsum = run[e] + v8[e];
+    if (last) {
+      const float eb = rsum * (1.0f / s.S);
+      const long long bi = (long long)u * s.maxBlk + blk;
+      st.sube[bi * s.P + sb] = eb;
+      st.se[bi] = (sb == 0) ? eb : fmaxf(st.se[bi], eb);
+    } else {
+      st.esum[u] = rsum;
+    }
   }
 }
 
+// Loads the running sums that store_item will need for rows f0 .. f0 + 7 of
+// request n (key rows: 8 from ksum; eviction rows: up to 8 from esum).
+__device__ __forceinline__ void prefetch_sums(const Shape& s, const State& st,
+                                              const FrontParams& p, int n, int f0, float* pre) {
+  const int Fq = s.Hq * s.d, Fk = Fq + s.Hkv * s.d, Fv = Fk + s.Hkv * s.d;
+  if (f0 >= Fq && f0 < Fk) {
+    const int r = f0 - Fq;
+    const float4* ks = reinterpret_cast<const float4*>(
+        st.ksum + (long long)(n * s.Hkv + r / s.d) * s.d + r % s.d);
+    const float4 a = ks[0], b = ks[1];
+    pre[0] = a.x; pre[1] = a.y; pre[2] = a.z; pre[3] = a.w;
+    pre[4] = b.x; pre[5] = b.y; pre[6] = b.z; pre[7] = b.w;
+  } else if (f0 >= Fv) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      pre[e] = (f0 + e < p.F) ? st.esum[n * s.Hkv + (f0 + e - Fv)] : 0.f;
+  }
+}
+
+// Distributed shared memory of the CTA cluster that shares a row tile.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before
+// the peers' reads (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kFrontThreads, 1)
-    frontend_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
-                    Shape s, State st, FrontParams p) {
+    frontend_kernel(const __grid_constant__ CUtensorMap tx, Shape s, State st, FrontParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int b_bytes = p.npad * 128;
-  uint8_t* sa = smem;                    // [kStages][128 rows][128 B]
-  uint8_t* sb = smem + kStages * kABytes;  // [kStages][npad rows][128 B]
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], accum;
+  const int kStages = p.stages;
+  uint8_t* sa = smem;                    // [stages][128 rows][128 B]
+  uint8_t* sb = smem + kStages * kABytes;  // [stages][npad rows][128 B]
+  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], accum;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_bad;
   __shared__ int s_issued, s_last;
@@ -198,6 +284,12 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // Items of the first chunk of requests handled by this thread in the epilogue
+  // (see below); their running sums are loaded while the tensor cores run.
+  constexpr int kItemsMax = 4;  // 512 items / (128 threads x ksplit >= 1)
+  const uint32_t rank = cluster_rank();
+  const int tid2 = threadIdx.x - 64;
+  float pre[kItemsMax][8];
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
@@ -212,8 +304,9 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
         }
         if (s_bad) break;
         mbar_arrive_expect_tx(&full[stg], (uint32_t)(kABytes + b_bytes));
-        tma_load_2d(smem_u32(sa + stg * kABytes), &tw, (kb0 + i) * kTileK, tile * kTileM,
-                    smem_u32(&full[stg]));
+        bulk_g2s(sa + stg * kABytes,
+                 p.w_packed + ((long long)tile * p.kblocks + kb0 + i) * kABytes, (uint32_t)kABytes,
+                 &full[stg]);
         tma_load_2d(smem_u32(sb + stg * b_bytes), &tx, (kb0 + i) * kTileK, 0, smem_u32(&full[stg]));
       }
       s_issued = i;
@@ -243,7 +336,6 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
     }
   } else {
     // Side work while the tensor cores run.
-    const int tid2 = threadIdx.x - 64;
     const int cta = blockIdx.y * gridDim.x + blockIdx.x, ncta = gridDim.x * gridDim.y;
     if (cta == 0 && tid2 == 0) {
       StepIO io;
@@ -270,61 +362,70 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
       __threadfence_system();
     }
 
-    // Epilogue.
+    if ((pos % s.S) != 0) {
+#pragma unroll
+      for (int q = 0; q < kItemsMax; ++q) {
+        const int it = (int)rank * 128 + tid2 + q * 128 * p.ksplit;
+        const int n = it >> 4, f0 = tile * kTileM + (it & 15) * 8;
+        if (it < 32 * 16 && n < p.batch && f0 < p.F) prefetch_sums(s, st, p, n, f0, pre[q]);
+      }
+    }
+
+    // Wait for the accumulator.
+    const bool okw = __all_sync(0xffffffffu, mbar_wait_bounded(&accum, 0));
+    if (!okw && lane == 0) {
+      s_bad = 1;
+      atomicExch(p.err, kDevErrWaitTimeout);
+    }
+    epi_barrier();
+    tc_fence_after();
+  }
+
+  // Epilogue, per chunk of 32 requests. Each CTA of the cluster (the splits of
+  // one row tile) leaves its fp32 partial of the chunk in its shared memory (the
+  // stages are idle by now); after a cluster barrier every CTA takes a share of
+  // the (request, 8-row group) items, sums the partials of all ranks in rank
+  // order (deterministic) through distributed shared memory, and stores them.
+  // A second barrier keeps every partial alive until the peers have read it.
+  {
     const int quarter = warp & 3;
-    const int f = tile * kTileM + quarter * 32 + lane;
+    const int row = quarter * 32 + lane;
     const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accum, 0));
-    ok = ok && !__any_sync(0xffffffffu, s_bad != 0);
-    if (!ok) {
-      if (lane == 0) {
-        s_bad = 1;
-        atomicExch(p.err, kDevErrWaitTimeout);
-      }
-    } else {
-      tc_fence_after();
-      float v[16];
-      if (p.ksplit == 1) {
-        for (int c0 = 0; c0 < p.npad; c0 += 16) {
-          __syncwarp();  // the load below is warp-collective; the stores above diverge
-          tmem_ld16(taddr + c0, v);
-          for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
-            if (n < p.batch && f < p.F) emit(s, st, p, f, n, v[j], blk, pos);
-          }
-        }
-      } else {
-        float* part = p.part + (long long)split * p.npad * p.Fpad;
-        for (int c0 = 0; c0 < p.npad; c0 += 16) {
-          __syncwarp();
-          tmem_ld16(taddr + c0, v);
-          for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
-            if (n < p.batch) part[(long long)n * p.Fpad + f] = v[j];
-          }
+    float* P = reinterpret_cast<float*>(sa);  // [32][128] fp32
+    const bool ok = (s_bad == 0);
+    for (int c0 = 0; c0 < p.batch; c0 += 32) {
+      if (warp >= 2 && ok) {
+        float v[16];
+        for (int cc = 0; cc < 32; cc += 16) {
+          if (c0 + cc >= p.batch) break;
+          tmem_ld16(taddr + c0 + cc, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) P[(cc + j) * kTileM + row] = v[j];
         }
       }
+      cluster_sync();
+      if (warp >= 2 && ok) {
+#pragma unroll
+        for (int q = 0; q < kItemsMax; ++q) {
+          const int it = (int)rank * 128 + tid2 + q * 128 * p.ksplit;
+          const int j = it >> 4, g = it & 15;
+          const int n = c0 + j, f0 = tile * kTileM + g * 8;
+          if (it >= 32 * 16 || n >= p.batch || f0 >= p.F) continue;
+          const void* local = P + j * kTileM + g * 8;
+          float v8[8];
+          for (int r = 0; r < p.ksplit; ++r) {
+            const uint32_t a = map_to_rank(local, (uint32_t)r);
+            const float4 x0 = ld_cluster_f4(a), x1 = ld_cluster_f4(a + 16);
+            const float t8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v8[e] = (r == 0) ? t8[e] : v8[e] + t8[e];
+          }
+          store_item(s, st, p, n, f0, v8, c0 == 0 ? pre[q] : nullptr, blk, pos);
+        }
+      }
+      cluster_sync();
     }
     tc_fence_before();
-    if (p.ksplit > 1) {
-      // The CTA that publishes a tile's last partial sums them all in split order.
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      // A CTA whose tile failed does not count itself: the tile is then never
-      // completed and the error word tells the host.
-      if (tid2 == 0) s_last = (s_bad == 0) && (atomicAdd(&p.counters[tile], 1) == p.ksplit - 1);
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (s_last) {
-        __threadfence();
-        for (int n = 0; n < p.batch; ++n) {
-          float y = 0.f;
-          for (int sp = 0; sp < p.ksplit; ++sp)
-            y += __ldcg(p.part + ((long long)sp * p.npad + n) * p.Fpad + f);
-          if (f < p.F) emit(s, st, p, f, n, y, blk, pos);
-        }
-        if (tid2 == 0) p.counters[tile] = 0;
-      }
-    }
   }
 
   __syncthreads();
@@ -342,6 +443,25 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(p.tmem_cols)
                  : "memory");
+  }
+}
+
+// Packed weights: tile (t, kb) = rows [128 t, 128 t + 128) x columns [64 kb, 64 kb + 64)
+// of W is 16 KB at ((t * kblocks + kb) * 16384); inside it row r's 16-byte chunk c
+// (columns 8c .. 8c + 7) sits at r * 128 + (c ^ (r % 8)) * 16, the 128-byte swizzle.
+// Rows past F are zeros. grid = (kblocks, tiles), 128 threads; thread r copies row r.
+__global__ void __launch_bounds__(128) frontend_pack_kernel(const __nv_bfloat16* __restrict__ w,
+                                                            uint8_t* __restrict__ packed, int F,
+                                                            int D) {
+  const int kb = blockIdx.x, t = blockIdx.y, r = threadIdx.x;
+  const int kblocks = gridDim.x;
+  const int row = t * kTileM + r;
+  uint8_t* dst = packed + ((long long)t * kblocks + kb) * kABytes + r * 128;
+  const int4* src = reinterpret_cast<const int4*>(w + (long long)row * D + kb * kTileK);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int4 v = (row < F) ? src[c] : make_int4(0, 0, 0, 0);
+    *reinterpret_cast<int4*>(dst + ((c ^ (r & 7)) * 16)) = v;
   }
 }
 
@@ -383,23 +503,76 @@ bool encode_rows(CUtensorMap* map, const void* base, long long rows, long long c
 
 bool frontend_available() { return encode_fn() != nullptr; }
 
-size_t frontend_smem_bytes(int npad) { return 1024 + (size_t)kStages * (kABytes + npad * 128); }
+int frontend_stages(int npad) {
+  const int per = kABytes + npad * 128;
+  int st = (205 * 1024) / per;
+  return st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
+}
 
-bool frontend_encode(FrontArgs& fa, const void* x, const void* w, int batch, int D, int F) {
-  return encode_rows(&fa.tx, x, batch, D, fa.p.npad) && encode_rows(&fa.tw, w, F, D, kTileM);
+size_t frontend_smem_bytes(int npad, int stages) {
+  return 1024 + (size_t)stages * (kABytes + npad * 128);
+}
+
+bool frontend_encode(FrontArgs& fa, const void* x, int batch, int D) {
+  return encode_rows(&fa.tx, x, batch, D, fa.p.npad);
+}
+
+size_t frontend_packed_bytes(int F, int D) {
+  return (size_t)((F + kTileM - 1) / kTileM) * (D / kTileK) * kABytes;
+}
+
+cudaError_t launch_frontend_pack(const void* w, void* packed, int F, int D, cudaStream_t stream) {
+  dim3 grid(D / kTileK, (F + kTileM - 1) / kTileM);
+  frontend_pack_kernel<<<grid, kTileM, 0, stream>>>(static_cast<const __nv_bfloat16*>(w),
+                                                    static_cast<uint8_t*>(packed), F, D);
+  return cudaGetLastError();
 }
 
 const void* frontend_kernel_ptr() { return reinterpret_cast<const void*>(frontend_kernel); }
 
+namespace {
+cudaLaunchConfig_t front_config(const FrontParams& p, cudaStream_t stream,
+                                cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3(p.tiles, p.ksplit, 1);
+  c.blockDim = dim3(kFrontThreads, 1, 1);
+  c.dynamicSmemBytes = frontend_smem_bytes(p.npad, p.stages);
+  c.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 1;
+  attr->val.clusterDim.y = (unsigned)p.ksplit;  // the splits of a row tile
+  attr->val.clusterDim.z = 1;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return c;
+}
+std::atomic<int> g_front_smem_lim[64];
+}  // namespace
+
+int frontend_max_clusters(const FrontParams& p) {
+  if (raise_smem_limit((const void*)frontend_kernel, frontend_smem_bytes(p.npad, p.stages),
+                       g_front_smem_lim) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t c = front_config(p, nullptr, &attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)frontend_kernel, &c) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t launch_frontend(const Shape& s, const State& st, const FrontArgs& fa,
                             cudaStream_t stream) {
-  const size_t smem = frontend_smem_bytes(fa.p.npad);
-  static std::atomic<int> lim[64];
-  cudaError_t err = raise_smem_limit((const void*)frontend_kernel, smem, lim);
+  cudaError_t err = raise_smem_limit((const void*)frontend_kernel,
+                                     frontend_smem_bytes(fa.p.npad, fa.p.stages), g_front_smem_lim);
   if (err != cudaSuccess) return err;
-  dim3 grid(fa.p.tiles, fa.p.ksplit);
-  frontend_kernel<<<grid, kFrontThreads, smem, stream>>>(fa.tw, fa.tx, s, st, fa.p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t c = front_config(fa.p, stream, &attr);
+  return cudaLaunchKernelEx(&c, frontend_kernel, fa.tx, s, st, fa.p);
 }
 
 }  // namespace nosa

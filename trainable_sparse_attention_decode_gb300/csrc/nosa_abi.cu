@@ -277,11 +277,9 @@ struct nosa_handle {
   double t_us[8];
   long long t_count = 0;
   long long launches = 0;  // kernels launched by decode steps
-  // Fused front-end buffers (allocated on the first nosa_decode_step_hidden).
+  // Fused front-end (set up on the first nosa_decode_step_hidden of a width).
   void* q_buf = nullptr;     // [batch][Hq][d] bf16 step queries
-  float* fe_part = nullptr;  // [ksplit][npad][Fpad] fp32 split partials
-  int* fe_cnt = nullptr;     // [tiles] tile counters
-  int fe_hidden = 0, fe_ksplit = 0;
+  int fe_hidden = 0, fe_ksplit = 0, fe_stages = 0;
 
   nosa_status fail(nosa_status code, const std::string& msg) {
     err = msg;
@@ -306,11 +304,8 @@ cudaError_t dev_alloc(nosa_handle* h, T** p, size_t bytes) {
 }
 
 void free_all(nosa_handle* h) {
-  for (void* p : {(void*)h->q_buf, (void*)h->fe_part, (void*)h->fe_cnt})
-    if (p) cudaFree(p);
+  if (h->q_buf) cudaFree(h->q_buf);
   h->q_buf = nullptr;
-  h->fe_part = nullptr;
-  h->fe_cnt = nullptr;
   for (void* p : h->dev_allocs) cudaFree(p);
   h->dev_allocs.clear();
   if (h->host_store) cudaFreeHost(h->host_store);
@@ -471,6 +466,8 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.part_ml, U * 2 * kMaxSplits * s.G * 2 * 4);
   A(&st.stats, sizeof(DevStats));
   A(&st.io, sizeof(StepIO));
+  A(&st.ksum, U * s.d * 4);
+  A(&st.esum, U * 4);
   if (e != cudaSuccess) {
     g_thread_err = std::string("device allocation failed: ") + cudaGetErrorString(e);
     cudaGetLastError();
@@ -497,6 +494,8 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(st.block_tab, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.tab_new, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.att_cnt, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.ksum, 0, U * s.d * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.esum, 0, U * 4);
   DevStats ds = fresh_stats();
   if (e == cudaSuccess) e = cudaMemcpy(st.stats, &ds, sizeof(ds), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
@@ -809,7 +808,7 @@ nosa_status run_step(nosa_handle* h, const StepArgs& args, const FrontArgs* fron
       StepArgs a = args;
       FrontArgs fa;
       void* kargs_append[3] = {const_cast<Shape*>(&h->s), &h->st, &a};
-      void* kargs_front[5] = {&fa.tw, &fa.tx, const_cast<Shape*>(&h->s), &h->st, &fa.p};
+      void* kargs_front[4] = {&fa.tx, const_cast<Shape*>(&h->s), &h->st, &fa.p};
       if (front) {
         fa = *front;
         kp.kernelParams = kargs_front;
@@ -884,8 +883,38 @@ size_t nosa_frontend_rows(const nosa_config* cfg) {
   return (size_t)(cfg->n_q_heads + 2 * cfg->n_kv_heads) * cfg->head_dim + cfg->n_kv_heads;
 }
 
-nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden, const void* w,
-                                    void* q_out, void* out, float* lse, void* stream) {
+size_t nosa_frontend_packed_bytes(const nosa_config* cfg, int32_t hidden) {
+  const size_t F = nosa_frontend_rows(cfg);
+  if (F == 0 || hidden < 64 || hidden > 65536 || hidden % 64 != 0) return 0;
+  return frontend_packed_bytes((int)F, hidden);
+}
+
+nosa_status nosa_frontend_pack(const nosa_config* cfg, int32_t hidden, const void* w,
+                               void* w_packed, void* stream) {
+  const size_t F = nosa_frontend_rows(cfg);
+  if (F == 0) { g_thread_err = "invalid configuration"; return NOSA_ERR_INVALID_ARG; }
+  if (hidden < 64 || hidden > 65536 || hidden % 64 != 0) {
+    g_thread_err = "hidden must be a multiple of 64 in [64, 65536]";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  if (!w || !w_packed || !aligned(w, 16) || !aligned(w_packed, 16)) {
+    g_thread_err = "w and w_packed must be non-NULL and 16-byte aligned";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  DeviceGuard guard(cfg->device);
+  const cudaError_t e = launch_frontend_pack(w, w_packed, (int)F, hidden,
+                                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("pack launch: ") + cudaGetErrorString(e);
+    return NOSA_ERR_CUDA;
+  }
+  return NOSA_OK;
+}
+
+nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden,
+                                    const void* w_packed, void* q_out, void* out, float* lse,
+                                    void* stream) {
+  const void* w = w_packed;
   if (!h) return NOSA_ERR_INVALID_ARG;
   const nosa_status cs = step_checks(h, out, lse);
   if (cs != NOSA_OK) return cs;
@@ -896,7 +925,7 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
   if (hidden < 64 || hidden > 65536 || hidden % 64 != 0)
     return h->fail(NOSA_ERR_INVALID_ARG, "hidden must be a multiple of 64 in [64, 65536]");
   if (!aligned(x, 16) || !aligned(w, 16) || (q_out && !aligned(q_out, 16)))
-    return h->fail(NOSA_ERR_INVALID_ARG, "x, w, q_out need 16-byte alignment");
+    return h->fail(NOSA_ERR_INVALID_ARG, "x, w_packed, q_out need 16-byte alignment");
   DeviceGuard guard(h->cfg.device);
   if (!frontend_available())
     return h->fail(NOSA_ERR_UNSUPPORTED, "the driver offers no tensor-map encoder");
@@ -904,27 +933,46 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
   const int tiles = (F + 127) / 128;
   const int kblocks = hidden / 64;
   const int npad = sh.batch <= 16 ? 16 : (sh.batch + 15) / 16 * 16;
-  int ksplit = std::max(1, std::min(std::min(kblocks, 8), sm_count_current() / tiles));
   if (h->fe_hidden != hidden) {
-    // (Re)size the front-end buffers: partials for this split count.
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
-    for (void** p : {(void**)&h->fe_part, (void**)&h->fe_cnt})
-      if (*p) cudaFree(*p), *p = nullptr;
-    e = cudaMalloc((void**)&h->fe_part, (size_t)ksplit * npad * tiles * 128 * 4);
-    if (e == cudaSuccess) e = cudaMalloc((void**)&h->fe_cnt, (size_t)tiles * 4);
-    if (e == cudaSuccess) e = cudaMemset(h->fe_cnt, 0, (size_t)tiles * 4);
-    if (e == cudaSuccess && !h->q_buf)
-      e = cudaMalloc(&h->q_buf, (size_t)sh.batch * sh.Hq * sh.d * 2);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      h->fe_hidden = 0;
-      return h->fail(NOSA_ERR_OOM, "front-end buffers");
+    // Splits per row tile (the cluster size): about one CTA per SM, at most 8,
+    // and every cluster resident at once (checked with the occupancy query).
+    // A shorter stage ring lets two CTAs share an SM, which raises the number
+    // of clusters that fit; the split count comes first, then the ring depth.
+    FrontParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.tiles = tiles;
+    q.npad = npad;
+    const int max_stages = frontend_stages(npad);
+    int ksplit = std::max(1, std::min(std::min(kblocks, 8), sm_count_current() / tiles));
+    if (const char* g = std::getenv("NOSA_FRONT_KSPLIT")) {  // tuning override
+      const int v = std::atoi(g);
+      if (v >= 1) ksplit = std::min(std::min(kblocks, 8), v);
+    }
+    auto fits = [&](int ks, int st) {
+      q.ksplit = ks;
+      q.stages = st;
+      return ks == 1 || frontend_max_clusters(q) >= tiles;
+    };
+    int stages = max_stages;
+    for (; ksplit > 1; --ksplit) {
+      for (stages = max_stages; stages >= 3 && !fits(ksplit, stages); --stages) {
+      }
+      if (stages >= 3) break;
+    }
+    if (ksplit == 1) stages = max_stages;
+    q.stages = stages;
+    if (!h->q_buf) {
+      const cudaError_t e = cudaMalloc(&h->q_buf, (size_t)sh.batch * sh.Hq * sh.d * 2);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return h->fail(NOSA_ERR_OOM, "front-end query buffer");
+      }
     }
     h->fe_hidden = hidden;
     h->fe_ksplit = ksplit;
+    h->fe_stages = q.stages;
   }
-  ksplit = h->fe_ksplit;
+  const int ksplit = h->fe_ksplit;
   FrontArgs fa;
   std::memset(&fa, 0, sizeof(fa));
   FrontParams& p = fa.p;
@@ -937,16 +985,16 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
   p.npad = npad;
   p.tmem_cols = 32;
   while (p.tmem_cols < npad) p.tmem_cols *= 2;
+  p.stages = h->fe_stages;
   p.batch = sh.batch;
   p.L_old = (int)h->L;
   p.q = q_out ? q_out : h->q_buf;
   p.out = out;
   p.lse = lse;
-  p.part = h->fe_part;
-  p.counters = h->fe_cnt;
   p.err = &h->st.stats->error;
-  if (!frontend_encode(fa, x, w, sh.batch, hidden, F))
-    return h->fail(NOSA_ERR_INVALID_ARG, "tensor-map encoding of x or w failed");
+  p.w_packed = static_cast<const uint8_t*>(w);
+  if (!frontend_encode(fa, x, sh.batch, hidden))
+    return h->fail(NOSA_ERR_INVALID_ARG, "tensor-map encoding of x failed");
   StepArgs args;
   std::memset(&args, 0, sizeof(args));
   args.q = p.q;

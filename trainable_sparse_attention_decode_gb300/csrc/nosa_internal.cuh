@@ -73,30 +73,34 @@ struct FrontParams {
   int F, Fpad;      // packed rows of W ((Hq + 2 Hkv) d + Hkv) and rows padded to the tile
   int D;            // hidden width (multiple of 64)
   int kblocks;      // D / 64
-  int ksplit;       // splits of the hidden width (<= kblocks)
+  int ksplit;       // splits of the hidden width (<= min(kblocks, 8)): one cluster per row tile
   int tiles;        // Fpad / 128
   int npad;         // batch padded to a multiple of 16 (the MMA's N)
   int tmem_cols;    // tensor-memory columns allocated (power of two >= max(32, npad))
+  int stages;       // TMA ring depth (frontend_stages)
   int batch;
   int L_old;        // context before this step's token
   void* q;          // [batch][Hq][d] bf16, written (the step's queries)
   void* out;        // published in StepIO
   float* lse;
-  float* part;      // [ksplit][npad][Fpad] fp32 split partials
-  int* counters;    // [tiles], self-resetting
   int* err;         // device error word
+  const uint8_t* w_packed;  // weights in the packed tile layout (frontend_pack)
 };
 struct FrontArgs {
-  CUtensorMap tw;   // W [F][D] bf16, box 64 x 128
-  CUtensorMap tx;   // x [batch][D] bf16, box 64 x npad
+  CUtensorMap tx;   // x [batch][D] bf16, box 64 x npad, 128-byte swizzle
   FrontParams p;
 };
 bool frontend_available();
-size_t frontend_smem_bytes(int npad);
-// Encodes fa.tx and fa.tw (fa.p.npad must be set). False if the driver's tensor-map
-// encoder is unavailable or rejects the arguments.
-bool frontend_encode(FrontArgs& fa, const void* x, const void* w, int batch, int D, int F);
+int frontend_stages(int npad);
+size_t frontend_smem_bytes(int npad, int stages);
+// Encodes fa.tx (fa.p.npad must be set). False if the driver's tensor-map encoder
+// is unavailable or rejects the arguments.
+bool frontend_encode(FrontArgs& fa, const void* x, int batch, int D);
+size_t frontend_packed_bytes(int F, int D);
+cudaError_t launch_frontend_pack(const void* w, void* packed, int F, int D, cudaStream_t stream);
 const void* frontend_kernel_ptr();
+// Clusters of the front-end that can be resident at once for these parameters (0 on error).
+int frontend_max_clusters(const FrontParams& p);
 
 struct State {
   uint8_t* slots;      // [U][k] block units (device)
@@ -123,6 +127,8 @@ struct State {
   float* part_ml;      // split-K partial (max, sum)
   DevStats* stats;
   StepIO* io;          // the current decode step's arguments
+  float* ksum;         // [U][d] fp32 running key sum of the open sub-block (token order)
+  float* esum;         // [U]    fp32 running eviction-logit sum of the open sub-block
 };
 
 // ---------------------------------------------------------------------------
