@@ -43,6 +43,11 @@ the plainest reading and says so at the spot (readings R1..R20):
       F = (Hq + 2 Hkv) d + Hkv (query heads, key heads, value heads, eviction).
 * R22 The projected q, k, v are stored in the handle's dtype (fp64 -> fp32 ->
       bf16, nearest even) and e in fp32, like the inputs of the plain step.
+* R23 Training-time forward: every query position t of a sequence is a decode
+      step with token t appended (causal): the dual selection with the
+      candidates and eligibility of that moment, then attention over the tokens
+      of Gamma(t)'s blocks plus those of t's own block up to t. Position 0 starts
+      from an empty context.
 
 Every other quantity is fp64.
 """
@@ -58,7 +63,7 @@ __all__ = [
     "HOST", "TAIL", "pool_block", "group_query", "block_scores", "decision_values",
     "top_m", "dual_select", "set_difference", "attend", "encode_payload",
     "payload_bytes", "UnitOracle", "pooled_keys_bf16", "round_bf16",
-    "frontend_rows", "project", "frontend_storage",
+    "frontend_rows", "project", "frontend_storage", "prefill_unit",
 ]
 
 
@@ -418,3 +423,45 @@ class UnitOracle:
     def block_payload(self, blk: int) -> np.ndarray:
         lo, hi = blk * self.B, (blk + 1) * self.B
         return encode_payload(self.k_raw[lo:hi], self.v_raw[lo:hi], self.e[lo:hi], self.dtype)
+
+
+# ----------------------------------------------------------------------------
+# Methodology §1: the locality constraint is imposed during training, so the
+# training-time forward applies the same dual selection causally at every query
+# position (R23).
+# ----------------------------------------------------------------------------
+def prefill_unit(k_raw: np.ndarray, v_raw: np.ndarray, e: np.ndarray, q_raw: np.ndarray,
+                 dtype: str, k: int, k_e: int, block: int = 64, sub_block: int = 16,
+                 positions=None, choose=None) -> dict:
+    """Training-time forward of one (request, KV head) unit over a sequence (R23).
+
+    k_raw, v_raw [L][d] and e [L] are the stored tokens, q_raw [L][G][d] the
+    stored queries. Positions are taken in order: token t is appended (R7), the
+    dual selection (R5, R6, R10, R12) runs on the candidates and eligibility of
+    that moment, eligibility becomes Gamma_e(t), and the attention (R9) covers the
+    blocks of Gamma(t) plus t's own block up to t. Returns {t: (g_e, g_q, out, lse)}
+    with out [G][d] and lse [G] for the positions in `positions` (every position by
+    default; the others carry None). choose(t, sq, se, elig, g_e, g_q) may return
+    a replacement (g_e, g_q): a harness adopting an equivalent choice at a near tie.
+    """
+    L, d = np.asarray(k_raw).shape
+    uo = UnitOracle(d, dtype, k, k_e, L, block, sub_block)
+    res = {}
+    for t in range(L):
+        if t == 0:
+            uo.append(k_raw[:1], v_raw[:1], e[:1])
+        else:
+            uo.begin_step(k_raw[t], v_raw[t], e[t])
+        sq, se = uo.scores(q_raw[t])
+        g_e, g_q, _ = uo.select(sq, se)
+        if choose is not None:
+            alt = choose(t, sq, se, uo.elig[:uo.n_cand].copy(), g_e, g_q)
+            if alt is not None:
+                g_e, g_q = alt
+        uo.commit(g_e, g_q)
+        if positions is None or t in positions:
+            out, lse = uo.attention(q_raw[t])
+            res[t] = (np.asarray(g_e), np.asarray(g_q), out, lse)
+        else:
+            res[t] = (np.asarray(g_e), np.asarray(g_q), None, None)
+    return res

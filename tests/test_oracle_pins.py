@@ -405,3 +405,80 @@ def test_frontend_storage_rounds_to_nearest_even():
     vals = (qs.astype(np.uint32) << np.uint32(16)).view(np.float32)
     assert list(vals) == [1.0, 1.0 + 2 ** -6, -2.5, 1.0 + 2 ** -7, 1.0]
     assert es.dtype == np.float32 and es[0] == np.float32(1.0 + 2 ** -8)
+
+
+# --------------------------------------------------------------------------
+# Training-time forward (R23)
+# --------------------------------------------------------------------------
+def _prefill_inputs(L, d, G, seed, e_scale=1.0):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((L, d)).astype(np.float32)
+    v = rng.standard_normal((L, d)).astype(np.float32)
+    e = (e_scale * rng.standard_normal(L)).astype(np.float32)
+    q = rng.standard_normal((L, G, d)).astype(np.float32)
+    return k, v, e, q
+
+
+def test_prefill_dense_equals_causal_sdpa():
+    # k larger than the number of blocks: every position attends to every earlier
+    # token, i.e. causal attention with the eviction logit as an additive bias.
+    L, d, G = 300, 16, 2
+    k, v, e, q = _prefill_inputs(L, d, G, 1)
+    res = O.prefill_unit(k, v, e, q, "f32", k=8, k_e=3)
+    kt = torch.tensor(k, dtype=torch.float64)
+    vt = torch.tensor(v, dtype=torch.float64)
+    qt = torch.tensor(q, dtype=torch.float64).permute(1, 0, 2)      # [G][L][d]
+    bias = torch.tensor(e, dtype=torch.float64)[None, :].expand(L, L).clone()
+    bias = bias.masked_fill(torch.triu(torch.ones(L, L, dtype=torch.bool), 1), float("-inf"))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt[None].expand(G, L, d), vt[None].expand(G, L, d), attn_mask=bias)
+    for t in (0, 1, 63, 64, 65, 127, 128, 200, 299):
+        assert np.allclose(res[t][2], ref[:, t].numpy(), atol=1e-12, rtol=0)
+
+
+def test_prefill_first_block_attends_causally():
+    L, d, G = 64, 8, 3
+    k, v, e, q = _prefill_inputs(L, d, G, 2)
+    res = O.prefill_unit(k, v, e, q, "f32", k=4, k_e=2)
+    for t in (0, 5, 63):
+        g_e, g_q, out, _ = res[t]
+        assert len(g_e) == 0 and len(g_q) == 0
+        ref, _ = O.attend(q[t].astype(np.float64), k[:t + 1].astype(np.float64),
+                          v[:t + 1].astype(np.float64), e[:t + 1].astype(np.float64))
+        assert np.allclose(out, ref, atol=1e-13, rtol=0)
+
+
+def test_prefill_eviction_sets_follow_the_block_recurrence():
+    # Distinct integer block eviction scores: Gamma_e at every position of block b
+    # is E_b with E_0 = {} and E_b = the k_e best of E_{b-1} + {b-1}, computed here
+    # by brute force on Python sets.
+    B, nblk, d, G, k_e = 64, 12, 8, 1, 4
+    rng = np.random.default_rng(3)
+    scores = rng.permutation(nblk).astype(np.float32)
+    e = np.repeat(scores, B)
+    L = nblk * B
+    k, v, _, q = _prefill_inputs(L, d, G, 4)
+    res = O.prefill_unit(k, v, e, q, "f32", k=6, k_e=k_e, positions=set())
+    E = set()
+    for b in range(nblk):
+        if b >= 1:
+            cand = sorted(E | {b - 1}, key=lambda j: (-scores[j], j))
+            E = set(cand[:k_e])
+        for t in range(b * B, (b + 1) * B):
+            assert set(int(x) for x in res[t][0]) == E, (b, t)
+
+
+def test_prefill_strict_eviction_and_budget():
+    L, d, G, kk, k_e = 64 * 14 + 9, 8, 2, 5, 3
+    k, v, e, q = _prefill_inputs(L, d, G, 5)
+    res = O.prefill_unit(k, v, e, q, "f32", k=kk, k_e=k_e, positions=set())
+    left = set()
+    prev = set()
+    for t in range(L):
+        g_e, g_q = set(int(x) for x in res[t][0]), set(int(x) for x in res[t][1])
+        n_cand = t // 64
+        assert not (g_e & g_q)
+        assert len(g_e | g_q) == min(kk, n_cand)
+        assert not (g_e & left)                     # once left out, never again
+        left |= prev - g_e
+        prev = g_e
