@@ -210,6 +210,34 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
                                     const void* w_packed, void* q_out, void* out, float* lse,
                                     void* stream);
 
+/*
+ * Training-time forward (NOSA technical summary, Methodology §1: the locality
+ * constraint is imposed during training, so the dual selection applies at every
+ * query position). For every position t of a sequence of seq_len tokens, with
+ * token t appended (causal): Gamma_e(t) = the k_e best eligible candidates by
+ * block eviction score, eligibility becoming Gamma_e(t) (strict eviction), and
+ * Gamma_q(t) = the k - |Gamma_e(t)| best other candidates by the two-stage pooled
+ * query score; the attention covers the blocks of Gamma(t) plus t's own block up
+ * to t, with the eviction logit added before the softmax. Position 0 starts from
+ * an empty context. Everything stays on the device; nothing is offloaded.
+ *   q    : device [batch][seq_len][n_q_heads][head_dim] cfg dtype
+ *   k, v : device [batch][seq_len][n_kv_heads][head_dim] cfg dtype
+ *   e    : device fp32 [batch][seq_len][n_kv_heads]
+ *   out  : device [batch][seq_len][n_q_heads][head_dim] cfg dtype (written)
+ *   lse  : device fp32 [batch][seq_len][n_q_heads] or NULL
+ *   sel  : device int32 [batch][seq_len][n_kv_heads][k] or NULL: the selection of
+ *          each position (Gamma_e ascending, then Gamma_q ascending, -1 pad)
+ *   workspace : device, nosa_prefill_workspace_bytes(cfg, seq_len) bytes,
+ *          256-byte aligned, owned by the caller (contents are scratch)
+ * seq_len in [1, cfg->max_context] and <= 131072. Async on stream. Errors:
+ * INVALID_ARG (sizes, NULL, alignment, workspace too small), UNSUPPORTED, CUDA.
+ */
+size_t nosa_prefill_workspace_bytes(const nosa_config* cfg, int32_t seq_len);
+nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const void* q,
+                                 const void* k, const void* v, const float* e, void* out,
+                                 float* lse, int32_t* sel, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Counters, host-readable. gamma_* covers steps after the first decode step
  * with at least k candidates; gamma(t) = |Gamma(t) ∩ R(t-1)| / k where R(t-1)
  * is the resident blocks plus the block that was the tail at t-1. */

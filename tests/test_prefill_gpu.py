@@ -1,0 +1,123 @@
+"""Parity of the training-time forward with the oracle, through the C ABI.
+
+Every position's selection (Gamma_e then Gamma_q) is compared with the oracle's
+(exact, except at near ties, where the oracle adopts the GPU's equivalent choice
+and carries on: the eviction sets carry over to later positions); the attention
+output within the decode path's tolerances on the checked positions.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import synth.gpu
+import trainable_sparse_attention_decode_gb300 as nosa
+from nosa_harness import near_tie_equivalent, attn_close, to_f64
+from oracle import nosa_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill(w, L, units=None, attn_every=1):
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                           max(L, 1))
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    k, v, e = synth.gpu.kv(w, 0, L)
+    q = synth.gpu.queries(w, L).permute(1, 0, 2, 3).contiguous()   # [batch][L][Hq][d]
+    out = torch.empty_like(q)
+    lse = torch.empty((w.batch, L, w.n_q_heads), dtype=torch.float32, device="cuda")
+    sel = torch.empty((w.batch, L, w.n_kv_heads, w.k), dtype=torch.int32, device="cuda")
+    nosa.nosa_prefill_forward(cfg, q, k, v, e, out, lse, sel)
+    torch.cuda.synchronize()
+    sel_h = sel.cpu().numpy()
+    out_h, lse_h = to_f64(out), lse.cpu().numpy().astype(np.float64)
+    G = w.group
+    units = range(w.units) if units is None else units
+    worst, worst_lse, ties = 0.0, 0.0, 0
+    for u in units:
+        b, h = divmod(u, w.n_kv_heads)
+        k_raw = synth.keys(w, b, h, 0, L)
+        v_raw = synth.values(w, b, h, 0, L)
+        e_raw = synth.evict(w, b, h, 0, L)
+        q_raw = synth.queries(w, b, range(h * G, (h + 1) * G), L)
+        tie_count = [0]
+
+        def choose(t, sq, se, elig, g_e, g_q):
+            row = sel_h[b, t, h]
+            ne, nq = len(g_e), len(g_q)
+            gpu_e, gpu_q = row[:ne], row[ne:ne + nq]
+            assert (row[ne + nq:] == -1).all(), f"unit {u} t {t}: selection longer than the oracle's"
+            n = len(sq)
+            eligible = [i for i in range(n) if elig[i]]
+            ok, tie = near_tie_equivalent(se, eligible, g_e, gpu_e)
+            assert ok, f"unit {u} t {t}: Gamma_e {sorted(gpu_e)} != oracle {sorted(g_e)}"
+            tie_count[0] += tie
+            ge = np.array(sorted(int(x) for x in gpu_e), dtype=np.int64)
+            rest = np.setdiff1d(np.arange(n), ge)
+            g_q_o = O.top_m(sq, rest, min(w.k - len(ge), len(rest)))
+            ok, tie = near_tie_equivalent(sq, rest, g_q_o, gpu_q)
+            assert ok, f"unit {u} t {t}: Gamma_q {sorted(gpu_q)} != oracle {sorted(g_q_o)}"
+            tie_count[0] += tie
+            assert list(gpu_e) == sorted(gpu_e) and list(gpu_q) == sorted(gpu_q)
+            return ge, np.array(sorted(int(x) for x in gpu_q), dtype=np.int64)
+
+        positions = set(range(0, L, attn_every)) | {L - 1}
+        res = O.prefill_unit(k_raw, v_raw, e_raw, q_raw, w.dtype, w.k, w.k_e,
+                             positions=positions, choose=choose)
+        ties += tie_count[0]
+        for t in sorted(positions):
+            o_ref, lse_ref = res[t][2], res[t][3]
+            rows = slice(h * G, (h + 1) * G)
+            worst = max(worst, attn_close(out_h[b, t, rows], o_ref, w.dtype))
+            worst_lse = max(worst_lse, float(np.max(np.abs(lse_h[b, t, rows] - lse_ref))))
+    assert worst <= 1.0, f"attention error / tolerance = {worst}"
+    assert worst_lse <= (1e-4 if w.dtype == "f32" else 1e-3)
+    return ties
+
+
+def test_tiny_f32_every_position():
+    w = synth.WORKLOADS["tiny-f32"]
+    _prefill(w, 2048 + 37)
+
+
+@pytest.mark.parametrize("L", [1, 37, 64, 65, 64 * 9])
+def test_short_sequences(L):
+    _prefill(synth.WORKLOADS["tiny-f32"], L)
+
+
+@pytest.mark.parametrize("k_e", [0, 8])
+def test_query_only_and_eviction_only(k_e):
+    w = synth.WORKLOADS["tiny-f32"].with_(k_e=k_e)
+    _prefill(w, 64 * 30 + 11)
+
+
+def test_1b_shape_sampled_units():
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=2)
+    _prefill(w, 8192 + 100, units=[0, 13], attn_every=7)
+
+
+def test_8b_shape_sampled_units():
+    w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=1)
+    _prefill(w, 4096 + 128 + 5, units=[0, 5], attn_every=11)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (12, 2, 64)])
+def test_group_variants(hq, hkv, d):
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+                                         k=16, k_e=12)
+    _prefill(w, 64 * 20 + 3, units=[0, hkv - 1], attn_every=3)
+
+
+def test_workspace_and_argument_errors():
+    cfg = nosa.nosa_config(1, 4, 1, 64, "f32", 8, 6, 1000)
+    assert nosa.nosa_prefill_workspace_bytes(cfg, 1001) == 0
+    assert nosa.nosa_prefill_workspace_bytes(cfg, 0) == 0
+    n = nosa.nosa_prefill_workspace_bytes(cfg, 500)
+    assert n > 0
+    ws = torch.empty(n - 256, dtype=torch.uint8, device="cuda")
+    q = torch.zeros((1, 500, 4, 64), device="cuda")
+    kv = torch.zeros((1, 500, 1, 64), device="cuda")
+    e = torch.zeros((1, 500, 1), device="cuda")
+    with pytest.raises(nosa.NosaError) as ei:
+        nosa.nosa_prefill_forward(cfg, q, kv, kv, e, torch.empty_like(q), workspace=ws)
+    assert ei.value.status == 1

@@ -23,7 +23,8 @@ __all__ = [
     "nosa_debug_read", "nosa_debug_size", "nosa_destroy", "nosa_last_error",
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
     "nosa_selftest_bounded_wait", "nosa_frontend_rows", "nosa_decode_step_hidden",
-    "nosa_frontend_packed_bytes", "nosa_frontend_pack",
+    "nosa_frontend_packed_bytes", "nosa_frontend_pack", "nosa_prefill_workspace_bytes",
+    "nosa_prefill_forward",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -91,6 +92,9 @@ def _load():
         "nosa_decode_step_hidden": (C.c_int, [VP, VP, I32, VP, VP, VP, VP, VP]),
         "nosa_frontend_packed_bytes": (SZ, [P(NosaConfig), I32]),
         "nosa_frontend_pack": (C.c_int, [P(NosaConfig), I32, VP, VP, VP]),
+        "nosa_prefill_workspace_bytes": (SZ, [P(NosaConfig), I32]),
+        "nosa_prefill_forward": (C.c_int, [P(NosaConfig), I32, VP, VP, VP, VP, VP, VP, VP, VP,
+                                           SZ, VP]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -242,6 +246,34 @@ def nosa_decode_step_hidden(h, x, w_packed, out, lse=None, q_out=None, stream=No
         _ptr(q_out, qs, torch.bfloat16, "q_out", allow_none=True),
         _ptr(out, qs, torch.bfloat16, "out"),
         _ptr(lse, qs[:2], torch.float32, "lse", 4, allow_none=True), _stream(stream)), h)
+
+
+def nosa_prefill_workspace_bytes(cfg: NosaConfig, seq_len: int) -> int:
+    return int(lib.nosa_prefill_workspace_bytes(C.byref(cfg), seq_len))
+
+
+def nosa_prefill_forward(cfg: NosaConfig, q, k, v, e, out, lse=None, sel=None, workspace=None,
+                         stream=None):
+    """Training-time forward over whole sequences: q [batch][L][Hq][d], k, v
+    [batch][L][Hkv][d], e [batch][L][Hkv] fp32; writes out (and lse, sel if given).
+    Returns the workspace (allocated here when not passed)."""
+    torch = _torch()
+    dt = _dtype_of(cfg)
+    L = q.shape[1]
+    qs = (cfg.batch, L, cfg.n_q_heads, cfg.head_dim)
+    ks = (cfg.batch, L, cfg.n_kv_heads, cfg.head_dim)
+    need = nosa_prefill_workspace_bytes(cfg, L)
+    if need == 0:
+        raise NosaError(1, nosa_last_error() or "invalid configuration or length")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.nosa_prefill_forward(
+        C.byref(cfg), L, _ptr(q, qs, dt, "q"), _ptr(k, ks, dt, "k"), _ptr(v, ks, dt, "v"),
+        _ptr(e, ks[:3], torch.float32, "e", 4), _ptr(out, qs, dt, "out"),
+        _ptr(lse, qs[:3], torch.float32, "lse", 4, allow_none=True),
+        _ptr(sel, ks[:3] + (cfg.k,), torch.int32, "sel", 4, allow_none=True),
+        _ptr(workspace, None, torch.uint8, "workspace", 256), workspace.numel(), _stream(stream)))
+    return workspace
 
 
 def nosa_stats(h) -> dict:

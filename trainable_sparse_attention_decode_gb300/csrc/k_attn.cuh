@@ -57,6 +57,8 @@ struct AttnKParams {
   float qscale;  // log2(e) / sqrt(d)
   int* err;
   const StepIO* dyn;  // decode step: q, out, lse, tail_len and the tail offset live here
+  const int32_t* tail_tab;   // per-unit tail unit index (or null)
+  const int32_t* tail_lens;  // per-unit tail length
 };
 
 template <typename T> struct Unpack16;
@@ -136,6 +138,10 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
     lse = p.dyn->lse;
     tail_len = p.dyn->tail_len;
     if (tail != nullptr) tail += p.dyn->tail_off;
+  }
+  if (p.tail_tab != nullptr) {  // per-unit tail (p.tail_stride is 0)
+    tail = p.units + (long long)p.tail_tab[p.unit_base + blockIdx.y] * p.payload;
+    tail_len = p.tail_lens[p.unit_base + blockIdx.y];
   }
   // Virtual item list: the n_blocks table entries, then the tail (if any),
   // spread evenly over the splits.
@@ -369,6 +375,26 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   }
   __syncthreads();
   const int nst = p.nsplit_total;
+  if (nst == 1) {  // a single partial: it is the output (same arithmetic as the merge)
+    for (int i = tid; i < G * D; i += NT) {
+      const int g = i / D, dim = i % D;
+      float M = red_m[g];
+#pragma unroll
+      for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w * G + g]);
+      float A = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float sc = exp2f(red_m[w * G + g] - M);
+        A += red_acc[(w * G + g) * D + dim] * sc;
+        L += red_l[w * G + g] * sc;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const long long row = (long long)b * p.Hq + (long long)h * G + g;
+      reinterpret_cast<T*>(out)[row * D + dim] = from_f32<T>(A * inv);
+      if (dim == 0 && lse != nullptr) lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    return;
+  }
   const long long pbase = ((long long)u * nst + p.split_base + sp) * G;
   for (int i = tid; i < G * D; i += NT) {
     const int g = i / D, dim = i % D;
@@ -465,6 +491,8 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.qscale = (float)(1.4426950408889634 / sqrt((double)D));
   p.err = a.err;
   p.dyn = a.dyn;
+  p.tail_tab = a.tail_tab;
+  p.tail_lens = a.tail_lens;
   const size_t smem = AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps);
   static std::atomic<int> lim[64];
   cudaError_t err = raise_smem_limit((const void*)attn_split_kernel<T, D, G, W>, smem, lim);

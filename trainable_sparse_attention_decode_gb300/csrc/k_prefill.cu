@@ -1,0 +1,348 @@
+// Training-time forward of NOSA (every query position of a sequence is a step).
+//
+// NOSA technical summary, Methodology §1: the locality constraint is imposed
+// during training, so the dual selection runs causally at every query position t
+// with token t appended: Gamma_e(t) = top-k_e of the eligible candidates by
+// eviction score (strict eviction: eligibility <- Gamma_e(t)), Gamma_q(t) = the
+// best k - |Gamma_e(t)| other candidates by the two-stage pooled query score; the
+// attention covers the blocks of Gamma(t) plus t's own block up to t.
+//
+// Candidates change only when a block completes, and Gamma_e does not depend on
+// the query, so Gamma_e is the same E_b for all 64 positions of block b and
+// follows a short recurrence over blocks: E_0 = {}, E_b = top-k_e(E_{b-1} + {b-1}).
+// The path:
+//   prefill_pack_kernel    block units (the decode layout), pooled keys and block
+//                          eviction scores of every block            (unit, block)
+//   prefill_evict_kernel   the E_b recurrence, one warp per unit
+//   prefill_select_kernel  per position: pooled query scores of the candidates
+//                          outside E_b, top-(k - |E_b|) by warp arg-max; writes
+//                          the position's block table and tail     (unit, block)
+//   attn_split_kernel      the split-K attention of the decode path, one virtual
+//                          unit per (request, position, KV head), with per-unit
+//                          tails (the causal partial block).
+#include "nosa_internal.cuh"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+
+namespace nosa {
+namespace {
+
+constexpr int kPackThreads = 256;
+constexpr int kSelWarps = 8;
+
+// Block unit of (unit u, block blk) from k, v [batch][L][Hkv][d], e [batch][L][Hkv];
+// tokens past L are zeros. Complete blocks are pooled: sub-block mean keys (fp32
+// token-order sums x 1/16) and the block's eviction score (max of the sub-block
+// means of e). grid = (nblk, U).
+template <typename T>
+__global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
+    Shape s, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ e, int L,
+    int nblk, uint8_t* __restrict__ units, float* __restrict__ pk, float* __restrict__ se) {
+  const int blk = blockIdx.x, u = blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
+  uint8_t* unit = units + ((long long)u * nblk + blk) * s.payload;
+  const int t0 = blk * s.B;
+  const int nt = min(s.B, L - t0);
+  for (int i = threadIdx.x; i < s.B * s.d; i += blockDim.x) {
+    const int t = i / s.d, dim = i % s.d;
+    T kv = from_f32<T>(0.f), vv = from_f32<T>(0.f);
+    if (t < nt) {
+      const long long src = (((long long)b * L + t0 + t) * s.Hkv + h) * s.d + dim;
+      kv = k[src];
+      vv = v[src];
+    }
+    *reinterpret_cast<T*>(unit + k_off(t, dim, s.B, s.elt)) = kv;
+    *reinterpret_cast<T*>(unit + v_off(t, dim, s.B, s.d, s.elt)) = vv;
+  }
+  for (int t = threadIdx.x; t < s.B; t += blockDim.x)
+    *reinterpret_cast<float*>(unit + e_off(t, s.B, s.d, s.elt)) =
+        (t < nt) ? e[((long long)b * L + t0 + t) * s.Hkv + h] : 0.f;
+  for (long long i = 2LL * s.B * s.d * s.elt + 4LL * s.B + threadIdx.x; i < s.payload; i += blockDim.x)
+    unit[i] = 0;
+  if (nt < s.B) return;  // an incomplete block is never a candidate
+  for (int i = threadIdx.x; i < s.P * s.d; i += blockDim.x) {
+    const int sb = i / s.d, dim = i % s.d;
+    float acc = 0.f;
+    for (int j = 0; j < s.S; ++j) {
+      const long long src = (((long long)b * L + t0 + sb * s.S + j) * s.Hkv + h) * s.d + dim;
+      acc += to_f32(k[src]);
+    }
+    pk[(((long long)u * nblk + blk) * s.P + sb) * s.d + dim] = acc * (1.0f / s.S);
+  }
+  if (threadIdx.x == 0) {
+    float best = 0.f;
+    for (int sb = 0; sb < s.P; ++sb) {
+      float acc = 0.f;
+      for (int j = 0; j < s.S; ++j) acc += e[((long long)b * L + t0 + sb * s.S + j) * s.Hkv + h];
+      const float m = acc * (1.0f / s.S);
+      best = (sb == 0) ? m : fmaxf(best, m);
+    }
+    se[(long long)u * nblk + blk] = best;
+  }
+}
+
+// The eviction sets: for every block b with positions, E_b (ascending block ids)
+// into Eb[u][b][k_e] and its size into Ecnt[u][b]. One warp per unit; the set is
+// kept in shared memory in ascending order (a new candidate is always the
+// largest id); when it exceeds k_e the lowest score leaves (at equal scores the
+// higher id, so the lower index wins).
+__global__ void __launch_bounds__(128) prefill_evict_kernel(Shape s, const float* __restrict__ se,
+                                                            int nblk, int32_t* __restrict__ Eb,
+                                                            int32_t* __restrict__ Ecnt) {
+  extern __shared__ int32_t ev_ids[];  // [4 warps][k_e + 1]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * 4 + warp;
+  if (u >= s.U) return;
+  int32_t* ids = ev_ids + warp * (s.ke + 1);
+  const float* seu = se + (long long)u * nblk;
+  int cnt = 0;
+  for (int b = 0; b < nblk; ++b) {
+    if (b >= 1 && s.ke > 0) {
+      if (lane == 0) ids[cnt] = b - 1;
+      __syncwarp();
+      ++cnt;
+      if (cnt > s.ke) {
+        // arg-min by (score, then larger id), over the cnt entries
+        float best = INFINITY;
+        int bpos = -1, bid = -1;
+        for (int i = lane; i < cnt; i += 32) {
+          const float x = seu[ids[i]];
+          if (x < best || (x == best && ids[i] > bid)) {
+            best = x;
+            bid = ids[i];
+            bpos = i;
+          }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+          const int opos = __shfl_xor_sync(0xffffffffu, bpos, o);
+          if (ob < best || (ob == best && oid > bid)) {
+            best = ob;
+            bid = oid;
+            bpos = opos;
+          }
+        }
+        // remove position bpos (keeps the ascending order)
+        int32_t carry[9];
+        const int nchunk = (cnt + 31) / 32;
+        for (int c = 0; c < nchunk && c < 9; ++c) {
+          const int i = c * 32 + lane + 1;
+          carry[c] = (i < cnt) ? ids[i] : 0;
+        }
+        __syncwarp();
+        for (int c = 0; c < nchunk && c < 9; ++c) {
+          const int i = c * 32 + lane;  // destination of element i + 1
+          if (i + 1 < cnt && i >= bpos) ids[i] = carry[c];
+        }
+        __syncwarp();
+        --cnt;
+      }
+    }
+    int32_t* out = Eb + ((long long)u * nblk + b) * s.ke;
+    for (int i = lane; i < cnt; i += 32) out[i] = ids[i];
+    if (lane == 0) Ecnt[(long long)u * nblk + b] = cnt;
+    __syncwarp();
+  }
+}
+
+// Per position t of block b (CTA (b, u); warp w takes positions 64 b + w, + 8, ...):
+// q_bar = mean of the G query heads, sq(j) = max over sub-blocks of
+// q_bar . K_bar[j][s] / sqrt(d) for candidates j < b outside E_b, then the
+// top-(k - |E_b|) by repeated warp arg-max (ties: lower index). Writes the
+// position's selection (E_b ascending, then Gamma_q ascending, -1 pad) into sel,
+// its attention block table (unit indices) and tail.
+template <typename T>
+__global__ void __launch_bounds__(kSelWarps * 32) prefill_select_kernel(
+    Shape s, const T* __restrict__ q, int L, int nblk, const float* __restrict__ pk,
+    const int32_t* __restrict__ Eb, const int32_t* __restrict__ Ecnt, int32_t* __restrict__ sel,
+    int32_t* __restrict__ block_tab, int32_t* __restrict__ tail_tab, int32_t* __restrict__ tail_len,
+    float inv_sqrt_d) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const int b = blockIdx.x, u = blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
+  const int W = (nblk + 31) / 32;
+  uint32_t* emask = reinterpret_cast<uint32_t*>(sm);             // [W] E_b membership
+  float* qbar_s = reinterpret_cast<float*>(emask + ((W + 3) & ~3));  // [kSelWarps][d]
+  float* sq_s = qbar_s + kSelWarps * s.d;                         // [kSelWarps][nblk]
+  uint32_t* taken_s = reinterpret_cast<uint32_t*>(sq_s + (long long)kSelWarps * nblk);  // [kSelWarps][W]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ecnt = Ecnt[(long long)u * nblk + b];
+  const int32_t* eb = Eb + ((long long)u * nblk + b) * s.ke;
+  for (int i = threadIdx.x; i < W; i += blockDim.x) emask[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < ecnt; i += blockDim.x) atomicOr(&emask[eb[i] >> 5], 1u << (eb[i] & 31));
+  __syncthreads();
+  const int n_cand = b;  // blocks before the position's own block
+  const int n_rest = n_cand - ecnt;
+  const int m = min(s.k - ecnt, n_rest);
+  float* qb = qbar_s + warp * s.d;
+  float* sqw = sq_s + (long long)warp * nblk;
+  uint32_t* tk = taken_s + warp * W;
+  const float inv_g = 1.0f / (float)s.G;
+  for (int p = warp; p < s.B; p += kSelWarps) {
+    const int t = b * s.B + p;
+    if (t >= L) break;
+    const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
+    // q_bar of the group
+    const T* qg = q + (((long long)req * L + t) * s.Hq + (long long)h * s.G) * s.d;
+    for (int dim = lane; dim < s.d; dim += 32) {
+      float acc = 0.f;
+      for (int g = 0; g < s.G; ++g) acc += to_f32(qg[g * s.d + dim]);
+      qb[dim] = acc * inv_g;
+    }
+    for (int i = lane; i < W; i += 32) tk[i] = 0u;
+    __syncwarp();
+    // scores of the candidates outside E_b: 8 lanes per pooled row, 4 rows
+    if (m > 0) {
+      const int r = lane >> 3, c = lane & 7;
+      for (int j = 0; j < n_cand; ++j) {
+        if ((emask[j >> 5] >> (j & 31)) & 1u) continue;
+        const float* row = pk + (((long long)u * nblk + j) * s.P + r) * s.d;
+        float acc = 0.f;
+        for (int dim = c * 4; dim < s.d; dim += 32) {
+          const float4 x = *reinterpret_cast<const float4*>(row + dim);
+          acc = fmaf(x.x, qb[dim], acc);
+          acc = fmaf(x.y, qb[dim + 1], acc);
+          acc = fmaf(x.z, qb[dim + 2], acc);
+          acc = fmaf(x.w, qb[dim + 3], acc);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc = fmaxf(acc, __shfl_xor_sync(0xffffffffu, acc, 8));
+        acc = fmaxf(acc, __shfl_xor_sync(0xffffffffu, acc, 16));
+        if (lane == 0) sqw[j] = acc * inv_sqrt_d;
+      }
+      __syncwarp();
+      // top-m: m rounds of warp arg-max over the untaken candidates outside E_b
+      for (int round = 0; round < m; ++round) {
+        float best = -INFINITY;
+        int bid = 0x7fffffff;
+        for (int j = lane; j < n_cand; j += 32) {
+          const uint32_t bit = 1u << (j & 31);
+          if ((emask[j >> 5] & bit) || (tk[j >> 5] & bit)) continue;
+          const float x = sqw[j];
+          if (x > best || (x == best && j < bid)) {
+            best = x;
+            bid = j;
+          }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+          if (ob > best || (ob == best && oid < bid)) {
+            best = ob;
+            bid = oid;
+          }
+        }
+        if (lane == 0 && bid < n_cand) tk[bid >> 5] |= 1u << (bid & 31);  // (none left: NaN scores)
+        __syncwarp();
+      }
+    }
+    // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the mask)
+    int32_t* selp = sel ? sel + vu * s.k : nullptr;
+    int32_t* tab = block_tab + vu * s.k;
+    const long long ubase = (long long)u * nblk;
+    for (int i = lane; i < ecnt; i += 32) {
+      if (selp) selp[i] = eb[i];
+      tab[i] = (int32_t)(ubase + eb[i]);
+    }
+    int run = ecnt;
+    for (int base = 0; base < n_cand; base += 32) {
+      const int j = base + lane;
+      const bool on = (j < n_cand) && ((tk[j >> 5] >> (j & 31)) & 1u);
+      const unsigned bal = __ballot_sync(0xffffffffu, on);
+      if (on) {
+        const int at = run + __popc(bal & ((1u << lane) - 1u));
+        if (selp) selp[at] = j;
+        tab[at] = (int32_t)(ubase + j);
+      }
+      run += __popc(bal);
+    }
+    for (int i = run + lane; i < s.k; i += 32) {
+      if (selp) selp[i] = -1;
+      tab[i] = -1;
+    }
+    if (lane == 0) {
+      tail_tab[vu] = (int32_t)(ubase + b);
+      tail_len[vu] = p + 1;
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+// Byte offsets of the training-time forward's workspace (each 256-byte aligned).
+PrefillLayout prefill_layout(const Shape& s, int L, int nsplit) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  PrefillLayout w;
+  const int nblk = (L + s.B - 1) / s.B;
+  const size_t U = s.U, V = (size_t)s.U * L;  // units, virtual units (request, position, head)
+  size_t off = 0;
+  w.units = off;     off += up(U * nblk * (size_t)s.payload);
+  w.pk = off;        off += up(U * nblk * s.P * s.d * 4);
+  w.se = off;        off += up(U * nblk * 4);
+  w.eb = off;        off += up(U * nblk * (size_t)std::max(s.ke, 1) * 4);
+  w.ecnt = off;      off += up(U * nblk * 4);
+  w.tab = off;       off += up(V * s.k * 4);
+  w.tail_tab = off;  off += up(V * 4);
+  w.tail_len = off;  off += up(V * 4);
+  w.part_acc = off;  off += nsplit > 1 ? up(V * nsplit * s.G * s.d * 4) : 0;
+  w.part_ml = off;   off += nsplit > 1 ? up(V * nsplit * s.G * 2 * 4) : 0;
+  w.counters = off;  off += up(V * 4);
+  w.err = off;       off += 256;
+  w.total = off;
+  return w;
+}
+
+size_t prefill_select_smem(const Shape& s, int nblk) {
+  const int W = (nblk + 31) / 32;
+  return (size_t)((W + 3) & ~3) * 4 + (size_t)kSelWarps * s.d * 4 + (size_t)kSelWarps * nblk * 4 +
+         (size_t)kSelWarps * W * 4;
+}
+
+cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
+                                 const void* v, const float* e, int32_t* sel, uint8_t* ws,
+                                 const PrefillLayout& w, cudaStream_t stream) {
+  const int nblk = (L + s.B - 1) / s.B;
+  uint8_t* units = ws + w.units;
+  float* pk = reinterpret_cast<float*>(ws + w.pk);
+  float* se = reinterpret_cast<float*>(ws + w.se);
+  int32_t* Eb = reinterpret_cast<int32_t*>(ws + w.eb);
+  int32_t* Ecnt = reinterpret_cast<int32_t*>(ws + w.ecnt);
+  dim3 grid(nblk, s.U);
+  if (s.dtype == 0)
+    prefill_pack_kernel<float><<<grid, kPackThreads, 0, stream>>>(
+        s, (const float*)k, (const float*)v, e, L, nblk, units, pk, se);
+  else
+    prefill_pack_kernel<__nv_bfloat16><<<grid, kPackThreads, 0, stream>>>(
+        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t esmem = (size_t)4 * (s.ke + 1) * 4;
+  prefill_evict_kernel<<<(s.U + 3) / 4, 128, esmem, stream>>>(s, se, nblk, Eb, Ecnt);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem = prefill_select_smem(s, nblk);
+  static std::atomic<int> lim32[64], lim16[64];
+  const float isd = (float)(1.0 / sqrt((double)s.d));
+  int32_t* tab = reinterpret_cast<int32_t*>(ws + w.tab);
+  int32_t* ttab = reinterpret_cast<int32_t*>(ws + w.tail_tab);
+  int32_t* tlen = reinterpret_cast<int32_t*>(ws + w.tail_len);
+  if (s.dtype == 0) {
+    err = raise_smem_limit((const void*)prefill_select_kernel<float>, smem, lim32);
+    if (err != cudaSuccess) return err;
+    prefill_select_kernel<float><<<grid, kSelWarps * 32, smem, stream>>>(
+        s, (const float*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd);
+  } else {
+    err = raise_smem_limit((const void*)prefill_select_kernel<__nv_bfloat16>, smem, lim16);
+    if (err != cudaSuccess) return err;
+    prefill_select_kernel<__nv_bfloat16><<<grid, kSelWarps * 32, smem, stream>>>(
+        s, (const __nv_bfloat16*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nosa

@@ -1197,6 +1197,102 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
   return NOSA_OK;
 }
 
+namespace {
+Shape prefill_virtual_shape(const Shape& s, int L) {
+  Shape sv = s;  // one virtual unit per (request, position, KV head)
+  sv.batch = s.batch * L;
+  sv.U = s.batch * L * s.Hkv;
+  return sv;
+}
+nosa_status prefill_checks(const nosa_config* cfg, int32_t seq_len) {
+  std::string why;
+  const nosa_status vs = validate(cfg, why);
+  if (vs != NOSA_OK) {
+    g_thread_err = why;
+    return vs;
+  }
+  if (seq_len < 1 || seq_len > cfg->max_context) {
+    g_thread_err = "seq_len must be in [1, max_context]";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  if (seq_len > 131072 || (long long)cfg->batch * seq_len * cfg->n_kv_heads > (1LL << 30)) {
+    g_thread_err = "seq_len must be <= 131072 and batch * seq_len * n_kv_heads <= 2^30";
+    return NOSA_ERR_UNSUPPORTED;
+  }
+  return NOSA_OK;
+}
+}  // namespace
+
+size_t nosa_prefill_workspace_bytes(const nosa_config* cfg, int32_t seq_len) {
+  if (prefill_checks(cfg, seq_len) != NOSA_OK) return 0;
+  DeviceGuard guard(cfg->device);
+  const Shape s = shape_of(*cfg);
+  const int nsplit = attention_pick_nsplit(prefill_virtual_shape(s, seq_len), s.k, 1);
+  return prefill_layout(s, seq_len, nsplit).total;
+}
+
+nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const void* q,
+                                 const void* k, const void* v, const float* e, void* out,
+                                 float* lse, int32_t* sel, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  const nosa_status cs = prefill_checks(cfg, seq_len);
+  if (cs != NOSA_OK) return cs;
+  if (!q || !k || !v || !e || !out || !workspace) {
+    g_thread_err = "NULL argument";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(e, 4) || (lse && !aligned(lse, 4)) || (sel && !aligned(sel, 4)) ||
+      !aligned(workspace, 256)) {
+    g_thread_err = "misaligned pointer (q, k, v, out 16 bytes; workspace 256 bytes)";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  DeviceGuard guard(cfg->device);
+  const Shape s = shape_of(*cfg);
+  const Shape sv = prefill_virtual_shape(s, seq_len);
+  const int nsplit = attention_pick_nsplit(sv, s.k, 1);
+  const PrefillLayout w = prefill_layout(s, seq_len, nsplit);
+  if (workspace_bytes < w.total) {
+    g_thread_err = "workspace too small (see nosa_prefill_workspace_bytes)";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int nblk = (seq_len + s.B - 1) / s.B;
+  cudaError_t err = cudaMemsetAsync(ws + w.counters, 0, w.err + 256 - w.counters, st);
+  if (err == cudaSuccess) err = launch_prefill_front(s, seq_len, q, k, v, e, sel, ws, w, st);
+  AttnArgs a;
+  a.units = ws + w.units;
+  a.n_units = (long long)s.U * nblk;
+  a.block_tab = reinterpret_cast<const int32_t*>(ws + w.tab);
+  a.n_blocks = s.k;
+  a.tail = ws + w.units;
+  a.tail_stride = 0;
+  a.tail_len = 0;
+  a.q = q;
+  a.out = out;
+  a.lse = lse;
+  a.part_acc = reinterpret_cast<float*>(ws + w.part_acc);
+  a.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  a.nsplit = nsplit;
+  a.split_base = 0;
+  a.nsplit_total = nsplit;
+  a.counters = reinterpret_cast<int*>(ws + w.counters);
+  a.err = reinterpret_cast<int*>(ws + w.err);
+  a.tail_tab = reinterpret_cast<const int32_t*>(ws + w.tail_tab);
+  a.tail_lens = reinterpret_cast<const int32_t*>(ws + w.tail_len);
+  for (long long base = 0; base < sv.U && err == cudaSuccess; base += 65535) {
+    a.unit_base = (int)base;
+    a.unit_count = (int)std::min<long long>(65535, sv.U - base);
+    err = launch_attention(sv, a, st);
+  }
+  if (err != cudaSuccess) {
+    g_thread_err = std::string("training-time forward launch: ") + cudaGetErrorString(err);
+    return NOSA_ERR_CUDA;
+  }
+  return NOSA_OK;
+}
+
 }  // extern "C"
 
 extern "C" nosa_status nosa_selftest_bounded_wait(int32_t device, int64_t limit_ns,

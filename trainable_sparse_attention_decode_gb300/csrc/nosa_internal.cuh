@@ -102,6 +102,19 @@ const void* frontend_kernel_ptr();
 // Clusters of the front-end that can be resident at once for these parameters (0 on error).
 int frontend_max_clusters(const FrontParams& p);
 
+// Training-time forward (k_prefill.cu): byte offsets into the caller's workspace.
+struct PrefillLayout {
+  size_t units, pk, se, eb, ecnt, tab, tail_tab, tail_len, part_acc, part_ml, counters, err, total;
+};
+// s describes the real units (batch * Hkv); L is the sequence length.
+PrefillLayout prefill_layout(const Shape& s, int L, int nsplit);
+size_t prefill_select_smem(const Shape& s, int nblk);
+// Packs, pools, runs the eviction-set recurrence and the per-position selection;
+// sel (optional) receives the selections [batch][L][Hkv][k].
+cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
+                                 const void* v, const float* e, int32_t* sel, uint8_t* ws,
+                                 const PrefillLayout& w, cudaStream_t stream);
+
 struct State {
   uint8_t* slots;      // [U][k] block units (device)
   uint8_t* tail;       // [U][2] block units (device); block b lives in buffer b % 2
@@ -182,6 +195,10 @@ struct AttnArgs {
   // Decode step: q, out, lse and tail_len come from *dyn, and the tail pointer
   // (when not null) is offset by dyn->tail_off. Null for the standalone call.
   const StepIO* dyn = nullptr;
+  // Per-unit tails (training-time forward): unit u's tail is units[tail_tab[u]]
+  // with tail_lens[u] tokens (tail must be non-null; tail_stride is then 0).
+  const int32_t* tail_tab = nullptr;
+  const int32_t* tail_lens = nullptr;
 };
 size_t attention_workspace_bytes(const Shape& s, int nsplit);
 int attention_pick_nsplit(const Shape& s, int n_blocks, int has_tail);
