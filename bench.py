@@ -296,6 +296,74 @@ def run_fullattn(args, rank, world, local_rank):
             "gpu_launches": K}
 
 
+def run_prefill(args, rank, world, local_rank):
+    """Training-time forward (causal dual selection at every position, then the
+    block-sparse attention) over whole sequences of the workload's shape. One step
+    = one nosa_prefill_forward over batch x L tokens."""
+    import torch
+    import synth
+    import synth.gpu
+    import trainable_sparse_attention_decode_gb300 as nosa
+    torch.cuda.set_device(local_rank)
+    w = synth.WORKLOADS[args.workload].with_(batch=args.batch or 1)
+    L = args.prompt or 32768
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e, L,
+                           device=local_rank)
+    k, v, e = synth.gpu.kv(w, 0, L)
+    q = synth.gpu.queries(w, L).permute(1, 0, 2, 3).contiguous()
+    out = torch.empty_like(q)
+    lse = torch.empty((w.batch, L, w.n_q_heads), dtype=torch.float32, device="cuda")
+    ws = torch.empty(nosa.nosa_prefill_workspace_bytes(cfg, L), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    W, K = args.warmup, max(1, min(args.steps, 20))
+    for _ in range(W):
+        nosa.nosa_prefill_forward(cfg, q, k, v, e, out, lse, workspace=ws, stream=stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(K):
+        nosa.nosa_prefill_forward(cfg, q, k, v, e, out, lse, workspace=ws, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    secs = ev0.elapsed_time(ev1) / 1e3 / K
+    max_secs, tokens = aggregate(secs, w.batch * L, world)
+    if rank != 0:
+        return None
+    elt = 2 if w.dtype == "bf16" else 4
+    payload = nosa.nosa_payload_bytes(cfg)
+    nblk = (L + 63) // 64
+    # bytes the attention reads per call: every position's selected blocks and its tail
+    sel_blocks = sum(min(w.k, t // 64) + 1 for t in range(L)) * w.batch * w.n_kv_heads
+    attn_bytes = sel_blocks * payload
+    # bytes that must cross HBM at least once: inputs, block units written and read,
+    # pooled keys, outputs
+    hbm_bytes = (w.batch * L * (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim * elt
+                 + w.batch * L * w.n_kv_heads * 4
+                 + 2 * w.units * nblk * payload + w.units * nblk * 4 * w.head_dim * 4
+                 + w.batch * L * w.n_q_heads * (w.head_dim * elt + 4))
+    peak, kind = measured_peaks()
+    gbs = attn_bytes / secs / 1e9
+    return {"metric": "training-time forward tokens/s per layer (causal dual selection + "
+                      "block-sparse attention)",
+            "value": round(tokens / max_secs, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(secs * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "mode": "prefill",
+            "config": {"workload": w.name + f"-prefill-L{L}", "batch": w.batch, "seq_len": L,
+                       "k": w.k, "k_e": w.k_e, "n_q_heads": w.n_q_heads,
+                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim},
+            # every position reads its selected blocks and its tail (most reads hit
+            # L2: the 64 positions of a block share most blocks); per call
+            "roofline": {"bound": "hbm", "kernel": "whole training-time forward (5 launches)",
+                         "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None, "peak_source": kind,
+                         "algorithmic_bytes_per_launch": attn_bytes,
+                         "note": "bytes gathered per position (mostly served by L2)"},
+            "hbm_unique_bytes_per_call": hbm_bytes,
+            "gpu_launches": 5 * K}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import synth
@@ -620,9 +688,11 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="nosa", choices=["nosa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="nosa", choices=["nosa", "infllmv2", "fullattn"],
+    ap.add_argument("--mode", default="nosa", choices=["nosa", "infllmv2", "fullattn", "prefill"],
                     help="nosa (the method); comparators: infllmv2 = k_e 0 (no query-agnostic "
-                         "part), fullattn = dense attention over the whole cache in HBM")
+                         "part), fullattn = dense attention over the whole cache in HBM; "
+                         "prefill = the training-time forward over whole sequences "
+                         "(--prompt sets the length, default 32768)")
     ap.add_argument("--attention-only", action="store_true",
                     help="time only the split-K attention on the step shape (profiling aid)")
     ap.add_argument("--pooled-bf16", action="store_true",
@@ -673,8 +743,9 @@ def main():
                           "gbs": round(nbytes / secs / 1e9, 1),
                           "frac_of_" + kind + "_peak": round(nbytes / secs / 1e9 / peak, 4)}))
         return
-    if args.mode == "fullattn":
-        line = run_fullattn(args, rank, world, local_rank)
+    if args.mode in ("fullattn", "prefill"):
+        line = (run_fullattn if args.mode == "fullattn" else run_prefill)(args, rank, world,
+                                                                           local_rank)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
