@@ -361,7 +361,7 @@ def run_prefill(args, rank, world, local_rank):
                          "algorithmic_bytes_per_launch": attn_bytes,
                          "note": "bytes gathered per position (mostly served by L2)"},
             "hbm_unique_bytes_per_call": hbm_bytes,
-            "gpu_launches": 5 * K}
+            "gpu_launches": (3 + -(-w.batch * L * w.n_kv_heads // 65535)) * K}
 
 
 def run_gpu(args, rank, world, local_rank):
