@@ -105,12 +105,255 @@ struct AttnGeom {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ---------------------------------------------------------------------------
+// Building blocks of the split-K attention.
+// ---------------------------------------------------------------------------
+
+// Online-softmax state of one warp over its TPW tokens of every block it sees.
 template <typename T, int D, int G, int W>
-__global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
+struct AttnWarpState {
+  static constexpr int CE = AttnGeom<T, D, G, W>::CE;
+  float m_run[G], l_run[G];
+  float2 acc[G][CE / 2];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m_run[g] = -1e30f;
+      l_run[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < CE / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
+    }
+  }
+};
+
+// The G queries of unit (b, h) into q_s (scaled by log2(e) / sqrt(d), split into
+// head-dim parts for the logit lanes).
+template <typename T, int D, int G, int W>
+__device__ __forceinline__ void attn_stage_q(float* q_s, const void* q_in, int b, int h, int Hq,
+                                             float qscale, int tid) {
+  using Gm = AttnGeom<T, D, G, W>;
+  constexpr int PARTS = Gm::PARTS, QP = Gm::QP;
+  const T* qg = reinterpret_cast<const T*>(q_in) + ((long long)b * Hq + (long long)h * G) * D;
+  for (int i = tid; i < G * D; i += Gm::NT) {
+    const int g = i / D, dim = i % D;
+    q_s[(g * PARTS + dim / (D / PARTS)) * QP + (dim % (D / PARTS))] = to_f32(qg[i]) * qscale;
+  }
+}
+
+// One block unit in shared memory: the warp's TPW tokens enter its online softmax.
+// valid: whether this lane's logit token counts (false: a tail position past the end).
+template <typename T, int D, int G, int W>
+__device__ __forceinline__ void attn_block(const uint8_t* buf, const float* q_s, float* p_s,
+                                           bool valid, AttnWarpState<T, D, G, W>& st, int warp,
+                                           int lane) {
   using Gm = AttnGeom<T, D, G, W>;
   constexpr int B = Gm::B, ELT = Gm::ELT, CE = Gm::CE, NCH = Gm::NCH, NCHP = Gm::NCHP;
   constexpr int TG = Gm::TG, TPL = Gm::TPL, GP = Gm::GP, QP = Gm::QP;
-  constexpr int NT = Gm::NT, TPW = Gm::TPW, PARTS = Gm::PARTS;
+  constexpr int TPW = Gm::TPW, PARTS = Gm::PARTS;
+  const int t = lane % TPW, hh = lane / TPW;  // logit lane: token, head-dim part
+  const int tok = warp * TPW + t;
+  const int c = lane % NCH, tg = lane / NCH;
+
+  // ---- logits of this warp's TPW tokens ----
+  float2 d2[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) d2[g] = make_float2(0.f, 0.f);
+  const uint4* kp = reinterpret_cast<const uint4*>(buf) + (hh * NCHP) * B + tok;
+#pragma unroll
+  for (int cc = 0; cc < NCHP; ++cc) {
+    float kf[CE];
+    Unpack16<T>::run(kp[cc * B], kf);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float4* qp = reinterpret_cast<const float4*>(q_s + (g * PARTS + hh) * QP + cc * CE);
+#pragma unroll
+      for (int e4 = 0; e4 < CE / 4; ++e4) {
+        const float4 qv = qp[e4];
+        d2[g] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kf[4 * e4], kf[4 * e4 + 1]), d2[g]);
+        d2[g] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kf[4 * e4 + 2], kf[4 * e4 + 3]), d2[g]);
+      }
+    }
+  }
+  const float ev = reinterpret_cast<const float*>(buf + 2 * B * D * ELT)[tok] * kLog2e;
+  float pg[G], alpha[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float dot = d2[g].x + d2[g].y;
+#pragma unroll
+    for (int o = TPW; o < 32; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    const float lg = valid ? dot + ev : -INFINITY;
+    float mx = lg;
+#pragma unroll
+    for (int o = 1; o < TPW; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float mn = fmaxf(st.m_run[g], mx);
+    alpha[g] = exp2f(st.m_run[g] - mn);
+    pg[g] = exp2f(lg - mn);
+    st.l_run[g] = st.l_run[g] * alpha[g] + pg[g];
+    st.m_run[g] = mn;
+  }
+  if (hh == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) p_s[tok * GP + g] = pg[g];
+  }
+  __syncwarp();
+
+  // ---- acc = acc * alpha + sum_t p_t v_t ----
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float2 a2 = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+    for (int e = 0; e < CE / 2; ++e) st.acc[g][e] = __fmul2_rn(st.acc[g][e], a2);
+  }
+  const uint8_t* vbase = buf + (size_t)B * D * ELT;
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) {
+    const int tk = warp * TPW + tg + i * TG;
+    float vf[CE];
+    Unpack16<T>::run(*reinterpret_cast<const uint4*>(vbase + ((size_t)tk * D + c * CE) * ELT), vf);
+    float pv[GP];
+#pragma unroll
+    for (int g4 = 0; g4 < GP / 4; ++g4) {
+      const float4 x = *reinterpret_cast<const float4*>(p_s + tk * GP + 4 * g4);
+      pv[4 * g4] = x.x;
+      pv[4 * g4 + 1] = x.y;
+      pv[4 * g4 + 2] = x.z;
+      pv[4 * g4 + 3] = x.w;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float2 p2 = make_float2(pv[g], pv[g]);
+#pragma unroll
+      for (int e = 0; e < CE / 2; ++e)
+        st.acc[g][e] = __ffma2_rn(p2, make_float2(vf[2 * e], vf[2 * e + 1]), st.acc[g][e]);
+    }
+  }
+  __syncwarp();
+}
+
+// Combines the W warps' states into the CTA's (M, A, L) per (query head, dim) and
+// writes them as partial `pidx` of the unit ([unit][nst][G][D] accumulators and
+// [unit][nst][G][2] (max, sum)), or, when pidx < 0, as the output itself (same
+// arithmetic as a merge of one partial). red: shared memory of [W][G][D] + 2 [W][G]
+// floats. The caller brackets it with __syncthreads (red may alias idle stages).
+template <typename T, int D, int G, int W>
+__device__ __forceinline__ void attn_reduce(AttnWarpState<T, D, G, W>& st, float* red, int tid,
+                                            int warp, int lane, float* part_acc, float* part_ml,
+                                            long long pbase, void* out, float* lse,
+                                            long long row0) {
+  using Gm = AttnGeom<T, D, G, W>;
+  constexpr int CE = Gm::CE, NCH = Gm::NCH, TPW = Gm::TPW, NT = Gm::NT;
+  const int c = lane % NCH, tg = lane / NCH;
+  // Warp totals: each token's p sits in every head-dim part of the warp; sum
+  // over the tokens of one part.
+  float lw[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float x = st.l_run[g];
+#pragma unroll
+    for (int o = 1; o < TPW; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    lw[g] = x;
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < CE / 2; ++e)
+#pragma unroll
+      for (int o = NCH; o < 32; o <<= 1) {
+        st.acc[g][e].x += __shfl_xor_sync(0xffffffffu, st.acc[g][e].x, o);
+        st.acc[g][e].y += __shfl_xor_sync(0xffffffffu, st.acc[g][e].y, o);
+      }
+  float* red_acc = red;                // [W][G][D]
+  float* red_m = red_acc + W * G * D;  // [W][G]
+  float* red_l = red_m + W * G;        // [W][G]
+  if (tg == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < CE / 2; ++e) {
+        red_acc[(warp * G + g) * D + c * CE + 2 * e] = st.acc[g][e].x;
+        red_acc[(warp * G + g) * D + c * CE + 2 * e + 1] = st.acc[g][e].y;
+      }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      red_m[warp * G + g] = st.m_run[g];
+      red_l[warp * G + g] = lw[g];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += NT) {
+    const int g = i / D, dim = i % D;
+    float M = red_m[g];
+#pragma unroll
+    for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w * G + g]);
+    float A = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float sc = exp2f(red_m[w * G + g] - M);
+      A += red_acc[(w * G + g) * D + dim] * sc;
+      L += red_l[w * G + g] * sc;
+    }
+    if (pbase < 0) {  // a single partial: it is the output
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      reinterpret_cast<T*>(out)[(row0 + g) * D + dim] = from_f32<T>(A * inv);
+      if (dim == 0 && lse != nullptr) lse[row0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    } else {
+      part_acc[(pbase + g) * D + dim] = A;
+      if (dim == 0) {
+        part_ml[(pbase + g) * 2] = M;
+        part_ml[(pbase + g) * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+// The unit's nst partials merged into out / lse (by the CTA that published the
+// last one): per-partial weights exp2(m_j - M) / L staged in shared memory, then
+// the accumulators summed in partial order with independent loads.
+// scratch: 3 * nst * G floats of shared memory.
+template <typename T, int D, int G, int W>
+__device__ __forceinline__ void attn_merge(const float* part_acc, const float* part_ml,
+                                           long long ubase, int nst, float* scratch, void* out,
+                                           float* lse, long long row0, int tid) {
+  constexpr int NT = AttnGeom<T, D, G, W>::NT;
+  float* ml_s = scratch;           // [nst][G][2]
+  float* w_s = ml_s + 2 * nst * G;  // [nst][G]
+  __shared__ float s_M[8], s_L[8];
+  for (int i = tid; i < 2 * nst * G; i += NT) ml_s[i] = __ldcg(part_ml + ubase * 2 + i);
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int j = 0; j < nst; ++j) M = fmaxf(M, ml_s[(j * G + tid) * 2]);
+    float L = 0.f;
+    for (int j = 0; j < nst; ++j) {
+      const float sc = exp2f(ml_s[(j * G + tid) * 2] - M);
+      w_s[j * G + tid] = sc;
+      L += ml_s[(j * G + tid) * 2 + 1] * sc;
+    }
+    s_M[tid] = M;
+    s_L[tid] = L;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int j = 0; j < nst; ++j) w_s[j * G + tid] *= inv;
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += NT) {
+    const int g = i / D, dim = i % D;
+    const float* ac = part_acc + (ubase + g) * D + dim;
+    float A = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < nst; ++j) A += __ldcg(ac + (long long)j * G * D) * w_s[j * G + g];
+    reinterpret_cast<T*>(out)[(row0 + g) * D + dim] = from_f32<T>(A);
+    if (dim == 0 && lse != nullptr)
+      lse[row0 + g] = s_L[g] > 0.f ? (s_M[g] + log2f(s_L[g])) * kLn2 : -INFINITY;
+  }
+}
+
+template <typename T, int D, int G, int W>
+__global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
+  using Gm = AttnGeom<T, D, G, W>;
+  constexpr int B = Gm::B, GP = Gm::GP, QP = Gm::QP, NT = Gm::NT, PARTS = Gm::PARTS;
+  constexpr int TPW = Gm::TPW;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const long long payload = p.payload;
@@ -193,28 +436,13 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
     }
     issued = pre;
   }
-  {
-    const T* qg = reinterpret_cast<const T*>(q_in) + ((long long)b * p.Hq + (long long)h * G) * D;
-    for (int i = tid; i < G * D; i += NT) {
-      const int g = i / D, dim = i % D;
-      q_s[(g * PARTS + dim / (D / PARTS)) * QP + (dim % (D / PARTS))] = to_f32(qg[i]) * p.qscale;
-    }
-  }
+  attn_stage_q<T, D, G, W>(q_s, q_in, b, h, p.Hq, p.qscale, tid);
   __syncthreads();
   const int nl = s_nl;
 
-  float m_run[G], l_run[G];
-  float2 acc[G][CE / 2];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m_run[g] = -1e30f;
-    l_run[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < CE / 2; ++e) acc[g][e] = make_float2(0.f, 0.f);
-  }
-  const int t = lane % TPW, hh = lane / TPW;  // logit lane: token, head-dim part
-  const int tok = warp * TPW + t;
-  const int c = lane % NCH, tg = lane / NCH;
+  AttnWarpState<T, D, G, W> st;
+  st.init();
+  const int tok = warp * TPW + lane % TPW;
 
   for (int it = 0; it < nl; ++it) {
     if (__any_sync(0xffffffffu, s_bad != 0)) break;
@@ -229,82 +457,7 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
       break;
     }
     const uint8_t* buf = stage_buf + (size_t)si * payload;
-    const bool valid = (list[it] >= 0) || (tok < tail_len);
-
-    // ---- logits of this warp's TPW tokens ----
-    float2 d2[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) d2[g] = make_float2(0.f, 0.f);
-    const uint4* kp = reinterpret_cast<const uint4*>(buf) + (hh * NCHP) * B + tok;
-#pragma unroll
-    for (int cc = 0; cc < NCHP; ++cc) {
-      float kf[CE];
-      Unpack16<T>::run(kp[cc * B], kf);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float4* qp = reinterpret_cast<const float4*>(q_s + (g * PARTS + hh) * QP + cc * CE);
-#pragma unroll
-        for (int e4 = 0; e4 < CE / 4; ++e4) {
-          const float4 qv = qp[e4];
-          d2[g] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kf[4 * e4], kf[4 * e4 + 1]), d2[g]);
-          d2[g] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kf[4 * e4 + 2], kf[4 * e4 + 3]), d2[g]);
-        }
-      }
-    }
-    const float ev = reinterpret_cast<const float*>(buf + 2 * B * D * ELT)[tok] * kLog2e;
-    float pg[G], alpha[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float dot = d2[g].x + d2[g].y;
-#pragma unroll
-      for (int o = TPW; o < 32; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      const float lg = valid ? dot + ev : -INFINITY;
-      float mx = lg;
-#pragma unroll
-      for (int o = 1; o < TPW; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float mn = fmaxf(m_run[g], mx);
-      alpha[g] = exp2f(m_run[g] - mn);
-      pg[g] = exp2f(lg - mn);
-      l_run[g] = l_run[g] * alpha[g] + pg[g];
-      m_run[g] = mn;
-    }
-    if (hh == 0) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) p_s[tok * GP + g] = pg[g];
-    }
-    __syncwarp();
-
-    // ---- acc = acc * alpha + sum_t p_t v_t ----
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float2 a2 = make_float2(alpha[g], alpha[g]);
-#pragma unroll
-      for (int e = 0; e < CE / 2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
-    }
-    const uint8_t* vbase = buf + (size_t)B * D * ELT;
-#pragma unroll
-    for (int i = 0; i < TPL; ++i) {
-      const int tk = warp * TPW + tg + i * TG;
-      float vf[CE];
-      Unpack16<T>::run(*reinterpret_cast<const uint4*>(vbase + ((size_t)tk * D + c * CE) * ELT), vf);
-      float pv[GP];
-#pragma unroll
-      for (int g4 = 0; g4 < GP / 4; ++g4) {
-        const float4 x = *reinterpret_cast<const float4*>(p_s + tk * GP + 4 * g4);
-        pv[4 * g4] = x.x;
-        pv[4 * g4 + 1] = x.y;
-        pv[4 * g4 + 2] = x.z;
-        pv[4 * g4 + 3] = x.w;
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float2 p2 = make_float2(pv[g], pv[g]);
-#pragma unroll
-        for (int e = 0; e < CE / 2; ++e)
-          acc[g][e] = __ffma2_rn(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[g][e]);
-      }
-    }
-    __syncwarp();
+    attn_block<T, D, G, W>(buf, q_s, p_s, (list[it] >= 0) || (tok < tail_len), st, warp, lane);
     if (lane == 0) mbar_arrive(&empty[si]);
 
     // ---- refill this stage with the block `stages` items ahead ----
@@ -323,26 +476,6 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
     }
   }
 
-  // Warp totals: each token's p sits in every head-dim part of the warp; sum
-  // over the tokens of one part.
-  float lw[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float x = l_run[g];
-#pragma unroll
-    for (int o = 1; o < TPW; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    lw[g] = x;
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < CE / 2; ++e)
-#pragma unroll
-      for (int o = NCH; o < 32; o <<= 1) {
-        acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
-        acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
-      }
-
   __syncthreads();
   if (s_bad != 0 && tid == 0) {
     // Drain: wait (bounded) for the last copy issued into each stage.
@@ -354,66 +487,13 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   }
   __syncthreads();
 
-  float* red_acc = reinterpret_cast<float*>(stage_buf);  // [W][G][D]
-  float* red_m = red_acc + W * G * D;                    // [W][G]
-  float* red_l = red_m + W * G;                          // [W][G]
-  if (tg == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < CE / 2; ++e) {
-        red_acc[(warp * G + g) * D + c * CE + 2 * e] = acc[g][e].x;
-        red_acc[(warp * G + g) * D + c * CE + 2 * e + 1] = acc[g][e].y;
-      }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      red_m[warp * G + g] = m_run[g];
-      red_l[warp * G + g] = lw[g];
-    }
-  }
-  __syncthreads();
   const int nst = p.nsplit_total;
-  if (nst == 1) {  // a single partial: it is the output (same arithmetic as the merge)
-    for (int i = tid; i < G * D; i += NT) {
-      const int g = i / D, dim = i % D;
-      float M = red_m[g];
-#pragma unroll
-      for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w * G + g]);
-      float A = 0.f, L = 0.f;
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float sc = exp2f(red_m[w * G + g] - M);
-        A += red_acc[(w * G + g) * D + dim] * sc;
-        L += red_l[w * G + g] * sc;
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const long long row = (long long)b * p.Hq + (long long)h * G + g;
-      reinterpret_cast<T*>(out)[row * D + dim] = from_f32<T>(A * inv);
-      if (dim == 0 && lse != nullptr) lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-    }
-    return;
-  }
-  const long long pbase = ((long long)u * nst + p.split_base + sp) * G;
-  for (int i = tid; i < G * D; i += NT) {
-    const int g = i / D, dim = i % D;
-    float M = red_m[g];
-#pragma unroll
-    for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w * G + g]);
-    float A = 0.f, L = 0.f;
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float sc = exp2f(red_m[w * G + g] - M);
-      A += red_acc[(w * G + g) * D + dim] * sc;
-      L += red_l[w * G + g] * sc;
-    }
-    p.part_acc[(pbase + g) * D + dim] = A;
-    if (dim == 0) {
-      p.part_ml[(pbase + g) * 2] = M;
-      p.part_ml[(pbase + g) * 2 + 1] = L;
-    }
-  }
+  const long long row0 = (long long)b * p.Hq + (long long)h * G;
+  float* red = reinterpret_cast<float*>(stage_buf);  // the stages are idle now
+  attn_reduce<T, D, G, W>(st, red, tid, warp, lane, p.part_acc, p.part_ml,
+                          nst == 1 ? -1 : ((long long)u * nst + p.split_base + sp) * G,
+                          out, lse, row0);
+  if (nst == 1) return;
 
   // The CTA that writes the unit's last partial merges all of them (no waiting:
   // every other CTA has already published its partial before counting itself).
@@ -424,41 +504,8 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // All (max, sum) pairs of the unit are contiguous: stage them, turn them into
-  // per-partial weights exp2(m_j - M) / L, then sum the accumulators with
-  // independent (unrolled) loads.
-  const long long ubase = (long long)u * nst * G;
-  float* ml_s = reinterpret_cast<float*>(stage_buf);   // [nst][G][2]
-  float* w_s = ml_s + 2 * nst * G;                     // [nst][G]
-  __shared__ float s_M[8], s_L[8];
-  for (int i = tid; i < 2 * nst * G; i += NT) ml_s[i] = __ldcg(p.part_ml + ubase * 2 + i);
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int j = 0; j < nst; ++j) M = fmaxf(M, ml_s[(j * G + tid) * 2]);
-    float L = 0.f;
-    for (int j = 0; j < nst; ++j) {
-      const float sc = exp2f(ml_s[(j * G + tid) * 2] - M);
-      w_s[j * G + tid] = sc;
-      L += ml_s[(j * G + tid) * 2 + 1] * sc;
-    }
-    s_M[tid] = M;
-    s_L[tid] = L;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int j = 0; j < nst; ++j) w_s[j * G + tid] *= inv;
-  }
-  __syncthreads();
-  for (int i = tid; i < G * D; i += NT) {
-    const int g = i / D, dim = i % D;
-    const float* ac = p.part_acc + (ubase + g) * D + dim;
-    float A = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < nst; ++j) A += __ldcg(ac + (long long)j * G * D) * w_s[j * G + g];
-    const long long row = (long long)b * p.Hq + (long long)h * G + g;
-    reinterpret_cast<T*>(out)[row * D + dim] = from_f32<T>(A);
-    if (dim == 0 && lse != nullptr)
-      lse[row] = s_L[g] > 0.f ? (s_M[g] + log2f(s_L[g])) * kLn2 : -INFINITY;
-  }
+  attn_merge<T, D, G, W>(p.part_acc, p.part_ml, (long long)u * nst * G, nst,
+                         reinterpret_cast<float*>(stage_buf), out, lse, row0, tid);
   if (tid == 0) p.counters[u] = 0;
 }
 
@@ -558,6 +605,7 @@ cudaError_t launch_attn_dispatch_w(const Shape& s, const AttnArgs& a, int stages
 
 cudaError_t launch_attention_f32(const Shape& s, const AttnArgs& a, int stages, int bps,
                                  int warps, cudaStream_t stream);
+
 cudaError_t launch_attention_bf16(const Shape& s, const AttnArgs& a, int stages, int bps,
                                   int warps, cudaStream_t stream);
 int attention_occupancy_f32(const Shape& s, int stages, int bps, int warps);
