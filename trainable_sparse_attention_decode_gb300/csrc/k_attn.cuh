@@ -497,10 +497,18 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
 
   // The CTA that writes the unit's last partial merges all of them (no waiting:
   // every other CTA has already published its partial before counting itself).
-  __threadfence();
+  // The barrier orders the CTA's partial writes before thread 0's release add,
+  // and the release makes them visible at GPU scope with the count.
   __syncthreads();
   __shared__ int s_last;
-  if (tid == 0) s_last = (atomicAdd(&p.counters[u], 1) == nst - 1);
+  if (tid == 0) {
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(p.counters + u)
+                 : "memory");
+    s_last = (prev == nst - 1);
+  }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
