@@ -186,23 +186,27 @@ int attention_pick_nsplit(const Shape& s, int n_blocks, int /*has_tail*/) {
 
 int attention_pick_nsplit_uncached(const Shape& s, int n_blocks) {
   const int nv = n_blocks + 1;
+  if (const char* g = std::getenv("NOSA_ATTN_SPLITS")) {  // tuning override
+    const int v = std::atoi(g);
+    if (v >= 1) return std::min(std::min(v, kMaxSplits), std::max(1, nv));
+  }
+  // CTAs are scheduled as others finish, not in lockstep waves: long CTAs (about
+  // 20 blocks) amortise each CTA's start-up and merge; small launches still get
+  // half a CTA per resident slot (in the decode step the attention shares the GPU
+  // with scoring and the gather). Measured on GB300 at the 8B-offload shape: 3
+  // splits (22 blocks each) 106 us alone against 113 us for 7; in the step 3
+  // splits per unit chunk beat 6 (101.6 k against 84 k tokens/s).
   const int stages = attn_stages(s.payload);
   const int bps_est = std::min(nv, 64);
   int occ = s.dtype == 0 ? attention_occupancy_f32(s, stages, bps_est, attn_warps())
                          : attention_occupancy_bf16(s, stages, bps_est, attn_warps());
   if (occ < 1) occ = 1;
   const double slots = (double)sm_count_current() * occ;
-  int best = 1;
-  double best_eff = 0.0;
+  if (s.U >= 2 * slots) return 1;  // enough CTAs already, and one split needs no merge
+  const int by_blocks = std::max(1, nv / 20);
+  const int by_fill = (int)std::ceil(0.5 * slots / std::max(s.U, 1));
   const int max_ns = std::max(1, std::min(kMaxSplits, nv / 2));
-  for (int ns = 1; ns <= max_ns; ++ns) {
-    const double w = (double)s.U * ns / slots;
-    const double eff = w / std::ceil(w);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = ns;
-    }
-  }
+  const int best = std::max(1, std::min(max_ns, std::max(by_blocks, by_fill)));
   return best;
 }
 
