@@ -421,7 +421,7 @@ def run_gpu(args, rank, world, local_rank):
             if r:
                 raise nosa.NosaError(r, nosa.nosa_last_error(h))
         e2e_hosts = lambda: [x_all[W + K:W + K + KE].cpu().pin_memory()]
-        e2e_step = lambda devs: nosa.nosa_decode_step_hidden(h, devs[0], Wf, out, None, stream=stream)
+        e2e_step = lambda devs, o: nosa.nosa_decode_step_hidden(h, devs[0], Wf, o, None, stream=stream)
     else:
         q_all = synth.gpu.queries(w, total_steps)
         k_all, v_all, e_all = synth.gpu.kv(w, w.prompt, total_steps, step_major=True)
@@ -438,7 +438,7 @@ def run_gpu(args, rank, world, local_rank):
             if r:
                 raise nosa.NosaError(r, nosa.nosa_last_error(h))
         e2e_hosts = lambda: [x[W + K:W + K + KE].cpu().pin_memory() for x in (q_all, k_all, v_all, e_all)]
-        e2e_step = lambda devs: nosa.nosa_decode_step(h, *devs, out, None, stream)
+        e2e_step = lambda devs, o: nosa.nosa_decode_step(h, *devs, o, None, stream)
     torch.cuda.synchronize()
     nosa.nosa_stats_reset(h)
     sampler = ClockSampler(gpu_index(local_rank)) if rank == 0 else None
@@ -464,20 +464,44 @@ def run_gpu(args, rank, world, local_rank):
     st = nosa.nosa_stats(h)
     context_after = st["context"]
 
-    # end to end: pinned host inputs -> device, step, result -> pinned host
+    # end to end: pinned host inputs -> device, step, result -> pinned host, every
+    # step, as a server pipelines them: double-buffered device inputs and outputs,
+    # the copies on a copy stream overlapping the previous step's kernels
     hosts = e2e_hosts()
-    devs = [torch.empty_like(x[0], device="cuda") for x in hosts]
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    devs = [[torch.empty_like(x[0], device="cuda") for x in hosts] for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    out_h = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    cs = torch.cuda.Stream()      # host -> device inputs
+    cs_out = torch.cuda.Stream()  # device -> host results (never ahead of the next inputs)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0t = time.time()
     e0.record(stream)
+    cs.wait_event(e0)
+    cs_out.wait_event(e0)
     for s in range(KE):
-        for d_, h_ in zip(devs, hosts):
-            d_.copy_(h_[s], non_blocking=True)
-        e2e_step(devs)
-        out_h.copy_(out, non_blocking=True)
+        i = s % 2
+        with torch.cuda.stream(cs):
+            if s >= 2:
+                cs.wait_event(ev_done[i])  # step s - 2 has read these inputs
+            for d_, h_ in zip(devs[i], hosts):
+                d_.copy_(h_[s], non_blocking=True)
+            ev_in[i].record(cs)
+        stream.wait_event(ev_in[i])
+        if s >= 2:
+            stream.wait_event(ev_out[i])  # step s - 2's output is on the host
+        e2e_step(devs[i], outs[i])
+        ev_done[i].record(stream)
+        with torch.cuda.stream(cs_out):
+            cs_out.wait_event(ev_done[i])
+            out_h[i].copy_(outs[i], non_blocking=True)
+            ev_out[i].record(cs_out)
+    for ev in ev_out:
+        stream.wait_event(ev)
     e1.record(stream)
     torch.cuda.synchronize()
     x1t = time.time()
@@ -485,7 +509,7 @@ def run_gpu(args, rank, world, local_rank):
         sampler.mark(x0t, x1t)
     e2e_secs = e0.elapsed_time(e1) / 1e3
     bi = sum(x[0].numel() * x.element_size() for x in hosts)
-    bo = out_h.numel() * out_h.element_size()
+    bo = out_h[0].numel() * out_h[0].element_size()
     clocks = sampler.stop() if sampler else None
 
     # Per-phase device times from the library's events, in a window of their own
@@ -591,7 +615,9 @@ def run_gpu(args, rank, world, local_rank):
         "gamma_mean": round(st["gamma_mean"], 4), "gamma_min": st["gamma_min"],
         "near_ties": st["near_ties"],
         "e2e": {"value": round(e2e_tokens / e2e_max, 3), "unit": "tokens/s",
-                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": KE},
+                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": KE,
+                "copies": "every step; double-buffered, on copy streams overlapping the "
+                          "previous step"},
         "gpu_launches": st["launches"],
         "loads_per_unit_step": round(loads_per_unit, 3),
         "host_enqueue_us_per_step": round(host_enqueue_us, 2),
