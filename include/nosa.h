@@ -231,12 +231,25 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
  *          256-byte aligned, owned by the caller (contents are scratch)
  * seq_len in [1, cfg->max_context] and <= 131072. Async on stream. Errors:
  * INVALID_ARG (sizes, NULL, alignment, workspace too small), UNSUPPORTED, CUDA.
+ * In bf16 with n_q_heads / n_kv_heads in {1, 2, 4} and head_dim in {64, 128} the
+ * attention runs per query block on the tensor cores (environment variable
+ * NOSA_PREFILL_TILED=0: the split-K decode attention per position instead).
  */
 size_t nosa_prefill_workspace_bytes(const nosa_config* cfg, int32_t seq_len);
 nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const void* q,
                                  const void* k, const void* v, const float* e, void* out,
                                  float* lse, int32_t* sel, void* workspace,
                                  size_t workspace_bytes, void* stream);
+/*
+ * The device error word of the last nosa_prefill_forward run in `workspace` with
+ * the same cfg and seq_len: 0 none, 1 a bounded wait in a kernel gave up (the
+ * outputs of the affected query blocks are not written), 2 a block table entry
+ * out of range (skipped). Waits for the device (cudaDeviceSynchronize) and then
+ * copies the 4-byte word to *err (host). INVALID_ARG on NULL or sizes outside the
+ * forward's limits; CUDA on a failed copy.
+ */
+nosa_status nosa_prefill_device_error(const nosa_config* cfg, int32_t seq_len,
+                                      const void* workspace, int32_t* err);
 
 /* Counters, host-readable. gamma_* covers steps after the first decode step
  * with at least k candidates; gamma(t) = |Gamma(t) ∩ R(t-1)| / k where R(t-1)

@@ -5,6 +5,8 @@ Every position's selection (Gamma_e then Gamma_q) is compared with the oracle's
 and carries on: the eviction sets carry over to later positions); the attention
 output within the decode path's tolerances on the checked positions.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,17 +20,33 @@ from oracle import nosa_oracle as O
 pytestmark = pytest.mark.gpu
 
 
-def _prefill(w, L, units=None, attn_every=1):
+def _forward(cfg, L, q, k, v, e, out, lse, sel, tiled):
+    """One forward with the tiled tensor-core attention on or off (the switch is
+    read at every call); checks the device error word."""
+    old = os.environ.get("NOSA_PREFILL_TILED")
+    os.environ["NOSA_PREFILL_TILED"] = "1" if tiled else "0"
+    try:
+        ws = nosa.nosa_prefill_forward(cfg, q, k, v, e, out, lse, sel)
+        assert nosa.nosa_prefill_device_error(cfg, L, ws) == 0
+    finally:
+        if old is None:
+            del os.environ["NOSA_PREFILL_TILED"]
+        else:
+            os.environ["NOSA_PREFILL_TILED"] = old
+    torch.cuda.synchronize()
+
+
+def _prefill(w, L, units=None, attn_every=1, tiled=True):
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
                            max(L, 1))
-    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     k, v, e = synth.gpu.kv(w, 0, L)
     q = synth.gpu.queries(w, L).permute(1, 0, 2, 3).contiguous()   # [batch][L][Hq][d]
-    out = torch.empty_like(q)
-    lse = torch.empty((w.batch, L, w.n_q_heads), dtype=torch.float32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((w.batch, L, w.n_q_heads), float("nan"), dtype=torch.float32, device="cuda")
     sel = torch.empty((w.batch, L, w.n_kv_heads, w.k), dtype=torch.int32, device="cuda")
-    nosa.nosa_prefill_forward(cfg, q, k, v, e, out, lse, sel)
-    torch.cuda.synchronize()
+    _forward(cfg, L, q, k, v, e, out, lse, sel, tiled)
+    assert not torch.isnan(out.float()).any(), "an output row was not written"
+    assert not torch.isnan(lse).any(), "an lse entry was not written"
     sel_h = sel.cpu().numpy()
     out_h, lse_h = to_f64(out), lse.cpu().numpy().astype(np.float64)
     G = w.group
@@ -91,21 +109,62 @@ def test_query_only_and_eviction_only(k_e):
     _prefill(w, 64 * 30 + 11)
 
 
-def test_1b_shape_sampled_units():
+@pytest.mark.parametrize("tiled", [True, False])
+def test_1b_shape_sampled_units(tiled):
+    # G = 2, d = 64: one 128-row tile per query block
     w = synth.WORKLOADS["1b-bf16"].with_(batch=2)
-    _prefill(w, 8192 + 100, units=[0, 13], attn_every=7)
+    _prefill(w, 8192 + 100, units=[0, 13], attn_every=7, tiled=tiled)
 
 
-def test_8b_shape_sampled_units():
+@pytest.mark.parametrize("tiled", [True, False])
+def test_8b_shape_sampled_units(tiled):
+    # G = 4, d = 128: two 128-row tiles per query block
     w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=1)
-    _prefill(w, 4096 + 128 + 5, units=[0, 5], attn_every=11)
+    _prefill(w, 4096 + 128 + 5, units=[0, 5], attn_every=11, tiled=tiled)
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (12, 2, 64)])
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (12, 2, 64), (8, 2, 64), (4, 4, 64)])
 def test_group_variants(hq, hkv, d):
+    # G = 1 (half of the 128-row tile empty), G = 6 (split-K path), G = 4 with d = 64
     w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
                                          k=16, k_e=12)
     _prefill(w, 64 * 20 + 3, units=[0, hkv - 1], attn_every=3)
+
+
+_TILE_W = synth.WORKLOADS["8b-offload-bf16"].with_(batch=2, n_q_heads=8, n_kv_heads=2, k=8, k_e=6)
+
+
+@pytest.mark.parametrize("L", [1, 37, 64, 65, 64 * 9 + 5])
+def test_tiled_short_and_ragged(L):
+    # a single partial block, exact block ends, a ragged last query block
+    _prefill(_TILE_W, L)
+
+
+@pytest.mark.parametrize("k_e", [0, 8])
+def test_tiled_query_only_and_eviction_only(k_e):
+    _prefill(_TILE_W.with_(k_e=k_e), 64 * 30 + 11, attn_every=2)
+
+
+def test_tiled_matches_split_path():
+    # both attention paths on the same inputs: same selections, outputs within
+    # the bf16 tolerance of each other
+    w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=1, n_kv_heads=4, n_q_heads=16)
+    L = 64 * 40 + 17
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e, L)
+    k, v, e = synth.gpu.kv(w, 0, L)
+    q = synth.gpu.queries(w, L).permute(1, 0, 2, 3).contiguous()
+    res = []
+    for tiled in (True, False):
+        out = torch.empty_like(q)
+        lse = torch.empty((1, L, w.n_q_heads), dtype=torch.float32, device="cuda")
+        sel = torch.empty((1, L, w.n_kv_heads, w.k), dtype=torch.int32, device="cuda")
+        _forward(cfg, L, q, k, v, e, out, lse, sel, tiled)
+        res.append((out.float(), lse, sel))
+    assert torch.equal(res[0][2], res[1][2])
+    d = (res[0][0] - res[1][0]).float()
+    rms = res[1][0].float().pow(2).mean().sqrt()
+    assert float(d.pow(2).mean().sqrt() / rms) <= 1e-2
+    assert float((res[0][1] - res[1][1]).abs().max()) <= 1e-3
 
 
 def test_workspace_and_argument_errors():

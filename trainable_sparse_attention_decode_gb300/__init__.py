@@ -24,7 +24,7 @@ __all__ = [
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
     "nosa_selftest_bounded_wait", "nosa_frontend_rows", "nosa_decode_step_hidden",
     "nosa_frontend_packed_bytes", "nosa_frontend_pack", "nosa_prefill_workspace_bytes",
-    "nosa_prefill_forward",
+    "nosa_prefill_forward", "nosa_prefill_device_error",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -95,6 +95,7 @@ def _load():
         "nosa_prefill_workspace_bytes": (SZ, [P(NosaConfig), I32]),
         "nosa_prefill_forward": (C.c_int, [P(NosaConfig), I32, VP, VP, VP, VP, VP, VP, VP, VP,
                                            SZ, VP]),
+        "nosa_prefill_device_error": (C.c_int, [P(NosaConfig), I32, VP, P(I32)]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -274,6 +275,17 @@ def nosa_prefill_forward(cfg: NosaConfig, q, k, v, e, out, lse=None, sel=None, w
         _ptr(sel, ks[:3] + (cfg.k,), torch.int32, "sel", 4, allow_none=True),
         _ptr(workspace, None, torch.uint8, "workspace", 256), workspace.numel(), _stream(stream)))
     return workspace
+
+
+def nosa_prefill_device_error(cfg: NosaConfig, seq_len: int, workspace) -> int:
+    """The device error word of the last training-time forward run in workspace
+    (0 none, 1 a bounded wait gave up, 2 a table entry out of range); waits for
+    the device."""
+    out = C.c_int32(0)
+    _check(lib.nosa_prefill_device_error(C.byref(cfg), seq_len,
+                                         _ptr(workspace, None, _torch().uint8, "workspace", 256),
+                                         C.byref(out)))
+    return out.value
 
 
 def nosa_stats(h) -> dict:

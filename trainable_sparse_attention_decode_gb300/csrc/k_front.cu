@@ -40,28 +40,19 @@
 // copies already issued are drained (bounded) and the tensor memory is freed
 // before the CTA exits.
 #include "nosa_internal.cuh"
+#include "tcgen05.cuh"
 
 #include <atomic>
 
 namespace nosa {
 namespace {
+using namespace tc;
 
 constexpr int kFrontThreads = 192;
 constexpr int kTileM = 128;                   // rows of W per CTA (MMA M)
 constexpr int kTileK = 64;                    // hidden elements per stage: 128 bytes of bf16
 constexpr int kMaxStages = 10;
 constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB weight tile per stage
-
-// Shared-memory matrix descriptor of a K-major operand tile in the canonical
-// 128-byte-swizzled layout (rows of 128 bytes, groups of 8 rows 1024 bytes apart).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address / 16
-  d |= (uint64_t)1 << 16;                           // leading-dimension offset (unused here)
-  d |= (uint64_t)(1024 >> 4) << 32;                 // stride between 8-row groups / 16
-  d |= (uint64_t)1 << 46;                           // descriptor version of tcgen05
-  d |= (uint64_t)2 << 61;                           // 128-byte swizzle
-  return d;
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
@@ -70,44 +61,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "%4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrives once on `bar` when every MMA this thread issued before it has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
 // Writes rows f0 .. f0 + 7 of the projection for request n (values v8, fp32).

@@ -17,9 +17,12 @@
 //   prefill_select_kernel  per position: pooled query scores of the candidates
 //                          outside E_b, top-(k - |E_b|) by warp arg-max; writes
 //                          the position's block table and tail     (unit, block)
-//   attn_split_kernel      the split-K attention of the decode path, one virtual
-//                          unit per (request, position, KV head), with per-unit
-//                          tails (the causal partial block).
+//   prefill_tile_kernel    (bf16, G <= 4, d in {64, 128}; k_prefill_tc.cu) the
+//                          attention of a whole query block on the tensor cores,
+//                          over the union of its positions' blocks;
+//   attn_split_kernel      otherwise the split-K attention of the decode path, one
+//                          virtual unit per (request, position, KV head), with
+//                          per-unit tails (the causal partial block).
 #include "nosa_internal.cuh"
 
 #include <algorithm>
@@ -32,11 +35,20 @@ namespace {
 constexpr int kPackThreads = 256;
 constexpr int kSelWarps = 8;
 
+// Byte offset of V element (t, dim) in a block unit packed for the tiled tensor-core
+// attention (bf16): V transposed into 8 x 8 core matrices, row = dim (the MMA's
+// N), column = token (its K): token chunks (8 tokens) d * 16 bytes apart, dim
+// groups of 8 rows 128 bytes apart. K keeps the decode layout, which already is
+// that form with rows = tokens (token groups 128 bytes apart, dim chunks B * 16).
+__device__ __forceinline__ long long vt_off(int t, int dim, int B, int d) {
+  return (long long)B * d * 2 + ((long long)(t >> 3) * d + dim) * 16 + (t & 7) * 2;
+}
+
 // Block unit of (unit u, block blk) from k, v [batch][L][Hkv][d], e [batch][L][Hkv];
 // tokens past L are zeros. Complete blocks are pooled: sub-block mean keys (fp32
 // token-order sums x 1/16) and the block's eviction score (max of the sub-block
-// means of e). grid = (nblk, U).
-template <typename T>
+// means of e). grid = (nblk, U). VT: V in the transposed form of vt_off.
+template <typename T, bool VT>
 __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
     Shape s, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ e, int L,
     int nblk, uint8_t* __restrict__ units, float* __restrict__ pk, float* __restrict__ se) {
@@ -53,7 +65,10 @@ __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
       vv = v[src];
     }
     *reinterpret_cast<T*>(unit + k_off(t, dim, s.B, s.elt)) = kv;
-    *reinterpret_cast<T*>(unit + v_off(t, dim, s.B, s.d, s.elt)) = vv;
+    if (VT)
+      *reinterpret_cast<T*>(unit + vt_off(t, dim, s.B, s.d)) = vv;
+    else
+      *reinterpret_cast<T*>(unit + v_off(t, dim, s.B, s.d, s.elt)) = vv;
   }
   for (int t = threadIdx.x; t < s.B; t += blockDim.x)
     *reinterpret_cast<float*>(unit + e_off(t, s.B, s.d, s.elt)) =
@@ -305,7 +320,7 @@ size_t prefill_select_smem(const Shape& s, int nblk) {
 
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
                                  const void* v, const float* e, int32_t* sel, uint8_t* ws,
-                                 const PrefillLayout& w, cudaStream_t stream) {
+                                 const PrefillLayout& w, bool vt, cudaStream_t stream) {
   const int nblk = (L + s.B - 1) / s.B;
   uint8_t* units = ws + w.units;
   float* pk = reinterpret_cast<float*>(ws + w.pk);
@@ -314,10 +329,13 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   int32_t* Ecnt = reinterpret_cast<int32_t*>(ws + w.ecnt);
   dim3 grid(nblk, s.U);
   if (s.dtype == 0)
-    prefill_pack_kernel<float><<<grid, kPackThreads, 0, stream>>>(
+    prefill_pack_kernel<float, false><<<grid, kPackThreads, 0, stream>>>(
         s, (const float*)k, (const float*)v, e, L, nblk, units, pk, se);
+  else if (vt)
+    prefill_pack_kernel<__nv_bfloat16, true><<<grid, kPackThreads, 0, stream>>>(
+        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se);
   else
-    prefill_pack_kernel<__nv_bfloat16><<<grid, kPackThreads, 0, stream>>>(
+    prefill_pack_kernel<__nv_bfloat16, false><<<grid, kPackThreads, 0, stream>>>(
         s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -1231,7 +1231,9 @@ size_t nosa_prefill_workspace_bytes(const nosa_config* cfg, int32_t seq_len) {
   if (prefill_checks(cfg, seq_len) != NOSA_OK) return 0;
   DeviceGuard guard(cfg->device);
   const Shape s = shape_of(*cfg);
-  const int nsplit = attention_pick_nsplit(prefill_virtual_shape(s, seq_len), s.k, 1);
+  const int nsplit = prefill_tiled_ok(s, seq_len)
+                         ? 1
+                         : attention_pick_nsplit(prefill_virtual_shape(s, seq_len), s.k, 1);
   return prefill_layout(s, seq_len, nsplit).total;
 }
 
@@ -1254,7 +1256,8 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
   DeviceGuard guard(cfg->device);
   const Shape s = shape_of(*cfg);
   const Shape sv = prefill_virtual_shape(s, seq_len);
-  const int nsplit = attention_pick_nsplit(sv, s.k, 1);
+  const bool tiled = prefill_tiled_ok(s, seq_len);
+  const int nsplit = tiled ? 1 : attention_pick_nsplit(sv, s.k, 1);
   const PrefillLayout w = prefill_layout(s, seq_len, nsplit);
   if (workspace_bytes < w.total) {
     g_thread_err = "workspace too small (see nosa_prefill_workspace_bytes)";
@@ -1264,7 +1267,17 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int nblk = (seq_len + s.B - 1) / s.B;
   cudaError_t err = cudaMemsetAsync(ws + w.counters, 0, w.err + 256 - w.counters, st);
-  if (err == cudaSuccess) err = launch_prefill_front(s, seq_len, q, k, v, e, sel, ws, w, st);
+  if (err == cudaSuccess) err = launch_prefill_front(s, seq_len, q, k, v, e, sel, ws, w, tiled, st);
+  if (tiled) {
+    if (err == cudaSuccess)
+      err = launch_prefill_tile(s, seq_len, ws + w.units, reinterpret_cast<const int32_t*>(ws + w.tab),
+                                q, out, lse, reinterpret_cast<int*>(ws + w.err), st);
+    if (err != cudaSuccess) {
+      g_thread_err = std::string("training-time forward launch: ") + cudaGetErrorString(err);
+      return NOSA_ERR_CUDA;
+    }
+    return NOSA_OK;
+  }
   AttnArgs a;
   a.units = ws + w.units;
   a.n_units = (long long)s.U * nblk;
@@ -1292,6 +1305,31 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
   }
   if (err != cudaSuccess) {
     g_thread_err = std::string("training-time forward launch: ") + cudaGetErrorString(err);
+    return NOSA_ERR_CUDA;
+  }
+  return NOSA_OK;
+}
+
+nosa_status nosa_prefill_device_error(const nosa_config* cfg, int32_t seq_len,
+                                      const void* workspace, int32_t* err) {
+  const nosa_status cs = prefill_checks(cfg, seq_len);
+  if (cs != NOSA_OK) return cs;
+  if (!workspace || !err) {
+    g_thread_err = "NULL argument";
+    return NOSA_ERR_INVALID_ARG;
+  }
+  DeviceGuard guard(cfg->device);
+  const Shape s = shape_of(*cfg);
+  const int nsplit = prefill_tiled_ok(s, seq_len)
+                         ? 1
+                         : attention_pick_nsplit(prefill_virtual_shape(s, seq_len), s.k, 1);
+  const PrefillLayout w = prefill_layout(s, seq_len, nsplit);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(err, static_cast<const uint8_t*>(workspace) + w.err, sizeof(int32_t),
+                   cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("reading the device error word: ") + cudaGetErrorString(e);
     return NOSA_ERR_CUDA;
   }
   return NOSA_OK;

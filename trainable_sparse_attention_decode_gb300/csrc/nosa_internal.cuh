@@ -111,9 +111,31 @@ PrefillLayout prefill_layout(const Shape& s, int L, int nsplit);
 size_t prefill_select_smem(const Shape& s, int nblk);
 // Packs, pools, runs the eviction-set recurrence and the per-position selection;
 // sel (optional) receives the selections [batch][L][Hkv][k].
+// vt: V of the block units in the transposed form of the tiled attention.
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
                                  const void* v, const float* e, int32_t* sel, uint8_t* ws,
-                                 const PrefillLayout& w, cudaStream_t stream);
+                                 const PrefillLayout& w, bool vt, cudaStream_t stream);
+// Tiled tensor-core attention of the training-time forward (k_prefill_tc.cu):
+// one CTA per (unit, query block), grid (nblk, unit_count).
+struct PrefillTileArgs {
+  const uint8_t* units;  // [U][nblk] block units (V transposed)
+  const int32_t* tab;    // [batch][L][Hkv][k] per-position block tables (unit index, -1 pad)
+  const void* q;         // [batch][L][Hq][d] bf16
+  void* out;             // [batch][L][Hq][d] bf16
+  float* lse;            // [batch][L][Hq] or null
+  int* err;              // device error word
+  int L, nblk;
+  int unit_base;         // first unit of this launch
+  int mt;                // 128-row M tiles: ceil(64 G / 128)
+  int tmem_cols;         // tensor-memory columns per CTA
+  float inv_sqrt_d;
+};
+// True when the tiled path covers this shape (bf16, G in {1, 2, 4}, d in {64, 128},
+// shared memory within the limit) and NOSA_PREFILL_TILED is not 0.
+bool prefill_tiled_ok(const Shape& s, int L);
+cudaError_t launch_prefill_tile(const Shape& s, int L, const uint8_t* units, const int32_t* tab,
+                                const void* q, void* out, float* lse, int* err,
+                                cudaStream_t stream);
 
 struct State {
   uint8_t* slots;      // [U][k] block units (device)
