@@ -25,6 +25,8 @@
 //                          per-unit tails (the causal partial block).
 #include "nosa_internal.cuh"
 
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -35,24 +37,48 @@ namespace {
 constexpr int kPackThreads = 256;
 constexpr int kSelWarps = 8;
 
-// Byte offset of V element (t, dim) in a block unit packed for the tiled tensor-core
-// attention (bf16): V transposed into 8 x 8 core matrices, row = dim (the MMA's
-// N), column = token (its K): token chunks (8 tokens) d * 16 bytes apart, dim
-// groups of 8 rows 128 bytes apart. K keeps the decode layout, which already is
-// that form with rows = tokens (token groups 128 bytes apart, dim chunks B * 16).
-__device__ __forceinline__ long long vt_off(int t, int dim, int B, int d) {
-  return (long long)B * d * 2 + ((long long)(t >> 3) * d + dim) * 16 + (t & 7) * 2;
+// Block units of the tiled tensor-core attention (bf16 inputs; k_prefill_tc.cu)
+// hold their operands in the canonical K-major layout with the 128-byte swizzle
+// (rows of 128 bytes = 64 elements along the MMA's K, 16-byte chunk c of row r
+// stored at chunk c ^ (r % 8), 8-row groups 1024 bytes apart), so the MMAs read
+// a unit where its bulk copy puts it (at a 1024-byte aligned stage):
+//   K   bf16, rows = tokens, K = head dim: 64-dim blocks of 64 x 128 bytes;
+//   V^T fp16, rows = head dim, K = tokens: d x 128 bytes, each value times 2^vs
+//       (vs from the largest |v| of the call, so every value converts exactly
+//       unless it is 2^29 below that maximum);
+//   e   fp32 x log2(e), as in the decode layout.
+__device__ __forceinline__ long long tk_off(int t, int dim) {  // K (bf16)
+  const int c = dim >> 3;
+  return (long long)(c >> 3) * 8192 + t * 128 + (((c & 7) ^ (t & 7)) << 4) + (dim & 7) * 2;
+}
+__device__ __forceinline__ long long tv_off(int t, int dim, int B, int d) {  // V^T (fp16)
+  return (long long)B * d * 2 + (long long)dim * 128 + ((((t >> 3) ^ (dim & 7))) << 4) + (t & 7) * 2;
+}
+
+// Largest |v| of the call (as fp32 bits; nonnegative floats order like their
+// bits) into *absmax, which starts at 0.
+__global__ void __launch_bounds__(256) prefill_vmax_kernel(const __nv_bfloat16* __restrict__ v,
+                                                           long long n, uint32_t* __restrict__ absmax) {
+  uint32_t best = 0;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    best = max(best, __float_as_uint(fabsf(__bfloat162float(v[i]))));
+  for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(absmax, best);
 }
 
 // Block unit of (unit u, block blk) from k, v [batch][L][Hkv][d], e [batch][L][Hkv];
 // tokens past L are zeros. Complete blocks are pooled: sub-block mean keys (fp32
 // token-order sums x 1/16) and the block's eviction score (max of the sub-block
-// means of e). grid = (nblk, U). VT: V in the transposed form of vt_off.
-template <typename T, bool VT>
+// means of e). grid = (nblk, U). TC: the tensor-core unit layout above (the pooled
+// scores use e itself); vmax is the largest |v| (bits), TC only.
+template <typename T, bool TC>
 __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
     Shape s, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ e, int L,
-    int nblk, uint8_t* __restrict__ units, float* __restrict__ pk, float* __restrict__ se) {
+    int nblk, uint8_t* __restrict__ units, float* __restrict__ pk, float* __restrict__ se,
+    const uint32_t* __restrict__ vmax) {
   const int blk = blockIdx.x, u = blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
+  const float vmul = TC ? ldexpf(1.0f, v_scale_exp(*vmax)) : 1.0f;
   uint8_t* unit = units + ((long long)u * nblk + blk) * s.payload;
   const int t0 = blk * s.B;
   const int nt = min(s.B, L - t0);
@@ -64,15 +90,19 @@ __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
       kv = k[src];
       vv = v[src];
     }
-    *reinterpret_cast<T*>(unit + k_off(t, dim, s.B, s.elt)) = kv;
-    if (VT)
-      *reinterpret_cast<T*>(unit + vt_off(t, dim, s.B, s.d)) = vv;
-    else
+    if (TC) {
+      *reinterpret_cast<T*>(unit + tk_off(t, dim)) = kv;
+      *reinterpret_cast<__half*>(unit + tv_off(t, dim, s.B, s.d)) = __float2half_rn(to_f32(vv) * vmul);
+    } else {
+      *reinterpret_cast<T*>(unit + k_off(t, dim, s.B, s.elt)) = kv;
       *reinterpret_cast<T*>(unit + v_off(t, dim, s.B, s.d, s.elt)) = vv;
+    }
   }
+  // (TC: the tiled attention works in base 2 and takes e x log2(e))
+  const float escale = TC ? 1.4426950408889634f : 1.0f;
   for (int t = threadIdx.x; t < s.B; t += blockDim.x)
     *reinterpret_cast<float*>(unit + e_off(t, s.B, s.d, s.elt)) =
-        (t < nt) ? e[((long long)b * L + t0 + t) * s.Hkv + h] : 0.f;
+        (t < nt) ? e[((long long)b * L + t0 + t) * s.Hkv + h] * escale : 0.f;
   for (long long i = 2LL * s.B * s.d * s.elt + 4LL * s.B + threadIdx.x; i < s.payload; i += blockDim.x)
     unit[i] = 0;
   if (nt < s.B) return;  // an incomplete block is never a candidate
@@ -307,6 +337,7 @@ PrefillLayout prefill_layout(const Shape& s, int L, int nsplit) {
   w.part_acc = off;  off += nsplit > 1 ? up(V * nsplit * s.G * s.d * 4) : 0;
   w.part_ml = off;   off += nsplit > 1 ? up(V * nsplit * s.G * 2 * 4) : 0;
   w.counters = off;  off += up(V * 4);
+  w.vmax = off;      off += 256;
   w.err = off;       off += 256;
   w.total = off;
   return w;
@@ -320,7 +351,7 @@ size_t prefill_select_smem(const Shape& s, int nblk) {
 
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
                                  const void* v, const float* e, int32_t* sel, uint8_t* ws,
-                                 const PrefillLayout& w, bool vt, cudaStream_t stream) {
+                                 const PrefillLayout& w, bool tc, cudaStream_t stream) {
   const int nblk = (L + s.B - 1) / s.B;
   uint8_t* units = ws + w.units;
   float* pk = reinterpret_cast<float*>(ws + w.pk);
@@ -328,15 +359,20 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   int32_t* Eb = reinterpret_cast<int32_t*>(ws + w.eb);
   int32_t* Ecnt = reinterpret_cast<int32_t*>(ws + w.ecnt);
   dim3 grid(nblk, s.U);
-  if (s.dtype == 0)
+  uint32_t* vmax = reinterpret_cast<uint32_t*>(ws + w.vmax);  // zeroed by the caller
+  if (s.dtype == 0) {
     prefill_pack_kernel<float, false><<<grid, kPackThreads, 0, stream>>>(
-        s, (const float*)k, (const float*)v, e, L, nblk, units, pk, se);
-  else if (vt)
+        s, (const float*)k, (const float*)v, e, L, nblk, units, pk, se, nullptr);
+  } else if (tc) {
+    const long long n = (long long)s.batch * L * s.Hkv * s.d;
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 4 * 152);
+    prefill_vmax_kernel<<<blocks, 256, 0, stream>>>((const __nv_bfloat16*)v, n, vmax);
     prefill_pack_kernel<__nv_bfloat16, true><<<grid, kPackThreads, 0, stream>>>(
-        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se);
-  else
+        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se, vmax);
+  } else {
     prefill_pack_kernel<__nv_bfloat16, false><<<grid, kPackThreads, 0, stream>>>(
-        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se);
+        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se, nullptr);
+  }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t esmem = (size_t)4 * (s.ke + 1) * 4;

@@ -1271,7 +1271,8 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
   if (tiled) {
     if (err == cudaSuccess)
       err = launch_prefill_tile(s, seq_len, ws + w.units, reinterpret_cast<const int32_t*>(ws + w.tab),
-                                q, out, lse, reinterpret_cast<int*>(ws + w.err), st);
+                                reinterpret_cast<const uint32_t*>(ws + w.vmax), q, out, lse,
+                                reinterpret_cast<int*>(ws + w.err), st);
     if (err != cudaSuccess) {
       g_thread_err = std::string("training-time forward launch: ") + cudaGetErrorString(err);
       return NOSA_ERR_CUDA;

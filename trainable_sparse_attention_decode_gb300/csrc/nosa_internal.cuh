@@ -104,22 +104,25 @@ int frontend_max_clusters(const FrontParams& p);
 
 // Training-time forward (k_prefill.cu): byte offsets into the caller's workspace.
 struct PrefillLayout {
-  size_t units, pk, se, eb, ecnt, tab, tail_tab, tail_len, part_acc, part_ml, counters, err, total;
+  size_t units, pk, se, eb, ecnt, tab, tail_tab, tail_len, part_acc, part_ml, counters, vmax, err,
+      total;
 };
 // s describes the real units (batch * Hkv); L is the sequence length.
 PrefillLayout prefill_layout(const Shape& s, int L, int nsplit);
 size_t prefill_select_smem(const Shape& s, int nblk);
 // Packs, pools, runs the eviction-set recurrence and the per-position selection;
 // sel (optional) receives the selections [batch][L][Hkv][k].
-// vt: V of the block units in the transposed form of the tiled attention.
+// tc: block units in the tensor-core layout of the tiled attention (K and V^T
+// 128-byte swizzled, V^T in fp16 scaled by 2^vs from the largest |v|).
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
                                  const void* v, const float* e, int32_t* sel, uint8_t* ws,
-                                 const PrefillLayout& w, bool vt, cudaStream_t stream);
+                                 const PrefillLayout& w, bool tc, cudaStream_t stream);
 // Tiled tensor-core attention of the training-time forward (k_prefill_tc.cu):
 // one CTA per (unit, query block), grid (nblk, unit_count).
 struct PrefillTileArgs {
   const uint8_t* units;  // [U][nblk] block units (V transposed)
   const int32_t* tab;    // [batch][L][Hkv][k] per-position block tables (unit index, -1 pad)
+  const uint32_t* vmax;  // largest |v| of the call (fp32 bits): the V scale 2^vs
   const void* q;         // [batch][L][Hq][d] bf16
   void* out;             // [batch][L][Hq][d] bf16
   float* lse;            // [batch][L][Hq] or null
@@ -134,8 +137,8 @@ struct PrefillTileArgs {
 // shared memory within the limit) and NOSA_PREFILL_TILED is not 0.
 bool prefill_tiled_ok(const Shape& s, int L);
 cudaError_t launch_prefill_tile(const Shape& s, int L, const uint8_t* units, const int32_t* tab,
-                                const void* q, void* out, float* lse, int* err,
-                                cudaStream_t stream);
+                                const uint32_t* vmax, const void* q, void* out, float* lse,
+                                int* err, cudaStream_t stream);
 
 struct State {
   uint8_t* slots;      // [U][k] block units (device)
@@ -277,6 +280,16 @@ __device__ __forceinline__ long long v_off(int t, int dim, int B, int d, int elt
 }
 __device__ __forceinline__ long long e_off(int t, int B, int d, int elt) {
   return 2LL * B * d * elt + 4LL * t;
+}
+
+// Power-of-two exponent vs applied to V for the fp16 P V product of the tiled
+// training-time attention: the largest |v| times 2^vs lies in [2^14, 2^15).
+__device__ __forceinline__ int v_scale_exp(uint32_t absmax_bits) {
+  const float m = __uint_as_float(absmax_bits);
+  if (!(m > 0.f) || !(m < INFINITY)) return 0;
+  int e;
+  frexpf(m, &e);  // m = f 2^e, f in [0.5, 1)
+  return 15 - e;
 }
 
 // Monotone map of fp32 scores to uint32 (larger float -> larger key); -0 == +0.
