@@ -192,129 +192,238 @@ __global__ void __launch_bounds__(128) prefill_evict_kernel(Shape s, const float
   }
 }
 
-// Per position t of block b (CTA (b, u); warp w takes positions 64 b + w, + 8, ...):
-// q_bar = mean of the G query heads, sq(j) = max over sub-blocks of
-// q_bar . K_bar[j][s] / sqrt(d) for candidates j < b outside E_b, then the
-// top-(k - |E_b|) by repeated warp arg-max (ties: lower index). Writes the
-// position's selection (E_b ascending, then Gamma_q ascending, -1 pad) into sel,
-// its attention block table (unit indices) and tail.
-template <typename T>
-__global__ void __launch_bounds__(kSelWarps * 32) prefill_select_kernel(
+// Loads 4 consecutive elements of q as fp32.
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+  const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+  return make_float4(a.x, a.y, c.x, c.y);
+}
+
+// Per position t of block b (CTA (b, u); warp w takes positions 64 b + w, + 8, ...,
+// PB of them at a time): q_bar = mean of the G query heads, sq(j) = max over
+// sub-blocks of q_bar . K_bar[j][s] / sqrt(d) for candidates j < b outside E_b,
+// then the top-(k - |E_b|) by repeated warp arg-max (ties: lower index). Writes
+// the position's selection (E_b ascending, then Gamma_q ascending, -1 pad) into
+// sel, its attention block table (unit indices) and tail.
+// Scoring: lane (r, c) = (lane / 8, lane % 8) holds sub-block r's dims c*4 + 32v
+// (v < D/32) of a pooled key row and the same dims of the PB positions' q_bar,
+// so one load of a row serves PB positions; the PB partial sums of the 8 lanes of
+// a sub-block are reduced and transposed in 7 shuffles (lane c ends with position
+// c % PB), then the max over the 4 sub-blocks takes 2 more.
+template <typename T, int D, int PB>
+__global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
     Shape s, const T* __restrict__ q, int L, int nblk, const float* __restrict__ pk,
     const int32_t* __restrict__ Eb, const int32_t* __restrict__ Ecnt, int32_t* __restrict__ sel,
     int32_t* __restrict__ block_tab, int32_t* __restrict__ tail_tab, int32_t* __restrict__ tail_len,
     float inv_sqrt_d) {
+  constexpr int NV = D / 32;  // float4 per lane of a pooled row
   extern __shared__ __align__(16) uint8_t sm[];
   const int b = blockIdx.x, u = blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
   const int W = (nblk + 31) / 32;
-  uint32_t* emask = reinterpret_cast<uint32_t*>(sm);             // [W] E_b membership
-  float* qbar_s = reinterpret_cast<float*>(emask + ((W + 3) & ~3));  // [kSelWarps][d]
-  float* sq_s = qbar_s + kSelWarps * s.d;                         // [kSelWarps][nblk]
-  uint32_t* taken_s = reinterpret_cast<uint32_t*>(sq_s + (long long)kSelWarps * nblk);  // [kSelWarps][W]
+  uint32_t* emask = reinterpret_cast<uint32_t*>(sm);                          // [W] E_b membership
+  float* sq_s = reinterpret_cast<float*>(emask + ((W + 3) & ~3));              // [kSelWarps][PB][nblk]
+  uint32_t* taken_s = reinterpret_cast<uint32_t*>(sq_s + (size_t)kSelWarps * PB * nblk);  // [kSelWarps][W]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 3, c = lane & 7;
   const int ecnt = Ecnt[(long long)u * nblk + b];
   const int32_t* eb = Eb + ((long long)u * nblk + b) * s.ke;
   for (int i = threadIdx.x; i < W; i += blockDim.x) emask[i] = 0u;
   __syncthreads();
   for (int i = threadIdx.x; i < ecnt; i += blockDim.x) atomicOr(&emask[eb[i] >> 5], 1u << (eb[i] & 31));
   __syncthreads();
-  const int n_cand = b;  // blocks before the position's own block
-  const int n_rest = n_cand - ecnt;
-  const int m = min(s.k - ecnt, n_rest);
-  float* qb = qbar_s + warp * s.d;
-  float* sqw = sq_s + (long long)warp * nblk;
+  const int n_cand = b;  // blocks before the positions' own block
+  const int m = min(s.k - ecnt, n_cand - ecnt);
+  const int npos = min(s.B, L - b * s.B);
+  float* sqw = sq_s + (size_t)warp * PB * nblk;
   uint32_t* tk = taken_s + warp * W;
   const float inv_g = 1.0f / (float)s.G;
-  for (int p = warp; p < s.B; p += kSelWarps) {
-    const int t = b * s.B + p;
-    if (t >= L) break;
-    const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
-    // q_bar of the group
-    const T* qg = q + (((long long)req * L + t) * s.Hq + (long long)h * s.G) * s.d;
-    for (int dim = lane; dim < s.d; dim += 32) {
-      float acc = 0.f;
-      for (int g = 0; g < s.G; ++g) acc += to_f32(qg[g * s.d + dim]);
-      qb[dim] = acc * inv_g;
-    }
-    for (int i = lane; i < W; i += 32) tk[i] = 0u;
-    __syncwarp();
-    // scores of the candidates outside E_b: 8 lanes per pooled row, 4 rows
-    if (m > 0) {
-      const int r = lane >> 3, c = lane & 7;
-      for (int j = 0; j < n_cand; ++j) {
-        if ((emask[j >> 5] >> (j & 31)) & 1u) continue;
-        const float* row = pk + (((long long)u * nblk + j) * s.P + r) * s.d;
-        float acc = 0.f;
-        for (int dim = c * 4; dim < s.d; dim += 32) {
-          const float4 x = *reinterpret_cast<const float4*>(row + dim);
-          acc = fmaf(x.x, qb[dim], acc);
-          acc = fmaf(x.y, qb[dim + 1], acc);
-          acc = fmaf(x.z, qb[dim + 2], acc);
-          acc = fmaf(x.w, qb[dim + 3], acc);
+  const long long ubase = (long long)u * nblk;
+  for (int g0 = 0; g0 < s.B / kSelWarps; g0 += PB) {
+    if (warp + kSelWarps * g0 >= npos) break;  // positions grow with g0
+    // q_bar of the batch's positions, this lane's dims
+    float4 qv[PB][NV];
+#pragma unroll
+    for (int i = 0; i < PB; ++i) {
+      const int p = warp + kSelWarps * (g0 + i);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) qv[i][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p < npos) {
+        const T* qg = q + (((long long)req * L + (long long)b * s.B + p) * s.Hq + (long long)h * s.G) * D;
+        for (int g = 0; g < s.G; ++g)
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            const float4 x = load4(qg + g * D + c * 4 + 32 * v);
+            qv[i][v].x += x.x;
+            qv[i][v].y += x.y;
+            qv[i][v].z += x.z;
+            qv[i][v].w += x.w;
+          }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          qv[i][v].x *= inv_g;
+          qv[i][v].y *= inv_g;
+          qv[i][v].z *= inv_g;
+          qv[i][v].w *= inv_g;
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        acc = fmaxf(acc, __shfl_xor_sync(0xffffffffu, acc, 8));
-        acc = fmaxf(acc, __shfl_xor_sync(0xffffffffu, acc, 16));
-        if (lane == 0) sqw[j] = acc * inv_sqrt_d;
+      }
+    }
+    if (m > 0) {
+      for (int j = 0; j < n_cand; ++j) {
+        if ((emask[j >> 5] >> (j & 31)) & 1u) continue;  // (warp-uniform)
+        const float* row = pk + ((ubase + j) * s.P + r) * D + c * 4;
+        float4 x[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) x[v] = *reinterpret_cast<const float4*>(row + 32 * v);
+        float acc[PB];
+#pragma unroll
+        for (int i = 0; i < PB; ++i) {
+          float a = 0.f;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            a = fmaf(x[v].x, qv[i][v].x, a);
+            a = fmaf(x[v].y, qv[i][v].y, a);
+            a = fmaf(x[v].z, qv[i][v].z, a);
+            a = fmaf(x[v].w, qv[i][v].w, a);
+          }
+          acc[i] = a;
+        }
+        // sum over the 8 lanes of sub-block r, transposed: lane c keeps position c % PB
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) {
+          if (o >= PB) {
+#pragma unroll
+            for (int i = 0; i < PB; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+          } else {
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < o; ++i) {
+              const float send = hi ? acc[i] : acc[i + o];
+              const float keep = hi ? acc[i + o] : acc[i];
+              acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+        }
+        float sc = acc[0];
+        sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
+        sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 16));
+        if (lane < PB) sqw[(size_t)lane * nblk + j] = sc * inv_sqrt_d;
       }
       __syncwarp();
-      // top-m: m rounds of warp arg-max over the untaken candidates outside E_b
-      for (int round = 0; round < m; ++round) {
-        float best = -INFINITY;
-        int bid = 0x7fffffff;
+    }
+    for (int i = 0; i < PB; ++i) {
+      const int p = warp + kSelWarps * (g0 + i);
+      if (p >= npos) break;
+      const int t = b * s.B + p;
+      const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
+      const float* sqp = sqw + (size_t)i * nblk;
+      for (int w = lane; w < W; w += 32) tk[w] = 0u;
+      __syncwarp();
+      // top-m: m rounds of warp arg-max over the untaken candidates outside E_b.
+      // Lane l owns candidates j = l mod 32 and keeps the best of them as an
+      // order-preserving key (0: none; a NaN score is never a candidate); a round
+      // takes the largest key, at equal keys the lowest index, and only the
+      // winning lane looks for its next best.
+      auto lane_best = [&](uint32_t& key, int& idx) {
+        key = 0u;
+        idx = 0x7fffffff;
         for (int j = lane; j < n_cand; j += 32) {
           const uint32_t bit = 1u << (j & 31);
           if ((emask[j >> 5] & bit) || (tk[j >> 5] & bit)) continue;
-          const float x = sqw[j];
-          if (x > best || (x == best && j < bid)) {
-            best = x;
-            bid = j;
+          const float x = sqp[j];
+          if (x != x) continue;
+          const uint32_t kx = ordered_key(x);
+          if (kx > key) {  // ascending j: the first of equal keys stays
+            key = kx;
+            idx = j;
           }
         }
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-          const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-          if (ob > best || (ob == best && oid < bid)) {
-            best = ob;
-            bid = oid;
-          }
+      };
+      uint32_t lkey;
+      int lidx;
+      if (m > 0) lane_best(lkey, lidx);
+      for (int round = 0; round < m; ++round) {
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
+        if (kmax == 0u) break;  // none left (NaN scores)
+        const int win = (int)__reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)lidx : 0xffffffffu);
+        if ((win & 31) == lane) {
+          tk[win >> 5] |= 1u << (win & 31);
+          lane_best(lkey, lidx);
         }
-        if (lane == 0 && bid < n_cand) tk[bid >> 5] |= 1u << (bid & 31);  // (none left: NaN scores)
         __syncwarp();
       }
-    }
-    // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the mask)
-    int32_t* selp = sel ? sel + vu * s.k : nullptr;
-    int32_t* tab = block_tab + vu * s.k;
-    const long long ubase = (long long)u * nblk;
-    for (int i = lane; i < ecnt; i += 32) {
-      if (selp) selp[i] = eb[i];
-      tab[i] = (int32_t)(ubase + eb[i]);
-    }
-    int run = ecnt;
-    for (int base = 0; base < n_cand; base += 32) {
-      const int j = base + lane;
-      const bool on = (j < n_cand) && ((tk[j >> 5] >> (j & 31)) & 1u);
-      const unsigned bal = __ballot_sync(0xffffffffu, on);
-      if (on) {
-        const int at = run + __popc(bal & ((1u << lane) - 1u));
-        if (selp) selp[at] = j;
-        tab[at] = (int32_t)(ubase + j);
+      // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the mask)
+      int32_t* selp = sel ? sel + vu * s.k : nullptr;
+      int32_t* tab = block_tab + vu * s.k;
+      for (int e = lane; e < ecnt; e += 32) {
+        if (selp) selp[e] = eb[e];
+        tab[e] = (int32_t)(ubase + eb[e]);
       }
-      run += __popc(bal);
+      int run = ecnt;
+      if (m > 0)
+        for (int base = 0; base < n_cand; base += 32) {
+          const int j = base + lane;
+          const bool on = (j < n_cand) && ((tk[j >> 5] >> (j & 31)) & 1u);
+          const unsigned bal = __ballot_sync(0xffffffffu, on);
+          if (on) {
+            const int at = run + __popc(bal & ((1u << lane) - 1u));
+            if (selp) selp[at] = j;
+            tab[at] = (int32_t)(ubase + j);
+          }
+          run += __popc(bal);
+        }
+      for (int e = run + lane; e < s.k; e += 32) {
+        if (selp) selp[e] = -1;
+        tab[e] = -1;
+      }
+      if (lane == 0) {
+        tail_tab[vu] = (int32_t)(ubase + b);
+        tail_len[vu] = p + 1;
+      }
+      __syncwarp();
     }
-    for (int i = run + lane; i < s.k; i += 32) {
-      if (selp) selp[i] = -1;
-      tab[i] = -1;
-    }
-    if (lane == 0) {
-      tail_tab[vu] = (int32_t)(ubase + b);
-      tail_len[vu] = p + 1;
-    }
-    __syncwarp();
   }
+}
+
+// Positions scored per pooled-key load: as many (<= 4) as the score scratch
+// of 8 warps x PB x nblk floats allows within 80 KB (two CTAs per SM).
+int select_pb(int nblk) {
+  int pb = 4;  // (8 would hold 128 q_bar registers per thread: one CTA per SM)
+  while (pb > 1 && (size_t)kSelWarps * pb * nblk * 4 > 80 * 1024) pb >>= 1;
+  return pb;
+}
+
+template <typename T, int D, int PB>
+cudaError_t launch_select_pb(const Shape& s, dim3 grid, size_t smem, const T* q, int L, int nblk,
+                             const float* pk, const int32_t* Eb, const int32_t* Ecnt, int32_t* sel,
+                             int32_t* tab, int32_t* ttab, int32_t* tlen, float isd, cudaStream_t stream) {
+  static std::atomic<int> lim[64];
+  cudaError_t err = raise_smem_limit((const void*)prefill_select_kernel<T, D, PB>, smem, lim);
+  if (err != cudaSuccess) return err;
+  prefill_select_kernel<T, D, PB><<<grid, kSelWarps * 32, smem, stream>>>(s, q, L, nblk, pk, Eb, Ecnt, sel,
+                                                                           tab, ttab, tlen, isd);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_select_d(const Shape& s, dim3 grid, size_t smem, int pb, const T* q, int L, int nblk,
+                            const float* pk, const int32_t* Eb, const int32_t* Ecnt, int32_t* sel,
+                            int32_t* tab, int32_t* ttab, int32_t* tlen, float isd, cudaStream_t stream) {
+  switch (pb) {
+    case 4: return launch_select_pb<T, D, 4>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
+    case 2: return launch_select_pb<T, D, 2>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
+    default: return launch_select_pb<T, D, 1>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
+  }
+}
+
+template <typename T>
+cudaError_t launch_select(const Shape& s, dim3 grid, size_t smem, int pb, const T* q, int L, int nblk,
+                          const float* pk, const int32_t* Eb, const int32_t* Ecnt, int32_t* sel,
+                          int32_t* tab, int32_t* ttab, int32_t* tlen, float isd, cudaStream_t stream) {
+  if (s.d == 64)
+    return launch_select_d<T, 64>(s, grid, smem, pb, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
+  return launch_select_d<T, 128>(s, grid, smem, pb, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
 }
 
 }  // namespace
@@ -345,7 +454,7 @@ PrefillLayout prefill_layout(const Shape& s, int L, int nsplit) {
 
 size_t prefill_select_smem(const Shape& s, int nblk) {
   const int W = (nblk + 31) / 32;
-  return (size_t)((W + 3) & ~3) * 4 + (size_t)kSelWarps * s.d * 4 + (size_t)kSelWarps * nblk * 4 +
+  return (size_t)((W + 3) & ~3) * 4 + (size_t)kSelWarps * select_pb(nblk) * nblk * 4 +
          (size_t)kSelWarps * W * 4;
 }
 
@@ -380,23 +489,16 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = prefill_select_smem(s, nblk);
-  static std::atomic<int> lim32[64], lim16[64];
+  const int pb = select_pb(nblk);
   const float isd = (float)(1.0 / sqrt((double)s.d));
   int32_t* tab = reinterpret_cast<int32_t*>(ws + w.tab);
   int32_t* ttab = reinterpret_cast<int32_t*>(ws + w.tail_tab);
   int32_t* tlen = reinterpret_cast<int32_t*>(ws + w.tail_len);
-  if (s.dtype == 0) {
-    err = raise_smem_limit((const void*)prefill_select_kernel<float>, smem, lim32);
-    if (err != cudaSuccess) return err;
-    prefill_select_kernel<float><<<grid, kSelWarps * 32, smem, stream>>>(
-        s, (const float*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd);
-  } else {
-    err = raise_smem_limit((const void*)prefill_select_kernel<__nv_bfloat16>, smem, lim16);
-    if (err != cudaSuccess) return err;
-    prefill_select_kernel<__nv_bfloat16><<<grid, kSelWarps * 32, smem, stream>>>(
-        s, (const __nv_bfloat16*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd);
-  }
-  return cudaGetLastError();
+  if (s.dtype == 0)
+    return launch_select<float>(s, grid, smem, pb, (const float*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab,
+                                tlen, isd, stream);
+  return launch_select<__nv_bfloat16>(s, grid, smem, pb, (const __nv_bfloat16*)q, L, nblk, pk, Eb, Ecnt,
+                                      sel, tab, ttab, tlen, isd, stream);
 }
 
 }  // namespace nosa

@@ -224,9 +224,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         if (!(ok = mbar_wait_bounded(&p_full, (uint32_t)(i & 1)))) break;
         tc_fence_after();
         const uint8_t* unit = stage + (size_t)(i % kStages) * sstride;
-        for (int mm = 0; mm < mt; ++mm)
+        // K steps outermost: the M-tiles' accumulations alternate (the tensor pipe
+        // runs two independent accumulators back to back faster than one chain)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < 4; ++kk)
+          for (int mm = 0; mm < mt; ++mm) {
             const uint64_t da = sw128_desc(smem_u32(Pt + (size_t)mm * 16384)) + 2 * kk;
             const uint64_t db = sw128_desc(smem_u32(unit + kbytes)) + 2 * kk;
             mma_bf16(tmem + o_col + (uint32_t)(mm * D), da, db, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
