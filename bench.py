@@ -327,23 +327,57 @@ def run_prefill(args, rank, world, local_rank):
     ev1.record(stream)
     torch.cuda.synchronize()
     secs = ev0.elapsed_time(ev1) / 1e3 / K
+    # per-phase device time (events the library records on the stream when the
+    # config asks for it), on the same inputs right after the timed region
+    cfg_t = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                             L, device=local_rank, flags=nosa.NOSA_FLAG_TIMING)
+    front_ms, attn_ms = [], []
+    for _ in range(K):
+        nosa.nosa_prefill_forward(cfg_t, q, k, v, e, out, lse, workspace=ws, stream=stream)
+        f_ms, a_ms = nosa.nosa_prefill_timing()
+        front_ms.append(f_ms)
+        attn_ms.append(a_ms)
     max_secs, tokens = aggregate(secs, w.batch * L, world)
     if rank != 0:
         return None
     elt = 2 if w.dtype == "bf16" else 4
     payload = nosa.nosa_payload_bytes(cfg)
     nblk = (L + 63) // 64
-    # bytes the attention reads per call: every position's selected blocks and its tail
-    sel_blocks = sum(min(w.k, t // 64) + 1 for t in range(L)) * w.batch * w.n_kv_heads
-    attn_bytes = sel_blocks * payload
+    attn_s = sum(attn_ms) / len(attn_ms) / 1e3
+    # tokens each position attends: its selected blocks and its own block up to itself
+    att_tokens = sum(min(w.k, t // 64) * 64 + t % 64 + 1 for t in range(L)) * w.batch
     # bytes that must cross HBM at least once: inputs, block units written and read,
     # pooled keys, outputs
     hbm_bytes = (w.batch * L * (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim * elt
                  + w.batch * L * w.n_kv_heads * 4
                  + 2 * w.units * nblk * payload + w.units * nblk * 4 * w.head_dim * 4
                  + w.batch * L * w.n_q_heads * (w.head_dim * elt + 4))
-    peak, kind = measured_peaks()
-    gbs = attn_bytes / secs / 1e9
+    tiled = (w.dtype == "bf16" and w.group in (1, 2, 4) and w.head_dim in (64, 128)
+             and os.environ.get("NOSA_PREFILL_TILED", "1") != "0")
+    if tiled:
+        # useful work of the tensor-core attention: Q K^T and P V over every
+        # position's attended tokens, per query head (the kernel also computes the
+        # masked entries of the union of a query block's selections)
+        flops = 4.0 * w.head_dim * w.n_q_heads * att_tokens
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk_d = json.load(f)
+        peak_t, kind = float(pk_d["bf16_tflops"]), "measured bf16 burst (P V runs in fp16, same rate)"
+        ach = flops / attn_s / 1e12
+        roof = {"bound": "tensor", "kernel": "prefill_tile_kernel (tcgen05 attention per query block)",
+                "achieved": round(ach, 1), "peak": peak_t, "unit": "TFLOP/s",
+                "frac": round(ach / peak_t, 4), "traffic": None, "peak_source": kind,
+                "algorithmic_flops_per_launch": flops,
+                "kernel_ms": round(attn_s * 1e3, 4)}
+    else:
+        peak, kind = measured_peaks()
+        attn_bytes = sum(min(w.k, t // 64) + 1 for t in range(L)) * w.batch * w.n_kv_heads * payload
+        gbs = attn_bytes / attn_s / 1e9
+        roof = {"bound": "hbm", "kernel": "attn_split_kernel (a virtual unit per position)",
+                "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gbs / peak, 4), "traffic": None, "peak_source": kind,
+                "algorithmic_bytes_per_launch": attn_bytes, "kernel_ms": round(attn_s * 1e3, 4),
+                "note": "bytes gathered per position (mostly served by L2)"}
+    launches = 5 if tiled else 3 + -(-w.batch * L * w.n_kv_heads // 65535)
     return {"metric": "training-time forward tokens/s per layer (causal dual selection + "
                       "block-sparse attention)",
             "value": round(tokens / max_secs, 3), "unit": "tokens/s", "n_gpus": world,
@@ -352,16 +386,13 @@ def run_prefill(args, rank, world, local_rank):
             "data": "synthetic", "mode": "prefill",
             "config": {"workload": w.name + f"-prefill-L{L}", "batch": w.batch, "seq_len": L,
                        "k": w.k, "k_e": w.k_e, "n_q_heads": w.n_q_heads,
-                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim},
-            # every position reads its selected blocks and its tail (most reads hit
-            # L2: the 64 positions of a block share most blocks); per call
-            "roofline": {"bound": "hbm", "kernel": "whole training-time forward (5 launches)",
-                         "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": None, "peak_source": kind,
-                         "algorithmic_bytes_per_launch": attn_bytes,
-                         "note": "bytes gathered per position (mostly served by L2)"},
+                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+                       "attention": "tiled tensor-core" if tiled else "split-K per position"},
+            "roofline": roof,
+            "phase_ms": {"front": round(sum(front_ms) / len(front_ms), 4),
+                         "attention": round(attn_s * 1e3, 4)},
             "hbm_unique_bytes_per_call": hbm_bytes,
-            "gpu_launches": (3 + -(-w.batch * L * w.n_kv_heads // 65535)) * K}
+            "gpu_launches": launches * K}
 
 
 def run_gpu(args, rank, world, local_rank):

@@ -250,6 +250,15 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
  */
 nosa_status nosa_prefill_device_error(const nosa_config* cfg, int32_t seq_len,
                                       const void* workspace, int32_t* err);
+/*
+ * Device time of the last nosa_prefill_forward called on this thread with
+ * NOSA_FLAG_TIMING in cfg->flags (which then records CUDA events on its stream
+ * around its two phases): *front_ms = packing, eviction sets and per-position
+ * selection; *attention_ms = the attention. Waits for the second phase's end
+ * event. Either pointer may be NULL. STATE if no timed forward ran on this
+ * thread; CUDA on an event error.
+ */
+nosa_status nosa_prefill_timing(float* front_ms, float* attention_ms);
 
 /* Counters, host-readable. gamma_* covers steps after the first decode step
  * with at least k candidates; gamma(t) = |Gamma(t) ∩ R(t-1)| / k where R(t-1)

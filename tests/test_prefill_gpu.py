@@ -180,3 +180,18 @@ def test_workspace_and_argument_errors():
     with pytest.raises(nosa.NosaError) as ei:
         nosa.nosa_prefill_forward(cfg, q, kv, kv, e, torch.empty_like(q), workspace=ws)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("tiled", [True, False])
+def test_phase_timing(tiled):
+    # NOSA_FLAG_TIMING in the config: the call records events around its phases
+    w = _TILE_W
+    L = 64 * 12 + 5
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e, L,
+                           flags=nosa.NOSA_FLAG_TIMING)
+    k, v, e = synth.gpu.kv(w, 0, L)
+    q = synth.gpu.queries(w, L).permute(1, 0, 2, 3).contiguous()
+    out = torch.empty_like(q)
+    _forward(cfg, L, q, k, v, e, out, None, None, tiled)
+    f_ms, a_ms = nosa.nosa_prefill_timing()
+    assert 0.0 < f_ms < 1000.0 and 0.0 < a_ms < 1000.0

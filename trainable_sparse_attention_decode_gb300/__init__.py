@@ -24,7 +24,7 @@ __all__ = [
     "nosa_attention_workspace_bytes", "nosa_sparse_attention", "nosa_sparse_attention_noalloc",
     "nosa_selftest_bounded_wait", "nosa_frontend_rows", "nosa_decode_step_hidden",
     "nosa_frontend_packed_bytes", "nosa_frontend_pack", "nosa_prefill_workspace_bytes",
-    "nosa_prefill_forward", "nosa_prefill_device_error",
+    "nosa_prefill_forward", "nosa_prefill_device_error", "nosa_prefill_timing",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -96,6 +96,7 @@ def _load():
         "nosa_prefill_forward": (C.c_int, [P(NosaConfig), I32, VP, VP, VP, VP, VP, VP, VP, VP,
                                            SZ, VP]),
         "nosa_prefill_device_error": (C.c_int, [P(NosaConfig), I32, VP, P(I32)]),
+        "nosa_prefill_timing": (C.c_int, [P(C.c_float), P(C.c_float)]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -286,6 +287,14 @@ def nosa_prefill_device_error(cfg: NosaConfig, seq_len: int, workspace) -> int:
                                          _ptr(workspace, None, _torch().uint8, "workspace", 256),
                                          C.byref(out)))
     return out.value
+
+
+def nosa_prefill_timing() -> tuple:
+    """(front_ms, attention_ms) of the last training-time forward run on this
+    thread with NOSA_FLAG_TIMING in its config's flags; waits for it."""
+    f, a = C.c_float(0.0), C.c_float(0.0)
+    _check(lib.nosa_prefill_timing(C.byref(f), C.byref(a)))
+    return f.value, a.value
 
 
 def nosa_stats(h) -> dict:

@@ -1202,6 +1202,25 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
 }
 
 namespace {
+// Events of the last timed training-time forward of this thread.
+struct PrefillTimer {
+  int dev = -1;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  bool pending = false;
+  cudaError_t ensure(int device) {
+    if (dev == device && ev[0]) return cudaSuccess;
+    for (auto& e : ev)
+      if (e) cudaEventDestroy(e), e = nullptr;
+    for (auto& e : ev) {
+      const cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+    }
+    dev = device;
+    return cudaSuccess;
+  }
+};
+thread_local PrefillTimer g_prefill_timer;
+
 Shape prefill_virtual_shape(const Shape& s, int L) {
   Shape sv = s;  // one virtual unit per (request, position, KV head)
   sv.batch = s.batch * L;
@@ -1266,13 +1285,29 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int nblk = (seq_len + s.B - 1) / s.B;
-  cudaError_t err = cudaMemsetAsync(ws + w.counters, 0, w.err + 256 - w.counters, st);
+  const bool timing = (cfg->flags & NOSA_FLAG_TIMING) != 0;
+  PrefillTimer& tm = g_prefill_timer;
+  cudaError_t err = cudaSuccess;
+  if (timing) {
+    tm.pending = false;
+    err = tm.ensure(cfg->device);
+    if (err == cudaSuccess) err = cudaEventRecord(tm.ev[0], st);
+  }
+  if (err == cudaSuccess) err = cudaMemsetAsync(ws + w.counters, 0, w.err + 256 - w.counters, st);
   if (err == cudaSuccess) err = launch_prefill_front(s, seq_len, q, k, v, e, sel, ws, w, tiled, st);
+  if (timing && err == cudaSuccess) err = cudaEventRecord(tm.ev[1], st);
+  auto finish = [&]() {
+    if (timing && err == cudaSuccess) {
+      err = cudaEventRecord(tm.ev[2], st);
+      tm.pending = err == cudaSuccess;
+    }
+  };
   if (tiled) {
     if (err == cudaSuccess)
       err = launch_prefill_tile(s, seq_len, ws + w.units, reinterpret_cast<const int32_t*>(ws + w.tab),
                                 reinterpret_cast<const uint32_t*>(ws + w.vmax), q, out, lse,
                                 reinterpret_cast<int*>(ws + w.err), st);
+    finish();
     if (err != cudaSuccess) {
       g_thread_err = std::string("training-time forward launch: ") + cudaGetErrorString(err);
       return NOSA_ERR_CUDA;
@@ -1304,10 +1339,31 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
     a.unit_count = (int)std::min<long long>(65535, sv.U - base);
     err = launch_attention(sv, a, st);
   }
+  finish();
   if (err != cudaSuccess) {
     g_thread_err = std::string("training-time forward launch: ") + cudaGetErrorString(err);
     return NOSA_ERR_CUDA;
   }
+  return NOSA_OK;
+}
+
+nosa_status nosa_prefill_timing(float* front_ms, float* attention_ms) {
+  PrefillTimer& tm = g_prefill_timer;
+  if (!tm.pending) {
+    g_thread_err = "no timed training-time forward on this thread";
+    return NOSA_ERR_STATE;
+  }
+  DeviceGuard guard(tm.dev);
+  float f = 0.f, a = 0.f;
+  cudaError_t e = cudaEventSynchronize(tm.ev[2]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&f, tm.ev[0], tm.ev[1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&a, tm.ev[1], tm.ev[2]);
+  if (e != cudaSuccess) {
+    g_thread_err = std::string("prefill timing events: ") + cudaGetErrorString(e);
+    return NOSA_ERR_CUDA;
+  }
+  if (front_ms) *front_ms = f;
+  if (attention_ms) *attention_ms = a;
   return NOSA_OK;
 }
 
