@@ -59,6 +59,11 @@ struct AttnKParams {
   const StepIO* dyn;  // decode step: q, out, lse, tail_len and the tail offset live here
   const int32_t* tail_tab;   // per-unit tail unit index (or null)
   const int32_t* tail_lens;  // per-unit tail length
+  // stream-K partition (attn_streamk_kernel): CTA c of sk_ctas takes items
+  // [c T / C, (c + 1) T / C) of the units' concatenated item lists (T = unit
+  // count x nv; nv = n_blocks + tail); a unit has up to seg_cap partials.
+  int sk_ctas, nv, seg_cap;
+  long long sk_items;
 };
 
 template <typename T> struct Unpack16;
@@ -517,6 +522,277 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   if (tid == 0) p.counters[u] = 0;
 }
 
+// attn_reduce for a CTA without a [W][G][D] buffer: the warps' states are
+// combined one query head at a time through a [W][D] buffer (same arithmetic).
+// red: W * D + 2 * W * G floats. Starts and ends with a __syncthreads.
+template <typename T, int D, int G, int W>
+__device__ __forceinline__ void attn_reduce_by_head(AttnWarpState<T, D, G, W>& st, float* red, int tid,
+                                                    int warp, int lane, float* part_acc,
+                                                    float* part_ml, long long pbase, void* out,
+                                                    float* lse, long long row0) {
+  using Gm = AttnGeom<T, D, G, W>;
+  constexpr int CE = Gm::CE, NCH = Gm::NCH, TPW = Gm::TPW, NT = Gm::NT;
+  const int c = lane % NCH, tg = lane / NCH;
+  float lw[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float x = st.l_run[g];
+#pragma unroll
+    for (int o = 1; o < TPW; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    lw[g] = x;
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < CE / 2; ++e)
+#pragma unroll
+      for (int o = NCH; o < 32; o <<= 1) {
+        st.acc[g][e].x += __shfl_xor_sync(0xffffffffu, st.acc[g][e].x, o);
+        st.acc[g][e].y += __shfl_xor_sync(0xffffffffu, st.acc[g][e].y, o);
+      }
+  float* red_acc = red;                // [W][D]
+  float* red_m = red_acc + W * D;      // [W][G]
+  float* red_l = red_m + W * G;        // [W][G]
+  __syncthreads();
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      red_m[warp * G + g] = st.m_run[g];
+      red_l[warp * G + g] = lw[g];
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (tg == 0) {
+#pragma unroll
+      for (int e = 0; e < CE / 2; ++e) {
+        red_acc[warp * D + c * CE + 2 * e] = st.acc[g][e].x;
+        red_acc[warp * D + c * CE + 2 * e + 1] = st.acc[g][e].y;
+      }
+    }
+    __syncthreads();
+    for (int dim = tid; dim < D; dim += NT) {
+      float M = red_m[g];
+#pragma unroll
+      for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w * G + g]);
+      float A = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float sc = exp2f(red_m[w * G + g] - M);
+        A += red_acc[w * D + dim] * sc;
+        L += red_l[w * G + g] * sc;
+      }
+      if (pbase < 0) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<T*>(out)[(row0 + g) * D + dim] = from_f32<T>(A * inv);
+        if (dim == 0 && lse != nullptr) lse[row0 + g] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+      } else {
+        part_acc[(pbase + g) * D + dim] = A;
+        if (dim == 0) {
+          part_ml[(pbase + g) * 2] = M;
+          part_ml[(pbase + g) * 2 + 1] = L;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Tail block unit of unit u (decode-step buffer, per-unit table, or standalone stride).
+__device__ __forceinline__ const uint8_t* attn_tail_src(const AttnKParams& p, const uint8_t* tail, int u) {
+  if (p.tail_tab != nullptr) return p.units + (long long)p.tail_tab[u] * p.payload;
+  return tail + (long long)u * p.tail_stride;
+}
+
+// CTA of the stream-K partition that holds item x.
+__device__ __forceinline__ int sk_cta_of(long long x, long long T, int C) {
+  return (int)(((x + 1) * C - 1) / T);
+}
+
+// Stream-K split of the same attention: one wave of CTAs, each streaming an equal
+// share of the concatenated item lists (a share crosses unit boundaries), so no
+// SM idles while a last partial wave runs. At a unit boundary the CTA folds its
+// state into the unit's partial (one partial per CTA that touches the unit; the
+// direct output when one CTA holds the whole unit) and restages the queries; the
+// copy ring keeps running across the boundary. The unit's last partial to land
+// triggers the merge, as in attn_split_kernel.
+template <typename T, int D, int G, int W>
+__global__ void __launch_bounds__(32 * W) attn_streamk_kernel(AttnKParams p) {
+  using Gm = AttnGeom<T, D, G, W>;
+  constexpr int B = Gm::B, GP = Gm::GP, QP = Gm::QP, PARTS = Gm::PARTS, TPW = Gm::TPW;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const long long payload = p.payload;
+  uint8_t* stage_buf = smem;
+  float* q_s = reinterpret_cast<float*>(smem + (size_t)p.stages * payload);
+  float* p_s = q_s + G * PARTS * QP;
+  float* red = p_s + B * GP;                                        // [W][D] + 2 [W][G]
+  int* list = reinterpret_cast<int*>(red + W * D + 2 * W * G);      // [bps + 1] block or -2 (tail)
+  int* lunit = list + p.bps + 1;                                    // [bps + 1] unit - u_first
+  uint64_t* full = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(lunit + p.bps + 1) + 7) & ~uintptr_t(7));
+  uint64_t* empty = full + p.stages;
+  __shared__ int s_nl, s_last;
+  __shared__ volatile int s_bad;
+
+  const int cta = blockIdx.x, C = p.sk_ctas, nv = p.nv;
+  const long long NI = p.sk_items;
+  const long long g0 = (long long)cta * NI / C, g1 = (long long)(cta + 1) * NI / C;
+  if (g0 >= g1) return;  // (whole CTA: no item, no unit touched)
+  const int u_first = p.unit_base + (int)(g0 / nv), u_last = p.unit_base + (int)((g1 - 1) / nv);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const void* q_in = p.q;
+  void* out = p.out;
+  float* lse = p.lse;
+  int tail_len0 = p.tail_len;
+  const uint8_t* tail = p.tail;
+  if (p.dyn != nullptr) {
+    q_in = p.dyn->q;
+    out = p.dyn->out;
+    lse = p.dyn->lse;
+    tail_len0 = p.dyn->tail_len;
+    if (tail != nullptr) tail += p.dyn->tail_off;
+  }
+  const bool with_tail = (tail != nullptr) || (p.tail_tab != nullptr);
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], W);
+    }
+    fence_mbar_init();
+    s_bad = 0;
+  }
+  if (warp == 0) {  // the CTA's items in order: valid blocks and tails, tagged by unit
+    int cnt = 0;
+    for (long long base = g0; base < g1; base += 32) {
+      const long long x = base + lane;
+      int idx = -1, lu = 0;
+      if (x < g1) {
+        const int uu = p.unit_base + (int)(x / nv), j = (int)(x % nv);
+        lu = uu - u_first;
+        if (j < p.n_blocks) {
+          idx = p.block_tab[(long long)uu * p.n_blocks + j];
+          if (idx >= 0 && (long long)idx >= p.n_units) {
+            atomicExch(p.err, kDevErrBadIndex);
+            idx = -1;
+          }
+        } else if (with_tail) {
+          idx = -2;
+        }
+      }
+      const bool on = idx >= 0 || idx == -2;
+      const unsigned m = __ballot_sync(0xffffffffu, on);
+      if (on) {
+        const int at = cnt + __popc(m & ((1u << lane) - 1u));
+        list[at] = idx;
+        lunit[at] = lu;
+      }
+      cnt += __popc(m);
+    }
+    if (lane == 0) s_nl = cnt;
+    __syncwarp();
+  }
+  __syncthreads();
+  const int nl = s_nl;
+  int issued = 0;  // meaningful in thread 0 only
+  auto src_of = [&](int i) -> const uint8_t* {
+    const int idx = list[i];
+    return idx >= 0 ? p.units + (long long)idx * payload : attn_tail_src(p, tail, u_first + lunit[i]);
+  };
+  if (tid == 0) {
+    const int pre = min(p.stages, nl);
+    for (int s = 0; s < pre; ++s) {
+      mbar_arrive_expect_tx(&full[s], (uint32_t)payload);
+      bulk_g2s(stage_buf + (size_t)s * payload, src_of(s), (uint32_t)payload, &full[s]);
+    }
+    issued = pre;
+  }
+
+  const int tok = warp * TPW + lane % TPW;
+  int it = 0;
+  for (int uu = u_first; uu <= u_last; ++uu) {
+    const int b = uu / p.Hkv, h = uu % p.Hkv;
+    const int tail_len = p.tail_lens != nullptr ? p.tail_lens[uu] : tail_len0;
+    __syncthreads();  // q_s, p_s and red are free
+    attn_stage_q<T, D, G, W>(q_s, q_in, b, h, p.Hq, p.qscale, tid);
+    __syncthreads();
+    AttnWarpState<T, D, G, W> st;
+    st.init();
+    for (; it < nl && lunit[it] == uu - u_first; ++it) {
+      if (__any_sync(0xffffffffu, s_bad != 0)) break;
+      const int si = it % p.stages;
+      const uint32_t par = (uint32_t)((it / p.stages) & 1);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[si], par));
+      if (!ok) {
+        if (lane == 0) {
+          s_bad = 1;
+          atomicExch(p.err, kDevErrWaitTimeout);
+        }
+        break;
+      }
+      attn_block<T, D, G, W>(stage_buf + (size_t)si * payload, q_s, p_s, (list[it] >= 0) || (tok < tail_len),
+                             st, warp, lane);
+      if (lane == 0) mbar_arrive(&empty[si]);
+      if (tid == 0 && issued < nl && s_bad == 0) {
+        if (!mbar_wait_bounded(&empty[si], par)) {
+          s_bad = 1;
+          atomicExch(p.err, kDevErrWaitTimeout);
+        } else {
+          mbar_arrive_expect_tx(&full[si], (uint32_t)payload);
+          bulk_g2s(stage_buf + (size_t)si * payload, src_of(issued), (uint32_t)payload, &full[si]);
+          ++issued;
+        }
+      }
+    }
+    __syncthreads();
+    if (s_bad != 0) break;
+    // this CTA's share of unit uu: the output itself or one of its partials
+    const long long ib = (long long)(uu - p.unit_base) * nv;
+    const int c_first = sk_cta_of(ib, NI, C), c_last = sk_cta_of(ib + nv - 1, NI, C);
+    const int nseg = c_last - c_first + 1;
+    const long long row0 = (long long)b * p.Hq + (long long)h * G;
+    attn_reduce_by_head<T, D, G, W>(st, red, tid, warp, lane, p.part_acc, p.part_ml,
+                                    nseg == 1 ? -1 : ((long long)uu * p.seg_cap + (cta - c_first)) * G,
+                                    out, lse, row0);
+    if (nseg == 1) continue;
+    if (tid == 0) {
+      int prev;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(p.counters + uu)
+                   : "memory");
+      s_last = (prev == nseg - 1);
+    }
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    attn_merge<T, D, G, W>(p.part_acc, p.part_ml, (long long)uu * p.seg_cap * G, nseg, red, out, lse,
+                           row0, tid);
+    if (tid == 0) p.counters[uu] = 0;
+  }
+  __syncthreads();
+  if (s_bad != 0 && tid == 0) {  // drain: the last copy issued into each stage
+    for (int s = 0; s < p.stages; ++s) {
+      int last = -1;
+      for (int li = s; li < issued; li += p.stages) last = li;
+      if (last >= 0) mbar_wait_bounded(&full[s], (uint32_t)((last / p.stages) & 1));
+    }
+  }
+}
+
+template <typename T, int D, int G, int W>
+size_t attn_streamk_smem(int stages, long long payload, int bps) {
+  using Gm = AttnGeom<T, D, G, W>;
+  size_t off = (size_t)stages * payload;
+  off += (size_t)G * Gm::PARTS * Gm::QP * 4 + (size_t)Gm::B * Gm::GP * 4;
+  off += (size_t)(W * D + 2 * W * G) * 4;
+  off += (size_t)2 * (bps + 1) * 4;
+  off = (off + 7) & ~(size_t)7;
+  off += (size_t)2 * stages * 8;
+  return off;
+}
+
 template <typename T, int D, int G, int W>
 cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, int bps,
                                 cudaStream_t stream) {
@@ -548,6 +824,18 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.dyn = a.dyn;
   p.tail_tab = a.tail_tab;
   p.tail_lens = a.tail_lens;
+  p.sk_ctas = a.sk_ctas;
+  p.nv = a.n_blocks + ((a.tail != nullptr || a.tail_tab != nullptr) ? 1 : 0);
+  p.seg_cap = a.seg_cap;
+  p.sk_items = (long long)a.unit_count * p.nv;
+  if (a.sk_ctas > 0) {
+    const size_t smem = attn_streamk_smem<T, D, G, W>(stages, s.payload, bps);
+    static std::atomic<int> lim_sk[64];
+    cudaError_t err = raise_smem_limit((const void*)attn_streamk_kernel<T, D, G, W>, smem, lim_sk);
+    if (err != cudaSuccess) return err;
+    attn_streamk_kernel<T, D, G, W><<<a.sk_ctas, 32 * W, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   const size_t smem = AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps);
   static std::atomic<int> lim[64];
   cudaError_t err = raise_smem_limit((const void*)attn_split_kernel<T, D, G, W>, smem, lim);
@@ -571,6 +859,32 @@ int attn_occupancy_variant(const Shape& s, int stages, int bps) {
   return n;
 }
 
+// CTAs per SM of the stream-K kernel (0 if it cannot run).
+template <typename T, int D, int G, int W>
+int attn_streamk_occupancy_variant(const Shape& s, int stages, int bps) {
+  const size_t smem = attn_streamk_smem<T, D, G, W>(stages, s.payload, bps);
+  static std::atomic<int> lim[64];
+  if (raise_smem_limit((const void*)attn_streamk_kernel<T, D, G, W>, smem, lim) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_streamk_kernel<T, D, G, W>, 32 * W, smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <typename T, int D, int W>
+int attn_streamk_occupancy_dispatch_g(const Shape& s, int stages, int bps) {
+  switch (s.G) {
+    case 1: return attn_streamk_occupancy_variant<T, D, 1, W>(s, stages, bps);
+    case 2: return attn_streamk_occupancy_variant<T, D, 2, W>(s, stages, bps);
+    case 3: return attn_streamk_occupancy_variant<T, D, 3, W>(s, stages, bps);
+    case 4: return attn_streamk_occupancy_variant<T, D, 4, W>(s, stages, bps);
+    case 6: return attn_streamk_occupancy_variant<T, D, 6, W>(s, stages, bps);
+    case 8: return attn_streamk_occupancy_variant<T, D, 8, W>(s, stages, bps);
+    default: return 0;
+  }
+}
+
 template <typename T, int D, int W>
 int attn_occupancy_dispatch_g(const Shape& s, int stages, int bps) {
   switch (s.G) {
@@ -588,6 +902,11 @@ template <typename T, int D>
 int attn_occupancy_dispatch_w(const Shape& s, int stages, int bps, int warps) {
   return warps == 8 ? attn_occupancy_dispatch_g<T, D, 8>(s, stages, bps)
                     : attn_occupancy_dispatch_g<T, D, 4>(s, stages, bps);
+}
+template <typename T, int D>
+int attn_streamk_occupancy_dispatch_w(const Shape& s, int stages, int bps, int warps) {
+  return warps == 8 ? attn_streamk_occupancy_dispatch_g<T, D, 8>(s, stages, bps)
+                    : attn_streamk_occupancy_dispatch_g<T, D, 4>(s, stages, bps);
 }
 
 template <typename T, int D, int W>
@@ -618,5 +937,7 @@ cudaError_t launch_attention_bf16(const Shape& s, const AttnArgs& a, int stages,
                                   int warps, cudaStream_t stream);
 int attention_occupancy_f32(const Shape& s, int stages, int bps, int warps);
 int attention_occupancy_bf16(const Shape& s, int stages, int bps, int warps);
+int attention_streamk_occupancy_f32(const Shape& s, int stages, int bps, int warps);
+int attention_streamk_occupancy_bf16(const Shape& s, int stages, int bps, int warps);
 
 }  // namespace nosa

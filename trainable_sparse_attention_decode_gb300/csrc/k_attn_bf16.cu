@@ -13,4 +13,9 @@ int attention_occupancy_bf16(const Shape& s, int stages, int bps, int warps) {
   if (s.d == 128) return attn_occupancy_dispatch_w<__nv_bfloat16, 128>(s, stages, bps, warps);
   return 0;
 }
+int attention_streamk_occupancy_bf16(const Shape& s, int stages, int bps, int warps) {
+  if (s.d == 64) return attn_streamk_occupancy_dispatch_w<__nv_bfloat16, 64>(s, stages, bps, warps);
+  if (s.d == 128) return attn_streamk_occupancy_dispatch_w<__nv_bfloat16, 128>(s, stages, bps, warps);
+  return 0;
+}
 }  // namespace nosa

@@ -13,4 +13,9 @@ int attention_occupancy_f32(const Shape& s, int stages, int bps, int warps) {
   if (s.d == 128) return attn_occupancy_dispatch_w<float, 128>(s, stages, bps, warps);
   return 0;
 }
+int attention_streamk_occupancy_f32(const Shape& s, int stages, int bps, int warps) {
+  if (s.d == 64) return attn_streamk_occupancy_dispatch_w<float, 64>(s, stages, bps, warps);
+  if (s.d == 128) return attn_streamk_occupancy_dispatch_w<float, 128>(s, stages, bps, warps);
+  return 0;
+}
 }  // namespace nosa

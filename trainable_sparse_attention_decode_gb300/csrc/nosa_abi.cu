@@ -210,13 +210,70 @@ int attention_pick_nsplit_uncached(const Shape& s, int n_blocks) {
   return best;
 }
 
+// Single-launch plan: stream-K over one wave of resident CTAs when each CTA's
+// share fits its item list (<= 256) and a unit spans at most 16 CTAs; otherwise
+// the classic split. NOSA_ATTN_STREAMK=0 forces the classic split. The partial
+// slots cover both a launch with a tail and one without.
+AttnPlan attention_plan_single_uncached(const Shape& s, int n_blocks) {
+  AttnPlan pl;
+  pl.nsplit = attention_pick_nsplit(s, n_blocks, 1);
+  pl.sk_ctas = 0;
+  pl.seg_cap = 0;
+  pl.slots = pl.nsplit;
+  const char* g = std::getenv("NOSA_ATTN_STREAMK");
+  if ((g && std::strcmp(g, "0") == 0) || n_blocks < 1) return pl;
+  const int stages = attn_stages(s.payload);
+  const int occ = s.dtype == 0 ? attention_streamk_occupancy_f32(s, stages, 256, attn_warps())
+                               : attention_streamk_occupancy_bf16(s, stages, 256, attn_warps());
+  if (occ < 1) return pl;
+  const long long C = (long long)sm_count_current() * occ;
+  int cap = 0;
+  for (int nv = n_blocks; nv <= n_blocks + 1; ++nv) {
+    const long long T = (long long)s.U * nv;
+    const long long minlen = T / C;  // items of the shortest share
+    if (minlen < 2 || (T + C - 1) / C > 256) return pl;
+    cap = std::max<int>(cap, (int)((nv + minlen - 1) / minlen + 1));
+  }
+  // the merge's scratch (3 x partials x G floats) lives in the CTA's reduce
+  // buffer (W x d + 2 W x G floats)
+  const int W = attn_warps();
+  if (cap > 16 || 3 * cap * s.G > W * s.d + 2 * W * s.G) return pl;
+  pl.sk_ctas = (int)C;
+  pl.seg_cap = cap;
+  pl.slots = std::max(cap, pl.nsplit);  // (a launch without items takes the classic split)
+  return pl;
+}
+
+AttnPlan attention_plan_single(const Shape& s, int n_blocks) {
+  static std::mutex mu;
+  static std::map<std::array<long long, 8>, AttnPlan> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const char* g = std::getenv("NOSA_ATTN_STREAMK");
+  const long long sk_off = (g && std::strcmp(g, "0") == 0) ? 1 : 0;
+  const std::array<long long, 8> key = {dev, s.dtype, s.d, s.G, s.U, n_blocks, attn_warps(), sk_off};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const AttnPlan pl = attention_plan_single_uncached(s, n_blocks);
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = pl;
+  return pl;
+}
+
 // Message returned by nosa_last_error(NULL) on this thread.
 void set_thread_error(const std::string& msg) { g_thread_err = msg; }
 
 cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t stream) {
   const int stages = attn_stages(s.payload);
-  const int nv = a.n_blocks + (a.tail ? 1 : 0);
-  const int bps = std::max(1, (nv + a.nsplit - 1) / a.nsplit);
+  const int nv = a.n_blocks + ((a.tail || a.tail_tab) ? 1 : 0);
+  int bps = std::max(1, (nv + a.nsplit - 1) / a.nsplit);
+  if (a.sk_ctas > 0) {  // items of the longest stream-K share
+    const long long T = (long long)a.unit_count * nv;
+    bps = (int)std::max<long long>(1, (T + a.sk_ctas - 1) / a.sk_ctas);
+  }
   return s.dtype == 0 ? launch_attention_f32(s, a, stages, bps, attn_warps(), stream)
                       : launch_attention_bf16(s, a, stages, bps, attn_warps(), stream);
 }
@@ -1137,7 +1194,7 @@ size_t nosa_attention_workspace_bytes(const nosa_config* cfg, int32_t n_blocks) 
   if (validate(cfg, why) != NOSA_OK || n_blocks < 0) return 0;
   DeviceGuard guard(cfg->device);
   const Shape s = shape_of(*cfg);
-  return attention_workspace_bytes(s, attention_pick_nsplit(s, n_blocks, 1));
+  return attention_workspace_bytes(s, attention_plan_single(s, n_blocks).slots);
 }
 
 nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int64_t n_units,
@@ -1160,8 +1217,10 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
   }
   DeviceGuard guard(cfg->device);
   const Shape s = shape_of(*cfg);
-  const int nsplit = attention_pick_nsplit(s, n_blocks, 1);
-  const size_t need = attention_workspace_bytes(s, nsplit);
+  const AttnPlan plan = attention_plan_single(s, n_blocks);
+  const bool streamk = plan.sk_ctas > 0 && (n_blocks + (tail ? 1 : 0)) > 0;
+  const int nsplit = streamk ? plan.seg_cap : plan.nsplit;
+  const size_t need = attention_workspace_bytes(s, plan.slots);
   if (workspace_bytes < need) {
     g_thread_err = "workspace too small (see nosa_attention_workspace_bytes)";
     return NOSA_ERR_INVALID_ARG;
@@ -1191,6 +1250,10 @@ nosa_status nosa_sparse_attention(const nosa_config* cfg, const void* units, int
   a.unit_count = s.U;
   a.counters = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes);
   a.err = reinterpret_cast<int*>(ws + acc_bytes + ml_bytes + cnt_bytes);
+  if (streamk) {
+    a.sk_ctas = plan.sk_ctas;
+    a.seg_cap = plan.seg_cap;
+  }
   // counters and error word start at zero (one memset over both)
   cudaError_t e = cudaMemsetAsync(a.counters, 0, cnt_bytes + sizeof(int), st);
   if (e == cudaSuccess) e = launch_attention(s, a, st);

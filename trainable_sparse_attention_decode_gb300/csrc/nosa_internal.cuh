@@ -224,7 +224,18 @@ struct AttnArgs {
   // with tail_lens[u] tokens (tail must be non-null; tail_stride is then 0).
   const int32_t* tail_tab = nullptr;
   const int32_t* tail_lens = nullptr;
+  // Stream-K (single launch over all items): sk_ctas > 0 CTAs share the items
+  // equally; seg_cap partial slots per unit (then also nsplit = nsplit_total).
+  int sk_ctas = 0;
+  int seg_cap = 0;
 };
+// How a single attention launch over n_blocks table entries (+ tail) per unit is
+// split: stream-K with sk_ctas CTAs (0: the classic split into nsplit per unit);
+// slots = partial slots per unit the workspace must hold.
+struct AttnPlan {
+  int nsplit, sk_ctas, seg_cap, slots;
+};
+AttnPlan attention_plan_single(const Shape& s, int n_blocks);
 size_t attention_workspace_bytes(const Shape& s, int nsplit);
 int attention_pick_nsplit(const Shape& s, int n_blocks, int has_tail);
 cudaError_t launch_attention(const Shape& s, const AttnArgs& a, cudaStream_t stream);
