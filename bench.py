@@ -183,7 +183,7 @@ ATTN_SOURCES = ["trainable_sparse_attention_decode_gb300/csrc/k_attn.cuh",
 def ncu_traffic(workload_name):
     """Per-launch DRAM bytes of the attention kernel from the committed ncu summary,
     or None when the summary is missing or the kernel source changed since."""
-    p = os.path.join(ROOT, "profiles", f"attn_split_kernel_{workload_name}.md")
+    p = os.path.join(ROOT, "profiles", f"attn_streamk_kernel_{workload_name}.md")
     if not os.path.exists(p):
         return None
     src_hash = kernel_source_hash(ATTN_SOURCES)
@@ -592,9 +592,10 @@ def run_gpu(args, rank, world, local_rank):
     host_bytes_step = st["host_bytes"] / K
     host_bytes_window = st_ph["host_bytes"] / KT if st_ph else 0.0
     recall_gbs = (host_bytes_window / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
-    # Roofline kernel: the split-K attention, timed alone on the step's shape (in the
-    # step it shares the GPU with the gather, which would blur its own bound).
-    dominant = "attn_split_kernel (alone, step shape)"
+    # Roofline kernel: the attention, timed alone on the step's shape as one
+    # launch over all the step's blocks (the stream-K split; in the step it
+    # shares the GPU with the gather, which would blur its own bound).
+    dominant = "attn_streamk_kernel (alone, step shape)"
     dom_bytes, dom_us = alone_bytes, alone_secs * 1e6
     traffic = ncu_traffic(w0.name)
     value = tokens / max_secs
