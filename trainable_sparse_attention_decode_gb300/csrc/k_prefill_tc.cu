@@ -16,25 +16,27 @@
 //             accumulator in tensor memory, M = 128, N = 64, K = d); each row:
 //             logits = S log2(e)/sqrt(d) + e_j log2(e), -inf where the row's
 //             position did not select the block (in the own block also past the
-//             position); P = exp2(logit - m) in fp16 into shared memory; O += P V
-//             on the tensor cores (fp16 in: V converted exactly with one power-of-
-//             two scale of the call; M = 128, N = d, K = 64), O in tensor memory.
+//             position); P = exp2(logit - m) in fp16 written over the S columns it
+//             came from; O += P V on the tensor cores with P read from tensor
+//             memory (fp16 in: V converted exactly with one power-of-two scale of
+//             the call; M = 128, N = d, K = 64), O in tensor memory.
 // Online softmax with a lazy reference: a row keeps its running max m until a
 // block raises it by more than 8 (base 2), so P <= 2^8; only then is the row's O
 // rescaled in tensor memory (and its sum l in fp32). The sum l adds the fp32
 // probabilities, so the log-sum-exp is exact to fp32 rounding.
 // Warp roles: warps 0 .. 4 mt - 1 own one row each per thread (warp w reads
 // tensor-memory lanes 32 (w % 4) ..), the last warp issues the MMAs and the bulk
-// copies. S is double-buffered in tensor memory and the block units take three
-// shared-memory stages, so S of block i + 1 and P V of block i - 1 run on the
-// tensor cores while the rows work on block i. Everything after the set-up is
-// ordered by mbarriers:
+// copies. S (then P) is double-buffered in tensor memory and the block units take
+// three shared-memory stages, so S of block i + 1 and P V of block i - 1 run on
+// the tensor cores while the rows work on block i; S of block i + 2 goes into
+// block i's buffer only once P V of block i, which reads P from it, completed.
+// Everything after the set-up is ordered by mbarriers:
 //   full[st]   a block unit landed (bulk copy)       s_full[sb] S of a block is in
 //   p_full     the rows wrote P (and rescaled O)      pv_done    P V completed
-// Operands are K-major with the 128-byte swizzle (rows of 128 bytes, 16-byte chunk
-// c of row r at chunk c ^ (r % 8), 8-row groups 1024 bytes apart): K and V^T as
-// the pack kernel lays out the units (stages 1024-byte aligned, so the MMAs read
-// a unit where its bulk copy put it), Q and P written in that form here. Every wait is
+// Shared-memory operands are K-major with the 128-byte swizzle (rows of 128 bytes,
+// 16-byte chunk c of row r at chunk c ^ (r % 8), 8-row groups 1024 bytes apart): K
+// and V^T as the pack kernel lays out the units (stages 1024-byte aligned, so the
+// MMAs read a unit where its bulk copy put it), Q written in that form here. Every wait is
 // bounded; one that gives up sets the error word and the CTA stops, waits
 // (bounded) for its copies and MMAs in flight and frees its tensor memory.
 #include "nosa_internal.cuh"
@@ -64,8 +66,7 @@ struct TileSmem {
   long long payload;
   __host__ __device__ size_t sstride() const { return ((size_t)payload + 1023) & ~(size_t)1023; }
   __host__ __device__ size_t qt() const { return 0; }                                     // [mt][d/64][128 x 128 B] bf16
-  __host__ __device__ size_t pt() const { return (size_t)mt * 256 * d; }                  // [mt][128 x 128 B] fp16
-  __host__ __device__ size_t stage() const { return pt() + (size_t)mt * 16384; }          // [kStages][sstride]
+  __host__ __device__ size_t stage() const { return (size_t)mt * 256 * d; }               // [kStages][sstride]
   __host__ __device__ size_t mask() const { return stage() + kStages * sstride(); }       // [nblk][2] u32
   __host__ __device__ size_t list() const { return mask() + 8 * (size_t)nblk; }           // [nblk] i32
   __host__ __device__ size_t total() const { return list() + 4 * (size_t)nblk + 1024; }
@@ -95,7 +96,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const int mt = a.mt, G = s.G;
   const TileSmem L{mt, D, a.nblk, s.payload};
   uint8_t* Qt = sm + L.qt();
-  uint8_t* Pt = sm + L.pt();
   uint8_t* stage = sm + L.stage();
   uint32_t* mask_s = reinterpret_cast<uint32_t*>(sm + L.mask());
   int32_t* list_s = reinterpret_cast<int32_t*>(sm + L.list());
@@ -225,19 +225,22 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         tc_fence_after();
         const uint8_t* unit = stage + (size_t)(i % kStages) * sstride;
         // K steps outermost: the M-tiles' accumulations alternate (the tensor pipe
-        // runs two independent accumulators back to back faster than one chain)
+        // runs two independent accumulators back to back faster than one chain).
+        // A = P of tile mm in S buffer i & 1 (8 columns per 16 tokens).
+        const uint32_t p_col = (uint32_t)((i & 1) * mt * 64);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           for (int mm = 0; mm < mt; ++mm) {
-            const uint64_t da = sw128_desc(smem_u32(Pt + (size_t)mm * 16384)) + 2 * kk;
             const uint64_t db = sw128_desc(smem_u32(unit + kbytes)) + 2 * kk;
-            mma_bf16(tmem + o_col + (uint32_t)(mm * D), da, db, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_tmem_a(tmem + o_col + (uint32_t)(mm * D), tmem + p_col + (uint32_t)(mm * 64 + kk * 8), db,
+                       idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
           }
         mma_commit(&pv_done);
         ++pv_issued;
+        // P V_i done: its stage is free and its P columns may take S_{i+2}
+        if (!(ok = mbar_wait_bounded(&pv_done, (uint32_t)(i & 1)))) break;
         if (i + 2 < cnt && !(ok = issue_s(i + 2))) break;
-        if (issued < cnt) {  // block i + kStages into block i's stage once P V_i is done
-          if (!(ok = mbar_wait_bounded(&pv_done, (uint32_t)(i & 1)))) break;
+        if (issued < cnt) {  // block i + kStages into block i's stage
           const int st = issued % kStages;
           mbar_arrive_expect_tx(&full[st], (uint32_t)payload);
           bulk_g2s(stage + (size_t)st * sstride, usrc + (long long)list_s[issued] * payload,
@@ -263,7 +266,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t t_o = tmem + lane_off + o_col + (uint32_t)(m * D);
     const float qs = 1.4426950408889634f * a.inv_sqrt_d;
-    uint8_t* prow = Pt + (size_t)m * 16384 + rr * 128;
     float m_run = -1e30f, l_run = 0.f;
     bool ok = true;
     for (int i = 0; i < cnt; ++i) {
@@ -330,7 +332,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       }
       l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m_run = m_use;
-      // P V of the previous block done: its P buffer is free and O is settled
+      // P V of the previous block done: O is settled. Every row warp observes
+      // every phase of pv_done in order (a parity wait cannot tell a phase from
+      // the one two later). A new reference scales O by alpha before P V of this
+      // block adds to it (grow is warp-uniform).
       if (i > 0) {
         ok = mbar_wait_bounded(&pv_done, (uint32_t)((i - 1) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
@@ -338,22 +343,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           break;
         }
         tc_fence_after();
-        if (grow) {
+      }
+      if (grow && i > 0) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            float v[16];
-            tmem_ld16(t_o + c0, v);
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          float v[16];
+          tmem_ld16(t_o + c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= alpha;
-            tmem_st16(t_o + c0, v);
-          }
+          for (int j = 0; j < 16; ++j) v[j] *= alpha;
+          tmem_st16(t_o + c0, v);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (rr & 7)) << 4)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      fence_proxy_async();
+      // P over the first 32 columns of this row's S (already in registers)
+      tmem_st32(tmem + lane_off + (uint32_t)(sb * mt * 64 + m * 64), pw);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full);
