@@ -36,6 +36,14 @@ namespace {
 
 constexpr int kPackThreads = 256;
 constexpr int kSelWarps = 8;
+constexpr int kSelRegSlots = 16;  // top-m keys per lane held in registers
+constexpr int kSelCH = 8;         // candidates per pooled-key chunk in shared memory
+
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Block units of the tiled tensor-core attention (bf16 inputs; k_prefill_tc.cu)
 // hold their operands in the canonical K-major layout with the 128-byte swizzle
@@ -207,11 +215,13 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
 // then the top-(k - |E_b|) by repeated warp arg-max (ties: lower index). Writes
 // the position's selection (E_b ascending, then Gamma_q ascending, -1 pad) into
 // sel, its attention block table (unit indices) and tail.
-// Scoring: lane (r, c) = (lane / 8, lane % 8) holds sub-block r's dims c*4 + 32v
-// (v < D/32) of a pooled key row and the same dims of the PB positions' q_bar,
-// so one load of a row serves PB positions; the PB partial sums of the 8 lanes of
-// a sub-block are reduced and transposed in 7 shuffles (lane c ends with position
-// c % PB), then the max over the 4 sub-blocks takes 2 more.
+// Scoring: the CTA copies the pooled rows of 8 candidates at a time into a
+// double-buffered shared-memory chunk (cp.async, all threads), and every warp
+// scores its positions from it. Lane (r, c) = (lane / 8, lane % 8) holds sub-block
+// r's dims c*4 + 32v (v < D/32) of a row and the same dims of the PB positions'
+// q_bar, so one read of a row serves PB positions; the PB partial sums of the 8
+// lanes of a sub-block are reduced and transposed in 7 shuffles (lane c ends with
+// position c % PB), then the max over the 4 sub-blocks takes 2 more.
 template <typename T, int D, int PB>
 __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
     Shape s, const T* __restrict__ q, int L, int nblk, const float* __restrict__ pk,
@@ -225,6 +235,9 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
   uint32_t* emask = reinterpret_cast<uint32_t*>(sm);                          // [W] E_b membership
   float* sq_s = reinterpret_cast<float*>(emask + ((W + 3) & ~3));              // [kSelWarps][PB][nblk]
   uint32_t* taken_s = reinterpret_cast<uint32_t*>(sq_s + (size_t)kSelWarps * PB * nblk);  // [kSelWarps][W]
+  int32_t* cl = reinterpret_cast<int32_t*>(taken_s + kSelWarps * W);          // [nblk] candidates outside E_b
+  float* pk_s = reinterpret_cast<float*>(cl + ((nblk + 3) & ~3));             // [2][kSelCH][4][D]
+  __shared__ int s_ncl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 3, c = lane & 7;
   const int ecnt = Ecnt[(long long)u * nblk + b];
@@ -235,13 +248,26 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
   __syncthreads();
   const int n_cand = b;  // blocks before the positions' own block
   const int m = min(s.k - ecnt, n_cand - ecnt);
+  if (warp == 0) {  // the candidates outside E_b, ascending (scores are kept in this order)
+    int run = 0;
+    for (int base = 0; base < n_cand; base += 32) {
+      const int j = base + lane;
+      const bool on = j < n_cand && !((emask[j >> 5] >> (j & 31)) & 1u);
+      const unsigned bal = __ballot_sync(0xffffffffu, on);
+      if (on) cl[run + __popc(bal & ((1u << lane) - 1u))] = j;
+      run += __popc(bal);
+    }
+    if (lane == 0) s_ncl = run;
+  }
+  __syncthreads();
+  const int ncl = s_ncl;
   const int npos = min(s.B, L - b * s.B);
   float* sqw = sq_s + (size_t)warp * PB * nblk;
   uint32_t* tk = taken_s + warp * W;
   const float inv_g = 1.0f / (float)s.G;
   const long long ubase = (long long)u * nblk;
   for (int g0 = 0; g0 < s.B / kSelWarps; g0 += PB) {
-    if (warp + kSelWarps * g0 >= npos) break;  // positions grow with g0
+    if (kSelWarps * g0 >= npos) break;  // (CTA-uniform: the chunk loop below syncs the CTA)
     // q_bar of the batch's positions, this lane's dims
     float4 qv[PB][NV];
 #pragma unroll
@@ -270,9 +296,28 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
       }
     }
     if (m > 0) {
-      for (int j = 0; j < n_cand; ++j) {
-        if ((emask[j >> 5] >> (j & 31)) & 1u) continue;  // (warp-uniform)
-        const float* row = pk + ((ubase + j) * s.P + r) * D + c * 4;
+      const int nch = (ncl + kSelCH - 1) / kSelCH;
+      auto load_chunk = [&](int ch) {
+        float* dst = pk_s + (size_t)(ch & 1) * kSelCH * 4 * D;
+        for (int i = threadIdx.x; i < kSelCH * D; i += blockDim.x) {  // float4 units: D per candidate
+          const int cc = i / D, f4 = i - cc * D, ci = ch * kSelCH + cc;
+          if (ci < ncl) cp_async16(dst + (size_t)cc * 4 * D + f4 * 4, pk + (ubase + cl[ci]) * s.P * D + f4 * 4);
+        }
+        cp_async_commit();
+      };
+      load_chunk(0);
+      for (int ch = 0; ch < nch; ++ch) {
+        if (ch + 1 < nch)
+          load_chunk(ch + 1);
+        else
+          cp_async_commit();  // (an empty group keeps wait_group 1 meaning "chunk ch landed")
+        cp_async_wait1();
+        __syncthreads();
+        const float* chunk = pk_s + (size_t)(ch & 1) * kSelCH * 4 * D;
+        const int ncc = min(kSelCH, ncl - ch * kSelCH);
+        for (int cc = 0; cc < ncc; ++cc) {
+        const int ci = ch * kSelCH + cc;
+        const float* row = chunk + ((size_t)cc * 4 + r) * D + c * 4;
         float4 x[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) x[v] = *reinterpret_cast<const float4*>(row + 32 * v);
@@ -308,7 +353,9 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
         float sc = acc[0];
         sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
         sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 16));
-        if (lane < PB) sqw[(size_t)lane * nblk + j] = sc * inv_sqrt_d;
+        if (lane < PB) sqw[(size_t)lane * nblk + ci] = sc * inv_sqrt_d;
+        }
+        __syncthreads();  // chunk buffer ch & 1 is refilled with chunk ch + 2 next
       }
       __syncwarp();
     }
@@ -320,38 +367,77 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
       const float* sqp = sqw + (size_t)i * nblk;
       for (int w = lane; w < W; w += 32) tk[w] = 0u;
       __syncwarp();
-      // top-m: m rounds of warp arg-max over the untaken candidates outside E_b.
-      // Lane l owns candidates j = l mod 32 and keeps the best of them as an
-      // order-preserving key (0: none; a NaN score is never a candidate); a round
-      // takes the largest key, at equal keys the lowest index, and only the
-      // winning lane looks for its next best.
-      auto lane_best = [&](uint32_t& key, int& idx) {
-        key = 0u;
-        idx = 0x7fffffff;
-        for (int j = lane; j < n_cand; j += 32) {
-          const uint32_t bit = 1u << (j & 31);
-          if ((emask[j >> 5] & bit) || (tk[j >> 5] & bit)) continue;
-          const float x = sqp[j];
-          if (x != x) continue;
-          const uint32_t kx = ordered_key(x);
-          if (kx > key) {  // ascending j: the first of equal keys stays
-            key = kx;
-            idx = j;
+      // top-m: m rounds of warp arg-max over the candidates outside E_b (scores
+      // in list order, so a lower list index is a lower block id). Lane l owns
+      // list entries l + 32 s as order-preserving keys (0: taken, or a NaN score,
+      // never a candidate); a round takes the largest key, at equal keys the
+      // lowest index, and only the winning lane looks for its next best. Up to
+      // 512 entries the keys live in registers, beyond in shared memory.
+      if (m > 0 && ncl <= 32 * kSelRegSlots) {
+        uint32_t kr[kSelRegSlots];
+#pragma unroll
+        for (int sl = 0; sl < kSelRegSlots; ++sl) {
+          const int ci = lane + 32 * sl;
+          const float x = ci < ncl ? sqp[ci] : 0.f;
+          kr[sl] = (ci < ncl && x == x) ? ordered_key(x) : 0u;
+        }
+        auto best_of = [&](uint32_t& key, int& slot) {
+          key = 0u;
+          slot = 0;
+#pragma unroll
+          for (int sl = 0; sl < kSelRegSlots; ++sl)
+            if (kr[sl] > key) {
+              key = kr[sl];
+              slot = sl;
+            }
+        };
+        uint32_t lkey;
+        int lslot;
+        best_of(lkey, lslot);
+        for (int round = 0; round < m; ++round) {
+          const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
+          if (kmax == 0u) break;  // none left (NaN scores)
+          const uint32_t win = __reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)(lane + 32 * lslot) : 0xffffffffu);
+          if ((int)(win & 31) == lane) {
+            const int j = cl[win];
+            atomicOr(&tk[j >> 5], 1u << (j & 31));  // (winners of other rounds share words)
+#pragma unroll
+            for (int sl = 0; sl < kSelRegSlots; ++sl)
+              if (sl == lslot) kr[sl] = 0u;
+            best_of(lkey, lslot);
           }
         }
-      };
-      uint32_t lkey;
-      int lidx;
-      if (m > 0) lane_best(lkey, lidx);
-      for (int round = 0; round < m; ++round) {
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
-        if (kmax == 0u) break;  // none left (NaN scores)
-        const int win = (int)__reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)lidx : 0xffffffffu);
-        if ((win & 31) == lane) {
-          tk[win >> 5] |= 1u << (win & 31);
-          lane_best(lkey, lidx);
-        }
         __syncwarp();
+      } else if (m > 0) {
+        auto lane_best = [&](uint32_t& key, int& idx) {
+          key = 0u;
+          idx = 0x7fffffff;
+          for (int ci = lane; ci < ncl; ci += 32) {
+            const int j = cl[ci];
+            if ((tk[j >> 5] >> (j & 31)) & 1u) continue;
+            const float x = sqp[ci];
+            if (x != x) continue;
+            const uint32_t kx = ordered_key(x);
+            if (kx > key) {  // ascending index: the first of equal keys stays
+              key = kx;
+              idx = ci;
+            }
+          }
+        };
+        uint32_t lkey;
+        int lidx;
+        lane_best(lkey, lidx);
+        for (int round = 0; round < m; ++round) {
+          const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
+          if (kmax == 0u) break;
+          const int win = (int)__reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)lidx : 0xffffffffu);
+          if ((win & 31) == lane) {
+            const int j = cl[win];
+            tk[j >> 5] |= 1u << (j & 31);
+            lane_best(lkey, lidx);
+          }
+          __syncwarp();
+        }
       }
       // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the mask)
       int32_t* selp = sel ? sel + vu * s.k : nullptr;
@@ -455,7 +541,7 @@ PrefillLayout prefill_layout(const Shape& s, int L, int nsplit) {
 size_t prefill_select_smem(const Shape& s, int nblk) {
   const int W = (nblk + 31) / 32;
   return (size_t)((W + 3) & ~3) * 4 + (size_t)kSelWarps * select_pb(nblk) * nblk * 4 +
-         (size_t)kSelWarps * W * 4;
+         (size_t)kSelWarps * W * 4 + (size_t)((nblk + 3) & ~3) * 4 + (size_t)2 * kSelCH * 4 * s.d * 4;
 }
 
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
