@@ -315,45 +315,58 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
         __syncthreads();
         const float* chunk = pk_s + (size_t)(ch & 1) * kSelCH * 4 * D;
         const int ncc = min(kSelCH, ncl - ch * kSelCH);
-        for (int cc = 0; cc < ncc; ++cc) {
-        const int ci = ch * kSelCH + cc;
-        const float* row = chunk + ((size_t)cc * 4 + r) * D + c * 4;
-        float4 x[NV];
+        // two candidates per pass: independent chains for the FMA and shuffle latencies
+        for (int cc = 0; cc < ncc; cc += 2) {
+          const int nc2 = min(2, ncc - cc);
+          float acc[2][PB];
 #pragma unroll
-        for (int v = 0; v < NV; ++v) x[v] = *reinterpret_cast<const float4*>(row + 32 * v);
-        float acc[PB];
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const float* row = chunk + ((size_t)(cc + (k2 < nc2 ? k2 : 0)) * 4 + r) * D + c * 4;
+            float4 x[NV];
 #pragma unroll
-        for (int i = 0; i < PB; ++i) {
-          float a = 0.f;
+            for (int v = 0; v < NV; ++v) x[v] = *reinterpret_cast<const float4*>(row + 32 * v);
 #pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            a = fmaf(x[v].x, qv[i][v].x, a);
-            a = fmaf(x[v].y, qv[i][v].y, a);
-            a = fmaf(x[v].z, qv[i][v].z, a);
-            a = fmaf(x[v].w, qv[i][v].w, a);
-          }
-          acc[i] = a;
-        }
-        // sum over the 8 lanes of sub-block r, transposed: lane c keeps position c % PB
+            for (int i = 0; i < PB; ++i) {
+              float a = 0.f;
 #pragma unroll
-        for (int o = 4; o >= 1; o >>= 1) {
-          if (o >= PB) {
-#pragma unroll
-            for (int i = 0; i < PB; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
-          } else {
-            const bool hi = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < o; ++i) {
-              const float send = hi ? acc[i] : acc[i + o];
-              const float keep = hi ? acc[i + o] : acc[i];
-              acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+              for (int v = 0; v < NV; ++v) {
+                a = fmaf(x[v].x, qv[i][v].x, a);
+                a = fmaf(x[v].y, qv[i][v].y, a);
+                a = fmaf(x[v].z, qv[i][v].z, a);
+                a = fmaf(x[v].w, qv[i][v].w, a);
+              }
+              acc[k2][i] = a;
             }
           }
-        }
-        float sc = acc[0];
-        sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
-        sc = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 16));
-        if (lane < PB) sqw[(size_t)lane * nblk + ci] = sc * inv_sqrt_d;
+          // sum over the 8 lanes of sub-block r, transposed: lane c keeps position c % PB
+#pragma unroll
+          for (int o = 4; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              if (o >= PB) {
+#pragma unroll
+                for (int i = 0; i < PB; ++i) acc[k2][i] += __shfl_xor_sync(0xffffffffu, acc[k2][i], o);
+              } else {
+                const bool hi = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < o; ++i) {
+                  const float send = hi ? acc[k2][i] : acc[k2][i + o];
+                  const float keep = hi ? acc[k2][i + o] : acc[k2][i];
+                  acc[k2][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+              }
+            }
+          }
+          float sc0 = acc[0][0], sc1 = acc[1][0];
+          sc0 = fmaxf(sc0, __shfl_xor_sync(0xffffffffu, sc0, 8));
+          sc1 = fmaxf(sc1, __shfl_xor_sync(0xffffffffu, sc1, 8));
+          sc0 = fmaxf(sc0, __shfl_xor_sync(0xffffffffu, sc0, 16));
+          sc1 = fmaxf(sc1, __shfl_xor_sync(0xffffffffu, sc1, 16));
+          if (lane < PB) {
+            const int ci = ch * kSelCH + cc;
+            sqw[(size_t)lane * nblk + ci] = sc0 * inv_sqrt_d;
+            if (nc2 == 2) sqw[(size_t)lane * nblk + ci + 1] = sc1 * inv_sqrt_d;
+          }
         }
         __syncthreads();  // chunk buffer ch & 1 is refilled with chunk ch + 2 next
       }
