@@ -87,13 +87,14 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&x);
 }
 
-template <int D>
+template <int D, int MT>
 __global__ void __launch_bounds__(kTileThreads, 1)
     prefill_tile_kernel(Shape s, PrefillTileArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int mt = a.mt, G = s.G;
+  constexpr int mt = MT;
+  const int G = s.G;
   const TileSmem L{mt, D, a.nblk, s.payload};
   uint8_t* Qt = sm + L.qt();
   uint8_t* stage = sm + L.stage();
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   }
   __syncthreads();
 
-  const uint32_t kbytes = (uint32_t)(s.B * D * 2);
+  constexpr uint32_t kbytes = (uint32_t)(64 * D * 2);
   const uint32_t o_col = (uint32_t)(2 * mt * 64);  // O tiles after the two S buffers
 
   if (warp == mma_warp) {
@@ -199,20 +200,25 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 64);
       constexpr uint32_t idesc_pv = idesc_f16(128, D);
+      // descriptor bases; a descriptor's start field counts 16-byte units and
+      // stays below 2^14 for any shared-memory address, so offsets add directly
+      const uint64_t dq = sw128_desc(smem_u32(Qt));
+      const uint64_t dstage = sw128_desc(smem_u32(stage));
+      const uint32_t sstride16 = (uint32_t)(sstride >> 4);
       bool ok = true;
       int s_issued = 0, pv_issued = 0;
       auto issue_s = [&](int j) {  // S_j = Q K_j^T into S buffer j & 1
         const int st = j % kStages;
         if (!mbar_wait_bounded(&full[st], (uint32_t)((j / kStages) & 1))) return false;
         tc_fence_after();
-        const uint8_t* unit = stage + (size_t)st * sstride;
+        const uint64_t dk = dstage + (uint64_t)(st * sstride16);
+        const uint32_t t_d = tmem + (uint32_t)((j & 1) * mt * 64);
+#pragma unroll
         for (int mm = 0; mm < mt; ++mm)
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // K16 step kk: 64-wide block kk / 4, +32 bytes each
-            const uint64_t da = sw128_desc(smem_u32(Qt + (size_t)mm * 256 * D + (kk >> 2) * 16384)) + 2 * (kk & 3);
-            const uint64_t db = sw128_desc(smem_u32(unit + (kk >> 2) * 8192)) + 2 * (kk & 3);
-            mma_bf16(tmem + (uint32_t)((j & 1) * mt * 64 + mm * 64), da, db, idesc_s, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)  // K16 step kk: 64-wide block kk / 4, +32 bytes each
+            mma_bf16(t_d + mm * 64, dq + (mm * 256 * D + (kk >> 2) * 16384) / 16 + 2 * (kk & 3),
+                     dk + (kk >> 2) * 8192 / 16 + 2 * (kk & 3), idesc_s, kk > 0 ? 1u : 0u);
         mma_commit(&s_full[j & 1]);
         ++s_issued;
         return true;
@@ -223,18 +229,17 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // the rows wrote P_i (and are done with S buffer i & 1)
         if (!(ok = mbar_wait_bounded(&p_full, (uint32_t)(i & 1)))) break;
         tc_fence_after();
-        const uint8_t* unit = stage + (size_t)(i % kStages) * sstride;
         // K steps outermost: the M-tiles' accumulations alternate (the tensor pipe
         // runs two independent accumulators back to back faster than one chain).
         // A = P of tile mm in S buffer i & 1 (8 columns per 16 tokens).
-        const uint32_t p_col = (uint32_t)((i & 1) * mt * 64);
+        const uint64_t dv = dstage + (uint64_t)((i % kStages) * sstride16) + kbytes / 16;
+        const uint32_t t_p = tmem + (uint32_t)((i & 1) * mt * 64);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          for (int mm = 0; mm < mt; ++mm) {
-            const uint64_t db = sw128_desc(smem_u32(unit + kbytes)) + 2 * kk;
-            mma_tmem_a(tmem + o_col + (uint32_t)(mm * D), tmem + p_col + (uint32_t)(mm * 64 + kk * 8), db,
-                       idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-          }
+#pragma unroll
+          for (int mm = 0; mm < mt; ++mm)
+            mma_tmem_a(tmem + o_col + mm * D, t_p + mm * 64 + kk * 8, dv + 2 * kk, idesc_pv,
+                       (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done);
         ++pv_issued;
         // P V_i done: its stage is free and its P columns may take S_{i+2}
@@ -437,8 +442,9 @@ cudaError_t launch_prefill_tile(const Shape& s, int L, const uint8_t* units, con
   a.mt = tile_mt(s);
   a.tmem_cols = tile_tmem_cols(s);
   a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)s.d));
-  const void* fn = s.d == 64 ? (const void*)prefill_tile_kernel<64> : (const void*)prefill_tile_kernel<128>;
-  static std::atomic<int> lim64[64], lim128[64];
+  const void* fn = s.d == 64 ? (a.mt == 1 ? (const void*)prefill_tile_kernel<64, 1> : (const void*)prefill_tile_kernel<64, 2>)
+                              : (a.mt == 1 ? (const void*)prefill_tile_kernel<128, 1> : (const void*)prefill_tile_kernel<128, 2>);
+  static std::atomic<int> lim[4][64];
   int dev = 0, optin = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -448,7 +454,7 @@ cudaError_t launch_prefill_tile(const Shape& s, int L, const uint8_t* units, con
   const size_t cap = (size_t)optin - fa.sharedSizeBytes;  // dynamic shared memory a CTA may have
   size_t smem = tile_smem(s, a.nblk);
   if (smem > cap) return cudaErrorInvalidConfiguration;
-  e = raise_smem_limit(fn, cap, s.d == 64 ? lim64 : lim128);
+  e = raise_smem_limit(fn, cap, lim[(s.d == 64 ? 0 : 2) + (a.mt - 1)]);
   if (e != cudaSuccess) return e;
   // CTAs resident on an SM must not ask for more than its 512 tensor-memory
   // columns together (an allocation would wait for another CTA's release):
@@ -464,10 +470,14 @@ cudaError_t launch_prefill_tile(const Shape& s, int L, const uint8_t* units, con
   for (int base = 0; base < s.U; base += 65535) {
     a.unit_base = base;
     const dim3 grid(a.nblk, std::min(65535, s.U - base));
-    if (s.d == 64)
-      prefill_tile_kernel<64><<<grid, kTileThreads, smem, stream>>>(s, a);
+    if (s.d == 64 && a.mt == 1)
+      prefill_tile_kernel<64, 1><<<grid, kTileThreads, smem, stream>>>(s, a);
+    else if (s.d == 64)
+      prefill_tile_kernel<64, 2><<<grid, kTileThreads, smem, stream>>>(s, a);
+    else if (a.mt == 1)
+      prefill_tile_kernel<128, 1><<<grid, kTileThreads, smem, stream>>>(s, a);
     else
-      prefill_tile_kernel<128><<<grid, kTileThreads, smem, stream>>>(s, a);
+      prefill_tile_kernel<128, 2><<<grid, kTileThreads, smem, stream>>>(s, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
