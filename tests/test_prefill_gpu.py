@@ -195,3 +195,12 @@ def test_phase_timing(tiled):
     _forward(cfg, L, q, k, v, e, out, None, None, tiled)
     f_ms, a_ms = nosa.nosa_prefill_timing()
     assert 0.0 < f_ms < 1000.0 and 0.0 < a_ms < 1000.0
+
+
+@pytest.mark.slow
+def test_long_sequence_fallback_paths():
+    # 700 blocks: up to 695 candidates outside E_b (the top-m keys no longer fit
+    # the registers: the shared-memory rounds) and more than 640 blocks (two
+    # positions per pooled-key pass); the tiled attention with 700-block unions
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=64, k=16, k_e=4)
+    _prefill(w, 64 * 700 + 13, attn_every=97)
