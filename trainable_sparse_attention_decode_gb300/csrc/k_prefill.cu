@@ -50,18 +50,13 @@ __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_g
 // (rows of 128 bytes = 64 elements along the MMA's K, 16-byte chunk c of row r
 // stored at chunk c ^ (r % 8), 8-row groups 1024 bytes apart), so the MMAs read
 // a unit where its bulk copy puts it (at a 1024-byte aligned stage):
-//   K   bf16, rows = tokens, K = head dim: 64-dim blocks of 64 x 128 bytes;
+//   K   bf16, rows = tokens, K = head dim: 64-dim blocks of 64 x 128 bytes
+//       (dims 8c .. 8c + 7 of token t at (c / 8) 8192 + 128 t + 16 ((c % 8) ^ (t % 8)));
 //   V^T fp16, rows = head dim, K = tokens: d x 128 bytes, each value times 2^vs
 //       (vs from the largest |v| of the call, so every value converts exactly
-//       unless it is 2^29 below that maximum);
+//       unless it is 2^29 below that maximum); tokens 8g .. 8g + 7 of dim r at
+//       128 d + 128 r + 16 (g ^ (r % 8));
 //   e   fp32 x log2(e), as in the decode layout.
-__device__ __forceinline__ long long tk_off(int t, int dim) {  // K (bf16)
-  const int c = dim >> 3;
-  return (long long)(c >> 3) * 8192 + t * 128 + (((c & 7) ^ (t & 7)) << 4) + (dim & 7) * 2;
-}
-__device__ __forceinline__ long long tv_off(int t, int dim, int B, int d) {  // V^T (fp16)
-  return (long long)B * d * 2 + (long long)dim * 128 + ((((t >> 3) ^ (dim & 7))) << 4) + (t & 7) * 2;
-}
 
 // Largest |v| of the call (as fp32 bits; nonnegative floats order like their
 // bits) into *absmax, which starts at 0.
@@ -78,15 +73,12 @@ __global__ void __launch_bounds__(256) prefill_vmax_kernel(const __nv_bfloat16* 
 // Block unit of (unit u, block blk) from k, v [batch][L][Hkv][d], e [batch][L][Hkv];
 // tokens past L are zeros. Complete blocks are pooled: sub-block mean keys (fp32
 // token-order sums x 1/16) and the block's eviction score (max of the sub-block
-// means of e). grid = (nblk, U). TC: the tensor-core unit layout above (the pooled
-// scores use e itself); vmax is the largest |v| (bits), TC only.
-template <typename T, bool TC>
+// means of e). grid = (nblk, U).
+template <typename T>
 __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
     Shape s, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ e, int L,
-    int nblk, uint8_t* __restrict__ units, float* __restrict__ pk, float* __restrict__ se,
-    const uint32_t* __restrict__ vmax) {
+    int nblk, uint8_t* __restrict__ units, float* __restrict__ pk, float* __restrict__ se) {
   const int blk = blockIdx.x, u = blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
-  const float vmul = TC ? ldexpf(1.0f, v_scale_exp(*vmax)) : 1.0f;
   uint8_t* unit = units + ((long long)u * nblk + blk) * s.payload;
   const int t0 = blk * s.B;
   const int nt = min(s.B, L - t0);
@@ -98,19 +90,12 @@ __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
       kv = k[src];
       vv = v[src];
     }
-    if (TC) {
-      *reinterpret_cast<T*>(unit + tk_off(t, dim)) = kv;
-      *reinterpret_cast<__half*>(unit + tv_off(t, dim, s.B, s.d)) = __float2half_rn(to_f32(vv) * vmul);
-    } else {
-      *reinterpret_cast<T*>(unit + k_off(t, dim, s.B, s.elt)) = kv;
-      *reinterpret_cast<T*>(unit + v_off(t, dim, s.B, s.d, s.elt)) = vv;
-    }
+    *reinterpret_cast<T*>(unit + k_off(t, dim, s.B, s.elt)) = kv;
+    *reinterpret_cast<T*>(unit + v_off(t, dim, s.B, s.d, s.elt)) = vv;
   }
-  // (TC: the tiled attention works in base 2 and takes e x log2(e))
-  const float escale = TC ? 1.4426950408889634f : 1.0f;
   for (int t = threadIdx.x; t < s.B; t += blockDim.x)
     *reinterpret_cast<float*>(unit + e_off(t, s.B, s.d, s.elt)) =
-        (t < nt) ? e[((long long)b * L + t0 + t) * s.Hkv + h] * escale : 0.f;
+        (t < nt) ? e[((long long)b * L + t0 + t) * s.Hkv + h] : 0.f;
   for (long long i = 2LL * s.B * s.d * s.elt + 4LL * s.B + threadIdx.x; i < s.payload; i += blockDim.x)
     unit[i] = 0;
   if (nt < s.B) return;  // an incomplete block is never a candidate
@@ -129,6 +114,75 @@ __global__ void __launch_bounds__(kPackThreads) prefill_pack_kernel(
       float acc = 0.f;
       for (int j = 0; j < s.S; ++j) acc += e[((long long)b * L + t0 + sb * s.S + j) * s.Hkv + h];
       const float m = acc * (1.0f / s.S);
+      best = (sb == 0) ? m : fmaxf(best, m);
+    }
+    se[(long long)u * nblk + blk] = best;
+  }
+}
+
+// The packing for the tiled tensor-core attention (bf16, the layout above), block
+// by block through shared memory: K and V staged with 16-byte loads; K written as
+// whole swizzled 16-byte chunks; V^T as 16-byte chunks of 8 tokens of one head
+// dim (consecutive threads take consecutive dims, so the gather from the staged V
+// is free of bank conflicts), scaled by 2^vs into fp16; e x log2(e); pooled keys
+// from the staged K in token order (the same fp32 sums as prefill_pack_kernel).
+template <int D>
+__global__ void __launch_bounds__(kPackThreads) prefill_pack_tc_kernel(
+    Shape s, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    const float* __restrict__ e, int L, int nblk, uint8_t* __restrict__ units, float* __restrict__ pk,
+    float* __restrict__ se, const uint32_t* __restrict__ vmax) {
+  constexpr int RS = D + 8;  // padded row of the staged tiles (bf16 elements; 16-byte multiple)
+  __shared__ __align__(16) __nv_bfloat16 k_s[64 * RS], v_s[64 * RS];
+  const int blk = blockIdx.x, u = blockIdx.y, b = u / s.Hkv, h = u % s.Hkv;
+  uint8_t* unit = units + ((long long)u * nblk + blk) * s.payload;
+  const int t0 = blk * 64, nt = min(64, L - t0);
+  const float vmul = ldexpf(1.0f, v_scale_exp(*vmax));
+  for (int i = threadIdx.x; i < 64 * (D / 8); i += blockDim.x) {
+    const int t = i / (D / 8), c = i % (D / 8);
+    uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
+    if (t < nt) {
+      const long long src = (((long long)b * L + t0 + t) * s.Hkv + h) * D + c * 8;
+      kx = *reinterpret_cast<const uint4*>(k + src);
+      vx = *reinterpret_cast<const uint4*>(v + src);
+    }
+    *reinterpret_cast<uint4*>(k_s + t * RS + c * 8) = kx;
+    *reinterpret_cast<uint4*>(v_s + t * RS + c * 8) = vx;
+    // K chunk c of token t (dims 8c .. 8c + 7 are one chunk of the swizzled row)
+    *reinterpret_cast<uint4*>(unit + (c >> 3) * 8192 + t * 128 + (((c & 7) ^ (t & 7)) << 4)) = kx;
+  }
+  __syncthreads();
+  // V^T: row dim holds tokens 0..63 (8 chunks of 8); thread (dim, chunk tg)
+  for (int i = threadIdx.x; i < D * 8; i += blockDim.x) {
+    const int dim = i % D, tg = i / D;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a0 = __bfloat162float(v_s[(8 * tg + 2 * q) * RS + dim]) * vmul;
+      const float a1 = __bfloat162float(v_s[(8 * tg + 2 * q + 1) * RS + dim]) * vmul;
+      const __half2 hh = __floats2half2_rn(a0, a1);
+      w[q] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    *reinterpret_cast<uint4*>(unit + 64 * D * 2 + dim * 128 + ((tg ^ (dim & 7)) << 4)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (threadIdx.x < 64) {  // e x log2(e) (the tiled attention works in base 2)
+    const int t = threadIdx.x;
+    reinterpret_cast<float*>(unit + 2 * 64 * D * 2)[t] =
+        (t < nt) ? e[((long long)b * L + t0 + t) * s.Hkv + h] * 1.4426950408889634f : 0.f;
+  }
+  if (nt < 64) return;  // an incomplete block is never a candidate
+  for (int i = threadIdx.x; i < 4 * D; i += blockDim.x) {
+    const int sb = i / D, dim = i % D;
+    float acc = 0.f;
+    for (int j = 0; j < 16; ++j) acc += __bfloat162float(k_s[(sb * 16 + j) * RS + dim]);
+    pk[(((long long)u * nblk + blk) * 4 + sb) * D + dim] = acc * (1.0f / 16);
+  }
+  if (threadIdx.x == 0) {
+    float best = 0.f;
+    for (int sb = 0; sb < 4; ++sb) {
+      float acc = 0.f;
+      for (int j = 0; j < 16; ++j) acc += e[((long long)b * L + t0 + sb * 16 + j) * s.Hkv + h];
+      const float m = acc * (1.0f / 16);
       best = (sb == 0) ? m : fmaxf(best, m);
     }
     se[(long long)u * nblk + blk] = best;
@@ -569,17 +623,21 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   dim3 grid(nblk, s.U);
   uint32_t* vmax = reinterpret_cast<uint32_t*>(ws + w.vmax);  // zeroed by the caller
   if (s.dtype == 0) {
-    prefill_pack_kernel<float, false><<<grid, kPackThreads, 0, stream>>>(
-        s, (const float*)k, (const float*)v, e, L, nblk, units, pk, se, nullptr);
+    prefill_pack_kernel<float><<<grid, kPackThreads, 0, stream>>>(
+        s, (const float*)k, (const float*)v, e, L, nblk, units, pk, se);
   } else if (tc) {
     const long long n = (long long)s.batch * L * s.Hkv * s.d;
     const int blocks = (int)std::min<long long>((n + 255) / 256, 4 * 152);
     prefill_vmax_kernel<<<blocks, 256, 0, stream>>>((const __nv_bfloat16*)v, n, vmax);
-    prefill_pack_kernel<__nv_bfloat16, true><<<grid, kPackThreads, 0, stream>>>(
-        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se, vmax);
+    if (s.d == 64)
+      prefill_pack_tc_kernel<64><<<grid, kPackThreads, 0, stream>>>(
+          s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se, vmax);
+    else
+      prefill_pack_tc_kernel<128><<<grid, kPackThreads, 0, stream>>>(
+          s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se, vmax);
   } else {
-    prefill_pack_kernel<__nv_bfloat16, false><<<grid, kPackThreads, 0, stream>>>(
-        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se, nullptr);
+    prefill_pack_kernel<__nv_bfloat16><<<grid, kPackThreads, 0, stream>>>(
+        s, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, e, L, nblk, units, pk, se);
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
