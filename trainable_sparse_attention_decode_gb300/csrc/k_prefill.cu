@@ -13,7 +13,7 @@
 // The path:
 //   prefill_pack_kernel    block units (the decode layout), pooled keys and block
 //                          eviction scores of every block            (unit, block)
-//   prefill_evict_kernel   the E_b recurrence, one warp per unit
+//   prefill_evict_kernel   the eviction sets E_b, one warp per block
 //   prefill_select_kernel  per position: pooled query scores of the candidates
 //                          outside E_b, top-(k - |E_b|) by warp arg-max; writes
 //                          the position's block table and tail     (unit, block)
@@ -190,68 +190,59 @@ __global__ void __launch_bounds__(kPackThreads) prefill_pack_tc_kernel(
 }
 
 // The eviction sets: for every block b with positions, E_b (ascending block ids)
-// into Eb[u][b][k_e] and its size into Ecnt[u][b]. One warp per unit; the set is
-// kept in shared memory in ascending order (a new candidate is always the
-// largest id); when it exceeds k_e the lowest score leaves (at equal scores the
-// higher id, so the lower index wins).
-__global__ void __launch_bounds__(128) prefill_evict_kernel(Shape s, const float* __restrict__ se,
+// into Eb[u][b][k_e] and its size into Ecnt[u][b]. The recurrence E_b =
+// top-k_e(E_{b-1} + {b-1}) (ties: the lower id stays) never brings an evicted block
+// back, and the smallest member only grows, so E_b is the top-k_e of the whole
+// prefix {0 .. b-1} in the order (score descending, id ascending): every block is
+// computed on its own. One warp per block b: the k_e-th largest order-preserving
+// score key by a bitwise threshold search over the prefix, then the members in
+// ascending id order (keys above the threshold, and keys equal to it by ascending
+// id until k_e). A NaN score ranks highest (the recurrence never removes one).
+// grid = (ceil(nblk / 8), U), 8 warps; the unit's keys staged in shared memory.
+__global__ void __launch_bounds__(256) prefill_evict_kernel(Shape s, const float* __restrict__ se,
                                                             int nblk, int32_t* __restrict__ Eb,
                                                             int32_t* __restrict__ Ecnt) {
-  extern __shared__ int32_t ev_ids[];  // [4 warps][k_e + 1]
+  extern __shared__ uint32_t ekeys[];  // [min(nblk, b0 + 8)]
+  const int u = blockIdx.y, b0 = blockIdx.x * 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u = blockIdx.x * 4 + warp;
-  if (u >= s.U) return;
-  int32_t* ids = ev_ids + warp * (s.ke + 1);
-  const float* seu = se + (long long)u * nblk;
-  int cnt = 0;
-  for (int b = 0; b < nblk; ++b) {
-    if (b >= 1 && s.ke > 0) {
-      if (lane == 0) ids[cnt] = b - 1;
-      __syncwarp();
-      ++cnt;
-      if (cnt > s.ke) {
-        // arg-min by (score, then larger id), over the cnt entries
-        float best = INFINITY;
-        int bpos = -1, bid = -1;
-        for (int i = lane; i < cnt; i += 32) {
-          const float x = seu[ids[i]];
-          if (x < best || (x == best && ids[i] > bid)) {
-            best = x;
-            bid = ids[i];
-            bpos = i;
-          }
-        }
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-          const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-          const int opos = __shfl_xor_sync(0xffffffffu, bpos, o);
-          if (ob < best || (ob == best && oid > bid)) {
-            best = ob;
-            bid = oid;
-            bpos = opos;
-          }
-        }
-        // remove position bpos (keeps the ascending order)
-        int32_t carry[9];
-        const int nchunk = (cnt + 31) / 32;
-        for (int c = 0; c < nchunk && c < 9; ++c) {
-          const int i = c * 32 + lane + 1;
-          carry[c] = (i < cnt) ? ids[i] : 0;
-        }
-        __syncwarp();
-        for (int c = 0; c < nchunk && c < 9; ++c) {
-          const int i = c * 32 + lane;  // destination of element i + 1
-          if (i + 1 < cnt && i >= bpos) ids[i] = carry[c];
-        }
-        __syncwarp();
-        --cnt;
-      }
-    }
-    int32_t* out = Eb + ((long long)u * nblk + b) * s.ke;
-    for (int i = lane; i < cnt; i += 32) out[i] = ids[i];
-    if (lane == 0) Ecnt[(long long)u * nblk + b] = cnt;
-    __syncwarp();
+  const int nk = min(nblk, b0 + 8);
+  for (int i = threadIdx.x; i < nk; i += blockDim.x) {
+    const float x = se[(long long)u * nblk + i];
+    ekeys[i] = (x != x) ? 0xffffffffu : ordered_key(x);
   }
+  __syncthreads();
+  const int b = b0 + warp;
+  if (b >= nblk) return;
+  const int n = b;  // candidates 0 .. b-1
+  int32_t* out = Eb + ((long long)u * nblk + b) * s.ke;
+  if (n <= s.ke) {
+    for (int i = lane; i < n; i += 32) out[i] = i;
+    if (lane == 0) Ecnt[(long long)u * nblk + b] = n;
+    return;
+  }
+  uint32_t thr = 0u;  // the largest key with at least k_e keys at or above it
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = thr | (1u << bit);
+    int c = 0;
+    for (int j = lane; j < n; j += 32) c += ekeys[j] >= cand ? 1 : 0;
+    if ((int)__reduce_add_sync(0xffffffffu, (uint32_t)c) >= s.ke) thr = cand;
+  }
+  int gt = 0;
+  for (int j = lane; j < n; j += 32) gt += ekeys[j] > thr ? 1 : 0;
+  const int need_eq = s.ke - (int)__reduce_add_sync(0xffffffffu, (uint32_t)gt);
+  int run = 0, eq_seen = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int j = base + lane;
+    const uint32_t kj = j < n ? ekeys[j] : 0u;
+    const bool eqj = j < n && kj == thr;
+    const unsigned beq = __ballot_sync(0xffffffffu, eqj);
+    const bool on = (j < n && kj > thr) || (eqj && eq_seen + __popc(beq & ((1u << lane) - 1u)) < need_eq);
+    const unsigned bal = __ballot_sync(0xffffffffu, on);
+    if (on) out[run + __popc(bal & ((1u << lane) - 1u))] = j;
+    run += __popc(bal);
+    eq_seen += __popc(beq);
+  }
+  if (lane == 0) Ecnt[(long long)u * nblk + b] = run;
 }
 
 // Loads 4 consecutive elements of q as fp32.
@@ -641,8 +632,7 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const size_t esmem = (size_t)4 * (s.ke + 1) * 4;
-  prefill_evict_kernel<<<(s.U + 3) / 4, 128, esmem, stream>>>(s, se, nblk, Eb, Ecnt);
+  prefill_evict_kernel<<<dim3((nblk + 7) / 8, s.U), 256, (size_t)nblk * 4, stream>>>(s, se, nblk, Eb, Ecnt);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = prefill_select_smem(s, nblk);
