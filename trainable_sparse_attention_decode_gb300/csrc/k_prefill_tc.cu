@@ -23,12 +23,13 @@
 //             scale of the call; N = d, K = 128).
 // Online softmax with a lazy reference: a row keeps its running max m until a
 // pair raises it by more than 8 (base 2), so P <= 2^8; only then is the row's O
-// rescaled in tensor memory. Two warps share a row quarter (tensor-memory lanes
-// 32 q ..), each owning one block of a pair: they exchange the row max through
-// shared memory (a named barrier per quarter), keep their own part of the row
-// sum l (fp32 probabilities, so the log-sum-exp is exact to fp32 rounding) and
-// rescale half of O each. Warp roles: warps 0-7 rows, warp 8 issues the MMAs,
-// warp 9 the bulk copies (two stages of a pair's K, two of its V^T and e; K rows
+// rescaled in tensor memory. Four warps share a row quarter (tensor-memory lanes
+// 32 q ..), each owning 32 tokens of one block of a pair: they exchange the row
+// max through shared memory (a bounded mbarrier meet per quarter), keep their own
+// part of the row sum l (fp32 probabilities, so the log-sum-exp is exact to fp32
+// rounding) and rescale a quarter of O each; a warp writes its P over the first 16
+// of its 32 S columns. Warp roles: warps 0-15 rows, warp 16 issues the MMAs,
+// warp 17 the bulk copies (two stages of a pair's K, two of its V^T and e; K rows
 // are interleaved at copy time, block a's 64 rows then block b's, per 64-wide
 // head-dim block, so that S is one N = 128 product; the K of pair j + 2 loads as
 // soon as S of pair j is done). Everything after the set-up is ordered by
@@ -59,7 +60,7 @@ namespace nosa {
 namespace {
 using namespace tc;
 
-constexpr int kRowWarps = 8;                         // 2 per tensor-memory lane quarter
+constexpr int kRowWarps = 16;                        // 4 per tensor-memory lane quarter
 constexpr int kTileThreads = 32 * (kRowWarps + 2);    // + the MMA warp and the copy warp
 constexpr int kPairStages = 2;
 constexpr float kLn2F = 0.6931471805599453f;
@@ -78,8 +79,8 @@ struct TileSmem {
   __host__ __device__ size_t qt() const { return 0; }                                 // [d/64][128 x 128 B] bf16
   __host__ __device__ size_t kst() const { return (size_t)256 * d; }                  // [kPairStages][pair_kstage]
   __host__ __device__ size_t vst() const { return kst() + kPairStages * pair_kstage(d); }  // [kPairStages][pair_vstage]
-  __host__ __device__ size_t mx() const { return vst() + kPairStages * pair_vstage(d); }   // [2][2][128] + [2][128] f32
-  __host__ __device__ size_t mask() const { return mx() + 3072; }                     // [nblk][2] u32
+  __host__ __device__ size_t mx() const { return vst() + kPairStages * pair_vstage(d); }   // [2][4][128] + [4][128] f32
+  __host__ __device__ size_t mask() const { return mx() + 6144; }                     // [nblk][2] u32
   __host__ __device__ size_t list() const { return mask() + 8 * (size_t)nblk; }       // [nblk] i32
   __host__ __device__ size_t total() const { return list() + 4 * (size_t)nblk + 1024; }
 };
@@ -97,8 +98,8 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 x = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&x);
 }
-// The two warps of a row quarter meet at `bar` (count 2, one arrival per warp
-// after its shared-memory writes); false if the partner did not come in time.
+// The four warps of a row quarter meet at `bar` (count 4, one arrival per warp
+// after its shared-memory writes); false if one did not come in time.
 __device__ __forceinline__ bool quarter_meet(uint64_t* bar, uint32_t parity, int lane) {
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
@@ -108,6 +109,7 @@ __device__ __forceinline__ bool quarter_meet(uint64_t* bar, uint32_t parity, int
 template <int D>
 __global__ void __launch_bounds__(kTileThreads, 1)
     prefill_tile_kernel(Shape s, PrefillTileArgs a) {
+  static_assert(kRowWarps == 16, "4 row warps per lane quarter");
   constexpr uint32_t KB = 64 * D * 2;  // bytes of a block's K (= of its V^T)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     mbar_init(&p_full, kRowWarps);
     mbar_init(&pv_done, 1);
     for (int q = 0; q < 4; ++q)
-      for (int k = 0; k < 3; ++k) mbar_init(&xch[q][k], 2);
+      for (int k = 0; k < 3; ++k) mbar_init(&xch[q][k], 4);
     fence_mbar_init();
     s_bad = 0;
   }
@@ -292,8 +294,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const int nb = min(2, cnt - 2 * j);
         const uint64_t dv = dvst + (uint64_t)((j % kPairStages) * vstride16);
         const uint32_t t_p = tmem + (uint32_t)((j & 1) * 128);
-        for (int kk = 0; kk < 4 * nb; ++kk)  // block kk / 4: P in its S columns 64 (kk / 4) ..
-          mma_tmem_a(tmem + o_col, t_p + (kk >> 2) * 64 + (kk & 3) * 8,
+        for (int kk = 0; kk < 4 * nb; ++kk)  // 16 tokens: block kk / 4, half (kk / 2) % 2 of it
+          mma_tmem_a(tmem + o_col, t_p + (kk >> 2) * 64 + ((kk >> 1) & 1) * 32 + (kk & 1) * 8,
                      dv + (uint64_t)((kk >> 2) * (pair_vslot(D) / 16)) + 2 * (kk & 3), idesc_pv,
                      (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done);
@@ -313,14 +315,15 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     }
   } else {
     // ======================= rows: softmax, P, O rescale ========================
-    const int q4 = warp & 3, hb = warp >> 2;  // lane quarter, block of the pair
+    // warp (q4, hb, hh): lane quarter q4, block hb of the pair, its token half hh
+    const int q4 = warp & 3, hb = (warp >> 2) & 1, hh = warp >> 3, wq = warp >> 2;  // wq: warp in the quarter
     const int rr = 32 * q4 + lane;
     const int p_loc = p_lo + rr / G;
     const bool row_valid = p_loc < p_hi;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    const uint32_t t_o = tmem + lane_off + o_col + (uint32_t)(hb * (D / 2));  // this warp's half of O
+    const uint32_t t_o = tmem + lane_off + o_col + (uint32_t)(wq * (D / 4));  // this warp's quarter of O
     const float qs = 1.4426950408889634f * a.inv_sqrt_d;
-    float m_run = -1e30f, l_run = 0.f;  // l: this warp's blocks only
+    float m_run = -1e30f, l_run = 0.f;  // l: this warp's tokens only
     bool ok = true;
     for (int j = 0; j < npair; ++j) {
       const int st = j % kPairStages;
@@ -334,21 +337,23 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       tc_fence_after();
       const int nb = min(2, cnt - 2 * j);
       const bool mine = hb < nb;  // (warp-uniform)
-      const uint32_t t_s = tmem + lane_off + (uint32_t)((j & 1) * 128 + hb * 64);
-      float x[64];
+      // this warp's 32 S columns (tokens 32 hh .. of block hb)
+      const uint32_t t_s = tmem + lane_off + (uint32_t)((j & 1) * 128 + hb * 64 + hh * 32);
+      float x[32];
       float mx = -INFINITY;
       if (mine) {
         const int jb = list_s[2 * j + hb];
         const uint32_t mb = row_valid ? mask_s[2 * jb + (p_loc >> 5)] : 0u;
-        const int lim = ((mb >> (p_loc & 31)) & 1u) ? ((jb == b) ? p_loc : s.B - 1) : -1;
-        uint32_t sr[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16_nowait(t_s + (uint32_t)c0, sr + c0);
+        // positions of the half this row attends: t < lim (token index inside the half)
+        const int lim = ((mb >> (p_loc & 31)) & 1u) ? ((jb == b) ? p_loc - 32 * hh : s.B) : -1;
+        uint32_t sr[32];
+        tmem_ld16_nowait(t_s, sr);
+        tmem_ld16_nowait(t_s + 16, sr + 16);
         tmem_wait_ld();
-        const float4* ev4 = reinterpret_cast<const float4*>(pvs + hb * pair_vslot(D) + KB);
-        if (__all_sync(0xffffffffu, lim == s.B - 1)) {
+        const float4* ev4 = reinterpret_cast<const float4*>(pvs + hb * pair_vslot(D) + KB) + 8 * hh;
+        if (__all_sync(0xffffffffu, lim >= 32)) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < 8; ++c) {
             const float4 e4 = ev4[c];
             x[4 * c + 0] = fmaf(__uint_as_float(sr[4 * c + 0]), qs, e4.x);
             x[4 * c + 1] = fmaf(__uint_as_float(sr[4 * c + 1]), qs, e4.y);
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < 8; ++c) {
             const float4 e4 = ev4[c];
             x[4 * c + 0] = 4 * c + 0 <= lim ? fmaf(__uint_as_float(sr[4 * c + 0]), qs, e4.x) : -INFINITY;
             x[4 * c + 1] = 4 * c + 1 <= lim ? fmaf(__uint_as_float(sr[4 * c + 1]), qs, e4.y) : -INFINITY;
@@ -367,7 +372,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int t = 4; t < 64; t += 4) {
+        for (int t = 4; t < 32; t += 4) {
           mx4[0] = fmaxf(mx4[0], x[t]);
           mx4[1] = fmaxf(mx4[1], x[t + 1]);
           mx4[2] = fmaxf(mx4[2], x[t + 2]);
@@ -375,31 +380,31 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       }
-      // the row's max over the pair: exchange with the other warp of the quarter
-      float* mxb = mx_s + (size_t)(j & 1) * 256;
-      mxb[hb * 128 + rr] = mx;
+      // the row's max over the pair: exchange among the 4 warps of the quarter
+      float* mxb = mx_s + (size_t)(j & 1) * 512;
+      mxb[wq * 128 + rr] = mx;
       if (!quarter_meet(&xch[q4][j & 1], (uint32_t)((j >> 1) & 1), lane)) {
         ok = false;
         break;
       }
-      const float mxp = fmaxf(mx, mxb[(hb ^ 1) * 128 + rr]);
+      const float mxp = fmaxf(fmaxf(mxb[rr], mxb[128 + rr]), fmaxf(mxb[256 + rr], mxb[384 + rr]));
       // lazy reference: move it (every row of the warp) only when a row's max
-      // rises by more than kRescale; both warps of the quarter decide alike
+      // rises by more than kRescale; the 4 warps of the quarter decide alike
       const bool grow = __any_sync(0xffffffffu, mxp > m_run + kRescale);
       const float m_use = grow ? fmaxf(m_run, mxp) : m_run;
       const float alpha = ex2(m_run - m_use);
       if (mine) {
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pw[32];
+        uint32_t pw[16];
 #pragma unroll
-        for (int t = 0; t < 64; t += 2) {
+        for (int t = 0; t < 32; t += 2) {
           const float p0 = ex2(x[t] - m_use), p1 = ex2(x[t + 1] - m_use);
           sum4[(t >> 1) & 3] += p0 + p1;
           pw[t >> 1] = pack_f16(p0, p1);
         }
         l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-        // P over the first 32 of this block's S columns (already in registers)
-        tmem_st32(t_s, pw);
+        // P over the first 16 of this warp's S columns (already in registers)
+        tmem_st16(t_s, reinterpret_cast<const float*>(pw));
       } else {
         l_run *= alpha;
       }
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       // P V of the previous pair done: O is settled. Every row warp observes every
       // phase of pv_done in order (a parity wait cannot tell a phase from the one
       // two later). A new reference scales O by alpha before P V of this pair adds
-      // to it (grow is warp-uniform; each warp of the quarter takes half of O).
+      // to it (grow is warp-uniform; each warp of the quarter takes a quarter of O).
       if (j > 0) {
         ok = mbar_wait_bounded(&pv_done, (uint32_t)((j - 1) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
@@ -417,7 +422,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         tc_fence_after();
         if (grow) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < D / 2; c0 += 16) {
+          for (int c0 = 0; c0 < D / 4; c0 += 16) {
             float v[16];
             tmem_ld16(t_o + c0, v);
 #pragma unroll
@@ -436,11 +441,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         atomicExch(a.err, kDevErrWaitTimeout);
       }
     }
-    // the row sum: the two warps' parts (same reference)
-    float* lsb = mx_s + 512;
-    lsb[hb * 128 + rr] = l_run;
+    // the row sum: the 4 warps' parts (same reference)
+    float* lsb = mx_s + 1024;
+    lsb[wq * 128 + rr] = l_run;
     if (ok && !quarter_meet(&xch[q4][2], 0u, lane)) ok = false;
-    const float l_tot = l_run + lsb[(hb ^ 1) * 128 + rr];
+    const float l_tot = (lsb[rr] + lsb[128 + rr]) + (lsb[256 + rr] + lsb[384 + rr]);
     if (ok && npair > 0 &&
         __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done, (uint32_t)((npair - 1) & 1)))) {
       tc_fence_after();
@@ -449,9 +454,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       const long long row = ((long long)req * a.L + t) * s.Hq + (long long)h * G + g;
       // O carries V's scale 2^vs
       const float inv = l_tot > 0.f ? ldexpf(1.f, -v_scale_exp(*a.vmax)) / l_tot : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + hb * (D / 2));
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D + wq * (D / 4));
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 16) {
+      for (int c0 = 0; c0 < D / 4; c0 += 16) {
         float v[16];
         tmem_ld16(t_o + c0, v);
         if (row_valid) {
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                          pack_bf16(v[12] * inv, v[13] * inv), pack_bf16(v[14] * inv, v[15] * inv));
         }
       }
-      if (row_valid && hb == 0 && a.lse) a.lse[row] = l_tot > 0.f ? (m_run + log2f(l_tot)) * kLn2F : -INFINITY;
+      if (row_valid && wq == 0 && a.lse) a.lse[row] = l_tot > 0.f ? (m_run + log2f(l_tot)) * kLn2F : -INFINITY;
     } else if (ok && npair > 0 && lane == 0) {
       s_bad = 1;
       atomicExch(a.err, kDevErrWaitTimeout);
