@@ -37,13 +37,19 @@ namespace {
 constexpr int kPackThreads = 256;
 constexpr int kSelWarps = 8;
 constexpr int kSelRegSlots = 16;  // top-m keys per lane held in registers
-constexpr int kSelCH = 8;         // candidates per pooled-key chunk in shared memory
+constexpr int kSelCC = 64;        // candidates per pooled-key chunk (two per lane)
+constexpr int kSelDS = 16;        // dims of a chunk per shared-memory slice
+constexpr int kSelNS = 3;         // slices in the cp.async ring
+constexpr int kSelCStr = 4 * kSelDS + 4;  // floats per candidate in a slice (272 bytes)
 
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Block units of the tiled tensor-core attention (bf16 inputs; k_prefill_tc.cu)
 // hold their operands in the canonical K-major layout with the 128-byte swizzle
@@ -254,42 +260,119 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
   return make_float4(a.x, a.y, c.x, c.y);
 }
 
-// Per position t of block b (CTA (b, u); warp w takes positions 64 b + w, + 8, ...,
+// Top-m of one position's scores by sorted per-lane lists: the NP = 32 / PB lanes
+// of position i (lane = i * NP + part) each keep the best MM entries of a
+// contiguous part of the candidate list, in the selection order (order-preserving
+// key descending, then list index ascending: lower block id first at equal
+// scores), then the position's m winners are drawn from the heads of its NP lists
+// by a shuffle tournament and marked in tk (one bit per block id). A NaN score is
+// never selected. Requires m <= MM.
+template <int MM, int PB>
+__device__ __forceinline__ void select_topm_lists(const float* sqw, int nblk, int ncl, int m,
+                                                  const int32_t* cl, uint32_t* taken, int W, int lane) {
+  constexpr int NP = 32 / PB;
+  const int i = lane / NP, part = lane % NP;
+  const int per = (ncl + NP - 1) / NP;
+  const int lo = min(ncl, part * per), hi = min(ncl, lo + per);
+  const float* sp = sqw + (size_t)i * nblk;
+  uint32_t key[MM];
+  int idx[MM];
+#pragma unroll
+  for (int r = 0; r < MM; ++r) {
+    key[r] = 0u;
+    idx[r] = 0x7fffffff;
+  }
+  for (int ci = lo; ci < hi; ++ci) {
+    const float x = sp[ci];
+    const uint32_t kx = x == x ? ordered_key(x) : 0u;
+    if (kx > key[MM - 1]) {
+      // insert at the first entry it beats (ci is above every index held, so
+      // an equal key stays behind); the entries below shift down by one
+      bool g[MM];
+#pragma unroll
+      for (int r = 0; r < MM; ++r) g[r] = kx > key[r];
+#pragma unroll
+      for (int r = MM - 1; r > 0; --r) {
+        key[r] = g[r] ? (g[r - 1] ? key[r - 1] : kx) : key[r];
+        idx[r] = g[r] ? (g[r - 1] ? idx[r - 1] : ci) : idx[r];
+      }
+      key[0] = g[0] ? kx : key[0];
+      idx[0] = g[0] ? ci : idx[0];
+    }
+  }
+  uint32_t* tk = taken + (size_t)i * W;
+  for (int round = 0; round < m; ++round) {
+    uint32_t bk = key[0];
+    int bi = idx[0];
+#pragma unroll
+    for (int o = 1; o < NP; o <<= 1) {
+      const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ok > bk || (ok == bk && oi < bi)) {
+        bk = ok;
+        bi = oi;
+      }
+    }
+    if (bk != 0u && idx[0] == bi) {  // the winning part pops its head and marks the block
+      // (bk == 0: nothing valid left; the rounds still run, as the shuffles span the warp)
+      const int j = cl[bi];
+      atomicOr(&tk[j >> 5], 1u << (j & 31));
+#pragma unroll
+      for (int r = 0; r < MM - 1; ++r) {
+        key[r] = key[r + 1];
+        idx[r] = idx[r + 1];
+      }
+      key[MM - 1] = 0u;
+      idx[MM - 1] = 0x7fffffff;
+    }
+  }
+}
+
+// Per position t of block b (CTA (u, b); warp w takes positions 64 b + w, + 8, ...,
 // PB of them at a time): q_bar = mean of the G query heads, sq(j) = max over
 // sub-blocks of q_bar . K_bar[j][s] / sqrt(d) for candidates j < b outside E_b,
-// then the top-(k - |E_b|) by repeated warp arg-max (ties: lower index). Writes
-// the position's selection (E_b ascending, then Gamma_q ascending, -1 pad) into
-// sel, its attention block table (unit indices) and tail.
-// Scoring: the CTA copies the pooled rows of 8 candidates at a time into a
-// double-buffered shared-memory chunk (cp.async, all threads), and every warp
-// scores its positions from it. Lane (r, c) = (lane / 8, lane % 8) holds sub-block
-// r's dims c*4 + 32v (v < D/32) of a row and the same dims of the PB positions'
-// q_bar, so one read of a row serves PB positions; the PB partial sums of the 8
-// lanes of a sub-block are reduced and transposed in 7 shuffles (lane c ends with
-// position c % PB), then the max over the 4 sub-blocks takes 2 more.
+// then the top-(k - |E_b|) (ties: lower block id). Writes the position's
+// selection (E_b ascending, then Gamma_q ascending, -1 pad) into sel, its
+// attention block table (unit indices) and tail.
+// Scoring: lane c of every warp owns candidates c and c + 32 of a chunk of 64 and
+// computes their 8 sub-block dot products with each of the warp's PB positions
+// (8 x PB accumulators, each a pair of fp32 partial sums over alternate dims,
+// paired FMAs): per 4 dims a lane reads 8 key rows and PB q_bar rows from shared
+// memory for 32 PB FMAs, which keeps the shared-memory reads under the FMA time.
+// The CTA streams each chunk through shared memory 16 dims at a time (cp.async
+// ring of kSelNS slices; a candidate's 4 x 16 floats at a 272-byte stride, so the
+// 8 lanes of a quarter warp read 8 different banks). Selection: sorted per-lane
+// lists (select_topm_lists) for all PB positions at once when m <= 32, else m
+// rounds of warp arg-max per position. Blocks run heaviest first (blockIdx.y
+// counts down from the last block): the scoring work of block b grows with b.
 template <typename T, int D, int PB>
-__global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
+__global__ void __launch_bounds__(kSelWarps * 32, PB >= 4 ? 1 : 2) prefill_select_kernel(
     Shape s, const T* __restrict__ q, int L, int nblk, const float* __restrict__ pk,
     const int32_t* __restrict__ Eb, const int32_t* __restrict__ Ecnt, int32_t* __restrict__ sel,
     int32_t* __restrict__ block_tab, int32_t* __restrict__ tail_tab, int32_t* __restrict__ tail_len,
     float inv_sqrt_d) {
-  constexpr int NV = D / 32;  // float4 per lane of a pooled row
+  constexpr int NDS = D / kSelDS;  // dim slices of a chunk
   extern __shared__ __align__(16) uint8_t sm[];
-  const int b = blockIdx.x, u = blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
+  const int u = blockIdx.x, b = nblk - 1 - (int)blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
   const int W = (nblk + 31) / 32;
-  uint32_t* emask = reinterpret_cast<uint32_t*>(sm);                          // [W] E_b membership
-  float* sq_s = reinterpret_cast<float*>(emask + ((W + 3) & ~3));              // [kSelWarps][PB][nblk]
-  uint32_t* taken_s = reinterpret_cast<uint32_t*>(sq_s + (size_t)kSelWarps * PB * nblk);  // [kSelWarps][W]
-  int32_t* cl = reinterpret_cast<int32_t*>(taken_s + kSelWarps * W);          // [nblk] candidates outside E_b
-  float* pk_s = reinterpret_cast<float*>(cl + ((nblk + 3) & ~3));             // [2][kSelCH][4][D]
+  float* stg = reinterpret_cast<float*>(sm);                                  // [kSelNS][64][kSelCStr]
+  float* qb_s = stg + kSelNS * kSelCC * kSelCStr;                              // [kSelWarps][PB][D]
+  float* sq_s = qb_s + kSelWarps * PB * D;                                     // [kSelWarps][PB][nblk]
+  uint32_t* emask = reinterpret_cast<uint32_t*>(sq_s + (size_t)kSelWarps * PB * nblk);  // [W] E_b membership
+  uint32_t* taken_s = emask + ((W + 3) & ~3);                                  // [kSelWarps][PB][W]
+  int32_t* cl = reinterpret_cast<int32_t*>(taken_s + kSelWarps * PB * W);     // [nblk] candidates outside E_b
+  int32_t* eb_s = cl + nblk;                                                   // [k_e] E_b ascending
   __shared__ int s_ncl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 3, c = lane & 7;
   const int ecnt = Ecnt[(long long)u * nblk + b];
   const int32_t* eb = Eb + ((long long)u * nblk + b) * s.ke;
   for (int i = threadIdx.x; i < W; i += blockDim.x) emask[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < ecnt; i += blockDim.x) atomicOr(&emask[eb[i] >> 5], 1u << (eb[i] & 31));
+  for (int i = threadIdx.x; i < ecnt; i += blockDim.x) {
+    const int j = eb[i];
+    eb_s[i] = j;
+    atomicOr(&emask[j >> 5], 1u << (j & 31));
+  }
   __syncthreads();
   const int n_cand = b;  // blocks before the positions' own block
   const int m = min(s.k - ecnt, n_cand - ecnt);
@@ -308,201 +391,204 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
   const int ncl = s_ncl;
   const int npos = min(s.B, L - b * s.B);
   float* sqw = sq_s + (size_t)warp * PB * nblk;
-  uint32_t* tk = taken_s + warp * W;
+  float* qw = qb_s + warp * PB * D;
+  uint32_t* tkw = taken_s + (size_t)warp * PB * W;
   const float inv_g = 1.0f / (float)s.G;
   const long long ubase = (long long)u * nblk;
   for (int g0 = 0; g0 < s.B / kSelWarps; g0 += PB) {
-    if (kSelWarps * g0 >= npos) break;  // (CTA-uniform: the chunk loop below syncs the CTA)
-    // q_bar of the batch's positions, this lane's dims
-    float4 qv[PB][NV];
+    if (kSelWarps * g0 >= npos) break;  // (CTA-uniform: the slice loop below syncs the CTA)
+    // q_bar of the batch's positions (fp32 sum over the heads in order, x 1/G)
+    if (lane < D / 4) {
+      float4 a[PB];
 #pragma unroll
-    for (int i = 0; i < PB; ++i) {
-      const int p = warp + kSelWarps * (g0 + i);
+      for (int i = 0; i < PB; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const T* qg = q + (((long long)req * L + (long long)b * s.B + warp + kSelWarps * g0) * s.Hq +
+                         (long long)h * s.G) * D + 4 * lane;
+      for (int g = 0; g < s.G; ++g)
 #pragma unroll
-      for (int v = 0; v < NV; ++v) qv[i][v] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (p < npos) {
-        const T* qg = q + (((long long)req * L + (long long)b * s.B + p) * s.Hq + (long long)h * s.G) * D;
-        for (int g = 0; g < s.G; ++g)
-#pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            const float4 x = load4(qg + g * D + c * 4 + 32 * v);
-            qv[i][v].x += x.x;
-            qv[i][v].y += x.y;
-            qv[i][v].z += x.z;
-            qv[i][v].w += x.w;
+        for (int i = 0; i < PB; ++i)
+          if (warp + kSelWarps * (g0 + i) < npos) {
+            const float4 x = load4(qg + ((long long)kSelWarps * i * s.Hq + g) * D);
+            a[i].x += x.x;
+            a[i].y += x.y;
+            a[i].z += x.z;
+            a[i].w += x.w;
           }
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          qv[i][v].x *= inv_g;
-          qv[i][v].y *= inv_g;
-          qv[i][v].z *= inv_g;
-          qv[i][v].w *= inv_g;
-        }
-      }
+      for (int i = 0; i < PB; ++i)
+        *reinterpret_cast<float4*>(qw + i * D + 4 * lane) =
+            make_float4(a[i].x * inv_g, a[i].y * inv_g, a[i].z * inv_g, a[i].w * inv_g);
     }
+    __syncwarp();
     if (m > 0) {
-      const int nch = (ncl + kSelCH - 1) / kSelCH;
-      auto load_chunk = [&](int ch) {
-        float* dst = pk_s + (size_t)(ch & 1) * kSelCH * 4 * D;
-        for (int i = threadIdx.x; i < kSelCH * D; i += blockDim.x) {  // float4 units: D per candidate
-          const int cc = i / D, f4 = i - cc * D, ci = ch * kSelCH + cc;
-          if (ci < ncl) cp_async16(dst + (size_t)cc * 4 * D + f4 * 4, pk + (ubase + cl[ci]) * s.P * D + f4 * 4);
+      const int nsl = (ncl + kSelCC - 1) / kSelCC * NDS;  // slices of this batch
+      auto load_slice = [&](int sl) {
+        if (sl < nsl) {
+          float* dst = stg + (sl % kSelNS) * kSelCC * kSelCStr;
+          const int ch = sl / NDS, ds = sl - ch * NDS;
+          for (int i = threadIdx.x; i < kSelCC * 4 * (kSelDS / 4); i += blockDim.x) {  // 16-byte pieces
+            const int c4 = i % (kSelDS / 4), r = (i / (kSelDS / 4)) & 3, cc = i / (kSelDS / 4) / 4;
+            const int ci = ch * kSelCC + cc;
+            if (ci < ncl)
+              cp_async16(dst + cc * kSelCStr + r * kSelDS + 4 * c4,
+                         pk + ((ubase + cl[ci]) * 4 + r) * D + ds * kSelDS + 4 * c4);
+          }
         }
-        cp_async_commit();
+        cp_async_commit();  // (empty groups keep the wait count below meaning "slice sl landed")
       };
-      load_chunk(0);
-      for (int ch = 0; ch < nch; ++ch) {
-        if (ch + 1 < nch)
-          load_chunk(ch + 1);
-        else
-          cp_async_commit();  // (an empty group keeps wait_group 1 meaning "chunk ch landed")
-        cp_async_wait1();
-        __syncthreads();
-        const float* chunk = pk_s + (size_t)(ch & 1) * kSelCH * 4 * D;
-        const int ncc = min(kSelCH, ncl - ch * kSelCH);
-        // two candidates per pass: independent chains for the FMA and shuffle latencies
-        for (int cc = 0; cc < ncc; cc += 2) {
-          const int nc2 = min(2, ncc - cc);
-          float acc[2][PB];
 #pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2) {
-            const float* row = chunk + ((size_t)(cc + (k2 < nc2 ? k2 : 0)) * 4 + r) * D + c * 4;
-            float4 x[NV];
+      for (int sl = 0; sl < kSelNS - 1; ++sl) load_slice(sl);
+      float2 acc[8][PB];  // [candidate half * 4 + sub-block][position]
 #pragma unroll
-            for (int v = 0; v < NV; ++v) x[v] = *reinterpret_cast<const float4*>(row + 32 * v);
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int i = 0; i < PB; ++i) acc[r][i] = make_float2(0.f, 0.f);
+      for (int sl = 0; sl < nsl; ++sl) {
+        cp_async_wait<kSelNS - 2>();
+        __syncthreads();  // slice sl visible to all; slice sl - 1's buffer is free
+        load_slice(sl + kSelNS - 1);
+        const int ch = sl / NDS, ds = sl - ch * NDS;
+        const float* kr = stg + (sl % kSelNS) * kSelCC * kSelCStr + lane * kSelCStr;
+        const float* qr = qw + ds * kSelDS;
+#pragma unroll
+        for (int d4 = 0; d4 < kSelDS / 4; ++d4) {
+          float4 kx[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            kx[r] = *reinterpret_cast<const float4*>(kr + (r >> 2) * 32 * kSelCStr + (r & 3) * kSelDS + 4 * d4);
+#pragma unroll
+          for (int i = 0; i < PB; ++i) {
+            const float4 qx = *reinterpret_cast<const float4*>(qr + i * D + 4 * d4);
+#pragma unroll
+            for (int r = 0; r < 8; ++r)  // (dims x, y of all 8 rows, then z, w: no back-to-back dependences)
+              acc[r][i] = __ffma2_rn(make_float2(kx[r].x, kx[r].y), make_float2(qx.x, qx.y), acc[r][i]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              acc[r][i] = __ffma2_rn(make_float2(kx[r].z, kx[r].w), make_float2(qx.z, qx.w), acc[r][i]);
+          }
+        }
+        if (ds == NDS - 1) {  // chunk done: the lane's two candidates' scores for the PB positions
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int ci = ch * kSelCC + 32 * c2 + lane;
 #pragma unroll
             for (int i = 0; i < PB; ++i) {
-              float a = 0.f;
-#pragma unroll
-              for (int v = 0; v < NV; ++v) {
-                a = fmaf(x[v].x, qv[i][v].x, a);
-                a = fmaf(x[v].y, qv[i][v].y, a);
-                a = fmaf(x[v].z, qv[i][v].z, a);
-                a = fmaf(x[v].w, qv[i][v].w, a);
-              }
-              acc[k2][i] = a;
+              const float sc = fmaxf(fmaxf(acc[4 * c2][i].x + acc[4 * c2][i].y,
+                                           acc[4 * c2 + 1][i].x + acc[4 * c2 + 1][i].y),
+                                     fmaxf(acc[4 * c2 + 2][i].x + acc[4 * c2 + 2][i].y,
+                                           acc[4 * c2 + 3][i].x + acc[4 * c2 + 3][i].y));
+              if (ci < ncl) sqw[(size_t)i * nblk + ci] = sc * inv_sqrt_d;
             }
           }
-          // sum over the 8 lanes of sub-block r, transposed: lane c keeps position c % PB
 #pragma unroll
-          for (int o = 4; o >= 1; o >>= 1) {
+          for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-              if (o >= PB) {
+            for (int i = 0; i < PB; ++i) acc[r][i] = make_float2(0.f, 0.f);
+        }
+      }
+      __syncthreads();  // the ring is refilled by the next batch
+    }
+    // top-m of every position of the batch
+    for (int w = lane; w < PB * W; w += 32) tkw[w] = 0u;
+    __syncwarp();
+    if (m > 0 && m <= 16) {
+      select_topm_lists<16, PB>(sqw, nblk, ncl, m, cl, tkw, W, lane);
+    } else if (m > 16 && m <= 32) {
+      select_topm_lists<32, PB>(sqw, nblk, ncl, m, cl, tkw, W, lane);
+    } else if (m > 0) {
+      for (int i = 0; i < PB; ++i) {
+        if (warp + kSelWarps * (g0 + i) >= npos) break;
+        const float* sqp = sqw + (size_t)i * nblk;
+        uint32_t* tk = tkw + (size_t)i * W;
+        // m rounds of warp arg-max over the candidates outside E_b (scores in
+        // list order, so a lower list index is a lower block id). Lane l owns
+        // list entries l + 32 s as order-preserving keys (0: taken, or a NaN
+        // score, never a candidate); a round takes the largest key, at equal
+        // keys the lowest index, and only the winning lane looks for its next
+        // best. Up to 512 entries the keys live in registers, beyond in shared
+        // memory.
+        if (ncl <= 32 * kSelRegSlots) {
+          uint32_t kr[kSelRegSlots];
 #pragma unroll
-                for (int i = 0; i < PB; ++i) acc[k2][i] += __shfl_xor_sync(0xffffffffu, acc[k2][i], o);
-              } else {
-                const bool hi = (lane & o) != 0;
+          for (int sl = 0; sl < kSelRegSlots; ++sl) {
+            const int ci = lane + 32 * sl;
+            const float x = ci < ncl ? sqp[ci] : 0.f;
+            kr[sl] = (ci < ncl && x == x) ? ordered_key(x) : 0u;
+          }
+          auto best_of = [&](uint32_t& key, int& slot) {
+            key = 0u;
+            slot = 0;
 #pragma unroll
-                for (int i = 0; i < o; ++i) {
-                  const float send = hi ? acc[k2][i] : acc[k2][i + o];
-                  const float keep = hi ? acc[k2][i + o] : acc[k2][i];
-                  acc[k2][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
+            for (int sl = 0; sl < kSelRegSlots; ++sl)
+              if (kr[sl] > key) {
+                key = kr[sl];
+                slot = sl;
               }
+          };
+          uint32_t lkey;
+          int lslot;
+          best_of(lkey, lslot);
+          for (int round = 0; round < m; ++round) {
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
+            if (kmax == 0u) break;  // none left (NaN scores)
+            const uint32_t win =
+                __reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)(lane + 32 * lslot) : 0xffffffffu);
+            if ((int)(win & 31) == lane) {
+              const int j = cl[win];
+              atomicOr(&tk[j >> 5], 1u << (j & 31));  // (winners of other rounds share words)
+#pragma unroll
+              for (int sl = 0; sl < kSelRegSlots; ++sl)
+                if (sl == lslot) kr[sl] = 0u;
+              best_of(lkey, lslot);
             }
           }
-          float sc0 = acc[0][0], sc1 = acc[1][0];
-          sc0 = fmaxf(sc0, __shfl_xor_sync(0xffffffffu, sc0, 8));
-          sc1 = fmaxf(sc1, __shfl_xor_sync(0xffffffffu, sc1, 8));
-          sc0 = fmaxf(sc0, __shfl_xor_sync(0xffffffffu, sc0, 16));
-          sc1 = fmaxf(sc1, __shfl_xor_sync(0xffffffffu, sc1, 16));
-          if (lane < PB) {
-            const int ci = ch * kSelCH + cc;
-            sqw[(size_t)lane * nblk + ci] = sc0 * inv_sqrt_d;
-            if (nc2 == 2) sqw[(size_t)lane * nblk + ci + 1] = sc1 * inv_sqrt_d;
+        } else {
+          auto lane_best = [&](uint32_t& key, int& idx) {
+            key = 0u;
+            idx = 0x7fffffff;
+            for (int ci = lane; ci < ncl; ci += 32) {
+              const int j = cl[ci];
+              if ((tk[j >> 5] >> (j & 31)) & 1u) continue;
+              const float x = sqp[ci];
+              if (x != x) continue;
+              const uint32_t kx = ordered_key(x);
+              if (kx > key) {  // ascending index: the first of equal keys stays
+                key = kx;
+                idx = ci;
+              }
+            }
+          };
+          uint32_t lkey;
+          int lidx;
+          lane_best(lkey, lidx);
+          for (int round = 0; round < m; ++round) {
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
+            if (kmax == 0u) break;
+            const int win = (int)__reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)lidx : 0xffffffffu);
+            if ((win & 31) == lane) {
+              const int j = cl[win];
+              tk[j >> 5] |= 1u << (j & 31);
+              lane_best(lkey, lidx);
+            }
+            __syncwarp();
           }
         }
-        __syncthreads();  // chunk buffer ch & 1 is refilled with chunk ch + 2 next
+        __syncwarp();
       }
-      __syncwarp();
     }
+    __syncwarp();
+    // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the mask)
     for (int i = 0; i < PB; ++i) {
       const int p = warp + kSelWarps * (g0 + i);
       if (p >= npos) break;
       const int t = b * s.B + p;
       const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
-      const float* sqp = sqw + (size_t)i * nblk;
-      for (int w = lane; w < W; w += 32) tk[w] = 0u;
-      __syncwarp();
-      // top-m: m rounds of warp arg-max over the candidates outside E_b (scores
-      // in list order, so a lower list index is a lower block id). Lane l owns
-      // list entries l + 32 s as order-preserving keys (0: taken, or a NaN score,
-      // never a candidate); a round takes the largest key, at equal keys the
-      // lowest index, and only the winning lane looks for its next best. Up to
-      // 512 entries the keys live in registers, beyond in shared memory.
-      if (m > 0 && ncl <= 32 * kSelRegSlots) {
-        uint32_t kr[kSelRegSlots];
-#pragma unroll
-        for (int sl = 0; sl < kSelRegSlots; ++sl) {
-          const int ci = lane + 32 * sl;
-          const float x = ci < ncl ? sqp[ci] : 0.f;
-          kr[sl] = (ci < ncl && x == x) ? ordered_key(x) : 0u;
-        }
-        auto best_of = [&](uint32_t& key, int& slot) {
-          key = 0u;
-          slot = 0;
-#pragma unroll
-          for (int sl = 0; sl < kSelRegSlots; ++sl)
-            if (kr[sl] > key) {
-              key = kr[sl];
-              slot = sl;
-            }
-        };
-        uint32_t lkey;
-        int lslot;
-        best_of(lkey, lslot);
-        for (int round = 0; round < m; ++round) {
-          const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
-          if (kmax == 0u) break;  // none left (NaN scores)
-          const uint32_t win = __reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)(lane + 32 * lslot) : 0xffffffffu);
-          if ((int)(win & 31) == lane) {
-            const int j = cl[win];
-            atomicOr(&tk[j >> 5], 1u << (j & 31));  // (winners of other rounds share words)
-#pragma unroll
-            for (int sl = 0; sl < kSelRegSlots; ++sl)
-              if (sl == lslot) kr[sl] = 0u;
-            best_of(lkey, lslot);
-          }
-        }
-        __syncwarp();
-      } else if (m > 0) {
-        auto lane_best = [&](uint32_t& key, int& idx) {
-          key = 0u;
-          idx = 0x7fffffff;
-          for (int ci = lane; ci < ncl; ci += 32) {
-            const int j = cl[ci];
-            if ((tk[j >> 5] >> (j & 31)) & 1u) continue;
-            const float x = sqp[ci];
-            if (x != x) continue;
-            const uint32_t kx = ordered_key(x);
-            if (kx > key) {  // ascending index: the first of equal keys stays
-              key = kx;
-              idx = ci;
-            }
-          }
-        };
-        uint32_t lkey;
-        int lidx;
-        lane_best(lkey, lidx);
-        for (int round = 0; round < m; ++round) {
-          const uint32_t kmax = __reduce_max_sync(0xffffffffu, lkey);
-          if (kmax == 0u) break;
-          const int win = (int)__reduce_min_sync(0xffffffffu, lkey == kmax ? (uint32_t)lidx : 0xffffffffu);
-          if ((win & 31) == lane) {
-            const int j = cl[win];
-            tk[j >> 5] |= 1u << (j & 31);
-            lane_best(lkey, lidx);
-          }
-          __syncwarp();
-        }
-      }
-      // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the mask)
+      const uint32_t* tk = tkw + (size_t)i * W;
       int32_t* selp = sel ? sel + vu * s.k : nullptr;
       int32_t* tab = block_tab + vu * s.k;
       for (int e = lane; e < ecnt; e += 32) {
-        if (selp) selp[e] = eb[e];
-        tab[e] = (int32_t)(ubase + eb[e]);
+        if (selp) selp[e] = eb_s[e];
+        tab[e] = (int32_t)(ubase + eb_s[e]);
       }
       int run = ecnt;
       if (m > 0)
@@ -525,16 +611,25 @@ __global__ void __launch_bounds__(kSelWarps * 32, 2) prefill_select_kernel(
         tail_tab[vu] = (int32_t)(ubase + b);
         tail_len[vu] = p + 1;
       }
-      __syncwarp();
     }
+    __syncwarp();
   }
 }
 
-// Positions scored per pooled-key load: as many (<= 4) as the score scratch
-// of 8 warps x PB x nblk floats allows within 80 KB (two CTAs per SM).
-int select_pb(int nblk) {
-  int pb = 4;  // (8 would hold 128 q_bar registers per thread: one CTA per SM)
-  while (pb > 1 && (size_t)kSelWarps * pb * nblk * 4 > 80 * 1024) pb >>= 1;
+// Dynamic shared memory of the selection: slice ring, q_bar, score scratch and
+// taken masks of 8 warps x PB positions, E_b mask, candidate list, E_b.
+size_t select_smem_bytes(int d, int ke, int nblk, int pb) {
+  const int W = (nblk + 31) / 32;
+  return (size_t)kSelNS * kSelCC * kSelCStr * 4 + (size_t)kSelWarps * pb * d * 4 +
+         (size_t)kSelWarps * pb * nblk * 4 + (size_t)((W + 3) & ~3) * 4 + (size_t)kSelWarps * pb * W * 4 +
+         (size_t)nblk * 4 + (size_t)std::max(ke, 1) * 4;
+}
+
+// Positions per warp scored in one pass over the candidates: the most (<= 8,
+// all of a warp's positions) whose score scratch fits in 220 KB.
+int select_pb(int d, int ke, int nblk) {
+  int pb = 8;
+  while (pb > 1 && select_smem_bytes(d, ke, nblk, pb) > 220 * 1024) pb >>= 1;
   return pb;
 }
 
@@ -555,6 +650,7 @@ cudaError_t launch_select_d(const Shape& s, dim3 grid, size_t smem, int pb, cons
                             const float* pk, const int32_t* Eb, const int32_t* Ecnt, int32_t* sel,
                             int32_t* tab, int32_t* ttab, int32_t* tlen, float isd, cudaStream_t stream) {
   switch (pb) {
+    case 8: return launch_select_pb<T, D, 8>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
     case 4: return launch_select_pb<T, D, 4>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
     case 2: return launch_select_pb<T, D, 2>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
     default: return launch_select_pb<T, D, 1>(s, grid, smem, q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab, tlen, isd, stream);
@@ -597,9 +693,7 @@ PrefillLayout prefill_layout(const Shape& s, int L, int nsplit) {
 }
 
 size_t prefill_select_smem(const Shape& s, int nblk) {
-  const int W = (nblk + 31) / 32;
-  return (size_t)((W + 3) & ~3) * 4 + (size_t)kSelWarps * select_pb(nblk) * nblk * 4 +
-         (size_t)kSelWarps * W * 4 + (size_t)((nblk + 3) & ~3) * 4 + (size_t)2 * kSelCH * 4 * s.d * 4;
+  return select_smem_bytes(s.d, s.ke, nblk, select_pb(s.d, s.ke, nblk));
 }
 
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
@@ -636,15 +730,16 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = prefill_select_smem(s, nblk);
-  const int pb = select_pb(nblk);
+  const int pb = select_pb(s.d, s.ke, nblk);
+  const dim3 sgrid(s.U, nblk);  // (unit, block counted down from the last)
   const float isd = (float)(1.0 / sqrt((double)s.d));
   int32_t* tab = reinterpret_cast<int32_t*>(ws + w.tab);
   int32_t* ttab = reinterpret_cast<int32_t*>(ws + w.tail_tab);
   int32_t* tlen = reinterpret_cast<int32_t*>(ws + w.tail_len);
   if (s.dtype == 0)
-    return launch_select<float>(s, grid, smem, pb, (const float*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab,
+    return launch_select<float>(s, sgrid, smem, pb, (const float*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab,
                                 tlen, isd, stream);
-  return launch_select<__nv_bfloat16>(s, grid, smem, pb, (const __nv_bfloat16*)q, L, nblk, pk, Eb, Ecnt,
+  return launch_select<__nv_bfloat16>(s, sgrid, smem, pb, (const __nv_bfloat16*)q, L, nblk, pk, Eb, Ecnt,
                                       sel, tab, ttab, tlen, isd, stream);
 }
 
