@@ -109,6 +109,14 @@ def test_query_only_and_eviction_only(k_e):
     _prefill(w, 64 * 30 + 11)
 
 
+@pytest.mark.parametrize("k,k_e", [(40, 16), (48, 8)])
+def test_selection_widths(k, k_e):
+    # Gamma_q of up to 24 blocks (the 32-entry per-lane lists of the selection)
+    # and of up to 37 (beyond 32: the warp arg-max rounds)
+    w = synth.WORKLOADS["tiny-f32"].with_(k=k, k_e=k_e)
+    _prefill(w, 64 * 45 + 7)
+
+
 @pytest.mark.parametrize("tiled", [True, False])
 def test_1b_shape_sampled_units(tiled):
     # G = 2, d = 64: one 128-row tile per query block
@@ -198,9 +206,11 @@ def test_phase_timing(tiled):
 
 
 @pytest.mark.slow
-def test_long_sequence_fallback_paths():
-    # 700 blocks: up to 695 candidates outside E_b (the top-m keys no longer fit
-    # the registers: the shared-memory rounds) and more than 640 blocks (two
-    # positions per pooled-key pass); the tiled attention with 700-block unions
-    w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=64, k=16, k_e=4)
+@pytest.mark.parametrize("k", [16, 40])
+def test_long_sequence_fallback_paths(k):
+    # 700 blocks: the score scratch of 8 positions per warp no longer fits (4 per
+    # pooled-key pass), up to 695 candidates outside E_b; with k = 40, Gamma_q of
+    # up to 36 blocks beyond 512 candidates (the arg-max rounds over keys in
+    # shared memory); the tiled attention with 700-block unions
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=64, k=k, k_e=4)
     _prefill(w, 64 * 700 + 13, attn_every=97)

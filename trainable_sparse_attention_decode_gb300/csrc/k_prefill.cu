@@ -15,8 +15,9 @@
 //                          eviction scores of every block            (unit, block)
 //   prefill_evict_kernel   the eviction sets E_b, one warp per block
 //   prefill_select_kernel  per position: pooled query scores of the candidates
-//                          outside E_b, top-(k - |E_b|) by warp arg-max; writes
-//                          the position's block table and tail     (unit, block)
+//                          outside E_b, top-(k - |E_b|) by sorted per-lane lists
+//                          (or warp arg-max rounds beyond 32); writes the
+//                          position's block table and tail         (unit, block)
 //   prefill_tile_kernel    (bf16, G <= 4, d in {64, 128}; k_prefill_tc.cu) the
 //                          attention of a whole query block on the tensor cores,
 //                          over the union of its positions' blocks;
