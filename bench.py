@@ -178,15 +178,17 @@ def kernel_source_hash(files):
 
 ATTN_SOURCES = ["trainable_sparse_attention_decode_gb300/csrc/k_attn.cuh",
                 "trainable_sparse_attention_decode_gb300/csrc/k_attn_bf16.cu"]
+TILE_SOURCES = ["trainable_sparse_attention_decode_gb300/csrc/k_prefill_tc.cu",
+                "trainable_sparse_attention_decode_gb300/csrc/tcgen05.cuh"]
 
 
-def ncu_traffic(workload_name):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary,
-    or None when the summary is missing or the kernel source changed since."""
-    p = os.path.join(ROOT, "profiles", f"attn_streamk_kernel_{workload_name}.md")
+def ncu_traffic(workload_name, kernel="attn_streamk_kernel", sources=None):
+    """Per-launch DRAM bytes of a kernel from its committed ncu summary, or None when
+    the summary is missing or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
     if not os.path.exists(p):
         return None
-    src_hash = kernel_source_hash(ATTN_SOURCES)
+    src_hash = kernel_source_hash(sources or ATTN_SOURCES)
     vals = {}
     with open(p) as f:
         for line in f:
@@ -365,7 +367,13 @@ def run_prefill(args, rank, world, local_rank):
         ach = flops / attn_s / 1e12
         roof = {"bound": "tensor", "kernel": "prefill_tile_kernel (tcgen05 attention per query block)",
                 "achieved": round(ach, 1), "peak": peak_t, "unit": "TFLOP/s",
-                "frac": round(ach / peak_t, 4), "traffic": None, "peak_source": kind,
+                "frac": round(ach / peak_t, 4),
+                # DRAM bytes of one launch from the committed capture of this
+                # sequence length (the union of a block's selections, and so the
+                # traffic, does not scale with L)
+                "traffic": ncu_traffic(f"8b-L{L}", "prefill_tile_kernel", TILE_SOURCES)
+                if w.name == "8b-offload-bf16" and w.batch == 1 else None,
+                "peak_source": kind,
                 "algorithmic_flops_per_launch": flops,
                 "kernel_ms": round(attn_s * 1e3, 4)}
     else:
