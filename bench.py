@@ -385,7 +385,10 @@ def run_prefill(args, rank, world, local_rank):
                 "frac": round(gbs / peak, 4), "traffic": None, "peak_source": kind,
                 "algorithmic_bytes_per_launch": attn_bytes, "kernel_ms": round(attn_s * 1e3, 4),
                 "note": "bytes gathered per position (mostly served by L2)"}
-    launches = 5 if tiled else 3 + -(-w.batch * L * w.n_kv_heads // 65535)
+    # the selection on the tensor cores adds the key-split launch
+    select_tc = (w.head_dim in (64, 128) and w.k - w.k_e <= 32
+                 and os.environ.get("NOSA_PREFILL_SELECT_TC", "1") != "0")
+    launches = (5 if tiled else 3 + -(-w.batch * L * w.n_kv_heads // 65535)) + (1 if select_tc else 0)
     return {"metric": "training-time forward tokens/s per layer (causal dual selection + "
                       "block-sparse attention)",
             "value": round(tokens / max_secs, 3), "unit": "tokens/s", "n_gpus": world,
@@ -395,7 +398,9 @@ def run_prefill(args, rank, world, local_rank):
             "config": {"workload": w.name + f"-prefill-L{L}", "batch": w.batch, "seq_len": L,
                        "k": w.k, "k_e": w.k_e, "n_q_heads": w.n_q_heads,
                        "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
-                       "attention": "tiled tensor-core" if tiled else "split-K per position"},
+                       "attention": "tiled tensor-core" if tiled else "split-K per position",
+                       "selection": "tensor-core (fp32 operands split in 3 bf16 terms)" if select_tc
+                       else "CUDA-core fp32"},
             "roofline": roof,
             "phase_ms": {"front": round(sum(front_ms) / len(front_ms), 4),
                          "attention": round(attn_s * 1e3, 4)},

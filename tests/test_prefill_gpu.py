@@ -20,23 +20,27 @@ from oracle import nosa_oracle as O
 pytestmark = pytest.mark.gpu
 
 
-def _forward(cfg, L, q, k, v, e, out, lse, sel, tiled):
-    """One forward with the tiled tensor-core attention on or off (the switch is
-    read at every call); checks the device error word."""
-    old = os.environ.get("NOSA_PREFILL_TILED")
-    os.environ["NOSA_PREFILL_TILED"] = "1" if tiled else "0"
+def _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc=True):
+    """One forward with the tiled tensor-core attention and the tensor-core
+    selection on or off (the switches are read at every call); checks the device
+    error word."""
+    switches = {"NOSA_PREFILL_TILED": "1" if tiled else "0",
+                "NOSA_PREFILL_SELECT_TC": "1" if select_tc else "0"}
+    old = {name: os.environ.get(name) for name in switches}
+    os.environ.update(switches)
     try:
         ws = nosa.nosa_prefill_forward(cfg, q, k, v, e, out, lse, sel)
         assert nosa.nosa_prefill_device_error(cfg, L, ws) == 0
     finally:
-        if old is None:
-            del os.environ["NOSA_PREFILL_TILED"]
-        else:
-            os.environ["NOSA_PREFILL_TILED"] = old
+        for name, value in old.items():
+            if value is None:
+                del os.environ[name]
+            else:
+                os.environ[name] = value
     torch.cuda.synchronize()
 
 
-def _prefill(w, L, units=None, attn_every=1, tiled=True):
+def _prefill(w, L, units=None, attn_every=1, tiled=True, select_tc=True):
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
                            max(L, 1))
     k, v, e = synth.gpu.kv(w, 0, L)
@@ -44,7 +48,7 @@ def _prefill(w, L, units=None, attn_every=1, tiled=True):
     out = torch.full_like(q, float("nan"))
     lse = torch.full((w.batch, L, w.n_q_heads), float("nan"), dtype=torch.float32, device="cuda")
     sel = torch.empty((w.batch, L, w.n_kv_heads, w.k), dtype=torch.int32, device="cuda")
-    _forward(cfg, L, q, k, v, e, out, lse, sel, tiled)
+    _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc)
     assert not torch.isnan(out.float()).any(), "an output row was not written"
     assert not torch.isnan(lse).any(), "an lse entry was not written"
     sel_h = sel.cpu().numpy()
@@ -103,18 +107,26 @@ def test_short_sequences(L):
     _prefill(synth.WORKLOADS["tiny-f32"], L)
 
 
+@pytest.mark.parametrize("select_tc", [True, False])
 @pytest.mark.parametrize("k_e", [0, 8])
-def test_query_only_and_eviction_only(k_e):
+def test_query_only_and_eviction_only(k_e, select_tc):
     w = synth.WORKLOADS["tiny-f32"].with_(k_e=k_e)
-    _prefill(w, 64 * 30 + 11)
+    _prefill(w, 64 * 30 + 11, select_tc=select_tc)
 
 
-@pytest.mark.parametrize("k,k_e", [(40, 16), (48, 8)])
-def test_selection_widths(k, k_e):
-    # Gamma_q of up to 24 blocks (the 32-entry per-lane lists of the selection)
-    # and of up to 37 (beyond 32: the warp arg-max rounds)
+@pytest.mark.parametrize("k,k_e,select_tc", [(40, 16, True), (40, 16, False), (48, 8, True)])
+def test_selection_widths(k, k_e, select_tc):
+    # Gamma_q of up to 24 blocks (32-entry lists: the tensor-core selection's per
+    # position, the CUDA-core selection's per lane) and of up to 37 (beyond 32:
+    # the CUDA-core selection's warp arg-max rounds, whatever the switch says)
     w = synth.WORKLOADS["tiny-f32"].with_(k=k, k_e=k_e)
-    _prefill(w, 64 * 45 + 7)
+    _prefill(w, 64 * 45 + 7, select_tc=select_tc)
+
+
+def test_8b_shape_cuda_core_selection():
+    # the CUDA-core selection (NOSA_PREFILL_SELECT_TC=0) at the 8B shape
+    w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=1)
+    _prefill(w, 4096 + 128 + 5, units=[0, 5], attn_every=11, select_tc=False)
 
 
 @pytest.mark.parametrize("tiled", [True, False])
@@ -206,11 +218,12 @@ def test_phase_timing(tiled):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("k", [16, 40])
-def test_long_sequence_fallback_paths(k):
-    # 700 blocks: the score scratch of 8 positions per warp no longer fits (4 per
-    # pooled-key pass), up to 695 candidates outside E_b; with k = 40, Gamma_q of
-    # up to 36 blocks beyond 512 candidates (the arg-max rounds over keys in
+@pytest.mark.parametrize("k,select_tc", [(16, True), (16, False), (40, True)])
+def test_long_sequence_fallback_paths(k, select_tc):
+    # 700 blocks, up to 695 candidates outside E_b: 22 chunks of the tensor-core
+    # selection; on the CUDA-core selection the score scratch of 8 positions per
+    # warp no longer fits (4 per pooled-key pass); with k = 40, Gamma_q of up to 36
+    # blocks beyond 512 candidates (the CUDA-core arg-max rounds over keys in
     # shared memory); the tiled attention with 700-block unions
     w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=64, k=k, k_e=4)
-    _prefill(w, 64 * 700 + 13, attn_every=97)
+    _prefill(w, 64 * 700 + 13, attn_every=97, select_tc=select_tc)

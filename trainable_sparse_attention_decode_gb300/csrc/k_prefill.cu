@@ -678,6 +678,7 @@ PrefillLayout prefill_layout(const Shape& s, int L, int nsplit) {
   size_t off = 0;
   w.units = off;     off += up(U * nblk * (size_t)s.payload);
   w.pk = off;        off += up(U * nblk * s.P * s.d * 4);
+  w.pk3 = off;       off += up(prefill_keysplit_bytes(s, nblk));
   w.se = off;        off += up(U * nblk * 4);
   w.eb = off;        off += up(U * nblk * (size_t)std::max(s.ke, 1) * 4);
   w.ecnt = off;      off += up(U * nblk * 4);
@@ -730,13 +731,16 @@ cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const voi
   prefill_evict_kernel<<<dim3((nblk + 7) / 8, s.U), 256, (size_t)nblk * 4, stream>>>(s, se, nblk, Eb, Ecnt);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  int32_t* tab = reinterpret_cast<int32_t*>(ws + w.tab);
+  int32_t* ttab = reinterpret_cast<int32_t*>(ws + w.tail_tab);
+  int32_t* tlen = reinterpret_cast<int32_t*>(ws + w.tail_len);
+  if (prefill_select_tc_ok(s, L))
+    return launch_prefill_select_tc(s, L, q, pk, ws + w.pk3, Eb, Ecnt, sel, tab, ttab, tlen,
+                                    reinterpret_cast<int*>(ws + w.err), stream);
   const size_t smem = prefill_select_smem(s, nblk);
   const int pb = select_pb(s.d, s.ke, nblk);
   const dim3 sgrid(s.U, nblk);  // (unit, block counted down from the last)
   const float isd = (float)(1.0 / sqrt((double)s.d));
-  int32_t* tab = reinterpret_cast<int32_t*>(ws + w.tab);
-  int32_t* ttab = reinterpret_cast<int32_t*>(ws + w.tail_tab);
-  int32_t* tlen = reinterpret_cast<int32_t*>(ws + w.tail_len);
   if (s.dtype == 0)
     return launch_select<float>(s, sgrid, smem, pb, (const float*)q, L, nblk, pk, Eb, Ecnt, sel, tab, ttab,
                                 tlen, isd, stream);

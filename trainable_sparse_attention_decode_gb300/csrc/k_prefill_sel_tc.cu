@@ -1,0 +1,525 @@
+// Training-time forward: the per-position selection with the pooled query scores
+// on the tensor cores.
+//
+// NOSA technical summary, Methodology §1: at every query position t the query-aware
+// part of the selection is the top-(k - |Gamma_e|) of the candidates outside
+// Gamma_e by the two-stage pooled score sq(j) = max over sub-blocks s of
+// q_bar(t) . K_bar[j][s] / sqrt(d). For the 64 positions of block b (which share
+// E_b and the candidate list) the scores are one product Q_bar K_bar^T: 64
+// positions x (4 sub-block rows per candidate) x d.
+//
+// The cut is decided in fp32 and the scores must keep fp32 accuracy, so each fp32
+// operand x is split into three bf16 terms x1 + x2 + x3 (x1 = bf16(x), x2 =
+// bf16(x - x1), x3 = bf16(x - x1 - x2): 24 significant bits, the split error at
+// most about 2^-24 |x|) and the product is the six-term sum
+//   a1 b1 + a1 b2 + a2 b1 + a1 b3 + a2 b2 + a3 b1
+// (the three terms left out are below 2^-24 |a b|), accumulated in fp32 in tensor
+// memory: the error of a score is that of an fp32 dot product. Non-finite inputs
+// keep x1 = x and zero tails.
+//
+// prefill_keysplit_kernel  the three bf16 planes of every block's pooled keys, as
+//                          two 128-byte-swizzled images (for an even and an odd
+//                          slot of a chunk), so that one bulk copy of 512 bytes
+//                          per plane and 64 dims lands a candidate's 4 rows
+//                          in place                                  (block, unit)
+// prefill_select_tc_kernel one CTA per (unit, block), heaviest blocks first:
+//   A     q_bar of the 64 positions, split in 3 planes, 128-byte-swizzled K-major
+//         tiles of 64 rows (M = 128: rows 64-127 of a tile read the next tile or a
+//         zero pad; their results are never read);
+//   B     chunks of 32 candidates (N = 128 rows: candidate c, sub-block s at row
+//         4 c + s), 64 dims per stage, a ring of 3 stages filled by bulk copies
+//         (copy warp) from the candidates' images;
+//   MMA   per stage 4 K16 steps x 6 terms (tcgen05.mma kind::f16, bf16 in, fp32
+//         accumulator), a chunk into one of two 128-column tensor-memory buffers;
+//   rows  4 epilogue warps (position = tensor-memory lane; two warps per lane
+//         quarter, one per half of a chunk's columns): the max over each
+//         candidate's 4 columns times 1/sqrt(d) goes into the warp's sorted
+//         register list of the best m (key descending, list index ascending:
+//         lower block id first at equal scores; a NaN score never enters); the
+//         two halves' lists are merged at the end, the winners marked, and the
+//         position's selection written in ascending block order.
+// Barriers: full / empty [stage] (copies landed / MMAs read the stage), mma_done
+// [buffer] (a chunk's scores are in), tmem_free [buffer] (the epilogue warps read
+// them). Every wait is bounded; one that gives up sets the error word, and the CTA
+// waits (bounded) for its copies and MMAs in flight, writes nothing and frees its
+// tensor memory.
+#include "nosa_internal.cuh"
+#include "tcgen05.cuh"
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+namespace nosa {
+namespace {
+using namespace tc;
+
+constexpr int kStThreads = 256;                      // 8 warps
+constexpr int kStCC = 32;                            // candidates per chunk (N = 128)
+constexpr int kStStages = 3;                         // ring of 64-dim stages
+constexpr uint32_t kStPlane = 16384;                 // one plane of a stage: 128 rows x 128 B
+constexpr uint32_t kStStage = 3 * kStPlane;          // the three planes
+constexpr int kStTmemCols = 256;                     // two 128-column score buffers
+constexpr int kMmaWarp = 2, kCopyWarp = 3;           // epilogue: warps 0, 1, 4, 5
+// the six (A plane, B plane) products kept
+__constant__ int kTermA[6] = {0, 0, 1, 0, 1, 2};
+__constant__ int kTermB[6] = {0, 1, 0, 2, 1, 0};
+
+__host__ __device__ constexpr uint32_t image_bytes(int d) { return 3u * (uint32_t)(d / 64) * 512u; }
+
+__device__ __forceinline__ void split3(float x, uint16_t& h1, uint16_t& h2, uint16_t& h3) {
+  const __nv_bfloat16 b1 = __float2bfloat16_rn(x);
+  const bool fin = isfinite(x);
+  const float r1 = fin ? x - __bfloat162float(b1) : 0.f;  // exact in fp32
+  const __nv_bfloat16 b2 = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(b2);              // exact in fp32
+  const __nv_bfloat16 b3 = __float2bfloat16_rn(r2);
+  h1 = __bfloat16_as_ushort(b1);
+  h2 = __bfloat16_as_ushort(b2);
+  h3 = __bfloat16_as_ushort(b3);
+}
+
+// 8 consecutive fp32 values -> their three bf16 planes (16 bytes each).
+__device__ __forceinline__ void split8(const float* x, uint4* v) {
+  uint16_t h[3][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) split3(x[i], h[0][i], h[1][i], h[2][i]);
+#pragma unroll
+  for (int p = 0; p < 3; ++p)
+    v[p] = make_uint4((uint32_t)h[p][0] | ((uint32_t)h[p][1] << 16), (uint32_t)h[p][2] | ((uint32_t)h[p][3] << 16),
+                      (uint32_t)h[p][4] | ((uint32_t)h[p][5] << 16), (uint32_t)h[p][6] | ((uint32_t)h[p][7] << 16));
+}
+
+__device__ __forceinline__ void load8(const float* p, float* x) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* x) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Images of block (u, j): [parity][plane][64-dim atom][row s][128 B], the 16-byte
+// chunk c (dims 64 atom + 8 c ..) of row s at chunk c ^ (4 parity + s): the rows
+// 4 parity + s of an 8-row group of the 128-byte swizzle. grid (nblk, U), 4 d / 8
+// threads.
+template <int D>
+__global__ void __launch_bounds__(4 * D / 8) prefill_keysplit_kernel(const float* __restrict__ pk, int nblk,
+                                                                     uint8_t* __restrict__ pk3) {
+  constexpr int NA = D / 64;
+  const long long blk = (long long)blockIdx.y * nblk + blockIdx.x;
+  const int s = threadIdx.x / (D / 8), cg = threadIdx.x % (D / 8), a = cg / 8, c = cg % 8;
+  float x[8];
+  load8(pk + (blk * 4 + s) * D + 8 * cg, x);
+  uint4 v[3];
+  split8(x, v);
+  uint8_t* img = pk3 + blk * 2 * image_bytes(D);
+#pragma unroll
+  for (int par = 0; par < 2; ++par)
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+      *reinterpret_cast<uint4*>(img + par * image_bytes(D) + (p * NA + a) * 512 + s * 128 +
+                                ((c ^ (4 * par + s)) << 4)) = v[p];
+}
+
+// Inserts (kx, ix) into a list sorted by (key descending, index ascending) when it
+// ranks above the last entry; entries below the insertion point move down one.
+template <int MM>
+__device__ __forceinline__ void list_insert(uint32_t (&key)[MM], int (&idx)[MM], uint32_t kx, int ix) {
+  bool g[MM];
+#pragma unroll
+  for (int r = 0; r < MM; ++r) g[r] = kx > key[r] || (kx == key[r] && ix < idx[r]);
+#pragma unroll
+  for (int r = MM - 1; r > 0; --r) {
+    key[r] = g[r] ? (g[r - 1] ? key[r - 1] : kx) : key[r];
+    idx[r] = g[r] ? (g[r - 1] ? idx[r - 1] : ix) : idx[r];
+  }
+  key[0] = g[0] ? kx : key[0];
+  idx[0] = g[0] ? ix : idx[0];
+}
+
+// Shared-memory carve-up (offsets from a 1024-byte aligned base).
+struct SelTcSmem {
+  int d, nblk, ke;
+  __host__ __device__ size_t a() const { return 0; }                                   // [3][d/64] 8 KB tiles + 8 KB zeros
+  __host__ __device__ size_t stg() const { return (size_t)(3 * (d / 64) + 1) * 8192; }  // [kStStages][kStStage]
+  __host__ __device__ size_t emask() const { return stg() + (size_t)kStStages * kStStage; }
+  __host__ __device__ size_t cl() const { return emask() + 4 * (size_t)(((nblk + 31) / 32 + 3) & ~3); }
+  __host__ __device__ size_t eb() const { return cl() + 4 * (size_t)nblk; }
+  __host__ __device__ size_t total() const { return eb() + 4 * (size_t)std::max(ke, 1) + 1024; }
+};
+
+template <typename T, int D, int MM>
+__global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
+    Shape s, const T* __restrict__ q, int L, int nblk, const uint8_t* __restrict__ pk3,
+    const int32_t* __restrict__ Eb, const int32_t* __restrict__ Ecnt, int32_t* __restrict__ sel,
+    int32_t* __restrict__ block_tab, int32_t* __restrict__ tail_tab, int32_t* __restrict__ tail_len,
+    int* __restrict__ err, float inv_sqrt_d) {
+  constexpr int NA = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SelTcSmem Lay{D, nblk, s.ke};
+  uint8_t* At = sm + Lay.a();
+  uint8_t* stg = sm + Lay.stg();
+  uint32_t* emask = reinterpret_cast<uint32_t*>(sm + Lay.emask());
+  int32_t* cl = reinterpret_cast<int32_t*>(sm + Lay.cl());
+  int32_t* eb_s = reinterpret_cast<int32_t*>(sm + Lay.eb());
+  // after the scoring the ring holds the second half's lists and the marks
+  uint32_t* lk = reinterpret_cast<uint32_t*>(stg);                 // [64][MM] keys
+  int32_t* li = reinterpret_cast<int32_t*>(stg + 64 * MM * 4);     // [64][MM] list indices
+  uint32_t* taken = reinterpret_cast<uint32_t*>(stg + 64 * MM * 8);  // [64][W] selected blocks
+  __shared__ __align__(8) uint64_t full[kStStages], empty[kStStages], mma_done[2], tmem_free[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_ncl;
+  __shared__ volatile int s_bad;
+
+  const int u = blockIdx.x, b = nblk - 1 - (int)blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int W = (nblk + 31) / 32;
+  const long long ubase = (long long)u * nblk;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&mma_done[i], 1);
+      mbar_init(&tmem_free[i], 4);
+    }
+    fence_mbar_init();
+    s_bad = 0;
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, kStTmemCols);
+  for (int i = tid; i < W; i += kStThreads) emask[i] = 0u;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  const int ecnt = Ecnt[ubase + b];
+  const int32_t* eb = Eb + (ubase + b) * s.ke;
+  for (int i = tid; i < ecnt; i += kStThreads) {
+    const int j = eb[i];
+    eb_s[i] = j;
+    atomicOr(&emask[j >> 5], 1u << (j & 31));
+  }
+  __syncthreads();
+  const int n_cand = b;  // blocks before the positions' own block
+  int m = min(s.k - ecnt, n_cand - ecnt);
+  if (m > MM) {  // (|E_b| = min(k_e, b) and k - k_e <= MM: cannot happen)
+    if (tid == 0) atomicExch(err, kDevErrBadIndex);
+    m = MM;
+  }
+  if (warp == 0) {  // the candidates outside E_b, ascending
+    int run = 0;
+    for (int base = 0; base < n_cand; base += 32) {
+      const int j = base + lane;
+      const bool on = j < n_cand && !((emask[j >> 5] >> (j & 31)) & 1u);
+      const unsigned bal = __ballot_sync(0xffffffffu, on);
+      if (on) cl[run + __popc(bal & ((1u << lane) - 1u))] = j;
+      run += __popc(bal);
+    }
+    if (lane == 0) s_ncl = run;
+  }
+  const int npos = min(s.B, L - b * s.B);
+  if (m > 0) {
+    // A: q_bar of the 64 positions (fp32 sum over the heads in order, x 1/G),
+    // split in 3 planes; positions past the sequence and the pad are zeros
+    const float inv_g = 1.0f / (float)s.G;
+    for (int i = tid; i < 512; i += kStThreads)
+      reinterpret_cast<uint4*>(At + 3 * NA * 8192)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < 64 * (D / 8); i += kStThreads) {
+      const int p = i / (D / 8), cg = i % (D / 8), a = cg / 8, c = cg % 8;
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (p < npos) {
+        const T* qg = q + (((long long)req * L + (long long)b * s.B + p) * s.Hq + (long long)h * s.G) * D + 8 * cg;
+        for (int g = 0; g < s.G; ++g) {
+          float y[8];
+          load8(qg + (long long)g * D, y);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] += y[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= inv_g;
+      }
+      uint4 v[3];
+      split8(x, v);
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl)
+        *reinterpret_cast<uint4*>(At + (pl * NA + a) * 8192 + (p >> 3) * 1024 + (p & 7) * 128 +
+                                  ((c ^ (p & 7)) << 4)) = v[pl];
+    }
+    fence_proxy_async();
+  }
+  __syncthreads();
+  const int ncl = s_ncl;
+
+  uint32_t key[MM];
+  int idx[MM];
+#pragma unroll
+  for (int r = 0; r < MM; ++r) {
+    key[r] = 0u;
+    idx[r] = 0x7fffffff;
+  }
+  const bool epi = warp == 0 || warp == 1 || warp == 4 || warp == 5;
+  if (m > 0) {
+    const int nch = (ncl + kStCC - 1) / kStCC, nst = nch * NA;
+    if (warp == kCopyWarp) {
+      // ---- bulk copies: stage i = (chunk i / NA, 64-dim atom i % NA) --------
+      bool ok = true;
+      int issued = 0;
+      for (int i = 0; i < nst; ++i) {
+        const int slot = i % kStStages, c = i / NA, a = i % NA;
+        if (i >= kStStages) ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((i - kStStages) / kStStages) & 1));
+        if (!__all_sync(0xffffffffu, ok) || s_bad) {
+          ok = false;
+          break;
+        }
+        const int n = min(kStCC, ncl - c * kStCC);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)n * 3u * 512u);
+        __syncwarp();
+        if (lane < n) {
+          const int j = cl[c * kStCC + lane];
+          const uint8_t* src = pk3 + ((ubase + j) * 2 + (lane & 1)) * image_bytes(D) + a * 512;
+          uint8_t* dst = stg + (size_t)slot * kStStage + (lane >> 1) * 1024 + (lane & 1) * 512;
+#pragma unroll
+          for (int p = 0; p < 3; ++p) bulk_g2s(dst + p * kStPlane, src + p * NA * 512, 512u, &full[slot]);
+        }
+        ++issued;
+      }
+      if (!ok) {
+        if (lane == 0) {
+          s_bad = 1;
+          atomicExch(err, kDevErrWaitTimeout);
+        }
+        for (int i = max(issued - kStStages, 0); i < issued; ++i)  // the copies in flight land first
+          mbar_wait_bounded(&full[i % kStStages], (uint32_t)((i / kStStages) & 1));
+      }
+    } else if (warp == kMmaWarp) {
+      // ---- MMA issue (one thread) -------------------------------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(128, 128);
+        const uint32_t a_base = smem_u32(At), s_base = smem_u32(stg);
+        bool ok = true;
+        int last = -1;  // last stage whose MMAs were committed
+        for (int c = 0; c < nch && ok; ++c) {
+          const uint32_t t_d = tmem + (uint32_t)((c & 1) * 128);
+          if (c >= 2 && !(ok = mbar_wait_bounded(&tmem_free[c & 1], (uint32_t)(((c - 2) >> 1) & 1)))) break;
+          tc_fence_after();
+          for (int a = 0; a < NA; ++a) {
+            const int i = c * NA + a, slot = i % kStStages;
+            if (!(ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kStStages) & 1))) || s_bad) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+              for (int t = 0; t < 6; ++t) {
+                const uint64_t da = sw128_desc(a_base + (uint32_t)((kTermA[t] * NA + a) * 8192)) + 2 * kk;
+                const uint64_t db = sw128_desc(s_base + (uint32_t)(slot * kStStage + kTermB[t] * kStPlane)) + 2 * kk;
+                mma_bf16(t_d, da, db, idesc, (a | kk | t) ? 1u : 0u);
+              }
+            mma_commit(&empty[slot]);  // the stage may be refilled once these MMAs read it
+            last = i;
+          }
+          if (ok) mma_commit(&mma_done[c & 1]);
+        }
+        if (!ok) {
+          s_bad = 1;
+          atomicExch(err, kDevErrWaitTimeout);
+          if (last >= 0) mbar_wait_bounded(&empty[last % kStStages], (uint32_t)((last / kStStages) & 1));
+        }
+      }
+    } else if (epi) {
+      // ---- rows: scores of a chunk half into the position's list -------------
+      const int qq = warp & 1, hc = warp >> 2;  // lane quarter (positions 32 qq + lane), column half
+      for (int c = 0; c < nch; ++c) {
+        const bool ok = mbar_wait_bounded(&mma_done[c & 1], (uint32_t)((c >> 1) & 1));
+        if (!__all_sync(0xffffffffu, ok) || s_bad) {
+          if (lane == 0) {
+            s_bad = 1;
+            atomicExch(err, kDevErrWaitTimeout);
+          }
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[64];
+        const uint32_t t_s = tmem + ((uint32_t)(32 * qq) << 16) + (uint32_t)((c & 1) * 128 + 64 * hc);
+        tmem_ld16_nowait(t_s, r);
+        tmem_ld16_nowait(t_s + 16, r + 16);
+        tmem_ld16_nowait(t_s + 32, r + 32);
+        tmem_ld16_nowait(t_s + 48, r + 48);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_free[c & 1]);
+        const int c0 = c * kStCC + 16 * hc;  // list index of the half's first candidate
+        const int nc = min(16, ncl - c0);
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          if (cc >= nc) break;  // (warp-uniform)
+          const float sc = fmaxf(fmaxf(__uint_as_float(r[4 * cc]), __uint_as_float(r[4 * cc + 1])),
+                                 fmaxf(__uint_as_float(r[4 * cc + 2]), __uint_as_float(r[4 * cc + 3]))) *
+                           inv_sqrt_d;
+          const uint32_t kx = sc == sc ? ordered_key(sc) : 0u;
+          if (kx > key[MM - 1]) list_insert<MM>(key, idx, kx, c0 + cc);  // (ascending index: '>' keeps ties)
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (s_bad) {  // a wait gave up: nothing is written (the error word is set)
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kStTmemCols);
+    }
+    return;
+  }
+  // merge the two halves' lists and mark the winners (the ring is free now)
+  if (m > 0) {
+    if (warp == 4 || warp == 5) {
+      const int pos = 32 * (warp & 1) + lane;
+#pragma unroll
+      for (int r = 0; r < MM; ++r) {
+        lk[pos * MM + r] = key[r];
+        li[pos * MM + r] = idx[r];
+      }
+    }
+    for (int i = tid; i < 64 * W; i += kStThreads) taken[i] = 0u;
+    __syncthreads();
+    if (warp == 0 || warp == 1) {
+      const int pos = 32 * warp + lane;
+      for (int r = 0; r < MM; ++r) {
+        const uint32_t kx = lk[pos * MM + r];
+        if (kx == 0u) break;  // (sorted: the rest are empty)
+        list_insert<MM>(key, idx, kx, li[pos * MM + r]);
+      }
+      uint32_t* tk = taken + pos * W;
+#pragma unroll
+      for (int r = 0; r < MM; ++r)
+        if (r < m && key[r] != 0u) {
+          const int j = cl[idx[r]];
+          tk[j >> 5] |= 1u << (j & 31);
+        }
+    }
+    __syncthreads();
+  }
+  // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the marks)
+  for (int p = warp; p < npos; p += kStThreads / 32) {
+    const int t = b * s.B + p;
+    const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
+    int32_t* selp = sel ? sel + vu * s.k : nullptr;
+    int32_t* tab = block_tab + vu * s.k;
+    for (int e = lane; e < ecnt; e += 32) {
+      if (selp) selp[e] = eb_s[e];
+      tab[e] = (int32_t)(ubase + eb_s[e]);
+    }
+    int run = ecnt;
+    if (m > 0) {
+      const uint32_t* tk = taken + p * W;
+      for (int base = 0; base < n_cand; base += 32) {
+        const int j = base + lane;
+        const bool on = (j < n_cand) && ((tk[j >> 5] >> (j & 31)) & 1u);
+        const unsigned bal = __ballot_sync(0xffffffffu, on);
+        if (on) {
+          const int at = run + __popc(bal & ((1u << lane) - 1u));
+          if (selp) selp[at] = j;
+          tab[at] = (int32_t)(ubase + j);
+        }
+        run += __popc(bal);
+      }
+    }
+    for (int e = run + lane; e < s.k; e += 32) {
+      if (selp) selp[e] = -1;
+      tab[e] = -1;
+    }
+    if (lane == 0) {
+      tail_tab[vu] = (int32_t)(ubase + b);
+      tail_len[vu] = p + 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kStTmemCols);
+  }
+}
+
+template <typename T, int D, int MM>
+cudaError_t launch_select_tc_t(const Shape& s, int L, int nblk, const void* q, const uint8_t* pk3,
+                               const int32_t* Eb, const int32_t* Ecnt, int32_t* sel, int32_t* tab,
+                               int32_t* ttab, int32_t* tlen, int* err, cudaStream_t stream) {
+  const void* fn = (const void*)prefill_select_tc_kernel<T, D, MM>;
+  static std::atomic<int> lim[64];
+  const size_t smem = SelTcSmem{D, nblk, s.ke}.total();
+  cudaError_t e = raise_smem_limit(fn, smem, lim);
+  if (e != cudaSuccess) return e;
+  const float isd = (float)(1.0 / std::sqrt((double)D));
+  prefill_select_tc_kernel<T, D, MM><<<dim3(s.U, nblk), kStThreads, smem, stream>>>(
+      s, (const T*)q, L, nblk, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, isd);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_select_tc_d(const Shape& s, int L, int nblk, const void* q, const uint8_t* pk3,
+                               const int32_t* Eb, const int32_t* Ecnt, int32_t* sel, int32_t* tab,
+                               int32_t* ttab, int32_t* tlen, int* err, cudaStream_t stream) {
+  if (s.k - s.ke <= 16)
+    return launch_select_tc_t<T, D, 16>(s, L, nblk, q, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, stream);
+  return launch_select_tc_t<T, D, 32>(s, L, nblk, q, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, stream);
+}
+
+}  // namespace
+
+bool prefill_select_tc_shape(const Shape& s) {
+  return (s.d == 64 || s.d == 128) && s.P == 4 && s.k - s.ke <= 32 && s.B == 64;
+}
+
+bool prefill_select_tc_ok(const Shape& s, int L) {
+  const char* env = std::getenv("NOSA_PREFILL_SELECT_TC");
+  if (env && std::strcmp(env, "0") == 0) return false;
+  if (!prefill_select_tc_shape(s)) return false;
+  const int nblk = (L + s.B - 1) / s.B;
+  return SelTcSmem{s.d, nblk, s.ke}.total() <= 227 * 1024 - 1024;
+}
+
+size_t prefill_keysplit_bytes(const Shape& s, int nblk) {
+  return prefill_select_tc_shape(s) ? (size_t)s.U * nblk * 2 * image_bytes(s.d) : 0;
+}
+
+cudaError_t launch_prefill_select_tc(const Shape& s, int L, const void* q, const float* pk, uint8_t* pk3,
+                                     const int32_t* Eb, const int32_t* Ecnt, int32_t* sel, int32_t* tab,
+                                     int32_t* ttab, int32_t* tlen, int* err, cudaStream_t stream) {
+  const int nblk = (L + s.B - 1) / s.B;
+  if (nblk > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 kgrid(nblk, s.U);
+  if (s.d == 64)
+    prefill_keysplit_kernel<64><<<kgrid, 4 * 64 / 8, 0, stream>>>(pk, nblk, pk3);
+  else
+    prefill_keysplit_kernel<128><<<kgrid, 4 * 128 / 8, 0, stream>>>(pk, nblk, pk3);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (s.dtype == 0)
+    return s.d == 64 ? launch_select_tc_d<float, 64>(s, L, nblk, q, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, stream)
+                     : launch_select_tc_d<float, 128>(s, L, nblk, q, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, stream);
+  return s.d == 64
+             ? launch_select_tc_d<__nv_bfloat16, 64>(s, L, nblk, q, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, stream)
+             : launch_select_tc_d<__nv_bfloat16, 128>(s, L, nblk, q, pk3, Eb, Ecnt, sel, tab, ttab, tlen, err, stream);
+}
+
+}  // namespace nosa

@@ -104,7 +104,7 @@ int frontend_max_clusters(const FrontParams& p);
 
 // Training-time forward (k_prefill.cu): byte offsets into the caller's workspace.
 struct PrefillLayout {
-  size_t units, pk, se, eb, ecnt, tab, tail_tab, tail_len, part_acc, part_ml, counters, vmax, err,
+  size_t units, pk, pk3, se, eb, ecnt, tab, tail_tab, tail_len, part_acc, part_ml, counters, vmax, err,
       total;
 };
 // s describes the real units (batch * Hkv); L is the sequence length.
@@ -117,6 +117,16 @@ size_t prefill_select_smem(const Shape& s, int nblk);
 cudaError_t launch_prefill_front(const Shape& s, int L, const void* q, const void* k,
                                  const void* v, const float* e, int32_t* sel, uint8_t* ws,
                                  const PrefillLayout& w, bool tc, cudaStream_t stream);
+// Selection with the pooled query scores on the tensor cores (k_prefill_sel_tc.cu):
+// shapes with d in {64, 128}, 64-token blocks of 4 sub-blocks and k - k_e <= 32.
+bool prefill_select_tc_shape(const Shape& s);
+// ... and NOSA_PREFILL_SELECT_TC is not 0 and the shared memory fits.
+bool prefill_select_tc_ok(const Shape& s, int L);
+// Bytes of the split pooled-key images (0 for shapes the path does not cover).
+size_t prefill_keysplit_bytes(const Shape& s, int nblk);
+cudaError_t launch_prefill_select_tc(const Shape& s, int L, const void* q, const float* pk, uint8_t* pk3,
+                                     const int32_t* Eb, const int32_t* Ecnt, int32_t* sel, int32_t* tab,
+                                     int32_t* ttab, int32_t* tlen, int* err, cudaStream_t stream);
 // Tiled tensor-core attention of the training-time forward (k_prefill_tc.cu):
 // one CTA per (unit, query block), grid (nblk, unit_count).
 struct PrefillTileArgs {
