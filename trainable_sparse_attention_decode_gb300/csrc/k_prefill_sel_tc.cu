@@ -17,27 +17,26 @@
 // memory: the error of a score is that of an fp32 dot product. Non-finite inputs
 // keep x1 = x and zero tails.
 //
-// prefill_keysplit_kernel  the three bf16 planes of every block's pooled keys, as
-//                          two 128-byte-swizzled images (for an even and an odd
-//                          slot of a chunk), so that one bulk copy of 512 bytes
-//                          per plane and 64 dims lands a candidate's 4 rows
-//                          in place                                  (block, unit)
+// prefill_keysplit_kernel  the three bf16 planes of the pooled keys of every
+//                          chunk of 32 consecutive blocks, per 64-dim atom, laid
+//                          out as the selection's shared-memory stage (128 rows:
+//                          block 32 c + i, sub-block s at row 4 i + s, 128-byte
+//                          swizzle), so one bulk copy per plane fills a stage
 // prefill_select_tc_kernel one CTA per (unit, block), heaviest blocks first:
 //   A     q_bar of the 64 positions, split in 3 planes, 128-byte-swizzled K-major
 //         tiles of 64 rows (M = 128: rows 64-127 of a tile read the next tile or a
 //         zero pad; their results are never read);
-//   B     chunks of 32 candidates (N = 128 rows: candidate c, sub-block s at row
-//         4 c + s), 64 dims per stage, a ring of 3 stages filled by bulk copies
-//         (copy warp) from the candidates' images;
+//   B     chunks of 32 consecutive blocks j < b (N = 128 rows), 64 dims per stage,
+//         a ring of 3 stages filled by bulk copies (copy warp); the blocks of E_b
+//         are scored too and left out in the epilogue;
 //   MMA   per stage 4 K16 steps x 6 terms (tcgen05.mma kind::f16, bf16 in, fp32
 //         accumulator), a chunk into one of two 128-column tensor-memory buffers;
-//   rows  4 epilogue warps (position = tensor-memory lane; two warps per lane
-//         quarter, one per half of a chunk's columns): the max over each
-//         candidate's 4 columns times 1/sqrt(d) goes into the warp's sorted
-//         register list of the best m (key descending, list index ascending:
-//         lower block id first at equal scores; a NaN score never enters); the
-//         two halves' lists are merged at the end, the winners marked, and the
-//         position's selection written in ascending block order.
+//   rows  2 epilogue warps (position = tensor-memory lane): the max over each
+//         candidate's 4 columns times 1/sqrt(d) goes into the position's sorted
+//         register list of the best m (key descending, block id ascending: the
+//         lower id first at equal scores; a NaN score and a block of E_b never
+//         enter); at the end the thread sorts its winners by id and writes the
+//         position's selection.
 // Barriers: full / empty [stage] (copies landed / MMAs read the stage), mma_done
 // [buffer] (a chunk's scores are in), tmem_free [buffer] (the epilogue warps read
 // them). Every wait is bounded; one that gives up sets the error word, and the CTA
@@ -64,12 +63,13 @@ constexpr int kStStages = 3;                         // ring of 64-dim stages
 constexpr uint32_t kStPlane = 16384;                 // one plane of a stage: 128 rows x 128 B
 constexpr uint32_t kStStage = 3 * kStPlane;          // the three planes
 constexpr int kStTmemCols = 256;                     // two 128-column score buffers
-constexpr int kMmaWarp = 2, kCopyWarp = 3;           // epilogue: warps 0, 1, 4, 5
+constexpr int kMmaWarp = 2, kCopyWarp = 3;           // epilogue: warps 0 and 1
 // the six (A plane, B plane) products kept
 __constant__ int kTermA[6] = {0, 0, 1, 0, 1, 2};
 __constant__ int kTermB[6] = {0, 1, 0, 2, 1, 0};
 
-__host__ __device__ constexpr uint32_t image_bytes(int d) { return 3u * (uint32_t)(d / 64) * 512u; }
+// bytes of the split keys of one chunk of 32 blocks (all atoms)
+__host__ __device__ constexpr uint32_t chunk_bytes(int d) { return (uint32_t)(d / 64) * kStStage; }
 
 __device__ __forceinline__ void split3(float x, uint16_t& h1, uint16_t& h2, uint16_t& h3) {
   const __nv_bfloat16 b1 = __float2bfloat16_rn(x);
@@ -108,27 +108,43 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float* x) {
   }
 }
 
-// Images of block (u, j): [parity][plane][64-dim atom][row s][128 B], the 16-byte
-// chunk c (dims 64 atom + 8 c ..) of row s at chunk c ^ (4 parity + s): the rows
-// 4 parity + s of an 8-row group of the 128-byte swizzle. grid (nblk, U), 4 d / 8
-// threads.
+// Split keys of chunk C of unit u: [atom][plane][128 rows x 128 B], block 32 C + i,
+// sub-block s at row r = 4 i + s (8-row groups 1024 bytes apart, 16-byte chunk c of
+// a row at chunk c ^ (r % 8)); blocks past the sequence are zeros. grid (32 x
+// chunks, U), 4 d / 8 threads.
 template <int D>
 __global__ void __launch_bounds__(4 * D / 8) prefill_keysplit_kernel(const float* __restrict__ pk, int nblk,
                                                                      uint8_t* __restrict__ pk3) {
-  constexpr int NA = D / 64;
-  const long long blk = (long long)blockIdx.y * nblk + blockIdx.x;
+  const int j = blockIdx.x, u = blockIdx.y, nch = gridDim.x / 32;
   const int s = threadIdx.x / (D / 8), cg = threadIdx.x % (D / 8), a = cg / 8, c = cg % 8;
-  float x[8];
-  load8(pk + (blk * 4 + s) * D + 8 * cg, x);
+  float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (j < nblk) load8(pk + (((long long)u * nblk + j) * 4 + s) * D + 8 * cg, x);
   uint4 v[3];
   split8(x, v);
-  uint8_t* img = pk3 + blk * 2 * image_bytes(D);
+  const int r = 4 * (j % 32) + s;
+  uint8_t* dst = pk3 + ((long long)u * nch + j / 32) * chunk_bytes(D) + (size_t)a * kStStage +
+                 (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
 #pragma unroll
-  for (int par = 0; par < 2; ++par)
+  for (int p = 0; p < 3; ++p) *reinterpret_cast<uint4*>(dst + p * kStPlane) = v[p];
+}
+
+// Sorts v ascending (bitonic network; N a power of two).
+template <int N>
+__device__ __forceinline__ void sort_asc(int (&v)[N]) {
 #pragma unroll
-    for (int p = 0; p < 3; ++p)
-      *reinterpret_cast<uint4*>(img + par * image_bytes(D) + (p * NA + a) * 512 + s * 128 +
-                                ((c ^ (4 * par + s)) << 4)) = v[p];
+  for (int k = 2; k <= N; k <<= 1)
+#pragma unroll
+    for (int jj = k >> 1; jj > 0; jj >>= 1)
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int l = i ^ jj;
+        if (l > i) {
+          const int x = v[i], y = v[l];
+          const bool up = (i & k) == 0;
+          v[i] = up ? min(x, y) : max(x, y);
+          v[l] = up ? max(x, y) : min(x, y);
+        }
+      }
 }
 
 // Inserts (kx, ix) into a list sorted by (key descending, index ascending) when it
@@ -153,8 +169,7 @@ struct SelTcSmem {
   __host__ __device__ size_t a() const { return 0; }                                   // [3][d/64] 8 KB tiles + 8 KB zeros
   __host__ __device__ size_t stg() const { return (size_t)(3 * (d / 64) + 1) * 8192; }  // [kStStages][kStStage]
   __host__ __device__ size_t emask() const { return stg() + (size_t)kStStages * kStStage; }
-  __host__ __device__ size_t cl() const { return emask() + 4 * (size_t)(((nblk + 31) / 32 + 3) & ~3); }
-  __host__ __device__ size_t eb() const { return cl() + 4 * (size_t)nblk; }
+  __host__ __device__ size_t eb() const { return emask() + 4 * (size_t)(((nblk + 31) / 32 + 3) & ~3); }
   __host__ __device__ size_t total() const { return eb() + 4 * (size_t)std::max(ke, 1) + 1024; }
 };
 
@@ -171,20 +186,14 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
   uint8_t* At = sm + Lay.a();
   uint8_t* stg = sm + Lay.stg();
   uint32_t* emask = reinterpret_cast<uint32_t*>(sm + Lay.emask());
-  int32_t* cl = reinterpret_cast<int32_t*>(sm + Lay.cl());
   int32_t* eb_s = reinterpret_cast<int32_t*>(sm + Lay.eb());
-  // after the scoring the ring holds the second half's lists and the marks
-  uint32_t* lk = reinterpret_cast<uint32_t*>(stg);                 // [64][MM] keys
-  int32_t* li = reinterpret_cast<int32_t*>(stg + 64 * MM * 4);     // [64][MM] list indices
-  uint32_t* taken = reinterpret_cast<uint32_t*>(stg + 64 * MM * 8);  // [64][W] selected blocks
   __shared__ __align__(8) uint64_t full[kStStages], empty[kStStages], mma_done[2], tmem_free[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int s_ncl;
   __shared__ volatile int s_bad;
 
   const int u = blockIdx.x, b = nblk - 1 - (int)blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int W = (nblk + 31) / 32;
+  const int W = (nblk + 31) / 32, nch_all = (nblk + 31) / 32;
   const long long ubase = (long long)u * nblk;
 
   if (tid == 0) {
@@ -194,7 +203,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&mma_done[i], 1);
-      mbar_init(&tmem_free[i], 4);
+      mbar_init(&tmem_free[i], 2);
     }
     fence_mbar_init();
     s_bad = 0;
@@ -213,23 +222,11 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     eb_s[i] = j;
     atomicOr(&emask[j >> 5], 1u << (j & 31));
   }
-  __syncthreads();
   const int n_cand = b;  // blocks before the positions' own block
   int m = min(s.k - ecnt, n_cand - ecnt);
   if (m > MM) {  // (|E_b| = min(k_e, b) and k - k_e <= MM: cannot happen)
     if (tid == 0) atomicExch(err, kDevErrBadIndex);
     m = MM;
-  }
-  if (warp == 0) {  // the candidates outside E_b, ascending
-    int run = 0;
-    for (int base = 0; base < n_cand; base += 32) {
-      const int j = base + lane;
-      const bool on = j < n_cand && !((emask[j >> 5] >> (j & 31)) & 1u);
-      const unsigned bal = __ballot_sync(0xffffffffu, on);
-      if (on) cl[run + __popc(bal & ((1u << lane) - 1u))] = j;
-      run += __popc(bal);
-    }
-    if (lane == 0) s_ncl = run;
   }
   const int npos = min(s.B, L - b * s.B);
   if (m > 0) {
@@ -238,7 +235,10 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     const float inv_g = 1.0f / (float)s.G;
     for (int i = tid; i < 512; i += kStThreads)
       reinterpret_cast<uint4*>(At + 3 * NA * 8192)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = tid; i < 64 * (D / 8); i += kStThreads) {
+    constexpr int kItems = 64 * (D / 8) / kStThreads;  // 8-dim pieces per thread
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      const int i = tid + it * kStThreads;
       const int p = i / (D / 8), cg = i % (D / 8), a = cg / 8, c = cg % 8;
       float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (p < npos) {
@@ -262,7 +262,6 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     fence_proxy_async();
   }
   __syncthreads();
-  const int ncl = s_ncl;
 
   uint32_t key[MM];
   int idx[MM];
@@ -271,39 +270,34 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     key[r] = 0u;
     idx[r] = 0x7fffffff;
   }
-  const bool epi = warp == 0 || warp == 1 || warp == 4 || warp == 5;
   if (m > 0) {
-    const int nch = (ncl + kStCC - 1) / kStCC, nst = nch * NA;
+    const int nch = (n_cand + kStCC - 1) / kStCC, nst = nch * NA;
     if (warp == kCopyWarp) {
       // ---- bulk copies: stage i = (chunk i / NA, 64-dim atom i % NA) --------
-      bool ok = true;
-      int issued = 0;
-      for (int i = 0; i < nst; ++i) {
-        const int slot = i % kStStages, c = i / NA, a = i % NA;
-        if (i >= kStStages) ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((i - kStStages) / kStStages) & 1));
-        if (!__all_sync(0xffffffffu, ok) || s_bad) {
-          ok = false;
-          break;
-        }
-        const int n = min(kStCC, ncl - c * kStCC);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)n * 3u * 512u);
-        __syncwarp();
-        if (lane < n) {
-          const int j = cl[c * kStCC + lane];
-          const uint8_t* src = pk3 + ((ubase + j) * 2 + (lane & 1)) * image_bytes(D) + a * 512;
-          uint8_t* dst = stg + (size_t)slot * kStStage + (lane >> 1) * 1024 + (lane & 1) * 512;
+      if (lane == 0) {
+        bool ok = true;
+        int issued = 0;
+        for (int i = 0; i < nst; ++i) {
+          const int slot = i % kStStages;
+          if (i >= kStStages && !(ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((i - kStStages) / kStStages) & 1))))
+            break;
+          if (s_bad) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[slot], kStStage);
+          const uint8_t* src = pk3 + ((long long)u * nch_all + i / NA) * chunk_bytes(D) + (size_t)(i % NA) * kStStage;
+          uint8_t* dst = stg + (size_t)slot * kStStage;
 #pragma unroll
-          for (int p = 0; p < 3; ++p) bulk_g2s(dst + p * kStPlane, src + p * NA * 512, 512u, &full[slot]);
+          for (int p = 0; p < 3; ++p) bulk_g2s(dst + p * kStPlane, src + p * kStPlane, kStPlane, &full[slot]);
+          ++issued;
         }
-        ++issued;
-      }
-      if (!ok) {
-        if (lane == 0) {
+        if (!ok) {
           s_bad = 1;
           atomicExch(err, kDevErrWaitTimeout);
+          for (int i = max(issued - kStStages, 0); i < issued; ++i)  // the copies in flight land first
+            mbar_wait_bounded(&full[i % kStStages], (uint32_t)((i / kStStages) & 1));
         }
-        for (int i = max(issued - kStStages, 0); i < issued; ++i)  // the copies in flight land first
-          mbar_wait_bounded(&full[i % kStStages], (uint32_t)((i / kStStages) & 1));
       }
     } else if (warp == kMmaWarp) {
       // ---- MMA issue (one thread) -------------------------------------------
@@ -342,9 +336,9 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
           if (last >= 0) mbar_wait_bounded(&empty[last % kStStages], (uint32_t)((last / kStStages) & 1));
         }
       }
-    } else if (epi) {
-      // ---- rows: scores of a chunk half into the position's list -------------
-      const int qq = warp & 1, hc = warp >> 2;  // lane quarter (positions 32 qq + lane), column half
+    } else if (warp < 2) {
+      // ---- rows: a chunk's scores into the position's list -------------------
+      const uint32_t t_lane = (uint32_t)(32 * warp) << 16;  // positions 32 warp + lane
       for (int c = 0; c < nch; ++c) {
         const bool ok = mbar_wait_bounded(&mma_done[c & 1], (uint32_t)((c >> 1) & 1));
         if (!__all_sync(0xffffffffu, ok) || s_bad) {
@@ -355,26 +349,32 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
           break;
         }
         tc_fence_after();
-        uint32_t r[64];
-        const uint32_t t_s = tmem + ((uint32_t)(32 * qq) << 16) + (uint32_t)((c & 1) * 128 + 64 * hc);
-        tmem_ld16_nowait(t_s, r);
-        tmem_ld16_nowait(t_s + 16, r + 16);
-        tmem_ld16_nowait(t_s + 32, r + 32);
-        tmem_ld16_nowait(t_s + 48, r + 48);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tmem_free[c & 1]);
-        const int c0 = c * kStCC + 16 * hc;  // list index of the half's first candidate
-        const int nc = min(16, ncl - c0);
+        // candidates of the chunk: blocks 32 c + i before b and outside E_b
+        const uint32_t live = ~emask[c] & (32 * c + 32 <= n_cand ? 0xffffffffu : ((1u << (n_cand - 32 * c)) - 1u));
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          if (cc >= nc) break;  // (warp-uniform)
-          const float sc = fmaxf(fmaxf(__uint_as_float(r[4 * cc]), __uint_as_float(r[4 * cc + 1])),
-                                 fmaxf(__uint_as_float(r[4 * cc + 2]), __uint_as_float(r[4 * cc + 3]))) *
-                           inv_sqrt_d;
-          const uint32_t kx = sc == sc ? ordered_key(sc) : 0u;
-          if (kx > key[MM - 1]) list_insert<MM>(key, idx, kx, c0 + cc);  // (ascending index: '>' keeps ties)
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[64];
+          const uint32_t t_s = tmem + t_lane + (uint32_t)((c & 1) * 128 + 64 * half);
+          tmem_ld16_nowait(t_s, r);
+          tmem_ld16_nowait(t_s + 16, r + 16);
+          tmem_ld16_nowait(t_s + 32, r + 32);
+          tmem_ld16_nowait(t_s + 48, r + 48);
+          tmem_wait_ld();
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_free[c & 1]);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const int i = 16 * half + cc;
+            if (!((live >> i) & 1u)) continue;  // (warp-uniform)
+            const float sc = fmaxf(fmaxf(__uint_as_float(r[4 * cc]), __uint_as_float(r[4 * cc + 1])),
+                                   fmaxf(__uint_as_float(r[4 * cc + 2]), __uint_as_float(r[4 * cc + 3]))) *
+                             inv_sqrt_d;
+            const uint32_t kx = sc == sc ? ordered_key(sc) : 0u;
+            if (kx > key[MM - 1]) list_insert<MM>(key, idx, kx, 32 * c + i);  // (ascending ids: '>' keeps ties)
+          }
         }
       }
     }
@@ -389,65 +389,35 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     }
     return;
   }
-  // merge the two halves' lists and mark the winners (the ring is free now)
-  if (m > 0) {
-    if (warp == 4 || warp == 5) {
-      const int pos = 32 * (warp & 1) + lane;
+  // outputs, one thread per position: E_b ascending, then Gamma_q ascending, -1 pad
+  if (warp < 2) {
+    const int p = 32 * warp + lane;
+    if (p < npos) {
+      int ids[MM];
 #pragma unroll
-      for (int r = 0; r < MM; ++r) {
-        lk[pos * MM + r] = key[r];
-        li[pos * MM + r] = idx[r];
+      for (int r = 0; r < MM; ++r) ids[r] = (r < m && key[r] != 0u) ? idx[r] : 0x7fffffff;
+      sort_asc<MM>(ids);
+      const int t = b * s.B + p;
+      const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
+      int32_t* selp = sel ? sel + vu * s.k : nullptr;
+      int32_t* tab = block_tab + vu * s.k;
+      for (int e = 0; e < ecnt; ++e) {
+        const int j = eb_s[e];
+        if (selp) selp[e] = j;
+        tab[e] = (int32_t)(ubase + j);
       }
-    }
-    for (int i = tid; i < 64 * W; i += kStThreads) taken[i] = 0u;
-    __syncthreads();
-    if (warp == 0 || warp == 1) {
-      const int pos = 32 * warp + lane;
-      for (int r = 0; r < MM; ++r) {
-        const uint32_t kx = lk[pos * MM + r];
-        if (kx == 0u) break;  // (sorted: the rest are empty)
-        list_insert<MM>(key, idx, kx, li[pos * MM + r]);
-      }
-      uint32_t* tk = taken + pos * W;
+      int run = ecnt;
 #pragma unroll
       for (int r = 0; r < MM; ++r)
-        if (r < m && key[r] != 0u) {
-          const int j = cl[idx[r]];
-          tk[j >> 5] |= 1u << (j & 31);
+        if (ids[r] != 0x7fffffff) {
+          if (selp) selp[run] = ids[r];
+          tab[run] = (int32_t)(ubase + ids[r]);
+          ++run;
         }
-    }
-    __syncthreads();
-  }
-  // outputs: E_b ascending, then Gamma_q ascending (ballot scan over the marks)
-  for (int p = warp; p < npos; p += kStThreads / 32) {
-    const int t = b * s.B + p;
-    const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
-    int32_t* selp = sel ? sel + vu * s.k : nullptr;
-    int32_t* tab = block_tab + vu * s.k;
-    for (int e = lane; e < ecnt; e += 32) {
-      if (selp) selp[e] = eb_s[e];
-      tab[e] = (int32_t)(ubase + eb_s[e]);
-    }
-    int run = ecnt;
-    if (m > 0) {
-      const uint32_t* tk = taken + p * W;
-      for (int base = 0; base < n_cand; base += 32) {
-        const int j = base + lane;
-        const bool on = (j < n_cand) && ((tk[j >> 5] >> (j & 31)) & 1u);
-        const unsigned bal = __ballot_sync(0xffffffffu, on);
-        if (on) {
-          const int at = run + __popc(bal & ((1u << lane) - 1u));
-          if (selp) selp[at] = j;
-          tab[at] = (int32_t)(ubase + j);
-        }
-        run += __popc(bal);
+      for (int e = run; e < s.k; ++e) {
+        if (selp) selp[e] = -1;
+        tab[e] = -1;
       }
-    }
-    for (int e = run + lane; e < s.k; e += 32) {
-      if (selp) selp[e] = -1;
-      tab[e] = -1;
-    }
-    if (lane == 0) {
       tail_tab[vu] = (int32_t)(ubase + b);
       tail_len[vu] = p + 1;
     }
@@ -499,7 +469,7 @@ bool prefill_select_tc_ok(const Shape& s, int L) {
 }
 
 size_t prefill_keysplit_bytes(const Shape& s, int nblk) {
-  return prefill_select_tc_shape(s) ? (size_t)s.U * nblk * 2 * image_bytes(s.d) : 0;
+  return prefill_select_tc_shape(s) ? (size_t)s.U * ((nblk + 31) / 32) * chunk_bytes(s.d) : 0;
 }
 
 cudaError_t launch_prefill_select_tc(const Shape& s, int L, const void* q, const float* pk, uint8_t* pk3,
@@ -507,7 +477,7 @@ cudaError_t launch_prefill_select_tc(const Shape& s, int L, const void* q, const
                                      int32_t* ttab, int32_t* tlen, int* err, cudaStream_t stream) {
   const int nblk = (L + s.B - 1) / s.B;
   if (nblk > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 kgrid(nblk, s.U);
+  const dim3 kgrid((nblk + 31) / 32 * 32, s.U);
   if (s.d == 64)
     prefill_keysplit_kernel<64><<<kgrid, 4 * 64 / 8, 0, stream>>>(pk, nblk, pk3);
   else
