@@ -31,12 +31,14 @@
 //         are scored too and left out in the epilogue;
 //   MMA   per stage 4 K16 steps x 6 terms (tcgen05.mma kind::f16, bf16 in, fp32
 //         accumulator), a chunk into one of two 128-column tensor-memory buffers;
-//   rows  2 epilogue warps (position = tensor-memory lane): the max over each
-//         candidate's 4 columns times 1/sqrt(d) goes into the position's sorted
-//         register list of the best m (key descending, block id ascending: the
-//         lower id first at equal scores; a NaN score and a block of E_b never
-//         enter); at the end the thread sorts its winners by id and writes the
-//         position's selection.
+//   rows  4 epilogue warps, two per lane quarter (position = tensor-memory lane),
+//         one pair on the even chunks (buffer 0), one on the odd (buffer 1): the
+//         max over each candidate's 4 columns times 1/sqrt(d) goes into the
+//         thread's sorted register list of the best m (key descending, block id
+//         ascending: the lower id first at equal scores; a NaN score and a block
+//         of E_b never enter); at the end the even-chunk thread of a position
+//         merges the two lists, sorts the winners by id and writes the position's
+//         selection.
 // Barriers: full / empty [stage] (copies landed / MMAs read the stage), mma_done
 // [buffer] (a chunk's scores are in), tmem_free [buffer] (the epilogue warps read
 // them). Every wait is bounded; one that gives up sets the error word, and the CTA
@@ -63,7 +65,7 @@ constexpr int kStStages = 3;                         // ring of 64-dim stages
 constexpr uint32_t kStPlane = 16384;                 // one plane of a stage: 128 rows x 128 B
 constexpr uint32_t kStStage = 3 * kStPlane;          // the three planes
 constexpr int kStTmemCols = 256;                     // two 128-column score buffers
-constexpr int kMmaWarp = 2, kCopyWarp = 3;           // epilogue: warps 0 and 1
+constexpr int kMmaWarp = 2, kCopyWarp = 3;           // epilogue: warps 0, 1 (even chunks), 4, 5 (odd)
 // the six (A plane, B plane) products kept
 __constant__ int kTermA[6] = {0, 0, 1, 0, 1, 2};
 __constant__ int kTermB[6] = {0, 1, 0, 2, 1, 0};
@@ -187,6 +189,9 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
   uint8_t* stg = sm + Lay.stg();
   uint32_t* emask = reinterpret_cast<uint32_t*>(sm + Lay.emask());
   int32_t* eb_s = reinterpret_cast<int32_t*>(sm + Lay.eb());
+  // after the scoring the ring holds the odd-chunk lists
+  uint32_t* lk = reinterpret_cast<uint32_t*>(stg);              // [64][MM] keys
+  int32_t* li = reinterpret_cast<int32_t*>(stg + 64 * MM * 4);  // [64][MM] block ids
   __shared__ __align__(8) uint64_t full[kStStages], empty[kStStages], mma_done[2], tmem_free[2];
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_bad;
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&mma_done[i], 1);
-      mbar_init(&tmem_free[i], 2);
+      mbar_init(&tmem_free[i], 2);  // the two warps of the buffer's chunk parity
     }
     fence_mbar_init();
     s_bad = 0;
@@ -336,10 +341,11 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
           if (last >= 0) mbar_wait_bounded(&empty[last % kStStages], (uint32_t)((last / kStStages) & 1));
         }
       }
-    } else if (warp < 2) {
+    } else if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
       // ---- rows: a chunk's scores into the position's list -------------------
-      const uint32_t t_lane = (uint32_t)(32 * warp) << 16;  // positions 32 warp + lane
-      for (int c = 0; c < nch; ++c) {
+      const int gp = warp >> 2;                                 // chunk parity (= score buffer)
+      const uint32_t t_lane = (uint32_t)(32 * (warp & 1)) << 16;  // positions 32 (warp & 1) + lane
+      for (int c = gp; c < nch; c += 2) {
         const bool ok = mbar_wait_bounded(&mma_done[c & 1], (uint32_t)((c >> 1) & 1));
         if (!__all_sync(0xffffffffu, ok) || s_bad) {
           if (lane == 0) {
@@ -389,13 +395,49 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
     }
     return;
   }
+  if (warp == 4 || warp == 5) {  // the odd-chunk lists (the ring is free now)
+    const int p = 32 * (warp & 1) + lane;
+#pragma unroll
+    for (int r = 0; r < MM; ++r) {
+      lk[p * MM + r] = key[r];
+      li[p * MM + r] = idx[r];
+    }
+  }
+  __syncthreads();
   // outputs, one thread per position: E_b ascending, then Gamma_q ascending, -1 pad
   if (warp < 2) {
     const int p = 32 * warp + lane;
     if (p < npos) {
+      // the best m of the two lists (both sorted; ids distinct), then by id
       int ids[MM];
+      int jb = 0;
+      uint32_t bk = lk[p * MM];
+      int bi = li[p * MM];
 #pragma unroll
-      for (int r = 0; r < MM; ++r) ids[r] = (r < m && key[r] != 0u) ? idx[r] : 0x7fffffff;
+      for (int r = 0; r < MM; ++r) {
+        int id = 0x7fffffff;
+        if (r < m) {
+          const bool own = key[0] > bk || (key[0] == bk && idx[0] < bi);
+          if ((own ? key[0] : bk) != 0u) {
+            if (own) {
+              id = idx[0];
+#pragma unroll
+              for (int t = 0; t < MM - 1; ++t) {
+                key[t] = key[t + 1];
+                idx[t] = idx[t + 1];
+              }
+              key[MM - 1] = 0u;
+              idx[MM - 1] = 0x7fffffff;
+            } else {
+              id = bi;
+              ++jb;
+              bk = jb < MM ? lk[p * MM + jb] : 0u;
+              bi = jb < MM ? li[p * MM + jb] : 0x7fffffff;
+            }
+          }
+        }
+        ids[r] = id;
+      }
       sort_asc<MM>(ids);
       const int t = b * s.B + p;
       const long long vu = ((long long)req * L + t) * s.Hkv + h;  // virtual unit of the position
