@@ -234,6 +234,9 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
  * In bf16 with n_q_heads / n_kv_heads in {1, 2, 4} and head_dim in {64, 128} the
  * attention runs per query block on the tensor cores (environment variable
  * NOSA_PREFILL_TILED=0: the split-K decode attention per position instead).
+ * With head_dim in {64, 128} and k - k_e <= 32 the selection's pooled query
+ * scores run on the tensor cores from a three-term bf16 split of the fp32
+ * operands (fp32-accurate; NOSA_PREFILL_SELECT_TC=0: fp32 on the CUDA cores).
  */
 size_t nosa_prefill_workspace_bytes(const nosa_config* cfg, int32_t seq_len);
 nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const void* q,
