@@ -15,9 +15,12 @@
 //                          eviction scores of every block            (unit, block)
 //   prefill_evict_kernel   the eviction sets E_b, one warp per block
 //   prefill_select_kernel  per position: pooled query scores of the candidates
-//                          outside E_b, top-(k - |E_b|) by sorted per-lane lists
-//                          (or warp arg-max rounds beyond 32); writes the
-//                          position's block table and tail         (unit, block)
+//                          outside E_b in fp32 on the CUDA cores, top-(k - |E_b|)
+//                          by sorted per-lane lists (or warp arg-max rounds beyond
+//                          32); writes the position's block table and tail
+//                          (unit, block). Where k - k_e <= 32 and d is 64 or 128
+//                          the selection runs on the tensor cores instead
+//                          (k_prefill_sel_tc.cu) unless NOSA_PREFILL_SELECT_TC=0.
 //   prefill_tile_kernel    (bf16, G <= 4, d in {64, 128}; k_prefill_tc.cu) the
 //                          attention of a whole query block on the tensor cores,
 //                          over the union of its positions' blocks;

@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(kStThreads, 1) prefill_select_tc_kernel(
 
   const int u = blockIdx.x, b = nblk - 1 - (int)blockIdx.y, req = u / s.Hkv, h = u % s.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int W = (nblk + 31) / 32, nch_all = (nblk + 31) / 32;
+  const int W = (nblk + 31) / 32;  // mask words = chunks of 32 blocks
+  const int nch_all = W;
   const long long ubase = (long long)u * nblk;
 
   if (tid == 0) {
