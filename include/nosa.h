@@ -246,8 +246,9 @@ nosa_status nosa_prefill_forward(const nosa_config* cfg, int32_t seq_len, const 
 /*
  * The device error word of the last nosa_prefill_forward run in `workspace` with
  * the same cfg and seq_len: 0 none, 1 a bounded wait in a kernel gave up (the
- * outputs of the affected query blocks are not written), 2 a block table entry
- * out of range (skipped). Waits for the device (cudaDeviceSynchronize) and then
+ * selections or outputs of the affected query blocks are not written), 2 a block
+ * table entry out of range (skipped) or a selection wider than the tensor-core
+ * selection's lists (clamped; not reachable with |Gamma_e| = min(k_e, blocks)). Waits for the device (cudaDeviceSynchronize) and then
  * copies the 4-byte word to *err (host). INVALID_ARG on NULL or sizes outside the
  * forward's limits; CUDA on a failed copy.
  */
