@@ -62,7 +62,7 @@ TAIL = 1
 __all__ = [
     "HOST", "TAIL", "pool_block", "group_query", "block_scores", "decision_values",
     "top_m", "dual_select", "set_difference", "attend", "encode_payload",
-    "payload_bytes", "UnitOracle", "pooled_keys_bf16", "round_bf16",
+    "payload_bytes", "UnitOracle", "pooled_keys_bf16", "round_bf16", "stored_means_f32",
     "frontend_rows", "project", "frontend_storage", "prefill_unit",
 ]
 
@@ -93,21 +93,33 @@ def round_bf16(x32: np.ndarray) -> np.ndarray:
     return r.view(np.float32).astype(np.float64)
 
 
+def stored_means_f32(x_blk: np.ndarray, sub_block: int) -> np.ndarray:
+    """Sub-block means in the precision the pooled state is kept in (R14).
+
+    The values of each sub-block are summed in fp32, in token order, starting
+    from 0, and the sum is multiplied by the fp32 value of 1/S. x_blk is [B][d]
+    (keys) or [B] (eviction logits) of stored values, exact in fp32. Returns the
+    fp32 means as fp64, [B/S][d] or [B/S]. The exact means of pool_block differ
+    from these by at most the rounding of a 16-term fp32 sum.
+    """
+    x = np.asarray(x_blk, dtype=np.float64)
+    B = x.shape[0]
+    P = B // sub_block
+    x32 = x.astype(np.float32).reshape((P, sub_block) + x.shape[1:])
+    acc = np.zeros((P,) + x.shape[1:], dtype=np.float32)
+    for j in range(sub_block):
+        acc = np.add(acc, x32[:, j], dtype=np.float32)
+    return np.multiply(acc, np.float32(1.0 / sub_block), dtype=np.float32).astype(np.float64)
+
+
 def pooled_keys_bf16(k_blk: np.ndarray, sub_block: int) -> np.ndarray:
     """Sub-block mean keys of the bf16 pooled-key variant (R14 with bf16 storage).
 
-    The sum of each sub-block's keys is taken in fp32, in token order, starting
-    from 0; it is multiplied by the fp32 value of 1/S and rounded to nearest even
-    in bf16. k_blk [B][d] holds the stored keys (exact in fp32). Returns [B/S][d] fp64.
+    The fp32 means of stored_means_f32 (token-order fp32 sum times fl32(1/S)),
+    rounded to nearest even in bf16. k_blk [B][d] holds the stored keys (exact in
+    fp32). Returns [B/S][d] fp64.
     """
-    B, d = k_blk.shape
-    P = B // sub_block
-    k32 = np.asarray(k_blk, dtype=np.float64).astype(np.float32).reshape(P, sub_block, d)
-    acc = np.zeros((P, d), dtype=np.float32)
-    for j in range(sub_block):
-        acc = np.add(acc, k32[:, j, :], dtype=np.float32)
-    mean = np.multiply(acc, np.float32(1.0 / sub_block), dtype=np.float32)
-    return round_bf16(mean)
+    return round_bf16(stored_means_f32(k_blk, sub_block))
 
 
 def group_query(q_group: np.ndarray) -> np.ndarray:

@@ -346,6 +346,33 @@ def test_pooled_bf16_follows_fp32_token_order():
     assert O.pool_block(k, np.zeros(64), 16)[0][0, 0] == 0.875
 
 
+def test_stored_means_f32_token_order_and_exact_cases():
+    # The same 2**24 construction in fp32 storage: token order decides the mean.
+    k = np.zeros((64, 2))
+    k[:16, 0] = [2.0 ** 24] + [1.0] * 14 + [-(2.0 ** 24)]
+    k[:16, 1] = [1.0] * 14 + [2.0 ** 24, -(2.0 ** 24)]
+    m = O.stored_means_f32(k, 16)
+    assert m.shape == (4, 2) and m[0, 0] == 0.0 and m[0, 1] == 0.875
+    # values whose every partial sum is exact in fp32: the model is the exact mean
+    r = np.random.default_rng(5)
+    ints = r.integers(-2000, 2000, size=(64, 8)) * 2.0 ** -7
+    assert np.array_equal(O.stored_means_f32(ints, 16), O.pool_block(ints, np.zeros(64), 16)[0])
+    # 1-D input (eviction logits) pools the same way as one key column
+    assert np.array_equal(O.stored_means_f32(ints[:, 3], 16), O.stored_means_f32(ints, 16)[:, 3])
+
+
+def test_stored_means_f32_within_the_fp32_summation_bound():
+    # |fl32 token-order mean - exact mean| <= 15 u sum|x| / 16 (15 additions, u = 2^-24;
+    # the product by 1/16 is exact), on values with many significant bits
+    r = np.random.default_rng(6)
+    x = r.standard_normal((64, 32)).astype(np.float32).astype(np.float64) * 2.0 ** r.integers(-6, 6, (64, 32))
+    m32 = O.stored_means_f32(x, 16)
+    exact = O.pool_block(x, np.zeros(64), 16)[0]
+    bound = 15 * 2.0 ** -24 * np.abs(x).reshape(4, 16, 32).sum(axis=1) / 16
+    assert np.all(np.abs(m32 - exact) <= bound)
+    assert np.any(m32 != exact)  # the rounding is really there
+
+
 # --------------------------------------------------------------------------
 # Fused front-end: the packed projection and its split (R21, R22)
 # --------------------------------------------------------------------------
