@@ -25,6 +25,10 @@ checked against this file bit for bit):
   ``q_s = rho * q_{s-1} + eps_s`` in fp64 (a product, then a sum: no fused
   multiply-add), stored as fp64 -> fp32 (RNE) -> dtype.
 * bf16 storage rounds fp32 to nearest even.
+* Real-valued front-end inputs (``hidden_real``, ``proj_weights_real``):
+  normals of the hidden-state and weight streams with head field 1 (the integer
+  inputs use 0), the weights scaled by ``2**-6``, both rounded to bf16; their
+  projections are not exact in fp32, so the order of the additions shows.
 * Front-end inputs (hidden states and the packed projection weights): small
   integers ``(word % 17) - 8`` from word ``j = 0`` of the counter, scaled by
   ``2**-3`` (hidden states, counter ``(5, b, 0, t, 4*i)``) and ``2**-8`` (weights,
@@ -46,6 +50,7 @@ __all__ = [
     "queries", "to_storage", "storage_to_f64", "bf16_bits_to_f64",
     "STREAM_CENTER", "STREAM_KNOISE", "STREAM_VALUE", "STREAM_EVICT", "STREAM_QINNOV",
     "STREAM_HIDDEN", "STREAM_WEIGHT", "small_ints", "hidden", "proj_weights", "hidden_width",
+    "hidden_real", "proj_weights_real",
 ]
 
 _M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
@@ -242,3 +247,21 @@ def proj_weights(w: Workload, D: int | None = None, rows=None) -> np.ndarray:
     r = np.arange(F, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
     col = np.arange(D, dtype=np.int64)[None, :]
     return small_ints(w.seed, STREAM_WEIGHT, 0, 0, r[:, None], col).astype(np.float64) * WEIGHT_SCALE
+
+
+def hidden_real(w: Workload, b: int, t0: int, n: int, D: int | None = None) -> np.ndarray:
+    """Real-valued hidden states of request b, tokens [t0, t0+n): [n][D] fp64, bf16-exact."""
+    D = hidden_width(w) if D is None else D
+    t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
+    col = np.arange(D, dtype=np.int64)[None, :]
+    return bf16_bits_to_f64(to_storage(normals(w.seed, STREAM_HIDDEN, b, 1, t, col), "bf16"))
+
+
+def proj_weights_real(w: Workload, D: int | None = None) -> np.ndarray:
+    """Real-valued packed front-end weights [F][D] fp64, bf16-exact (normals x 2**-6)."""
+    D = hidden_width(w) if D is None else D
+    F = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim + w.n_kv_heads
+    r = np.arange(F, dtype=np.int64)[:, None]
+    col = np.arange(D, dtype=np.int64)[None, :]
+    x = normals(w.seed, STREAM_WEIGHT, 0, 1, r, col) * 2.0 ** -6
+    return bf16_bits_to_f64(to_storage(x, "bf16"))

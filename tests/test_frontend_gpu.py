@@ -21,9 +21,9 @@ from nosa_harness import FrontRun
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, units=None, steps=None, plain_first=0, check_bytes=True):
+def _run(w, units=None, steps=None, plain_first=0, check_bytes=True, real=False):
     steps = w.steps if steps is None else steps
-    run = FrontRun(w, units=units, check_bytes=check_bytes)
+    run = FrontRun(w, units=units, real=real, **({} if real else {"check_bytes": check_bytes}))
     q = synth.gpu.queries(w, plain_first) if plain_first else None
     worst, worst_lse = 0.0, 0.0
     try:
@@ -40,6 +40,8 @@ def _run(w, units=None, steps=None, plain_first=0, check_bytes=True):
     assert st["device_error"] == 0
     assert worst <= 1.0, f"attention error / tolerance = {worst}"
     assert worst_lse <= 1e-3
+    if real:
+        assert run.proj_checked == (steps - plain_first) * len(run.units)
     return st
 
 
@@ -74,6 +76,20 @@ def test_plain_steps_then_hidden_steps():
     # the handle switches from the plain step to the front-end (a new step graph)
     w = synth.WORKLOADS["tiny-f32"].with_(name="tiny-bf16", dtype="bf16", steps=40)
     _run(w, plain_first=12)
+
+
+def test_real_valued_inputs_tiny():
+    # hidden states and weights are bf16 normals: the projection's fp32 sums are
+    # inexact, so q, k, v and e are checked elementwise against the oracle's fp64
+    # projection within the accumulation bound plus one rounding of the stored type
+    w = synth.WORKLOADS["tiny-f32"].with_(name="tiny-bf16", dtype="bf16", steps=40)
+    _run(w, real=True)
+
+
+def test_real_valued_inputs_8b_shape():
+    # hidden 4096 (the bench's shape): 49 row tiles, cluster split-K over the hidden width
+    w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=4, prompt=4096 + 50, steps=24)
+    _run(w, units=[0, 13, 31], real=True)
 
 
 def test_pack_layout():

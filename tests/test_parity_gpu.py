@@ -1,9 +1,12 @@
 """Parity of the CUDA decode path with the fp64 oracle, through the C ABI.
 
 Every step: selections (lock-step near-tie rule), load lists, slot tables and
-gathered bytes exact; attention within 1e-5 absolute (fp32) or 1e-2 x row RMS
-(bf16). The five workloads run at their full shapes; the large ones are checked
-on sampled units (units are independent, so a sampled unit is checked exactly).
+gathered bytes exact; the device state (pooled keys, eviction scores,
+eligibility, query scores, host-store bytes) against the oracle as the harness
+describes; attention within 1e-5 absolute (fp32) or 1e-2 x row RMS (bf16). The
+five workloads run at their full shapes and over their full step counts; the
+large ones are checked on sampled units (units are independent, so a sampled
+unit is checked exactly).
 """
 import numpy as np
 import pytest
@@ -18,10 +21,10 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(w, units=None, steps=None, check_every=1, attn_every=1, pieces=None, check_bytes=True,
-         flags=0):
+         flags=0, state_every=1):
     steps = w.steps if steps is None else steps
     run = GpuRun(w, units=units, flags=flags, prompt_pieces=pieces, check_bytes=check_bytes,
-                 oracle_attention_every=attn_every)
+                 oracle_attention_every=attn_every, state_every=state_every)
     q = synth.gpu.queries(w, steps)
     worst, worst_lse = 0.0, 0.0
     try:
@@ -53,15 +56,23 @@ def test_1b_bf16_sampled_units():
 
 
 def test_3b_bf16_sampled_units():
+    # all 256 decode steps of the workload
     w = synth.WORKLOADS["3b-bf16"]
-    st, _ = _run(w, units=[5, 127], steps=96)
+    st, run = _run(w, units=[5, 127])
+    assert st["steps"] == 256
     assert st["gamma_min"] >= w.k_e / w.k - 1e-12
+    assert st["max_host_loads_unit"] <= w.k - w.k_e
+    assert run.state_checks == 2 * (256 + 1)
 
 
 def test_8b_offload_sampled_units():
+    # all 64 decode steps of the workload, prompt appended in the bench's 4096-token pieces
     w = synth.WORKLOADS["8b-offload-bf16"]
-    st, _ = _run(w, units=[0, 255], steps=24, pieces=[4096] * 16, check_bytes=True)
+    st, run = _run(w, units=[0, 255], pieces=[4096] * 16, check_bytes=True)
+    assert st["steps"] == 64
     assert st["gamma_min"] >= w.k_e / w.k - 1e-12
+    assert st["max_host_loads_unit"] <= w.k - w.k_e
+    assert run.state_checks == 2 * (64 + 1)
 
 
 @pytest.mark.parametrize("case", [
@@ -129,8 +140,9 @@ def test_capacity_and_state_errors():
 @pytest.mark.slow
 def test_8b_longgen_sampled_units_long_horizon():
     # 16384 decode steps: selection, loads and slots checked every step on two
-    # units, attention every 16th step.
+    # units, attention and the device state every 16th step, the host-store bytes
+    # of every block that completes.
     w = synth.WORKLOADS["8b-longgen-bf16"]
-    st, run = _run(w, units=[3, 100], attn_every=16, check_bytes=False)
+    st, run = _run(w, units=[3, 100], attn_every=16, check_bytes=False, state_every=16)
     assert st["gamma_min"] >= w.k_e / w.k - 1e-12
     assert st["max_host_loads_unit"] <= w.k - w.k_e

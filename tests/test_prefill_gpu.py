@@ -20,12 +20,12 @@ from oracle import nosa_oracle as O
 pytestmark = pytest.mark.gpu
 
 
-def _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc=True):
+def _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc=True, env=None):
     """One forward with the tiled tensor-core attention and the tensor-core
-    selection on or off (the switches are read at every call); checks the device
-    error word."""
+    selection on or off (the switches are read at every call; env adds more);
+    checks the device error word."""
     switches = {"NOSA_PREFILL_TILED": "1" if tiled else "0",
-                "NOSA_PREFILL_SELECT_TC": "1" if select_tc else "0"}
+                "NOSA_PREFILL_SELECT_TC": "1" if select_tc else "0", **(env or {})}
     old = {name: os.environ.get(name) for name in switches}
     os.environ.update(switches)
     try:
@@ -40,7 +40,7 @@ def _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc=True):
     torch.cuda.synchronize()
 
 
-def _prefill(w, L, units=None, attn_every=1, tiled=True, select_tc=True):
+def _prefill(w, L, units=None, attn_every=1, tiled=True, select_tc=True, env=None):
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
                            max(L, 1))
     k, v, e = synth.gpu.kv(w, 0, L)
@@ -48,7 +48,7 @@ def _prefill(w, L, units=None, attn_every=1, tiled=True, select_tc=True):
     out = torch.full_like(q, float("nan"))
     lse = torch.full((w.batch, L, w.n_q_heads), float("nan"), dtype=torch.float32, device="cuda")
     sel = torch.empty((w.batch, L, w.n_kv_heads, w.k), dtype=torch.int32, device="cuda")
-    _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc)
+    _forward(cfg, L, q, k, v, e, out, lse, sel, tiled, select_tc, env)
     assert not torch.isnan(out.float()).any(), "an output row was not written"
     assert not torch.isnan(lse).any(), "an lse entry was not written"
     sel_h = sel.cpu().numpy()
@@ -227,3 +227,24 @@ def test_long_sequence_fallback_paths(k, select_tc):
     # shared memory); the tiled attention with 700-block unions
     w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=64, k=k, k_e=4)
     _prefill(w, 64 * 700 + 13, attn_every=97, select_tc=select_tc)
+
+
+@pytest.mark.parametrize("pb", [1, 2])
+@pytest.mark.parametrize("name", ["tiny-f32", "1b-bf16"])
+def test_cuda_core_selection_narrow_passes(pb, name):
+    # The CUDA-core selection scores 8, 4, 2 or 1 positions per warp in one pass
+    # over the pooled keys, the most whose score scratch fits in shared memory;
+    # widths 2 and 1 take over only beyond about 1 200 and 2 400 blocks.
+    # NOSA_PREFILL_SELECT_PB caps the width, so a short sequence runs them.
+    w = synth.WORKLOADS[name].with_(batch=1, k=24, k_e=8)
+    _prefill(w, 64 * 45 + 7, units=[0, w.n_kv_heads - 1] if w.n_kv_heads > 1 else None,
+             attn_every=5, select_tc=False, env={"NOSA_PREFILL_SELECT_PB": str(pb)})
+
+
+@pytest.mark.slow
+def test_cuda_core_selection_two_position_pass_natural():
+    # 1 216 blocks at d = 64: the score scratch of 4 positions per warp no longer
+    # fits, so the CUDA-core selection takes its 2-position passes on its own;
+    # every position's selection is checked, the attention on sampled positions
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=64, k=16, k_e=8)
+    _prefill(w, 64 * 1215 + 9, attn_every=1999, select_tc=False)

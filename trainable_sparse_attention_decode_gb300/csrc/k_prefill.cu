@@ -34,6 +34,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 
 namespace nosa {
 namespace {
@@ -630,9 +631,16 @@ size_t select_smem_bytes(int d, int ke, int nblk, int pb) {
 }
 
 // Positions per warp scored in one pass over the candidates: the most (<= 8,
-// all of a warp's positions) whose score scratch fits in 220 KB.
+// all of a warp's positions) whose score scratch fits in 220 KB. The widths 2
+// and 1 take over beyond about 1 200 and 2 400 blocks; NOSA_PREFILL_SELECT_PB
+// (1, 2, 4 or 8, read at every call) caps the width, which changes how often
+// the pooled keys are streamed, never the result.
 int select_pb(int d, int ke, int nblk) {
   int pb = 8;
+  if (const char* g = std::getenv("NOSA_PREFILL_SELECT_PB")) {
+    const int v = std::atoi(g);
+    if (v == 1 || v == 2 || v == 4) pb = v;
+  }
   while (pb > 1 && select_smem_bytes(d, ke, nblk, pb) > 220 * 1024) pb >>= 1;
   return pb;
 }
