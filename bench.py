@@ -57,6 +57,16 @@ def aggregate(seconds: float, tokens: int, world: int):
     return float(t.item()), int(n.item())
 
 
+def rank_requests(batch: int, world: int, rank: int):
+    """Requests (first, count) of the job's world * batch that rank runs: weak
+    scaling, every rank its own batch of requests, disjoint, covering the job."""
+    import synth
+    if world * batch > synth.MAX_REQUESTS:
+        raise ValueError(f"{world} ranks x {batch} requests exceed the generator's "
+                         f"{synth.MAX_REQUESTS} requests")
+    return rank * batch, batch
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -123,6 +133,16 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(use), "samples_in_timed_region": sum(1 for i, _ in rows if i)}
+
+
+def pct(sorted_vals, q):
+    """q-th percentile (linear interpolation) of an ascending list."""
+    if not sorted_vals:
+        return 0.0
+    x = (len(sorted_vals) - 1) * q / 100.0
+    lo = int(math.floor(x))
+    hi = min(lo + 1, len(sorted_vals) - 1)
+    return sorted_vals[lo] + (sorted_vals[hi] - sorted_vals[lo]) * (x - lo)
 
 
 def gpu_index(local_rank: int) -> int:
@@ -221,11 +241,28 @@ def h2d_peak_gbs(torch, nbytes=1 << 30, reps=5):
     return nbytes / best / 1e9
 
 
-def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20):
+def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20, classic=False):
     """Times the split-K attention kernel alone on the step's shape: every unit
     attends over min(k, N) full blocks plus a tail of tail_len tokens, all block
-    units fresh in HBM (more than L2).
+    units fresh in HBM (more than L2). classic: the classic split the decode step
+    launches (attn_split_kernel; the planner's split count for one launch over
+    every unit: the step launches it per unit chunk), else the standalone call's
+    own plan (stream-K when it fits).
     Returns (seconds per launch, algorithmic bytes per launch)."""
+    saved = os.environ.get("NOSA_ATTN_STREAMK")
+    if classic:
+        os.environ["NOSA_ATTN_STREAMK"] = "0"
+    try:
+        return _attention_alone(nosa, torch, w, n_cand, tail_len, reps)
+    finally:
+        if classic:
+            if saved is None:
+                os.environ.pop("NOSA_ATTN_STREAMK", None)
+            else:
+                os.environ["NOSA_ATTN_STREAMK"] = saved
+
+
+def _attention_alone(nosa, torch, w, n_cand, tail_len, reps):
     # the standalone call uses only the shape fields of the config (k is capped to
     # the decode step's limit for validation; the block table sets the blocks)
     kk = min(w.k, 256)
@@ -259,6 +296,39 @@ def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20):
     return a.elapsed_time(b) / 1e3 / reps, attn_bytes_per_launch(w, n_cand, tail_len)
 
 
+def budget_batch(args, w, mode):
+    """Largest batch whose GPU-resident state fits the HBM budget (--hbm-budget GB).
+
+    fullattn: the whole cache of a request in HBM, every complete block and the
+    tail as block units. nosa / infllmv2: the handle's device state of a request
+    (slot pool, tail buffers, pooled metadata, bitmasks, split-K partials),
+    measured on a 4-request handle; capped so that the pinned host store stays
+    within --host-budget GB."""
+    import torch
+    import trainable_sparse_attention_decode_gb300 as nosa
+    budget = args.hbm_budget * 1e9
+    cfg1 = nosa.nosa_config(1, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                            w.max_context)
+    payload = nosa.nosa_payload_bytes(cfg1)
+    if mode == "fullattn":
+        per_req = w.n_kv_heads * (w.prompt // w.block + 1) * payload
+        return max(1, int(budget // per_req)), per_req, 0
+    probe = 4
+    cfg = nosa.nosa_config(probe, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                           w.max_context)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    h = nosa.nosa_create(cfg)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    nosa.nosa_destroy(h)
+    per_req = (free0 - free1) / probe
+    host_req = w.n_kv_heads * ((w.max_context + w.block - 1) // w.block) * payload
+    b = int(budget // per_req)
+    b = min(b, int(args.host_budget * 1e9 // host_req), 65535 // w.n_kv_heads)
+    return max(1, b), per_req, host_req
+
+
 def run_fullattn(args, rank, world, local_rank):
     """Comparator: dense decode attention with the whole KV cache resident in HBM
     (no selection, no recall), on the same split-K kernel: every unit attends
@@ -271,6 +341,12 @@ def run_fullattn(args, rank, world, local_rank):
     w = synth.WORKLOADS[args.workload]
     if args.batch:
         w = w.with_(batch=args.batch)
+    budget = None
+    if args.hbm_budget:
+        b, per_req, _ = budget_batch(args, w, "fullattn")
+        w = w.with_(batch=b)
+        budget = {"hbm_budget_gb": args.hbm_budget, "hbm_bytes_per_request": per_req,
+                  "batch_from_budget": b}
     n_cand = w.prompt // w.block
     wf = w.with_(k=n_cand)               # attend to every block
     W, K = args.warmup, args.steps
@@ -290,7 +366,7 @@ def run_fullattn(args, rank, world, local_rank):
             "config": {"workload": w.name + "-fullattn", "batch": w.batch,
                        "context": w.prompt, "blocks_per_unit": n_cand,
                        "kv_bytes_in_hbm": w.units * (n_cand + 1) * 33024,
-                       "l2": "inputs larger than L2"},
+                       "l2": "inputs larger than L2", **(budget or {})},
             "roofline": {"bound": "hbm", "kernel": "attn_split_kernel (dense)",
                          "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "traffic": None, "peak_source": kind,
@@ -416,8 +492,20 @@ def run_gpu(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     w0 = synth.WORKLOADS[args.workload]
+    budget = None
+    if args.hbm_budget:
+        wb = w0.with_(k_e=0) if args.mode == "infllmv2" else w0
+        b, per_req, host_req = budget_batch(args, wb.with_(steps=args.warmup + args.steps
+                                                           + args.e2e_steps + args.phase_steps),
+                                            args.mode)
+        args.batch = b
+        budget = {"hbm_budget_gb": args.hbm_budget, "host_budget_gb": args.host_budget,
+                  "hbm_bytes_per_request": round(per_req), "host_bytes_per_request": host_req,
+                  "batch_from_budget": b}
     if args.batch:
         w0 = w0.with_(name=f"{w0.name}-b{args.batch}", batch=args.batch)
+    if world > 1:  # this rank's own requests of the job
+        w0 = w0.with_(request_base=rank_requests(w0.batch, world, rank)[0])
     if args.prompt:
         w0 = w0.with_(name=f"{w0.name}-p{args.prompt}", prompt=args.prompt)
     if args.mode == "infllmv2":
@@ -454,7 +542,7 @@ def run_gpu(args, rank, world, local_rank):
         # the step starts from hidden states: the fused front-end projects them
         Wf = nosa.nosa_frontend_pack(cfg, synth.gpu.proj_weights(w, D))  # packed once
         x_all = synth.gpu.hidden(w, w.prompt, total_steps, D)
-        for s in range(W):
+        def warm_step(s):
             nosa.nosa_decode_step_hidden(h, x_all[s], Wf, out, lse, stream=stream)
         ptrs = [x_all[s].data_ptr() for s in range(total_steps)]
         w_p = Wf.data_ptr()
@@ -469,7 +557,7 @@ def run_gpu(args, rank, world, local_rank):
     else:
         q_all = synth.gpu.queries(w, total_steps)
         k_all, v_all, e_all = synth.gpu.kv(w, w.prompt, total_steps, step_major=True)
-        for s in range(W):
+        def warm_step(s):
             nosa.nosa_decode_step(h, q_all[s], k_all[s], v_all[s], e_all[s], out, lse, stream)
         # raw pointers for the timed loop (shapes were checked by the warm-up calls)
         ptrs = [(q_all[s].data_ptr(), k_all[s].data_ptr(), v_all[s].data_ptr(), e_all[s].data_ptr())
@@ -483,28 +571,42 @@ def run_gpu(args, rank, world, local_rank):
                 raise nosa.NosaError(r, nosa.nosa_last_error(h))
         e2e_hosts = lambda: [x[W + K:W + K + KE].cpu().pin_memory() for x in (q_all, k_all, v_all, e_all)]
         e2e_step = lambda devs, o: nosa.nosa_decode_step(h, *devs, o, None, stream)
+    # Step 0 is the cold start (every slot empty: min(k, N) blocks per unit come
+    # from the host store). It runs with the library's phase events, so its recall
+    # rate is reported on its own; the other warm-up steps follow untimed.
+    torch.cuda.synchronize()
+    nosa.nosa_stats_reset(h)
+    nosa.nosa_set_timing(h, True)
+    warm_step(0)
+    st_cold = nosa.nosa_stats(h)
+    nosa.nosa_set_timing(h, False)
+    for s in range(1, W):
+        warm_step(s)
     torch.cuda.synchronize()
     nosa.nosa_stats_reset(h)
     sampler = ClockSampler(gpu_index(local_rank)) if rank == 0 else None
     time.sleep(0.15 if sampler else 0)
     barrier(world)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event before every timed step (and one after the last): the whole-run
+    # time is first to last, and the per-step times give the median and spread
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     w0t = time.time()
     torch.cuda.nvtx.range_push("timed")
-    ev0.record(stream)
     h0 = time.perf_counter()
-    for s in range(W, W + K):
+    for i, s in enumerate(range(W, W + K)):
+        evs[i].record(stream)
         raw_step(s)
     host_enqueue_us = (time.perf_counter() - h0) / K * 1e6
-    ev1.record(stream)
+    evs[K].record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     w1t = time.time()
     barrier(world)
     if sampler:
         sampler.mark(w0t, w1t)
-    secs = ev0.elapsed_time(ev1) / 1e3
+    secs = evs[0].elapsed_time(evs[K]) / 1e3
+    step_us = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(K)]
     st = nosa.nosa_stats(h)
     context_after = st["context"]
 
@@ -569,8 +671,9 @@ def run_gpu(args, rank, world, local_rank):
     nosa.nosa_destroy(h)
     del ptrs
     n_mid = (w.prompt + W + K // 2) // w.block
-    alone_secs, alone_bytes = attention_alone(nosa, torch, w, n_mid,
-                                              (w.prompt + W + K // 2) % w.block + 1)
+    tail_alone = (w.prompt + W + K // 2) % w.block + 1
+    alone_secs, alone_bytes = attention_alone(nosa, torch, w, n_mid, tail_alone, classic=True)
+    sk_secs, _ = attention_alone(nosa, torch, w, n_mid, tail_alone)
 
     max_secs, tokens = aggregate(secs, w.batch * K, world)
     e2e_max, e2e_tokens = aggregate(e2e_secs, w.batch * KE, world)
@@ -605,13 +708,27 @@ def run_gpu(args, rank, world, local_rank):
     host_bytes_step = st["host_bytes"] / K
     host_bytes_window = st_ph["host_bytes"] / KT if st_ph else 0.0
     recall_gbs = (host_bytes_window / (phase_us["gather"] * 1e-6) / 1e9) if phase_us["gather"] else 0.0
-    # Roofline kernel: the attention, timed alone on the step's shape as one
-    # launch over all the step's blocks (the stream-K split; in the step it
-    # shares the GPU with the gather, which would blur its own bound).
-    dominant = "attn_streamk_kernel (alone, step shape)"
+    # Roofline kernel: the attention kernel the step launches (attn_split_kernel,
+    # the classic split with the step's split count per unit), timed alone on the
+    # step's shape; inside the step it runs at low priority beside the gather and
+    # the scoring, so its in-step rate (attn_kept_in_step_gbs) measures sharing,
+    # not the kernel. The stream-K form of the standalone call is reported apart.
+    dominant = "attn_split_kernel (alone, the step's shape, one launch over every unit)"
     dom_bytes, dom_us = alone_bytes, alone_secs * 1e6
-    traffic = ncu_traffic(w0.name)
+    traffic = ncu_traffic(w0.name, kernel="attn_split_kernel")
     value = tokens / max_secs
+    srt = sorted(step_us)
+    t_step = {"median": round(pct(srt, 50), 3), "p10": round(pct(srt, 10), 3),
+              "p90": round(pct(srt, 90), 3), "mean": round(sum(srt) / len(srt), 3),
+              "tokens_per_s_at_median": round(w.batch / (pct(srt, 50) * 1e-6), 3)}
+    cold_gather_us = st_cold["t_us"][4] / max(st_cold["t_count"], 1)
+    cold = {"step_us": round(st_cold["t_us"][7] / max(st_cold["t_count"], 1), 3),
+            "host_bytes": st_cold["host_bytes"],
+            "gather_us": round(cold_gather_us, 3),
+            "recall_h2d_gbs": round(st_cold["host_bytes"] / (cold_gather_us * 1e-6) / 1e9, 2)
+            if cold_gather_us > 0 else None}
+    if peak_h2d and cold["recall_h2d_gbs"]:
+        cold["recall_frac_of_h2d_peak"] = round(cold["recall_h2d_gbs"] / peak_h2d, 4)
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -633,7 +750,8 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (slot pool %.0f MiB, pooled keys %.0f MiB > %d MiB)"
                          % (w.units * w.k * 33024 / 2 ** 20,
                             w.units * n_cand * 4 * w.head_dim * 4 / 2 ** 20, L2_BYTES >> 20),
-                   "parallelism": f"replicas x{world} (independent requests per GPU)"},
+                   "parallelism": f"replicas x{world} (independent requests per GPU)",
+                   **(budget or {})},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(dom_bytes / (dom_us * 1e-6) / 1e9, 1),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(dom_bytes / (dom_us * 1e-6) / 1e9 / peak, 4),
@@ -642,6 +760,10 @@ def run_gpu(args, rank, world, local_rank):
         "attn_hbm_gbs": round(dom_bytes / (dom_us * 1e-6) / 1e9, 1),
         "attn_frac_of_peak": round(dom_bytes / (dom_us * 1e-6) / 1e9 / peak, 4),
         "attn_kept_in_step_gbs": round(attn_gbs, 1),
+        "attn_streamk_alone": {"kernel": "attn_streamk_kernel (the standalone call's plan)",
+                               "us": round(sk_secs * 1e6, 2),
+                               "gbs": round(alone_bytes / sk_secs / 1e9, 1),
+                               "frac_of_peak": round(alone_bytes / sk_secs / 1e9 / peak, 4)},
         **({"frontend": {"hidden": D, "rows": (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim
                          + w.n_kv_heads,
                          "kernel_us": round(phase_us["append_pool"], 3),
@@ -657,6 +779,8 @@ def run_gpu(args, rank, world, local_rank):
         "recall_frac_of_h2d_peak": round(recall_gbs / peak_h2d, 4) if peak_h2d else None,
         "host_bytes_per_step": round(host_bytes_step),
         "phase_us": {k_: round(v_, 3) for k_, v_ in phase_us.items()},
+        "t_step_us": t_step,
+        "cold_step": cold,
         "gamma_mean": round(st["gamma_mean"], 4), "gamma_min": st["gamma_min"],
         "near_ties": st["near_ties"],
         "e2e": {"value": round(e2e_tokens / e2e_max, 3), "unit": "tokens/s",
@@ -673,84 +797,223 @@ def run_gpu(args, rank, world, local_rank):
     return line
 
 
+def run_horizon(args, rank, world, local_rank):
+    """The workload's whole decode horizon (every step of `steps`), graph-replayed
+    back to back; `args.horizon` windows of `window` steps, spread from the first
+    warm step to the last, are timed with an event before every step and their
+    counters read (host loads, locality). Reports each window's median step time,
+    tokens/s, host bytes per step and the recall rate those bytes need."""
+    import torch
+    import synth
+    import synth.gpu
+    import trainable_sparse_attention_decode_gb300 as nosa
+    torch.cuda.set_device(local_rank)
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(batch=args.batch)
+    n = w.steps
+    win = max(16, min(256, n // (2 * args.horizon)))
+    starts = [1 + round(i * (n - 1 - win) / max(1, args.horizon - 1)) for i in range(args.horizon)]
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                           w.max_context, device=local_rank)
+    h = nosa.nosa_create(cfg)
+    t = 0
+    while t < w.prompt:
+        m = min(4096, w.prompt - t)
+        k, v, e = synth.gpu.kv(w, t, m)
+        nosa.nosa_append_kv(h, k, v, e)
+        t += m
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
+    stream = torch.cuda.current_stream()
+    q_all = synth.gpu.queries(w, n)
+    k_all, v_all, e_all = synth.gpu.kv(w, w.prompt, n, step_major=True)
+    peak_h2d = h2d_peak_gbs(torch)
+    step_fn = nosa.lib.nosa_decode_step
+    out_p, s_p = out.data_ptr(), stream.cuda_stream
+    ptrs = [(q_all[s].data_ptr(), k_all[s].data_ptr(), v_all[s].data_ptr(), e_all[s].data_ptr())
+            for s in range(n)]
+    windows = []
+    s = 0
+    torch.cuda.synchronize()
+    t_wall = time.time()
+    for w0s in starts + [n]:
+        while s < w0s:  # untimed steps up to the window
+            p_ = ptrs[s]
+            if step_fn(h, p_[0], p_[1], p_[2], p_[3], out_p, None, s_p):
+                raise nosa.NosaError(0, nosa.nosa_last_error(h))
+            s += 1
+        if w0s == n:
+            break
+        nosa.nosa_stats_reset(h)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(win + 1)]
+        for i in range(win):
+            evs[i].record(stream)
+            p_ = ptrs[s]
+            if step_fn(h, p_[0], p_[1], p_[2], p_[3], out_p, None, s_p):
+                raise nosa.NosaError(0, nosa.nosa_last_error(h))
+            s += 1
+        evs[win].record(stream)
+        st = nosa.nosa_stats(h)
+        us = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(win))
+        med = pct(us, 50)
+        hb = st["host_bytes"] / win
+        windows.append({"steps": [w0s, w0s + win], "context": [w.prompt + w0s + 1, w.prompt + w0s + win],
+                        "t_step_us_median": round(med, 2), "t_step_us_p10": round(pct(us, 10), 2),
+                        "t_step_us_p90": round(pct(us, 90), 2),
+                        "tokens_per_s": round(w.batch / (med * 1e-6), 1),
+                        "host_bytes_per_step": round(hb),
+                        "link_time_frac": round(hb / (peak_h2d * 1e9) / (med * 1e-6), 4),
+                        "gamma_mean": round(st["gamma_mean"], 4), "gamma_min": st["gamma_min"],
+                        "max_host_loads_unit": st["max_host_loads_unit"]})
+    wall = time.time() - t_wall
+    nosa.nosa_destroy(h)
+    if rank != 0:
+        return None
+    return {"metric": METRIC, "mode": "horizon", "unit": "tokens/s", "n_gpus": world,
+            "config": {"workload": w.name, "batch": w.batch, "steps": n, "window_steps": win,
+                       "context_start": w.prompt, "context_end": w.prompt + n},
+            "h2d_peak_gbs": round(peak_h2d, 2), "windows": windows, "wall_s": round(wall, 1),
+            "note": "link_time_frac = host bytes per step / measured pinned-copy peak / median "
+                    "step time: the share of a step the recall alone needs on the host link"}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_step_rate(workload: str, units, steps: int, warm: int = 1):
-    """Seconds per (unit, decode step) of the fp64 oracle, steady state."""
+def _oracle_proc(workload, units, warm, steps, batch, barrier, out_q):
+    """One process of the oracle pool: builds its units (prompt appended, the
+    step inputs generated), runs `warm` untimed decode steps, waits for the other
+    processes, then times `steps` decode steps of all its units in lock-step."""
     import synth
     from oracle import nosa_oracle as O
-    w = synth.WORKLOADS[workload]
-    w = w.with_(steps=max(w.steps, warm + steps))
-    per = []
-    for u in units:
-        b, h = divmod(u, w.n_kv_heads)
-        uo = O.UnitOracle(w.head_dim, w.dtype, w.k, w.k_e, w.max_context, w.block, w.sub_block)
-        uo.append(synth.keys(w, b, h, 0, w.prompt), synth.values(w, b, h, 0, w.prompt),
-                  synth.evict(w, b, h, 0, w.prompt))
+    try:
+        w = synth.WORKLOADS[workload]
+        if batch:
+            w = w.with_(batch=batch)
+        w = w.with_(steps=max(w.steps, warm + steps))
         G = w.group
-        q = synth.queries(w, b, range(h * G, (h + 1) * G), warm + steps)
-        toks = [(synth.keys(w, b, h, w.prompt + s, 1)[0], synth.values(w, b, h, w.prompt + s, 1)[0],
-                 synth.evict(w, b, h, w.prompt + s, 1)[0]) for s in range(warm + steps)]
+        state = []
+        for u in units:
+            b, h = divmod(u, w.n_kv_heads)
+            uo = O.UnitOracle(w.head_dim, w.dtype, w.k, w.k_e, w.max_context, w.block, w.sub_block)
+            uo.append(synth.keys(w, b, h, 0, w.prompt), synth.values(w, b, h, 0, w.prompt),
+                      synth.evict(w, b, h, 0, w.prompt))
+            q = synth.queries(w, b, range(h * G, (h + 1) * G), warm + steps)
+            kk = synth.keys(w, b, h, w.prompt, warm + steps)
+            vv = synth.values(w, b, h, w.prompt, warm + steps)
+            ee = synth.evict(w, b, h, w.prompt, warm + steps)
+            state.append((uo, q, kk, vv, ee))
         for s in range(warm):
-            uo.decode_step(q[s], *toks[s])
+            for uo, q, kk, vv, ee in state:
+                uo.decode_step(q[s], kk[s], vv[s], ee[s])
+        barrier.wait()
         t0 = time.perf_counter()
         for s in range(warm, warm + steps):
-            uo.decode_step(q[s], *toks[s])
-        per.append((time.perf_counter() - t0) / steps)
-    return statistics.mean(per)
+            for uo, q, kk, vv, ee in state:
+                uo.decode_step(q[s], kk[s], vv[s], ee[s])
+        out_q.put(("ok", time.perf_counter() - t0))
+    except Exception as exc:  # reported to the parent, which prints the reason
+        out_q.put(("error", repr(exc)))
+        try:
+            barrier.abort()
+        except Exception:
+            pass
 
 
-def cpu_baseline(workload: str, units=(0, 1), steps=6):
-    """Runs the oracle in a single-threaded child process (BLAS pinned to one thread)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", workload,
-           ",".join(map(str, units)), str(steps)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1200)
-    if r.returncode != 0:
-        return None
-    sec = float(r.stdout.strip().splitlines()[-1])
+def oracle_timing(workload, units, warm, steps, batch=0, procs=None):
+    """Times the fp64 oracle on the host cores: `units` split over `procs` spawned
+    processes (default: every core; BLAS pinned to one thread each), `warm`
+    untimed steps, then `steps` timed ones. Returns (seconds of the timed steps,
+    the slowest process; processes used)."""
+    import multiprocessing as mp
+    procs = min(procs or os.cpu_count() or 1, len(units))
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                            "MKL_NUM_THREADS")}
+    os.environ.update({k: "1" for k in saved})
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    out_q = ctx.Queue()
+    ps = [ctx.Process(target=_oracle_proc,
+                      args=(workload, units[i::procs], warm, steps, batch, barrier, out_q))
+          for i in range(procs)]
+    try:
+        for p_ in ps:
+            p_.start()
+        res = [out_q.get(timeout=3000) for _ in ps]
+    finally:
+        for p_ in ps:
+            p_.join(timeout=60)
+            if p_.is_alive():
+                p_.kill()
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    errs = [r[1] for r in res if r[0] != "ok"]
+    if errs:
+        raise RuntimeError("oracle process failed: " + errs[0])
+    return max(r[1] for r in res), procs
+
+
+def cpu_baseline(workload, batch=0, n_units=64, steps=20):
+    """The oracle on all host cores over a bounded sample of the workload's units
+    (spread over the batch), scaled to the whole batch."""
     import synth
     w = synth.WORKLOADS[workload]
-    return {"value": round(w.batch / (sec * w.units), 4), "unit": "tokens/s", "cores": 1,
+    if batch:
+        w = w.with_(batch=batch)
+    n_units = min(n_units, w.units)
+    units = [i * w.units // n_units for i in range(n_units)]
+    try:
+        secs, procs = oracle_timing(workload, units, 1, steps, batch)
+    except Exception as exc:
+        return {"value": None, "unit": "tokens/s", "kind": "oracle", "error": str(exc)[:200]}
+    per_step_batch = secs / steps * w.units / n_units
+    return {"value": round(w.batch / per_step_batch, 4), "unit": "tokens/s", "cores": procs,
             "kind": "oracle",
-            "sample": f"{len(units)} of {w.units} units x {steps} decode steps (after 1 warm step), "
-                      f"scaled to the full batch; fp64 numpy, one thread"}
+            "sample": f"{n_units} of {w.units} units x {steps} decode steps (after 1 untimed step), "
+                      f"{procs} processes (one per core, BLAS one thread each), scaled to the full "
+                      f"batch; fp64 numpy"}
 
 
 def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle times the whole batch of the workload on
+    every host core: W untimed decode steps (the first is the cold step), then
+    exactly K timed ones; rank 0 only."""
     if rank != 0:
         return None
     import synth
     w = synth.WORKLOADS[args.workload]
-    units = [0] if args.steps > 4 else [0, 1]
-    steps_per = max(1, min(args.steps, 40))
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker", args.workload,
-           ",".join(map(str, units)), str(steps_per)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=3000)
-    if r.returncode != 0:
-        return {"impl": "reference", "unavailable": "oracle worker failed: " + r.stderr[-200:]}
-    sec = float(r.stdout.strip().splitlines()[-1])
-    value = w.batch / (sec * w.units)
+    if args.batch:
+        w = w.with_(batch=args.batch)
+    K, W = args.steps, args.warmup
+    units = list(range(w.units))
+    t0 = time.time()
+    try:
+        secs, procs = oracle_timing(args.workload, units, W, K, args.batch)
+    except Exception as exc:
+        return {"impl": "reference", "unavailable": "oracle pool failed: " + str(exc)[:200]}
+    wall = time.time() - t0
+    value = w.batch * K / secs
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(sec * w.units * 1e3, 3), "higher_is_better": True,
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(secs / K * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "context_start": w.prompt},
-            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
+            "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k,
+                       "k_e": w.k_e, "context_start": w.prompt},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": procs,
                              "kind": "oracle",
-                             "sample": f"{len(units)} unit(s) x {steps_per} steps per timed pass, "
-                                       "scaled to the full batch"},
+                             "sample": f"the whole batch ({w.units} units) x {K} timed decode "
+                                       f"steps after {W} untimed, {procs} processes"},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+                    "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
 
 
 def main():
-    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-worker":
-        wl, units, steps = sys.argv[2], [int(x) for x in sys.argv[3].split(",")], int(sys.argv[4])
-        print(oracle_step_rate(wl, units, steps))
-        return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -776,6 +1039,14 @@ def main():
     ap.add_argument("--phase-steps", type=int, default=64,
                     help="decode steps of the per-phase timing window (after the timed loops)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
+    ap.add_argument("--hbm-budget", type=float, default=0.0,
+                    help="GB of HBM for the GPU-resident state: the batch is the largest that "
+                         "fits (fullattn: the whole cache; nosa/infllmv2: the handle's state)")
+    ap.add_argument("--host-budget", type=float, default=96.0,
+                    help="GB of pinned host memory the host store may take (with --hbm-budget)")
+    ap.add_argument("--horizon", type=int, default=0,
+                    help="run the workload's whole decode horizon and report this many "
+                         "windows along it (tokens/s, recall, locality)")
     ap.add_argument("--prompt", type=int, default=0, help="override the workload's prompt")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -814,6 +1085,11 @@ def main():
                           "gbs": round(nbytes / secs / 1e9, 1),
                           "frac_of_" + kind + "_peak": round(nbytes / secs / 1e9 / peak, 4)}))
         return
+    if args.horizon:
+        line = run_horizon(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.mode in ("fullattn", "prefill"):
         line = (run_fullattn if args.mode == "fullattn" else run_prefill)(args, rank, world,
                                                                            local_rank)
@@ -823,7 +1099,7 @@ def main():
     line = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(args.workload)
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.batch)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -18,6 +18,8 @@ checked against this file bit for bit):
   ``(sum - 393210) / 65536``. Mean 0, variance 1 - 2**-32, support (-6, 6).
   Every value is a multiple of 2**-16 below 2**3, so it is exact in fp32 and
   fp64 on any machine; no transcendental function is involved.
+* The request field is the request's index in the job: a workload's request b is
+  ``request_base + b`` (ranks of a multi-GPU job run disjoint requests).
 * Keys: ``k = c[b, h, block(t)] + 0.5 * n[b, h, t]``, one centre ``c`` per
   (request, KV head, 64-token block) and i.i.d. noise ``n``; exact in fp32.
 * Values ``v ~ N(0, 1)``; eviction logits ``e ~ N(0, 1)`` (fp32, fixed at write).
@@ -50,7 +52,7 @@ __all__ = [
     "queries", "to_storage", "storage_to_f64", "bf16_bits_to_f64",
     "STREAM_CENTER", "STREAM_KNOISE", "STREAM_VALUE", "STREAM_EVICT", "STREAM_QINNOV",
     "STREAM_HIDDEN", "STREAM_WEIGHT", "small_ints", "hidden", "proj_weights", "hidden_width",
-    "hidden_real", "proj_weights_real",
+    "hidden_real", "proj_weights_real", "MAX_REQUESTS",
 ]
 
 _M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
@@ -89,6 +91,7 @@ class Workload:
     block: int = 64
     sub_block: int = 16
     seed: int = 0
+    request_base: int = 0  # index of request 0 in the job (ranks of a multi-GPU job shard requests)
 
     @property
     def group(self) -> int:
@@ -176,10 +179,22 @@ def storage_to_f64(s: np.ndarray, dtype: str) -> np.ndarray:
     return bf16_bits_to_f64(np.asarray(s, dtype=np.uint16))
 
 
+MAX_REQUESTS = 1 << 10  # the counter's request field
+
+
+def _req(w: Workload, b) -> int:
+    """Request index in the job of the workload's request b (the counter field)."""
+    a = w.request_base + int(b)
+    if not 0 <= a < MAX_REQUESTS:
+        raise ValueError(f"request {a} outside the generator's {MAX_REQUESTS} requests")
+    return a
+
+
 def keys(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
     """Stored keys of tokens [t0, t0+n) of (request b, KV head h): [n][d] storage dtype."""
     t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
     dim = np.arange(w.head_dim, dtype=np.int64)[None, :]
+    b = _req(w, b)
     c = normals(w.seed, STREAM_CENTER, b, h, t // w.block, dim)
     noise = normals(w.seed, STREAM_KNOISE, b, h, t, dim)
     return to_storage(c + 0.5 * noise, w.dtype)
@@ -188,13 +203,13 @@ def keys(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
 def values(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
     t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
     dim = np.arange(w.head_dim, dtype=np.int64)[None, :]
-    return to_storage(normals(w.seed, STREAM_VALUE, b, h, t, dim), w.dtype)
+    return to_storage(normals(w.seed, STREAM_VALUE, _req(w, b), h, t, dim), w.dtype)
 
 
 def evict(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
     """Per-token eviction logits of (b, KV head h): [n] fp32."""
     t = np.arange(t0, t0 + n, dtype=np.int64)
-    return normals(w.seed, STREAM_EVICT, b, h, t, 0).astype(np.float32)
+    return normals(w.seed, STREAM_EVICT, _req(w, b), h, t, 0).astype(np.float32)
 
 
 def queries(w: Workload, b: int, heads, steps: int) -> np.ndarray:
@@ -204,8 +219,9 @@ def queries(w: Workload, b: int, heads, steps: int) -> np.ndarray:
     out = np.empty((steps, len(heads), w.head_dim),
                    dtype=np.float32 if w.dtype == "f32" else np.uint16)
     q = None
+    a = _req(w, b)
     for s in range(steps):
-        eps = normals(w.seed, STREAM_QINNOV, b, heads[:, None], s, dim)
+        eps = normals(w.seed, STREAM_QINNOV, a, heads[:, None], s, dim)
         if q is None:
             q = eps
         else:
@@ -233,7 +249,7 @@ def hidden(w: Workload, b: int, t0: int, n: int, D: int | None = None) -> np.nda
     D = hidden_width(w) if D is None else D
     t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
     col = np.arange(D, dtype=np.int64)[None, :]
-    return small_ints(w.seed, STREAM_HIDDEN, b, 0, t, col).astype(np.float64) * HIDDEN_SCALE
+    return small_ints(w.seed, STREAM_HIDDEN, _req(w, b), 0, t, col).astype(np.float64) * HIDDEN_SCALE
 
 
 def proj_weights(w: Workload, D: int | None = None, rows=None) -> np.ndarray:
@@ -254,7 +270,7 @@ def hidden_real(w: Workload, b: int, t0: int, n: int, D: int | None = None) -> n
     D = hidden_width(w) if D is None else D
     t = np.arange(t0, t0 + n, dtype=np.int64)[:, None]
     col = np.arange(D, dtype=np.int64)[None, :]
-    return bf16_bits_to_f64(to_storage(normals(w.seed, STREAM_HIDDEN, b, 1, t, col), "bf16"))
+    return bf16_bits_to_f64(to_storage(normals(w.seed, STREAM_HIDDEN, _req(w, b), 1, t, col), "bf16"))
 
 
 def proj_weights_real(w: Workload, D: int | None = None) -> np.ndarray:

@@ -38,7 +38,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 store_as<__nv_bfloat16>(dou
 // (token-major [n][batch][Hkv][d] and [n][batch][Hkv] when step_major).
 template <typename T>
 __global__ void kv_kernel(T* k, T* v, float* e, int batch, int hkv, int d, long long t0, int n,
-                          int block, uint64_t smix, int step_major) {
+                          int block, uint64_t smix, int step_major, int b0) {
   const long long total = (long long)batch * n * hkv * d;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -55,6 +55,7 @@ __global__ void kv_kernel(T* k, T* v, float* e, int batch, int hkv, int d, long 
       t = t0 + r % n;
       b = (int)(r / n);
     }
+    b += b0;  // request index in the job (a rank's requests start at b0)
     const double c = ih_normal(smix, 0, b, h, t / block, dim);
     const double nz = ih_normal(smix, 1, b, h, t, dim);
     k[i] = store_as<T>(c + 0.5 * nz);
@@ -65,11 +66,12 @@ __global__ void kv_kernel(T* k, T* v, float* e, int batch, int hkv, int d, long 
 
 // q: [steps][batch][hq][d], AR(1) over steps, fp64 state (no fused multiply-add).
 template <typename T>
-__global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, uint64_t smix) {
+__global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, uint64_t smix,
+                         int b0) {
   const int total = batch * hq * d;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= total) return;
-  const int dim = i % d, g = (i / d) % hq, b = i / (d * hq);
+  const int dim = i % d, g = (i / d) % hq, b = b0 + i / (d * hq);
   double x = 0.0;
   for (int s = 0; s < steps; ++s) {
     const double eps = ih_normal(smix, 4, b, g, s, dim);
@@ -87,13 +89,13 @@ __device__ __forceinline__ int small_int(uint64_t smix, uint64_t stream, uint64_
 
 // x: [n][batch][D] bf16 hidden states of tokens t0 .. t0+n-1 (integers x 2^-3).
 __global__ void hidden_kernel(__nv_bfloat16* x, int batch, int D, long long t0, int n,
-                              uint64_t smix) {
+                              uint64_t smix, int b0) {
   const long long total = (long long)n * batch * D;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int col = (int)(i % D);
     const long long r = i / D;
-    const int b = (int)(r % batch);
+    const int b = b0 + (int)(r % batch);
     const long long t = t0 + r / batch;
     x[i] = __float2bfloat16_rn((float)small_int(smix, 5, b, 0, t, col) * 0.125f);
   }
@@ -122,8 +124,9 @@ uint64_t seed_mix(uint64_t seed) {
 extern "C" {
 
 // dtype 0 = fp32, 1 = bf16. Returns a cudaError_t.
+// b0: index of the first request (requests b0 .. b0 + batch - 1 of the job).
 int synth_kv(void* k, void* v, float* e, int batch, int hkv, int d, long long t0, int n,
-             int block, unsigned long long seed, int dtype, int step_major, void* stream) {
+             int block, unsigned long long seed, int dtype, int step_major, int b0, void* stream) {
   const uint64_t smix = seed_mix(seed);
   const long long total = (long long)batch * n * hkv * d;
   const int threads = 256;
@@ -133,34 +136,36 @@ int synth_kv(void* k, void* v, float* e, int batch, int hkv, int d, long long t0
   if (total == 0) return 0;
   if (dtype == 0)
     kv_kernel<float><<<grid, threads, 0, s>>>((float*)k, (float*)v, e, batch, hkv, d, t0, n,
-                                               block, smix, step_major);
+                                               block, smix, step_major, b0);
   else
     kv_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>((__nv_bfloat16*)k, (__nv_bfloat16*)v, e,
-                                                       batch, hkv, d, t0, n, block, smix, step_major);
+                                                       batch, hkv, d, t0, n, block, smix, step_major,
+                                                       b0);
   return (int)cudaGetLastError();
 }
 
 int synth_queries(void* q, int batch, int hq, int d, int steps, double rho,
-                  unsigned long long seed, int dtype, void* stream) {
+                  unsigned long long seed, int dtype, int b0, void* stream) {
   const uint64_t smix = seed_mix(seed);
   const int total = batch * hq * d;
   cudaStream_t s = (cudaStream_t)stream;
   if (total == 0 || steps == 0) return 0;
   if (dtype == 0)
-    q_kernel<float><<<(total + 127) / 128, 128, 0, s>>>((float*)q, batch, hq, d, steps, rho, smix);
+    q_kernel<float><<<(total + 127) / 128, 128, 0, s>>>((float*)q, batch, hq, d, steps, rho, smix,
+                                                         b0);
   else
     q_kernel<__nv_bfloat16><<<(total + 127) / 128, 128, 0, s>>>((__nv_bfloat16*)q, batch, hq, d,
-                                                                 steps, rho, smix);
+                                                                 steps, rho, smix, b0);
   return (int)cudaGetLastError();
 }
 
 int synth_hidden(void* x, int batch, int D, long long t0, int n, unsigned long long seed,
-                 void* stream) {
+                 int b0, void* stream) {
   const long long total = (long long)n * batch * D;
   if (total == 0) return 0;
   const long long want = (total + 255) / 256;
   hidden_kernel<<<(int)(want < 65536 ? want : 65536), 256, 0, (cudaStream_t)stream>>>(
-      (__nv_bfloat16*)x, batch, D, t0, n, seed_mix(seed));
+      (__nv_bfloat16*)x, batch, D, t0, n, seed_mix(seed), b0);
   return (int)cudaGetLastError();
 }
 

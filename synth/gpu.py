@@ -40,15 +40,15 @@ def _get():
         L.synth_kv.restype = C.c_int
         L.synth_kv.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                C.c_longlong, C.c_int, C.c_int, C.c_ulonglong, C.c_int, C.c_int,
-                               C.c_void_p]
+                               C.c_int, C.c_void_p]
         L.synth_hidden.restype = C.c_int
         L.synth_hidden.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_longlong, C.c_int,
-                                   C.c_ulonglong, C.c_void_p]
+                                   C.c_ulonglong, C.c_int, C.c_void_p]
         L.synth_proj_weights.restype = C.c_int
         L.synth_proj_weights.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_ulonglong, C.c_void_p]
         L.synth_queries.restype = C.c_int
         L.synth_queries.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double,
-                                    C.c_ulonglong, C.c_int, C.c_void_p]
+                                    C.c_ulonglong, C.c_int, C.c_int, C.c_void_p]
         _lib = L
     return _lib
 
@@ -75,7 +75,8 @@ def kv(w: Workload, t0: int, n: int, device="cuda", step_major=False):
     e = torch.empty(shp[:3], dtype=torch.float32, device=device)
     err = _get().synth_kv(k.data_ptr(), v.data_ptr(), e.data_ptr(), w.batch, w.n_kv_heads,
                           w.head_dim, t0, n, w.block, w.seed, 0 if w.dtype == "f32" else 1,
-                          1 if step_major else 0, torch.cuda.current_stream().cuda_stream)
+                          1 if step_major else 0, w.request_base,
+                          torch.cuda.current_stream().cuda_stream)
     if err:
         raise RuntimeError(f"synth_kv: CUDA error {err}")
     return k, v, e
@@ -86,7 +87,7 @@ def queries(w: Workload, steps: int, device="cuda"):
     import torch
     q = torch.empty((steps, w.batch, w.n_q_heads, w.head_dim), dtype=_torch_dtype(w), device=device)
     err = _get().synth_queries(q.data_ptr(), w.batch, w.n_q_heads, w.head_dim, steps, w.rho,
-                               w.seed, 0 if w.dtype == "f32" else 1,
+                               w.seed, 0 if w.dtype == "f32" else 1, w.request_base,
                                torch.cuda.current_stream().cuda_stream)
     if err:
         raise RuntimeError(f"synth_queries: CUDA error {err}")
@@ -99,7 +100,7 @@ def hidden(w: Workload, t0: int, n: int, D: int | None = None, device="cuda"):
     from . import hidden_width
     D = hidden_width(w) if D is None else D
     x = torch.empty((n, w.batch, D), dtype=torch.bfloat16, device=device)
-    err = _get().synth_hidden(x.data_ptr(), w.batch, D, t0, n, w.seed,
+    err = _get().synth_hidden(x.data_ptr(), w.batch, D, t0, n, w.seed, w.request_base,
                               torch.cuda.current_stream().cuda_stream)
     if err:
         raise RuntimeError(f"synth_hidden: CUDA error {err}")

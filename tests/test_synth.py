@@ -66,3 +66,14 @@ def test_queries_ar1():
                                        np.arange(64)[None, :])
     assert np.array_equal(q[5], qq.astype(np.float32))
     assert eps5.shape == (4, 64)
+
+
+def test_request_base_offsets_the_request_field():
+    w = synth.WORKLOADS["1b-bf16"]
+    ws = w.with_(request_base=8)
+    # request b of a rank whose requests start at 8 is request 8 + b of the job
+    assert np.array_equal(synth.keys(ws, 0, 3, 50, 9), synth.keys(w, 8, 3, 50, 9))
+    assert np.array_equal(synth.evict(ws, 2, 1, 7, 5), synth.evict(w, 10, 1, 7, 5))
+    assert np.array_equal(synth.queries(ws, 1, [0, 2], 4), synth.queries(w, 9, [0, 2], 4))
+    with pytest.raises(ValueError):
+        synth.keys(w.with_(request_base=synth.MAX_REQUESTS - 1), 1, 0, 0, 1)

@@ -48,3 +48,21 @@ def test_frontend_inputs_match_numpy(name):
         assert np.array_equal(_np(x[:, b]), ref)
     rows = np.array([0, 1, 777, W.shape[0] - 1])
     assert np.array_equal(_np(W[rows]), synth.to_storage(synth.proj_weights(w, D, rows), "bf16"))
+
+
+@pytest.mark.parametrize("base", [32, 992])
+def test_request_base_shards_the_job(base):
+    # a rank's requests start at request_base: both generators agree there, and
+    # the values differ from those of the job's first requests
+    w = synth.WORKLOADS["8b-offload-bf16"].with_(request_base=base)
+    w0 = synth.WORKLOADS["8b-offload-bf16"]
+    k, v, e = synth.gpu.kv(w, 100, 70)
+    q = synth.gpu.queries(w, 5)
+    x = synth.gpu.hidden(w, 100, 2)
+    for b, h in [(0, 0), (w.batch - 1, w.n_kv_heads - 1)]:
+        assert np.array_equal(_np(k[b, :, h]), synth.keys(w, b, h, 100, 70))
+        assert np.array_equal(_np(v[b, :, h]), synth.values(w, b, h, 100, 70))
+        assert np.array_equal(_np(e[b, :, h]), synth.evict(w, b, h, 100, 70))
+        assert np.array_equal(_np(q[:, b, [0, 5]]), synth.queries(w, b, [0, 5], 5))
+        assert np.array_equal(_np(x[:, b]), synth.to_storage(synth.hidden(w, b, 100, 2), "bf16"))
+        assert not np.array_equal(synth.keys(w, b, h, 100, 70), synth.keys(w0, b, h, 100, 70))
