@@ -282,7 +282,7 @@ typedef struct {
   int64_t near_ties;             /* top-k cuts whose k-th and (k+1)-th fp32 scores
                                     differ by < 1e-5 * max |score|                  */
   int32_t device_error;          /* nonzero: a bounded wait in a kernel gave up     */
-  int32_t pad_;
+  int32_t host_numa_node;        /* NUMA node the host store is bound to, -1: none  */
   /* Accumulated device time (microseconds) of each phase when NOSA_FLAG_TIMING.
    * The step is pipelined over chunks of units on internal streams, so the
    * phases overlap; each entry spans a phase's first start to its last end:
@@ -295,6 +295,23 @@ typedef struct {
   int64_t t_count;
   int64_t launches;              /* kernels launched by decode steps (host count)    */
 } nosa_stats_t;
+
+/*
+ * Placement rule of the pinned host store (no counterpart in the NOSA pages; a
+ * property of this implementation). The recall reads the store over the GPU's
+ * host link, so on a host with several memory nodes nosa_create binds the
+ * store's pages (preferred policy) to the GPU's own node before pinning them.
+ * This pure function is the rule: it returns gpu_node when at least two nodes
+ * with CPUs and memory exist (mem_nodes, n_mem), gpu_node is one of them and
+ * the process may allocate on it (allowed, n_allowed); else -1 (nothing bound:
+ * a plain pinned allocation). nosa_create feeds it the GPU's node from sysfs
+ * (/sys/bus/pci/devices/<bus id>/numa_node), the nodes of
+ * /sys/devices/system/node/has_memory that have CPUs, and Mems_allowed_list of
+ * /proc/self/status; nosa_stats reports the outcome (host_numa_node). No GPU
+ * is touched; NULL arrays return -1.
+ */
+int32_t nosa_numa_choose(int32_t gpu_node, const int32_t* mem_nodes, int32_t n_mem,
+                         const int32_t* allowed, int32_t n_allowed);
 
 /* Synchronises the handle's last stream and fills *out. */
 nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out);
@@ -327,11 +344,19 @@ nosa_status nosa_set_timing(nosa_handle* h, int32_t on);
  *   NOSA_DBG_SLOTPOOL bytes [U][k][payload]  slot pool
  *   NOSA_DBG_HOST     bytes [U][maxBlk][payload] host store
  *   NOSA_DBG_TAIL     bytes [U][2][payload] tail buffers (block b uses buffer b % 2)
+ *   NOSA_DBG_TRACE    uint64 [48][2] step trace of the last decode step: per traced
+ *                     launch, the first CTA's start and the last CTA's end on the
+ *                     device's global timer (ns; start UINT64_MAX = not run); slot 0
+ *                     the append, 1 + c scoring (and selection) of unit chunk c,
+ *                     9 + c a separate selection, 17 + c the gather, 25 + c the
+ *                     attention over kept slots, 33 + c over filled slots. Present
+ *                     (size > 0) only when the environment variable NOSA_TRACE=1 was
+ *                     set at nosa_create; the records cost a few atomics per CTA.
  */
 enum {
   NOSA_DBG_SEL = 0, NOSA_DBG_NSEL, NOSA_DBG_ELIG, NOSA_DBG_SLOTS, NOSA_DBG_LOADS,
   NOSA_DBG_NLOAD, NOSA_DBG_POOLED, NOSA_DBG_SE, NOSA_DBG_SQ, NOSA_DBG_SLOTPOOL,
-  NOSA_DBG_HOST, NOSA_DBG_TAIL, NOSA_DBG_COUNT_
+  NOSA_DBG_HOST, NOSA_DBG_TAIL, NOSA_DBG_TRACE, NOSA_DBG_COUNT_
 };
 nosa_status nosa_debug_read(nosa_handle* h, int32_t what, size_t offset, void* dst, size_t bytes);
 
@@ -394,7 +419,9 @@ nosa_status nosa_selftest_bounded_wait(int32_t device, int64_t limit_ns, int32_t
  * 16 MiB array in the library's device memory, held by every GPU that loads the
  * library until the process exits; nothing is allocated. The first call on a
  * device (with cfg->device made current for the lookup) finds that array's
- * device address; make it before any stream capture. All calls share the array
+ * device address; make it before any stream capture. The address is kept with
+ * the device's context: the first call after a cudaDeviceReset (a new context)
+ * looks it up again, so it too must come before any capture. All calls share the array
  * and it keeps the last call's contents (each call clears its counters and
  * error word); calls that overlap on the GPU race. Shapes whose scratch
  * (nosa_attention_workspace_bytes) exceeds 16 MiB are rejected with

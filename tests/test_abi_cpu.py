@@ -126,3 +126,24 @@ def test_prefill_timing_without_a_timed_forward():
     t.join()
     assert out["st"] == 6  # STATE
     assert out["vals"] == (1.0, 1.0)  # outputs untouched
+
+
+# --------------------------------------------------------------------------
+# NUMA placement of the pinned host store: the pure rule, on fake topologies
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("gpu_node,mem_nodes,allowed,want", [
+    (1, [0, 1], [0, 1], 1),          # two Grace dies: the GPU's own node
+    (0, [0, 1], [0, 1], 0),
+    (3, [0, 1, 2, 3], [0, 1, 2, 3], 3),  # four sockets
+    (1, [0, 1], [0], -1),            # the GPU's node is not allowed to this process
+    (2, [0, 1], [0, 1, 2], -1),      # the GPU's node has no CPUs with memory (a GPU-memory node)
+    (0, [0], [0], -1),               # one memory node: nothing to choose
+    (-1, [0, 1], [0, 1], -1),        # node unknown (sysfs reports -1)
+    (1, [], [0, 1], -1),
+])
+def test_numa_placement_rule(gpu_node, mem_nodes, allowed, want):
+    assert nosa.nosa_numa_choose(gpu_node, mem_nodes, allowed) == want
+
+
+def test_numa_rule_null_arrays():
+    assert nosa.lib.nosa_numa_choose(1, None, 2, None, 2) == -1

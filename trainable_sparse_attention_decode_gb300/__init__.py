@@ -25,6 +25,7 @@ __all__ = [
     "nosa_selftest_bounded_wait", "nosa_frontend_rows", "nosa_decode_step_hidden",
     "nosa_frontend_packed_bytes", "nosa_frontend_pack", "nosa_prefill_workspace_bytes",
     "nosa_prefill_forward", "nosa_prefill_device_error", "nosa_prefill_timing",
+    "nosa_numa_choose",
 ]
 
 NOSA_F32, NOSA_BF16 = 0, 1
@@ -34,7 +35,7 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "OOM", 3: "HOST_OOM", 4: "CAPACITY", 5: 
           6: "STATE", 7: "UNSUPPORTED"}
 DBG = {name: i for i, name in enumerate(
     ["SEL", "NSEL", "ELIG", "SLOTS", "LOADS", "NLOAD", "POOLED", "SE", "SQ", "SLOTPOOL",
-     "HOST", "TAIL"])}
+     "HOST", "TAIL", "TRACE"])}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "_lib", "libnosa.so")
@@ -59,7 +60,8 @@ class NosaStats(C.Structure):
                 ("cold_host_loads", C.c_int64), ("max_host_loads_unit", C.c_int32),
                 ("min_hits", C.c_int32), ("sum_hits", C.c_int64), ("hit_samples", C.c_int64),
                 ("gamma_min", C.c_double), ("gamma_mean", C.c_double),
-                ("near_ties", C.c_int64), ("device_error", C.c_int32), ("pad_", C.c_int32),
+                ("near_ties", C.c_int64), ("device_error", C.c_int32),
+                ("host_numa_node", C.c_int32),
                 ("t_us", C.c_double * 8), ("t_count", C.c_int64), ("launches", C.c_int64)]
 
 
@@ -97,6 +99,7 @@ def _load():
                                            SZ, VP]),
         "nosa_prefill_device_error": (C.c_int, [P(NosaConfig), I32, VP, P(I32)]),
         "nosa_prefill_timing": (C.c_int, [P(C.c_float), P(C.c_float)]),
+        "nosa_numa_choose": (I32, [I32, P(I32), I32, P(I32), I32]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -174,6 +177,13 @@ def nosa_config_validate(cfg: NosaConfig):
 
 def nosa_payload_bytes(cfg: NosaConfig) -> int:
     return int(lib.nosa_payload_bytes(C.byref(cfg)))
+
+
+def nosa_numa_choose(gpu_node: int, mem_nodes, allowed) -> int:
+    """The host-store placement rule (see include/nosa.h): the node to bind, or -1."""
+    m = (C.c_int32 * max(1, len(mem_nodes)))(*mem_nodes)
+    a = (C.c_int32 * max(1, len(allowed)))(*allowed)
+    return lib.nosa_numa_choose(gpu_node, m, len(mem_nodes), a, len(allowed))
 
 
 def nosa_last_error(handle=None) -> str:

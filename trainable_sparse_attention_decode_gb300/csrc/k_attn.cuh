@@ -64,6 +64,8 @@ struct AttnKParams {
   // count x nv; nv = n_blocks + tail); a unit has up to seg_cap partials.
   int sk_ctas, nv, seg_cap;
   long long sk_items;
+  unsigned long long* trace;  // step trace (or null) and this launch's slot
+  int trace_slot;
 };
 
 template <typename T> struct Unpack16;
@@ -356,6 +358,7 @@ __device__ __forceinline__ void attn_merge(const float* part_acc, const float* p
 
 template <typename T, int D, int G, int W>
 __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
+  TraceScope trace_scope(p.trace, p.trace_slot);
   using Gm = AttnGeom<T, D, G, W>;
   constexpr int B = Gm::B, GP = Gm::GP, QP = Gm::QP, NT = Gm::NT, PARTS = Gm::PARTS;
   constexpr int TPW = Gm::TPW;
@@ -828,6 +831,8 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.nv = a.n_blocks + ((a.tail != nullptr || a.tail_tab != nullptr) ? 1 : 0);
   p.seg_cap = a.seg_cap;
   p.sk_items = (long long)a.unit_count * p.nv;
+  p.trace = a.trace;
+  p.trace_slot = a.trace_slot;
   if (a.sk_ctas > 0) {
     const size_t smem = attn_streamk_smem<T, D, G, W>(stages, s.payload, bps);
     static std::atomic<int> lim_sk[64];
@@ -836,7 +841,8 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
     attn_streamk_kernel<T, D, G, W><<<a.sk_ctas, 32 * W, smem, stream>>>(p);
     return cudaGetLastError();
   }
-  const size_t smem = AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps);
+  const size_t smem = std::max(AttnGeom<T, D, G, W>::smem_bytes(stages, s.payload, bps),
+                               smem_for_occupancy(a.max_ctas_per_sm));
   static std::atomic<int> lim[64];
   cudaError_t err = raise_smem_limit((const void*)attn_split_kernel<T, D, G, W>, smem, lim);
   if (err != cudaSuccess) return err;

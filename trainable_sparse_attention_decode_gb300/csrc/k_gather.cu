@@ -59,6 +59,7 @@ template <typename V>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State st, int ubase,
                                                                 int chunk) {
   constexpr int kPer = Mover<V>::kPer;
+  TraceScope trace_scope(st.trace, chunk < 8 ? kTrGather + chunk : -1);
   const int n = st.work_count[chunk];
   const int32_t* work = st.work + (long long)ubase * s.k;  // this chunk's list
   const int vpp = (int)(s.payload / sizeof(V));            // payload is a multiple of 256 B
@@ -124,6 +125,18 @@ __global__ void bounded_wait_probe_kernel(unsigned long long limit_ns, int* resu
   }
 }
 }  // namespace
+
+namespace {
+__global__ void trace_reset_kernel(unsigned long long* trace) {
+  const int i = threadIdx.x;
+  if (i < kTraceSlots) trace[2 * i] = ~0ull;  // starts: min-reduced; ends stay 0
+}
+}  // namespace
+
+cudaError_t launch_trace_reset(unsigned long long* trace, cudaStream_t stream) {
+  trace_reset_kernel<<<1, 64, 0, stream>>>(trace);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bounded_wait_probe(unsigned long long limit_ns, int* result,
                                       cudaStream_t stream) {

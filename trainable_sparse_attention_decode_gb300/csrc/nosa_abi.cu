@@ -299,17 +299,25 @@ struct StepGraph {
   cudaEvent_t done = nullptr;  // recorded after each launch: a rebuild waits for it
 };
 
+struct InjectFailFlags {
+  bool host = false;
+  int dev_index = -1;
+};
+
 struct nosa_handle {
   nosa_config cfg;
+  InjectFailFlags inject;  // failure injection of nosa_create (NOSA_INJECT_FAIL)
   Shape s;
   State st;
   std::vector<void*> dev_allocs;
   uint8_t* host_store = nullptr;
   size_t host_bytes = 0;
+  bool host_registered = false;  // the store was bound to a node and registered
+  int host_node = -1;            // NUMA node the store is bound to (-1: not bound)
   long long L = 0;
   long long steps = 0;
   int nsplit = 1;       // attention splits over the slots kept from the previous step
-  int nsplit_new = 2;   // attention splits over the slots the gather filled (warm steps)
+  int nsplit_new = 4;   // attention splits over the slots the gather filled (warm steps)
   int gather_grid = 1;
   bool broken = false;
   std::string err;
@@ -319,9 +327,19 @@ struct nosa_handle {
   // slots (medium); events order them per unit chunk.
   cudaStream_t s_sco = nullptr, s_sel = nullptr, s_gat = nullptr, s_att = nullptr, s_new = nullptr;
   cudaEvent_t ev_in = nullptr, ev_att = nullptr, ev_new = nullptr;
+  cudaEvent_t ev_app = nullptr;  // the step's append is done
+  // Fused step: chunk c is scored and selected on its own stream (priority
+  // falling with c) and attended over its kept slots on its own lowest-priority
+  // stream, and over its filled slots on its own stream as well; ev_jch / ev_jka
+  // / ev_jfa join them into the origin stream.
+  cudaStream_t s_chunk[kMaxChunks] = {}, s_katt[kMaxChunks] = {}, s_fatt[kMaxChunks] = {};
+  cudaEvent_t ev_jch[kMaxChunks] = {}, ev_jka[kMaxChunks] = {}, ev_jfa[kMaxChunks] = {};
   cudaEvent_t ev_jsco = nullptr, ev_jsel = nullptr, ev_jgat = nullptr;  // joins of a captured step
   cudaStream_t s_cap = nullptr;                       // origin stream of captures
   bool use_graphs = true;
+  bool fused_select = true;  // selection in the last scoring CTA of each unit
+  int score_occ = 0;         // resident scoring CTAs per SM cap (0: none)
+  int attn_occ = 0;          // resident attention CTAs per SM cap in the step (0: none)
   StepGraph plain;               // step graph without timing events
   StepGraph graphs[kGraphRing];  // step graphs with timing events (ring)
   cudaEvent_t gev[kGraphRing][kNumEv];
@@ -354,8 +372,22 @@ struct nosa_handle {
 
 namespace {
 
+// Failure injection on the host (no GPU fault involved): NOSA_INJECT_FAIL, read
+// at every nosa_create, makes one of its allocations report exhaustion without
+// being attempted. "host": the pinned host store; "dev:N": the N-th device
+// allocation (from 0). Anything else: no injection.
+InjectFailFlags inject_fail_from_env() {
+  InjectFailFlags f;
+  const char* g = std::getenv("NOSA_INJECT_FAIL");
+  if (g == nullptr) return f;
+  if (std::strcmp(g, "host") == 0) f.host = true;
+  else if (std::strncmp(g, "dev:", 4) == 0 && g[4] >= '0' && g[4] <= '9') f.dev_index = std::atoi(g + 4);
+  return f;
+}
+
 template <typename T>
 cudaError_t dev_alloc(nosa_handle* h, T** p, size_t bytes) {
+  if (h->inject.dev_index == (int)h->dev_allocs.size()) return cudaErrorMemoryAllocation;
   void* q = nullptr;
   cudaError_t e = cudaMalloc(&q, std::max<size_t>(bytes, 16));
   if (e != cudaSuccess) return e;
@@ -369,7 +401,7 @@ void free_all(nosa_handle* h) {
   h->q_buf = nullptr;
   for (void* p : h->dev_allocs) cudaFree(p);
   h->dev_allocs.clear();
-  if (h->host_store) cudaFreeHost(h->host_store);
+  host_store_free(h->host_store, h->host_bytes, h->host_registered);
   h->host_store = nullptr;
   for (StepGraph* gp : {&h->plain}) {
     if (gp->exec) cudaGraphExecDestroy(gp->exec);
@@ -391,8 +423,17 @@ void free_all(nosa_handle* h) {
     h->ev_made = false;
     h->timing = false;
   }
-  for (cudaEvent_t* e : {&h->ev_in, &h->ev_att, &h->ev_new, &h->ev_jsco, &h->ev_jsel, &h->ev_jgat})
+  for (cudaEvent_t* e : {&h->ev_in, &h->ev_att, &h->ev_new, &h->ev_jsco, &h->ev_jsel, &h->ev_jgat,
+                         &h->ev_app})
     if (*e) cudaEventDestroy(*e), *e = nullptr;
+  for (int c = 0; c < kMaxChunks; ++c) {
+    if (h->ev_jch[c]) cudaEventDestroy(h->ev_jch[c]), h->ev_jch[c] = nullptr;
+    if (h->ev_jka[c]) cudaEventDestroy(h->ev_jka[c]), h->ev_jka[c] = nullptr;
+    if (h->ev_jfa[c]) cudaEventDestroy(h->ev_jfa[c]), h->ev_jfa[c] = nullptr;
+    if (h->s_fatt[c]) cudaStreamDestroy(h->s_fatt[c]), h->s_fatt[c] = nullptr;
+    if (h->s_chunk[c]) cudaStreamDestroy(h->s_chunk[c]), h->s_chunk[c] = nullptr;
+    if (h->s_katt[c]) cudaStreamDestroy(h->s_katt[c]), h->s_katt[c] = nullptr;
+  }
   for (int c = 0; c < kMaxChunks; ++c) {
     if (h->ev_sco[c]) cudaEventDestroy(h->ev_sco[c]), h->ev_sco[c] = nullptr;
     if (h->ev_sel[c]) cudaEventDestroy(h->ev_sel[c]), h->ev_sel[c] = nullptr;
@@ -491,6 +532,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   DeviceGuard guard(cfg->device);
   nosa_handle* h = new nosa_handle();
   h->cfg = *cfg;
+  h->inject = inject_fail_from_env();
   h->s = shape_of(*cfg);
   std::memset(&h->st, 0, sizeof(h->st));
   std::memset(h->pending, 0, sizeof(h->pending));
@@ -523,12 +565,17 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.block_tab, U * k * 4);
   A(&st.tab_new, U * k * 4);
   A(&st.att_cnt, U * 4);
+  A(&st.sel_cnt, U * 4);
+  A(&st.qhint, U * 4);
   A(&st.part_acc, U * 2 * kMaxSplits * s.G * s.d * 4);
   A(&st.part_ml, U * 2 * kMaxSplits * s.G * 2 * 4);
   A(&st.stats, sizeof(DevStats));
   A(&st.io, sizeof(StepIO));
   A(&st.ksum, U * s.d * 4);
   A(&st.esum, U * 4);
+  st.trace = nullptr;
+  if (const char* g = std::getenv("NOSA_TRACE"))  // step trace (diagnostics)
+    if (std::atoi(g) != 0) A(&st.trace, kTraceSlots * 2 * 8);
   if (e != cudaSuccess) {
     g_thread_err = std::string("device allocation failed: ") + cudaGetErrorString(e);
     cudaGetLastError();
@@ -555,6 +602,8 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(st.block_tab, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.tab_new, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.att_cnt, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.sel_cnt, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(st.qhint, 0, U * 4);
   if (e == cudaSuccess) e = cudaMemset(st.ksum, 0, U * s.d * 4);
   if (e == cudaSuccess) e = cudaMemset(st.esum, 0, U * 4);
   DevStats ds = fresh_stats();
@@ -567,7 +616,11 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   }
   h->host_bytes = U * mb * (size_t)s.payload;
   void* hp = nullptr;
-  e = cudaHostAlloc(&hp, h->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  // On the GPU's NUMA node when the host has several (host_store.cu).
+  h->host_node = host_store_node(cfg->device);
+  e = h->inject.host ? cudaErrorMemoryAllocation
+                     : host_store_alloc(h->host_bytes, h->host_node, &hp, &h->host_registered);
+  if (!h->host_registered) h->host_node = -1;
   if (e != cudaSuccess) {
     g_thread_err = std::string("pinned host allocation failed: ") + cudaGetErrorString(e);
     cudaGetLastError();
@@ -597,30 +650,43 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     const int v = std::atoi(g);
     if (v > 0 && v <= kMaxSplits) h->nsplit_new = v;
   }
-  // Unit chunks of the pipelined step (NOSA_UNIT_CHUNKS overrides the count).
-  int nchunks = 2;
+  // Unit chunks of the pipelined step, by relative size: NOSA_CHUNK_SIZES (a
+  // comma-separated list of weights, up to 16), else NOSA_UNIT_CHUNKS chunks
+  // growing by NOSA_CHUNK_GROWTH, else the default weights.
+  std::vector<double> weights = {1, 2, 3, 4, 1};
   if (const char* g = std::getenv("NOSA_UNIT_CHUNKS")) {
     const int v = std::atoi(g);
-    if (v > 0) nchunks = v;
+    if (v > 0) {
+      double growth = 1.0;
+      if (const char* gr = std::getenv("NOSA_CHUNK_GROWTH")) {
+        const double x = std::atof(gr);
+        if (x >= 0.25 && x <= 16.0) growth = x;
+      }
+      weights.clear();
+      double w = 1.0;
+      for (int c = 0; c < std::min(v, kMaxChunks); ++c, w *= growth) weights.push_back(w);
+    }
   }
-  nchunks = std::max(1, std::min(std::min(nchunks, kMaxChunks), s.U));
+  if (const char* g = std::getenv("NOSA_CHUNK_SIZES")) {
+    std::vector<double> ws;
+    for (const char* p = g; *p && (int)ws.size() < kMaxChunks;) {
+      char* end = nullptr;
+      const double x = std::strtod(p, &end);
+      if (end == p) break;
+      if (x > 0) ws.push_back(x);
+      p = (*end == ',') ? end + 1 : end;
+    }
+    if (!ws.empty()) weights = ws;
+  }
+  const int nchunks = std::max(1, std::min((int)weights.size(), s.U));
   h->nchunks = nchunks;
-  // Chunk c holds a share of the units proportional to growth^c: a small first
-  // chunk starts the gather early, later chunks are scored while it runs
-  // (NOSA_CHUNK_GROWTH overrides the ratio).
-  double growth = 1.0;
-  if (const char* g = std::getenv("NOSA_CHUNK_GROWTH")) {
-    const double v = std::atof(g);
-    if (v >= 0.25 && v <= 16.0) growth = v;
-  }
   {
-    double total = 0.0, w = 1.0;
-    for (int c = 0; c < nchunks; ++c, w *= growth) total += w;
+    double total = 0.0;
+    for (int c = 0; c < nchunks; ++c) total += weights[c];
     double acc = 0.0;
-    w = 1.0;
     int prev = 0;
-    for (int c = 0; c < nchunks; ++c, w *= growth) {
-      acc += w;
+    for (int c = 0; c < nchunks; ++c) {
+      acc += weights[c];
       int end = (c == nchunks - 1) ? s.U : (int)std::llround(s.U * acc / total);
       end = std::max(end, prev + 1);                    // every chunk holds a unit
       end = std::min(end, s.U - (nchunks - 1 - c));     // and leaves one for each later chunk
@@ -634,20 +700,47 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     sc.U = h->cu_count[c];
     h->nsplit_c[c] = attention_pick_nsplit(sc, s.k, 1);
   }
+  // The selection runs in the scoring kernel where its arrays fit shared memory
+  // (NOSA_FUSED_SELECT=0: a selection kernel of its own after each chunk's scoring).
+  h->fused_select = score_select_fused_ok(s);
+  if (const char* g = std::getenv("NOSA_FUSED_SELECT"))
+    if (std::atoi(g) == 0) h->fused_select = false;
   int prio_lo = 0, prio_hi = 0;
   cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
   const int prio_mid = (prio_lo + prio_hi) / 2;
-  // Priorities: gather (keeps the host link busy) over selection (short, on the
-  // path to the next gather) over scoring and the filled-slot attention over the
-  // kept-slot attention (the bulk of the HBM work, with the most slack).
+  // Priorities (prio_hi is the most urgent): the gather (keeps the host link
+  // busy); the chunks' scoring and selection, chunk 0 first, so that they finish
+  // in chunk order without a gap between them; the attention over filled slots
+  // (it ends the step); the attention over kept slots last (the bulk of the HBM
+  // work, with the most slack). The unfused step keeps one scoring stream and a
+  // selection stream.
   const int prio_sel = (prio_hi < prio_mid) ? prio_hi + 1 : prio_hi;
   e = cudaStreamCreateWithPriority(&h->s_gat, cudaStreamNonBlocking, prio_hi);
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sel, cudaStreamNonBlocking, prio_sel);
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sco, cudaStreamNonBlocking, prio_mid);
-  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_new, cudaStreamNonBlocking, prio_mid);
+  // (the filled-slot attention of a fused step stays below every chunk's scoring:
+  // a chunk whose scoring is starved delays its gather)
+  const int prio_new = h->fused_select && prio_hi < prio_lo ? prio_lo - 1 : prio_sel;
+  // the kept-slot attention of a fused step: the lowest level (NOSA_KEPT_PRIO=1:
+  // one level up, with the filled-slot attention)
+  int prio_katt = prio_lo;
+  if (const char* g = std::getenv("NOSA_KEPT_PRIO"))
+    if (std::atoi(g) == 1 && prio_hi < prio_lo) prio_katt = prio_lo - 1;
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_new, cudaStreamNonBlocking, prio_new);
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_att, cudaStreamNonBlocking, prio_lo);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_cap, cudaStreamNonBlocking);
-  for (cudaEvent_t* ep : {&h->ev_in, &h->ev_att, &h->ev_new, &h->ev_jsco, &h->ev_jsel, &h->ev_jgat})
+  for (int c = 0; c < h->nchunks && e == cudaSuccess; ++c) {
+    // chunk c's scoring: one level below the previous chunk's, above the kept-slot attention
+    const int pc = prio_hi < prio_lo ? std::min(prio_hi + 1 + c, prio_lo - 1) : prio_hi;
+    e = cudaStreamCreateWithPriority(&h->s_chunk[c], cudaStreamNonBlocking, pc);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_katt[c], cudaStreamNonBlocking, prio_katt);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_jch[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_jka[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_fatt[c], cudaStreamNonBlocking, prio_new);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_jfa[c], cudaEventDisableTiming);
+  }
+  for (cudaEvent_t* ep : {&h->ev_in, &h->ev_att, &h->ev_new, &h->ev_jsco, &h->ev_jsel, &h->ev_jgat,
+                          &h->ev_app})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ep, cudaEventDisableTiming);
   for (int c = 0; c < kMaxChunks && e == cudaSuccess; ++c) {
     e = cudaEventCreateWithFlags(&h->ev_sel[c], cudaEventDisableTiming);
@@ -673,6 +766,15 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // Warm decode steps replay a captured graph (NOSA_GRAPHS=0 launches every
   // kernel from the host instead).
   if (const char* g = std::getenv("NOSA_GRAPHS")) h->use_graphs = std::atoi(g) != 0;
+
+  // Caps on resident CTAs per SM of the step's scoring and attention kernels
+  // (NOSA_SCORE_OCC, NOSA_ATTN_OCC; launch shapes only).
+  if (const char* g = std::getenv("NOSA_SCORE_OCC")) h->score_occ = std::max(0, std::atoi(g));
+  if (const char* g = std::getenv("NOSA_ATTN_OCC")) h->attn_occ = std::max(0, std::atoi(g));
+  // Gamma_q from the previous step's threshold hint (NOSA_SELECT_HINT=0: the
+  // radix cut at every step; the result is the same).
+  if (const char* g = std::getenv("NOSA_SELECT_HINT"))
+    if (std::atoi(g) == 0) st.qhint = nullptr;
   *out = h;
   return NOSA_OK;
 }
@@ -720,7 +822,12 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     else cudaEventRecord(e, t);
   };
   if (ev) mark(ev[0], origin);
-  cudaError_t err = cudaEventRecord(h->ev_in, origin);
+  cudaError_t err = cudaSuccess;
+  if (st.trace != nullptr) {  // fresh trace: starts at the maximum, ends at 0
+    err = cudaMemsetAsync(st.trace, 0, kTraceSlots * 2 * 8, origin);
+    if (err == cudaSuccess) err = launch_trace_reset(st.trace, origin);
+  }
+  if (err == cudaSuccess) err = cudaEventRecord(h->ev_in, origin);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sco, h->ev_in, 0);
   if (err == cudaSuccess)
     err = front ? launch_frontend(sh, st, *front, h->s_sco) : launch_append_step(sh, st, args, h->s_sco);
@@ -734,9 +841,23 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     if (err == cudaSuccess) *append_node = deps[0];
   }
   if (ev) mark(ev[1], h->s_sco);
-  // Scoring of every chunk back to back on one stream; each chunk's selection
-  // on another, as soon as its scores exist.
-  for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
+  // Fused step: every chunk's scoring + selection on its own stream, all started
+  // together after the append, chunk 0 at the highest priority, so that the
+  // chunks complete in order with no idle gap between them (each chunk's
+  // selection tail overlaps the next chunk's scoring). Unfused: scoring of every
+  // chunk back to back on one stream, each chunk's selection on another.
+  const bool fused = h->fused_select;
+  if (fused) {
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_app, h->s_sco);
+    for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
+      err = cudaStreamWaitEvent(h->s_chunk[c], h->ev_app, 0);
+      if (err == cudaSuccess)
+        err = launch_score_select(sh, st, n_cap, h->cu_base[c], h->cu_count[c], cold ? 1 : 0, c,
+                                  h->s_chunk[c], h->score_occ);
+      if (err == cudaSuccess) err = cudaEventRecord(h->ev_sel[c], h->s_chunk[c]);
+    }
+  }
+  for (int c = 0; c < h->nchunks && err == cudaSuccess && !fused; ++c) {
     err = launch_score(sh, st, n_cap, h->cu_base[c], h->cu_count[c], h->s_sco);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_sco[c], h->s_sco);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sel, h->ev_sco[c], 0);
@@ -744,7 +865,7 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
       err = launch_select_setdiff(sh, st, cold ? 1 : 0, h->cu_base[c], h->cu_count[c], c, h->s_sel);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_sel[c], h->s_sel);
   }
-  if (ev) mark(ev[2], h->s_sel);
+  if (ev) mark(ev[2], fused ? h->s_chunk[h->nchunks - 1] : h->s_sel);
   AttnArgs a;
   a.units = st.slots;
   a.n_units = (long long)sh.U * sh.k;
@@ -759,6 +880,7 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
   a.part_ml = st.part_ml;
   a.counters = st.att_cnt;
   a.err = &st.stats->error;
+  a.max_ctas_per_sm = h->attn_occ;
   for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
     const int ns_kept = h->nsplit_c[c];
     const int ns_new = cold ? ns_kept : h->nsplit_new;
@@ -771,38 +893,60 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], c, h->s_gat);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], h->s_gat);
     if (ev && c == h->nchunks - 1) mark(ev[5], h->s_gat);
-    // attention over the slots kept from the previous step, plus the tail
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_att, h->ev_sel[c], 0);
-    if (ev && c == 0) mark(ev[3], h->s_att);
+    // attention over the slots kept from the previous step, plus the tail (fused
+    // step: on the chunk's own stream, so chunks do not wait for one another)
+    cudaStream_t ta = fused ? h->s_katt[c] : h->s_att;
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(ta, h->ev_sel[c], 0);
+    if (ev && c == 0) mark(ev[3], ta);
     if (err == cudaSuccess) {
       a.block_tab = st.block_tab;
       a.tail = st.tail;  // + StepIO::tail_off
       a.nsplit = ns_kept;
       a.split_base = 0;
-      err = launch_attention(sh, a, h->s_att);
+      a.trace = st.trace;
+      a.trace_slot = c < 8 ? kTrAttnKept + c : -1;
+      err = launch_attention(sh, a, ta);
     }
-    // attention over the slots this chunk's gather filled
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_new, h->ev_gat[c], 0);
+    // attention over the slots this chunk's gather filled (fused step: on the
+    // chunk's own stream, so a chunk's launch does not wait for the previous one's)
+    cudaStream_t tf = fused ? h->s_fatt[c] : h->s_new;
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(tf, h->ev_gat[c], 0);
     if (err == cudaSuccess) {
       a.block_tab = st.tab_new;
       a.tail = nullptr;
       a.nsplit = ns_new;
       a.split_base = ns_kept;
-      err = launch_attention(sh, a, h->s_new);
+      a.trace_slot = c < 8 ? kTrAttnNew + c : -1;
+      err = launch_attention(sh, a, tf);
     }
+    if (fused && err == cudaSuccess) err = cudaEventRecord(h->ev_jfa[c], tf);
   }
-  if (ev) mark(ev[6], h->s_att);
-  if (err == cudaSuccess) err = cudaEventRecord(h->ev_att, h->s_att);
-  if (err == cudaSuccess) err = cudaEventRecord(h->ev_new, h->s_new);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_att, 0);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_new, 0);
+  if (ev) mark(ev[6], fused ? h->s_katt[h->nchunks - 1] : h->s_att);
+  if (fused) {  // join every chunk's attention streams (after the timing mark)
+    for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
+      err = cudaEventRecord(h->ev_jka[c], h->s_katt[c]);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jka[c], 0);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jfa[c], 0);
+    }
+  } else {
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_att, h->s_att);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_att, 0);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_new, h->s_new);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_new, 0);
+  }
   if (capture) {
     // A capture must join every stream it forked, including their last nodes.
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_jsco, h->s_sco);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jsco, 0);
-    if (err == cudaSuccess) err = cudaEventRecord(h->ev_jsel, h->s_sel);
+    if (!h->fused_select) {  // (the fused step never forks the selection stream)
+      if (err == cudaSuccess) err = cudaEventRecord(h->ev_jsel, h->s_sel);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jsel, 0);
+    }
+    for (int c = 0; c < h->nchunks && fused; ++c) {  // the chunks' scoring streams
+      if (err == cudaSuccess) err = cudaEventRecord(h->ev_jch[c], h->s_chunk[c]);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jch[c], 0);
+    }
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_jgat, h->s_gat);
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jsel, 0);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jgat, 0);
   }
   if (ev) mark(ev[7], origin);
@@ -897,7 +1041,9 @@ nosa_status run_step(nosa_handle* h, const StepArgs& args, const FrontArgs* fron
     err = enqueue_step(h, s, args, front, N, cold, ev, false, nullptr);
   }
   if (err != cudaSuccess) return h->cuda_fail(err, "decode step launch");
-  h->launches += 1 + h->nchunks * ((N > 0 ? 1 : 0) + 4);  // first kernel; per chunk score, select, gather, 2 x attention
+  // first kernel; per chunk: scoring and selection (fused: one launch), gather,
+  // attention over kept and over filled slots
+  h->launches += 1 + h->nchunks * (h->fused_select ? 4 : ((N > 0 ? 1 : 0) + 4));
   h->L += 1;
   h->steps += 1;
   h->last_stream = s;
@@ -1089,6 +1235,7 @@ nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out) {
   out->gamma_mean = ds.hit_samples ? (double)ds.sum_hits / ((double)h->s.k * ds.hit_samples) : 0.0;
   out->near_ties = (int64_t)ds.near_ties;
   out->device_error = ds.error;
+  out->host_numa_node = h->host_node;
   for (int i = 0; i < 8; ++i) out->t_us[i] = h->t_us[i];
   out->t_count = h->t_count;
   out->launches = h->launches;
@@ -1144,6 +1291,7 @@ size_t nosa_debug_size(const nosa_handle* h, int32_t what) {
     case NOSA_DBG_SLOTPOOL: return U * k * (size_t)s.payload;
     case NOSA_DBG_HOST: return h->host_bytes;
     case NOSA_DBG_TAIL: return U * 2 * (size_t)s.payload;
+    case NOSA_DBG_TRACE: return h->st.trace ? (size_t)kTraceSlots * 2 * 8 : 0;
     default: return 0;
   }
 }
@@ -1170,6 +1318,7 @@ nosa_status nosa_debug_read(nosa_handle* h, int32_t what, size_t offset, void* d
     case NOSA_DBG_SQ: base = st.sq; break;
     case NOSA_DBG_SLOTPOOL: base = st.slots; break;
     case NOSA_DBG_TAIL: base = st.tail; break;
+    case NOSA_DBG_TRACE: base = st.trace; break;
     case NOSA_DBG_HOST:
       std::memcpy(dst, h->host_store + offset, bytes);
       return NOSA_OK;

@@ -171,13 +171,30 @@ struct State {
   int32_t* block_tab;  // [U][k]            slots kept from the previous step (slot pool index), -1 none
   int32_t* tab_new;    // [U][k]            slots filled by this step's loads, -1 none
   int32_t* att_cnt;    // [U]               split CTAs finished (the last one merges; self-resetting)
+  int32_t* sel_cnt;    // [U]               scoring CTAs finished (the last one selects; self-resetting)
+  uint32_t* qhint;     // [U]               Gamma_q threshold hint (ordered key) for the next step, or null
   float* part_acc;     // split-K partial accumulators
   float* part_ml;      // split-K partial (max, sum)
   DevStats* stats;
   StepIO* io;          // the current decode step's arguments
   float* ksum;         // [U][d] fp32 running key sum of the open sub-block (token order)
   float* esum;         // [U]    fp32 running eviction-logit sum of the open sub-block
+  // Step trace (NOSA_TRACE=1 at create, else null): per traced launch of a step,
+  // the first CTA's start and the last CTA's end on the global timer (ns).
+  unsigned long long* trace;  // [kTraceSlots][2]
 };
+
+// Trace slots of a decode step's launches (chunk c < 8).
+constexpr int kTraceSlots = 48;
+enum : int {
+  kTrAppend = 0, kTrScore = 1, kTrSelect = 9, kTrGather = 17, kTrAttnKept = 25, kTrAttnNew = 33
+};
+
+// Pinned host store placement (host_store.cu): the node to bind the store of a
+// device to (-1: none), and allocation / release of the store.
+int host_store_node(int device);
+cudaError_t host_store_alloc(size_t bytes, int node, void** out, bool* registered);
+void host_store_free(void* p, size_t bytes, bool registered);
 
 // ---------------------------------------------------------------------------
 // Host-side launchers (each returns the launch error, if any).
@@ -196,8 +213,16 @@ cudaError_t launch_score(const Shape& s, const State& st, int n_cap, int ubase, 
                          cudaStream_t stream);
 cudaError_t launch_select_setdiff(const Shape& s, const State& st, int cold, int ubase,
                                   int ucount, int chunk, cudaStream_t stream);
+// Scoring with the selection and set-difference fused into the last scoring CTA
+// of each unit (one launch instead of launch_score + launch_select_setdiff), for
+// shapes whose selection arrays fit the CTA's shared memory.
+bool score_select_fused_ok(const Shape& s);
+cudaError_t launch_score_select(const Shape& s, const State& st, int n_cap, int ubase, int ucount,
+                                int cold, int chunk, cudaStream_t stream, int max_ctas_per_sm = 0);
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
                           cudaStream_t stream);
+// Sets every trace slot's start to the maximum (the ends are zeroed by the caller).
+cudaError_t launch_trace_reset(unsigned long long* trace, cudaStream_t stream);
 // result[0] = error code of a bounded wait that nothing completes, result[1] = ms waited.
 cudaError_t launch_bounded_wait_probe(unsigned long long limit_ns, int* result,
                                       cudaStream_t stream);
@@ -238,7 +263,20 @@ struct AttnArgs {
   // equally; seg_cap partial slots per unit (then also nsplit = nsplit_total).
   int sk_ctas = 0;
   int seg_cap = 0;
+  // Cap on resident CTAs per SM (0: none), reached by asking for more shared
+  // memory than the kernel uses: fewer copies in flight leave more of the
+  // memory system to a concurrent host-link gather. Launch shape only.
+  int max_ctas_per_sm = 0;
+  // Step trace (see State::trace): the array and this launch's slot (-1: none).
+  unsigned long long* trace = nullptr;
+  int trace_slot = -1;
 };
+// Dynamic shared memory that caps a kernel at `ctas` resident CTAs per SM
+// (0 when ctas <= 0): the SM's 228 KB split `ctas` ways, less the per-CTA
+// reservation and a margin for static shared memory.
+inline size_t smem_for_occupancy(int ctas) {
+  return ctas > 0 ? (size_t)(233472 / ctas) - 8192 : 0;
+}
 // How a single attention launch over n_blocks table entries (+ tail) per unit is
 // split: stream-K with sk_ctas CTAs (0: the classic split into nsplit per unit);
 // slots = partial slots per unit the workspace must hold.
@@ -328,6 +366,20 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
+
+// Records a CTA's start on entry and its end when the scope closes (any return)
+// in a trace slot: the slot keeps the earliest start and the latest end. No-op
+// without a trace array or slot.
+struct TraceScope {
+  unsigned long long* slot;
+  __device__ __forceinline__ TraceScope(unsigned long long* trace, int id)
+      : slot((trace != nullptr && id >= 0 && threadIdx.x == 0) ? trace + 2 * id : nullptr) {
+    if (slot) atomicMin(slot, (unsigned long long)global_ns());
+  }
+  __device__ __forceinline__ ~TraceScope() {
+    if (slot) atomicMax(slot + 1, (unsigned long long)global_ns());
+  }
+};
 
 // ---- mbarrier and bulk-copy primitives (inline PTX, sm_90+ forms) ----------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -14,8 +14,11 @@
 // (16 MiB): every GPU that loads the library holds it until the process exits.
 // In host code its name is only a host-side stand-in, never a device address,
 // so the first call on each device (with that device current) asks the runtime
-// for the array's device address once and caches it; make that first call before
-// any stream capture. All calls share the array and it keeps the last call's
+// for the array's device address once and caches it with the device's current
+// context; make that first call before any stream capture. A call that finds
+// another context current (after cudaDeviceReset the module loads again and
+// the array may move) looks the address up again, so that call too must come
+// before any stream capture. All calls share the array and it keeps the last call's
 // contents: the merge counters and the error word are cleared by each call
 // (cudaMemsetAsync on the caller's stream), and calls that overlap on the GPU
 // (different streams, or different host threads without ordering) race on it.
@@ -38,15 +41,40 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices];
+CUcontext g_scratch_ctx[kMaxDevices];
 
-// Device address of the scratch array on device `dev` (current), looked up once.
+// The calling thread's current driver context (nullptr if the driver offers no
+// query); fetched through the runtime's entry-point lookup, so the library needs
+// no link to the driver library.
+CUcontext current_context() {
+  using CtxGetCurrent = CUresult (*)(CUcontext*);
+  static CtxGetCurrent fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return (CtxGetCurrent) nullptr;
+    }
+    return reinterpret_cast<CtxGetCurrent>(ptr);
+  }();
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of the scratch array on device `dev` (current): looked up on
+// the first call and again whenever the device's current context has changed.
 cudaError_t scratch_address(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const CUcontext ctx = current_context();
+  if (g_scratch_addr[dev] == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = current_context();  // (the lookup makes the context current)
   }
   *out = g_scratch_addr[dev];
   return cudaSuccess;
