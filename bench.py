@@ -1029,6 +1029,9 @@ def main():
                          "(--prompt sets the length, default 32768)")
     ap.add_argument("--attention-only", action="store_true",
                     help="time only the split-K attention on the step shape (profiling aid)")
+    ap.add_argument("--classic", action="store_true",
+                    help="with --attention-only: the classic split the decode step launches "
+                         "(attn_split_kernel) instead of the standalone plan")
     ap.add_argument("--pooled-bf16", action="store_true",
                     help="variant: pooled keys stored in bf16 (halves the scoring traffic)")
     ap.add_argument("--frontend", action="store_true",
@@ -1078,7 +1081,8 @@ def main():
             w = w.with_(batch=args.batch)
         n_cand = w.prompt // w.block
         torch.cuda.nvtx.range_push("attention")
-        secs, nbytes = attention_alone(nosa, torch, w, n_cand, 33, reps=args.steps)
+        secs, nbytes = attention_alone(nosa, torch, w, n_cand, 33, reps=args.steps,
+                                       classic=args.classic)
         torch.cuda.nvtx.range_pop()
         peak, kind = measured_peaks()
         print(json.dumps({"attention_alone_us": round(secs * 1e6, 2), "bytes": nbytes,

@@ -146,3 +146,13 @@ def test_8b_longgen_sampled_units_long_horizon():
     st, run = _run(w, units=[3, 100], attn_every=16, check_bytes=False, state_every=16)
     assert st["gamma_min"] >= w.k_e / w.k - 1e-12
     assert st["max_host_loads_unit"] <= w.k - w.k_e
+
+
+@pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2"])
+def test_unequal_chunks_every_unit(sizes, monkeypatch):
+    # The step's unit chunks run concurrently and differ in split counts; every
+    # unit (not a sample) is checked, so a partial buffer shared across chunks
+    # would show on some unit.
+    monkeypatch.setenv("NOSA_CHUNK_SIZES", sizes)
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=2, prompt=64 * 40 + 9, steps=40)
+    _run(w)

@@ -48,6 +48,7 @@ struct AttnKParams {
   float* part_ml;
   int nsplit, bps, stages;
   int split_base, nsplit_total;
+  int part_stride;  // partial slots per unit in part_acc / part_ml (>= nsplit_total)
   int unit_base;
   int* counters;
   void* out;
@@ -395,12 +396,11 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
     tail_len = p.tail_lens[p.unit_base + blockIdx.y];
   }
   // Virtual item list: the n_blocks table entries, then the tail (if any),
-  // spread evenly over the splits.
-  const int nv = p.n_blocks + (tail != nullptr ? 1 : 0);
-  const int v0 = (int)((long long)sp * nv / p.nsplit);
-  const int v1 = (int)((long long)(sp + 1) * nv / p.nsplit);
-  const int j0 = v0, j1 = min(v1, p.n_blocks);
-  const bool has_tail = (tail != nullptr) && (v1 > p.n_blocks);
+  // dealt to the splits in turn (split sp takes items sp, sp + nsplit, ...), so
+  // that a table whose valid entries sit at its front (the slots a gather just
+  // filled) still spreads them over every split.
+  const int ns = p.nsplit;
+  const bool has_tail = (tail != nullptr) && (p.n_blocks % ns == sp);
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -412,9 +412,9 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   }
   if (warp == 0) {  // compact the valid blocks of this split, in order
     int cnt = 0;
-    for (int base = j0; base < j1; base += 32) {
-      const int j = base + lane;
-      int idx = (j < j1) ? p.block_tab[(long long)u * p.n_blocks + j] : -1;
+    for (int base = sp; base < p.n_blocks; base += 32 * ns) {
+      const int j = base + lane * ns;
+      int idx = (j < p.n_blocks) ? p.block_tab[(long long)u * p.n_blocks + j] : -1;
       if (idx >= 0 && (long long)idx >= p.n_units) {  // bad index: skip it, flag it
         atomicExch(p.err, kDevErrBadIndex);
         idx = -1;
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   const long long row0 = (long long)b * p.Hq + (long long)h * G;
   float* red = reinterpret_cast<float*>(stage_buf);  // the stages are idle now
   attn_reduce<T, D, G, W>(st, red, tid, warp, lane, p.part_acc, p.part_ml,
-                          nst == 1 ? -1 : ((long long)u * nst + p.split_base + sp) * G,
+                          nst == 1 ? -1 : ((long long)u * p.part_stride + p.split_base + sp) * G,
                           out, lse, row0);
   if (nst == 1) return;
 
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  attn_merge<T, D, G, W>(p.part_acc, p.part_ml, (long long)u * nst * G, nst,
+  attn_merge<T, D, G, W>(p.part_acc, p.part_ml, (long long)u * p.part_stride * G, nst,
                          reinterpret_cast<float*>(stage_buf), out, lse, row0, tid);
   if (tid == 0) p.counters[u] = 0;
 }
@@ -813,6 +813,7 @@ cudaError_t launch_attn_variant(const Shape& s, const AttnArgs& a, int stages, i
   p.nsplit = a.nsplit;
   p.split_base = a.split_base;
   p.nsplit_total = a.nsplit_total;
+  p.part_stride = a.part_stride > 0 ? a.part_stride : a.nsplit_total;
   p.unit_base = a.unit_base;
   p.counters = a.counters;
   p.out = a.out;

@@ -322,16 +322,20 @@ __device__ bool mark_top_hint(const uint32_t* key, uint8_t* flag, uint8_t tmask,
   return true;
 }
 
+// selm: the unit's selection mask words (this CTA's shared copy); s2b_s: a shared
+// copy of its slot table, loaded at the start of the selection and kept up to
+// date here; res0: the residency word of this thread (word threadIdx.x), loaded
+// at the start too, valid when nw <= NT.
 template <int NT>
 __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
-                              int cold, int ubase, int chunk) {
+                              int cold, int ubase, int chunk, const uint32_t* selm, int* s2b_s,
+                              uint32_t res0) {
   constexpr int kDiffThreads = NT;
   constexpr int kDiffWarps = NT / 32;
   __shared__ int load_blk[kMaxK];
   __shared__ int free_list[kMaxK];
   __shared__ int warp_tot[kDiffWarps];
   __shared__ int s_base, s_tail_loaded;
-  const uint32_t* selm = st.selmask + (long long)u * s.W;
   uint32_t* resm = st.resmask + (long long)u * s.W;
   int32_t* s2b = st.slot2blk + (long long)u * s.k;
   const int nw = (n + 31) >> 5;
@@ -341,7 +345,8 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
   int nload = 0;
   for (int base = 0; base < nw; base += kDiffThreads) {
     const int w = base + threadIdx.x;
-    uint32_t lw = (w < nw) ? (selm[w] & ~resm[w]) : 0u;
+    const uint32_t rw = (nw <= kDiffThreads) ? res0 : ((w < nw) ? resm[w] : 0u);
+    uint32_t lw = (w < nw) ? (selm[w] & ~rw) : 0u;
     int tot;
     int pos = nload + block_excl_scan<kDiffWarps>(__popc(lw), warp_tot, &tot);
     while (lw) {
@@ -357,7 +362,7 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
     const int sl = base + threadIdx.x;
     int f = 0;
     if (sl < s.k) {
-      const int b = s2b[sl];
+      const int b = s2b_s[sl];
       f = (b < 0) || !((selm[b >> 5] >> (b & 31)) & 1u);
     }
     int tot;
@@ -375,9 +380,13 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
     loads[3 * j + 1] = slot;
     loads[3 * j + 2] = src;
     s2b[slot] = blk;
+    s2b_s[slot] = blk;
     if (src) s_tail_loaded = 1;
   }
-  for (int j = nload + threadIdx.x; j < nfree; j += kDiffThreads) s2b[free_list[j]] = -1;
+  for (int j = nload + threadIdx.x; j < nfree; j += kDiffThreads) {
+    s2b[free_list[j]] = -1;
+    s2b_s[free_list[j]] = -1;
+  }
   for (int w = threadIdx.x; w < s.W; w += kDiffThreads) resm[w] = (w < nw) ? selm[w] : 0u;
   if (threadIdx.x == 0) {
     st.nload[u] = nload;
@@ -388,7 +397,7 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
   // runs) and slots that this step's loads fill.
   int32_t* tres = st.block_tab + (long long)u * s.k;
   int32_t* tnew = st.tab_new + (long long)u * s.k;
-  for (int sl = threadIdx.x; sl < s.k; sl += kDiffThreads) tres[sl] = (s2b[sl] >= 0) ? u * s.k + sl : -1;
+  for (int sl = threadIdx.x; sl < s.k; sl += kDiffThreads) tres[sl] = (s2b_s[sl] >= 0) ? u * s.k + sl : -1;
   __syncthreads();
   for (int j = threadIdx.x; j < s.k; j += kDiffThreads) {
     if (j < nload) {
@@ -435,6 +444,12 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
   const float* se = st.se + (long long)u * s.maxBlk;
   const float* sq = st.sq + (long long)u * s.maxBlk;  // read through L2 (other CTAs wrote it)
   uint32_t* elig = st.elig + (long long)u * s.W;
+  // Loaded now for the set-difference at the end, so that their latency overlaps
+  // the selection: the slot table (shared copy) and this thread's residency word.
+  __shared__ int s2b_s[kMaxK];
+  for (int sl = threadIdx.x; sl < s.k; sl += kSelThreads) s2b_s[sl] = st.slot2blk[(long long)u * s.k + sl];
+  const uint32_t res0 =
+      ((int)threadIdx.x < ((n + 31) >> 5)) ? st.resmask[(long long)u * s.W + threadIdx.x] : 0u;
 
   int my_elig = 0;
   for (int i = threadIdx.x; i < n; i += kSelThreads) {
@@ -500,6 +515,7 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
       const int w = (base + (threadIdx.x & ~31)) >> 5;
       elig[w] = be;
       st.selmask[(long long)u * s.W + w] = bs;
+      key[w] = bs;  // shared copy for the set-difference (key[] is free by now)
     }
   }
   for (int j = need_e + need_q + threadIdx.x; j < s.k; j += kSelThreads) sel[j] = -1;
@@ -507,8 +523,8 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
     st.nsel[2 * u] = need_e;
     st.nsel[2 * u + 1] = need_q;
   }
-  __syncthreads();  // selmask and nsel of this unit are visible to the whole CTA
-  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, ubase, chunk);
+  __syncthreads();  // the selection mask copy and nsel are visible to the whole CTA
+  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, ubase, chunk, key, s2b_s, res0);
 }
 
 }  // namespace

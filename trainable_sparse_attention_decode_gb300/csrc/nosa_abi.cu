@@ -652,8 +652,15 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   }
   // Unit chunks of the pipelined step, by relative size: NOSA_CHUNK_SIZES (a
   // comma-separated list of weights, up to 16), else NOSA_UNIT_CHUNKS chunks
-  // growing by NOSA_CHUNK_GROWTH, else the default weights.
-  std::vector<double> weights = {1, 2, 3, 4, 1};
+  // growing by NOSA_CHUNK_GROWTH, else by the unit count. Measured on GB300:
+  // every chunk adds a selection tail and four launches, which pay off only when
+  // the units are many (64 units: one chunk, 55 us against 71 us with five; 128
+  // units: two; 256 units: 1,2,3,4,1, small first chunks so that the first gather
+  // starts early and a small last one so that little attention is left after the
+  // last gather).
+  std::vector<double> weights = s.U <= 96 ? std::vector<double>{1}
+                                : s.U <= 192 ? std::vector<double>{1, 1}
+                                             : std::vector<double>{1, 2, 3, 4, 1};
   if (const char* g = std::getenv("NOSA_UNIT_CHUNKS")) {
     const int v = std::atoi(g);
     if (v > 0) {
@@ -881,6 +888,7 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
   a.counters = st.att_cnt;
   a.err = &st.stats->error;
   a.max_ctas_per_sm = h->attn_occ;
+  a.part_stride = 2 * kMaxSplits;  // every unit's own range of the partial buffers
   for (int c = 0; c < h->nchunks && err == cudaSuccess; ++c) {
     const int ns_kept = h->nsplit_c[c];
     const int ns_new = cold ? ns_kept : h->nsplit_new;

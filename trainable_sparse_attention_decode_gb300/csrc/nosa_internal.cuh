@@ -248,6 +248,10 @@ struct AttnArgs {
   int nsplit;
   int split_base;
   int nsplit_total;
+  // Partial slots per unit in part_acc / part_ml (0: nsplit_total). The decode
+  // step's chunks have different split counts and run concurrently, so there
+  // every unit owns a fixed range of slots.
+  int part_stride = 0;
   int unit_base;            // this launch covers units [unit_base, unit_base + unit_count)
   int unit_count;
   int* counters;            // [U]
