@@ -878,6 +878,60 @@ def run_horizon(args, rank, world, local_rank):
                     "step time: the share of a step the recall alone needs on the host link"}
 
 
+def run_trace(args, rank, world, local_rank):
+    """Timeline of isolated decode steps from the library's step trace
+    (NOSA_TRACE=1): after the warm-up, `args.trace` steps each followed by a
+    synchronisation; per traced launch the first CTA's start and the last CTA's
+    end (us from the step's first start), and the step's host bytes."""
+    os.environ["NOSA_TRACE"] = "1"
+    import numpy as np
+    import torch
+    import synth
+    import synth.gpu
+    import trainable_sparse_attention_decode_gb300 as nosa
+    torch.cuda.set_device(local_rank)
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(batch=args.batch)
+    n = args.warmup + args.trace
+    w = w.with_(steps=n + 1)
+    cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
+                           w.max_context, device=local_rank)
+    h = nosa.nosa_create(cfg)
+    t = 0
+    while t < w.prompt:
+        m = min(4096, w.prompt - t)
+        k, v, e = synth.gpu.kv(w, t, m)
+        nosa.nosa_append_kv(h, k, v, e)
+        t += m
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
+    q = synth.gpu.queries(w, n)
+    kk, vv, ee = synth.gpu.kv(w, w.prompt, n, step_major=True)
+    for s_ in range(args.warmup):
+        nosa.nosa_decode_step(h, q[s_], kk[s_], vv[s_], ee[s_], out)
+    names = {0: "append"}
+    for c in range(8):
+        names.update({1 + c: f"score+select {c}", 9 + c: f"select {c}", 17 + c: f"gather {c}",
+                      25 + c: f"attention kept {c}", 33 + c: f"attention filled {c}"})
+    steps = []
+    for s_ in range(args.warmup, n):
+        hb0 = nosa.nosa_stats(h)["host_bytes"]
+        nosa.nosa_decode_step(h, q[s_], kk[s_], vv[s_], ee[s_], out)
+        torch.cuda.synchronize()
+        hb = nosa.nosa_stats(h)["host_bytes"] - hb0
+        tr = np.frombuffer(nosa.nosa_debug_read(h, "TRACE").tobytes(), np.uint64).reshape(-1, 2)
+        used = [i for i in range(tr.shape[0]) if int(tr[i, 0]) != 0xFFFFFFFFFFFFFFFF]
+        t0 = min(int(tr[i, 0]) for i in used)
+        launches = sorted(((names[i], round((int(tr[i, 0]) - t0) / 1e3, 1),
+                            round((int(tr[i, 1]) - t0) / 1e3, 1)) for i in used), key=lambda x: x[1])
+        steps.append({"step": s_, "span_us": max(x[2] for x in launches), "host_bytes": hb,
+                      "launches": launches})
+    nosa.nosa_destroy(h)
+    return {"mode": "trace", "config": {"workload": w.name, "batch": w.batch},
+            "steps": steps}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
@@ -1047,6 +1101,9 @@ def main():
                          "fits (fullattn: the whole cache; nosa/infllmv2: the handle's state)")
     ap.add_argument("--host-budget", type=float, default=96.0,
                     help="GB of pinned host memory the host store may take (with --hbm-budget)")
+    ap.add_argument("--trace", type=int, default=0,
+                    help="print the launch timeline of this many isolated decode steps after "
+                         "the warm-up (the library's step trace)")
     ap.add_argument("--horizon", type=int, default=0,
                     help="run the workload's whole decode horizon and report this many "
                          "windows along it (tokens/s, recall, locality)")
@@ -1088,6 +1145,11 @@ def main():
         print(json.dumps({"attention_alone_us": round(secs * 1e6, 2), "bytes": nbytes,
                           "gbs": round(nbytes / secs / 1e9, 1),
                           "frac_of_" + kind + "_peak": round(nbytes / secs / 1e9 / peak, 4)}))
+        return
+    if args.trace:
+        line = run_trace(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         return
     if args.horizon:
         line = run_horizon(args, rank, world, local_rank)
