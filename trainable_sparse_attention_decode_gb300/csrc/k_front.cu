@@ -20,11 +20,10 @@
 // width: a CTA streams one contiguous range with bulk copies (full DRAM pages),
 // and TMA brings the matching N x 64 hidden-state tiles (same swizzle) into a
 // ring of shared-memory stages.
-// The hidden width is split over ksplit CTAs per row tile (enough CTAs to cover
-// every SM): each CTA writes its fp32 partial tile to a scratch buffer in global
-// memory and counts itself out (fence, add on the tile's counter); the tile's
-// last CTA sums the ksplit partials in split order (deterministic) and runs the
-// epilogue for every (request, 8-row group) item of the tile:
+// The splits of a row tile form one thread-block cluster: each CTA leaves its
+// fp32 partial tile in shared memory and, after a cluster barrier, sums a share
+// of the tile's entries over all ranks (rank order, deterministic) through
+// distributed shared memory, then runs the epilogue for that share:
 //   query rows    -> q [batch][Hq][d], bf16 (nearest even);
 //   key rows      -> the unit's tail block (chunk-major K), value rows -> V
 //                    (token-major), both bf16; eviction rows -> e (fp32);
@@ -146,9 +145,56 @@ __device__ __forceinline__ void store_item(const Shape& s, const State& st, cons
   }
 }
 
+// Loads the running sums that store_item will need for rows f0 .. f0 + 7 of
+// request n (key rows: 8 from ksum; eviction rows: up to 8 from esum).
+__device__ __forceinline__ void prefetch_sums(const Shape& s, const State& st,
+                                              const FrontParams& p, int n, int f0, float* pre) {
+  const int Fq = s.Hq * s.d, Fk = Fq + s.Hkv * s.d, Fv = Fk + s.Hkv * s.d;
+  if (f0 >= Fq && f0 < Fk) {
+    const int r = f0 - Fq;
+    const float4* ks = reinterpret_cast<const float4*>(
+        st.ksum + (long long)(n * s.Hkv + r / s.d) * s.d + r % s.d);
+    const float4 a = ks[0], b = ks[1];
+    pre[0] = a.x; pre[1] = a.y; pre[2] = a.z; pre[3] = a.w;
+    pre[4] = b.x; pre[5] = b.y; pre[6] = b.z; pre[7] = b.w;
+  } else if (f0 >= Fv) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      pre[e] = (f0 + e < p.F) ? st.esum[n * s.Hkv + (f0 + e - Fv)] : 0.f;
+  }
+}
+
+// Distributed shared memory of the CTA cluster that shares a row tile.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before
+// the peers' reads (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kFrontThreads)
+__global__ void __launch_bounds__(kFrontThreads, 1)
     frontend_kernel(const __grid_constant__ CUtensorMap tx, Shape s, State st, FrontParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -191,7 +237,12 @@ __global__ void __launch_bounds__(kFrontThreads)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int tid2 = threadIdx.x - 64;  // epilogue thread (warps 2-5)
+  // Items of the first chunk of requests handled by this thread in the epilogue
+  // (see below); their running sums are loaded while the tensor cores run.
+  constexpr int kItemsMax = 4;  // 512 items / (128 threads x ksplit >= 1)
+  const uint32_t rank = cluster_rank();
+  const int tid2 = threadIdx.x - 64;
+  float pre[kItemsMax][8];
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
@@ -264,6 +315,15 @@ __global__ void __launch_bounds__(kFrontThreads)
       __threadfence_system();
     }
 
+    if ((pos % s.S) != 0) {
+#pragma unroll
+      for (int q = 0; q < kItemsMax; ++q) {
+        const int it = (int)rank * 128 + tid2 + q * 128 * p.ksplit;
+        const int n = it >> 4, f0 = tile * kTileM + (it & 15) * 8;
+        if (it < 32 * 16 && n < p.batch && f0 < p.F) prefetch_sums(s, st, p, n, f0, pre[q]);
+      }
+    }
+
     // Wait for the accumulator.
     const bool okw = __all_sync(0xffffffffu, mbar_wait_bounded(&accum, 0));
     if (!okw && lane == 0) {
@@ -274,54 +334,51 @@ __global__ void __launch_bounds__(kFrontThreads)
     tc_fence_after();
   }
 
-  // Epilogue. Every CTA writes its fp32 partial tile (row-contiguous per request:
-  // part[tile][split][request][128 rows]) and counts itself out; the tile's last
-  // CTA sums the splits' partials in split order and stores every item of the
-  // tile (the requests' q, k, v, e rows of this tile, with the pooling).
+  // Epilogue, per chunk of 32 requests. Each CTA of the cluster (the splits of
+  // one row tile) leaves its fp32 partial of the chunk in its shared memory (the
+  // stages are idle by now); after a cluster barrier every CTA takes a share of
+  // the (request, 8-row group) items, sums the partials of all ranks in rank
+  // order (deterministic) through distributed shared memory, and stores them.
+  // A second barrier keeps every partial alive until the peers have read it.
   {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* mine = p.part + (long long)(tile * p.ksplit + split) * p.npad * kTileM;
-    if (warp >= 2 && s_bad == 0) {
-      float v[16];
-      for (int cc = 0; cc < p.batch; cc += 16) {
-        tmem_ld16(taddr + cc, v);
+    float* P = reinterpret_cast<float*>(sa);  // [32][128] fp32
+    const bool ok = (s_bad == 0);
+    for (int c0 = 0; c0 < p.batch; c0 += 32) {
+      if (warp >= 2 && ok) {
+        float v[16];
+        for (int cc = 0; cc < 32; cc += 16) {
+          if (c0 + cc >= p.batch) break;
+          tmem_ld16(taddr + c0 + cc, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (cc + j < p.batch) mine[(cc + j) * kTileM + row] = v[j];
+          for (int j = 0; j < 16; ++j) P[(cc + j) * kTileM + row] = v[j];
+        }
       }
-    }
-    tc_fence_before();
-    __syncthreads();  // the CTA's partial is written
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const int prev = atomicAdd(p.tile_cnt + tile, 1);
-      s_last = (prev == p.ksplit - 1);
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      if (warp >= 2 && s_bad == 0) {
-        const float* pt = p.part + (long long)tile * p.ksplit * p.npad * kTileM;
-        for (int it = tid2; it < 16 * p.batch; it += 128) {
-          const int n = it >> 4, g = it & 15;
-          const int f0 = tile * kTileM + g * 8;
-          if (f0 >= p.F) continue;
+      cluster_sync();
+      if (warp >= 2 && ok) {
+#pragma unroll
+        for (int q = 0; q < kItemsMax; ++q) {
+          const int it = (int)rank * 128 + tid2 + q * 128 * p.ksplit;
+          const int j = it >> 4, g = it & 15;
+          const int n = c0 + j, f0 = tile * kTileM + g * 8;
+          if (it >= 32 * 16 || n >= p.batch || f0 >= p.F) continue;
+          const void* local = P + j * kTileM + g * 8;
           float v8[8];
           for (int r = 0; r < p.ksplit; ++r) {
-            const float4* src =
-                reinterpret_cast<const float4*>(pt + ((long long)r * p.npad + n) * kTileM + g * 8);
-            const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+            const uint32_t a = map_to_rank(local, (uint32_t)r);
+            const float4 x0 = ld_cluster_f4(a), x1 = ld_cluster_f4(a + 16);
             const float t8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) v8[e] = (r == 0) ? t8[e] : v8[e] + t8[e];
           }
-          store_item(s, st, p, n, f0, v8, nullptr, blk, pos);
+          store_item(s, st, p, n, f0, v8, c0 == 0 ? pre[q] : nullptr, blk, pos);
         }
       }
-      if (threadIdx.x == 0) p.tile_cnt[tile] = 0;  // ready for the next step
+      cluster_sync();
     }
+    tc_fence_before();
   }
 
   __syncthreads();
@@ -427,18 +484,34 @@ cudaError_t launch_frontend_pack(const void* w, void* packed, int F, int D, cuda
 const void* frontend_kernel_ptr() { return reinterpret_cast<const void*>(frontend_kernel); }
 
 namespace {
+cudaLaunchConfig_t front_config(const FrontParams& p, cudaStream_t stream,
+                                cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3(p.tiles, p.ksplit, 1);
+  c.blockDim = dim3(kFrontThreads, 1, 1);
+  c.dynamicSmemBytes = frontend_smem_bytes(p.npad, p.stages);
+  c.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 1;
+  attr->val.clusterDim.y = (unsigned)p.ksplit;  // the splits of a row tile
+  attr->val.clusterDim.z = 1;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return c;
+}
 std::atomic<int> g_front_smem_lim[64];
 }  // namespace
 
-int frontend_occupancy(int npad, int stages) {
-  const size_t smem = frontend_smem_bytes(npad, stages);
-  if (raise_smem_limit((const void*)frontend_kernel, smem, g_front_smem_lim) != cudaSuccess) {
+int frontend_max_clusters(const FrontParams& p) {
+  if (raise_smem_limit((const void*)frontend_kernel, frontend_smem_bytes(p.npad, p.stages),
+                       g_front_smem_lim) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t c = front_config(p, nullptr, &attr);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, frontend_kernel, kFrontThreads, smem) !=
-      cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)frontend_kernel, &c) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -447,12 +520,12 @@ int frontend_occupancy(int npad, int stages) {
 
 cudaError_t launch_frontend(const Shape& s, const State& st, const FrontArgs& fa,
                             cudaStream_t stream) {
-  const size_t smem = frontend_smem_bytes(fa.p.npad, fa.p.stages);
-  cudaError_t err = raise_smem_limit((const void*)frontend_kernel, smem, g_front_smem_lim);
+  cudaError_t err = raise_smem_limit((const void*)frontend_kernel,
+                                     frontend_smem_bytes(fa.p.npad, fa.p.stages), g_front_smem_lim);
   if (err != cudaSuccess) return err;
-  frontend_kernel<<<dim3(fa.p.tiles, fa.p.ksplit, 1), kFrontThreads, smem, stream>>>(fa.tx, s, st,
-                                                                                   fa.p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t c = front_config(fa.p, stream, &attr);
+  return cudaLaunchKernelEx(&c, frontend_kernel, fa.tx, s, st, fa.p);
 }
 
 }  // namespace nosa

@@ -358,8 +358,6 @@ struct nosa_handle {
   long long launches = 0;  // kernels launched by decode steps
   // Fused front-end (set up on the first nosa_decode_step_hidden of a width).
   void* q_buf = nullptr;     // [batch][Hq][d] bf16 step queries
-  void* fe_part = nullptr;   // front-end split partials [tiles][ksplit][npad][128] fp32
-  void* fe_cnt = nullptr;    // front-end tile counters [tiles]
   int fe_hidden = 0, fe_ksplit = 0, fe_stages = 0;
 
   nosa_status fail(nosa_status code, const std::string& msg) {
@@ -401,10 +399,6 @@ cudaError_t dev_alloc(nosa_handle* h, T** p, size_t bytes) {
 void free_all(nosa_handle* h) {
   if (h->q_buf) cudaFree(h->q_buf);
   h->q_buf = nullptr;
-  if (h->fe_part) cudaFree(h->fe_part);
-  h->fe_part = nullptr;
-  if (h->fe_cnt) cudaFree(h->fe_cnt);
-  h->fe_cnt = nullptr;
   for (void* p : h->dev_allocs) cudaFree(p);
   h->dev_allocs.clear();
   host_store_free(h->host_store, h->host_bytes, h->host_registered);
@@ -1155,21 +1149,33 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
   const int kblocks = hidden / 64;
   const int npad = sh.batch <= 16 ? 16 : (sh.batch + 15) / 16 * 16;
   if (h->fe_hidden != hidden) {
-    // Splits of the hidden width per row tile: as many as fill every SM once
-    // (tiles x ksplit <= SMs x resident CTAs per SM), at least one, at most the
-    // 64-column blocks of the width; the ring is as deep as one CTA per SM allows
-    // (NOSA_FRONT_STAGES / NOSA_FRONT_KSPLIT override, for tuning).
-    int stages = frontend_stages(npad);
-    if (const char* g = std::getenv("NOSA_FRONT_STAGES")) {
-      const int v = std::atoi(g);
-      if (v >= 2 && v <= stages) stages = v;
-    }
-    const int occ = std::max(1, frontend_occupancy(npad, stages));
-    int ksplit = std::max(1, std::min(kblocks, sm_count_current() * occ / tiles));
+    // Splits per row tile (the cluster size): about one CTA per SM, at most 8,
+    // and every cluster resident at once (checked with the occupancy query).
+    // A shorter stage ring lets two CTAs share an SM, which raises the number
+    // of clusters that fit; the split count comes first, then the ring depth.
+    FrontParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.tiles = tiles;
+    q.npad = npad;
+    const int max_stages = frontend_stages(npad);
+    int ksplit = std::max(1, std::min(std::min(kblocks, 8), sm_count_current() / tiles));
     if (const char* g = std::getenv("NOSA_FRONT_KSPLIT")) {  // tuning override
       const int v = std::atoi(g);
-      if (v >= 1) ksplit = std::min(kblocks, v);
+      if (v >= 1) ksplit = std::min(std::min(kblocks, 8), v);
     }
+    auto fits = [&](int ks, int st) {
+      q.ksplit = ks;
+      q.stages = st;
+      return ks == 1 || frontend_max_clusters(q) >= tiles;
+    };
+    int stages = max_stages;
+    for (; ksplit > 1; --ksplit) {
+      for (stages = max_stages; stages >= 3 && !fits(ksplit, stages); --stages) {
+      }
+      if (stages >= 3) break;
+    }
+    if (ksplit == 1) stages = max_stages;
+    q.stages = stages;
     if (!h->q_buf) {
       const cudaError_t e = cudaMalloc(&h->q_buf, (size_t)sh.batch * sh.Hq * sh.d * 2);
       if (e != cudaSuccess) {
@@ -1177,20 +1183,9 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
         return h->fail(NOSA_ERR_OOM, "front-end query buffer");
       }
     }
-    // split partials and tile counters (replacing those of another width)
-    if (h->fe_part) cudaFree(h->fe_part), h->fe_part = nullptr;
-    if (h->fe_cnt) cudaFree(h->fe_cnt), h->fe_cnt = nullptr;
-    cudaError_t e = cudaMalloc(&h->fe_part, (size_t)tiles * ksplit * npad * 128 * 4);
-    if (e == cudaSuccess) e = cudaMalloc(&h->fe_cnt, (size_t)tiles * 4);
-    if (e == cudaSuccess) e = cudaMemset(h->fe_cnt, 0, (size_t)tiles * 4);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      h->fe_hidden = 0;
-      return h->fail(NOSA_ERR_OOM, "front-end split partials");
-    }
     h->fe_hidden = hidden;
     h->fe_ksplit = ksplit;
-    h->fe_stages = stages;
+    h->fe_stages = q.stages;
   }
   const int ksplit = h->fe_ksplit;
   FrontArgs fa;
@@ -1213,8 +1208,6 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
   p.lse = lse;
   p.err = &h->st.stats->error;
   p.w_packed = static_cast<const uint8_t*>(w);
-  p.part = static_cast<float*>(h->fe_part);
-  p.tile_cnt = static_cast<int*>(h->fe_cnt);
   if (!frontend_encode(fa, x, sh.batch, hidden))
     return h->fail(NOSA_ERR_INVALID_ARG, "tensor-map encoding of x failed");
   StepArgs args;

@@ -73,7 +73,7 @@ struct FrontParams {
   int F, Fpad;      // packed rows of W ((Hq + 2 Hkv) d + Hkv) and rows padded to the tile
   int D;            // hidden width (multiple of 64)
   int kblocks;      // D / 64
-  int ksplit;       // splits of the hidden width per row tile (<= kblocks)
+  int ksplit;       // splits of the hidden width (<= min(kblocks, 8)): one cluster per row tile
   int tiles;        // Fpad / 128
   int npad;         // batch padded to a multiple of 16 (the MMA's N)
   int tmem_cols;    // tensor-memory columns allocated (power of two >= max(32, npad))
@@ -85,8 +85,6 @@ struct FrontParams {
   float* lse;
   int* err;         // device error word
   const uint8_t* w_packed;  // weights in the packed tile layout (frontend_pack)
-  float* part;      // [tiles][ksplit][npad][128] fp32 split partials (scratch)
-  int* tile_cnt;    // [tiles] splits done (the last one sums; self-resetting)
 };
 struct FrontArgs {
   CUtensorMap tx;   // x [batch][D] bf16, box 64 x npad, 128-byte swizzle
@@ -101,8 +99,8 @@ bool frontend_encode(FrontArgs& fa, const void* x, int batch, int D);
 size_t frontend_packed_bytes(int F, int D);
 cudaError_t launch_frontend_pack(const void* w, void* packed, int F, int D, cudaStream_t stream);
 const void* frontend_kernel_ptr();
-// Resident front-end CTAs per SM with this batch padding and ring depth (0 on error).
-int frontend_occupancy(int npad, int stages);
+// Clusters of the front-end that can be resident at once for these parameters (0 on error).
+int frontend_max_clusters(const FrontParams& p);
 
 // Training-time forward (k_prefill.cu): byte offsets into the caller's workspace.
 struct PrefillLayout {
