@@ -326,6 +326,9 @@ struct nosa_handle {
   // gather (highest), attention over kept slots (lowest), attention over filled
   // slots (medium); events order them per unit chunk.
   cudaStream_t s_sco = nullptr, s_sel = nullptr, s_gat = nullptr, s_att = nullptr, s_new = nullptr;
+  cudaStream_t s_gat2 = nullptr;  // gathers of odd chunks (fused step)
+  cudaEvent_t ev_jgat2 = nullptr;
+  int gather_streams = 2;
   cudaEvent_t ev_in = nullptr, ev_att = nullptr, ev_new = nullptr;
   cudaEvent_t ev_app = nullptr;  // the step's append is done
   // Fused step: chunk c is scored and selected on its own stream (priority
@@ -439,8 +442,10 @@ void free_all(nosa_handle* h) {
     if (h->ev_sel[c]) cudaEventDestroy(h->ev_sel[c]), h->ev_sel[c] = nullptr;
     if (h->ev_gat[c]) cudaEventDestroy(h->ev_gat[c]), h->ev_gat[c] = nullptr;
   }
-  for (cudaStream_t* t : {&h->s_sco, &h->s_sel, &h->s_gat, &h->s_att, &h->s_new, &h->s_cap})
+  for (cudaStream_t* t : {&h->s_sco, &h->s_sel, &h->s_gat, &h->s_att, &h->s_new, &h->s_cap,
+                          &h->s_gat2})
     if (*t) cudaStreamDestroy(*t), *t = nullptr;
+  if (h->ev_jgat2) cudaEventDestroy(h->ev_jgat2), h->ev_jgat2 = nullptr;
 }
 
 // Events of one step: e0 start (caller's stream); e1 after the append (scoring
@@ -655,12 +660,12 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // growing by NOSA_CHUNK_GROWTH, else by the unit count. Measured on GB300:
   // every chunk adds a selection tail and four launches, which pay off only when
   // the units are many (64 units: one chunk, 55 us against 71 us with five; 128
-  // units: two; 256 units: 1,2,3,4,1, small first chunks so that the first gather
-  // starts early and a small last one so that little attention is left after the
-  // last gather).
+  // units: two; 256 units: 0.5,1,2,3,3,1, small first chunks so that the first
+  // gather starts early and a small last one so that little attention is left
+  // after the last gather).
   std::vector<double> weights = s.U <= 96 ? std::vector<double>{1}
                                 : s.U <= 192 ? std::vector<double>{1, 1}
-                                             : std::vector<double>{1, 2, 3, 4, 1};
+                                             : std::vector<double>{0.5, 1, 2, 3, 3, 1};
   if (const char* g = std::getenv("NOSA_UNIT_CHUNKS")) {
     const int v = std::atoi(g);
     if (v > 0) {
@@ -723,6 +728,17 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // selection stream.
   const int prio_sel = (prio_hi < prio_mid) ? prio_hi + 1 : prio_hi;
   e = cudaStreamCreateWithPriority(&h->s_gat, cudaStreamNonBlocking, prio_hi);
+  // A second gather stream (fused step; NOSA_GATHER_STREAMS=1: one): the chunks'
+  // gathers alternate between the two, so chunk c + 1's starts as soon as its
+  // selection exists instead of after chunk c's gather kernel ends (GB300,
+  // 8B-offload: 280 us against 292 us per step).
+  if (const char* g = std::getenv("NOSA_GATHER_STREAMS"))
+    if (std::atoi(g) == 1) h->gather_streams = 1;
+  if (!h->fused_select) h->gather_streams = 1;
+  if (e == cudaSuccess && h->gather_streams == 2) {
+    e = cudaStreamCreateWithPriority(&h->s_gat2, cudaStreamNonBlocking, prio_hi);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_jgat2, cudaEventDisableTiming);
+  }
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sel, cudaStreamNonBlocking, prio_sel);
   if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->s_sco, cudaStreamNonBlocking, prio_mid);
   // (the filled-slot attention of a fused step stays below every chunk's scoring:
@@ -896,11 +912,12 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     a.unit_base = h->cu_base[c];
     a.unit_count = h->cu_count[c];
     // gather of chunk c (host link)
-    err = cudaStreamWaitEvent(h->s_gat, h->ev_sel[c], 0);
-    if (ev && c == 0) mark(ev[4], h->s_gat);
-    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], c, h->s_gat);
-    if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], h->s_gat);
-    if (ev && c == h->nchunks - 1) mark(ev[5], h->s_gat);
+    cudaStream_t tg = (h->gather_streams == 2 && (c & 1)) ? h->s_gat2 : h->s_gat;
+    err = cudaStreamWaitEvent(tg, h->ev_sel[c], 0);
+    if (ev && c == 0) mark(ev[4], tg);
+    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], c, tg);
+    if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], tg);
+    if (ev && c == h->nchunks - 1) mark(ev[5], tg);
     // attention over the slots kept from the previous step, plus the tail (fused
     // step: on the chunk's own stream, so chunks do not wait for one another)
     cudaStream_t ta = fused ? h->s_katt[c] : h->s_att;
@@ -955,6 +972,10 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
       if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jch[c], 0);
     }
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_jgat, h->s_gat);
+    if (h->gather_streams == 2 && h->nchunks >= 2) {  // the second gather stream
+      if (err == cudaSuccess) err = cudaEventRecord(h->ev_jgat2, h->s_gat2);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jgat2, 0);
+    }
     if (err == cudaSuccess) err = cudaStreamWaitEvent(origin, h->ev_jgat, 0);
   }
   if (ev) mark(ev[7], origin);
