@@ -491,7 +491,7 @@ def run_gpu(args, rank, world, local_rank):
     import trainable_sparse_attention_decode_gb300 as nosa
 
     torch.cuda.set_device(local_rank)
-    w0 = synth.WORKLOADS[args.workload]
+    w0 = synth.WORKLOADS[args.workload].with_(q_stationary=not args.q_innovation_start)
     budget = None
     if args.hbm_budget:
         wb = w0.with_(k_e=0) if args.mode == "infllmv2" else w0
@@ -751,6 +751,8 @@ def run_gpu(args, rank, world, local_rank):
                          % (w.units * w.k * 33024 / 2 ** 20,
                             w.units * n_cand * 4 * w.head_dim * 4 / 2 ** 20, L2_BYTES >> 20),
                    "parallelism": f"replicas x{world} (independent requests per GPU)",
+                   "queries": "AR(1), rho %g, %s" % (w.rho, "stationary start" if w.q_stationary
+                                                     else "started from one innovation"),
                    **(budget or {})},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(dom_bytes / (dom_us * 1e-6) / 1e9, 1),
                      "peak": peak, "unit": "GB/s",
@@ -1108,6 +1110,8 @@ def main():
                     help="run the workload's whole decode horizon and report this many "
                          "windows along it (tokens/s, recall, locality)")
     ap.add_argument("--prompt", type=int, default=0, help="override the workload's prompt")
+    ap.add_argument("--q-innovation-start", action="store_true",
+                    help="AR(1) queries from q_0 = eps_0 instead of their stationary distribution")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

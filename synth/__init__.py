@@ -23,9 +23,13 @@ checked against this file bit for bit):
 * Keys: ``k = c[b, h, block(t)] + 0.5 * n[b, h, t]``, one centre ``c`` per
   (request, KV head, 64-token block) and i.i.d. noise ``n``; exact in fp32.
 * Values ``v ~ N(0, 1)``; eviction logits ``e ~ N(0, 1)`` (fp32, fixed at write).
-* Queries: AR(1) per (request, query head, dim), ``q_0 = eps_0``,
+* Queries: AR(1) per (request, query head, dim), started in its stationary
+  distribution: ``q_0 = a * eps_0`` with ``a = 1 / sqrt(1 - rho**2)`` (fp64; the
+  process then has the same variance and lag-1 correlation rho at every step),
   ``q_s = rho * q_{s-1} + eps_s`` in fp64 (a product, then a sum: no fused
-  multiply-add), stored as fp64 -> fp32 (RNE) -> dtype.
+  multiply-add), stored as fp64 -> fp32 (RNE) -> dtype. ``q_stationary=False``
+  starts from ``q_0 = eps_0`` instead (variance 1 growing to ``a**2`` over the
+  first steps).
 * bf16 storage rounds fp32 to nearest even.
 * Real-valued front-end inputs (``hidden_real``, ``proj_weights_real``):
   normals of the hidden-state and weight streams with head field 1 (the integer
@@ -45,6 +49,7 @@ CUDA twin) writes.
 from __future__ import annotations
 
 from dataclasses import dataclass, replace
+import math
 import numpy as np
 
 __all__ = [
@@ -92,6 +97,7 @@ class Workload:
     sub_block: int = 16
     seed: int = 0
     request_base: int = 0  # index of request 0 in the job (ranks of a multi-GPU job shard requests)
+    q_stationary: bool = True  # AR(1) queries start in their stationary distribution
 
     @property
     def group(self) -> int:
@@ -212,6 +218,12 @@ def evict(w: Workload, b: int, h: int, t0: int, n: int) -> np.ndarray:
     return normals(w.seed, STREAM_EVICT, _req(w, b), h, t, 0).astype(np.float32)
 
 
+def q_start_scale(w: Workload) -> float:
+    """Factor a on the first innovation of the AR(1) queries: 1 / sqrt(1 - rho^2)
+    (stationary start, fp64), or 1."""
+    return 1.0 / math.sqrt(1.0 - w.rho * w.rho) if w.q_stationary else 1.0
+
+
 def queries(w: Workload, b: int, heads, steps: int) -> np.ndarray:
     """AR(1) queries of request b for the given query heads: [steps][len(heads)][d] storage."""
     heads = np.asarray(list(heads), dtype=np.int64)
@@ -223,7 +235,7 @@ def queries(w: Workload, b: int, heads, steps: int) -> np.ndarray:
     for s in range(steps):
         eps = normals(w.seed, STREAM_QINNOV, a, heads[:, None], s, dim)
         if q is None:
-            q = eps
+            q = np.float64(q_start_scale(w)) * eps
         else:
             q = np.float64(w.rho) * q
             q = q + eps

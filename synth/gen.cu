@@ -64,10 +64,11 @@ __global__ void kv_kernel(T* k, T* v, float* e, int batch, int hkv, int d, long 
   }
 }
 
-// q: [steps][batch][hq][d], AR(1) over steps, fp64 state (no fused multiply-add).
+// q: [steps][batch][hq][d], AR(1) over steps, fp64 state (no fused multiply-add);
+// the first innovation is scaled by a0 (1 / sqrt(1 - rho^2) for a stationary start).
 template <typename T>
-__global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, uint64_t smix,
-                         int b0) {
+__global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, double a0,
+                         uint64_t smix, int b0) {
   const int total = batch * hq * d;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= total) return;
@@ -75,7 +76,7 @@ __global__ void q_kernel(T* q, int batch, int hq, int d, int steps, double rho, 
   double x = 0.0;
   for (int s = 0; s < steps; ++s) {
     const double eps = ih_normal(smix, 4, b, g, s, dim);
-    x = (s == 0) ? eps : __dadd_rn(__dmul_rn(rho, x), eps);
+    x = (s == 0) ? __dmul_rn(a0, eps) : __dadd_rn(__dmul_rn(rho, x), eps);
     q[(long long)s * total + i] = store_as<T>(x);
   }
 }
@@ -144,18 +145,18 @@ int synth_kv(void* k, void* v, float* e, int batch, int hkv, int d, long long t0
   return (int)cudaGetLastError();
 }
 
-int synth_queries(void* q, int batch, int hq, int d, int steps, double rho,
+int synth_queries(void* q, int batch, int hq, int d, int steps, double rho, double a0,
                   unsigned long long seed, int dtype, int b0, void* stream) {
   const uint64_t smix = seed_mix(seed);
   const int total = batch * hq * d;
   cudaStream_t s = (cudaStream_t)stream;
   if (total == 0 || steps == 0) return 0;
   if (dtype == 0)
-    q_kernel<float><<<(total + 127) / 128, 128, 0, s>>>((float*)q, batch, hq, d, steps, rho, smix,
-                                                         b0);
+    q_kernel<float><<<(total + 127) / 128, 128, 0, s>>>((float*)q, batch, hq, d, steps, rho, a0,
+                                                         smix, b0);
   else
     q_kernel<__nv_bfloat16><<<(total + 127) / 128, 128, 0, s>>>((__nv_bfloat16*)q, batch, hq, d,
-                                                                 steps, rho, smix, b0);
+                                                                 steps, rho, a0, smix, b0);
   return (int)cudaGetLastError();
 }
 

@@ -10,7 +10,7 @@ import ctypes as C
 import os
 import subprocess
 
-from . import Workload
+from . import Workload, q_start_scale
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.cu")
@@ -48,6 +48,7 @@ def _get():
         L.synth_proj_weights.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_ulonglong, C.c_void_p]
         L.synth_queries.restype = C.c_int
         L.synth_queries.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double,
+                                    C.c_double,
                                     C.c_ulonglong, C.c_int, C.c_int, C.c_void_p]
         _lib = L
     return _lib
@@ -87,6 +88,7 @@ def queries(w: Workload, steps: int, device="cuda"):
     import torch
     q = torch.empty((steps, w.batch, w.n_q_heads, w.head_dim), dtype=_torch_dtype(w), device=device)
     err = _get().synth_queries(q.data_ptr(), w.batch, w.n_q_heads, w.head_dim, steps, w.rho,
+                               q_start_scale(w),
                                w.seed, 0 if w.dtype == "f32" else 1, w.request_base,
                                torch.cuda.current_stream().cuda_stream)
     if err:

@@ -55,17 +55,31 @@ def test_queries_ar1():
     w = synth.WORKLOADS["tiny-f32"].with_(head_dim=64)
     q = synth.queries(w, 0, range(4), 400).astype(np.float64)
     eps0 = synth.normals(0, synth.STREAM_QINNOV, 0, np.arange(4)[:, None], 0, np.arange(64)[None, :])
-    assert np.array_equal(q[0], eps0.astype(np.float32))
+    a = 1.0 / np.sqrt(1.0 - 0.95 ** 2)  # stationary start: Var q_0 = 1 / (1 - rho^2)
+    assert np.array_equal(q[0], (a * eps0).astype(np.float32))
     lag1 = np.mean([np.corrcoef(q[:-1, 0, j], q[1:, 0, j])[0, 1] for j in range(64)])
     assert lag1 == pytest.approx(0.95, abs=0.05)
     # one more step by hand, from the definition
     eps5 = synth.normals(0, synth.STREAM_QINNOV, 0, np.arange(4)[:, None], 5, np.arange(64)[None, :])
-    qq = eps0
+    qq = a * eps0
     for s in range(1, 6):
         qq = 0.95 * qq + synth.normals(0, synth.STREAM_QINNOV, 0, np.arange(4)[:, None], s,
                                        np.arange(64)[None, :])
     assert np.array_equal(q[5], qq.astype(np.float32))
     assert eps5.shape == (4, 64)
+
+
+def test_queries_stationary_from_the_first_step():
+    # the variance of q_s is 1 / (1 - rho^2) at every step, so early steps look
+    # like late ones; the unnormalised start grows from 1 instead
+    w = synth.WORKLOADS["1b-bf16"].with_(dtype="f32")
+    q = synth.queries(w, 0, range(w.n_q_heads), 200).astype(np.float64)
+    var = (q ** 2).mean(axis=(1, 2))
+    target = 1.0 / (1.0 - w.rho ** 2)
+    assert var[:5].mean() == pytest.approx(target, rel=0.15)
+    assert var[150:].mean() == pytest.approx(target, rel=0.15)
+    q0 = synth.queries(w.with_(q_stationary=False), 0, range(w.n_q_heads), 3).astype(np.float64)
+    assert (q0[0] ** 2).mean() == pytest.approx(1.0, rel=0.15)
 
 
 def test_request_base_offsets_the_request_field():
