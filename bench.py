@@ -908,30 +908,56 @@ def run_trace(args, rank, world, local_rank):
         t += m
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device="cuda")
-    q = synth.gpu.queries(w, n)
-    kk, vv, ee = synth.gpu.kv(w, w.prompt, n, step_major=True)
+    if args.frontend:  # steps from hidden states: the first kernel is the fused front-end
+        D = synth.hidden_width(w)
+        Wf = nosa.nosa_frontend_pack(cfg, synth.gpu.proj_weights(w, D))
+        x = synth.gpu.hidden(w, w.prompt, n, D)
+        step = lambda s_: nosa.nosa_decode_step_hidden(h, x[s_], Wf, out, None)
+    else:
+        q = synth.gpu.queries(w, n)
+        kk, vv, ee = synth.gpu.kv(w, w.prompt, n, step_major=True)
+        step = lambda s_: nosa.nosa_decode_step(h, q[s_], kk[s_], vv[s_], ee[s_], out)
     for s_ in range(args.warmup):
-        nosa.nosa_decode_step(h, q[s_], kk[s_], vv[s_], ee[s_], out)
-    names = {0: "append"}
+        step(s_)
+    names = {0: "front-end" if args.frontend else "append", 41: "front-end main loop done",
+             42: "front-end epilogue done"}
     for c in range(8):
         names.update({1 + c: f"score+select {c}", 9 + c: f"select {c}", 17 + c: f"gather {c}",
                       25 + c: f"attention kept {c}", 33 + c: f"attention filled {c}"})
     steps = []
     for s_ in range(args.warmup, n):
         hb0 = nosa.nosa_stats(h)["host_bytes"]
-        nosa.nosa_decode_step(h, q[s_], kk[s_], vv[s_], ee[s_], out)
+        step(s_)
         torch.cuda.synchronize()
         hb = nosa.nosa_stats(h)["host_bytes"] - hb0
         tr = np.frombuffer(nosa.nosa_debug_read(h, "TRACE").tobytes(), np.uint64).reshape(-1, 2)
         used = [i for i in range(tr.shape[0]) if int(tr[i, 0]) != 0xFFFFFFFFFFFFFFFF]
         t0 = min(int(tr[i, 0]) for i in used)
-        launches = sorted(((names[i], round((int(tr[i, 0]) - t0) / 1e3, 1),
+        launches = sorted(((names.get(i, f"slot {i}"), round((int(tr[i, 0]) - t0) / 1e3, 1),
                             round((int(tr[i, 1]) - t0) / 1e3, 1)) for i in used), key=lambda x: x[1])
         steps.append({"step": s_, "span_us": max(x[2] for x in launches), "host_bytes": hb,
                       "launches": launches})
     nosa.nosa_destroy(h)
-    return {"mode": "trace", "config": {"workload": w.name, "batch": w.batch},
-            "steps": steps}
+    line = {"mode": "trace" + ("+frontend" if args.frontend else ""),
+            "config": {"workload": w.name, "batch": w.batch}, "steps": steps}
+    if args.frontend:
+        # the front-end kernel's own span (first CTA start to last CTA end) per
+        # traced step, and its rate on the algorithmic bytes of one launch
+        us = [dict((x[0], x[2] - x[1]) for x in st["launches"])["front-end"] for st in steps]
+        phases = []
+        for st in steps:
+            at = {x[0]: (x[1], x[2]) for x in st["launches"]}
+            f0 = at["front-end"][0]
+            phases.append({k.replace("front-end ", ""): [round(a - f0, 1), round(b - f0, 1)]
+                           for k, (a, b) in at.items() if k.startswith("front-end ")})
+        nbytes = frontend_bytes_per_launch(w, synth.hidden_width(w))
+        peak, kind = measured_peaks()
+        med = float(np.median(us))
+        line["frontend"] = {"kernel_us": us, "median_us": med, "bytes": nbytes,
+                            "phases_us (earliest, latest CTA)": phases,
+                            "hbm_gbs": round(nbytes / (med * 1e-6) / 1e9, 1),
+                            "frac_of_" + kind + "_peak": round(nbytes / (med * 1e-6) / 1e9 / peak, 4)}
+    return line
 
 
 # ---------------------------------------------------------------------------

@@ -203,8 +203,11 @@ nosa_status nosa_frontend_pack(const nosa_config* cfg, int32_t hidden, const voi
  *   out, lse, stream: as for nosa_decode_step.
  * x, w_packed, q_out and out need 16-byte alignment. UNSUPPORTED unless cfg->dtype is
  * NOSA_BF16 and batch <= 256 (or when the driver offers no tensor-map encoder);
- * OOM if the front-end's scratch (split partials, about ksplit * batch * F * 4
- * bytes) cannot be allocated on the first call. Other errors as nosa_decode_step.
+ * OOM if the front-end's query buffer cannot be allocated on the first call.
+ * Other errors as nosa_decode_step. The projection splits the hidden width over
+ * the CTAs of a thread-block cluster per 128-row tile of W (all clusters
+ * resident at once) and sums the splits through distributed shared memory in
+ * rank order.
  */
 nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidden,
                                     const void* w_packed, void* q_out, void* out, float* lse,

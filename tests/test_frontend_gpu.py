@@ -60,7 +60,7 @@ def test_1b_shape_sampled_units():
 
 
 def test_8b_offload_shape_sampled_units():
-    # hidden 4096, 6152 packed rows: 49 row tiles x 3 splits, the bench's shape
+    # hidden 4096, 6152 packed rows: 49 row tiles x 2 splits, the bench's shape
     w = synth.WORKLOADS["8b-offload-bf16"].with_(steps=20)
     _run(w, units=[7, 200], check_bytes=False)
 
@@ -70,6 +70,14 @@ def test_padded_batch_and_ragged_prompt():
     # mid sub-block
     w = synth.WORKLOADS["1b-bf16"].with_(batch=40, prompt=4096 + 17, steps=40)
     _run(w, units=[0, 161, 319])
+
+
+def test_max_batch():
+    # batch 256, the largest the front-end takes: N = 256 per MMA (256
+    # tensor-memory columns), the epilogue in eight chunks of 32 requests
+    w = synth.WORKLOADS["tiny-f32"].with_(name="tiny-bf16", dtype="bf16", batch=256,
+                                          prompt=300, steps=20)
+    _run(w, units=[0, 77, 255])
 
 
 def test_plain_steps_then_hidden_steps():
@@ -87,7 +95,7 @@ def test_real_valued_inputs_tiny():
 
 
 def test_real_valued_inputs_8b_shape():
-    # hidden 4096 (the bench's shape): 49 row tiles, cluster split-K over the hidden width
+    # hidden 4096 (the bench's shape): 49 row tiles, split-K over the hidden width
     w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=4, prompt=4096 + 50, steps=24)
     _run(w, units=[0, 13, 31], real=True)
 

@@ -196,6 +196,7 @@ __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" 
 
 __global__ void __launch_bounds__(kFrontThreads, 1)
     frontend_kernel(const __grid_constant__ CUtensorMap tx, Shape s, State st, FrontParams p) {
+  TraceScope trace_scope(st.trace, kTrAppend);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
     }
     epi_barrier();
     tc_fence_after();
+    if (tid2 == 0) trace_mark(st.trace, kTrFrontMain);
   }
 
   // Epilogue, per chunk of 32 requests. Each CTA of the cluster (the splits of
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
       }
       cluster_sync();
     }
+    if (threadIdx.x == 64) trace_mark(st.trace, kTrFrontEpi);
     tc_fence_before();
   }
 

@@ -295,6 +295,7 @@ struct StepGraph {
   cudaKernelNodeParams append_params{};
   int n_cap = 0;
   bool front = false;          // first node is the fused front-end (else the append)
+  int front_gen = 0;           // ... set up for this front-end configuration
   bool pending = false;        // timing events of the last launch not yet read
   cudaEvent_t done = nullptr;  // recorded after each launch: a rebuild waits for it
 };
@@ -362,6 +363,7 @@ struct nosa_handle {
   // Fused front-end (set up on the first nosa_decode_step_hidden of a width).
   void* q_buf = nullptr;     // [batch][Hq][d] bf16 step queries
   int fe_hidden = 0, fe_ksplit = 0, fe_stages = 0;
+  int fe_gen = 0;               // bumped when the front-end's launch shape changes
 
   nosa_status fail(nosa_status code, const std::string& msg) {
     err = msg;
@@ -1017,6 +1019,7 @@ cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args,
   g.append_node = node;
   g.n_cap = n_cap;
   g.front = front != nullptr;
+  g.front_gen = h->fe_gen;
   h->graph_builds += 1;
   return cudaSuccess;
 }
@@ -1034,7 +1037,8 @@ nosa_status run_step(nosa_handle* h, const StepArgs& args, const FrontArgs* fron
     StepGraph& g = h->timing ? h->graphs[r] : h->plain;
     cudaEvent_t* ev = h->timing ? h->gev[r] : nullptr;
     if (h->timing) harvest_set(h, ev, &g.pending);
-    if (g.exec == nullptr || g.front != (front != nullptr) || N >= g.n_cap ||
+    if (g.exec == nullptr || g.front != (front != nullptr) ||
+        (front != nullptr && g.front_gen != h->fe_gen) || N >= g.n_cap ||
         N < g.n_cap - kScoreCap) {
       err = build_step_graph(h, g, args, front, N, ev);
     } else {
@@ -1207,6 +1211,7 @@ nosa_status nosa_decode_step_hidden(nosa_handle* h, const void* x, int32_t hidde
     h->fe_hidden = hidden;
     h->fe_ksplit = ksplit;
     h->fe_stages = q.stages;
+    h->fe_gen += 1;
   }
   const int ksplit = h->fe_ksplit;
   FrontArgs fa;

@@ -187,7 +187,10 @@ struct State {
 // Trace slots of a decode step's launches (chunk c < 8).
 constexpr int kTraceSlots = 48;
 enum : int {
-  kTrAppend = 0, kTrScore = 1, kTrSelect = 9, kTrGather = 17, kTrAttnKept = 25, kTrAttnNew = 33
+  kTrAppend = 0, kTrScore = 1, kTrSelect = 9, kTrGather = 17, kTrAttnKept = 25, kTrAttnNew = 33,
+  // phases of the fused front-end (earliest and latest CTA at each point):
+  kTrFrontMain = 41,  // the main loop's accumulator complete
+  kTrFrontEpi = 42    // epilogue done
 };
 
 // Pinned host store placement (host_store.cu): the node to bind the store of a
@@ -374,6 +377,15 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Records a CTA's start on entry and its end when the scope closes (any return)
 // in a trace slot: the slot keeps the earliest start and the latest end. No-op
 // without a trace array or slot.
+// One point in time of one CTA (thread 0 of the calling group): the slot keeps
+// the earliest and the latest over the CTAs.
+__device__ __forceinline__ void trace_mark(unsigned long long* trace, int id) {
+  if (trace == nullptr) return;
+  const unsigned long long t = global_ns();
+  atomicMin(trace + 2 * id, t);
+  atomicMax(trace + 2 * id + 1, t);
+}
+
 struct TraceScope {
   unsigned long long* slot;
   __device__ __forceinline__ TraceScope(unsigned long long* trace, int id)
