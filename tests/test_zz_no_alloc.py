@@ -68,6 +68,52 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype, d, hq, hkv, batch, n
         assert torch.allclose(lse, ref_lse, rtol=0, atol=1e-5)
 
 
+@pytest.mark.parametrize("dtype,d,hq,hkv,batch,n_blocks,tail_len", [
+    ("bf16", 128, 32, 8, 4, 24, 41), ("f32", 64, 4, 1, 2, 9, 64)])
+def test_noalloc_matches_oracle(dtype, d, hq, hkv, batch, n_blocks, tail_len):
+    # the oracle's attend() over each unit's blocks and tail, element by element,
+    # with some table entries empty and one unit without any block
+    from nosa_harness import attn_close, to_f64
+    rng = np.random.default_rng(5)
+    U, G = batch * hkv, hq // hkv
+    pool = U * n_blocks + 1
+    units = np.zeros((pool + U, O.payload_bytes(64, d, dtype)), np.uint8)
+    toks = []
+    for i in range(pool + U):
+        k = synth.to_storage(rng.normal(size=(64, d)), dtype)
+        v = synth.to_storage(rng.normal(size=(64, d)), dtype)
+        e = rng.normal(size=64).astype(np.float32)
+        units[i] = O.encode_payload(k, v, e, dtype)
+        toks.append((synth.storage_to_f64(k, dtype), synth.storage_to_f64(v, dtype),
+                     e.astype(np.float64)))
+    tab = rng.integers(0, pool, size=(U, n_blocks)).astype(np.int32)
+    tab[rng.random(size=(U, n_blocks)) < 0.15] = -1
+    tab[1] = -1
+    q = synth.to_storage(rng.normal(size=(batch, hq, d)) * 2, dtype)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    qt = torch.from_numpy(q.view(np.int16) if dtype == "bf16" else q).cuda().view(dt)
+    cfg = nosa.nosa_config(batch, hq, hkv, d, dtype, 8, 4, 4096)
+    out = torch.full((batch, hq, d), float("nan"), dtype=dt, device="cuda")
+    lse = torch.full((batch, hq), float("nan"), dtype=torch.float32, device="cuda")
+    nosa.nosa_sparse_attention_noalloc(cfg, torch.from_numpy(units[:pool].reshape(-1)).cuda(),
+                                       torch.from_numpy(tab).cuda(),
+                                       torch.from_numpy(units[pool:].reshape(-1)).cuda(),
+                                       tail_len, qt, out, lse)
+    torch.cuda.synchronize()
+    out_np, lse_np = to_f64(out), lse.cpu().numpy()
+    q64 = synth.storage_to_f64(q, dtype)
+    for u in range(U):
+        b, h = divmod(u, hkv)
+        kt, vt, et = toks[pool + u]
+        parts = [toks[i] for i in tab[u] if i >= 0] + [(kt[:tail_len], vt[:tail_len], et[:tail_len])]
+        rows = slice(h * G, (h + 1) * G)
+        o_ref, lse_ref = O.attend(q64[b, rows], np.concatenate([p_[0] for p_ in parts]),
+                                  np.concatenate([p_[1] for p_ in parts]),
+                                  np.concatenate([p_[2] for p_ in parts]))
+        assert attn_close(out_np[b, rows], o_ref, dtype) <= 1.0, f"unit {u}"
+        assert np.max(np.abs(lse_np[b, rows] - lse_ref)) < 1e-4, f"unit {u}"
+
+
 def test_noalloc_rejects_shapes_beyond_the_static_scratch():
     # 8192 units x 8 heads x 128 dims of fp32 partials is 32 MiB per split: more
     # than the 16 MiB array whatever the split count.
