@@ -920,7 +920,9 @@ def run_trace(args, rank, world, local_rank):
     for s_ in range(args.warmup):
         step(s_)
     names = {0: "front-end" if args.frontend else "append", 41: "front-end main loop done",
-             42: "front-end epilogue done"}
+             42: "front-end epilogue done", 43: "chunk 0 selection begins",
+             44: "chunk 0 selection done", 45: "chunk 0 Gamma_e done",
+             46: "chunk 0 Gamma_q done", 47: "chunk 0 lists written"}
     for c in range(8):
         names.update({1 + c: f"score+select {c}", 9 + c: f"select {c}", 17 + c: f"gather {c}",
                       25 + c: f"attention kept {c}", 33 + c: f"attention filled {c}"})

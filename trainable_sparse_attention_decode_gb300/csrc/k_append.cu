@@ -38,7 +38,6 @@ __global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st, Ste
   const int t = a.L_old;
   const int blk = t / s.B, pos = t % s.B;
   uint8_t* cur = st.tail + ((long long)u * 2 + (blk & 1)) * s.payload;
-  if (u == 0 && threadIdx.x < kMaxChunks) st.work_count[threadIdx.x] = 0;
   if (u == 0 && threadIdx.x == 0) {
     StepIO io;
     io.q = a.q;

@@ -303,7 +303,6 @@ __global__ void __launch_bounds__(kFrontThreads, 1)
       io.tail_off = (long long)(blk & 1) * s.payload;
       *st.io = io;
     }
-    if (cta == 0 && tid2 < kMaxChunks) st.work_count[tid2] = 0;
     if (pos == 0 && blk > 0) {  // the previous block becomes a candidate
       const int cb = blk - 1;
       const int nvec = (int)(s.payload / 16);

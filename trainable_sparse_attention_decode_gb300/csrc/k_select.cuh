@@ -54,6 +54,14 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* total)
 
 constexpr int kSmallCut = 256;  // candidates ranked directly (one per thread)
 
+// Rank (1-based) of the key kept as the next step's Gamma_q threshold hint for a
+// cut of `need`: far enough below the cut that the next step's scores rarely
+// drift past it (4 need), while the candidates at or above it stay within the
+// directly ranked kSmallCut.
+__device__ __forceinline__ int hint_rank(int need) {
+  return min(4 * need, max(2 * need, kSmallCut / 2));
+}
+
 struct SelShared {
   uint32_t hist[256];
   int warp_tot[kSelWarps];
@@ -258,7 +266,7 @@ __device__ void near_tie_stat(const uint32_t* key, const uint8_t* flag, uint8_t 
 // by (key, lower index first); the `need` best get setbit. Exact whenever it
 // answers; returns false (nothing marked) otherwise, and the caller runs the
 // radix cut. Also counts a near-tie at the cut (as near_tie_stat) and leaves in
-// *hint_out the key of rank min(count, 2 need) - 1 for the next step.
+// *hint_out the key of rank min(count, hint_rank(need)) for the next step.
 // Candidates: (flag & tmask) == tval. Requires 1 <= need < number of candidates.
 __device__ bool mark_top_hint(const uint32_t* key, uint8_t* flag, uint8_t tmask, uint8_t tval,
                               uint8_t setbit, int n, int need, uint32_t hint, SelShared& sh,
@@ -303,7 +311,7 @@ __device__ bool mark_top_hint(const uint32_t* key, uint8_t* flag, uint8_t tmask,
     base += tot;
   }
   __syncthreads();
-  const int r_hint = min(count, 2 * need) - 1;
+  const int r_hint = min(count, hint_rank(need)) - 1;
   if (threadIdx.x < count) {
     const unsigned long long c = sh.comp[threadIdx.x];
     int rank = 0;
@@ -328,14 +336,14 @@ __device__ bool mark_top_hint(const uint32_t* key, uint8_t* flag, uint8_t tmask,
 // at the start too, valid when nw <= NT.
 template <int NT>
 __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
-                              int cold, int ubase, int chunk, const uint32_t* selm, int* s2b_s,
+                              int cold, int gamma, const uint32_t* selm, int* s2b_s,
                               uint32_t res0) {
   constexpr int kDiffThreads = NT;
   constexpr int kDiffWarps = NT / 32;
   __shared__ int load_blk[kMaxK];
   __shared__ int free_list[kMaxK];
   __shared__ int warp_tot[kDiffWarps];
-  __shared__ int s_base, s_tail_loaded;
+  __shared__ int s_tail_loaded;
   uint32_t* resm = st.resmask + (long long)u * s.W;
   int32_t* s2b = st.slot2blk + (long long)u * s.k;
   const int nw = (n + 31) >> 5;
@@ -388,10 +396,7 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
     s2b_s[free_list[j]] = -1;
   }
   for (int w = threadIdx.x; w < s.W; w += kDiffThreads) resm[w] = (w < nw) ? selm[w] : 0u;
-  if (threadIdx.x == 0) {
-    st.nload[u] = nload;
-    s_base = chunk >= 0 ? atomicAdd(&st.work_count[chunk], nload) : 0;
-  }
+  if (threadIdx.x == 0) st.nload[u] = nload;  // the gather numbers the chunk's entries from these
   __syncthreads();
   // Attention tables: slots kept from the previous step (usable while the gather
   // runs) and slots that this step's loads fill.
@@ -407,14 +412,9 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
       tnew[j] = -1;
     }
   }
-  int32_t* work = st.work + (long long)ubase * s.k;  // this chunk's list (none: chunk < 0)
-  if (chunk >= 0)
-    for (int j = threadIdx.x; j < nload; j += kDiffThreads) work[s_base + j] = u * s.k + j;
-
   if (threadIdx.x == 0) {
     const int n_tail = s_tail_loaded;
     const int n_host = nload - n_tail;
-    const int gamma = st.nsel[2 * u] + st.nsel[2 * u + 1];
     DevStats* ds = st.stats;
     atomicAdd(&ds->host_loads, (unsigned long long)n_host);
     atomicAdd(&ds->tail_loads, (unsigned long long)n_tail);
@@ -450,6 +450,16 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
   for (int sl = threadIdx.x; sl < s.k; sl += kSelThreads) s2b_s[sl] = st.slot2blk[(long long)u * s.k + sl];
   const uint32_t res0 =
       ((int)threadIdx.x < ((n + 31) >> 5)) ? st.resmask[(long long)u * s.W + threadIdx.x] : 0u;
+  // The query-aware scores of the first kSqPre * kSelThreads candidates and the
+  // threshold hint, loaded with the eviction scores below (one round trip).
+  constexpr int kSqPre = 4;
+  float sqv[kSqPre];
+#pragma unroll
+  for (int r = 0; r < kSqPre; ++r) {
+    const int i = threadIdx.x + r * kSelThreads;
+    sqv[r] = (i < n) ? __ldcg(sq + i) : 0.f;
+  }
+  const uint32_t qhint0 = (st.qhint != nullptr) ? st.qhint[u] : 0u;
 
   int my_elig = 0;
   for (int i = threadIdx.x; i < n; i += kSelThreads) {
@@ -469,22 +479,30 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
       near_tie_stat(key, flag, 1, 1, 2, n, sh, &st.stats->near_ties);
   }
 
-  for (int i = threadIdx.x; i < n; i += kSelThreads) key[i] = ordered_key(__ldcg(sq + i));
+  if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0E);
+#pragma unroll
+  for (int r = 0; r < kSqPre; ++r) {
+    const int i = threadIdx.x + r * kSelThreads;
+    if (i < n) key[i] = ordered_key(sqv[r]);
+  }
+  for (int i = threadIdx.x + kSqPre * kSelThreads; i < n; i += kSelThreads)
+    key[i] = ordered_key(__ldcg(sq + i));
   __syncthreads();
   const int cnt_q = n - need_e;
   const int need_q = min(s.k - need_e, cnt_q);
   // Gamma_q: from the previous step's threshold hint when it brackets the cut,
-  // else the radix cut (then the hint for the next step is the key of rank 2 need)
+  // else the radix cut (then the hint for the next step is the key of rank
+  // hint_rank(need))
   bool cut = false;
   if (need_q > 0 && need_q < cnt_q && st.qhint != nullptr)
-    cut = mark_top_hint(key, flag, 2, 0, 4, n, need_q, st.qhint[u], sh, &st.stats->near_ties,
+    cut = mark_top_hint(key, flag, 2, 0, 4, n, need_q, qhint0, sh, &st.stats->near_ties,
                         st.qhint + u);
   if (!cut) {
     mark_top(key, flag, 2, 0, 4, n, need_q, cnt_q, sh);
     if (need_q > 0 && need_q < cnt_q) {
       near_tie_stat(key, flag, 2, 0, 4, n, sh, &st.stats->near_ties);
       if (st.qhint != nullptr) {
-        const int need2 = min(2 * need_q, cnt_q);
+        const int need2 = min(hint_rank(need_q), cnt_q);
         uint32_t thr2 = 0u;
         if (need2 < cnt_q) {
           int take_eq, count_eq;
@@ -495,6 +513,7 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
     }
   }
 
+  if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0Q);
   // Gamma_e ascending, then Gamma_q ascending; eligibility and selection masks.
   int32_t* sel = st.sel + (long long)u * s.k;
   int run_e = 0, run_q = 0;
@@ -524,7 +543,8 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
     st.nsel[2 * u + 1] = need_q;
   }
   __syncthreads();  // the selection mask copy and nsel are visible to the whole CTA
-  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, ubase, chunk, key, s2b_s, res0);
+  if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0Emit);
+  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, need_e + need_q, key, s2b_s, res0);
 }
 
 }  // namespace

@@ -567,8 +567,6 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.slot2blk, U * k * 4);
   A(&st.loads, U * k * 3 * 4);
   A(&st.nload, U * 4);
-  A(&st.work, U * k * 4);
-  A(&st.work_count, kMaxChunks * 4);
   A(&st.block_tab, U * k * 4);
   A(&st.tab_new, U * k * 4);
   A(&st.att_cnt, U * 4);
@@ -605,7 +603,6 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(st.slot2blk, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.loads, 0, U * k * 3 * 4);
   if (e == cudaSuccess) e = cudaMemset(st.nload, 0, U * 4);
-  if (e == cudaSuccess) e = cudaMemset(st.work_count, 0, kMaxChunks * 4);
   if (e == cudaSuccess) e = cudaMemset(st.block_tab, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.tab_new, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.att_cnt, 0, U * 4);
@@ -919,7 +916,7 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     cudaStream_t tg = (h->gather_streams == 2 && (c & 1)) ? h->s_gat2 : h->s_gat;
     err = cudaStreamWaitEvent(tg, h->ev_sel[c], 0);
     if (ev && c == 0) mark(ev[4], tg);
-    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], c, tg);
+    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], h->cu_count[c], c, tg);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], tg);
     if (ev && c == h->nchunks - 1) mark(ev[5], tg);
     // attention over the slots kept from the previous step, plus the tail (fused

@@ -165,9 +165,7 @@ struct State {
   int32_t* nsel;       // [U][2]
   int32_t* slot2blk;   // [U][k]
   int32_t* loads;      // [U][k][3]         (block, slot, src)
-  int32_t* nload;      // [U]
-  int32_t* work;       // [U*k]             gather work list (entry = u*k + j)
-  int32_t* work_count; // [kMaxChunks]     entries per chunk (chunk c's list starts at c's first unit * k)
+  int32_t* nload;      // [U]               entries of the unit's load list
   int32_t* block_tab;  // [U][k]            slots kept from the previous step (slot pool index), -1 none
   int32_t* tab_new;    // [U][k]            slots filled by this step's loads, -1 none
   int32_t* att_cnt;    // [U]               split CTAs finished (the last one merges; self-resetting)
@@ -190,7 +188,13 @@ enum : int {
   kTrAppend = 0, kTrScore = 1, kTrSelect = 9, kTrGather = 17, kTrAttnKept = 25, kTrAttnNew = 33,
   // phases of the fused front-end (earliest and latest CTA at each point):
   kTrFrontMain = 41,  // the main loop's accumulator complete
-  kTrFrontEpi = 42    // epilogue done
+  kTrFrontEpi = 42,   // epilogue done
+  // the first chunk's fused selection, per unit (earliest and latest unit):
+  kTrSel0Begin = 43,  // the unit's scores complete, its selecting CTA starts
+  kTrSel0E = 45,      // ... Gamma_e marked
+  kTrSel0Q = 46,      // ... Gamma_q marked
+  kTrSel0Emit = 47,   // ... selection lists and masks written
+  kTrSel0End = 44     // its selection and set-difference done
 };
 
 // Pinned host store placement (host_store.cu): the node to bind the store of a
@@ -222,8 +226,9 @@ cudaError_t launch_select_setdiff(const Shape& s, const State& st, int cold, int
 bool score_select_fused_ok(const Shape& s);
 cudaError_t launch_score_select(const Shape& s, const State& st, int n_cap, int ubase, int ucount,
                                 int cold, int chunk, cudaStream_t stream, int max_ctas_per_sm = 0);
-cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int chunk,
-                          cudaStream_t stream);
+// Copies the load-list entries of units [ubase, ubase + ucount) (grid: CTAs).
+cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int ucount,
+                          int chunk, cudaStream_t stream);
 // Sets every trace slot's start to the maximum (the ends are zeroed by the caller).
 cudaError_t launch_trace_reset(unsigned long long* trace, cudaStream_t stream);
 // result[0] = error code of a bounded wait that nothing completes, result[1] = ms waited.
