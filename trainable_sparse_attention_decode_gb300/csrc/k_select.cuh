@@ -330,58 +330,67 @@ __device__ bool mark_top_hint(const uint32_t* key, uint8_t* flag, uint8_t tmask,
   return true;
 }
 
+// The set-difference of unit u, by warp 0 alone (the CTA's other warps return):
+// with at most a few hundred mask words and k <= 256 slots, lane-strided words,
+// shuffles and ballots do it without a block-wide barrier, which costs a
+// microsecond or more while the scoring kernels fill the SMs.
 // selm: the unit's selection mask words (this CTA's shared copy); s2b_s: a shared
-// copy of its slot table, loaded at the start of the selection and kept up to
-// date here; res0: the residency word of this thread (word threadIdx.x), loaded
-// at the start too, valid when nw <= NT.
+// copy of its slot table, kept up to date here; res_s: a shared copy of its
+// residency words, valid when nw <= NT (else they are read from the state).
 template <int NT>
 __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int just_completed,
                               int cold, int gamma, const uint32_t* selm, int* s2b_s,
-                              uint32_t res0) {
-  constexpr int kDiffThreads = NT;
-  constexpr int kDiffWarps = NT / 32;
+                              const uint32_t* res_s) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const unsigned below = (1u << lane) - 1u;
   __shared__ int load_blk[kMaxK];
   __shared__ int free_list[kMaxK];
-  __shared__ int warp_tot[kDiffWarps];
-  __shared__ int s_tail_loaded;
+  __shared__ uint32_t fresh[kMaxK / 32];  // slots this step's loads fill
   uint32_t* resm = st.resmask + (long long)u * s.W;
   int32_t* s2b = st.slot2blk + (long long)u * s.k;
   const int nw = (n + 31) >> 5;
-  if (threadIdx.x == 0) s_tail_loaded = 0;
 
   // Loads: selected and not held by a slot, ascending block index.
   int nload = 0;
-  for (int base = 0; base < nw; base += kDiffThreads) {
-    const int w = base + threadIdx.x;
-    const uint32_t rw = (nw <= kDiffThreads) ? res0 : ((w < nw) ? resm[w] : 0u);
-    uint32_t lw = (w < nw) ? (selm[w] & ~rw) : 0u;
-    int tot;
-    int pos = nload + block_excl_scan<kDiffWarps>(__popc(lw), warp_tot, &tot);
+  for (int w0 = 0; w0 < nw; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t lw = 0u;
+    if (w < nw) lw = selm[w] & ~((nw <= NT) ? res_s[w] : resm[w]);
+    const int c = __popc(lw);
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    int pos = nload + x - c;
     while (lw) {
-      const int bit = __ffs(lw) - 1;
-      load_blk[pos++] = w * 32 + bit;
+      load_blk[pos++] = w * 32 + __ffs(lw) - 1;
       lw &= lw - 1;
     }
-    nload += tot;
+    nload += __shfl_sync(0xffffffffu, x, 31);
   }
   // Free slots: empty, or holding a block outside Gamma; ascending slot index.
+  // (|Gamma| <= k, so there are at least nload of them.)
   int nfree = 0;
-  for (int base = 0; base < s.k; base += kDiffThreads) {
-    const int sl = base + threadIdx.x;
-    int f = 0;
+  for (int s0 = 0; s0 < s.k; s0 += 32) {
+    const int sl = s0 + lane;
+    bool f = false;
     if (sl < s.k) {
       const int b = s2b_s[sl];
       f = (b < 0) || !((selm[b >> 5] >> (b & 31)) & 1u);
     }
-    int tot;
-    const int ex = block_excl_scan<kDiffWarps>(f, warp_tot, &tot);
-    if (f) free_list[nfree + ex] = sl;
-    nfree += tot;
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (f) free_list[nfree + __popc(m & below)] = sl;
+    nfree += __popc(m);
   }
-  __syncthreads();
+  if (lane < kMaxK / 32) fresh[lane] = 0u;
+  __syncwarp();
 
   int32_t* loads = st.loads + (long long)u * s.k * 3;
-  for (int j = threadIdx.x; j < nload; j += kDiffThreads) {
+  bool tail_loaded = false;
+  for (int j = lane; j < nload; j += 32) {
     const int blk = load_blk[j], slot = free_list[j];
     const int src = (blk == just_completed) ? 1 : 0;
     loads[3 * j] = blk;
@@ -389,31 +398,28 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
     loads[3 * j + 2] = src;
     s2b[slot] = blk;
     s2b_s[slot] = blk;
-    if (src) s_tail_loaded = 1;
+    atomicOr(&fresh[slot >> 5], 1u << (slot & 31));
+    tail_loaded |= (src != 0);
   }
-  for (int j = nload + threadIdx.x; j < nfree; j += kDiffThreads) {
+  for (int j = nload + lane; j < nfree; j += 32) {
     s2b[free_list[j]] = -1;
     s2b_s[free_list[j]] = -1;
   }
-  for (int w = threadIdx.x; w < s.W; w += kDiffThreads) resm[w] = (w < nw) ? selm[w] : 0u;
-  if (threadIdx.x == 0) st.nload[u] = nload;  // the gather numbers the chunk's entries from these
-  __syncthreads();
+  for (int w = lane; w < s.W; w += 32) resm[w] = (w < nw) ? selm[w] : 0u;
+  if (lane == 0) st.nload[u] = nload;  // the gather numbers the chunk's entries from these
+  __syncwarp();
   // Attention tables: slots kept from the previous step (usable while the gather
   // runs) and slots that this step's loads fill.
   int32_t* tres = st.block_tab + (long long)u * s.k;
   int32_t* tnew = st.tab_new + (long long)u * s.k;
-  for (int sl = threadIdx.x; sl < s.k; sl += kDiffThreads) tres[sl] = (s2b_s[sl] >= 0) ? u * s.k + sl : -1;
-  __syncthreads();
-  for (int j = threadIdx.x; j < s.k; j += kDiffThreads) {
-    if (j < nload) {
-      tres[free_list[j]] = -1;
-      tnew[j] = u * s.k + free_list[j];
-    } else {
-      tnew[j] = -1;
-    }
+  for (int sl = lane; sl < s.k; sl += 32) {
+    const bool filled = (fresh[sl >> 5] >> (sl & 31)) & 1u;
+    tres[sl] = (!filled && s2b_s[sl] >= 0) ? u * s.k + sl : -1;
+    tnew[sl] = (sl < nload) ? u * s.k + free_list[sl] : -1;
   }
-  if (threadIdx.x == 0) {
-    const int n_tail = s_tail_loaded;
+  const int n_tail = __any_sync(0xffffffffu, tail_loaded) ? 1 : 0;
+
+  if (lane == 0) {
     const int n_host = nload - n_tail;
     DevStats* ds = st.stats;
     atomicAdd(&ds->host_loads, (unsigned long long)n_host);
@@ -450,6 +456,7 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
   for (int sl = threadIdx.x; sl < s.k; sl += kSelThreads) s2b_s[sl] = st.slot2blk[(long long)u * s.k + sl];
   const uint32_t res0 =
       ((int)threadIdx.x < ((n + 31) >> 5)) ? st.resmask[(long long)u * s.W + threadIdx.x] : 0u;
+  __shared__ uint32_t res_s[kSelThreads];
   // The query-aware scores of the first kSqPre * kSelThreads candidates and the
   // threshold hint, loaded with the eviction scores below (one round trip).
   constexpr int kSqPre = 4;
@@ -542,9 +549,10 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
     st.nsel[2 * u] = need_e;
     st.nsel[2 * u + 1] = need_q;
   }
-  __syncthreads();  // the selection mask copy and nsel are visible to the whole CTA
+  if ((int)threadIdx.x < ((n + 31) >> 5)) res_s[threadIdx.x] = res0;
+  __syncthreads();  // the selection mask copy, nsel and res_s are visible to the whole CTA
   if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0Emit);
-  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, need_e + need_q, key, s2b_s, res0);
+  setdiff_phase<kSelThreads>(s, st, u, n, just_completed, cold, need_e + need_q, key, s2b_s, res_s);
 }
 
 }  // namespace
