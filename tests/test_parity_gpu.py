@@ -148,7 +148,7 @@ def test_8b_longgen_sampled_units_long_horizon():
     assert st["max_host_loads_unit"] <= w.k - w.k_e
 
 
-@pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2"])
+@pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2", "0.5,1,2,3,3,1"])
 def test_unequal_chunks_every_unit(sizes, monkeypatch):
     # The step's unit chunks run concurrently and differ in split counts; every
     # unit (not a sample) is checked, so a partial buffer shared across chunks

@@ -253,14 +253,8 @@ __device__ void near_tie_stat(const uint32_t* key, const uint8_t* flag, uint8_t 
   __syncthreads();
 }
 
-// Set-difference of the unit's Gamma (selmask) against its slots (chunk < 0: no
-// gather work list is written). Writes the
-// load list (ascending block, paired by rank with the ascending free slots), the
-// new slot table and residency mask, the two attention block tables (slots kept
-// from the previous step; slots filled by this step's loads) and the gather
-// work list entries.
-// Gamma_q from a threshold hint (the key that admitted about twice the cut's size
-// at the unit's previous step): when at least `need` and at most kSmallCut
+// Gamma_q from a threshold hint (the key that admitted about four times the cut's
+// size at the unit's previous step): when at least `need` and at most kSmallCut
 // candidates have a key >= hint, the cut lies among them (every other key is
 // smaller), so they are compacted in index order and ranked against each other
 // by (key, lower index first); the `need` best get setbit. Exact whenever it
@@ -330,10 +324,14 @@ __device__ bool mark_top_hint(const uint32_t* key, uint8_t* flag, uint8_t tmask,
   return true;
 }
 
-// The set-difference of unit u, by warp 0 alone (the CTA's other warps return):
-// with at most a few hundred mask words and k <= 256 slots, lane-strided words,
-// shuffles and ballots do it without a block-wide barrier, which costs a
-// microsecond or more while the scoring kernels fill the SMs.
+// The set-difference of unit u against its slots, by warp 0 alone (the CTA's
+// other warps return). Writes the load list (ascending block, paired by rank with
+// the ascending free slots) and its length, the new slot table and residency
+// mask, and the two attention block tables (slots kept from the previous step;
+// slots filled by this step's loads). With at most a few hundred mask words and
+// k <= 256 slots, lane-strided words, shuffles and ballots do it without a
+// block-wide barrier, which costs a microsecond or more while the scoring kernels
+// fill the SMs.
 // selm: the unit's selection mask words (this CTA's shared copy); s2b_s: a shared
 // copy of its slot table, kept up to date here; res_s: a shared copy of its
 // residency words, valid when nw <= NT (else they are read from the state).
