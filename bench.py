@@ -57,6 +57,26 @@ def aggregate(seconds: float, tokens: int, world: int):
     return float(t.item()), int(n.item())
 
 
+def arm_config(w, world, budget=None):
+    """The `config` object of a decode line (both arms): the workload and how it
+    is laid out and run."""
+    n_cand = w.prompt // w.block
+    slot_mib = w.units * w.k * (64 * w.head_dim * 2 * (4 if w.dtype == "f32" else 2) + 256) / 2 ** 20
+    pk_mib = w.units * n_cand * 4 * w.head_dim * 4 / 2 ** 20
+    big = (slot_mib + pk_mib) * 2 ** 20 > L2_BYTES
+    return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
+            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k, "k_e": w.k_e,
+            "context_start": w.prompt,
+            "l2": ("inputs larger than L2 (slot pool %.0f MiB, pooled keys %.0f MiB > %d MiB)"
+                   if big else
+                   "inputs within L2 (slot pool %.1f MiB, pooled keys %.1f MiB < %d MiB): "
+                   "steps run with a warm L2") % (slot_mib, pk_mib, L2_BYTES >> 20),
+            "parallelism": f"replicas x{world} (independent requests per GPU)",
+            "queries": "AR(1), rho %g, %s" % (w.rho, "stationary start" if w.q_stationary
+                                              else "started from one innovation"),
+            **(budget or {})}
+
+
 def rank_requests(batch: int, world: int, rank: int):
     """Requests (first, count) of the job's world * batch that rank runs: weak
     scaling, every rank its own batch of requests, disjoint, covering the job."""
@@ -744,16 +764,8 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic (seeded counter-based generator; shapes of the workload)",
         "mode": args.mode + ("+pooled_bf16" if args.pooled_bf16 else "")
                 + ("+frontend" if args.frontend else ""),
-        "config": {"workload": w0.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
-                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k, "k_e": w.k_e,
-                   "context_start": w.prompt, "context_end": context_after,
-                   "l2": "inputs larger than L2 (slot pool %.0f MiB, pooled keys %.0f MiB > %d MiB)"
-                         % (w.units * w.k * 33024 / 2 ** 20,
-                            w.units * n_cand * 4 * w.head_dim * 4 / 2 ** 20, L2_BYTES >> 20),
-                   "parallelism": f"replicas x{world} (independent requests per GPU)",
-                   "queries": "AR(1), rho %g, %s" % (w.rho, "stationary start" if w.q_stationary
-                                                     else "started from one innovation"),
-                   **(budget or {})},
+        "config": arm_config(w0, world, budget),
+        "context_end": context_after,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(dom_bytes / (dom_us * 1e-6) / 1e9, 1),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(dom_bytes / (dom_us * 1e-6) / 1e9 / peak, 4),
@@ -1069,9 +1081,9 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     import synth
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS[args.workload].with_(q_stationary=not args.q_innovation_start)
     if args.batch:
-        w = w.with_(batch=args.batch)
+        w = w.with_(name=f"{w.name}-b{args.batch}", batch=args.batch)
     K, W = args.steps, args.warmup
     units = list(range(w.units))
     t0 = time.time()
@@ -1085,9 +1097,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(secs / K * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
-                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k": w.k,
-                       "k_e": w.k_e, "context_start": w.prompt},
+            "config": arm_config(w, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": procs,
                              "kind": "oracle",
                              "sample": f"the whole batch ({w.units} units) x {K} timed decode "
