@@ -148,6 +148,16 @@ def test_8b_longgen_sampled_units_long_horizon():
     assert st["max_host_loads_unit"] <= w.k - w.k_e
 
 
+def test_gather_numbers_entries_across_unit_tiles(monkeypatch):
+    # one chunk of 2 112 units: the gather numbers a chunk's load-list entries
+    # 2 048 units at a time in shared memory, so units on both sides of that
+    # boundary are checked (slot bytes included)
+    monkeypatch.setenv("NOSA_CHUNK_SIZES", "1")
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=264, prompt=64 * 12 + 9, steps=12, k=8, k_e=6)
+    st, _ = _run(w, units=[0, 2047, 2048, 2049, 2111])
+    assert st["host_loads"] > 0
+
+
 @pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2", "0.5,1,2,3,3,1"])
 def test_unequal_chunks_every_unit(sizes, monkeypatch):
     # The step's unit chunks run concurrently and differ in split counts; every
