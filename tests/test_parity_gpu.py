@@ -158,6 +158,20 @@ def test_gather_numbers_entries_across_unit_tiles(monkeypatch):
     assert st["host_loads"] > 0
 
 
+@pytest.mark.parametrize("env", [{"NOSA_FUSED_SELECT": "0"}, {"NOSA_GATHER_STREAMS": "1"},
+                                 {"NOSA_SELECT_HINT": "0"}, {"NOSA_GATHER_VEC": "32"}])
+def test_step_switches_every_unit(env, monkeypatch):
+    # The documented switches of the step (read at nosa_create) change launch
+    # shapes and schedules, never the result: a selection kernel of its own, one
+    # gather stream, the radix cut at every step, 32-byte gather loads; three
+    # chunks so the stream switches matter, every unit checked.
+    for key, val in env.items():
+        monkeypatch.setenv(key, val)
+    monkeypatch.setenv("NOSA_CHUNK_SIZES", "1,2,1")
+    w = synth.WORKLOADS["1b-bf16"].with_(batch=2, prompt=64 * 40 + 9, steps=40)
+    _run(w)
+
+
 @pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2", "0.5,1,2,3,3,1"])
 def test_unequal_chunks_every_unit(sizes, monkeypatch):
     # The step's unit chunks run concurrently and differ in split counts; every

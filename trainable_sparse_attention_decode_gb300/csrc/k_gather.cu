@@ -142,11 +142,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State s
 }  // namespace
 
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int ucount,
-                          int chunk, cudaStream_t stream) {
-  static const bool wide = [] {
-    const char* g = std::getenv("NOSA_GATHER_VEC");
-    return g != nullptr && std::atoi(g) == 32;
-  }();
+                          int chunk, bool wide, cudaStream_t stream) {
   if (wide)
     gather_kernel<V32><<<grid, kGatherThreads, 0, stream>>>(s, st, ubase, ucount, chunk);
   else

@@ -330,6 +330,7 @@ struct nosa_handle {
   cudaStream_t s_gat2 = nullptr;  // gathers of odd chunks (fused step)
   cudaEvent_t ev_jgat2 = nullptr;
   int gather_streams = 2;
+  bool gather_wide = false;  // 32-byte gather loads (NOSA_GATHER_VEC=32)
   cudaEvent_t ev_in = nullptr, ev_att = nullptr, ev_new = nullptr;
   cudaEvent_t ev_app = nullptr;  // the step's append is done
   // Fused step: chunk c is scored and selected on its own stream (priority
@@ -736,6 +737,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (const char* g = std::getenv("NOSA_GATHER_STREAMS"))
     if (std::atoi(g) == 1) h->gather_streams = 1;
   if (!h->fused_select) h->gather_streams = 1;
+  if (const char* g = std::getenv("NOSA_GATHER_VEC")) h->gather_wide = std::atoi(g) == 32;
   if (e == cudaSuccess && h->gather_streams == 2) {
     e = cudaStreamCreateWithPriority(&h->s_gat2, cudaStreamNonBlocking, prio_hi);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_jgat2, cudaEventDisableTiming);
@@ -916,7 +918,8 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     cudaStream_t tg = (h->gather_streams == 2 && (c & 1)) ? h->s_gat2 : h->s_gat;
     err = cudaStreamWaitEvent(tg, h->ev_sel[c], 0);
     if (ev && c == 0) mark(ev[4], tg);
-    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], h->cu_count[c], c, tg);
+    if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], h->cu_count[c], c,
+                                                  h->gather_wide, tg);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], tg);
     if (ev && c == h->nchunks - 1) mark(ev[5], tg);
     // attention over the slots kept from the previous step, plus the tail (fused

@@ -226,9 +226,10 @@ cudaError_t launch_select_setdiff(const Shape& s, const State& st, int cold, int
 bool score_select_fused_ok(const Shape& s);
 cudaError_t launch_score_select(const Shape& s, const State& st, int n_cap, int ubase, int ucount,
                                 int cold, int chunk, cudaStream_t stream, int max_ctas_per_sm = 0);
-// Copies the load-list entries of units [ubase, ubase + ucount) (grid: CTAs).
+// Copies the load-list entries of units [ubase, ubase + ucount) (grid: CTAs;
+// wide: 32-byte loads with a 256-byte L2 fetch hint instead of 16-byte loads).
 cudaError_t launch_gather(const Shape& s, const State& st, int grid, int ubase, int ucount,
-                          int chunk, cudaStream_t stream);
+                          int chunk, bool wide, cudaStream_t stream);
 // Sets every trace slot's start to the maximum (the ends are zeroed by the caller).
 cudaError_t launch_trace_reset(unsigned long long* trace, cudaStream_t stream);
 // result[0] = error code of a bounded wait that nothing completes, result[1] = ms waited.
