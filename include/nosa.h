@@ -352,7 +352,13 @@ nosa_status nosa_set_timing(nosa_handle* h, int32_t on);
  *                     device's global timer (ns; start UINT64_MAX = not run); slot 0
  *                     the append, 1 + c scoring (and selection) of unit chunk c,
  *                     9 + c a separate selection, 17 + c the gather, 25 + c the
- *                     attention over kept slots, 33 + c over filled slots. Present
+ *                     attention over kept slots, 33 + c over filled slots (slot 0
+ *                     is the fused front-end for nosa_decode_step_hidden). Points
+ *                     (earliest and latest CTA): 41 / 42 the front-end's
+ *                     accumulator complete / epilogue done; 43 - 47 the first
+ *                     chunk's selection per unit: begins (scores complete), Gamma_e
+ *                     and Gamma_q marked, lists written (45, 46, 47), set-difference
+ *                     done (44). Present
  *                     (size > 0) only when the environment variable NOSA_TRACE=1 was
  *                     set at nosa_create; the records cost a few atomics per CTA.
  */
