@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, float inv
     __threadfence();
     if (threadIdx.x == 0) st.sel_cnt[u] = 0;  // ready for the next step
     if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0Begin);
-    select_setdiff_unit(s, st, u, cold, ubase, chunk, sel_dyn);
+    select_setdiff_unit(s, st, u, cold, chunk, sel_dyn);
     if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0End);
   }
 }

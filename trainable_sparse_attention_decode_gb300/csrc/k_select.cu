@@ -13,7 +13,7 @@ __global__ void __launch_bounds__(kSelThreads) select_setdiff_kernel(Shape s, St
                                                                      int ubase, int chunk) {
   extern __shared__ __align__(16) uint8_t dyn[];
   TraceScope trace_scope(st.trace, chunk < 8 ? kTrSelect + chunk : -1);
-  select_setdiff_unit(s, st, ubase + blockIdx.x, cold, ubase, chunk, dyn);
+  select_setdiff_unit(s, st, ubase + blockIdx.x, cold, chunk, dyn);
 }
 
 }  // namespace

@@ -439,7 +439,7 @@ __device__ void setdiff_phase(const Shape& s, const State& st, int u, int n, int
 // flag bits: 1 = eligible, 2 = in Gamma_e, 4 = in Gamma_q. The set-difference
 // against the unit's slots runs once Gamma is known.
 __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State& st, int u, int cold,
-                                                 int ubase, int chunk, uint8_t* dyn) {
+                                                 int chunk, uint8_t* dyn) {
   const int n = st.io->n_cand;
   const int just_completed = st.io->just_completed;
   __shared__ SelShared sh;
