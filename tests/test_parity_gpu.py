@@ -80,6 +80,8 @@ def test_8b_offload_sampled_units():
     dict(prompt=64 * 3, steps=70, k=8, k_e=3),        # fewer candidates than k for a while
     dict(prompt=64 * 10 + 5, steps=80, k=4, k_e=0),   # no query-agnostic part
     dict(prompt=64 * 10 + 63, steps=80, k=4, k_e=4),  # no query-aware part
+    dict(prompt=1, steps=70, k=4, k_e=2),             # a one-token context (none: STATE error)
+    dict(prompt=64 * 300 + 7, steps=40, k=256, k_e=128),  # the largest k the kernels take
 ])
 def test_edge_cases_f32(case):
     w = synth.WORKLOADS["tiny-f32"].with_(**case)
