@@ -54,14 +54,31 @@ def _create_raw(cfg):
     return st, h
 
 
+def _last_device_allocation(cfg, monkeypatch):
+    # the index of nosa_create's last device allocation: the largest N whose
+    # injected failure still fails the create
+    n = 0
+    while True:
+        monkeypatch.setenv("NOSA_INJECT_FAIL", f"dev:{n + 1}")
+        st, h = _create_raw(cfg)
+        if st == 0:
+            nosa.lib.nosa_destroy(h)
+            monkeypatch.delenv("NOSA_INJECT_FAIL")
+            return n
+        n += 1
+        assert n < 200
+
+
 @pytest.mark.parametrize("spec,status", [("host", 3), ("dev:0", 2), ("dev:1", 2), ("dev:9", 2),
-                                         ("dev:24", 2)])
+                                         ("dev:last", 2)])
 def test_injected_allocation_failure(spec, status, monkeypatch):
     # about 140 MB of device state (the slot pool and the pooled keys are 67 MB
     # each) and 1.1 GB of pinned host store; a leaked device allocation would show
     w = synth.WORKLOADS["8b-offload-bf16"].with_(batch=4)
     cfg = nosa.nosa_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.dtype, w.k, w.k_e,
                            w.max_context)
+    if spec == "dev:last":
+        spec = f"dev:{_last_device_allocation(cfg, monkeypatch)}"
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     monkeypatch.setenv("NOSA_INJECT_FAIL", spec)

@@ -519,30 +519,24 @@ __device__ __forceinline__ void select_setdiff_unit(const Shape& s, const State&
   }
 
   if (threadIdx.x == 0 && chunk == 0) trace_mark(st.trace, kTrSel0Q);
-  // Gamma_e ascending, then Gamma_q ascending; eligibility and selection masks.
-  int32_t* sel = st.sel + (long long)u * s.k;
-  int run_e = 0, run_q = 0;
+  // Eligibility and selection masks, one ballot per 32-candidate word. After the
+  // step the eligibility words are Gamma_e (strict eviction) and the selection
+  // words Gamma_e + Gamma_q, so Gamma_e = sel & elig and Gamma_q = sel & ~elig; the
+  // ascending index lists are derived from them where they are read (the debug
+  // read), not written here.
+  __syncthreads();  // the cuts are done reading key[]
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + threadIdx.x;
     const uint8_t f = (i < n) ? flag[i] : 0;
-    int tot;  // Gamma_e count in the low 16 bits, Gamma_q count in the high 16 bits
-    const int x = block_excl_scan<kSelWarps>(((f & 2) ? 1 : 0) | ((f & 4) ? 0x10000 : 0),
-                                             sh.warp_tot, &tot);
-    const int xe = x & 0xFFFF, xq = x >> 16, te = tot & 0xFFFF, tq = tot >> 16;
-    if (f & 2) sel[run_e + xe] = i;
-    if (f & 4) sel[need_e + run_q + xq] = i;
-    run_e += te;
-    run_q += tq;
     const unsigned be = __ballot_sync(0xffffffffu, (f & 2) != 0);
     const unsigned bs = __ballot_sync(0xffffffffu, (f & 6) != 0);
     if ((threadIdx.x & 31) == 0 && base + (threadIdx.x & ~31) < n) {
       const int w = (base + (threadIdx.x & ~31)) >> 5;
       elig[w] = be;
       st.selmask[(long long)u * s.W + w] = bs;
-      key[w] = bs;  // shared copy for the set-difference (key[] is free by now)
+      key[w] = bs;  // shared copy for the set-difference
     }
   }
-  for (int j = need_e + need_q + threadIdx.x; j < s.k; j += kSelThreads) sel[j] = -1;
   if (threadIdx.x == 0) {
     st.nsel[2 * u] = need_e;
     st.nsel[2 * u + 1] = need_q;

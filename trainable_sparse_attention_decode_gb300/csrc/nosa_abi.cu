@@ -563,7 +563,6 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   A(&st.elig, U * W * 4);
   A(&st.selmask, U * W * 4);
   A(&st.resmask, U * W * 4);
-  A(&st.sel, U * k * 4);
   A(&st.nsel, U * 2 * 4);
   A(&st.slot2blk, U * k * 4);
   A(&st.loads, U * k * 3 * 4);
@@ -599,7 +598,6 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(st.elig, 0, U * W * 4);
   if (e == cudaSuccess) e = cudaMemset(st.selmask, 0, U * W * 4);
   if (e == cudaSuccess) e = cudaMemset(st.resmask, 0, U * W * 4);
-  if (e == cudaSuccess) e = cudaMemset(st.sel, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.nsel, 0, U * 2 * 4);
   if (e == cudaSuccess) e = cudaMemset(st.slot2blk, 0xFF, U * k * 4);
   if (e == cudaSuccess) e = cudaMemset(st.loads, 0, U * k * 3 * 4);
@@ -1341,9 +1339,34 @@ nosa_status nosa_debug_read(nosa_handle* h, int32_t what, size_t offset, void* d
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return h->cuda_fail(e, "synchronise");
   const State& st = h->st;
+  if (what == NOSA_DBG_SEL) {
+    if (bytes == 0) return NOSA_OK;
+    // The lists are not kept on the device: between steps the eligibility words are
+    // the last step's Gamma_e (strict eviction; blocks completed since are in no
+    // list) and the selection words its Gamma, so Gamma_e = sel & elig ascending,
+    // then Gamma_q = sel & ~elig ascending, -1 padded to k.
+    const size_t k = (size_t)h->s.k, W = (size_t)h->s.W, row = k * 4;
+    const size_t u0 = offset / row, u1 = (offset + bytes + row - 1) / row;
+    std::vector<uint32_t> sm((u1 - u0) * W), el((u1 - u0) * W);
+    e = cudaMemcpy(sm.data(), st.selmask + u0 * W, sm.size() * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(el.data(), st.elig + u0 * W, el.size() * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return h->cuda_fail(e, "debug read");
+    std::vector<int32_t> lists((u1 - u0) * k, -1);
+    for (size_t u = 0; u < u1 - u0; ++u) {
+      size_t j = 0;
+      for (int pass = 0; pass < 2; ++pass)
+        for (size_t w = 0; w < W; ++w) {
+          uint32_t bits = sm[u * W + w] & (pass == 0 ? el[u * W + w] : ~el[u * W + w]);
+          for (; bits != 0u && j < k; bits &= bits - 1)
+            lists[u * k + j++] = (int32_t)(w * 32 + __builtin_ctz(bits));
+        }
+    }
+    std::memcpy(dst, reinterpret_cast<const uint8_t*>(lists.data()) + (offset - u0 * row), bytes);
+    return NOSA_OK;
+  }
   const void* base = nullptr;
   switch (what) {
-    case NOSA_DBG_SEL: base = st.sel; break;
     case NOSA_DBG_NSEL: base = st.nsel; break;
     case NOSA_DBG_ELIG: base = st.elig; break;
     case NOSA_DBG_SLOTS: base = st.slot2blk; break;

@@ -161,7 +161,6 @@ struct State {
   uint32_t* elig;      // [U][W]            eviction eligibility bitmask
   uint32_t* selmask;   // [U][W]            Gamma of the current step
   uint32_t* resmask;   // [U][W]            blocks held by slots
-  int32_t* sel;        // [U][k]            Gamma_e ascending, then Gamma_q ascending, -1 pad
   int32_t* nsel;       // [U][2]
   int32_t* slot2blk;   // [U][k]
   int32_t* loads;      // [U][k][3]         (block, slot, src)
