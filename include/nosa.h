@@ -336,6 +336,7 @@ nosa_status nosa_set_timing(nosa_handle* h, int32_t on);
  * byte `offset` of the chosen array into host memory `dst`. INVALID_ARG if the
  * range is outside the array. Arrays (U units, W = ceil(maxBlk / 32)):
  *   NOSA_DBG_SEL      int32 [U][k]   Gamma_e ascending then Gamma_q ascending, -1 pad
+ *                     (derived at read time from the selection and eligibility masks)
  *   NOSA_DBG_NSEL     int32 [U][2]   |Gamma_e|, |Gamma_q|
  *   NOSA_DBG_ELIG     uint32 [U][W]  eligibility bitmask (bit i%32 of word i/32)
  *   NOSA_DBG_SLOTS    int32 [U][k]   block held by each slot, -1 empty
