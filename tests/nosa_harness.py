@@ -108,6 +108,10 @@ class GpuRun:
         self.attn_every = oracle_attention_every
         self.ties = 0
         self.step_idx = 0
+        self.expected = {"host_loads": 0, "tail_loads": 0, "cold_host_loads": 0, "sum_hits": 0,
+                         "hit_samples": 0, "min_hits": 0, "max_host_loads_unit": 0,
+                         "unit_steps": 0}
+        self.stats_checked = False
         self.dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         pieces = prompt_pieces or self._default_pieces(w.prompt)
         assert sum(pieces) == w.prompt
@@ -291,6 +295,7 @@ class GpuRun:
             self.ties += tie
             assert list(g_e_gpu) == sorted(g_e_gpu) and list(g_q_gpu) == sorted(g_q_gpu)
             info = uo.commit(g_e, np.array(sorted(int(x) for x in g_q_gpu), dtype=np.int64))
+            self._count(s, n, len(g_e) + len(g_q_gpu), info["loads"])
             nload = int(self._i32("NLOAD", u, 1)[0])
             loads = self._i32("LOADS", u, self.k * 3).reshape(self.k, 3)[:nload]
             assert [tuple(map(int, l)) for l in loads] == [tuple(l) for l in info["loads"]], (
@@ -329,8 +334,36 @@ class GpuRun:
             self.q_all[key] = synth.queries(self.w, b, range(hh * self.G, (hh + 1) * self.G), steps)
         return self.q_all[key][s]
 
+    def _count(self, s, n, gamma, loads):
+        """The library's load statistics, rebuilt from the oracle's load lists: every
+        load is a host or a tail load; the handle's first decode step counts its host
+        loads as cold; any later step of a unit with at least k candidates is a hit
+        sample, hits = |Gamma| - host loads."""
+        e = self.expected
+        n_host = sum(1 for ld in loads if ld[2] == 0)
+        e["host_loads"] += n_host
+        e["tail_loads"] += len(loads) - n_host
+        if s == 0:
+            e["cold_host_loads"] += n_host
+        elif n >= self.k:
+            hits = gamma - n_host
+            e["min_hits"] = hits if e["hit_samples"] == 0 else min(e["min_hits"], hits)
+            e["sum_hits"] += hits
+            e["hit_samples"] += 1
+            e["max_host_loads_unit"] = max(e["max_host_loads_unit"], n_host)
+        e["unit_steps"] += 1
+
     def stats(self):
-        return nosa.nosa_stats(self.h)
+        """nosa_stats; when every unit was checked at every step, its load statistics
+        must equal the ones rebuilt from the oracle."""
+        st = nosa.nosa_stats(self.h)
+        e = self.expected
+        if e["unit_steps"] == self.U * self.step_idx and self.step_idx > 0:
+            for key in ("host_loads", "tail_loads", "cold_host_loads", "sum_hits", "hit_samples",
+                        "min_hits", "max_host_loads_unit"):
+                assert st[key] == e[key], f"stats {key}: library {st[key]} != oracle {e[key]}"
+            self.stats_checked = True
+        return st
 
     def close(self):
         nosa.nosa_destroy(self.h)

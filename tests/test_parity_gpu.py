@@ -45,6 +45,7 @@ def _run(w, units=None, steps=None, check_every=1, attn_every=1, pieces=None, ch
 def test_tiny_f32_full():
     st, run = _run(synth.WORKLOADS["tiny-f32"])
     assert st["steps"] == 32 and st["cold_host_loads"] in (7, 8)
+    assert run.stats_checked  # every unit at every step: load statistics equal the oracle's
 
 
 def test_1b_bf16_sampled_units():
