@@ -246,19 +246,22 @@ def ncu_traffic(workload_name, kernel="attn_streamk_kernel", sources=None):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def h2d_peak_gbs(torch, nbytes=1 << 30, reps=5):
+def h2d_peak_gbs(torch, nbytes=1 << 30, reps=5, median=False):
+    """Pinned host -> device copy rate (GB/s): the best of `reps` copies, or their
+    median."""
     src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    best = float("inf")
+    times = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         dst.copy_(src, non_blocking=True)
         b.record()
         b.synchronize()
-        best = min(best, a.elapsed_time(b) / 1e3)
+        times.append(a.elapsed_time(b) / 1e3)
     del src, dst
-    return nbytes / best / 1e9
+    t = sorted(times)[len(times) // 2] if median else min(times)
+    return nbytes / t / 1e9
 
 
 def attention_alone(nosa, torch, w, n_cand, tail_len, reps=20, classic=False):
@@ -629,6 +632,9 @@ def run_gpu(args, rank, world, local_rank):
     step_us = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(K)]
     st = nosa.nosa_stats(h)
     context_after = st["context"]
+    # the pinned-copy rate again, right after the timed steps: a diagnostic of the
+    # host link's state during them (the one before the setup is `h2d_peak_gbs`)
+    h2d_after = h2d_peak_gbs(torch, nbytes=256 << 20, reps=3, median=True) if rank == 0 else None
 
     # end to end: pinned host inputs -> device, step, result -> pinned host, every
     # step, as a server pipelines them: double-buffered device inputs and outputs,
@@ -790,6 +796,7 @@ def run_gpu(args, rank, world, local_rank):
         "score_hbm_gbs": round(score_gbs, 1),
         "recall_h2d_gbs": round(recall_gbs, 2),
         "h2d_peak_gbs": round(peak_h2d, 2) if peak_h2d else None,
+        "h2d_after_timed_gbs": round(h2d_after, 2) if h2d_after else None,
         "recall_frac_of_h2d_peak": round(recall_gbs / peak_h2d, 4) if peak_h2d else None,
         "host_bytes_per_step": round(host_bytes_step),
         "phase_us": {k_: round(v_, 3) for k_, v_ in phase_us.items()},
