@@ -246,6 +246,76 @@ def ncu_traffic(workload_name, kernel="attn_streamk_kernel", sources=None):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+def pinned_kb():
+    """VmPin + VmLck of this process in kB (None where the kernel does not say)."""
+    try:
+        tot, seen = 0, False
+        with open("/proc/self/status") as f:
+            for line in f:
+                if line.startswith(("VmPin:", "VmLck:")):
+                    tot += int(line.split()[1])
+                    seen = True
+        return tot if seen else None
+    except OSError:
+        return None
+
+
+def anon_huge_kb():
+    """AnonHugePages of this process in kB (None where the kernel does not say)."""
+    try:
+        with open("/proc/self/smaps_rollup") as f:
+            for line in f:
+                if line.startswith("AnonHugePages:"):
+                    return int(line.split()[1])
+    except OSError:
+        pass
+    return None
+
+
+VM_EVENTS = ("thp_fault_alloc", "thp_fault_fallback", "thp_collapse_alloc",
+             "thp_collapse_alloc_failed", "thp_split_page", "thp_split_page_failed",
+             "thp_deferred_split_page", "thp_underused_split_page", "thp_migration_split",
+             "thp_migration_success", "thp_migration_fail", "thp_split_pmd", "thp_swpout",
+             "thp_swpout_fallback", "pswpout", "pgsteal_anon", "compact_stall",
+             "compact_migrate_scanned", "pgmigrate_success", "pgmigrate_fail",
+             "numa_hint_faults", "numa_pages_migrated")
+
+
+def vm_events():
+    """A few of the kernel's memory-management event counters (/proc/vmstat), or
+    None where the kernel does not say: their change over the timed region tells
+    whether the host rearranged pages (huge-page collapse, compaction, migration)
+    while the GPU was reading the host store."""
+    try:
+        out = {}
+        with open("/proc/vmstat") as f:
+            for line in f:
+                k, _, v = line.partition(" ")
+                if k in VM_EVENTS:
+                    out[k] = int(v)
+        return out
+    except OSError:
+        return None
+
+
+STORE_LAYOUTS = {0: "cudaHostAlloc", 1: "mapping bound to the GPU's node",
+                 2: "transparent huge pages"}
+
+
+def host_store_report(st, huge_kb, huge_kb_after, pin_kb, vm_created, vm_t0, vm_t1):
+    """How the host store was laid out, how much of the process was in huge pages
+    and pinned after the create and after the timed steps, and the host's
+    memory-management events during the setup and the timed steps."""
+    mb = lambda kb: round(kb / 1024) if kb is not None else None
+    delta = lambda a, b: {k_: b[k_] - a[k_] for k_ in b if b[k_] != a.get(k_)}
+    return {"layout": STORE_LAYOUTS.get(st["host_store_kind"], st["host_store_kind"]),
+            "long_term_pins": bool(st["host_store_pinned"]),
+            "huge_pages_mb": mb(huge_kb), "huge_pages_mb_after_timed": mb(huge_kb_after),
+            "pinned_mb": mb(pin_kb),
+            "vm_events": ({"setup": delta(vm_created, vm_t0), "timed": delta(vm_t0, vm_t1)}
+                          if vm_created and vm_t0 and vm_t1 else None)}
+
+
 def h2d_peak_gbs(torch, nbytes=1 << 30, reps=5, median=False):
     """Pinned host -> device copy rate (GB/s): the best of `reps` copies, or their
     median."""
@@ -543,6 +613,9 @@ def run_gpu(args, rank, world, local_rank):
                            w.max_context, device=local_rank,
                            flags=(nosa.NOSA_FLAG_POOLED_BF16 if args.pooled_bf16 else 0))
     h = nosa.nosa_create(cfg)
+    huge_kb = anon_huge_kb()  # how much of the process is backed by huge pages (Linux)
+    pin_kb = pinned_kb()  # how much of it is pinned or locked by the process itself
+    vm_created = vm_events()
     # prompt, appended in chunks generated on the device
     chunk = 4096
     t = 0
@@ -614,6 +687,7 @@ def run_gpu(args, rank, world, local_rank):
     # one event before every timed step (and one after the last): the whole-run
     # time is first to last, and the per-step times give the median and spread
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    vm_t0 = vm_events()
     w0t = time.time()
     torch.cuda.nvtx.range_push("timed")
     h0 = time.perf_counter()
@@ -625,6 +699,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     w1t = time.time()
+    vm_t1 = vm_events()
+    huge_kb_after = anon_huge_kb()
     barrier(world)
     if sampler:
         sampler.mark(w0t, w1t)
@@ -797,6 +873,8 @@ def run_gpu(args, rank, world, local_rank):
         "recall_h2d_gbs": round(recall_gbs, 2),
         "h2d_peak_gbs": round(peak_h2d, 2) if peak_h2d else None,
         "h2d_after_timed_gbs": round(h2d_after, 2) if h2d_after else None,
+        "host_store": host_store_report(st, huge_kb, huge_kb_after, pin_kb,
+                                        vm_created, vm_t0, vm_t1),
         "recall_frac_of_h2d_peak": round(recall_gbs / peak_h2d, 4) if peak_h2d else None,
         "host_bytes_per_step": round(host_bytes_step),
         "phase_us": {k_: round(v_, 3) for k_, v_ in phase_us.items()},

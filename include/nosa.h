@@ -297,6 +297,11 @@ typedef struct {
   double t_us[8];
   int64_t t_count;
   int64_t launches;              /* kernels launched by decode steps (host count)    */
+  int32_t host_store_kind;       /* how the host store was made: 0 cudaHostAlloc,
+                                    1 a mapping bound to host_numa_node, 2 a mapping
+                                    in transparent huge pages (unbound)             */
+  int32_t host_store_pinned;     /* 1: the process holds long-term pins on the
+                                    store's pages (they cannot move or be split)   */
 } nosa_stats_t;
 
 /*

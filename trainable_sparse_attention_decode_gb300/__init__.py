@@ -62,7 +62,8 @@ class NosaStats(C.Structure):
                 ("gamma_min", C.c_double), ("gamma_mean", C.c_double),
                 ("near_ties", C.c_int64), ("device_error", C.c_int32),
                 ("host_numa_node", C.c_int32),
-                ("t_us", C.c_double * 8), ("t_count", C.c_int64), ("launches", C.c_int64)]
+                ("t_us", C.c_double * 8), ("t_count", C.c_int64), ("launches", C.c_int64),
+                ("host_store_kind", C.c_int32), ("host_store_pinned", C.c_int32)]
 
 
 def _load():

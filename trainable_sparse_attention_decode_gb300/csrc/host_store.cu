@@ -7,12 +7,14 @@
 // pages to the GPU's node (a preferred policy: the kernel falls back to other
 // nodes rather than fail) before pinning them. With one memory node, or when
 // the GPU's node is unknown, has no memory or is not allowed to this process,
-// nothing is bound and the store is an ordinary cudaHostAlloc.
+// nothing is bound; a store of 1 GiB or more is then laid out in pinned
+// transparent huge pages (host_store_alloc).
 #include "nosa.h"
 #include "nosa_internal.cuh"
 
 #include <sys/mman.h>
 #include <sys/syscall.h>
+#include <sys/uio.h>
 #include <unistd.h>
 
 #include <cctype>
@@ -92,36 +94,148 @@ int host_store_node(int device) {
                           (int)allowed.size());
 }
 
-// Pinned, mapped host memory of `bytes`: bound (preferred) to `node` and then
-// registered, or a plain cudaHostAlloc when node < 0 or binding is refused.
-// *registered tells host_store_free which way it was made.
-cudaError_t host_store_alloc(size_t bytes, int node, void** out, bool* registered) {
+// madvise advice values of Linux 5.14 (populate for writing) and 6.1 (collapse into
+// huge pages); older kernels answer EINVAL and the call does nothing.
+constexpr int kMadvPopulateWrite = 23;
+constexpr int kMadvCollapse = 25;
+
+// io_uring system calls (the same numbers on every architecture since Linux 5.1).
+#ifdef SYS_io_uring_setup
+constexpr long kSysUringSetup = SYS_io_uring_setup;
+constexpr long kSysUringRegister = SYS_io_uring_register;
+#else
+constexpr long kSysUringSetup = 425;
+constexpr long kSysUringRegister = 427;
+#endif
+
+// The size of a transparent huge page (the page-middle-directory size: 2 MB with
+// 4 KB base pages, 512 MB with 64 KB ones), or 0 where the kernel has none.
+size_t thp_size() {
+  std::FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r");
+  if (f == nullptr) return 0;
+  unsigned long long v = 0;
+  if (std::fscanf(f, "%llu", &v) != 1) v = 0;
+  std::fclose(f);
+  return (v & (v - 1)) == 0 ? (size_t)v : 0;  // a power of two, or nothing
+}
+
+// An anonymous mapping of `len` bytes that starts on a multiple of `align` (a
+// power of two), or nullptr.
+void* map_aligned(size_t len, size_t align) {
+  void* raw = mmap(nullptr, len + align, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS,
+                   -1, 0);
+  if (raw == MAP_FAILED) return nullptr;
+  const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
+  const uintptr_t a = (r + align - 1) & ~(uintptr_t)(align - 1);
+  if (a > r) munmap(raw, a - r);
+  munmap(reinterpret_cast<void*>(a + len), r + align - a);
+  return reinterpret_cast<void*>(a);
+}
+
+// Pins [p, p + len) for as long as the returned descriptor stays open (-1: not
+// pinned). The range is registered as the fixed buffers of an io_uring instance,
+// which holds long-term pins on its pages: the kernel can then neither migrate
+// nor split them while the GPU reads them (cudaHostRegister does not prevent
+// either where the GPU reaches host memory through the host's own page tables).
+// Buffers of 1 GiB at most each. Needs CAP_IPC_LOCK or a locked-memory limit
+// above `len`; the descriptor is close-on-exec.
+int pin_long_term(void* p, size_t len) {
+  unsigned char params[120];  // struct io_uring_params, all zero: defaults
+  std::memset(params, 0, sizeof(params));
+  const long fd = syscall(kSysUringSetup, 1, params);
+  if (fd < 0) return -1;
+  const size_t gib = (size_t)1 << 30;
+  std::vector<struct iovec> iov;
+  for (size_t off = 0; off < len; off += gib) {
+    struct iovec v;
+    v.iov_base = static_cast<char*>(p) + off;
+    v.iov_len = len - off < gib ? len - off : gib;
+    iov.push_back(v);
+  }
+  const long r = syscall(kSysUringRegister, (int)fd, 0 /* IORING_REGISTER_BUFFERS */,
+                         iov.data(), (unsigned)iov.size());
+  if (r < 0) {
+    close((int)fd);
+    return -1;
+  }
+  return (int)fd;
+}
+
+// Drops the pins of pin_long_term at once (closing the descriptor alone releases
+// them only when the kernel tears the instance down, some time later).
+void unpin(int fd) {
+  if (fd < 0) return;
+  syscall(kSysUringRegister, fd, 1 /* IORING_UNREGISTER_BUFFERS */, nullptr, 0U);
+  close(fd);
+}
+
+// Pinned host memory of at least `bytes`, reachable by the device. *kind says how
+// it was made (host_store_free needs it), *mapped its mapped length, *pin_fd the
+// descriptor that holds its pages (-1: none):
+//   kind 1: an anonymous mapping bound (preferred) to `node` (node >= 0), faulted
+//           in, pinned where pin_long_term can, registered;
+//   kind 2: an anonymous mapping in transparent huge pages (stores of 1 GiB or
+//           more, unbound): aligned to and rounded up to the huge-page size,
+//           faulted in, what came out small collapsed, pinned, registered; taken
+//           only when the pin holds;
+//   kind 0: a plain cudaHostAlloc (everything else, and the fallback).
+// Why the huge pages: the recall reads about 1 300 scattered blocks of the store
+// per step, and with 64 KB pages their address translation, not the link, set the
+// rate in most short runs on the GB300 machines (medians well above the link-bound
+// step, up to 2.9x); with 512 MB pages every run kept the link's rate. Why the pins: without
+// them the kernel split the huge pages of a running store now and then, and every
+// step of that run took milliseconds. NOSA_HOST_HUGEPAGE=0 keeps the plain store.
+cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size_t* mapped,
+                             int* pin_fd) {
+  *pin_fd = -1;
   *out = nullptr;
-  *registered = false;
-  if (node >= 0 && node < 1024) {
-    void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-    if (p != MAP_FAILED) {
-      unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {0};
-      mask[node / (8 * sizeof(unsigned long))] |= 1UL << (node % (8 * sizeof(unsigned long)));
-      const long r = syscall(SYS_mbind, p, bytes, 1 /* MPOL_PREFERRED */, mask, 1024UL, 0U);
-      if (r == 0 &&
-          cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+  *kind = 0;
+  *mapped = bytes;
+  const char* g = std::getenv("NOSA_HOST_HUGEPAGE");
+  const bool bind = node >= 0 && node < 1024;
+  const size_t huge =
+      (g == nullptr || std::atoi(g) != 0) && bytes >= ((size_t)1 << 30) ? thp_size() : 0;
+  if (bind || huge != 0) {
+    const size_t page = huge != 0 ? huge : (size_t)sysconf(_SC_PAGESIZE);
+    const size_t len = (bytes + page - 1) / page * page;
+    if (void* p = map_aligned(len, page)) {
+      bool ok = true;
+      if (bind) {
+        unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {0};
+        mask[node / (8 * sizeof(unsigned long))] |= 1UL << (node % (8 * sizeof(unsigned long)));
+        ok = syscall(SYS_mbind, p, len, 1 /* MPOL_PREFERRED */, mask, 1024UL, 0U) == 0;
+      }
+      if (ok) {
+        if (huge != 0) madvise(p, len, MADV_HUGEPAGE);
+        madvise(p, len, MADV_DONTFORK);  // a forked child never sees the store
+        madvise(p, len, kMadvPopulateWrite);
+        if (huge != 0) madvise(p, len, kMadvCollapse);
+        *pin_fd = pin_long_term(p, len);
+        ok = bind || *pin_fd >= 0;  // unpinned huge pages may be split under the GPU
+      }
+      if (ok &&
+          cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
+              cudaSuccess) {
         *out = p;
-        *registered = true;
+        *kind = bind ? 1 : 2;
+        *mapped = len;
         return cudaSuccess;
       }
       cudaGetLastError();
-      munmap(p, bytes);
+      unpin(*pin_fd);
+      *pin_fd = -1;
+      munmap(p, len);
     }
   }
   return cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
 }
 
-void host_store_free(void* p, size_t bytes, bool registered) {
+void host_store_free(void* p, size_t mapped, int kind, int pin_fd) {
   if (p == nullptr) return;
-  if (registered) {
+  if (kind == 1 || kind == 2) {
     cudaHostUnregister(p);
-    munmap(p, bytes);
+    unpin(pin_fd);
+    munmap(p, mapped);
   } else {
     cudaFreeHost(p);
   }

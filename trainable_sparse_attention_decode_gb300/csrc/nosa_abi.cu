@@ -313,7 +313,9 @@ struct nosa_handle {
   std::vector<void*> dev_allocs;
   uint8_t* host_store = nullptr;
   size_t host_bytes = 0;
-  bool host_registered = false;  // the store was bound to a node and registered
+  int host_kind = 0;           // how the store was made (host_store_alloc)
+  int host_pin_fd = -1;          // holds long-term pins on the store (-1: none)
+  size_t host_map_bytes = 0;   // ... its mapped length
   int host_node = -1;            // NUMA node the store is bound to (-1: not bound)
   long long L = 0;
   long long steps = 0;
@@ -407,7 +409,7 @@ void free_all(nosa_handle* h) {
   h->q_buf = nullptr;
   for (void* p : h->dev_allocs) cudaFree(p);
   h->dev_allocs.clear();
-  host_store_free(h->host_store, h->host_bytes, h->host_registered);
+  host_store_free(h->host_store, h->host_map_bytes, h->host_kind, h->host_pin_fd);
   h->host_store = nullptr;
   for (StepGraph* gp : {&h->plain}) {
     if (gp->exec) cudaGraphExecDestroy(gp->exec);
@@ -622,8 +624,9 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // On the GPU's NUMA node when the host has several (host_store.cu).
   h->host_node = host_store_node(cfg->device);
   e = h->inject.host ? cudaErrorMemoryAllocation
-                     : host_store_alloc(h->host_bytes, h->host_node, &hp, &h->host_registered);
-  if (!h->host_registered) h->host_node = -1;
+                     : host_store_alloc(h->host_bytes, h->host_node, &hp, &h->host_kind,
+                                        &h->host_map_bytes, &h->host_pin_fd);
+  if (h->host_kind != 1) h->host_node = -1;  // only kind 1 is bound to a node
   if (e != cudaSuccess) {
     g_thread_err = std::string("pinned host allocation failed: ") + cudaGetErrorString(e);
     cudaGetLastError();
@@ -1270,6 +1273,8 @@ nosa_status nosa_stats(nosa_handle* h, nosa_stats_t* out) {
   out->near_ties = (int64_t)ds.near_ties;
   out->device_error = ds.error;
   out->host_numa_node = h->host_node;
+  out->host_store_kind = h->host_kind;
+  out->host_store_pinned = h->host_pin_fd >= 0 ? 1 : 0;
   for (int i = 0; i < 8; ++i) out->t_us[i] = h->t_us[i];
   out->t_count = h->t_count;
   out->launches = h->launches;
@@ -1379,7 +1384,8 @@ nosa_status nosa_debug_read(nosa_handle* h, int32_t what, size_t offset, void* d
     case NOSA_DBG_TAIL: base = st.tail; break;
     case NOSA_DBG_TRACE: base = st.trace; break;
     case NOSA_DBG_HOST:
-      std::memcpy(dst, h->host_store + offset, bytes);
+      e = cudaMemcpy(dst, st.host + offset, bytes, cudaMemcpyDefault);
+      if (e != cudaSuccess) return h->cuda_fail(e, "debug read");
       return NOSA_OK;
   }
   e = cudaMemcpy(dst, static_cast<const uint8_t*>(base) + offset, bytes, cudaMemcpyDeviceToHost);

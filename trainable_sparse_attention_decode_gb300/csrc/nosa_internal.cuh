@@ -199,8 +199,12 @@ enum : int {
 // Pinned host store placement (host_store.cu): the node to bind the store of a
 // device to (-1: none), and allocation / release of the store.
 int host_store_node(int device);
-cudaError_t host_store_alloc(size_t bytes, int node, void** out, bool* registered);
-void host_store_free(void* p, size_t bytes, bool registered);
+// kind: 0 cudaHostAlloc, 1 a registered mapping bound to `node`, 2 a registered,
+// pinned mapping in transparent huge pages (unbound). *pin_fd: a descriptor that holds
+// long-term pins on the store's pages until host_store_free closes it (-1: none).
+cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size_t* mapped,
+                             int* pin_fd);
+void host_store_free(void* p, size_t mapped, int kind, int pin_fd);
 
 // ---------------------------------------------------------------------------
 // Host-side launchers (each returns the launch error, if any).
