@@ -161,8 +161,9 @@ size_t attention_workspace_bytes(const Shape& s, int nsplit) {
   return ((acc + 15) & ~(size_t)15) + ((ml + 15) & ~(size_t)15) + ((cnt + 15) & ~(size_t)15) + 16;
 }
 
-// Splits per unit: the smallest count whose CTA total fills the GPU's resident
-// CTA slots in whole waves within 2% of the best, with >= 2 blocks per split.
+// Splits per unit: about 20 blocks per split, at least half a CTA per resident
+// slot, one split when the units alone fill the slots twice (and >= 2 blocks per
+// split); NOSA_ATTN_SPLITS overrides.
 int attention_pick_nsplit_uncached(const Shape& s, int n_blocks);
 
 // The pick depends only on the shape and the device; it is cached (the
