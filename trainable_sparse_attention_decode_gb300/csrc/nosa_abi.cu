@@ -187,10 +187,6 @@ int attention_pick_nsplit(const Shape& s, int n_blocks, int /*has_tail*/) {
 
 int attention_pick_nsplit_uncached(const Shape& s, int n_blocks) {
   const int nv = n_blocks + 1;
-  if (const char* g = std::getenv("NOSA_ATTN_SPLITS")) {  // tuning override
-    const int v = std::atoi(g);
-    if (v >= 1) return std::min(std::min(v, kMaxSplits), std::max(1, nv));
-  }
   // CTAs are scheduled as others finish, not in lockstep waves: long CTAs (about
   // 20 blocks) amortise each CTA's start-up and merge; small launches still get
   // half a CTA per resident slot (in the decode step the attention shares the GPU
@@ -202,6 +198,14 @@ int attention_pick_nsplit_uncached(const Shape& s, int n_blocks) {
   int occ = s.dtype == 0 ? attention_occupancy_f32(s, stages, bps_est, attn_warps())
                          : attention_occupancy_bf16(s, stages, bps_est, attn_warps());
   if (occ < 1) occ = 1;
+  // The occupancy query above also raises the kernel's shared-memory limit, here at
+  // create; the tuning override comes after it so that it leaves the kernel in the
+  // same state (a limit first raised while a cold step is being enqueued held that
+  // step's gathers to a fifth of the link on GB300).
+  if (const char* g = std::getenv("NOSA_ATTN_SPLITS")) {
+    const int v = std::atoi(g);
+    if (v >= 1) return std::min(std::min(v, kMaxSplits), std::max(1, nv));
+  }
   const double slots = (double)sm_count_current() * occ;
   if (s.U >= 2 * slots) return 1;  // enough CTAs already, and one split needs no merge
   const int by_blocks = std::max(1, nv / 20);
@@ -645,16 +649,6 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
     return NOSA_ERR_CUDA;
   }
   st.host = static_cast<uint8_t*>(dp);
-  // The gather shares the GPU with scoring and attention, and the fused step runs
-  // two gathers at once: 32 CTAs each keep enough host reads in flight for the
-  // link (one CTA moves about 28 GB/s) and leave the SMs to the scoring and the
-  // attention (GB300, 8B-offload: 269 us per step against 282 us with 64 CTAs;
-  // NOSA_GATHER_CTAS overrides the grid, for tuning).
-  h->gather_grid = 32;
-  if (const char* g = std::getenv("NOSA_GATHER_CTAS")) {
-    const int v = std::atoi(g);
-    if (v > 0) h->gather_grid = v;
-  }
   if (const char* g = std::getenv("NOSA_LOADED_SPLITS")) {
     const int v = std::atoi(g);
     if (v > 0 && v <= kMaxSplits) h->nsplit_new = v;
@@ -664,12 +658,13 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // growing by NOSA_CHUNK_GROWTH, else by the unit count. Measured on GB300:
   // every chunk adds a selection tail and four launches, which pay off only when
   // the units are many (64 units: one chunk, 55 us against 71 us with five; 128
-  // units: two; 256 units: 0.5,1,2,3,3,1, small first chunks so that the first
-  // gather starts early and a small last one so that little attention is left
-  // after the last gather).
+  // units: two; 256 units: 0.5,1,2,3,2.5,1.5, small first chunks so that the first
+  // gather starts early and smaller last ones so that little attention is left
+  // after the last gather: 262.5 us against 263.5 for 0.5,1,2,3,3,1 with the same
+  // splits, 263.7 for 0.5,1,1.5,2.5,2.5,2 and 266.5 for 0.5,1,2,3,2,2).
   std::vector<double> weights = s.U <= 96 ? std::vector<double>{1}
                                 : s.U <= 192 ? std::vector<double>{1, 1}
-                                             : std::vector<double>{0.5, 1, 2, 3, 3, 1};
+                                             : std::vector<double>{0.5, 1, 2, 3, 2.5, 1.5};
   if (const char* g = std::getenv("NOSA_UNIT_CHUNKS")) {
     const int v = std::atoi(g);
     if (v > 0) {
@@ -711,10 +706,37 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
       prev = end;
     }
   }
+  // Splits of the step's attention launches (one per chunk, over its kept slots).
+  // With one or two chunks, each chunk's own plan (about 20 blocks per split, half
+  // a CTA per resident slot). With more, the chunks' launches overlap one another,
+  // the scoring and the gathers: the fill rule then counts the whole step's units,
+  // not the chunk's (a 12-unit chunk alone would take 19 splits), and a split
+  // takes about 16 blocks. GB300, 8B-offload (six chunks): 4 splits per chunk
+  // 262.5 us per step, 3 266.6, 5 263.9, the chunk-wise plans 266.1; 8B-longgen
+  // (two chunks, k = 128): its chunk-wise 6 splits 136.2 us, 8 splits 143.3.
+  // NOSA_ATTN_SPLITS forces the count.
   for (int c = 0; c < nchunks; ++c) {
     Shape sc = s;
     sc.U = h->cu_count[c];
     h->nsplit_c[c] = attention_pick_nsplit(sc, s.k, 1);
+  }
+  // The gather shares the GPU with scoring and attention, and the fused step runs
+  // two gathers at once: 24 CTAs each keep enough host reads in flight for the
+  // link (one CTA moves about 28 GB/s) and leave the SMs to the scoring and the
+  // attention (GB300, 300-step medians: 8B-offload 262.5-263 us per step with 20
+  // or 24 CTAs, 263.5 with 28 or 32, 282 with 64 at an earlier chunking; 3B and
+  // 8B-longgen the same with 24 as with 32); NOSA_GATHER_CTAS overrides the grid.
+  h->gather_grid = 24;
+  if (const char* g = std::getenv("NOSA_GATHER_CTAS")) {
+    const int v = std::atoi(g);
+    if (v > 0) h->gather_grid = v;
+  }
+  if (nchunks > 2 && std::getenv("NOSA_ATTN_SPLITS") == nullptr) {
+    const int nv = s.k + 1;
+    const int by_len = std::max(1, (nv + 8) / 16);
+    const int ns = std::min(std::max(attention_pick_nsplit(s, s.k, 1), by_len),
+                            std::max(1, std::min(kMaxSplits, nv / 2)));
+    for (int c = 0; c < nchunks; ++c) h->nsplit_c[c] = ns;
   }
   // The selection runs in the scoring kernel where its arrays fit shared memory
   // (NOSA_FUSED_SELECT=0: a selection kernel of its own after each chunk's scoring).
