@@ -7,8 +7,8 @@
 // pages to the GPU's node (a preferred policy: the kernel falls back to other
 // nodes rather than fail) before pinning them. With one memory node, or when
 // the GPU's node is unknown, has no memory or is not allowed to this process,
-// nothing is bound; a store of 1 GiB or more is then laid out in pinned
-// transparent huge pages (host_store_alloc).
+// nothing is bound. A store of 1 GiB or more, bound or not, is laid out in
+// pinned transparent huge pages (host_store_alloc).
 #include "nosa.h"
 #include "nosa_internal.cuh"
 
@@ -169,22 +169,59 @@ void unpin(int fd) {
   close(fd);
 }
 
+// One registered anonymous mapping of at least `bytes`: aligned to and rounded up
+// to `page`, bound (preferred) to `node` when node >= 0, advised into transparent
+// huge pages when `huge`, faulted in (what came out small collapsed), pinned where
+// pin_long_term can, then registered with cudaHostRegister. Returns nullptr (and
+// releases everything) when a step fails or when `need_pin` and the pin did not hold.
+void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_pin,
+                     size_t* len_out, int* pin_fd) {
+  *pin_fd = -1;
+  const size_t len = (bytes + page - 1) / page * page;
+  void* p = map_aligned(len, page);
+  if (p == nullptr) return nullptr;
+  bool ok = true;
+  if (node >= 0) {
+    unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {0};
+    mask[node / (8 * sizeof(unsigned long))] |= 1UL << (node % (8 * sizeof(unsigned long)));
+    ok = syscall(SYS_mbind, p, len, 1 /* MPOL_PREFERRED */, mask, 1024UL, 0U) == 0;
+  }
+  if (ok) {
+    if (huge) madvise(p, len, MADV_HUGEPAGE);
+    madvise(p, len, MADV_DONTFORK);  // a forked child never sees the store
+    madvise(p, len, kMadvPopulateWrite);
+    if (huge) madvise(p, len, kMadvCollapse);
+    *pin_fd = pin_long_term(p, len);
+    ok = !need_pin || *pin_fd >= 0;
+  }
+  if (ok && cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
+                cudaSuccess) {
+    *len_out = len;
+    return p;
+  }
+  cudaGetLastError();
+  unpin(*pin_fd);
+  *pin_fd = -1;
+  munmap(p, len);
+  return nullptr;
+}
+
 // Pinned host memory of at least `bytes`, reachable by the device. *kind says how
 // it was made (host_store_free needs it), *mapped its mapped length, *pin_fd the
 // descriptor that holds its pages (-1: none):
-//   kind 1: an anonymous mapping bound (preferred) to `node` (node >= 0), faulted
-//           in, pinned where pin_long_term can, registered;
-//   kind 2: an anonymous mapping in transparent huge pages (stores of 1 GiB or
-//           more, unbound): aligned to and rounded up to the huge-page size,
-//           faulted in, what came out small collapsed, pinned, registered; taken
-//           only when the pin holds;
+//   kind 1: a mapping bound to `node` (node >= 0): in pinned transparent huge pages
+//           for stores of 1 GiB or more; where the pin does not hold, in base pages
+//           (pinned if it can be), as huge pages may be split under the GPU;
+//   kind 2: an unbound mapping in transparent huge pages (stores of 1 GiB or more),
+//           taken only when the pin holds;
 //   kind 0: a plain cudaHostAlloc (everything else, and the fallback).
 // Why the huge pages: the recall reads about 1 300 scattered blocks of the store
 // per step, and with 64 KB pages their address translation, not the link, set the
 // rate in most short runs on the GB300 machines (medians well above the link-bound
-// step, up to 2.9x); with 512 MB pages every run kept the link's rate. Why the pins: without
-// them the kernel split the huge pages of a running store now and then, and every
-// step of that run took milliseconds. NOSA_HOST_HUGEPAGE=0 keeps the plain store.
+// step, up to 2.9x); with 512 MB pages every run kept the link's rate. Why the
+// pins: without them the kernel split the huge pages of a running store now and
+// then, and every step of that run took milliseconds. NOSA_HOST_HUGEPAGE=0 keeps
+// the plain store (or the bound base-page mapping).
 cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size_t* mapped,
                              int* pin_fd) {
   *pin_fd = -1;
@@ -195,38 +232,17 @@ cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size
   const bool bind = node >= 0 && node < 1024;
   const size_t huge =
       (g == nullptr || std::atoi(g) != 0) && bytes >= ((size_t)1 << 30) ? thp_size() : 0;
-  if (bind || huge != 0) {
-    const size_t page = huge != 0 ? huge : (size_t)sysconf(_SC_PAGESIZE);
-    const size_t len = (bytes + page - 1) / page * page;
-    if (void* p = map_aligned(len, page)) {
-      bool ok = true;
-      if (bind) {
-        unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {0};
-        mask[node / (8 * sizeof(unsigned long))] |= 1UL << (node % (8 * sizeof(unsigned long)));
-        ok = syscall(SYS_mbind, p, len, 1 /* MPOL_PREFERRED */, mask, 1024UL, 0U) == 0;
-      }
-      if (ok) {
-        if (huge != 0) madvise(p, len, MADV_HUGEPAGE);
-        madvise(p, len, MADV_DONTFORK);  // a forked child never sees the store
-        madvise(p, len, kMadvPopulateWrite);
-        if (huge != 0) madvise(p, len, kMadvCollapse);
-        *pin_fd = pin_long_term(p, len);
-        ok = bind || *pin_fd >= 0;  // unpinned huge pages may be split under the GPU
-      }
-      if (ok &&
-          cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
-              cudaSuccess) {
-        *out = p;
-        *kind = bind ? 1 : 2;
-        *mapped = len;
-        return cudaSuccess;
-      }
-      cudaGetLastError();
-      unpin(*pin_fd);
-      *pin_fd = -1;
-      munmap(p, len);
-    }
+  const size_t base = (size_t)sysconf(_SC_PAGESIZE);
+  void* p = nullptr;
+  if (huge != 0) p = map_registered(bytes, huge, bind ? node : -1, true, true, mapped, pin_fd);
+  if (p == nullptr && bind)
+    p = map_registered(bytes, base, node, false, false, mapped, pin_fd);
+  if (p != nullptr) {
+    *out = p;
+    *kind = bind ? 1 : 2;
+    return cudaSuccess;
   }
+  *mapped = bytes;
   return cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
 }
 
