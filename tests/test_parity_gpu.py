@@ -162,12 +162,14 @@ def test_gather_numbers_entries_across_unit_tiles(monkeypatch):
 
 
 @pytest.mark.parametrize("env", [{"NOSA_FUSED_SELECT": "0"}, {"NOSA_GATHER_STREAMS": "1"},
-                                 {"NOSA_SELECT_HINT": "0"}, {"NOSA_GATHER_VEC": "32"}])
+                                 {"NOSA_SELECT_HINT": "0"}, {"NOSA_GATHER_VEC": "32"},
+                                 {"NOSA_PDL": "0"}, {"NOSA_ATTN_SPLITS": "2"}])
 def test_step_switches_every_unit(env, monkeypatch):
     # The documented switches of the step (read at nosa_create) change launch
     # shapes and schedules, never the result: a selection kernel of its own, one
-    # gather stream, the radix cut at every step, 32-byte gather loads; three
-    # chunks so the stream switches matter, every unit checked.
+    # gather stream, the radix cut at every step, 32-byte gather loads, ordinary
+    # instead of programmatic graph edges, a forced split count; three chunks so
+    # the stream switches matter, every unit checked.
     for key, val in env.items():
         monkeypatch.setenv(key, val)
     monkeypatch.setenv("NOSA_CHUNK_SIZES", "1,2,1")
@@ -175,7 +177,7 @@ def test_step_switches_every_unit(env, monkeypatch):
     _run(w)
 
 
-@pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2", "0.5,1,2,3,3,1"])
+@pytest.mark.parametrize("sizes", ["1,2,3,4,1", "3,1,1,2", "0.5,1,2,3,3,1", "0.5,1,2,3,2.5,1.5"])
 def test_unequal_chunks_every_unit(sizes, monkeypatch):
     # The step's unit chunks run concurrently and differ in split counts; every
     # unit (not a sample) is checked, so a partial buffer shared across chunks

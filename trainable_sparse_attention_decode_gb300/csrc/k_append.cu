@@ -30,6 +30,7 @@ __device__ __forceinline__ void copy_unit(uint8_t* dst, const uint8_t* src, long
 // CTA 0 also publishes the step's arguments (StepIO) for the kernels after it.
 template <typename T>
 __global__ void __launch_bounds__(128) append_step_kernel(Shape s, State st, StepArgs a) {
+  griddep_launch_dependents();  // the chunks' scoring may become resident (it waits)
   TraceScope trace_scope(st.trace, kTrAppend);
   const T* __restrict__ k_new = static_cast<const T*>(a.k_new);
   const T* __restrict__ v_new = static_cast<const T*>(a.v_new);

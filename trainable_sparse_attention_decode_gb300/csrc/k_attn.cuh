@@ -359,6 +359,7 @@ __device__ __forceinline__ void attn_merge(const float* part_acc, const float* p
 
 template <typename T, int D, int G, int W>
 __global__ void __launch_bounds__(32 * W) attn_split_kernel(AttnKParams p) {
+  griddep_wait();  // the chunk's gather (programmatic edge in the step graph)
   TraceScope trace_scope(p.trace, p.trace_slot);
   using Gm = AttnGeom<T, D, G, W>;
   constexpr int B = Gm::B, GP = Gm::GP, QP = Gm::QP, NT = Gm::NT, PARTS = Gm::PARTS;

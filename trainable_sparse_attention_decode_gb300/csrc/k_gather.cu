@@ -67,6 +67,7 @@ template <typename V>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State st, int ubase,
                                                                 int ucount, int chunk) {
   constexpr int kPer = Mover<V>::kPer;
+  griddep_wait();  // the chunk's selection (programmatic edge in the step graph)
   TraceScope trace_scope(st.trace, chunk < 8 ? kTrGather + chunk : -1);
   __shared__ int pre[kGatherTile + 1];  // exclusive prefix of the tile's load counts
   __shared__ int warp_tot[kGatherThreads / 32];
@@ -137,6 +138,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(Shape s, State s
     done += tot;
     __syncthreads();  // pre and warp_tot are rewritten by the next tile
   }
+  // only now: the filled-slot attention's CTAs would otherwise hold SMs while waiting
+  griddep_launch_dependents();
 }
 
 }  // namespace

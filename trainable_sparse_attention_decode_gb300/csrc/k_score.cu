@@ -47,6 +47,8 @@ template <typename T, typename PT, int D, int MODE>
 __global__ void __launch_bounds__(256) score_kernel(Shape s, State st, float inv_sqrt_d,
                                                     int ubase, int cold, int chunk) {
   constexpr bool FUSED = MODE >= 1;
+  griddep_wait();               // the append (programmatic edge in the step graph)
+  griddep_launch_dependents();  // the chunk's gather may become resident (it waits)
   TraceScope trace_scope(st.trace, chunk >= 0 && chunk < 8 ? kTrScore + chunk : -1);
   constexpr int EPC = 16 / (int)sizeof(PT);  // pooled values per 16-byte chunk
   constexpr int M = D / EPC / 8;             // chunks per lane per pooled row

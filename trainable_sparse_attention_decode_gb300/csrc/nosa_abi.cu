@@ -327,6 +327,7 @@ struct nosa_handle {
   int nsplit = 1;       // attention splits over the slots kept from the previous step
   int nsplit_new = 4;   // attention splits over the slots the gather filled (warm steps)
   int gather_grid = 1;
+  bool pdl = true;               // programmatic edges in the step graph (NOSA_PDL=0: off)
   bool broken = false;
   std::string err;
   cudaStream_t last_stream = nullptr;
@@ -727,6 +728,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   // or 24 CTAs, 263.5 with 28 or 32, 282 with 64 at an earlier chunking; 3B and
   // 8B-longgen the same with 24 as with 32); NOSA_GATHER_CTAS overrides the grid.
   h->gather_grid = 24;
+  if (const char* g = std::getenv("NOSA_PDL")) h->pdl = std::atoi(g) != 0;
   if (const char* g = std::getenv("NOSA_GATHER_CTAS")) {
     const int v = std::atoi(g);
     if (v > 0) h->gather_grid = v;
@@ -856,6 +858,47 @@ nosa_status nosa_append_kv(nosa_handle* h, int32_t n_tokens, const void* k, cons
 
 namespace {
 
+// Kernel nodes of a captured step whose edges can become programmatic.
+struct CapNodes {
+  cudaGraphNode_t append = nullptr;
+  cudaGraphNode_t score[kMaxChunks] = {};
+  cudaGraphNode_t gather[kMaxChunks] = {};
+  cudaGraphNode_t attn_new[kMaxChunks] = {};
+};
+
+// Turns the step graph's edges on the critical path into programmatic ones (the
+// dependent kernel becomes resident while its producer runs and waits in
+// griddep_wait for the producer's completion and memory): append -> each chunk's
+// fused scoring + selection, a chunk's selection -> its gather, its gather -> the
+// attention over the slots it filled. An edge that capture did not produce
+// directly (timing event nodes between the two) is left as it is.
+cudaError_t make_programmatic_edges(cudaGraph_t graph, const CapNodes& n, int nchunks) {
+  cudaGraphEdgeData pe;
+  std::memset(&pe, 0, sizeof(pe));
+  pe.from_port = cudaGraphKernelNodePortProgrammatic;
+  pe.type = cudaGraphDependencyTypeProgrammatic;
+  auto convert = [&](cudaGraphNode_t from, cudaGraphNode_t to) -> cudaError_t {
+    if (from == nullptr || to == nullptr) return cudaSuccess;
+    if (cudaGraphRemoveDependencies(graph, &from, &to, nullptr, 1) != cudaSuccess) {
+      cudaGetLastError();  // no direct edge: nothing to convert
+      return cudaSuccess;
+    }
+    cudaError_t e = cudaGraphAddDependencies(graph, &from, &to, &pe, 1);
+    if (e != cudaSuccess) {  // put the ordinary edge back
+      cudaGetLastError();
+      e = cudaGraphAddDependencies(graph, &from, &to, nullptr, 1);
+    }
+    return e;
+  };
+  cudaError_t e = cudaSuccess;
+  for (int c = 0; c < nchunks && c < kMaxChunks && e == cudaSuccess; ++c) {
+    e = convert(n.append, n.score[c]);
+    if (e == cudaSuccess) e = convert(n.score[c], n.gather[c]);
+    if (e == cudaSuccess) e = convert(n.gather[c], n.attn_new[c]);
+  }
+  return e;
+}
+
 // Enqueues one decode step on `origin`: the units are processed in chunks that
 // form a pipeline over five internal streams. Scoring of chunk c+1 (HBM) runs
 // while chunk c is selected, gathered (host link) and attended over its kept
@@ -864,12 +907,22 @@ namespace {
 // returned in *append_node.
 cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& args,
                          const FrontArgs* front, int n_cap, bool cold, cudaEvent_t* ev,
-                         bool capture, cudaGraphNode_t* append_node) {
+                         bool capture, CapNodes* nodes) {
   const Shape& sh = h->s;
   State& st = h->st;
   auto mark = [&](cudaEvent_t e, cudaStream_t t) {
     if (capture) cudaEventRecordWithFlags(e, t, cudaEventRecordExternal);
     else cudaEventRecord(e, t);
+  };
+  // Under capture: the node just captured on stream t (the kernel launched last).
+  auto last_node = [&](cudaStream_t t) -> cudaGraphNode_t {
+    cudaStreamCaptureStatus cs;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(t, &cs, nullptr, nullptr, &deps, nullptr, &nd) != cudaSuccess ||
+        nd != 1 || cs != cudaStreamCaptureStatusActive)
+      return nullptr;
+    return deps[0];
   };
   if (ev) mark(ev[0], origin);
   cudaError_t err = cudaSuccess;
@@ -881,14 +934,9 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
   if (err == cudaSuccess) err = cudaStreamWaitEvent(h->s_sco, h->ev_in, 0);
   if (err == cudaSuccess)
     err = front ? launch_frontend(sh, st, *front, h->s_sco) : launch_append_step(sh, st, args, h->s_sco);
-  if (err == cudaSuccess && capture && append_node) {
-    cudaStreamCaptureStatus cs;
-    const cudaGraphNode_t* deps = nullptr;
-    size_t nd = 0;
-    err = cudaStreamGetCaptureInfo(h->s_sco, &cs, nullptr, nullptr, &deps, nullptr, &nd);
-    if (err == cudaSuccess && (nd != 1 || cs != cudaStreamCaptureStatusActive))
-      err = cudaErrorStreamCaptureInvalidated;
-    if (err == cudaSuccess) *append_node = deps[0];
+  if (err == cudaSuccess && capture && nodes) {
+    nodes->append = last_node(h->s_sco);
+    if (nodes->append == nullptr) err = cudaErrorStreamCaptureInvalidated;
   }
   if (ev) mark(ev[1], h->s_sco);
   // Fused step: every chunk's scoring + selection on its own stream, all started
@@ -904,6 +952,8 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
       if (err == cudaSuccess)
         err = launch_score_select(sh, st, n_cap, h->cu_base[c], h->cu_count[c], cold ? 1 : 0, c,
                                   h->s_chunk[c], h->score_occ);
+      if (err == cudaSuccess && capture && nodes && c < kMaxChunks)
+        nodes->score[c] = last_node(h->s_chunk[c]);
       if (err == cudaSuccess) err = cudaEventRecord(h->ev_sel[c], h->s_chunk[c]);
     }
   }
@@ -944,6 +994,7 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
     if (ev && c == 0) mark(ev[4], tg);
     if (err == cudaSuccess) err = launch_gather(sh, st, h->gather_grid, h->cu_base[c], h->cu_count[c], c,
                                                   h->gather_wide, tg);
+    if (err == cudaSuccess && capture && nodes && c < kMaxChunks) nodes->gather[c] = last_node(tg);
     if (err == cudaSuccess) err = cudaEventRecord(h->ev_gat[c], tg);
     if (ev && c == h->nchunks - 1) mark(ev[5], tg);
     // attention over the slots kept from the previous step, plus the tail (fused
@@ -971,6 +1022,7 @@ cudaError_t enqueue_step(nosa_handle* h, cudaStream_t origin, const StepArgs& ar
       a.split_base = ns_kept;
       a.trace_slot = c < 8 ? kTrAttnNew + c : -1;
       err = launch_attention(sh, a, tf);
+      if (err == cudaSuccess && capture && nodes && c < kMaxChunks) nodes->attn_new[c] = last_node(tf);
     }
     if (fused && err == cudaSuccess) err = cudaEventRecord(h->ev_jfa[c], tf);
   }
@@ -1027,11 +1079,14 @@ cudaError_t build_step_graph(nosa_handle* h, StepGraph& g, const StepArgs& args,
   const int n_cap = (N / kScoreCap + 1) * kScoreCap;
   cudaError_t err = cudaStreamBeginCapture(h->s_cap, cudaStreamCaptureModeRelaxed);
   if (err != cudaSuccess) return err;
-  cudaGraphNode_t node = nullptr;
-  const cudaError_t e_enq = enqueue_step(h, h->s_cap, args, front, n_cap, false, ev, true, &node);
+  CapNodes nodes;
+  const cudaError_t e_enq = enqueue_step(h, h->s_cap, args, front, n_cap, false, ev, true, &nodes);
+  const cudaGraphNode_t node = nodes.append;
   cudaGraph_t graph = nullptr;
   err = cudaStreamEndCapture(h->s_cap, &graph);
   if (e_enq != cudaSuccess) err = e_enq;
+  if (err == cudaSuccess && h->pdl && h->fused_select)
+    err = make_programmatic_edges(graph, nodes, h->nchunks);
   if (err == cudaSuccess)
     err = cudaGraphInstantiateWithFlags(&g.exec, graph, cudaGraphInstantiateFlagUseNodePriority);
   if (err == cudaSuccess) err = cudaGraphKernelNodeGetParams(node, &g.append_params);

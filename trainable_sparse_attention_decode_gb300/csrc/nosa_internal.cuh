@@ -395,6 +395,17 @@ __device__ __forceinline__ void trace_mark(unsigned long long* trace, int id) {
   atomicMax(trace + 2 * id + 1, t);
 }
 
+// Programmatic dependent launch inside the step graph: a kernel whose incoming
+// edge is programmatic may become resident before its producer has finished and
+// waits here until the producer grids have completed and their memory is
+// visible; with ordinary edges (and outside graphs) both are no-ops. A producer
+// lets its programmatic dependents be scheduled once all of its CTAs have called
+// griddep_launch_dependents or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 struct TraceScope {
   unsigned long long* slot;
   __device__ __forceinline__ TraceScope(unsigned long long* trace, int id)
