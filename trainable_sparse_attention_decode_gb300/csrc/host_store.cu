@@ -94,6 +94,8 @@ int host_store_node(int device) {
                           (int)allowed.size());
 }
 
+namespace {
+
 // madvise advice values of Linux 5.14 (populate for writing) and 6.1 (collapse into
 // huge pages); older kernels answer EINVAL and the call does nothing.
 constexpr int kMadvPopulateWrite = 23;
@@ -205,6 +207,8 @@ void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_p
   munmap(p, len);
   return nullptr;
 }
+
+}  // namespace
 
 // Pinned host memory of at least `bytes`, reachable by the device. *kind says how
 // it was made (host_store_free needs it), *mapped its mapped length, *pin_fd the

@@ -324,7 +324,6 @@ struct nosa_handle {
   int host_node = -1;            // NUMA node the store is bound to (-1: not bound)
   long long L = 0;
   long long steps = 0;
-  int nsplit = 1;       // attention splits over the slots kept from the previous step
   int nsplit_new = 4;   // attention splits over the slots the gather filled (warm steps)
   int gather_grid = 1;
   bool pdl = true;               // programmatic edges in the step graph (NOSA_PDL=0: off)
@@ -556,7 +555,6 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   const Shape& s = h->s;
   State& st = h->st;
   const size_t U = s.U, k = s.k, mb = s.maxBlk, W = s.W;
-  h->nsplit = attention_pick_nsplit(s, s.k, 1);
   cudaError_t e = cudaSuccess;
   auto A = [&](auto** p, size_t bytes) {
     if (e == cudaSuccess) e = dev_alloc(h, p, bytes);
