@@ -1,9 +1,9 @@
 """The pinned host store's layout (csrc/host_store.cu). On a host with one memory
 node, a store of 1 GiB or more is laid out in transparent huge pages on which the
 process holds long-term pins (the kernel may neither move nor split pages that
-the GPU reads); NOSA_HOST_HUGEPAGE=0 keeps a plain cudaHostAlloc. The store is
-only memory: both layouts must give bit-identical decode results."""
-import os
+the GPU reads); NOSA_HOST_HUGEPAGE=0 keeps a plain cudaHostAlloc, and so does a
+host that refuses the pin (injected on the host with NOSA_INJECT_FAIL=pin). The
+store is only memory: every layout must give bit-identical decode results."""
 
 import pytest
 import torch
@@ -95,17 +95,38 @@ def test_plain_store_switch(monkeypatch):
         nosa.nosa_destroy(h)
 
 
+def test_refused_pin_falls_back(monkeypatch):
+    monkeypatch.delenv("NOSA_HOST_HUGEPAGE", raising=False)
+    monkeypatch.setenv("NOSA_INJECT_FAIL", "pin")
+    pin0 = _status_kb("VmPin")
+    h = nosa.nosa_create(_cfg())
+    try:
+        st = nosa.nosa_stats(h)
+        assert st["host_store_pinned"] == 0
+        assert _status_kb("VmPin") == pin0
+        # unpinned huge pages are never kept: a plain store, or a bound one in base pages
+        assert st["host_store_kind"] == (1 if st["host_numa_node"] >= 0 else 0)
+    finally:
+        nosa.nosa_destroy(h)
+
+
 def test_layouts_decode_identically(monkeypatch):
     res = {}
-    for mode in ("1", "0"):
+    for mode, inject in (("1", None), ("0", None), ("1", "pin")):
         monkeypatch.setenv("NOSA_HOST_HUGEPAGE", mode)
+        if inject:
+            monkeypatch.setenv("NOSA_INJECT_FAIL", inject)
+        else:
+            monkeypatch.delenv("NOSA_INJECT_FAIL", raising=False)
         h = nosa.nosa_create(_cfg())
         try:
-            res[mode] = _decode(h)
+            res[(mode, inject)] = _decode(h)
         finally:
             nosa.nosa_destroy(h)
-    (a, sa), (b, sb) = res["1"], res["0"]
+    a, sa = res[("1", None)]
     assert sa["host_loads"] > sa["cold_host_loads"] > 0  # warm steps recalled from the host
-    assert sa["host_loads"] == sb["host_loads"]
-    assert torch.equal(a, b)
+    for key in (("0", None), ("1", "pin")):
+        b, sb = res[key]
+        assert sa["host_loads"] == sb["host_loads"]
+        assert torch.equal(a, b)
     assert torch.isfinite(a.float()).all()

@@ -174,10 +174,11 @@ void unpin(int fd) {
 // One registered anonymous mapping of at least `bytes`: aligned to and rounded up
 // to `page`, bound (preferred) to `node` when node >= 0, advised into transparent
 // huge pages when `huge`, faulted in (what came out small collapsed), pinned where
-// pin_long_term can, then registered with cudaHostRegister. Returns nullptr (and
+// pin_long_term can (not tried without `try_pin`), then registered with
+// cudaHostRegister. Returns nullptr (and
 // releases everything) when a step fails or when `need_pin` and the pin did not hold.
 void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_pin,
-                     size_t* len_out, int* pin_fd) {
+                     bool try_pin, size_t* len_out, int* pin_fd) {
   *pin_fd = -1;
   const size_t len = (bytes + page - 1) / page * page;
   void* p = map_aligned(len, page);
@@ -193,7 +194,7 @@ void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_p
     madvise(p, len, MADV_DONTFORK);  // a forked child never sees the store
     madvise(p, len, kMadvPopulateWrite);
     if (huge) madvise(p, len, kMadvCollapse);
-    *pin_fd = pin_long_term(p, len);
+    *pin_fd = try_pin ? pin_long_term(p, len) : -1;
     ok = !need_pin || *pin_fd >= 0;
   }
   if (ok && cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
@@ -227,7 +228,7 @@ void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_p
 // then, and every step of that run took milliseconds. NOSA_HOST_HUGEPAGE=0 keeps
 // the plain store (or the bound base-page mapping).
 cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size_t* mapped,
-                             int* pin_fd) {
+                             int* pin_fd, bool try_pin) {
   *pin_fd = -1;
   *out = nullptr;
   *kind = 0;
@@ -238,9 +239,10 @@ cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size
       (g == nullptr || std::atoi(g) != 0) && bytes >= ((size_t)1 << 30) ? thp_size() : 0;
   const size_t base = (size_t)sysconf(_SC_PAGESIZE);
   void* p = nullptr;
-  if (huge != 0) p = map_registered(bytes, huge, bind ? node : -1, true, true, mapped, pin_fd);
+  if (huge != 0)
+    p = map_registered(bytes, huge, bind ? node : -1, true, true, try_pin, mapped, pin_fd);
   if (p == nullptr && bind)
-    p = map_registered(bytes, base, node, false, false, mapped, pin_fd);
+    p = map_registered(bytes, base, node, false, false, try_pin, mapped, pin_fd);
   if (p != nullptr) {
     *out = p;
     *kind = bind ? 1 : 2;

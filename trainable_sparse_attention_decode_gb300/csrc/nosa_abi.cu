@@ -307,6 +307,7 @@ struct StepGraph {
 
 struct InjectFailFlags {
   bool host = false;
+  bool pin = false;
   int dev_index = -1;
 };
 
@@ -387,13 +388,15 @@ namespace {
 
 // Failure injection on the host (no GPU fault involved): NOSA_INJECT_FAIL, read
 // at every nosa_create, makes one of its allocations report exhaustion without
-// being attempted. "host": the pinned host store; "dev:N": the N-th device
-// allocation (from 0). Anything else: no injection.
+// being attempted. "host": the pinned host store; "pin": the long-term pin of the
+// host store (the store then falls back as it does where pinning is refused);
+// "dev:N": the N-th device allocation (from 0). Anything else: no injection.
 InjectFailFlags inject_fail_from_env() {
   InjectFailFlags f;
   const char* g = std::getenv("NOSA_INJECT_FAIL");
   if (g == nullptr) return f;
   if (std::strcmp(g, "host") == 0) f.host = true;
+  else if (std::strcmp(g, "pin") == 0) f.pin = true;
   else if (std::strncmp(g, "dev:", 4) == 0 && g[4] >= '0' && g[4] <= '9') f.dev_index = std::atoi(g + 4);
   return f;
 }
@@ -629,7 +632,7 @@ nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out) {
   h->host_node = host_store_node(cfg->device);
   e = h->inject.host ? cudaErrorMemoryAllocation
                      : host_store_alloc(h->host_bytes, h->host_node, &hp, &h->host_kind,
-                                        &h->host_map_bytes, &h->host_pin_fd);
+                                        &h->host_map_bytes, &h->host_pin_fd, !h->inject.pin);
   if (h->host_kind != 1) h->host_node = -1;  // only kind 1 is bound to a node
   if (e != cudaSuccess) {
     g_thread_err = std::string("pinned host allocation failed: ") + cudaGetErrorString(e);

@@ -202,8 +202,9 @@ int host_store_node(int device);
 // kind: 0 cudaHostAlloc, 1 a registered mapping bound to `node`, 2 a registered,
 // pinned mapping in transparent huge pages (unbound). *pin_fd: a descriptor that holds
 // long-term pins on the store's pages until host_store_free closes it (-1: none).
+// try_pin = false: the pin is not attempted (as if the host refused it).
 cudaError_t host_store_alloc(size_t bytes, int node, void** out, int* kind, size_t* mapped,
-                             int* pin_fd);
+                             int* pin_fd, bool try_pin);
 void host_store_free(void* p, size_t mapped, int kind, int pin_fd);
 
 // ---------------------------------------------------------------------------
