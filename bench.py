@@ -307,7 +307,7 @@ def host_store_report(st, huge_kb, huge_kb_after, pin_kb, vm_created, vm_t0, vm_
     and pinned after the create and after the timed steps, and the host's
     memory-management events during the setup and the timed steps."""
     mb = lambda kb: round(kb / 1024) if kb is not None else None
-    delta = lambda a, b: {k_: b[k_] - a[k_] for k_ in b if b[k_] != a.get(k_)}
+    delta = lambda a, b: {k_: b[k_] - a.get(k_, 0) for k_ in b if b[k_] != a.get(k_, 0)}
     return {"layout": STORE_LAYOUTS.get(st["host_store_kind"], st["host_store_kind"]),
             "long_term_pins": bool(st["host_store_pinned"]),
             "huge_pages_mb": mb(huge_kb), "huge_pages_mb_after_timed": mb(huge_kb_after),

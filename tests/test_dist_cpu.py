@@ -89,3 +89,31 @@ def test_rank_requests_limits():
 def test_aggregate_single_rank_is_identity():
     import bench
     assert bench.aggregate(2.0, 7, 1) == (2.0, 7)
+
+
+def test_host_store_report_deltas():
+    import bench
+    st = {"host_store_kind": 2, "host_store_pinned": 1}
+    created = {"thp_split_page": 3, "pgmigrate_success": 10}
+    t0 = {"thp_split_page": 3, "pgmigrate_success": 14}
+    t1 = {"thp_split_page": 5, "pgmigrate_success": 14, "thp_split_page_failed": 2}
+    r = bench.host_store_report(st, 8704 * 1024, 5632 * 1024, 8704 * 1024, created, t0, t1)
+    assert r["layout"] == "transparent huge pages" and r["long_term_pins"] is True
+    assert (r["huge_pages_mb"], r["huge_pages_mb_after_timed"], r["pinned_mb"]) == (8704, 5632, 8704)
+    # only the counters that moved, over the setup and over the timed steps
+    assert r["vm_events"] == {"setup": {"pgmigrate_success": 4},
+                              "timed": {"thp_split_page": 2, "thp_split_page_failed": 2}}
+    r = bench.host_store_report({"host_store_kind": 0, "host_store_pinned": 0},
+                                None, None, None, None, t0, t1)
+    assert r["layout"] == "cudaHostAlloc" and r["vm_events"] is None
+    assert r["huge_pages_mb"] is None and r["pinned_mb"] is None
+
+
+def test_proc_readers_on_this_host():
+    import bench
+    ev = bench.vm_events()
+    if ev is not None:  # Linux: the named counters that this kernel has, as integers
+        assert set(ev) <= set(bench.VM_EVENTS)
+        assert all(isinstance(v, int) and v >= 0 for v in ev.values())
+    for kb in (bench.anon_huge_kb(), bench.pinned_kb()):
+        assert kb is None or (isinstance(kb, int) and kb >= 0)
