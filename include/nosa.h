@@ -119,6 +119,14 @@ typedef struct nosa_handle nosa_handle;
  * eviction scores, eligibility bitmasks, slot tables and scratch; and the host
  * store [U][maxBlk] units in pinned, mapped host memory (U = batch *
  * n_kv_heads, maxBlk = ceil(max_context / B)). The handle owns all of it.
+ * A host store of 1 GiB or more is laid out in transparent huge pages, faulted
+ * in at once and held by long-term page pins (an io_uring buffer registration,
+ * close-on-exec, excluded from fork) so that the host kernel cannot split or
+ * move its pages while the GPU reads them; the pins count against the process's
+ * locked-memory limit unless it holds CAP_IPC_LOCK, and where they are refused
+ * the store is a plain cudaHostAlloc (environment NOSA_HOST_HUGEPAGE=0 asks
+ * for that directly). nosa_stats reports which (host_store_kind,
+ * host_store_pinned); nosa_destroy drops the pins.
  * Errors: INVALID_ARG, UNSUPPORTED, OOM, HOST_OOM, CUDA. *out is NULL on error.
  */
 nosa_status nosa_create(const nosa_config* cfg, nosa_handle** out);
