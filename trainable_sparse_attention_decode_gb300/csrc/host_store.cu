@@ -111,8 +111,16 @@ constexpr long kSysUringRegister = 427;
 #endif
 
 // The size of a transparent huge page (the page-middle-directory size: 2 MB with
-// 4 KB base pages, 512 MB with 64 KB ones), or 0 where the kernel has none.
+// 4 KB base pages, 512 MB with 64 KB ones), or 0 where the kernel has none or
+// they are switched off ("[never]": MADV_HUGEPAGE would then do nothing).
 size_t thp_size() {
+  if (std::FILE* e = std::fopen("/sys/kernel/mm/transparent_hugepage/enabled", "r")) {
+    char mode[128] = {0};
+    const size_t n = std::fread(mode, 1, sizeof(mode) - 1, e);
+    std::fclose(e);
+    mode[n] = 0;
+    if (std::strstr(mode, "[never]") != nullptr) return 0;
+  }
   std::FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r");
   if (f == nullptr) return 0;
   unsigned long long v = 0;
