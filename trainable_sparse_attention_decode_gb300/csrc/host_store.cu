@@ -171,6 +171,21 @@ int pin_long_term(void* p, size_t len) {
   return (int)fd;
 }
 
+// Whether this process may create io_uring instances at all (a seccomp filter or
+// kernel.io_uring_disabled can forbid it); probed once, so that a store that needs
+// the pin is not faulted in only to be thrown away.
+bool uring_available() {
+  static const bool ok = [] {
+    unsigned char params[120];
+    std::memset(params, 0, sizeof(params));
+    const long fd = syscall(kSysUringSetup, 1, params);
+    if (fd < 0) return false;
+    close((int)fd);
+    return true;
+  }();
+  return ok;
+}
+
 // Drops the pins of pin_long_term at once (closing the descriptor alone releases
 // them only when the kernel tears the instance down, some time later).
 void unpin(int fd) {
@@ -188,6 +203,8 @@ void unpin(int fd) {
 void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_pin,
                      bool try_pin, size_t* len_out, int* pin_fd) {
   *pin_fd = -1;
+  const bool can_pin = try_pin && uring_available();
+  if (need_pin && !can_pin) return nullptr;
   const size_t len = (bytes + page - 1) / page * page;
   void* p = map_aligned(len, page);
   if (p == nullptr) return nullptr;
@@ -202,7 +219,7 @@ void* map_registered(size_t bytes, size_t page, int node, bool huge, bool need_p
     madvise(p, len, MADV_DONTFORK);  // a forked child never sees the store
     madvise(p, len, kMadvPopulateWrite);
     if (huge) madvise(p, len, kMadvCollapse);
-    *pin_fd = try_pin ? pin_long_term(p, len) : -1;
+    *pin_fd = can_pin ? pin_long_term(p, len) : -1;
     ok = !need_pin || *pin_fd >= 0;
   }
   if (ok && cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
